@@ -1,0 +1,265 @@
+"""CPU float64 oracle for grouped-query attention over a preallocated KV cache.
+
+TEST INFRASTRUCTURE ONLY.  This module is the definition the GPU library is
+checked against.  Only the test suite, the package smoke check and the CPU
+baseline leg of the benchmark may import it; the product path never does, and
+it shares no code with the CUDA library (no kernels, headers, helpers or
+constants).  It is deliberately plain and slow: NumPy float64, an explicit
+loop over every (row, query head, query), an explicit repeat of the KV heads
+to the query heads, and a plain softmax over keys 0..position.
+
+Sources (three web pages; "p1", "p2", "p3" below):
+
+* p1  "Implement grouped-query attention over a preallocated KV cache, with no
+       torch.cat, for both prefill chunks and decode" (inferenceinterviews.com)
+       - section "A strong answer": the ``KVCache`` class (allocate
+         [B, Hkv, max_len, d] once, write in place at the row's length, raise
+         past max_len) and ``gqa_attention`` (scale 1/sqrt(d), query t at
+         absolute position lens - n_new + t, keys past lens masked, padded
+         queries masked, fully masked rows -> zeros).
+       - "The decisions an interviewer reads for", items 1-3, and the
+         paragraph after them: the direct reference this oracle restates
+         (repeat KV heads, loop over every query, plain softmax over keys 0
+         to its position).
+       - "Common mistakes": h // G (not h % Hkv); increment lengths only
+         after the write.
+* p2  "Write the causal mask for a decode step with a KV cache, where the
+       query is shorter than the keys" (inferenceinterviews.com)
+       - TL;DR and "A strong answer": bottom-right mask j <= i + (S - T),
+         ``decode_causal_mask``; the top-left ``tril(ones(T, S))`` as the
+         wrong convention; the T = 4, S = 4096 count.
+* p3  "16. Prefill, decode and the KV cache" (inference.shantanugoel.com)
+       - "Layout and validity": per-layer lengths, ``length`` refusing when a
+         forward pass stopped part-way, ``update`` shape checks,
+         ``truncate`` / ``reset``.
+       - "How big is the cache?": the KV byte formula.
+
+Readings where the pages are silent or loose (each is also listed in the
+design notes):
+
+* Overflow in one row of a batch: p1's loop would already have written the
+  earlier rows when it raises.  Here every row is validated first and nothing
+  is written on error, so an error leaves data and lengths unchanged.
+* ``n_new[b]`` must satisfy 0 <= n_new[b] <= T; anything else is an error.
+* Lengths are kept per layer and per row (p3 keeps one length per layer, p1
+  one per row).  ``truncate`` takes one new length per row, applies it to
+  every layer, and requires 0 <= new <= current for every row.
+* ``length`` returns the per-row lengths shared by all layers and raises if
+  any two layers disagree.
+* Output for a padded query (t >= n_new[b]), for an empty batch, an empty
+  chunk (T = 0) or an empty cache is zero.
+"""
+
+from __future__ import annotations
+
+import math
+
+import numpy as np
+
+__all__ = [
+    "CacheError",
+    "OracleCache",
+    "kv_head_of",
+    "query_position",
+    "score_scale",
+    "attend_one_query",
+    "gqa_attention",
+    "append_attention",
+    "decode_causal_mask",
+    "top_left_causal_mask",
+    "kv_cache_bytes",
+]
+
+
+class CacheError(ValueError):
+    """Raised for every rejected cache operation (overflow, bad shape, ...)."""
+
+
+# ---------------------------------------------------------------------------
+# Small named steps.  Each is one rule from the pages; keeping them separate
+# lets the self-check suite swap in a plausible wrong version and confirm
+# that some check fails.
+# ---------------------------------------------------------------------------
+
+
+def kv_head_of(h: int, G: int) -> int:
+    """KV head read by query head h: h // G (p1 TL;DR; p1 "Common mistakes")."""
+    return h // G
+
+
+def query_position(lens_b: int, n_new_b: int, t: int) -> int:
+    """Absolute position of query t of the chunk just appended to row b.
+
+    p1 TL;DR and ``gqa_attention``: the chunk's queries are the last n_new
+    positions of the row, so query t sits at lens - n_new + t (p2 TL;DR: the
+    same rule written as S - T + i).
+    """
+    return lens_b - n_new_b + t
+
+
+def score_scale(d: int) -> float:
+    """Scores are q.k / sqrt(d) (p1 ``gqa_attention``)."""
+    return 1.0 / math.sqrt(d)
+
+
+def attend_one_query(q_vec: np.ndarray, K_rows: np.ndarray, V_rows: np.ndarray, pos: int) -> np.ndarray:
+    """Output of one query at absolute position ``pos`` against one head's keys.
+
+    Plain softmax over keys 0..pos (p1, the direct reference described after
+    "The decisions an interviewer reads for").  ``K_rows``/``V_rows`` are that
+    head's [len, d] rows; only rows 0..pos are read.  A query that sees no key
+    (pos < 0) returns zeros (p1 decision 3).
+    """
+    d = q_vec.shape[-1]
+    if pos < 0:
+        return np.zeros(d, dtype=np.float64)
+    keys = np.asarray(K_rows[: pos + 1], dtype=np.float64)
+    vals = np.asarray(V_rows[: pos + 1], dtype=np.float64)
+    s = (keys @ np.asarray(q_vec, dtype=np.float64)) * score_scale(d)
+    s = s - s.max()
+    p = np.exp(s)
+    p = p / p.sum()
+    return p @ vals
+
+
+class OracleCache:
+    """Preallocated KV cache with per-layer, per-row valid lengths.
+
+    K and V of each layer are float64 arrays [B, Hkv, max_len, d] allocated
+    once (p1 ``KVCache.__init__``; p3 "Layout and validity" with one buffer
+    pair per layer).  ``lens[layer, b]`` counts the valid tokens of row b.
+    """
+
+    def __init__(self, layers: int, batch: int, kv_heads: int, max_len: int, head_dim: int):
+        if layers < 1 or batch < 0 or kv_heads < 1 or max_len < 0 or head_dim < 1:
+            raise CacheError("bad cache geometry")
+        self.layers, self.B, self.Hkv, self.max_len, self.d = layers, batch, kv_heads, max_len, head_dim
+        shape = (batch, kv_heads, max_len, head_dim)
+        self.k = [np.zeros(shape, dtype=np.float64) for _ in range(layers)]
+        self.v = [np.zeros(shape, dtype=np.float64) for _ in range(layers)]
+        self.lens = np.zeros((layers, batch), dtype=np.int64)
+
+    # -- p1 ``KVCache.append`` / p3 ``KVCache.update`` ----------------------
+    def append(self, layer: int, k_new: np.ndarray, v_new: np.ndarray, n_new) -> None:
+        """Write k_new[b, :, :n_new[b]] at rows lens[b] .. lens[b]+n_new[b]-1.
+
+        All rows are checked before any write; lengths grow only after every
+        write (p1 "Common mistakes", last item).  Raises ``CacheError`` on a
+        shape mismatch (p3 ``update``), on n_new outside 0..T, or when a row
+        would pass max_len (p1 ``append``, p3 ``update``).
+        """
+        if not 0 <= layer < self.layers:
+            raise CacheError(f"layer {layer} out of range")
+        k_new = np.asarray(k_new)
+        v_new = np.asarray(v_new)
+        if k_new.ndim != 4 or k_new.shape != v_new.shape:
+            raise CacheError("k_new and v_new must both be [B, Hkv, T, d]")
+        Bn, Hn, T, dn = k_new.shape
+        if Bn != self.B or Hn != self.Hkv or dn != self.d:
+            raise CacheError("cache batch/head/width shapes differ")
+        n_new = np.asarray(n_new, dtype=np.int64).reshape(-1)
+        if n_new.shape[0] != self.B:
+            raise CacheError("n_new must have one entry per row")
+        lens = self.lens[layer]
+        for b in range(self.B):
+            if n_new[b] < 0 or n_new[b] > T:
+                raise CacheError(f"row {b}: n_new={n_new[b]} outside 0..{T}")
+            if lens[b] + n_new[b] > self.max_len:
+                raise CacheError(f"row {b}: {lens[b] + n_new[b]} tokens > max_len {self.max_len}")
+        for b in range(self.B):
+            s, n = int(lens[b]), int(n_new[b])
+            self.k[layer][b, :, s : s + n] = k_new[b, :, :n]
+            self.v[layer][b, :, s : s + n] = v_new[b, :, :n]
+        self.lens[layer] = lens + n_new
+
+    def lens_of(self, layer: int) -> np.ndarray:
+        return self.lens[layer].copy()
+
+    # -- p3 ``length`` / ``truncate`` / ``reset`` -----------------------------
+    def length(self) -> np.ndarray:
+        """Per-row lengths shared by every layer; raises if layers disagree."""
+        if self.layers > 1 and np.any(self.lens != self.lens[0][None, :]):
+            raise CacheError("a forward pass stopped part-way; reset or truncate the cache")
+        return self.lens[0].copy()
+
+    def truncate(self, new_lens) -> None:
+        """Forget everything after new_lens[b] tokens in every layer; no data moves."""
+        new_lens = np.asarray(new_lens, dtype=np.int64).reshape(-1)
+        if new_lens.shape[0] != self.B:
+            raise CacheError("new_lens must have one entry per row")
+        cur = self.length()
+        if np.any(new_lens < 0) or np.any(new_lens > cur):
+            raise CacheError("invalid truncation length")
+        self.lens[:] = new_lens[None, :]
+
+    def reset(self) -> None:
+        self.truncate(np.zeros(self.B, dtype=np.int64))
+
+    def bytes(self) -> int:
+        """Bytes held by every K and V buffer (p3 ``bytes``), at 8 B a value."""
+        return sum(a.nbytes for a in self.k + self.v)
+
+
+def gqa_attention(q: np.ndarray, cache: OracleCache, layer: int, n_new) -> np.ndarray:
+    """Attention of the T queries of the chunk just appended (p1 ``gqa_attention``).
+
+    q is [B, Hq, T, d] with Hq a multiple of Hkv.  The KV heads are explicitly
+    repeated to Hq heads, then every query (b, h, t) with t < n_new[b] attends
+    to keys 0..lens[b]-n_new[b]+t of KV head h // G with a plain softmax.
+    Padded queries and empty cases give zeros.  Returns float64 [B, Hq, T, d].
+    """
+    q = np.asarray(q, dtype=np.float64)
+    if q.ndim != 4:
+        raise CacheError("q must be [B, Hq, T, d]")
+    B, Hq, T, d = q.shape
+    if B != cache.B or d != cache.d:
+        raise CacheError("q batch/width differ from the cache")
+    if Hq % cache.Hkv != 0:
+        raise CacheError("Hq must be a multiple of Hkv")
+    G = Hq // cache.Hkv
+    n_new = np.asarray(n_new, dtype=np.int64).reshape(-1)
+    if n_new.shape[0] != B:
+        raise CacheError("n_new must have one entry per row")
+    lens = cache.lens[layer]
+    if np.any(n_new < 0) or np.any(n_new > T) or np.any(n_new > lens):
+        raise CacheError("n_new must satisfy 0 <= n_new <= min(T, lens)")
+    out = np.zeros((B, Hq, T, d), dtype=np.float64)
+    if B == 0 or T == 0:
+        return out
+    # The direct reference materialises one copy of KV head h // G for every
+    # query head h (the repeat the GPU path avoids).
+    k_rep = np.stack([cache.k[layer][:, kv_head_of(h, G)] for h in range(Hq)], axis=1)
+    v_rep = np.stack([cache.v[layer][:, kv_head_of(h, G)] for h in range(Hq)], axis=1)
+    for b in range(B):
+        for h in range(Hq):
+            K_rows = k_rep[b, h]
+            V_rows = v_rep[b, h]
+            for t in range(T):
+                if t >= n_new[b]:
+                    continue  # padded query slot: stays zero
+                pos = query_position(int(lens[b]), int(n_new[b]), t)
+                out[b, h, t] = attend_one_query(q[b, h, t], K_rows, V_rows, pos)
+    return out
+
+
+def append_attention(cache: OracleCache, layer: int, q, k_new, v_new, n_new) -> np.ndarray:
+    """One call of the path: in-place append, then attention of the chunk."""
+    cache.append(layer, k_new, v_new, n_new)
+    return gqa_attention(q, cache, layer, n_new)
+
+
+def decode_causal_mask(T: int, S: int) -> np.ndarray:
+    """Bool [T, S], True where query i may see key j: j <= i + (S - T) (p2)."""
+    q_pos = np.arange(S - T, S)[:, None]
+    k_pos = np.arange(S)[None, :]
+    return k_pos <= q_pos
+
+
+def top_left_causal_mask(T: int, S: int) -> np.ndarray:
+    """The wrong convention p2 warns about: tril(ones(T, S)), aligned top-left."""
+    return np.tril(np.ones((T, S), dtype=bool))
+
+
+def kv_cache_bytes(layers: int, batch: int, tokens: int, kv_heads: int, head_dim: int, bytes_per_value: int = 2) -> int:
+    """2 (K and V) x layers x batch x tokens x Hkv x d x bytes (p3 "How big is the cache?")."""
+    return 2 * layers * batch * tokens * kv_heads * head_dim * bytes_per_value
