@@ -1,0 +1,454 @@
+#!/usr/bin/env python
+"""Benchmark of the GQA-over-preallocated-KV-cache hot path on one GB300.
+
+Default workload: Llama-3.1-8B-shaped single-layer decode (B=32, Hq=32,
+Hkv=8, d=128, bf16 cache [32, 8, 8192, 128], initial lengths uniform in
+[1024, 7936], T=1, one appended token per row per step).  A step is one pass
+of the whole path: the in-place append of the step's K/V and the attention of
+the step's queries (libkvc kernels, one launch each).  The headline metric is
+KV-read GB/s: live K/V bytes the attention must read (sum over rows of
+lens * Hkv * d * 2 (K and V) * 2 B) divided by the step time.
+
+Other workloads (--workload): verify (B=64, S=4096, T=4), prefill (B=4,
+Hkv=8, chunk T=512 on priors that are multiples of 512; metric attention
+TFLOP/s over visible pairs), longctx (32 layers of [4, 8, 131072, 128]).
+
+--impl reference times the CPU float64 oracle (the only reference this
+method has) on a bounded sample of the same workload, on the host cores.
+Multi-GPU: replicas only (each rank runs its own independent cache; no
+collective), weak scaling, max time over ranks.
+"""
+
+from __future__ import annotations
+
+import argparse
+import json
+import math
+import os
+import subprocess
+import sys
+import time
+
+for _v in ("OPENBLAS_NUM_THREADS", "OMP_NUM_THREADS", "MKL_NUM_THREADS"):
+    os.environ.setdefault(_v, "1")  # the CPU baseline runs on one thread, stated as cores = 1
+
+import numpy as np
+import torch
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+from gqa_attention_preallocated_gb300 import workloads as wl  # noqa: E402
+
+FALLBACK_HBM_GBS = 6800.0
+FALLBACK_BF16_TFLOPS = 1900.0
+
+
+def _peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        d = json.load(open(p))
+        return float(d["hbm_gbs"]), float(d["bf16_tflops"]), float(d.get("bf16_tflops_sustained", d["bf16_tflops"])), "measured"
+    return FALLBACK_HBM_GBS, FALLBACK_BF16_TFLOPS, 1700.0, "fallback"
+
+
+class ClockSampler:
+    """nvidia-smi clocks and throttle reasons sampled during the timed region."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index: int):
+        self.index = index
+        self.proc = None
+        self.path = os.path.join(ROOT, "gpurun_out", f"clocks_gpu{index}.csv")
+
+    def __enter__(self):
+        try:
+            os.makedirs(os.path.dirname(self.path), exist_ok=True)
+            self.f = open(self.path, "w")
+            self.proc = subprocess.Popen(["nvidia-smi", "-i", str(self.index), "--query-gpu=" + self.FIELDS,
+                                          "--format=csv,noheader,nounits", "-lms", "100"],
+                                         stdout=self.f, stderr=subprocess.DEVNULL)
+            time.sleep(0.3)
+        except Exception:
+            self.proc = None
+        return self
+
+    def __exit__(self, *a):
+        if self.proc is not None:
+            time.sleep(0.25)
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except Exception:
+                self.proc.kill()
+            self.f.close()
+
+    def summary(self):
+        if self.proc is None or not os.path.exists(self.path):
+            return None
+        sm, mx, reasons = [], 0.0, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in open(self.path):
+            parts = [x.strip() for x in line.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                mx = max(mx, float(parts[2]))
+            except ValueError:
+                continue
+            for n, v in zip(names, parts[5:9]):
+                if v.lower() == "active":
+                    reasons.add(n)
+        if not sm:
+            return None
+        return {"sm_mhz": float(np.median(sm)), "sm_max_mhz": mx, "reasons": sorted(reasons), "samples": len(sm)}
+
+
+# ---------------------------------------------------------------------------
+# Workload set-up (inputs resident in HBM before timing starts)
+# ---------------------------------------------------------------------------
+
+
+def kv_bytes(lens, Hkv, d, esize=2):
+    return int(np.sum(lens)) * Hkv * d * 2 * esize
+
+
+def visible_pairs(priors, n_new):
+    # sum over rows of sum_{t < n} (prior + t + 1)
+    return int(sum(int(n) * int(p) + int(n) * (int(n) + 1) // 2 for p, n in zip(priors, n_new)))
+
+
+def make_cache(shape, layers, lens0, seed):
+    from gqa_attention_preallocated_gb300 import KVCache
+
+    cache = KVCache(layers, shape.B, shape.Hkv, shape.max_len, shape.d, dtype=torch.bfloat16, device="cuda")
+    for layer in range(layers):
+        wl.fill_normal_(cache.k[layer], seed, wl.STREAM_CACHE_K + 16 * layer)
+        wl.fill_normal_(cache.v[layer], seed, wl.STREAM_CACHE_V + 16 * layer)
+        cache.set_lens(layer, lens0)
+    return cache
+
+
+def step_inputs(shape, Hq, T, n_distinct, seed, device="cuda"):
+    q = [wl.to_storage(wl.normal(seed, 5000 + i, (shape.B, Hq, T, shape.d), device=device), torch.bfloat16)
+         for i in range(n_distinct)]
+    k = [wl.to_storage(wl.normal(seed, 1000 + 2 * i, (shape.B, shape.Hkv, T, shape.d), device=device), torch.bfloat16)
+         for i in range(n_distinct)]
+    v = [wl.to_storage(wl.normal(seed, 1001 + 2 * i, (shape.B, shape.Hkv, T, shape.d), device=device), torch.bfloat16)
+         for i in range(n_distinct)]
+    return q, k, v
+
+
+class Workload:
+    """One named workload: set-up, one step, and the step's algorithmic work."""
+
+    def __init__(self, name, seed=0):
+        self.name = name
+        self.seed = seed
+        if name == "decode8b":
+            s = self.shape = wl.DECODE_8B
+            self.layers, self.Hq, self.T = 1, s.Hq, 1
+            self.lens0 = wl.decode_lens(seed, s.B, 1024, s.max_len - 256)
+            self.n_new = np.ones(s.B, dtype=np.int64)
+            self.rollback_every = 256  # the workload's 256 steps, then back to the initial lengths
+            self.metric, self.unit = "GQA decode KV-read HBM GB/s", "GB/s"
+        elif name == "verify":
+            s = self.shape = wl.VERIFY
+            self.layers, self.Hq, self.T = 1, s.Hq, 4
+            self.lens0 = np.full(s.B, s.max_len - self.T, dtype=np.int64)
+            self.n_new = np.full(s.B, self.T, dtype=np.int64)
+            self.rollback_every = 1  # speculative verify: append T, attend, truncate back
+            self.metric, self.unit = "GQA speculative-verify KV-read HBM GB/s", "GB/s"
+        elif name == "prefill":
+            s = self.shape = wl.PREFILL
+            self.layers, self.Hq, self.T = 1, s.Hq, 512
+            self.lens0 = wl.prefill_priors(seed, s.B)
+            self.n_new = np.full(s.B, 512, dtype=np.int64)
+            self.rollback_every = 1
+            self.metric, self.unit = "GQA chunked-prefill attention TFLOP/s", "TFLOP/s"
+        elif name == "longctx":
+            s = self.shape = wl.LONGCTX
+            self.layers, self.Hq, self.T = s.layers, s.Hq, 1
+            self.lens0 = wl.decode_lens(seed, s.B, 32768, s.max_len - 64)
+            self.n_new = np.ones(s.B, dtype=np.int64)
+            self.rollback_every = 64
+            self.metric, self.unit = "GQA long-context 32-layer decode KV-read HBM GB/s", "GB/s"
+        else:
+            raise SystemExit(f"unknown workload {name}")
+
+    def config(self):
+        s = self.shape
+        return {"workload": s.name, "B": s.B, "Hq": self.Hq, "Hkv": s.Hkv, "d": s.d, "max_len": s.max_len,
+                "layers": self.layers, "T": self.T, "dtype": "bf16",
+                "initial_lens": {"min": int(self.lens0.min()), "max": int(self.lens0.max()),
+                                 "mean": float(self.lens0.mean())},
+                "l2": "inputs larger than L2 (live KV per step exceeds the 129 MB L2)" if self.name != "prefill"
+                else "per-step K/V working set exceeds L2 for long priors; not flushed"}
+
+    def lens_at(self, i):
+        """Lengths after the append of step i (steps counted from the last rollback)."""
+        return self.lens0 + self.n_new * ((i % self.rollback_every) + 1)
+
+    def work(self, i):
+        """Algorithmic units of step i in the metric's unit numerator (bytes or FLOPs)."""
+        s = self.shape
+        if self.unit == "TFLOP/s":
+            return 4 * s.d * self.Hq * visible_pairs(self.lens0, self.n_new)
+        return kv_bytes(self.lens_at(i), s.Hkv, s.d) * self.layers
+
+    def kernel_bytes(self, i):
+        """Algorithmic bytes of one attention launch: live K/V + q + out."""
+        s = self.shape
+        qo = 2 * s.B * self.Hq * self.T * s.d * 2
+        return kv_bytes(self.lens_at(i), s.Hkv, s.d) + qo
+
+
+def run_native(w: Workload, steps: int, warmup: int, rank: int, world: int):
+    from gqa_attention_preallocated_gb300 import KVCache  # noqa: F401
+
+    s = w.shape
+    torch.cuda.synchronize()
+    cache = make_cache(s, w.layers, w.lens0, w.seed + rank)
+    n_distinct = min(max(steps, 1), 16)
+    q, k, v = step_inputs(s, w.Hq, w.T, n_distinct, w.seed + rank)
+    out = torch.empty_like(q[0])
+    ws = cache.workspace(w.Hq, w.T)
+    stream = torch.cuda.current_stream()
+
+    def one_step(i, ev=None):
+        if i > 0 and i % w.rollback_every == 0:
+            cache.truncate(w.lens0)
+        j = i % n_distinct
+        for layer in range(w.layers):
+            if ev is not None and layer == 0:
+                ev[0].record(stream)
+            cache.append(layer, k[j], v[j], w.n_new)
+            if ev is not None and layer == 0:
+                ev[1].record(stream)
+            cache.gqa_attention(layer, q[j], w.n_new, out=out, workspace=ws)
+            if ev is not None and layer == 0:
+                ev[2].record(stream)
+
+    for i in range(warmup):
+        one_step(i)
+    cache.truncate(w.lens0)
+    torch.cuda.synchronize()
+
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(steps)]
+    start, stop = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    if world > 1:
+        torch.distributed.barrier()
+    torch.cuda.synchronize()
+    with ClockSampler(torch.cuda.current_device()) as clk:
+        t_wall = time.perf_counter()
+        start.record(stream)
+        for i in range(steps):
+            one_step(i, evs[i])
+        stop.record(stream)
+        torch.cuda.synchronize()
+        t_wall = time.perf_counter() - t_wall
+    if world > 1:
+        torch.distributed.barrier()
+    ms = start.elapsed_time(stop)
+    attn_ms = [e[1].elapsed_time(e[2]) for e in evs]
+    append_ms = [e[0].elapsed_time(e[1]) for e in evs]
+    status = cache.device_status(ws)
+    work = sum(w.work(i) for i in range(steps))
+    kbytes = [w.kernel_bytes(i) for i in range(steps)]
+    # layer-0 attention launches are the ones timed per kernel (same shape on every layer)
+    res = {
+        "ms": ms, "wall_s": t_wall, "work": work, "attn_ms": attn_ms, "append_ms": append_ms,
+        "kernel_bytes": kbytes, "launches": steps * w.layers * 2, "clocks": clk.summary(), "status": status,
+    }
+    res["e2e"] = run_e2e(w, cache, steps, q, k, v)
+    return res
+
+
+def run_e2e(w: Workload, cache, steps: int, q, k, v):
+    """Same steps through the public API with the step's inputs in pinned host memory.
+
+    Per step: host->device copy of q, k_new, v_new; append + attention; device->host copy of out.
+    """
+    s = w.shape
+    n_distinct = len(q)
+    hq = [t.cpu().pin_memory() for t in q]
+    hk = [t.cpu().pin_memory() for t in k]
+    hv = [t.cpu().pin_memory() for t in v]
+    dq, dk, dv = torch.empty_like(q[0]), torch.empty_like(k[0]), torch.empty_like(v[0])
+    out = torch.empty_like(q[0])
+    hout = torch.empty(out.shape, dtype=out.dtype, pin_memory=True)
+    ws = cache.workspace(w.Hq, w.T)
+    stream = torch.cuda.current_stream()
+    cache.truncate(w.lens0)
+    torch.cuda.synchronize()
+    start, stop = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    start.record(stream)
+    for i in range(steps):
+        if i > 0 and i % w.rollback_every == 0:
+            cache.truncate(w.lens0)
+        j = i % n_distinct
+        dq.copy_(hq[j], non_blocking=True)
+        dk.copy_(hk[j], non_blocking=True)
+        dv.copy_(hv[j], non_blocking=True)
+        for layer in range(w.layers):
+            cache.append_attention(layer, dq, dk, dv, w.n_new, out=out, workspace=ws)
+        hout.copy_(out, non_blocking=True)
+    stop.record(stream)
+    torch.cuda.synchronize()
+    ms = start.elapsed_time(stop)
+    work = sum(w.work(i) for i in range(steps))
+    h2d = (q[0].numel() + k[0].numel() + v[0].numel()) * 2
+    return {"ms": ms, "work": work, "h2d": h2d, "d2h": out.numel() * 2}
+
+
+# ---------------------------------------------------------------------------
+# CPU oracle baseline (bounded sample)
+# ---------------------------------------------------------------------------
+
+
+def run_oracle_sample(w: Workload, budget_s: float = 12.0):
+    """Time the float64 oracle on a bounded sample of the workload (one thread).
+
+    Sample: one row of the batch (all its query heads) per oracle call, with
+    that row's real length, repeated over rows until the time budget is spent.
+    Returns (value in the metric's unit, sample description).
+    """
+    import oracle.ref as ref
+
+    s = w.shape
+    rng = np.random.default_rng(0)
+    done_work, t_total, calls, rows = 0, 0.0, 0, 0
+    b = 0
+    while t_total < budget_s and rows < 64:
+        L = int(w.lens_at(0)[b])
+        n = int(w.n_new[b])
+        c = ref.OracleCache(1, 1, s.Hkv, L, s.d)
+        c.k[0][:] = rng.standard_normal(c.k[0].shape)
+        c.v[0][:] = rng.standard_normal(c.v[0].shape)
+        c.lens[0] = [L]
+        q = rng.standard_normal((1, w.Hq, w.T, s.d))
+        t0 = time.perf_counter()
+        ref.gqa_attention(q, c, 0, np.array([n]))
+        t_total += time.perf_counter() - t0
+        rows += 1
+        calls += 1
+        if w.unit == "TFLOP/s":
+            done_work += 4 * s.d * w.Hq * visible_pairs([L - n], [n])
+        else:
+            done_work += L * s.Hkv * s.d * 2 * 2
+        b = (b + 1) % s.B
+    scale = 1e-12 if w.unit == "TFLOP/s" else 1e-9
+    value = done_work * scale / t_total
+    sample = (f"{rows} rows of the batch (all {w.Hq} query heads, real lengths), one oracle call each, "
+              f"{t_total:.1f} s of CPU time on one thread; value = the rows' algorithmic "
+              f"{'FLOPs' if w.unit == 'TFLOP/s' else 'KV bytes (bf16 sizes)'} / that time")
+    return value, sample, t_total
+
+
+# ---------------------------------------------------------------------------
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=256)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["native", "reference"], default="native")
+    ap.add_argument("--workload", choices=["decode8b", "verify", "prefill", "longctx"], default="decode8b")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    w = Workload(args.workload)
+    scale = 1e-12 if w.unit == "TFLOP/s" else 1e-9
+
+    if args.impl == "reference":
+        if rank != 0:
+            return
+        value, sample, t_total = run_oracle_sample(w)
+        line = {"metric": w.metric, "value": value, "unit": w.unit, "n_gpus": args.gpus, "steps": args.steps,
+                "warmup": args.warmup, "higher_is_better": True, "impl": "reference", "dtype": "f64",
+                "data": "synthetic", "config": w.config(),
+                "cpu_baseline": {"value": value, "unit": w.unit, "cores": 1, "kind": "oracle", "sample": sample},
+                "e2e": {"value": value, "unit": w.unit, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+                "vs_baseline": None}
+        print(json.dumps(line))
+        return
+
+    if world > 1:
+        torch.cuda.set_device(local)
+        torch.distributed.init_process_group("nccl", device_id=torch.device("cuda", local))
+    else:
+        torch.cuda.set_device(0)
+
+    res = run_native(w, args.steps, args.warmup, rank, world)
+    ms = res["ms"]
+    e2e_ms = res["e2e"]["ms"]
+    if world > 1:
+        t = torch.tensor([ms, e2e_ms], device="cuda")
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+        ms, e2e_ms = float(t[0]), float(t[1])
+    value = res["work"] * world * scale / (ms * 1e-3)
+    e2e_value = res["e2e"]["work"] * world * scale / (e2e_ms * 1e-3)
+
+    hbm, bf16, bf16_sus, peak_kind = _peaks()
+    attn_ms = float(np.mean(res["attn_ms"]))
+    kb = float(np.mean(res["kernel_bytes"]))
+    if w.unit == "TFLOP/s":
+        flops = w.work(0)
+        roof = {"bound": "tensor", "achieved": flops / (attn_ms * 1e-3) * 1e-12, "peak": bf16, "unit": "TFLOP/s"}
+    else:
+        roof = {"bound": "hbm", "achieved": kb / (attn_ms * 1e-3) * 1e-9, "peak": hbm, "unit": "GB/s"}
+    roof["frac"] = roof["achieved"] / roof["peak"]
+    roof["peak_source"] = f"{peak_kind} (MEASURED_PEAKS.json)" if peak_kind == "measured" else "fallback"
+    roof["kernel"] = "decode_splitkv_bf16_kernel"
+    roof["kernel_ms"] = attn_ms
+    roof["traffic"] = _committed_traffic(w)
+
+    line = {
+        "metric": w.metric, "value": value, "unit": w.unit, "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": ms / args.steps, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "bf16", "data": "synthetic (seeded counter-based generator, ~N(0,1))",
+        "config": dict(w.config(), parallelism="replicas only" if world > 1 else "single GPU"),
+        "roofline": roof,
+        "e2e": {"value": e2e_value, "unit": w.unit, "h2d_bytes_per_step": res["e2e"]["h2d"],
+                "d2h_bytes_per_step": res["e2e"]["d2h"]},
+        "gpu_launches": res["launches"],
+        "clocks": res["clocks"],
+        "device_status": res["status"],
+    }
+    if w.unit == "GB/s":
+        line["tokens_per_s"] = w.shape.B * args.steps * world / (ms * 1e-3)
+        line["frac_of_hbm_peak"] = value / hbm
+    if rank == 0 and not args.no_cpu_baseline:
+        cv, sample, _ = run_oracle_sample(w)
+        line["cpu_baseline"] = {"value": cv, "unit": w.unit, "cores": 1, "kind": "oracle", "sample": sample}
+    if rank == 0:
+        print(json.dumps(line))
+    if world > 1:
+        torch.distributed.destroy_process_group()
+
+
+def _committed_traffic(w: Workload):
+    """DRAM bytes per launch from the committed ncu summary, if taken on the current kernel source."""
+    import hashlib
+
+    path = os.path.join(ROOT, "profiles", f"traffic_{w.name}.txt")
+    if not os.path.exists(path):
+        return None
+    kv = dict(line.strip().split("=", 1) for line in open(path) if "=" in line and not line.startswith("#"))
+    src = os.path.join(ROOT, "gqa_attention_preallocated_gb300", "csrc", "decode_bf16.cu")
+    sha = hashlib.sha256(open(src, "rb").read()).hexdigest()[:16]
+    if kv.get("kernel_source_sha256_16") != sha:
+        return None
+    return float(kv["dram_bytes_per_launch"])
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,202 @@
+"""Python binding: argument marshalling over the libkvc C ABI.
+
+Every step of the path runs in libkvc's kernels; this module only allocates
+device memory through PyTorch, checks tensor shapes, and passes raw pointers,
+host length arrays and the current CUDA stream.
+
+The API mirrors the pages' ``KVCache.append`` / ``gqa_attention``
+("Implement grouped-query attention over a preallocated KV cache...",
+"A strong answer") and ``truncate`` / ``reset`` / ``length`` ("16. Prefill,
+decode and the KV cache", "Layout and validity").
+"""
+
+from __future__ import annotations
+
+import ctypes
+
+import numpy as np
+import torch
+
+from ._lib import KVC_BF16, KVC_F32, KVCError, check, lib
+
+_I32P = ctypes.POINTER(ctypes.c_int32)
+_I64P = ctypes.POINTER(ctypes.c_int64)
+
+_DTYPES = {torch.float32: KVC_F32, torch.bfloat16: KVC_BF16}
+
+
+def _stream_ptr(device: torch.device, stream=None) -> int:
+    s = stream if stream is not None else torch.cuda.current_stream(device)
+    return s.cuda_stream
+
+
+def _i32(a, n: int) -> np.ndarray:
+    if isinstance(a, torch.Tensor):
+        a = a.detach().cpu().numpy()
+    arr = np.ascontiguousarray(np.asarray(a, dtype=np.int64).reshape(-1))
+    if arr.shape[0] != n:
+        raise KVCError(1, f"expected {n} per-row entries, got {arr.shape[0]}")
+    if np.any(arr > np.iinfo(np.int32).max) or np.any(arr < np.iinfo(np.int32).min):
+        raise KVCError(1, "per-row entry out of int32 range")
+    return arr.astype(np.int32)
+
+
+def _ptr(t: torch.Tensor | None) -> int | None:
+    return None if t is None else t.data_ptr()
+
+
+class KVCache:
+    """Preallocated K/V buffers [B, Hkv, max_len, d] per layer plus the C handle.
+
+    ``k_bufs`` / ``v_bufs`` may be given (lists of contiguous CUDA tensors of
+    that shape); otherwise they are allocated here with ``torch.empty``.  The
+    handle borrows them; this object keeps them alive.
+    """
+
+    def __init__(self, layers: int, batch: int, kv_heads: int, max_len: int, head_dim: int,
+                 dtype: torch.dtype = torch.bfloat16, device="cuda", k_bufs=None, v_bufs=None):
+        if dtype not in _DTYPES:
+            raise KVCError(1, f"unsupported dtype {dtype}")
+        self.layers, self.B, self.Hkv, self.max_len, self.d = layers, batch, kv_heads, max_len, head_dim
+        self.dtype = dtype
+        dev = torch.device(device)
+        if dev.type == "cuda" and dev.index is None:
+            dev = torch.device("cuda", torch.cuda.current_device())
+        self.device = dev
+        shape = (batch, kv_heads, max_len, head_dim)
+        if k_bufs is None:
+            k_bufs = [torch.empty(shape, dtype=dtype, device=self.device) for _ in range(layers)]
+        if v_bufs is None:
+            v_bufs = [torch.empty(shape, dtype=dtype, device=self.device) for _ in range(layers)]
+        for t in list(k_bufs) + list(v_bufs):
+            if tuple(t.shape) != shape or t.dtype != dtype or not t.is_contiguous():
+                raise KVCError(1, f"cache buffers must be contiguous {shape} {dtype}")
+        self.k, self.v = list(k_bufs), list(v_bufs)
+        kp = (ctypes.c_void_p * layers)(*[t.data_ptr() for t in self.k])
+        vp = (ctypes.c_void_p * layers)(*[t.data_ptr() for t in self.v])
+        h = ctypes.c_void_p()
+        check(lib().kvc_create(ctypes.byref(h), layers, batch, kv_heads, max_len, head_dim, _DTYPES[dtype], kp, vp))
+        self._h = h
+        self._ws = None
+
+    # ------------------------------------------------------------------ state
+    def close(self) -> None:
+        if getattr(self, "_h", None) is not None and self._h.value:
+            lib().kvc_destroy(self._h)
+            self._h = None
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass
+
+    def lens(self, layer: int = 0) -> np.ndarray:
+        out = np.zeros(self.B, dtype=np.int64)
+        check(lib().kvc_get_lens(self._h, layer, out.ctypes.data_as(_I64P)))
+        return out
+
+    def set_lens(self, layer: int, lens) -> None:
+        """Adopt lengths for a layer whose buffers were filled by other means."""
+        arr = np.ascontiguousarray(np.asarray(lens, dtype=np.int64).reshape(-1))
+        if arr.shape[0] != self.B:
+            raise KVCError(1, f"expected {self.B} lengths")
+        check(lib().kvc_set_lens(self._h, layer, arr.ctypes.data_as(_I64P)))
+
+    def length(self) -> np.ndarray:
+        """Per-row length shared by every layer; raises if a forward pass stopped part-way."""
+        out = np.zeros(self.B, dtype=np.int64)
+        check(lib().kvc_length(self._h, out.ctypes.data_as(_I64P)))
+        return out
+
+    def truncate(self, new_lens) -> None:
+        arr = np.ascontiguousarray(np.asarray(new_lens, dtype=np.int64).reshape(-1))
+        if arr.shape[0] != self.B:
+            raise KVCError(1, f"expected {self.B} lengths")
+        check(lib().kvc_truncate(self._h, arr.ctypes.data_as(_I64P)))
+
+    def reset(self) -> None:
+        check(lib().kvc_reset(self._h))
+
+    # ------------------------------------------------------------------ compute
+    def workspace_bytes(self, q_heads: int, T: int) -> int:
+        return int(lib().kvc_workspace_bytes(self._h, q_heads, T))
+
+    def workspace(self, q_heads: int, T: int) -> torch.Tensor | None:
+        """A workspace buffer owned by this cache, grown as needed (reused across calls)."""
+        need = self.workspace_bytes(q_heads, T)
+        if need == 0:
+            return None
+        if self._ws is None or self._ws.numel() < need:
+            self._ws = torch.empty(need, dtype=torch.uint8, device=self.device)
+        return self._ws
+
+    def _check_tensor(self, t: torch.Tensor, shape, name: str) -> None:
+        if tuple(t.shape) != tuple(shape) or t.dtype != self.dtype or not t.is_contiguous() or t.device != self.device:
+            raise KVCError(1, f"{name} must be a contiguous {self.dtype} tensor of shape {tuple(shape)} on {self.device}")
+
+    def append(self, layer: int, k_new: torch.Tensor, v_new: torch.Tensor, n_new, stream=None) -> None:
+        """Write k_new[b, :, :n_new[b]] at each row's current length (in place)."""
+        T = k_new.shape[2] if k_new.dim() == 4 else -1
+        self._check_tensor(k_new, (self.B, self.Hkv, T, self.d), "k_new")
+        self._check_tensor(v_new, (self.B, self.Hkv, T, self.d), "v_new")
+        nn = _i32(n_new, self.B)
+        check(lib().kvc_append(self._h, layer, _ptr(k_new), _ptr(v_new), T, nn.ctypes.data_as(_I32P),
+                               _stream_ptr(self.device, stream)))
+
+    def gqa_attention(self, layer: int, q: torch.Tensor, n_new, out: torch.Tensor | None = None,
+                      workspace: torch.Tensor | None = None, stream=None) -> torch.Tensor:
+        """Attention of the chunk just appended: q [B, Hq, T, d] -> out [B, Hq, T, d]."""
+        if q.dim() != 4:
+            raise KVCError(1, "q must be [B, Hq, T, d]")
+        B, Hq, T, d = q.shape
+        self._check_tensor(q, (self.B, Hq, T, self.d), "q")
+        if out is None:
+            out = torch.empty_like(q)
+        self._check_tensor(out, q.shape, "out")
+        ws = workspace if workspace is not None else self.workspace(Hq, T)
+        nn = _i32(n_new, self.B)
+        check(lib().kvc_gqa_attention(self._h, layer, _ptr(q), Hq, T, nn.ctypes.data_as(_I32P), _ptr(out),
+                                      _ptr(ws), 0 if ws is None else ws.numel(), _stream_ptr(self.device, stream)))
+        return out
+
+    def append_attention(self, layer: int, q: torch.Tensor, k_new: torch.Tensor, v_new: torch.Tensor, n_new,
+                         out: torch.Tensor | None = None, workspace: torch.Tensor | None = None,
+                         stream=None) -> torch.Tensor:
+        """Append then attend, validated together (an error runs neither step)."""
+        if q.dim() != 4:
+            raise KVCError(1, "q must be [B, Hq, T, d]")
+        B, Hq, T, d = q.shape
+        self._check_tensor(q, (self.B, Hq, T, self.d), "q")
+        self._check_tensor(k_new, (self.B, self.Hkv, T, self.d), "k_new")
+        self._check_tensor(v_new, (self.B, self.Hkv, T, self.d), "v_new")
+        if out is None:
+            out = torch.empty_like(q)
+        self._check_tensor(out, q.shape, "out")
+        ws = workspace if workspace is not None else self.workspace(Hq, T)
+        nn = _i32(n_new, self.B)
+        check(lib().kvc_append_attention(self._h, layer, _ptr(q), _ptr(k_new), _ptr(v_new), Hq, T,
+                                         nn.ctypes.data_as(_I32P), _ptr(out), _ptr(ws),
+                                         0 if ws is None else ws.numel(), _stream_ptr(self.device, stream)))
+        return out
+
+    def selftest_bounded_wait(self, limit_ns: int, workspace: torch.Tensor | None = None, stream=None) -> None:
+        """Launch the bounded-wait self-test into the workspace's error word."""
+        ws = workspace if workspace is not None else self._ws
+        if ws is None:
+            raise KVCError(7, "no workspace")
+        check(lib().kvc_selftest_bounded_wait(_ptr(ws), int(limit_ns), _stream_ptr(self.device, stream)))
+
+    def device_status(self, workspace: torch.Tensor | None = None, stream=None) -> int:
+        """Synchronize and read the workspace error word (0 = clean); raises on a non-zero code."""
+        ws = workspace if workspace is not None else self._ws
+        if ws is None:
+            return 0
+        code = ctypes.c_int32(0)
+        check(lib().kvc_device_status(self._h, _ptr(ws), _stream_ptr(self.device, stream), ctypes.byref(code)))
+        return code.value
+
+
+def gqa_attention(q: torch.Tensor, cache: KVCache, n_new, layer: int = 0, **kw) -> torch.Tensor:
+    """Module-level form of ``KVCache.gqa_attention`` (the pages' call signature)."""
+    return cache.gqa_attention(layer, q, n_new, **kw)

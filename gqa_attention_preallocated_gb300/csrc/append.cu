@@ -1,0 +1,43 @@
+// In-place KV append ("Implement grouped-query attention over a preallocated
+// KV cache...", section "A strong answer", KVCache.append): row b's chunk
+// k_new[b, h, 0:n_new[b], :] lands at K[b, h, lens[b] : lens[b]+n_new[b], :].
+//
+// For one (b, h) both the source rows and the destination rows are
+// contiguous, so the copy is n_new[b] * d * elem bytes of 16-byte vectors:
+// every thread moves one uint4, consecutive threads consecutive vectors, so
+// loads and stores are fully coalesced 128-bit accesses.  blockIdx.y selects
+// (h, K or V), blockIdx.z the row b.
+
+#include "kvc_internal.h"
+
+namespace kvc {
+
+namespace {
+
+constexpr int kAppendThreads = 256;
+
+__global__ void __launch_bounds__(kAppendThreads) kv_append_kernel(const __grid_constant__ AppendParams p) {
+    const int b = blockIdx.z;
+    const int h = blockIdx.y >> 1;
+    const bool is_v = (blockIdx.y & 1) != 0;
+    const int n = p.n_new[b];
+    const size_t bytes = static_cast<size_t>(n) * p.row_bytes;
+    const size_t vec = static_cast<size_t>(blockIdx.x) * kAppendThreads + threadIdx.x;
+    if (vec * 16 >= bytes) return;
+    const size_t unit = static_cast<size_t>(b) * p.Hkv + h;
+    const uint8_t* src = (is_v ? p.v_new : p.k_new) + unit * p.T * p.row_bytes;
+    uint8_t* dst = (is_v ? p.v_cache : p.k_cache) + (unit * p.max_len + p.lens[b]) * p.row_bytes;
+    const uint4 val = __ldg(reinterpret_cast<const uint4*>(src) + vec);
+    reinterpret_cast<uint4*>(dst)[vec] = val;
+}
+
+}  // namespace
+
+cudaError_t launch_append(const AppendParams& p, int max_n_new, cudaStream_t stream) {
+    const size_t vecs = (static_cast<size_t>(max_n_new) * p.row_bytes) / 16;
+    dim3 grid(static_cast<unsigned>((vecs + kAppendThreads - 1) / kAppendThreads), 2u * p.Hkv, p.B);
+    kv_append_kernel<<<grid, kAppendThreads, 0, stream>>>(p);
+    return cudaGetLastError();
+}
+
+}  // namespace kvc

@@ -1,0 +1,158 @@
+// GQA attention for fp32 storage (any d <= 256 with d % 4 == 0).
+//
+// Semantics ("Implement grouped-query attention over a preallocated KV
+// cache...", "A strong answer", gqa_attention): query (b, h, t) with
+// t < n_new[b] sits at position prior[b] + t (prior = lens - n_new) and
+// attends to keys 0 .. prior[b] + t of KV head h / G with softmax scale
+// 1/sqrt(d); padded queries give 0.  The mask is index arithmetic ("Write
+// the causal mask for a decode step...", bottom-right rule j <= i + S - T).
+//
+// One CTA serves a block of 16 query rows r = g*T + t of one KV head, so the
+// K/V tile it stages in shared memory is read once for up to 16 query rows
+// (all G heads of the group when G*T <= 16).  Each warp owns 4 rows; lane j
+// scores key j of the 32-key tile, the warp keeps a running max and sum
+// (online softmax) and lane e accumulates output dims e, e+32, ...  Masked
+// keys are skipped outright, so stale or NaN slots past lens never enter.
+
+#include <math.h>
+
+#include "kvc_internal.h"
+
+namespace kvc {
+
+namespace {
+
+constexpr int kRows = 16;
+constexpr int kKeys = 32;
+constexpr int kWarps = 4;
+constexpr int kMaxD = 256;
+
+__global__ void __launch_bounds__(kWarps * 32) attn_f32_kernel(const __grid_constant__ F32Params p) {
+    extern __shared__ float4 smem4[];
+    float* sq = reinterpret_cast<float*>(smem4);  // [kRows][d]
+    float* sk = sq + kRows * p.d;                 // [kKeys][d]
+    float* sv = sk + kKeys * p.d;                 // [kKeys][d]
+
+    const int b = blockIdx.z, kvh = blockIdx.y, row0 = blockIdx.x * kRows;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int d = p.d, T = p.T;
+    const int prior = p.prior[b], nn = p.n_new[b];
+
+    // Row limits (largest visible key; -1 = padded / missing row) and extent.
+    int lim[4];
+    int extent = 0;
+    for (int i = 0; i < kRows; ++i) {
+        const int r = row0 + i;
+        int l = -1;
+        if (r < p.R && (r % T) < nn) l = prior + (r % T);
+        if (l + 1 > extent) extent = l + 1;
+        if ((i & 3) == warp) lim[i >> 2] = l;
+    }
+
+    // Stage the block's query rows.
+    for (int idx = threadIdx.x; idx < kRows * d; idx += blockDim.x) {
+        const int i = idx / d, e = idx % d, r = row0 + i;
+        float v = 0.f;
+        if (r < p.R) {
+            const int g = r / T, t = r % T;
+            v = p.q[((static_cast<size_t>(b) * p.Hq + kvh * p.G + g) * T + t) * d + e];
+        }
+        sq[idx] = v;
+    }
+
+    float m[4], l[4], o[4][kMaxD / 32];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        m[i] = -INFINITY;
+        l[i] = 0.f;
+#pragma unroll
+        for (int c = 0; c < kMaxD / 32; ++c) o[i][c] = 0.f;
+    }
+
+    const size_t unit_base = (static_cast<size_t>(b) * p.Hkv + kvh) * p.max_len;
+    for (int k0 = 0; k0 < extent; k0 += kKeys) {
+        __syncthreads();
+        const int nk = min(kKeys, extent - k0);
+        for (int idx = threadIdx.x; idx < kKeys * d / 4; idx += blockDim.x) {
+            const int j = (idx * 4) / d;
+            float4 kv4 = make_float4(0.f, 0.f, 0.f, 0.f), vv4 = kv4;
+            if (j < nk) {
+                const size_t off = (unit_base + k0) * d + static_cast<size_t>(idx) * 4;
+                kv4 = *reinterpret_cast<const float4*>(p.k_cache + off);
+                vv4 = *reinterpret_cast<const float4*>(p.v_cache + off);
+            }
+            reinterpret_cast<float4*>(sk)[idx] = kv4;
+            reinterpret_cast<float4*>(sv)[idx] = vv4;
+        }
+        __syncthreads();
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            const int li = lim[i];
+            if (li < k0) continue;  // row sees nothing in this tile (warp-uniform)
+            const float* qr = sq + (warp + 4 * i) * d;
+            const int key = k0 + lane;
+            float s = -INFINITY;
+            if (lane < nk && key <= li) {
+                float acc = 0.f;
+                const float* kr = sk + lane * d;
+                for (int e = 0; e < d; ++e) acc = fmaf(qr[e], kr[e], acc);
+                s = acc * p.scale;
+            }
+            float tmax = s;
+#pragma unroll
+            for (int off = 16; off > 0; off >>= 1) tmax = fmaxf(tmax, __shfl_xor_sync(0xffffffffu, tmax, off));
+            const float mnew = fmaxf(m[i], tmax);  // finite: key k0 <= li is visible
+            const float alpha = expf(m[i] - mnew);
+            const float pj = (s == -INFINITY) ? 0.f : expf(s - mnew);
+            float psum = pj;
+#pragma unroll
+            for (int off = 16; off > 0; off >>= 1) psum += __shfl_xor_sync(0xffffffffu, psum, off);
+            l[i] = l[i] * alpha + psum;
+            m[i] = mnew;
+#pragma unroll
+            for (int c = 0; c < kMaxD / 32; ++c) o[i][c] *= alpha;
+            const int jmax = min(nk, li - k0 + 1);
+            for (int j = 0; j < jmax; ++j) {
+                const float pb = __shfl_sync(0xffffffffu, pj, j);
+                const float* vr = sv + j * d;
+#pragma unroll
+                for (int c = 0; c < kMaxD / 32; ++c) {
+                    const int e = lane + 32 * c;
+                    if (e < d) o[i][c] = fmaf(pb, vr[e], o[i][c]);
+                }
+            }
+        }
+    }
+
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        const int r = row0 + warp + 4 * i;
+        if (r >= p.R) continue;
+        const int g = r / T, t = r % T;
+        float* dst = p.out + ((static_cast<size_t>(b) * p.Hq + kvh * p.G + g) * T + t) * d;
+        const float inv = (lim[i] >= 0 && l[i] > 0.f) ? 1.f / l[i] : 0.f;
+#pragma unroll
+        for (int c = 0; c < kMaxD / 32; ++c) {
+            const int e = lane + 32 * c;
+            if (e < d) dst[e] = (lim[i] >= 0) ? o[i][c] * inv : 0.f;
+        }
+    }
+}
+
+}  // namespace
+
+cudaError_t launch_attn_f32(const F32Params& p, cudaStream_t stream) {
+    const size_t smem = static_cast<size_t>(kRows + 2 * kKeys) * p.d * sizeof(float);
+    static bool attr_set = false;
+    if (!attr_set) {
+        cudaError_t e = cudaFuncSetAttribute(attn_f32_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                             static_cast<int>((kRows + 2 * kKeys) * kMaxD * sizeof(float)));
+        if (e != cudaSuccess) return e;
+        attr_set = true;
+    }
+    dim3 grid((p.R + kRows - 1) / kRows, p.Hkv, p.B);
+    attn_f32_kernel<<<grid, kWarps * 32, smem, stream>>>(p);
+    return cudaGetLastError();
+}
+
+}  // namespace kvc

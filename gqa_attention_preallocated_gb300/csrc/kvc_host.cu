@@ -1,0 +1,569 @@
+// Host side of libkvc: the C ABI declared in kvc.h.
+//
+// Holds per-layer, per-row lengths (host-authoritative), validates every
+// argument before anything is enqueued (so an error changes nothing), plans
+// the split-KV work partition from the host lengths without a device sync,
+// and launches the kernels on the caller's stream.
+//
+// Cache semantics follow "Implement grouped-query attention over a
+// preallocated KV cache..." ("A strong answer": KVCache.append raises past
+// max_len, lengths grow after the write) and "16. Prefill, decode and the KV
+// cache" ("Layout and validity": per-layer lengths, length refusing when a
+// forward pass stopped part-way, truncate, reset).
+
+#include <math.h>
+#include <stdarg.h>
+#include <stdio.h>
+#include <string.h>
+
+#include <algorithm>
+#include <string>
+#include <vector>
+
+#include "kvc_internal.h"
+
+using namespace kvc;
+
+struct kvc_cache {
+    int layers = 0, B = 0, Hkv = 0, max_len = 0, d = 0;
+    kvc_dtype dtype = KVC_F32;
+    int esize = 4;
+    std::vector<void*> k, v;
+    std::vector<int64_t> lens;  // [layers * B]
+    // device state, set up on first launch
+    bool dev_ready = false;
+    int device = -1;
+    int num_sms = 0;
+    std::vector<CUtensorMap> tmK, tmV;
+    std::vector<char> tm_ready;
+    const void* last_ws = nullptr;
+};
+
+namespace {
+
+thread_local std::string g_last_error;
+
+kvc_status fail(kvc_status s, const char* fmt, ...) __attribute__((format(printf, 2, 3)));
+kvc_status fail(kvc_status s, const char* fmt, ...) {
+    char buf[512];
+    va_list ap;
+    va_start(ap, fmt);
+    vsnprintf(buf, sizeof buf, fmt, ap);
+    va_end(ap);
+    g_last_error = buf;
+    return s;
+}
+
+kvc_status ok() { return KVC_OK; }
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+kvc_status cuda_fail(cudaError_t e, const char* what) {
+    return fail(KVC_ERR_CUDA, "%s: %s", what, cudaGetErrorString(e));
+}
+
+typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
+                                  const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
+                                  CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn encode_fn() {
+    static EncodeTiledFn fn = nullptr;
+    if (!fn) {
+        void* ptr = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000, cudaEnableDefault, &q) ==
+                cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<EncodeTiledFn>(ptr);
+    }
+    return fn;
+}
+
+kvc_status ensure_device(kvc_cache* c) {
+    if (c->dev_ready) return ok();
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaGetDevice");
+    int sms = 0;
+    e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaDeviceGetAttribute");
+    c->device = dev;
+    c->num_sms = sms;
+    c->dev_ready = true;
+    return ok();
+}
+
+// 2-D view of one layer's K or V: rows = B*Hkv*max_len, 128 bf16 per row;
+// boxes of 64 rows x 64 columns (128 bytes) with the 128-byte swizzle.
+kvc_status encode_layer_maps(kvc_cache* c, int layer) {
+    if (c->tm_ready[layer]) return ok();
+    EncodeTiledFn fn = encode_fn();
+    if (!fn) return fail(KVC_ERR_CUDA, "cuTensorMapEncodeTiled unavailable");
+    const cuuint64_t rows = static_cast<cuuint64_t>(c->B) * c->Hkv * c->max_len;
+    cuuint64_t dims[2] = {static_cast<cuuint64_t>(c->d), rows};
+    cuuint64_t strides[1] = {static_cast<cuuint64_t>(c->d) * 2};
+    cuuint32_t box[2] = {64, static_cast<cuuint32_t>(kKeyTile)};
+    cuuint32_t estr[2] = {1, 1};
+    for (int w = 0; w < 2; ++w) {
+        CUtensorMap* m = w ? &c->tmV[layer] : &c->tmK[layer];
+        CUresult r = fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, w ? c->v[layer] : c->k[layer], dims, strides, box, estr,
+                        CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                        CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+        if (r != CUDA_SUCCESS) return fail(KVC_ERR_CUDA, "cuTensorMapEncodeTiled failed (%d)", static_cast<int>(r));
+    }
+    c->tm_ready[layer] = 1;
+    return ok();
+}
+
+// ---------------------------------------------------------------------------
+// Validation shared by append / attention
+// ---------------------------------------------------------------------------
+
+kvc_status check_layer(const kvc_cache* c, int layer) {
+    if (!c) return fail(KVC_ERR_ARG, "null cache handle");
+    if (layer < 0 || layer >= c->layers) return fail(KVC_ERR_ARG, "layer %d outside 0..%d", layer, c->layers - 1);
+    return ok();
+}
+
+kvc_status validate_append(const kvc_cache* c, int layer, const void* k_new, const void* v_new, int T,
+                           const int32_t* n_new, int* max_n) {
+    kvc_status s = check_layer(c, layer);
+    if (s) return s;
+    if (T < 0) return fail(KVC_ERR_ARG, "T = %d < 0", T);
+    if (c->B > 0 && !n_new) return fail(KVC_ERR_ARG, "n_new is null");
+    const int64_t* lens = c->lens.data() + static_cast<size_t>(layer) * c->B;
+    int mx = 0;
+    for (int b = 0; b < c->B; ++b) {
+        if (n_new[b] < 0 || n_new[b] > T)
+            return fail(KVC_ERR_SHAPE, "row %d: n_new = %d outside 0..%d", b, n_new[b], T);
+        mx = std::max(mx, static_cast<int>(n_new[b]));
+    }
+    for (int b = 0; b < c->B; ++b) {
+        if (lens[b] + n_new[b] > c->max_len)
+            return fail(KVC_ERR_OVERFLOW, "row %d: %lld tokens > max_len %d", b,
+                        static_cast<long long>(lens[b] + n_new[b]), c->max_len);
+    }
+    if (mx > 0) {
+        if (!k_new || !v_new) return fail(KVC_ERR_ARG, "k_new / v_new is null");
+        if (!aligned16(k_new) || !aligned16(v_new)) return fail(KVC_ERR_ARG, "k_new / v_new not 16-byte aligned");
+    }
+    *max_n = mx;
+    return ok();
+}
+
+struct AttnPlan {
+    int Hq = 0, G = 0, T = 0, R = 0;
+    int mt = 0, RPB = 0, RB = 0, NB = 0, units = 0;
+    size_t ws_err = 0, ws_counters = 0, ws_partials = 0, ws_total = 0;
+};
+
+size_t round_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
+
+kvc_status plan_shape(const kvc_cache* c, int Hq, int T, int num_ctas, AttnPlan* pl) {
+    if (Hq <= 0) return fail(KVC_ERR_ARG, "q_heads = %d", Hq);
+    if (Hq % c->Hkv != 0) return fail(KVC_ERR_SHAPE, "q_heads %d is not a multiple of kv_heads %d", Hq, c->Hkv);
+    if (T < 0) return fail(KVC_ERR_ARG, "T = %d < 0", T);
+    pl->Hq = Hq;
+    pl->G = Hq / c->Hkv;
+    pl->T = T;
+    const long long R = static_cast<long long>(pl->G) * T;
+    if (R > (1ll << 30)) return fail(KVC_ERR_ARG, "G * T too large");
+    pl->R = static_cast<int>(R);
+    if (c->dtype == KVC_BF16) {
+        pl->mt = pl->R <= 16 ? 1 : (pl->R <= 32 ? 2 : 4);
+        pl->RPB = 16 * pl->mt;
+        pl->RB = std::max(1, (pl->R + pl->RPB - 1) / pl->RPB);
+        const long long NB = static_cast<long long>(c->B) * pl->RB;
+        if (NB > kMaxGroups)
+            return fail(KVC_ERR_ARG, "B * ceil(G*T / %d) = %lld exceeds %d row blocks", pl->RPB, NB, kMaxGroups);
+        pl->NB = static_cast<int>(NB);
+        pl->units = pl->NB * c->Hkv;
+        // Fixed layout for every call shape of this handle: error word, then
+        // room for the largest possible number of unit counters, then the
+        // partials.  The counters therefore always sit at the same place and
+        // stay zero between calls, whatever shapes the calls have.
+        pl->ws_err = 256;
+        pl->ws_counters = round_up(static_cast<size_t>(kMaxGroups) * c->Hkv * sizeof(int), 256);
+        pl->ws_partials = static_cast<size_t>(pl->units + num_ctas) * pl->RPB * (kHeadDimBf16 + 4) * sizeof(float);
+        pl->ws_total = pl->ws_err + pl->ws_counters + pl->ws_partials;
+    }
+    return ok();
+}
+
+kvc_status validate_attention(const kvc_cache* c, int layer, const void* q, int Hq, int T, const int32_t* n_new,
+                              const void* out, const int64_t* lens_after, AttnPlan* pl, int num_ctas) {
+    kvc_status s = check_layer(c, layer);
+    if (s) return s;
+    s = plan_shape(c, Hq, T, num_ctas, pl);
+    if (s) return s;
+    if (c->B > 0 && !n_new) return fail(KVC_ERR_ARG, "n_new is null");
+    for (int b = 0; b < c->B; ++b) {
+        if (n_new[b] < 0 || n_new[b] > T)
+            return fail(KVC_ERR_SHAPE, "row %d: n_new = %d outside 0..%d", b, n_new[b], T);
+        if (n_new[b] > lens_after[b])
+            return fail(KVC_ERR_SHAPE, "row %d: n_new = %d exceeds the row length %lld", b, n_new[b],
+                        static_cast<long long>(lens_after[b]));
+    }
+    if (c->B > 0 && T > 0) {
+        if (!q || !out) return fail(KVC_ERR_ARG, "q / out is null");
+        if (!aligned16(q) || !aligned16(out)) return fail(KVC_ERR_ARG, "q / out not 16-byte aligned");
+    }
+    return ok();
+}
+
+// ---------------------------------------------------------------------------
+// Launches (arguments already validated)
+// ---------------------------------------------------------------------------
+
+kvc_status do_append(kvc_cache* c, int layer, const void* k_new, const void* v_new, int T, const int32_t* n_new,
+                     int max_n, cudaStream_t stream) {
+    if (max_n == 0) return ok();
+    static_assert(sizeof(AppendParams) < 32000, "kernel parameter block too large");
+    AppendParams p;
+    p.k_new = static_cast<const uint8_t*>(k_new);
+    p.v_new = static_cast<const uint8_t*>(v_new);
+    p.k_cache = static_cast<uint8_t*>(c->k[layer]);
+    p.v_cache = static_cast<uint8_t*>(c->v[layer]);
+    p.B = c->B;
+    p.Hkv = c->Hkv;
+    p.T = T;
+    p.max_len = c->max_len;
+    p.row_bytes = c->d * c->esize;
+    const int64_t* lens = c->lens.data() + static_cast<size_t>(layer) * c->B;
+    for (int b = 0; b < c->B; ++b) {
+        p.lens[b] = static_cast<int>(lens[b]);
+        p.n_new[b] = n_new[b];
+    }
+    cudaError_t e = launch_append(p, max_n, stream);
+    if (e != cudaSuccess) return cuda_fail(e, "kv_append launch");
+    return ok();
+}
+
+kvc_status do_attention(kvc_cache* c, int layer, const void* q, const AttnPlan& pl, const int32_t* n_new, void* out,
+                        void* ws, size_t ws_bytes, cudaStream_t stream) {
+    const int64_t* lens = c->lens.data() + static_cast<size_t>(layer) * c->B;
+    if (c->B == 0 || pl.T == 0) return ok();
+    if (c->dtype == KVC_F32) {
+        static_assert(sizeof(F32Params) < 32000, "kernel parameter block too large");
+        F32Params p;
+        p.q = static_cast<const float*>(q);
+        p.k_cache = static_cast<const float*>(c->k[layer]);
+        p.v_cache = static_cast<const float*>(c->v[layer]);
+        p.out = static_cast<float*>(out);
+        p.B = c->B;
+        p.Hq = pl.Hq;
+        p.Hkv = c->Hkv;
+        p.G = pl.G;
+        p.T = pl.T;
+        p.max_len = c->max_len;
+        p.d = c->d;
+        p.R = pl.R;
+        p.scale = 1.0f / sqrtf(static_cast<float>(c->d));
+        for (int b = 0; b < c->B; ++b) {
+            p.prior[b] = static_cast<int>(lens[b] - n_new[b]);
+            p.n_new[b] = n_new[b];
+        }
+        cudaError_t e = launch_attn_f32(p, stream);
+        if (e != cudaSuccess) return cuda_fail(e, "attn_f32 launch");
+        return ok();
+    }
+
+    // bf16 split-KV path
+    kvc_status s = encode_layer_maps(c, layer);
+    if (s) return s;
+    static_assert(sizeof(DecodeParams) < 32000, "kernel parameter block too large");
+    DecodeParams p;
+    uint8_t* wsb = static_cast<uint8_t*>(ws);
+    p.err = reinterpret_cast<int*>(wsb);
+    p.counters = reinterpret_cast<int*>(wsb + pl.ws_err);
+    p.partials = reinterpret_cast<float*>(wsb + pl.ws_err + pl.ws_counters);
+    p.q = q;
+    p.out = out;
+    p.B = c->B;
+    p.Hq = pl.Hq;
+    p.Hkv = c->Hkv;
+    p.G = pl.G;
+    p.T = pl.T;
+    p.max_len = c->max_len;
+    p.R = pl.R;
+    p.RPB = pl.RPB;
+    p.RB = pl.RB;
+    p.NB = pl.NB;
+    p.scale_log2 = static_cast<float>(1.4426950408889634 / sqrt(static_cast<double>(c->d)));
+    long long tiles = 0;
+    for (int b = 0; b < c->B; ++b) {
+        p.prior[b] = static_cast<int>(lens[b] - n_new[b]);
+        p.n_new[b] = n_new[b];
+    }
+    for (int b = 0; b < c->B; ++b) {
+        for (int rb = 0; rb < pl.RB; ++rb) {
+            // Extent of the row block: one past the largest visible key of its valid rows.
+            int extent = 0;
+            const int r0 = rb * pl.RPB, r1 = std::min(pl.R, r0 + pl.RPB);
+            if (r1 - r0 >= pl.T) {
+                if (n_new[b] > 0) extent = p.prior[b] + std::min(pl.T, static_cast<int>(n_new[b]));
+            } else {
+                for (int r = r0; r < r1; ++r) {
+                    const int t = r % pl.T;
+                    if (t < n_new[b]) extent = std::max(extent, p.prior[b] + t + 1);
+                }
+            }
+            p.gstart[b * pl.RB + rb] = static_cast<int>(tiles);
+            tiles += static_cast<long long>((extent + kKeyTile - 1) / kKeyTile) * c->Hkv;
+        }
+    }
+    if (tiles > 0x7fffffffll) return fail(KVC_ERR_ARG, "too many key tiles in one call");
+    p.gstart[pl.NB] = static_cast<int>(tiles);
+    p.total_tiles = static_cast<int>(tiles);
+    // At most one CTA per SM, and never more CTAs than tiles: then every CTA
+    // owns at least one tile, so the CTAs covering a unit's tiles are exactly
+    // the contiguous range cta_of(first tile) .. cta_of(last tile), all of
+    // which contribute a partial.
+    const int grid = static_cast<int>(std::max(1ll, std::min<long long>(c->num_sms, tiles)));
+    p.num_ctas = grid;
+
+    if (ws != c->last_ws) {
+        // New workspace: clear the error word and the per-unit counters once;
+        // every later call leaves them zero again.
+        cudaError_t e = cudaMemsetAsync(ws, 0, pl.ws_err + pl.ws_counters, stream);
+        if (e != cudaSuccess) return cuda_fail(e, "cudaMemsetAsync(workspace)");
+        c->last_ws = ws;
+    }
+    cudaError_t e = launch_decode_bf16(p, c->tmK[layer], c->tmV[layer], pl.mt, grid, stream);
+    if (e != cudaSuccess) return cuda_fail(e, "split-KV attention launch");
+    (void)ws_bytes;
+    return ok();
+}
+
+kvc_status check_workspace(const kvc_cache* c, const AttnPlan& pl, const void* ws, size_t ws_bytes) {
+    if (c->dtype != KVC_BF16 || c->B == 0 || pl.T == 0) return ok();
+    if (!ws) return fail(KVC_ERR_WORKSPACE, "workspace is null (need %zu bytes)", pl.ws_total);
+    if ((reinterpret_cast<uintptr_t>(ws) & 255u) != 0) return fail(KVC_ERR_WORKSPACE, "workspace not 256-byte aligned");
+    if (ws_bytes < pl.ws_total)
+        return fail(KVC_ERR_WORKSPACE, "workspace has %zu bytes, needs %zu", ws_bytes, pl.ws_total);
+    return ok();
+}
+
+}  // namespace
+
+// ===========================================================================
+// C ABI
+// ===========================================================================
+
+extern "C" {
+
+kvc_status kvc_create(kvc_cache** out, int layers, int batch, int kv_heads, int max_len, int head_dim,
+                      kvc_dtype dtype, void* const* k_bufs, void* const* v_bufs) {
+    if (!out) return fail(KVC_ERR_ARG, "out is null");
+    *out = nullptr;
+    if (layers < 1 || batch < 0 || kv_heads < 1 || max_len < 1 || head_dim < 1)
+        return fail(KVC_ERR_ARG, "bad geometry: layers=%d batch=%d kv_heads=%d max_len=%d head_dim=%d", layers, batch,
+                    kv_heads, max_len, head_dim);
+    if (batch > KVC_MAX_BATCH) return fail(KVC_ERR_ARG, "batch %d > %d", batch, KVC_MAX_BATCH);
+    if (dtype != KVC_F32 && dtype != KVC_BF16) return fail(KVC_ERR_ARG, "unknown dtype %d", static_cast<int>(dtype));
+    const int esize = dtype == KVC_F32 ? 4 : 2;
+    if ((head_dim * esize) % 16 != 0) return fail(KVC_ERR_ARG, "head_dim * element size must be a multiple of 16");
+    if (dtype == KVC_F32 && head_dim > 256) return fail(KVC_ERR_ARG, "f32 path takes head_dim <= 256");
+    if (dtype == KVC_BF16 && head_dim != kHeadDimBf16)
+        return fail(KVC_ERR_ARG, "bf16 path takes head_dim = %d", kHeadDimBf16);
+    const long long rows = static_cast<long long>(batch) * kv_heads * max_len;
+    if (rows + kKeyTile >= (1ll << 31)) return fail(KVC_ERR_ARG, "batch * kv_heads * max_len too large");
+    if (!k_bufs || !v_bufs) return fail(KVC_ERR_ARG, "k_bufs / v_bufs is null");
+    for (int l = 0; l < layers; ++l) {
+        if (!k_bufs[l] || !v_bufs[l]) return fail(KVC_ERR_ARG, "layer %d buffer is null", l);
+        if (!aligned16(k_bufs[l]) || !aligned16(v_bufs[l]))
+            return fail(KVC_ERR_ARG, "layer %d buffer not 16-byte aligned", l);
+    }
+    kvc_cache* c = new kvc_cache;
+    c->layers = layers;
+    c->B = batch;
+    c->Hkv = kv_heads;
+    c->max_len = max_len;
+    c->d = head_dim;
+    c->dtype = dtype;
+    c->esize = esize;
+    c->k.assign(k_bufs, k_bufs + layers);
+    c->v.assign(v_bufs, v_bufs + layers);
+    c->lens.assign(static_cast<size_t>(layers) * batch, 0);
+    c->tmK.resize(layers);
+    c->tmV.resize(layers);
+    c->tm_ready.assign(layers, 0);
+    *out = c;
+    return ok();
+}
+
+void kvc_destroy(kvc_cache* c) { delete c; }
+
+kvc_status kvc_append(kvc_cache* c, int layer, const void* k_new, const void* v_new, int T, const int32_t* n_new,
+                      void* stream) {
+    int max_n = 0;
+    kvc_status s = validate_append(c, layer, k_new, v_new, T, n_new, &max_n);
+    if (s) return s;
+    if (max_n > 0) {
+        s = ensure_device(c);
+        if (s) return s;
+        s = do_append(c, layer, k_new, v_new, T, n_new, max_n, static_cast<cudaStream_t>(stream));
+        if (s) return s;
+    }
+    int64_t* lens = c->lens.data() + static_cast<size_t>(layer) * c->B;
+    for (int b = 0; b < c->B; ++b) lens[b] += n_new[b];
+    return ok();
+}
+
+size_t kvc_workspace_bytes(const kvc_cache* c, int q_heads, int T) {
+    if (!c) return 0;
+    if (c->dtype != KVC_BF16) return 0;
+    kvc_cache* mc = const_cast<kvc_cache*>(c);
+    if (ensure_device(mc) != KVC_OK) return 0;
+    AttnPlan pl;
+    if (plan_shape(c, q_heads, T, c->num_sms, &pl) != KVC_OK) return 0;
+    return pl.ws_total;
+}
+
+kvc_status kvc_gqa_attention(kvc_cache* c, int layer, const void* q, int q_heads, int T, const int32_t* n_new,
+                             void* out, void* workspace, size_t workspace_bytes, void* stream) {
+    kvc_status s = check_layer(c, layer);
+    if (s) return s;
+    AttnPlan pl;
+    const int64_t* lens = c->lens.data() + static_cast<size_t>(layer) * c->B;
+    s = validate_attention(c, layer, q, q_heads, T, n_new, out, lens, &pl, 0);
+    if (s) return s;
+    if (c->dtype == KVC_BF16 && c->B > 0 && T > 0) {
+        s = ensure_device(c);
+        if (s) return s;
+        s = plan_shape(c, q_heads, T, c->num_sms, &pl);
+        if (s) return s;
+    }
+    s = check_workspace(c, pl, workspace, workspace_bytes);
+    if (s) return s;
+    if (c->B == 0 || T == 0) return ok();
+    s = ensure_device(c);
+    if (s) return s;
+    return do_attention(c, layer, q, pl, n_new, out, workspace, workspace_bytes, static_cast<cudaStream_t>(stream));
+}
+
+kvc_status kvc_append_attention(kvc_cache* c, int layer, const void* q, const void* k_new, const void* v_new,
+                                int q_heads, int T, const int32_t* n_new, void* out, void* workspace,
+                                size_t workspace_bytes, void* stream) {
+    int max_n = 0;
+    kvc_status s = validate_append(c, layer, k_new, v_new, T, n_new, &max_n);
+    if (s) return s;
+    // Validate the attention step against the lengths the append will produce.
+    std::vector<int64_t> after(c->B);
+    const int64_t* lens = c->lens.data() + static_cast<size_t>(layer) * c->B;
+    for (int b = 0; b < c->B; ++b) after[b] = lens[b] + n_new[b];
+    AttnPlan pl;
+    s = validate_attention(c, layer, q, q_heads, T, n_new, out, after.data(), &pl, 0);
+    if (s) return s;
+    if (c->dtype == KVC_BF16 && c->B > 0 && T > 0) {
+        s = ensure_device(c);
+        if (s) return s;
+        s = plan_shape(c, q_heads, T, c->num_sms, &pl);
+        if (s) return s;
+    }
+    s = check_workspace(c, pl, workspace, workspace_bytes);
+    if (s) return s;
+    if (c->B == 0 || T == 0) {
+        return ok();
+    }
+    s = ensure_device(c);
+    if (s) return s;
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    s = do_append(c, layer, k_new, v_new, T, n_new, max_n, st);
+    if (s) return s;
+    int64_t* lw = c->lens.data() + static_cast<size_t>(layer) * c->B;
+    for (int b = 0; b < c->B; ++b) lw[b] += n_new[b];
+    s = do_attention(c, layer, q, pl, n_new, out, workspace, workspace_bytes, st);
+    if (s) {
+        // The append already ran on the stream; its lengths stand.
+        return s;
+    }
+    return ok();
+}
+
+kvc_status kvc_length(const kvc_cache* c, int64_t* out) {
+    if (!c || !out) return fail(KVC_ERR_ARG, "null argument");
+    for (int l = 1; l < c->layers; ++l)
+        for (int b = 0; b < c->B; ++b)
+            if (c->lens[static_cast<size_t>(l) * c->B + b] != c->lens[b])
+                return fail(KVC_ERR_LAYER_MISMATCH,
+                            "a forward pass stopped part-way: layer %d row %d has %lld tokens, layer 0 has %lld", l, b,
+                            static_cast<long long>(c->lens[static_cast<size_t>(l) * c->B + b]),
+                            static_cast<long long>(c->lens[b]));
+    for (int b = 0; b < c->B; ++b) out[b] = c->lens[b];
+    return ok();
+}
+
+kvc_status kvc_truncate(kvc_cache* c, const int64_t* new_lens) {
+    if (!c) return fail(KVC_ERR_ARG, "null cache handle");
+    if (c->B > 0 && !new_lens) return fail(KVC_ERR_ARG, "new_lens is null");
+    std::vector<int64_t> cur(c->B);
+    kvc_status s = kvc_length(c, cur.data());
+    if (s) return s;
+    for (int b = 0; b < c->B; ++b)
+        if (new_lens[b] < 0 || new_lens[b] > cur[b])
+            return fail(KVC_ERR_ARG, "row %d: invalid truncation length %lld (length %lld)", b,
+                        static_cast<long long>(new_lens[b]), static_cast<long long>(cur[b]));
+    for (int l = 0; l < c->layers; ++l)
+        for (int b = 0; b < c->B; ++b) c->lens[static_cast<size_t>(l) * c->B + b] = new_lens[b];
+    return ok();
+}
+
+kvc_status kvc_reset(kvc_cache* c) {
+    if (!c) return fail(KVC_ERR_ARG, "null cache handle");
+    std::fill(c->lens.begin(), c->lens.end(), 0);
+    return ok();
+}
+
+kvc_status kvc_set_lens(kvc_cache* c, int layer, const int64_t* lens) {
+    kvc_status s = check_layer(c, layer);
+    if (s) return s;
+    if (!lens && c->B > 0) return fail(KVC_ERR_ARG, "lens is null");
+    for (int b = 0; b < c->B; ++b)
+        if (lens[b] < 0 || lens[b] > c->max_len)
+            return fail(KVC_ERR_ARG, "row %d: length %lld outside 0..%d", b, static_cast<long long>(lens[b]),
+                        c->max_len);
+    for (int b = 0; b < c->B; ++b) c->lens[static_cast<size_t>(layer) * c->B + b] = lens[b];
+    return ok();
+}
+
+kvc_status kvc_get_lens(const kvc_cache* c, int layer, int64_t* out) {
+    kvc_status s = check_layer(c, layer);
+    if (s) return s;
+    if (!out && c->B > 0) return fail(KVC_ERR_ARG, "out is null");
+    for (int b = 0; b < c->B; ++b) out[b] = c->lens[static_cast<size_t>(layer) * c->B + b];
+    return ok();
+}
+
+kvc_status kvc_device_status(kvc_cache* c, void* workspace, void* stream, int32_t* code) {
+    if (!c || !workspace || !code) return fail(KVC_ERR_ARG, "null argument");
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    int32_t v = 0;
+    cudaError_t e = cudaMemcpyAsync(&v, workspace, sizeof v, cudaMemcpyDeviceToHost, st);
+    if (e == cudaSuccess) e = cudaStreamSynchronize(st);
+    if (e != cudaSuccess) return cuda_fail(e, "reading the device error word");
+    *code = v;
+    if (v != 0) {
+        // An interrupted call may have left unit counters set: make the next
+        // call on this handle clear the workspace header again.
+        c->last_ws = nullptr;
+        e = cudaMemsetAsync(workspace, 0, sizeof v, st);
+        if (e == cudaSuccess) e = cudaStreamSynchronize(st);
+        if (e != cudaSuccess) return cuda_fail(e, "clearing the device error word");
+        return fail(KVC_ERR_DEVICE_TIMEOUT, "a kernel's bounded wait expired (code %d)", v);
+    }
+    return ok();
+}
+
+kvc_status kvc_selftest_bounded_wait(void* workspace, uint64_t limit_ns, void* stream) {
+    if (!workspace) return fail(KVC_ERR_ARG, "workspace is null");
+    cudaError_t e = launch_wait_selftest(static_cast<int*>(workspace), limit_ns, static_cast<cudaStream_t>(stream));
+    if (e != cudaSuccess) return cuda_fail(e, "self-test launch");
+    return ok();
+}
+
+const char* kvc_last_error(void) { return g_last_error.c_str(); }
+
+const char* kvc_version(void) { return "kvc 0.1 (sm_103a)"; }
+
+}  // extern "C"

@@ -1,0 +1,106 @@
+// Internal declarations shared by the host library and the kernels of libkvc.
+#pragma once
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "kvc.h"
+
+namespace kvc {
+
+constexpr int kMaxBatch = KVC_MAX_BATCH;
+constexpr int kMaxGroups = 1024;  // (row, row-block) groups of one attention call
+
+// Keys per K/V tile of the split-KV kernel, and the head width it is built for.
+constexpr int kKeyTile = 64;
+constexpr int kHeadDimBf16 = 128;
+
+// ---------------------------------------------------------------------------
+// In-place append: k_new/v_new [B, Hkv, T, d] -> cache rows lens[b] .. lens[b]+n_new[b]-1.
+// ---------------------------------------------------------------------------
+struct AppendParams {
+    const uint8_t* k_new;
+    const uint8_t* v_new;
+    uint8_t* k_cache;
+    uint8_t* v_cache;
+    int B, Hkv, T, max_len;
+    int row_bytes;  // d * element size, a multiple of 16
+    int lens[kMaxBatch];
+    int n_new[kMaxBatch];
+};
+
+cudaError_t launch_append(const AppendParams& p, int max_n_new, cudaStream_t stream);
+
+// ---------------------------------------------------------------------------
+// Split-KV attention (bf16 storage, fp32 accumulation).
+//
+// Rows.  For one KV head the G*T query rows are r = g*T + t (query head
+// kvh*G + g, query t).  Rows are cut into row blocks of RPB = 16*MT rows.
+// A "group" is one (b, row block); a "unit" is one (group, kvh); unit
+// u = group*Hkv + kvh.  A unit's keys are 0 .. E-1 where E is one past the
+// largest visible key of its valid rows; it has nt = ceil(E / 64) tiles.
+// Tiles are numbered unit after unit: group q's units own tiles
+// gstart[q] .. gstart[q+1]-1, kvh after kvh.  CTA i of P processes tiles
+// floor(i*N/P) .. floor((i+1)*N/P)-1, so every CTA gets the same number of
+// tiles (+-1) whatever the row lengths.
+// ---------------------------------------------------------------------------
+struct DecodeParams {
+    const void* q;      // [B, Hq, T, d] bf16
+    void* out;          // [B, Hq, T, d] bf16
+    float* partials;    // [(units + P) slots][RPB rows][d + 2] : O (d), m, l
+    int* counters;      // [units] contributor counters, zero between calls
+    int* err;           // device error word
+    int B, Hq, Hkv, G, T, max_len;
+    int R, RPB, RB, NB;
+    int total_tiles;
+    int num_ctas;
+    float scale_log2;   // log2(e) / sqrt(d)
+    int prior[kMaxBatch];    // lens[b] - n_new[b]
+    int n_new[kMaxBatch];
+    int gstart[kMaxGroups + 1];
+};
+
+// Grid / block / shared memory of the split-KV kernel for a given MT.
+struct DecodeLaunch {
+    int mt;
+    int threads;
+    size_t smem_bytes;
+};
+DecodeLaunch decode_launch_shape(int mt);
+
+cudaError_t launch_decode_bf16(const DecodeParams& p, const CUtensorMap& tmK, const CUtensorMap& tmV, int mt,
+                               int grid, cudaStream_t stream);
+
+// ---------------------------------------------------------------------------
+// f32 attention (any d <= 256, d % 4 == 0): one CTA per (16-row block, kvh, b),
+// all keys of the unit, output written directly; no workspace.
+// ---------------------------------------------------------------------------
+struct F32Params {
+    const float* q;
+    const float* k_cache;
+    const float* v_cache;
+    float* out;
+    int B, Hq, Hkv, G, T, max_len, d;
+    int R;
+    float scale;  // 1 / sqrt(d)
+    int prior[kMaxBatch];
+    int n_new[kMaxBatch];
+};
+
+cudaError_t launch_attn_f32(const F32Params& p, cudaStream_t stream);
+
+// Device error codes written to the workspace error word.
+enum DeviceError : int {
+    kDevOk = 0,
+    kDevTimeoutFull = 1,   // consumer gave up waiting for a K/V tile
+    kDevTimeoutEmpty = 2,  // producer gave up waiting for a free stage
+    kDevTimeoutDrain = 3,  // abort path gave up waiting for copies in flight
+    kDevTimeoutTest = 4    // the self-test wait expired, as it is meant to
+};
+
+// Self-test of the bounded wait: waits on an mbarrier that nothing arrives at,
+// for at most `limit_ns`, then records kDevTimeoutTest in *err.
+cudaError_t launch_wait_selftest(int* err, unsigned long long limit_ns, cudaStream_t stream);
+
+}  // namespace kvc

@@ -1,0 +1,178 @@
+/*
+ * kvc.h -- grouped-query attention over a contiguous preallocated KV cache.
+ *
+ * C ABI of libkvc.so (GB300 / sm_103a).  Plain pointers and sizes only.
+ *
+ * The operation (three web pages, cited by title and section):
+ *  - "Implement grouped-query attention over a preallocated KV cache, with no
+ *    torch.cat, for both prefill chunks and decode" (inferenceinterviews.com),
+ *    section "A strong answer": K and V are allocated once as
+ *    [B, Hkv, max_len, d]; a call writes the new chunk in place at each row's
+ *    current length (KVCache.append) and then lets the chunk's T queries
+ *    attend (gqa_attention) with query head h reading KV head h / G
+ *    (G = Hq / Hkv), scores scaled by 1/sqrt(d), query t of row b at absolute
+ *    position lens[b] - n_new[b] + t, keys past lens[b] and padded queries
+ *    (t >= n_new[b]) masked, and fully masked queries returning zeros.
+ *  - "Write the causal mask for a decode step with a KV cache, where the query
+ *    is shorter than the keys" (inferenceinterviews.com), TL;DR and "A strong
+ *    answer": the mask is bottom-right aligned (key j visible to query i iff
+ *    j <= i + S - T) and lives in the kernel as index arithmetic.
+ *  - "16. Prefill, decode and the KV cache" (inference.shantanugoel.com),
+ *    "Layout and validity": one K/V buffer pair per layer, per-layer lengths,
+ *    a length query that refuses when layers disagree, truncate and reset.
+ *
+ * Layout.  Every tensor is dense, row-major, in the cache's element type
+ * (KVC_F32 = float, KVC_BF16 = bfloat16):
+ *   K, V cache of one layer   [B, Hkv, max_len, d]
+ *   k_new, v_new              [B, Hkv, T, d]
+ *   q, out                    [B, Hq, T, d]
+ * All device pointers must be 16-byte aligned.  d * sizeof(element) must be a
+ * multiple of 16.  The bf16 attention path takes d = 128 (the other sizes of
+ * d are served by the f32 path only).
+ *
+ * Ownership.  The caller allocates every device buffer (cache, inputs,
+ * outputs, workspace) and keeps it alive while the handle or a launched call
+ * uses it.  The handle owns only host state: per-layer, per-row lengths and
+ * launch descriptors.  kvc_destroy frees the handle, never a buffer.
+ *
+ * Lengths are host-authoritative.  kvc_append grows lens only after its
+ * kernel was enqueued successfully.  Kernels run asynchronously on the given
+ * stream (a cudaStream_t passed as void*, NULL = legacy default stream).
+ *
+ * Errors.  Every entry point returns a kvc_status and never throws.  All
+ * arguments are validated before anything is enqueued, so an error leaves
+ * cache data, lengths and outputs untouched (the pages' "appending past
+ * max_len raises and leaves the row's length unchanged", applied to every
+ * row).  kvc_last_error() gives a message for the calling thread's last
+ * failure.
+ */
+#ifndef KVC_H
+#define KVC_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum { KVC_F32 = 0, KVC_BF16 = 1 } kvc_dtype;
+
+typedef enum {
+    KVC_OK = 0,
+    KVC_ERR_ARG = 1,             /* bad pointer, size, dtype, alignment, layer index */
+    KVC_ERR_SHAPE = 2,           /* Hq not a multiple of Hkv, n_new outside 0..T, ... */
+    KVC_ERR_OVERFLOW = 3,        /* lens[b] + n_new[b] > max_len for some row */
+    KVC_ERR_LAYER_MISMATCH = 4,  /* layers disagree on a row's length */
+    KVC_ERR_CUDA = 5,            /* a CUDA runtime/driver call failed (no GPU, launch error) */
+    KVC_ERR_DEVICE_TIMEOUT = 6,  /* a kernel's bounded wait ran out (see kvc_device_status) */
+    KVC_ERR_WORKSPACE = 7        /* workspace missing, too small or misaligned */
+} kvc_status;
+
+/* Largest batch the attention kernels accept (per-row offsets travel as
+ * kernel parameters, so no device metadata buffer is needed). */
+#define KVC_MAX_BATCH 1024
+
+typedef struct kvc_cache kvc_cache;
+
+/* Create a handle over caller-owned cache buffers.
+ * k_bufs[l], v_bufs[l] (l < layers) each point to [B, Hkv, max_len, d]
+ * elements of `dtype` on the current device.  All lengths start at 0.
+ * No CUDA call is made here; device state (tensor-map descriptors, SM
+ * count) is set up on the first launch.
+ * Errors: KVC_ERR_ARG for non-positive sizes, B > KVC_MAX_BATCH, null or
+ * misaligned buffers, or d * element size not a multiple of 16. */
+kvc_status kvc_create(kvc_cache** out, int layers, int batch, int kv_heads, int max_len, int head_dim,
+                      kvc_dtype dtype, void* const* k_bufs, void* const* v_bufs);
+
+/* Free the handle (not the buffers).  NULL is accepted. */
+void kvc_destroy(kvc_cache* c);
+
+/* Append in place ("A strong answer", KVCache.append): for every row b and
+ * t < n_new[b], copy k_new[b, :, t, :] to K[b, :, lens[b] + t, :] (same for
+ * V), then lens[layer][b] += n_new[b].  n_new is a HOST array of B entries.
+ * The copy is bit-exact.  Rows with n_new[b] = 0 are untouched.
+ * Errors (nothing written, lens unchanged): KVC_ERR_ARG (layer, pointers,
+ * T < 0), KVC_ERR_SHAPE (n_new[b] < 0 or > T), KVC_ERR_OVERFLOW
+ * (lens[b] + n_new[b] > max_len for any row), KVC_ERR_CUDA (launch failed). */
+kvc_status kvc_append(kvc_cache* c, int layer, const void* k_new, const void* v_new, int T,
+                      const int32_t* n_new, void* stream);
+
+/* Bytes of device workspace kvc_gqa_attention needs for this handle, q_heads
+ * and T (split-KV partial results, per-unit counters and an error word).
+ * 0 means no workspace is needed (f32 path).  Returns 0 for invalid input. */
+size_t kvc_workspace_bytes(const kvc_cache* c, int q_heads, int T);
+
+/* Attention of the chunk just appended ("A strong answer", gqa_attention):
+ * q [B, Hq, T, d] -> out [B, Hq, T, d].  For t < n_new[b], out[b,h,t,:] is
+ * the softmax(q.K^T / sqrt(d)) weighted sum of V over keys
+ * 0 .. lens[b] - n_new[b] + t of KV head h / (Hq / Hkv); for t >= n_new[b]
+ * it is 0.  lens are the current lengths of `layer` (after the append).
+ * Accumulation is fp32; out has the cache's element type.
+ * workspace: device buffer of at least kvc_workspace_bytes(c, Hq, T) bytes,
+ * 256-byte aligned, used by one call at a time (calls that share a workspace
+ * must be ordered on one stream).  The library keeps its counters zero
+ * between calls; it clears them itself when a call sees a workspace pointer
+ * different from the previous call's.
+ * Errors (out untouched): KVC_ERR_ARG, KVC_ERR_SHAPE (Hq % Hkv != 0,
+ * n_new[b] < 0, n_new[b] > T, n_new[b] > lens[b]), KVC_ERR_WORKSPACE,
+ * KVC_ERR_CUDA. */
+kvc_status kvc_gqa_attention(kvc_cache* c, int layer, const void* q, int q_heads, int T,
+                             const int32_t* n_new, void* out, void* workspace, size_t workspace_bytes,
+                             void* stream);
+
+/* kvc_append followed by kvc_gqa_attention with the same n_new, validated
+ * together first: on any error neither step runs. */
+kvc_status kvc_append_attention(kvc_cache* c, int layer, const void* q, const void* k_new, const void* v_new,
+                                int q_heads, int T, const int32_t* n_new, void* out, void* workspace,
+                                size_t workspace_bytes, void* stream);
+
+/* Forget everything after new_lens[b] tokens of row b in every layer
+ * ("Layout and validity", truncate; speculative-decoding rollback).  No data
+ * moves.  Requires the layers to agree (else KVC_ERR_LAYER_MISMATCH) and
+ * 0 <= new_lens[b] <= length[b] (else KVC_ERR_ARG).  Host only. */
+kvc_status kvc_truncate(kvc_cache* c, const int64_t* new_lens);
+
+/* Set every length of every layer to 0 (truncate to 0).  Host only. */
+kvc_status kvc_reset(kvc_cache* c);
+
+/* Declare that the first lens[b] slots of every row of `layer` already hold
+ * valid K/V (written by another producer or restored from storage), i.e.
+ * set lens[layer][b] = lens[b].  Host only; no data moves.  Requires
+ * 0 <= lens[b] <= max_len (else KVC_ERR_ARG, nothing changed).  This is the
+ * one way to start from a non-empty cache without appending through it. */
+kvc_status kvc_set_lens(kvc_cache* c, int layer, const int64_t* lens);
+
+/* Copy lens[layer][0..B) into out (host array). */
+kvc_status kvc_get_lens(const kvc_cache* c, int layer, int64_t* out);
+
+/* Per-row length shared by all layers ("Layout and validity", length).
+ * KVC_ERR_LAYER_MISMATCH if a forward pass stopped part-way (layers differ). */
+kvc_status kvc_length(const kvc_cache* c, int64_t* out);
+
+/* Read the device error word of a workspace used by handle c after the
+ * stream's work ends: synchronizes `stream`, copies the word and stores it in
+ * *code (0 = clean; otherwise a kernel's bounded wait expired and that call's
+ * output is not valid), then clears the word and makes the handle's next call
+ * re-clear the workspace's counters.  Returns KVC_ERR_DEVICE_TIMEOUT when
+ * *code != 0. */
+kvc_status kvc_device_status(kvc_cache* c, void* workspace, void* stream, int32_t* code);
+
+/* Self-test of the kernels' bounded waits: launches one CTA that waits on an
+ * mbarrier nothing ever arrives at, for at most limit_ns nanoseconds, then
+ * writes its error code into the workspace's error word (the first 4 bytes),
+ * so a following kvc_device_status reports KVC_ERR_DEVICE_TIMEOUT.  No fault,
+ * no hang. */
+kvc_status kvc_selftest_bounded_wait(void* workspace, uint64_t limit_ns, void* stream);
+
+/* Message of the calling thread's last failed call ("" if none). */
+const char* kvc_last_error(void);
+
+/* Library version string. */
+const char* kvc_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* KVC_H */

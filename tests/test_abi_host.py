@@ -1,0 +1,189 @@
+"""CPU tests of the C ABI: the library loads, exports what include/kvc.h
+declares, and its host logic (validation, lengths, truncate, layer
+agreement) behaves as the pages state.  No compute call runs here: the
+buffer pointers are fake, and every call tested either fails validation
+before any CUDA call or is host-only.
+"""
+
+import ctypes
+import os
+import re
+
+import numpy as np
+import pytest
+
+from gqa_attention_preallocated_gb300 import _lib
+from gqa_attention_preallocated_gb300.build import build_library
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+I32P = ctypes.POINTER(ctypes.c_int32)
+I64P = ctypes.POINTER(ctypes.c_int64)
+
+
+@pytest.fixture(scope="module")
+def L():
+    build_library()
+    return _lib.lib()
+
+
+def _declared():
+    text = open(os.path.join(ROOT, "include", "kvc.h")).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(kvc_[a-z_]+)\s*\(", text)))
+
+
+def test_exports_every_declared_symbol(L):
+    declared = _declared()
+    assert "kvc_create" in declared and "kvc_gqa_attention" in declared
+    for name in declared:
+        assert hasattr(L, name), name
+    bound = {n for n, _, _ in _lib.SIGNATURES}
+    assert set(declared) == bound  # the binding covers exactly the header
+
+
+def _fake_buffers(layers):
+    # 16-byte aligned fake device addresses; never dereferenced by these tests
+    base = 1 << 40
+    k = (ctypes.c_void_p * layers)(*[base + (2 * i) * (1 << 30) for i in range(layers)])
+    v = (ctypes.c_void_p * layers)(*[base + (2 * i + 1) * (1 << 30) for i in range(layers)])
+    return k, v
+
+
+def _create(L, layers=2, B=3, Hkv=2, max_len=16, d=16, dtype=_lib.KVC_F32):
+    h = ctypes.c_void_p()
+    k, v = _fake_buffers(layers)
+    st = L.kvc_create(ctypes.byref(h), layers, B, Hkv, max_len, d, dtype, k, v)
+    return st, h
+
+
+def _i32(*xs):
+    a = np.array(xs, dtype=np.int32)
+    return a, a.ctypes.data_as(I32P)
+
+
+def _i64(*xs):
+    a = np.array(xs, dtype=np.int64)
+    return a, a.ctypes.data_as(I64P)
+
+
+def _lens(L, h, layer, B):
+    out = np.zeros(B, dtype=np.int64)
+    assert L.kvc_get_lens(h, layer, out.ctypes.data_as(I64P)) == 0
+    return out
+
+
+def test_create_validation(L):
+    h = ctypes.c_void_p()
+    k, v = _fake_buffers(1)
+    assert L.kvc_create(ctypes.byref(h), 0, 2, 2, 8, 16, 0, k, v) == 1
+    assert L.kvc_create(ctypes.byref(h), 1, 2, 2, 8, 6, 0, k, v) == 1  # 6 * 4 B not a multiple of 16
+    assert L.kvc_create(ctypes.byref(h), 1, 2, 2, 8, 64, 1, k, v) == 1  # bf16 path takes d = 128
+    assert L.kvc_create(ctypes.byref(h), 1, _lib.KVC_MAX_BATCH + 1, 2, 8, 16, 0, k, v) == 1
+    bad = (ctypes.c_void_p * 1)(12345)  # misaligned
+    assert L.kvc_create(ctypes.byref(h), 1, 2, 2, 8, 16, 0, bad, v) == 1
+    assert b"aligned" in L.kvc_last_error()
+    st, h = _create(L)
+    assert st == 0
+    L.kvc_destroy(h)
+    L.kvc_destroy(None)
+
+
+def test_append_validation_leaves_state(L):
+    st, h = _create(L, layers=1, B=3, max_len=10)
+    assert st == 0
+    _, full = _i64(8, 2, 10)
+    assert L.kvc_set_lens(h, 0, full) == 0
+    kn = ctypes.c_void_p(1 << 41)
+    # overflow in the last row: nothing changes, including the earlier rows
+    a, p = _i32(1, 1, 1)
+    assert L.kvc_append(h, 0, kn, kn, 3, p, None) == 3
+    assert b"max_len" in L.kvc_last_error()
+    assert list(_lens(L, h, 0, 3)) == [8, 2, 10]
+    # n_new outside 0..T
+    a, p = _i32(4, 0, 0)
+    assert L.kvc_append(h, 0, kn, kn, 3, p, None) == 2
+    a, p = _i32(-1, 0, 0)
+    assert L.kvc_append(h, 0, kn, kn, 3, p, None) == 2
+    # bad layer, T < 0, misaligned inputs
+    a, p = _i32(0, 0, 0)
+    assert L.kvc_append(h, 1, kn, kn, 3, p, None) == 1
+    assert L.kvc_append(h, 0, kn, kn, -1, p, None) == 1
+    a, p = _i32(1, 0, 0)
+    assert L.kvc_append(h, 0, ctypes.c_void_p((1 << 41) + 4), kn, 3, p, None) == 1
+    # all-zero n_new is a no-op that needs no GPU
+    a, p = _i32(0, 0, 0)
+    assert L.kvc_append(h, 0, None, None, 3, p, None) == 0
+    assert list(_lens(L, h, 0, 3)) == [8, 2, 10]
+    L.kvc_destroy(h)
+
+
+def test_attention_validation(L):
+    st, h = _create(L, layers=1, B=2, Hkv=2, max_len=10, d=16)
+    _, full = _i64(5, 0)
+    assert L.kvc_set_lens(h, 0, full) == 0
+    q = ctypes.c_void_p(1 << 42)
+    a, p = _i32(1, 0)
+    assert L.kvc_gqa_attention(h, 0, q, 3, 1, p, q, None, 0, None) == 2  # Hq % Hkv != 0
+    a, p = _i32(2, 0)
+    assert L.kvc_gqa_attention(h, 0, q, 4, 1, p, q, None, 0, None) == 2  # n_new > T
+    a, p = _i32(0, 1)
+    assert L.kvc_gqa_attention(h, 0, q, 4, 1, p, q, None, 0, None) == 2  # n_new > lens (row 1 empty)
+    a, p = _i32(1, 0)
+    assert L.kvc_gqa_attention(h, 0, None, 4, 1, p, q, None, 0, None) == 1  # null q
+    # T = 0 and an empty batch are valid no-ops
+    a, p = _i32(0, 0)
+    assert L.kvc_gqa_attention(h, 0, None, 4, 0, p, None, None, 0, None) == 0
+    L.kvc_destroy(h)
+    st, h0 = _create(L, layers=1, B=0)
+    assert st == 0
+    assert L.kvc_gqa_attention(h0, 0, None, 4, 3, None, None, None, 0, None) == 0
+    L.kvc_destroy(h0)
+
+
+def test_append_attention_validates_both_steps_first(L):
+    st, h = _create(L, layers=1, B=2, Hkv=2, max_len=10, d=16)
+    kn = ctypes.c_void_p(1 << 41)
+    a, p = _i32(1, 1)
+    # the attention step is invalid (Hq = 3): the append must not happen
+    assert L.kvc_append_attention(h, 0, kn, kn, kn, 3, 1, p, kn, None, 0, None) == 2
+    assert list(_lens(L, h, 0, 2)) == [0, 0]
+    L.kvc_destroy(h)
+
+
+def test_set_lens_truncate_reset_length(L):
+    st, h = _create(L, layers=3, B=2, max_len=16)
+    for layer in range(3):
+        _, p = _i64(7, 3)
+        assert L.kvc_set_lens(h, layer, p) == 0
+    out = np.zeros(2, dtype=np.int64)
+    assert L.kvc_length(h, out.ctypes.data_as(I64P)) == 0 and list(out) == [7, 3]
+    _, p = _i64(17, 0)
+    assert L.kvc_set_lens(h, 0, p) == 1  # past max_len
+    # a forward pass that stopped part-way: layer 0 ahead of the others
+    _, p = _i64(8, 4)
+    assert L.kvc_set_lens(h, 0, p) == 0
+    assert L.kvc_length(h, out.ctypes.data_as(I64P)) == 4
+    assert b"part-way" in L.kvc_last_error()
+    _, p = _i64(2, 2)
+    assert L.kvc_truncate(h, p) == 4  # refuses while layers disagree
+    _, p = _i64(7, 3)
+    assert L.kvc_set_lens(h, 0, p) == 0
+    _, p = _i64(8, 3)
+    assert L.kvc_truncate(h, p) == 1  # cannot grow
+    _, p = _i64(-1, 3)
+    assert L.kvc_truncate(h, p) == 1
+    _, p = _i64(5, 0)
+    assert L.kvc_truncate(h, p) == 0
+    for layer in range(3):
+        assert list(_lens(L, h, layer, 2)) == [5, 0]
+    assert L.kvc_reset(h) == 0
+    assert L.kvc_length(h, out.ctypes.data_as(I64P)) == 0 and list(out) == [0, 0]
+    assert L.kvc_get_lens(h, 3, out.ctypes.data_as(I64P)) == 1
+    L.kvc_destroy(h)
+
+
+def test_workspace_query_without_gpu_or_for_f32(L):
+    st, h = _create(L, dtype=_lib.KVC_F32)
+    assert L.kvc_workspace_bytes(h, 4, 1) == 0  # the f32 path needs no workspace
+    L.kvc_destroy(h)
+    assert L.kvc_workspace_bytes(None, 4, 1) == 0

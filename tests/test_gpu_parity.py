@@ -1,0 +1,347 @@
+"""GPU parity: the CUDA path through the C ABI against the float64 CPU oracle.
+
+Every input comes from the seeded generators in ``workloads``; the oracle
+sees the values exactly as stored (bf16 or fp32 widened to float64), so only
+kernel error is measured.  Bars (stated for this method): the append and all
+lengths bit-exact; outputs within max-abs 1e-4 for fp32 storage and 2e-2 for
+bf16 storage; padded queries exactly 0.
+
+Cache slots past the valid lengths are filled with NaN before each case
+("poison"), so any output that touched them fails.
+"""
+
+import math
+
+import numpy as np
+import pytest
+import torch
+
+import oracle.ref as ref
+from gqa_attention_preallocated_gb300 import KVCache, KVCError
+from gqa_attention_preallocated_gb300 import workloads as wl
+
+pytestmark = pytest.mark.gpu
+
+TOL = {torch.float32: 1e-4, torch.bfloat16: 2e-2}
+
+
+def _cuda_or_skip():
+    if not torch.cuda.is_available():
+        pytest.skip("needs a GPU")
+
+
+def _store(x64, dtype):
+    return wl.to_storage(x64, dtype)
+
+
+def _run_calls(seed, B, Hkv, G, d, max_len, dtype, calls, poison=True):
+    """Feed the same appends+queries to the GPU cache and the oracle; compare every call."""
+    _cuda_or_skip()
+    cache = KVCache(1, B, Hkv, max_len, d, dtype=dtype)
+    if poison:
+        cache.k[0].fill_(float("nan"))
+        cache.v[0].fill_(float("nan"))
+    orc = ref.OracleCache(1, B, Hkv, max_len, d)
+    tol = TOL[dtype]
+    worst = 0.0
+    for ci, n_new in enumerate(calls):
+        n_new = np.asarray(n_new, dtype=np.int64)
+        T = int(n_new.max()) if B else 0
+        k_new = _store(wl.normal(seed, 100 + 3 * ci, (B, Hkv, T, d)), dtype)
+        v_new = _store(wl.normal(seed, 101 + 3 * ci, (B, Hkv, T, d)), dtype)
+        q = _store(wl.normal(seed, 102 + 3 * ci, (B, Hkv * G, T, d)), dtype)
+        out = cache.append_attention(0, q.cuda(), k_new.cuda(), v_new.cuda(), n_new)
+        want = ref.append_attention(orc, 0, q.double().numpy(), k_new.double().numpy(), v_new.double().numpy(), n_new)
+        got = out.double().cpu().numpy()
+        assert np.array_equal(cache.lens(0), orc.lens[0])
+        for b in range(B):
+            assert np.all(got[b, :, n_new[b]:] == 0.0), "padded queries must be exactly 0"
+        assert np.all(np.isfinite(got))
+        err = float(np.max(np.abs(got - want))) if got.size else 0.0
+        worst = max(worst, err)
+        assert err <= tol, (ci, err)
+    # cache state: every valid slot bit-exact
+    lens = cache.lens(0)
+    kc = cache.k[0].double().cpu().numpy()
+    vc = cache.v[0].double().cpu().numpy()
+    for b in range(B):
+        L = int(lens[b])
+        assert np.array_equal(kc[b, :, :L], orc.k[0][b, :, :L])
+        assert np.array_equal(vc[b, :, :L], orc.v[0][b, :, :L])
+    assert cache.device_status() == 0
+    return worst
+
+
+# ---------------------------------------------------------------------------
+# Tiny ragged configuration (fp32, d = 16) and the pages' randomized trials
+# ---------------------------------------------------------------------------
+
+
+@pytest.mark.parametrize("seed", range(12))
+def test_tiny_ragged_f32(seed):
+    s = wl.TINY
+    _, calls = wl.tiny_schedule(seed, s.B)
+    _run_calls(seed, s.B, s.Hkv, s.G, s.d, s.max_len, torch.float32, calls)
+
+
+def test_randomized_trials_f32():
+    for seed in range(40):
+        B, Hkv, G, d = wl.trial_geometry(seed)
+        _, calls = wl.tiny_schedule(seed, B)
+        _run_calls(seed, B, Hkv, G, d, 48, torch.float32, calls)
+
+
+# ---------------------------------------------------------------------------
+# bf16 split-KV kernel, small sizes that still span many tiles and CTAs
+# ---------------------------------------------------------------------------
+
+
+@pytest.mark.parametrize(
+    "B,Hkv,G,chunks",
+    [
+        (3, 2, 4, [300, 1, 1, 1]),  # prefill then decode (G*T = 4 rows)
+        (2, 1, 8, [130, 4, 8, 1]),  # MQA, verify chunks (32 and 64 rows)
+        (3, 4, 1, [77, 5, 16, 1]),  # MHA
+        (2, 2, 4, [520, 37, 100]),  # several row blocks per unit, ragged tails
+        (1, 8, 4, [1, 63, 64, 65, 129]),  # tile boundaries
+    ],
+)
+def test_bf16_chunked(B, Hkv, G, chunks):
+    rng = np.random.default_rng(B * 100 + Hkv * 10 + G)
+    calls = []
+    for c in chunks:
+        n = rng.integers(max(0, c - 3), c + 1, size=B)
+        n[0] = c  # T = c
+        calls.append(n)
+    max_len = int(sum(chunks)) + 7
+    _run_calls(11, B, Hkv, G, 128, max_len, torch.bfloat16, calls)
+
+
+def test_bf16_rows_with_zero_tokens_and_empty_rows():
+    calls = [np.array([0, 5, 0]), np.array([3, 0, 0]), np.array([1, 1, 0])]
+    _run_calls(5, 3, 2, 4, 128, 40, torch.bfloat16, calls)
+
+
+def test_bf16_many_short_units_sole_path():
+    """Many units with total tiles >> SMs: most units finish inside one CTA."""
+    B, Hkv, G = 64, 8, 4
+    rng = np.random.default_rng(3)
+    first = rng.integers(60, 200, size=B)
+    calls = [first, np.ones(B, dtype=np.int64), np.ones(B, dtype=np.int64)]
+    _run_calls(7, B, Hkv, G, 128, 256, torch.bfloat16, calls)
+
+
+def test_incremental_equals_full_on_gpu():
+    """S = 37, T = 5: the chunked GPU output matches the full-sequence GPU output's last rows."""
+    _cuda_or_skip()
+    S, T, d, Hkv, G = 37, 5, 128, 2, 4
+    k = _store(wl.normal(3, 1, (1, Hkv, S, d)), torch.bfloat16).cuda()
+    v = _store(wl.normal(3, 2, (1, Hkv, S, d)), torch.bfloat16).cuda()
+    q = _store(wl.normal(3, 3, (1, Hkv * G, S, d)), torch.bfloat16).cuda()
+    full = KVCache(1, 1, Hkv, 64, d).append_attention(0, q, k, v, [S])
+    inc_cache = KVCache(1, 1, Hkv, 64, d)
+    inc_cache.append(0, k[:, :, : S - T].contiguous(), v[:, :, : S - T].contiguous(), [S - T])
+    inc = inc_cache.append_attention(0, q[:, :, S - T :].contiguous(), k[:, :, S - T :].contiguous(),
+                                     v[:, :, S - T :].contiguous(), [T])
+    assert float((inc.float() - full[:, :, S - T :].float()).abs().max()) <= 2e-2
+
+
+# ---------------------------------------------------------------------------
+# Errors leave everything unchanged; canaries around every buffer
+# ---------------------------------------------------------------------------
+
+
+def test_overflow_on_gpu_changes_nothing():
+    _cuda_or_skip()
+    c = KVCache(1, 2, 2, 10, 128)
+    k = _store(wl.normal(1, 1, (2, 2, 8, 128)), torch.bfloat16).cuda()
+    c.append(0, k, k, [8, 3])
+    before = c.k[0].clone()
+    with pytest.raises(KVCError) as e:
+        c.append(0, k, k, [1, 8])
+    assert e.value.status == 3
+    torch.cuda.synchronize()
+    assert torch.equal(c.k[0], before)
+    assert list(c.lens(0)) == [8, 3]
+
+
+def test_guard_regions_untouched():
+    _cuda_or_skip()
+    B, Hkv, G, d, max_len, T = 3, 2, 4, 128, 96, 9
+    pad = 4096
+    n_cache = B * Hkv * max_len * d
+    n_q = B * Hkv * G * T * d
+    sentinel = 1232.0  # exactly representable in bf16
+    bufs = {name: torch.full((n + 2 * pad,), sentinel, dtype=torch.bfloat16, device="cuda")
+            for name, n in (("k", n_cache), ("v", n_cache), ("out", n_q))}
+    view = lambda name, n, shape: bufs[name][pad : pad + n].view(shape)
+    k_buf = view("k", n_cache, (B, Hkv, max_len, d))
+    v_buf = view("v", n_cache, (B, Hkv, max_len, d))
+    out = view("out", n_q, (B, Hkv * G, T, d))
+    c = KVCache(1, B, Hkv, max_len, d, k_bufs=[k_buf], v_bufs=[v_buf])
+    for step, n in enumerate([[9, 4, 0], [9, 9, 9], [1, 2, 3]] * 3):
+        q = _store(wl.normal(2, step, (B, Hkv * G, T, d)), torch.bfloat16).cuda()
+        kn = _store(wl.normal(3, step, (B, Hkv, T, d)), torch.bfloat16).cuda()
+        c.append_attention(0, q, kn, kn, n, out=out)
+    torch.cuda.synchronize()
+    for name, t in bufs.items():
+        assert bool((t[:pad] == sentinel).all()) and bool((t[-pad:] == sentinel).all()), name
+
+
+# ---------------------------------------------------------------------------
+# Failure detection without a fault: the bounded wait expires and reports
+# ---------------------------------------------------------------------------
+
+
+def test_bounded_wait_reports_timeout():
+    _cuda_or_skip()
+    c = KVCache(1, 2, 2, 64, 128)
+    ws = c.workspace(8, 1)
+    assert c.device_status(ws) == 0
+    c.selftest_bounded_wait(10_000_000, ws)  # 10 ms
+    with pytest.raises(KVCError) as e:
+        c.device_status(ws)
+    assert e.value.status == 6
+    assert c.device_status(ws) == 0  # the word was cleared
+    # the context is still usable afterwards
+    k = _store(wl.normal(1, 1, (2, 2, 3, 128)), torch.bfloat16).cuda()
+    q = _store(wl.normal(1, 2, (2, 8, 3, 128)), torch.bfloat16).cuda()
+    out = c.append_attention(0, q, k, k, [3, 2])
+    assert bool(torch.isfinite(out.float()).all())
+
+
+# ---------------------------------------------------------------------------
+# Full-size workloads: sampled outputs against the oracle, one by one
+# ---------------------------------------------------------------------------
+
+
+def _seq_rows(seed, stream, B, H, max_len, d, b, h, lo, hi):
+    """Generator rows [lo, hi) of unit (b, h) of a [B, H, max_len, d] sequence tensor, float64 on CPU."""
+    base = ((b * H + h) * max_len + lo) * d
+    idx = torch.arange(base, base + (hi - lo) * d, dtype=torch.int64)
+    return wl.to_storage(wl.normal_at(seed, stream, idx), torch.bfloat16).double().reshape(hi - lo, d).numpy()
+
+
+def _fill_poisoned(cache, layer, seed, lens):
+    """Cache content from the generator; every slot at or past lens[b] set to NaN."""
+    wl.fill_normal_(cache.k[layer], seed, wl.STREAM_CACHE_K)
+    wl.fill_normal_(cache.v[layer], seed, wl.STREAM_CACHE_V)
+    for b, L in enumerate(lens):
+        cache.k[layer][b, :, int(L):] = float("nan")
+        cache.v[layer][b, :, int(L):] = float("nan")
+    cache.set_lens(layer, lens)
+
+
+def _new_tokens(seed, step, B, Hkv, T, d):
+    """Appended K/V of one step, generated on the CPU (the oracle regenerates the same values)."""
+    k = _store(wl.normal(seed, 1000 + 2 * step, (B, Hkv, T, d)), torch.bfloat16)
+    v = _store(wl.normal(seed, 1001 + 2 * step, (B, Hkv, T, d)), torch.bfloat16)
+    return k, v
+
+
+def _queries(seed, step, B, Hq, T, d):
+    return _store(wl.normal(seed, 5000 + step, (B, Hq, T, d)), torch.bfloat16)
+
+
+def _check_units(seed, shape, lens0, steps, q_last, n_last, out_last, units, T_last, Hq):
+    """Oracle check of every query row of the sampled (b, kvh) units after the last step.
+
+    The row's keys are the generator's cache content for positions < lens0[b]
+    and the appended tokens after that (step s wrote position lens0[b] + ...).
+    """
+    d, Hkv, G = shape.d, shape.Hkv, Hq // shape.Hkv
+    worst = 0.0
+    q_np = q_last.double().numpy()
+    got = out_last.double().cpu().numpy()
+    for b, kvh in units:
+        L0 = int(lens0[b])
+        K = [_seq_rows(seed, wl.STREAM_CACHE_K, shape.B, Hkv, shape.max_len, d, b, kvh, 0, L0)]
+        V = [_seq_rows(seed, wl.STREAM_CACHE_V, shape.B, Hkv, shape.max_len, d, b, kvh, 0, L0)]
+        for step, (nn, T) in enumerate(steps):
+            kn, vn = _new_tokens(seed, step, shape.B, Hkv, T, d)
+            K.append(kn[b, kvh, : nn[b]].double().cpu().numpy())
+            V.append(vn[b, kvh, : nn[b]].double().cpu().numpy())
+        K = np.concatenate(K)
+        V = np.concatenate(V)
+        L = K.shape[0]
+        for g in range(G):
+            h = kvh * G + g
+            for t in range(T_last):
+                if t >= n_last[b]:
+                    assert np.all(got[b, h, t] == 0.0)
+                    continue
+                pos = ref.query_position(L, int(n_last[b]), t)
+                want = ref.attend_one_query(q_np[b, h, t], K, V, pos)
+                worst = max(worst, float(np.max(np.abs(got[b, h, t] - want))))
+    assert worst <= 2e-2, worst
+    return worst
+
+
+def _decode_case(shape, Hq, lens0, steps_T, n_steps_list, seed, units):
+    _cuda_or_skip()
+    cache = KVCache(1, shape.B, shape.Hkv, shape.max_len, shape.d)
+    _fill_poisoned(cache, 0, seed, lens0)
+    steps = []
+    out = q = None
+    for step, nn in enumerate(n_steps_list):
+        T = int(steps_T[step])
+        kn, vn = _new_tokens(seed, step, shape.B, shape.Hkv, T, shape.d)
+        q = _queries(seed, step, shape.B, Hq, T, shape.d)
+        out = cache.append_attention(0, q.cuda(), kn.cuda(), vn.cuda(), nn)
+        steps.append((nn, T))
+    torch.cuda.synchronize()
+    assert np.array_equal(cache.lens(0), lens0 + sum(np.asarray(n) for n, _ in steps))
+    assert bool(torch.isfinite(out.float()).all())
+    assert cache.device_status() == 0
+    return _check_units(seed, shape, lens0, steps, q, np.asarray(n_steps_list[-1]), out, units, int(steps_T[-1]), Hq)
+
+
+def test_decode_llama8b_shape_sampled():
+    s = wl.DECODE_8B
+    lens0 = wl.decode_lens(0, s.B, 1024, s.max_len - 256)
+    n_steps = [np.ones(s.B, dtype=np.int64)] * 3
+    rng = np.random.default_rng(1)
+    units = [(int(b), int(h)) for b, h in zip(rng.integers(0, s.B, 6), rng.integers(0, s.Hkv, 6))]
+    units.append((int(np.argmax(lens0)), 7))
+    _decode_case(s, s.Hq, lens0, [1, 1, 1], n_steps, 0, units)
+
+
+@pytest.mark.parametrize("T", [4, 8])
+@pytest.mark.parametrize("Hq", [8, 16, 32, 64])
+def test_verify_sampled_and_rollback(T, Hq):
+    s = wl.VERIFY
+    _cuda_or_skip()
+    lens0 = np.full(s.B, s.max_len - T, dtype=np.int64)
+    nn = np.full(s.B, T, dtype=np.int64)
+    units = [(0, 0), (37, 5), (63, 7)]
+    _decode_case(s, Hq, lens0, [T], [nn], 2, units)
+
+
+def test_verify_truncate_loop():
+    """Append T -> attend -> truncate back, repeatedly: lengths and outputs stay consistent."""
+    _cuda_or_skip()
+    s = wl.VERIFY
+    B, T = 8, 4
+    cache = KVCache(1, B, s.Hkv, s.max_len, s.d)
+    lens0 = np.full(B, s.max_len - T, dtype=np.int64)
+    _fill_poisoned(cache, 0, 4, lens0)
+    outs = []
+    for rep in range(3):
+        kn, vn = _new_tokens(4, 0, B, s.Hkv, T, s.d)
+        q = _queries(4, 0, B, s.Hq, T, s.d)
+        outs.append(cache.append_attention(0, q.cuda(), kn.cuda(), vn.cuda(), np.full(B, T)))
+        assert list(cache.length()) == [s.max_len] * B
+        cache.truncate(lens0)
+        assert list(cache.length()) == list(lens0)
+    torch.cuda.synchronize()
+    assert torch.equal(outs[0], outs[1]) and torch.equal(outs[1], outs[2])
+
+
+@pytest.mark.parametrize("ragged", [False, True])
+def test_prefill_chunk_sampled(ragged):
+    s = wl.PREFILL
+    priors = wl.prefill_priors(0, s.B)
+    T = 512
+    nn = wl.ragged_chunk(0, s.B) if ragged else np.full(s.B, T, dtype=np.int64)
+    units = [(int(np.argmax(priors)), 3), (int(np.argmin(priors)), 0)]
+    _decode_case(s, s.Hq, priors, [T], [nn], 3, units)
