@@ -160,6 +160,25 @@ class KVCache:
                                       _ptr(ws), 0 if ws is None else ws.numel(), _stream_ptr(self.device, stream)))
         return out
 
+    def gqa_attention_noalloc(self, layer: int, q: torch.Tensor, n_new, out: torch.Tensor | None = None,
+                              stream=None) -> torch.Tensor:
+        """``gqa_attention`` through the allocation-free entry point (library-owned static scratch).
+
+        For callers that cannot allocate device memory; ``out`` must then be
+        passed in.  Shapes whose scratch exceeds the static array are rejected.
+        """
+        if q.dim() != 4:
+            raise KVCError(1, "q must be [B, Hq, T, d]")
+        B, Hq, T, d = q.shape
+        self._check_tensor(q, (self.B, Hq, T, self.d), "q")
+        if out is None:
+            out = torch.empty_like(q)
+        self._check_tensor(out, q.shape, "out")
+        nn = _i32(n_new, self.B)
+        check(lib().kvc_gqa_attention_noalloc(self._h, layer, _ptr(q), Hq, T, nn.ctypes.data_as(_I32P), _ptr(out),
+                                              _stream_ptr(self.device, stream)))
+        return out
+
     def append_attention(self, layer: int, q: torch.Tensor, k_new: torch.Tensor, v_new: torch.Tensor, n_new,
                          out: torch.Tensor | None = None, workspace: torch.Tensor | None = None,
                          stream=None) -> torch.Tensor:

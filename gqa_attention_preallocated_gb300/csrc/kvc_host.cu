@@ -17,6 +17,7 @@
 #include <string.h>
 
 #include <algorithm>
+#include <mutex>
 #include <string>
 #include <vector>
 
@@ -567,3 +568,73 @@ const char* kvc_last_error(void) { return g_last_error.c_str(); }
 const char* kvc_version(void) { return "kvc 0.1 (sm_103a)"; }
 
 }  // extern "C"
+
+// ===========================================================================
+// Allocation-free attention (kvc_gqa_attention_noalloc)
+//
+// For callers that cannot allocate device memory themselves: the split-KV
+// scratch (error word, unit counters, partial results) lives in one
+// file-scope device array instead of a caller-provided workspace.  The array
+// is part of this library's device image, so every GPU that loads the
+// library holds its KVC_NOALLOC_SCRATCH_BYTES until the process exits.
+// ===========================================================================
+
+static __device__ __align__(256) unsigned char kvc_noalloc_scratch[KVC_NOALLOC_SCRATCH_BYTES];
+
+namespace {
+
+constexpr int kNoAllocMaxDevices = 64;
+std::mutex g_noalloc_mutex;
+void* g_noalloc_addr[kNoAllocMaxDevices] = {};
+
+// Device address of the scratch array on the current device.  In host code
+// the array's name only stands for the symbol; the address a kernel can use
+// comes from cudaGetSymbolAddress, looked up once per device with that
+// device current and cached.
+kvc_status noalloc_scratch_address(int device, void** out) {
+    if (device < 0 || device >= kNoAllocMaxDevices) return fail(KVC_ERR_ARG, "device %d out of range", device);
+    std::lock_guard<std::mutex> lock(g_noalloc_mutex);
+    if (!g_noalloc_addr[device]) {
+        void* addr = nullptr;
+        cudaError_t e = cudaGetSymbolAddress(&addr, kvc_noalloc_scratch);
+        if (e != cudaSuccess) return cuda_fail(e, "cudaGetSymbolAddress(static scratch)");
+        g_noalloc_addr[device] = addr;
+    }
+    *out = g_noalloc_addr[device];
+    return ok();
+}
+
+}  // namespace
+
+extern "C" kvc_status kvc_gqa_attention_noalloc(kvc_cache* c, int layer, const void* q, int q_heads, int T,
+                                                const int32_t* n_new, void* out, void* stream) {
+    kvc_status s = check_layer(c, layer);
+    if (s) return s;
+    if (c->dtype != KVC_BF16) return fail(KVC_ERR_ARG, "the allocation-free variant serves bf16 caches only");
+    AttnPlan pl;
+    const int64_t* lens = c->lens.data() + static_cast<size_t>(layer) * c->B;
+    s = validate_attention(c, layer, q, q_heads, T, n_new, out, lens, &pl, 0);
+    if (s) return s;
+    if (c->B == 0 || T == 0) return ok();
+    s = ensure_device(c);
+    if (s) return s;
+    int dev = -1;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaGetDevice");
+    if (dev != c->device) return fail(KVC_ERR_ARG, "current device %d is not the cache's device %d", dev, c->device);
+    s = plan_shape(c, q_heads, T, c->num_sms, &pl);
+    if (s) return s;
+    if (pl.ws_total > static_cast<size_t>(KVC_NOALLOC_SCRATCH_BYTES))
+        return fail(KVC_ERR_WORKSPACE, "this call needs %zu bytes of scratch; the static scratch holds %zu",
+                    pl.ws_total, static_cast<size_t>(KVC_NOALLOC_SCRATCH_BYTES));
+    void* scratch = nullptr;
+    s = noalloc_scratch_address(dev, &scratch);
+    if (s) return s;
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    // The array keeps whatever the previous call left: zero the error word and
+    // the unit counters, which the kernel needs to start at zero.
+    e = cudaMemsetAsync(scratch, 0, pl.ws_err + pl.ws_counters, st);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaMemsetAsync(static scratch)");
+    c->last_ws = scratch;
+    return do_attention(c, layer, q, pl, n_new, out, scratch, KVC_NOALLOC_SCRATCH_BYTES, st);
+}

@@ -127,6 +127,35 @@ kvc_status kvc_append_attention(kvc_cache* c, int layer, const void* q, const vo
                                 int q_heads, int T, const int32_t* n_new, void* out, void* workspace,
                                 size_t workspace_bytes, void* stream);
 
+/* Size of the device scratch array behind kvc_gqa_attention_noalloc. */
+#define KVC_NOALLOC_SCRATCH_BYTES (16u << 20)
+
+/* kvc_gqa_attention without a workspace argument, for callers that cannot
+ * allocate device memory: for instance a plugin inside a host program that
+ * owns the whole device-memory budget and gives libraries no allocator, or
+ * a latency-critical loop that must not pay cudaMalloc's cost and implicit
+ * synchronization.  The pages have no counterpart of this entry point; it
+ * computes exactly what kvc_gqa_attention computes (same kernel, same
+ * result) and serves bf16 caches only.
+ *
+ * Its scratch is one static device array of KVC_NOALLOC_SCRATCH_BYTES
+ * (16 MiB) inside the library: every GPU that loads the library holds it
+ * until the process exits.  No cudaMalloc, cudaFree or other allocating
+ * call is made.  A call whose split-KV scratch would exceed the array
+ * (kvc_workspace_bytes(c, q_heads, T) > KVC_NOALLOC_SCRATCH_BYTES, e.g.
+ * long prefill chunks) is rejected with KVC_ERR_WORKSPACE before anything
+ * is enqueued; decode and speculative-verify shapes fit.
+ *
+ * The first call on each device looks up the array's device address
+ * (cudaGetSymbolAddress, with that device current) and caches it; make that
+ * first call before any stream capture.  Every call on a device shares the
+ * one array, which keeps the last call's contents; each call clears the
+ * parts that must start at zero.  Calls that overlap on the GPU (different
+ * streams, or several caches at once) race on the array: order them on one
+ * stream.  The device must be the cache's device (else KVC_ERR_ARG). */
+kvc_status kvc_gqa_attention_noalloc(kvc_cache* c, int layer, const void* q, int q_heads, int T,
+                                     const int32_t* n_new, void* out, void* stream);
+
 /* Forget everything after new_lens[b] tokens of row b in every layer
  * ("Layout and validity", truncate; speculative-decoding rollback).  No data
  * moves.  Requires the layers to agree (else KVC_ERR_LAYER_MISMATCH) and

@@ -1,0 +1,76 @@
+"""The allocation-free attention entry point against the workspace one.
+
+kvc_gqa_attention_noalloc exists for callers that cannot allocate device
+memory (a host program that owns the whole device-memory budget, or a loop
+that cannot pay for cudaMalloc): its split-KV scratch is a static device
+array inside the library instead of a caller-provided workspace.  Here it is
+called through the C ABI on two calls in a row (different shapes, so the
+scratch is reused with a different layout) and must give the existing
+entry point's output within the bf16 tolerance of the parity tests.  This
+file is collected last on purpose; it passes alone or after the others.
+"""
+
+import ctypes
+
+import numpy as np
+import pytest
+import torch
+
+from gqa_attention_preallocated_gb300 import KVCache, _lib
+from gqa_attention_preallocated_gb300 import workloads as wl
+from gqa_attention_preallocated_gb300.build import build_library
+
+pytestmark = pytest.mark.gpu
+
+TOL_BF16 = 2e-2
+I32P = ctypes.POINTER(ctypes.c_int32)
+
+
+def _bf16(seed, stream, shape):
+    return wl.to_storage(wl.normal(seed, stream, shape), torch.bfloat16).cuda()
+
+
+def _noalloc(cache, q, n_new, out):
+    nn = np.ascontiguousarray(np.asarray(n_new, dtype=np.int32))
+    st = _lib.lib().kvc_gqa_attention_noalloc(cache._h, 0, q.data_ptr(), q.shape[1], q.shape[2],
+                                              nn.ctypes.data_as(I32P), out.data_ptr(),
+                                              torch.cuda.current_stream().cuda_stream)
+    return st
+
+
+def test_noalloc_matches_workspace_entry_point_twice():
+    if not torch.cuda.is_available():
+        pytest.skip("needs a GPU")
+    build_library()
+    B, Hkv, G, d, max_len = 8, 4, 4, 128, 2048
+    cache = KVCache(1, B, Hkv, max_len, d)
+    rng = np.random.default_rng(5)
+    prefill = rng.integers(600, 1500, size=B)
+    T0 = int(prefill.max())
+    cache.append(0, _bf16(1, 1, (B, Hkv, T0, d)), _bf16(1, 2, (B, Hkv, T0, d)), prefill)
+    for call, T in enumerate([1, 4]):  # decode, then speculative verify
+        n_new = np.full(B, T)
+        cache.append(0, _bf16(2, 10 + call, (B, Hkv, T, d)), _bf16(2, 20 + call, (B, Hkv, T, d)), n_new)
+        q = _bf16(3, 30 + call, (B, Hkv * G, T, d))
+        ref_out = cache.gqa_attention(0, q, n_new)
+        out = torch.full_like(q, float("nan"))
+        assert _noalloc(cache, q, n_new, out) == 0, _lib.lib().kvc_last_error()
+        torch.cuda.synchronize()
+        assert bool(torch.isfinite(out.float()).all())
+        err = float((out.float() - ref_out.float()).abs().max())
+        assert err <= TOL_BF16, (call, err)
+
+
+def test_noalloc_rejects_oversized_calls():
+    if not torch.cuda.is_available():
+        pytest.skip("needs a GPU")
+    build_library()
+    B, Hkv, G, d, T = 4, 8, 4, 128, 512  # a long prefill chunk needs more than the static scratch
+    cache = KVCache(1, B, Hkv, 1024, d)
+    cache.append(0, _bf16(1, 1, (B, Hkv, T, d)), _bf16(1, 2, (B, Hkv, T, d)), np.full(B, T))
+    assert cache.workspace_bytes(Hkv * G, T) > (16 << 20)
+    q = _bf16(3, 3, (B, Hkv * G, T, d))
+    out = torch.zeros_like(q)
+    assert _noalloc(cache, q, np.full(B, T), out) == 7  # KVC_ERR_WORKSPACE, nothing enqueued
+    torch.cuda.synchronize()
+    assert bool((out == 0).all())
