@@ -409,7 +409,7 @@ def main():
     roof["peak_source"] = f"{peak_kind} (MEASURED_PEAKS.json)" if peak_kind == "measured" else "fallback"
     roof["kernel"] = "decode_splitkv_bf16_kernel"
     roof["kernel_ms"] = attn_ms
-    roof["traffic"] = _committed_traffic(w)
+    roof["traffic"] = _committed_traffic(w, kb)
 
     line = {
         "metric": w.metric, "value": value, "unit": w.unit, "n_gpus": world, "steps": args.steps,
@@ -435,8 +435,12 @@ def main():
         torch.distributed.destroy_process_group()
 
 
-def _committed_traffic(w: Workload):
-    """DRAM bytes per launch from the committed ncu summary, if taken on the current kernel source."""
+def _committed_traffic(w: Workload, mean_kernel_bytes: float):
+    """DRAM bytes per launch from the committed ncu summary, if taken on the current kernel source.
+
+    The capture is one launch; its DRAM bytes are scaled to the average timed
+    launch by the ratio of algorithmic bytes (traffic grows with the live K/V).
+    """
     import hashlib
 
     path = os.path.join(ROOT, "profiles", f"traffic_{w.name}.txt")
@@ -447,7 +451,9 @@ def _committed_traffic(w: Workload):
     sha = hashlib.sha256(open(src, "rb").read()).hexdigest()[:16]
     if kv.get("kernel_source_sha256_16") != sha:
         return None
-    return float(kv["dram_bytes_per_launch"])
+    dram = float(kv["dram_bytes_per_launch"])
+    alg = float(kv.get("algorithmic_bytes_of_captured_launch", 0) or 0)
+    return dram * (mean_kernel_bytes / alg) if alg > 0 else dram
 
 
 if __name__ == "__main__":
