@@ -200,11 +200,17 @@ class Workload:
             return 4 * s.d * self.Hq * visible_pairs(self.lens0, self.n_new)
         return kv_bytes(self.lens_at(i), s.Hkv, s.d) * self.layers
 
+    @property
+    def fused(self):
+        """The library appends inside the attention launch when G*T <= 16 (warps own whole tiles)."""
+        return (self.Hq // self.shape.Hkv) * self.T <= 16
+
     def kernel_bytes(self, i):
-        """Algorithmic bytes of one attention launch: live K/V + q + out."""
+        """Algorithmic bytes of the timed attention call: live K/V + q + out (+ the append when fused)."""
         s = self.shape
         qo = 2 * s.B * self.Hq * self.T * s.d * 2
-        return kv_bytes(self.lens_at(i), s.Hkv, s.d) + qo
+        app = 2 * int(np.sum(self.n_new)) * s.Hkv * s.d * 2 * 2 if self.fused else 0
+        return kv_bytes(self.lens_at(i), s.Hkv, s.d) + qo + app
 
 
 def run_native(w: Workload, steps: int, warmup: int, rank: int, world: int):
@@ -219,50 +225,71 @@ def run_native(w: Workload, steps: int, warmup: int, rank: int, world: int):
     ws = cache.workspace(w.Hq, w.T)
     stream = torch.cuda.current_stream()
 
-    def one_step(i, ev=None):
+    def one_step(i):
+        # One pass of the whole path: append + attention for every layer (one
+        # C-ABI call per layer; the library fuses the append into the
+        # attention launch where warps own whole tiles).
         if i > 0 and i % w.rollback_every == 0:
             cache.truncate(w.lens0)
         j = i % n_distinct
         for layer in range(w.layers):
-            if ev is not None and layer == 0:
-                ev[0].record(stream)
-            cache.append(layer, k[j], v[j], w.n_new)
-            if ev is not None and layer == 0:
-                ev[1].record(stream)
-            cache.gqa_attention(layer, q[j], w.n_new, out=out, workspace=ws)
-            if ev is not None and layer == 0:
-                ev[2].record(stream)
+            cache.append_attention(layer, q[j], k[j], v[j], w.n_new, out=out, workspace=ws)
 
     for i in range(warmup):
         one_step(i)
     cache.truncate(w.lens0)
     torch.cuda.synchronize()
 
-    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(steps)]
+    # Timed region: K steps back to back, events only at its two ends.
     start, stop = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     if world > 1:
         torch.distributed.barrier()
     torch.cuda.synchronize()
+    launches0 = cache.kernel_launches()
     with ClockSampler(torch.cuda.current_device()) as clk:
         t_wall = time.perf_counter()
         start.record(stream)
         for i in range(steps):
-            one_step(i, evs[i])
+            one_step(i)
         stop.record(stream)
         torch.cuda.synchronize()
         t_wall = time.perf_counter() - t_wall
+    launches = cache.kernel_launches() - launches0
     if world > 1:
         torch.distributed.barrier()
     ms = start.elapsed_time(stop)
-    attn_ms = [e[1].elapsed_time(e[2]) for e in evs]
-    append_ms = [e[0].elapsed_time(e[1]) for e in evs]
+
+    # Kernel timing for the roofline: the same K steps again, with an event
+    # pair around the layer-0 attention call of every step (for fused steps
+    # the pair holds the attention kernel, which also appends, and the
+    # combine kernel; otherwise the append runs before the first event).
+    cache.truncate(w.lens0)
+    torch.cuda.synchronize()
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(steps)]
+    for i in range(steps):
+        if i > 0 and i % w.rollback_every == 0:
+            cache.truncate(w.lens0)
+        j = i % n_distinct
+        for layer in range(w.layers):
+            if layer == 0:
+                if not w.fused:
+                    cache.append(layer, k[j], v[j], w.n_new)
+                evs[i][0].record(stream)
+                if w.fused:
+                    cache.append_attention(layer, q[j], k[j], v[j], w.n_new, out=out, workspace=ws)
+                else:
+                    cache.gqa_attention(layer, q[j], w.n_new, out=out, workspace=ws)
+                evs[i][1].record(stream)
+            else:
+                cache.append_attention(layer, q[j], k[j], v[j], w.n_new, out=out, workspace=ws)
+    torch.cuda.synchronize()
+    attn_ms = [e[0].elapsed_time(e[1]) for e in evs]
     status = cache.device_status(ws)
     work = sum(w.work(i) for i in range(steps))
     kbytes = [w.kernel_bytes(i) for i in range(steps)]
-    # layer-0 attention launches are the ones timed per kernel (same shape on every layer)
     res = {
-        "ms": ms, "wall_s": t_wall, "work": work, "attn_ms": attn_ms, "append_ms": append_ms,
-        "kernel_bytes": kbytes, "launches": steps * w.layers * 2, "clocks": clk.summary(), "status": status,
+        "ms": ms, "wall_s": t_wall, "work": work, "attn_ms": attn_ms,
+        "kernel_bytes": kbytes, "launches": launches, "clocks": clk.summary(), "status": status,
     }
     res["e2e"] = run_e2e(w, cache, steps, q, k, v)
     return res
@@ -407,7 +434,7 @@ def main():
         roof = {"bound": "hbm", "achieved": kb / (attn_ms * 1e-3) * 1e-9, "peak": hbm, "unit": "GB/s"}
     roof["frac"] = roof["achieved"] / roof["peak"]
     roof["peak_source"] = f"{peak_kind} (MEASURED_PEAKS.json)" if peak_kind == "measured" else "fallback"
-    roof["kernel"] = "decode_splitkv_bf16_kernel"
+    roof["kernel"] = "decode_splitkv_bf16_kernel (+ combine_bf16_kernel" + (", append fused in)" if w.fused else ")")
     roof["kernel_ms"] = attn_ms
     roof["traffic"] = _committed_traffic(w, kb)
 

@@ -118,6 +118,10 @@ class KVCache:
     def reset(self) -> None:
         check(lib().kvc_reset(self._h))
 
+    def kernel_launches(self) -> int:
+        """Kernels this cache's handle has enqueued so far."""
+        return int(lib().kvc_kernel_launches(self._h))
+
     # ------------------------------------------------------------------ compute
     def workspace_bytes(self, q_heads: int, T: int) -> int:
         return int(lib().kvc_workspace_bytes(self._h, q_heads, T))

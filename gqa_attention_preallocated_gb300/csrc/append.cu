@@ -17,6 +17,11 @@ namespace {
 constexpr int kAppendThreads = 256;
 
 __global__ void __launch_bounds__(kAppendThreads) kv_append_kernel(const __grid_constant__ AppendParams p) {
+    // Chained launch: wait for the previous kernel in the stream to finish
+    // (it may still read the cache or write the inputs), then let the next
+    // kernel start its prologue.
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
     const int b = blockIdx.z;
     const int h = blockIdx.y >> 1;
     const bool is_v = (blockIdx.y & 1) != 0;
@@ -36,7 +41,17 @@ __global__ void __launch_bounds__(kAppendThreads) kv_append_kernel(const __grid_
 cudaError_t launch_append(const AppendParams& p, int max_n_new, cudaStream_t stream) {
     const size_t vecs = (static_cast<size_t>(max_n_new) * p.row_bytes) / 16;
     dim3 grid(static_cast<unsigned>((vecs + kAppendThreads - 1) / kAppendThreads), 2u * p.Hkv, p.B);
-    kv_append_kernel<<<grid, kAppendThreads, 0, stream>>>(p);
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = dim3(kAppendThreads);
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    cudaError_t e = cudaLaunchKernelEx(&cfg, kv_append_kernel, p);
+    if (e != cudaSuccess) return e;
     return cudaGetLastError();
 }
 

@@ -10,18 +10,24 @@
 // How (GB300):
 //  * One persistent CTA per SM.  All (unit, 64-key tile) pairs of the call are
 //    numbered and cut into equal contiguous ranges, one per CTA, so ragged row
-//    lengths never leave SMs idle; a unit whose tiles straddle CTAs is merged
-//    by the last CTA to finish it (per-unit counter, log-sum-exp merge), so
-//    the whole call is one launch.
+//    lengths never leave SMs idle.  A unit finished inside one CTA is written
+//    straight to `out`; a unit whose tiles straddle CTAs leaves one partial
+//    (m, l, O) per CTA, merged by the small combine kernel that follows in the
+//    stream (log-sum-exp merge).  Launches are chained with programmatic
+//    dependent launch, so a kernel's launch and prologue overlap the previous
+//    kernel's tail.
 //  * Warp 4 is the producer: one lane streams K and V tiles (64 keys x 128)
-//    through TMA (cp.async.bulk.tensor, 128-byte swizzle) into a 4-stage ring
-//    guarded by mbarriers.  Each tile is loaded once and serves all G*T query
-//    rows of the group (no KV repeat).
-//  * Warps 0-3 consume.  With G*T <= 16 rows (decode) the four warps split the
-//    tile's keys and merge their softmax states at the end of a unit; with up
-//    to 32 or 64 rows they split rows as well.  QK^T and PV run on mma.sync
-//    bf16 tiles (16 rows x 8 keys / 8 dims) with fp32 accumulators; softmax is
-//    online in base 2 with log2(e)/sqrt(d) folded into one scale.
+//    through TMA (cp.async.bulk.tensor, 128-byte swizzle) into a ring of
+//    stages guarded by mbarriers.  Each tile is loaded once and serves all G*T
+//    query rows of the group (no KV repeat).
+//  * Warps 0-3 consume.  With G*T <= 16 rows (decode, short verify) each warp
+//    owns whole tiles in turn (tile i goes to warp i mod 4) and keeps its own
+//    softmax state, so four tiles are in flight at once and each warp runs
+//    eight independent MMA chains per tile; the four states merge at the end
+//    of a unit.  With up to 32 or 64 rows the warps split rows (and keys).
+//    QK^T and PV run on mma.sync bf16 tiles (16 rows x 8 keys / 8 dims) with
+//    fp32 accumulators; softmax is online in base 2 with log2(e)/sqrt(d)
+//    folded into one scale.
 //  * Tile classification ("Write the causal mask...", tiled-kernel paragraph):
 //    a tile whose last key is at or below every valid row's limit is fully
 //    visible and skips the mask; tiles past the last visible key are never
@@ -29,10 +35,12 @@
 //  * Cache slots past lens may hold anything (stale or NaN).  Masked scores
 //    are replaced, never multiplied, and V rows past the unit's last visible
 //    key are cleared in shared memory before PV, so 0 * NaN cannot occur.
-//  * Every mbarrier wait is bounded in time; on expiry the kernel records an
-//    error code in the workspace and finishes instead of hanging.
+//  * Every wait is bounded in time; on expiry the kernel records an error code
+//    in the workspace and finishes instead of hanging.
 
 #include <math.h>
+
+#include <utility>
 
 #include "kvc_internal.h"
 #include "ptx.cuh"
@@ -44,21 +52,37 @@ namespace {
 constexpr int kConsumerWarps = 4;
 constexpr int kConsumerThreads = kConsumerWarps * 32;
 constexpr int kThreads = kConsumerThreads + 32;
-constexpr int kStages = 4;
 constexpr int kD = kHeadDimBf16;
 constexpr int kHalfBytes = kKeyTile * 128;   // 64 keys x 64 dims x 2 B (one swizzled box)
 constexpr int kTileBytes = 2 * kHalfBytes;   // 64 keys x 128 dims
 constexpr int kStageBytes = 2 * kTileBytes;  // K tile + V tile
 constexpr int kPartStride = kD + 4;          // floats per partial row: O[128], m, l, pad
 constexpr uint64_t kWaitLimitNs = 2000000000ull;
-
 constexpr size_t kObufBytes = 3 * 16 * kD * sizeof(float);
 constexpr size_t kMlBytes = kConsumerWarps * 16 * 2 * sizeof(float);
-constexpr size_t kSmemBytes = 1024 + kStages * kStageBytes + kObufBytes + kMlBytes + 2 * kStages * 8 + 16;
 
-__device__ __forceinline__ int cta_of_tile(long long x, long long N, long long P) {
-    return static_cast<int>(((x + 1) * P - 1) / N);
-}
+// Compile-time shape of the kernel for MT m-tiles (16 query rows each).
+//
+// Warps that own whole tiles (MT = 1) never meet: each writes its own partial
+// softmax state of a unit to the workspace and the combine kernel merges them,
+// so no shared merge buffer is needed and the ring gets a seventh stage.  With
+// MT = 2 or 4 the warps split every tile and merge their states in shared
+// memory at the end of a unit.
+template <int MT>
+struct Shape {
+    static constexpr bool kTilePar = (MT == 1);                // warps own whole tiles
+    static constexpr int kStages = kTilePar ? 7 : 4;
+    static constexpr int kKeySlices = kTilePar ? 1 : kConsumerWarps / MT;
+    static constexpr int kKW = kKeyTile / kKeySlices;          // keys per warp per tile
+    static constexpr int kMerge = kTilePar ? 1 : kKeySlices;   // states per m-tile merged in shared memory
+    static constexpr int kWays = kTilePar ? kConsumerWarps : 1;  // partial sub-slots per (unit, CTA)
+    static constexpr int kRPB = 16 * MT;
+    static constexpr int kEmptyCount = kTilePar ? 1 : kConsumerWarps;
+    static constexpr size_t kObuf = kTilePar ? 0 : kObufBytes;
+    static constexpr size_t kMl = kTilePar ? 0 : kMlBytes;
+    static constexpr size_t kSmem = 1024 + kStages * kStageBytes + kObuf + kMl + 2 * kStages * 8 + (kStages + 4) * 4;
+    static_assert(kSmem <= 232448, "shared memory per CTA");
+};
 
 // Largest q with gstart[q] <= x (gstart nondecreasing, x < gstart[NB]).
 __device__ __forceinline__ int locate_group(const DecodeParams& p, int x) {
@@ -97,38 +121,14 @@ __device__ __forceinline__ void store_bf16x4(void* dst, float a, float b, float 
     *reinterpret_cast<uint2*>(dst) = v;
 }
 
-// Merge the partial (m, l, O) of every CTA that worked on unit u and write the
-// unit's valid rows of `out`.  Run by the 128 consumer threads of the last CTA.
-template <int RPB>
-__device__ void merge_unit(const DecodeParams& p, int u, int c0, int c1, int b, int rb, int kvh, int ctid) {
-    const int nn = p.n_new[b];
-    for (int idx = ctid; idx < RPB * (kD / 4); idx += kConsumerThreads) {
-        const int lr = idx >> 5, c4 = idx & 31;
-        const int r = rb * RPB + lr;
-        if (r >= p.R || (r % p.T) >= nn) continue;
-        float mstar = -INFINITY;
-        for (int i = c0; i <= c1; ++i) {
-            const float* part = p.partials + (static_cast<size_t>(u + i) * RPB + lr) * kPartStride;
-            mstar = fmaxf(mstar, __ldcg(part + kD));
-        }
-        float lsum = 0.f;
-        float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-        for (int i = c0; i <= c1; ++i) {
-            const float* part = p.partials + (static_cast<size_t>(u + i) * RPB + lr) * kPartStride;
-            const float mi = __ldcg(part + kD);
-            const float w = (mi == -INFINITY) ? 0.f : ptx::ex2(mi - mstar);
-            lsum += w * __ldcg(part + kD + 1);
-            const float4 oi = __ldcg(reinterpret_cast<const float4*>(part) + c4);
-            acc.x += w * oi.x;
-            acc.y += w * oi.y;
-            acc.z += w * oi.z;
-            acc.w += w * oi.w;
-        }
-        const float inv = lsum > 0.f ? 1.f / lsum : 0.f;
-        const int g = r / p.T, t = r % p.T;
-        __nv_bfloat16* dst = static_cast<__nv_bfloat16*>(p.out) +
-                             ((static_cast<size_t>(b) * p.Hq + kvh * p.G + g) * p.T + t) * kD + c4 * 4;
-        store_bf16x4(dst, acc.x * inv, acc.y * inv, acc.z * inv, acc.w * inv);
+// Wait until the producer has claimed stage s for tile `it` (bounded).
+__device__ __forceinline__ bool wait_stage_tag(const volatile int* tag, int it, uint64_t limit_ns) {
+    if (*tag == it) return true;
+    const uint64_t t0 = ptx::globaltimer_ns();
+    for (;;) {
+        for (int i = 0; i < 64; ++i)
+            if (*tag == it) return true;
+        if (ptx::globaltimer_ns() - t0 > limit_ns) return false;
     }
 }
 
@@ -136,21 +136,47 @@ template <int MT>
 __global__ void __launch_bounds__(kThreads, 1)
     decode_splitkv_bf16_kernel(const __grid_constant__ DecodeParams p, const __grid_constant__ CUtensorMap tmK,
                                const __grid_constant__ CUtensorMap tmV) {
-    constexpr int KS = kConsumerWarps / MT;  // key slices per tile
-    constexpr int KW = kKeyTile / KS;        // keys per warp per tile (16 * MT)
-    constexpr int RPB = 16 * MT;             // query rows per block
-    constexpr int NBS = KW / 8;              // score n-blocks per warp
+    using S = Shape<MT>;
+    constexpr int kStages = S::kStages;
+    constexpr int KW = S::kKW;
+    constexpr int RPB = S::kRPB;
+    constexpr int NBS = KW / 8;   // score n-blocks per warp per tile
+    constexpr int KB = KW / 16;   // 16-key blocks per warp per tile
+    constexpr int NM = S::kMerge;
 
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     uint8_t* stages = smem;
     float* obuf = reinterpret_cast<float*>(smem + kStages * kStageBytes);
-    float* ml = obuf + 3 * 16 * kD;
-    uint64_t* bars = reinterpret_cast<uint64_t*>(ml + kConsumerWarps * 16 * 2);
-    volatile int* flag = reinterpret_cast<volatile int*>(bars + 2 * kStages);
-    volatile int* abort_flag = flag + 1;
+    float* ml = reinterpret_cast<float*>(smem + kStages * kStageBytes + S::kObuf);
+    uint64_t* bars = reinterpret_cast<uint64_t*>(smem + kStages * kStageBytes + S::kObuf + S::kMl);
+    volatile int* abort_flag = reinterpret_cast<volatile int*>(bars + 2 * kStages);
+    volatile int* stage_tag = abort_flag + 4;  // tile index the producer last put in each stage
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const long long N = p.total_tiles, P = gridDim.x;
+    const int x0 = static_cast<int>(static_cast<long long>(blockIdx.x) * N / P);
+    const int x1 = static_cast<int>(static_cast<long long>(blockIdx.x + 1) * N / P);
+
+    // Prologue: touches no memory that earlier work in the stream may write.
+    const uint32_t stage0 = ptx::smem_addr(stages);
+    const uint32_t bar0 = ptx::smem_addr(bars);  // full[s] = bar0 + 8s, empty[s] = bar0 + 8(kStages + s)
+    if (tid == 0) {
+        for (int s = 0; s < kStages; ++s) {
+            ptx::mbar_init(bar0 + 8 * s, 1);
+            ptx::mbar_init(bar0 + 8 * (kStages + s), S::kEmptyCount);
+            stage_tag[s] = -1;
+        }
+        *abort_flag = 0;
+        ptx::fence_barrier_init();
+    }
+    if (warp == kConsumerWarps && lane == 0) {
+        ptx::tma_prefetch_desc(&tmK);
+        ptx::tma_prefetch_desc(&tmV);
+    }
+    __syncthreads();
+    ptx::grid_dependency_wait();
+    ptx::launch_dependents();
 
     // Padded queries (t >= n_new[b]) output zeros; spread over the whole grid.
     {
@@ -165,30 +191,11 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
         }
     }
-
-    const long long N = p.total_tiles, P = gridDim.x;
-    const int x0 = static_cast<int>(static_cast<long long>(blockIdx.x) * N / P);
-    const int x1 = static_cast<int>(static_cast<long long>(blockIdx.x + 1) * N / P);
     if (x0 >= x1) return;
-
-    const uint32_t stage0 = ptx::smem_addr(stages);
-    const uint32_t bar0 = ptx::smem_addr(bars);  // full[s] = bar0 + 8s, empty[s] = bar0 + 8(kStages + s)
-    if (tid == 0) {
-        for (int s = 0; s < kStages; ++s) {
-            ptx::mbar_init(bar0 + 8 * s, 1);
-            ptx::mbar_init(bar0 + 8 * (kStages + s), kConsumerWarps);
-        }
-        *flag = 0;
-        *abort_flag = 0;
-        ptx::fence_barrier_init();
-    }
-    __syncthreads();
 
     // ------------------------------------------------------------------ producer
     if (warp == kConsumerWarps) {
         if (lane == 0) {
-            ptx::tma_prefetch_desc(&tmK);
-            ptx::tma_prefetch_desc(&tmV);
             Cursor cur;
             cur.init(p, x0);
             int issued = 0;
@@ -205,6 +212,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 const int row = (b * p.Hkv + cur.kvh) * p.max_len + cur.j * kKeyTile;
                 const uint32_t full = bar0 + 8 * s;
                 const uint32_t sK = stage0 + s * kStageBytes;
+                stage_tag[s] = it;
                 ptx::mbar_arrive_expect_tx(full, kStageBytes);
                 ptx::tma_load_2d(sK, &tmK, 0, row, full);
                 ptx::tma_load_2d(sK + kHalfBytes, &tmK, 64, row, full);
@@ -227,7 +235,11 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
 
     // ------------------------------------------------------------------ consumers
-    const int mt = warp % MT, ks = warp / MT;
+    // mt: this warp's m-tile; ms: its index among the NM softmax states of that
+    // m-tile merged at a unit's end; koff: first key of its slice of a tile.
+    const int mt = S::kTilePar ? 0 : warp % MT;
+    const int ms = S::kTilePar ? warp : warp / MT;
+    const int koff = S::kTilePar ? 0 : ms * KW;
     const int quad = lane & 3;
     const int lrow0 = mt * 16 + (lane >> 2);  // this thread's block rows: lrow0, lrow0 + 8
 
@@ -237,7 +249,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     float o[16][4];
     float m0 = -INFINITY, m1 = -INFINITY, l0 = 0.f, l1 = 0.f;
     uint32_t qa[8][4];
-    int lim0 = -1, lim1 = -1, min_lim = 0, extent = 0, seg_j0 = 0;
+    int lim0 = -1, lim1 = -1, min_lim = 0, extent = 0, seg_j0 = 0, seg_tiles = 0;
+    int seg_prior = 0, seg_nn = 0;
+    uint4 new_row0 = make_uint4(0u, 0u, 0u, 0u);  // first appended row, lane's 16-byte chunk (K: lanes 0-15, V: 16-31)
 
     for (int x = x0, it = 0; x < x1; ++x, ++it) {
         const int s = it % kStages;
@@ -259,6 +273,14 @@ __global__ void __launch_bounds__(kThreads, 1)
                 }
             }
             seg_j0 = j;
+            seg_tiles = 0;
+            seg_prior = prior;
+            seg_nn = nn;
+            if (S::kTilePar && p.append_new && nn > 0) {
+                const uint8_t* src = static_cast<const uint8_t*>((lane < 16) ? p.k_new : p.v_new) +
+                                     (static_cast<size_t>(b) * p.Hkv + kvh) * p.Tn * (kD * 2) + (lane & 15) * 16;
+                new_row0 = __ldg(reinterpret_cast<const uint4*>(src));
+            }
 #pragma unroll
             for (int h = 0; h < 2; ++h) {
                 const int r = rb * RPB + lrow0 + 8 * h;
@@ -283,124 +305,166 @@ __global__ void __launch_bounds__(kThreads, 1)
             l0 = l1 = 0.f;
         }
 
-        // On expiry the warp records the error and carries on with whatever the
-        // stage holds (the call's output is then invalid): consumer warps meet
-        // at named barriers, so none may leave the loop alone.  After the first
-        // expiry further waits try once only.
-        if (!ptx::mbar_wait_bounded(bar0 + 8 * s, (it / kStages) & 1, *abort_flag ? 0ull : kWaitLimitNs)) {
-            atomicExch(p.err, kDevTimeoutFull);
-            *abort_flag = 1;
-        }
-
-        const uint32_t sK = stage0 + s * kStageBytes;
-        const uint32_t sV = sK + kTileBytes;
-        const int tile0 = j * kKeyTile;
-
-        if (tile0 + kKeyTile > extent) {
-            // Clear V rows at or past the unit's last visible key (slots past
-            // lens may hold NaN; their probabilities are 0 but 0 * NaN is NaN).
-            const int vr0 = extent - tile0;
-            const int per_half = (kKeyTile - vr0) * 8;
-            uint8_t* vbase = stages + s * kStageBytes + kTileBytes;
-            for (int idx = tid; idx < 2 * per_half; idx += kConsumerThreads) {
-                const int hf = idx / per_half, rem = idx - hf * per_half;
-                *reinterpret_cast<uint4*>(vbase + hf * kHalfBytes + (vr0 + (rem >> 3)) * 128 + (rem & 7) * 16) =
-                    make_uint4(0u, 0u, 0u, 0u);
-            }
-            ptx::fence_proxy_async_smem();
-            ptx::named_barrier_sync(1, kConsumerThreads);
-        }
-        const bool full_tile = (tile0 + kKeyTile - 1 <= min_lim);
-
-        // S = Q K^T for this warp's 16 rows x KW keys.
-        float sc[NBS][4];
-#pragma unroll
-        for (int nb = 0; nb < NBS; ++nb) sc[nb][0] = sc[nb][1] = sc[nb][2] = sc[nb][3] = 0.f;
-#pragma unroll
-        for (int kk = 0; kk < 8; ++kk) {
-#pragma unroll
-            for (int kb = 0; kb < MT; ++kb) {
-                const int mi = lane >> 3;
-                const int key = ks * KW + kb * 16 + (mi >> 1) * 8 + (lane & 7);
-                const int chunk = 2 * kk + (mi & 1);
-                const uint32_t addr = sK + (chunk >> 3) * kHalfBytes + key * 128 + (((chunk & 7) ^ (key & 7)) << 4);
-                uint32_t b0, b1, b2, b3;
-                ptx::ldmatrix_x4(addr, b0, b1, b2, b3);
-                ptx::mma_bf16_16816(sc[2 * kb], qa[kk], b0, b1);
-                ptx::mma_bf16_16816(sc[2 * kb + 1], qa[kk], b2, b3);
-            }
-        }
-
-        // Mask (diagonal / ragged tiles only) and online softmax in base 2.
-        const int kbase = tile0 + ks * KW + 2 * quad;
-        float mx0 = -INFINITY, mx1 = -INFINITY;
-#pragma unroll
-        for (int nb = 0; nb < NBS; ++nb) {
-#pragma unroll
-            for (int e = 0; e < 4; ++e) {
-                float v = sc[nb][e] * p.scale_log2;
-                if (!full_tile) {
-                    const int key = kbase + nb * 8 + (e & 1);
-                    if (key > ((e < 2) ? lim0 : lim1)) v = -INFINITY;
+        const bool mine = S::kTilePar ? ((it & (kConsumerWarps - 1)) == warp) : true;
+        if (mine) {
+            ++seg_tiles;
+            // On expiry the warp records the error and carries on with whatever
+            // the stage holds (the call's output is then invalid): consumer warps
+            // meet at named barriers, so none may leave the loop alone.  After
+            // the first expiry further waits try once only.
+            const uint64_t limit = *abort_flag ? 0ull : kWaitLimitNs;
+            if (S::kTilePar) {
+                // With warps taking tiles in turn, the warp that owns tile `it`
+                // may reach stage s while an earlier tile of another warp still
+                // occupies it.  The mbarrier parity cannot tell phases two apart,
+                // so first wait until the producer has put tile `it` in stage s.
+                if (!wait_stage_tag(stage_tag + s, it, limit)) {
+                    atomicExch(p.err, kDevTimeoutTag);
+                    *abort_flag = 1;
                 }
-                sc[nb][e] = v;
             }
-            mx0 = fmaxf(mx0, fmaxf(sc[nb][0], sc[nb][1]));
-            mx1 = fmaxf(mx1, fmaxf(sc[nb][2], sc[nb][3]));
-        }
-        mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, 1));
-        mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, 2));
-        mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, 1));
-        mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, 2));
-        const float mn0 = fmaxf(m0, mx0), mn1 = fmaxf(m1, mx1);
-        const float mu0 = (mn0 == -INFINITY) ? 0.f : mn0;
-        const float mu1 = (mn1 == -INFINITY) ? 0.f : mn1;
-        const float al0 = ptx::ex2(m0 - mu0), al1 = ptx::ex2(m1 - mu1);
-        m0 = mn0;
-        m1 = mn1;
-        float ps0 = 0.f, ps1 = 0.f;
-#pragma unroll
-        for (int nb = 0; nb < NBS; ++nb) {
-            sc[nb][0] = ptx::ex2(sc[nb][0] - mu0);
-            sc[nb][1] = ptx::ex2(sc[nb][1] - mu0);
-            sc[nb][2] = ptx::ex2(sc[nb][2] - mu1);
-            sc[nb][3] = ptx::ex2(sc[nb][3] - mu1);
-            ps0 += sc[nb][0] + sc[nb][1];
-            ps1 += sc[nb][2] + sc[nb][3];
-        }
-        l0 = l0 * al0 + ps0;
-        l1 = l1 * al1 + ps1;
-#pragma unroll
-        for (int nb = 0; nb < 16; ++nb) {
-            o[nb][0] *= al0;
-            o[nb][1] *= al0;
-            o[nb][2] *= al1;
-            o[nb][3] *= al1;
-        }
-
-        // O += P V.
-#pragma unroll
-        for (int kb = 0; kb < MT; ++kb) {
-            uint32_t a[4];
-            a[0] = ptx::pack_bf16x2(sc[2 * kb][0], sc[2 * kb][1]);
-            a[1] = ptx::pack_bf16x2(sc[2 * kb][2], sc[2 * kb][3]);
-            a[2] = ptx::pack_bf16x2(sc[2 * kb + 1][0], sc[2 * kb + 1][1]);
-            a[3] = ptx::pack_bf16x2(sc[2 * kb + 1][2], sc[2 * kb + 1][3]);
-#pragma unroll
-            for (int dc = 0; dc < 8; ++dc) {
-                const int mi = lane >> 3;
-                const int key = ks * KW + kb * 16 + (mi & 1) * 8 + (lane & 7);
-                const int chunk = 2 * dc + (mi >> 1);
-                const uint32_t addr = sV + (chunk >> 3) * kHalfBytes + key * 128 + (((chunk & 7) ^ (key & 7)) << 4);
-                uint32_t b0, b1, b2, b3;
-                ptx::ldmatrix_x4_trans(addr, b0, b1, b2, b3);
-                ptx::mma_bf16_16816(o[2 * dc], a, b0, b1);
-                ptx::mma_bf16_16816(o[2 * dc + 1], a, b2, b3);
+            if (!ptx::mbar_wait_bounded(bar0 + 8 * s, (it / kStages) & 1, limit)) {
+                atomicExch(p.err, kDevTimeoutFull);
+                *abort_flag = 1;
             }
-        }
 
-        __syncwarp();
-        if (lane == 0) ptx::mbar_arrive(bar0 + 8 * (kStages + s));
+            const uint32_t sK = stage0 + s * kStageBytes;
+            const uint32_t sV = sK + kTileBytes;
+            const int tile0 = j * kKeyTile;
+
+            if (S::kTilePar && p.append_new) {
+                // In-kernel append: rows prior .. prior+n_new-1 of this unit that
+                // fall in this tile come from k_new / v_new.  The staged copy of
+                // those cache slots is stale, so patch it, and write the rows to
+                // the cache (this tile is processed exactly once).
+                const int lo = max(seg_prior, tile0), hi = min(seg_prior + seg_nn, tile0 + kKeyTile);
+                if (lo < hi) {
+                    const int chunk = lane & 15;  // 16-byte chunk of the 256-byte row
+                    const bool is_v = lane >= 16;
+                    const size_t unit = static_cast<size_t>(b) * p.Hkv + kvh;
+                    const uint8_t* src = static_cast<const uint8_t*>(is_v ? p.v_new : p.k_new) + unit * p.Tn * (kD * 2);
+                    uint8_t* dst = static_cast<uint8_t*>(is_v ? p.v_cache : p.k_cache) + unit * p.max_len * (kD * 2);
+                    uint8_t* stg = stages + s * kStageBytes + (is_v ? kTileBytes : 0) + (chunk >> 3) * kHalfBytes;
+                    for (int pos = lo; pos < hi; ++pos) {
+                        const int t = pos - seg_prior, r = pos - tile0;
+                        const uint4 val = (t == 0) ? new_row0
+                                                   : __ldg(reinterpret_cast<const uint4*>(src + t * (kD * 2) + chunk * 16));
+                        *reinterpret_cast<uint4*>(stg + r * 128 + (((chunk & 7) ^ (r & 7)) << 4)) = val;
+                        *reinterpret_cast<uint4*>(dst + static_cast<size_t>(pos) * (kD * 2) + chunk * 16) = val;
+                    }
+                    ptx::fence_proxy_async_smem();
+                    __syncwarp();
+                }
+            }
+
+            if (tile0 + kKeyTile > extent) {
+                // Clear V rows at or past the unit's last visible key (slots past
+                // lens may hold NaN; their probabilities are 0 but 0 * NaN is NaN).
+                const int vr0 = extent - tile0;
+                const int per_half = (kKeyTile - vr0) * 8;
+                uint8_t* vbase = stages + s * kStageBytes + kTileBytes;
+                const int t0 = S::kTilePar ? lane : tid;
+                const int step = S::kTilePar ? 32 : kConsumerThreads;
+                for (int idx = t0; idx < 2 * per_half; idx += step) {
+                    const int hf = idx / per_half, rem = idx - hf * per_half;
+                    *reinterpret_cast<uint4*>(vbase + hf * kHalfBytes + (vr0 + (rem >> 3)) * 128 + (rem & 7) * 16) =
+                        make_uint4(0u, 0u, 0u, 0u);
+                }
+                ptx::fence_proxy_async_smem();
+                if (S::kTilePar) __syncwarp(); else ptx::named_barrier_sync(1, kConsumerThreads);
+            }
+            const bool full_tile = (tile0 + kKeyTile - 1 <= min_lim);
+
+            // S = Q K^T for this warp's 16 rows x KW keys.
+            float sc[NBS][4];
+#pragma unroll
+            for (int nb = 0; nb < NBS; ++nb) sc[nb][0] = sc[nb][1] = sc[nb][2] = sc[nb][3] = 0.f;
+#pragma unroll
+            for (int kk = 0; kk < 8; ++kk) {
+#pragma unroll
+                for (int kb = 0; kb < KB; ++kb) {
+                    const int mi = lane >> 3;
+                    const int key = koff + kb * 16 + (mi >> 1) * 8 + (lane & 7);
+                    const int chunk = 2 * kk + (mi & 1);
+                    const uint32_t addr = sK + (chunk >> 3) * kHalfBytes + key * 128 + (((chunk & 7) ^ (key & 7)) << 4);
+                    uint32_t b0, b1, b2, b3;
+                    ptx::ldmatrix_x4(addr, b0, b1, b2, b3);
+                    ptx::mma_bf16_16816(sc[2 * kb], qa[kk], b0, b1);
+                    ptx::mma_bf16_16816(sc[2 * kb + 1], qa[kk], b2, b3);
+                }
+            }
+
+            // Mask (diagonal / ragged tiles only) and online softmax in base 2.
+            const int kbase = tile0 + koff + 2 * quad;
+            float mx0 = -INFINITY, mx1 = -INFINITY;
+#pragma unroll
+            for (int nb = 0; nb < NBS; ++nb) {
+#pragma unroll
+                for (int e = 0; e < 4; ++e) {
+                    float v = sc[nb][e] * p.scale_log2;
+                    if (!full_tile) {
+                        const int key = kbase + nb * 8 + (e & 1);
+                        if (key > ((e < 2) ? lim0 : lim1)) v = -INFINITY;
+                    }
+                    sc[nb][e] = v;
+                }
+                mx0 = fmaxf(mx0, fmaxf(sc[nb][0], sc[nb][1]));
+                mx1 = fmaxf(mx1, fmaxf(sc[nb][2], sc[nb][3]));
+            }
+            mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, 1));
+            mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, 2));
+            mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, 1));
+            mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, 2));
+            const float mn0 = fmaxf(m0, mx0), mn1 = fmaxf(m1, mx1);
+            const float mu0 = (mn0 == -INFINITY) ? 0.f : mn0;
+            const float mu1 = (mn1 == -INFINITY) ? 0.f : mn1;
+            const float al0 = ptx::ex2(m0 - mu0), al1 = ptx::ex2(m1 - mu1);
+            m0 = mn0;
+            m1 = mn1;
+            float ps0 = 0.f, ps1 = 0.f;
+#pragma unroll
+            for (int nb = 0; nb < NBS; ++nb) {
+                sc[nb][0] = ptx::ex2(sc[nb][0] - mu0);
+                sc[nb][1] = ptx::ex2(sc[nb][1] - mu0);
+                sc[nb][2] = ptx::ex2(sc[nb][2] - mu1);
+                sc[nb][3] = ptx::ex2(sc[nb][3] - mu1);
+                ps0 += sc[nb][0] + sc[nb][1];
+                ps1 += sc[nb][2] + sc[nb][3];
+            }
+            l0 = l0 * al0 + ps0;
+            l1 = l1 * al1 + ps1;
+#pragma unroll
+            for (int nb = 0; nb < 16; ++nb) {
+                o[nb][0] *= al0;
+                o[nb][1] *= al0;
+                o[nb][2] *= al1;
+                o[nb][3] *= al1;
+            }
+
+            // O += P V.
+#pragma unroll
+            for (int kb = 0; kb < KB; ++kb) {
+                uint32_t a[4];
+                a[0] = ptx::pack_bf16x2(sc[2 * kb][0], sc[2 * kb][1]);
+                a[1] = ptx::pack_bf16x2(sc[2 * kb][2], sc[2 * kb][3]);
+                a[2] = ptx::pack_bf16x2(sc[2 * kb + 1][0], sc[2 * kb + 1][1]);
+                a[3] = ptx::pack_bf16x2(sc[2 * kb + 1][2], sc[2 * kb + 1][3]);
+#pragma unroll
+                for (int dc = 0; dc < 8; ++dc) {
+                    const int mi = lane >> 3;
+                    const int key = koff + kb * 16 + (mi & 1) * 8 + (lane & 7);
+                    const int chunk = 2 * dc + (mi >> 1);
+                    const uint32_t addr = sV + (chunk >> 3) * kHalfBytes + key * 128 + (((chunk & 7) ^ (key & 7)) << 4);
+                    uint32_t b0, b1, b2, b3;
+                    ptx::ldmatrix_x4_trans(addr, b0, b1, b2, b3);
+                    ptx::mma_bf16_16816(o[2 * dc], a, b0, b1);
+                    ptx::mma_bf16_16816(o[2 * dc + 1], a, b2, b3);
+                }
+            }
+
+            __syncwarp();
+            if (lane == 0) ptx::mbar_arrive(bar0 + 8 * (kStages + s));
+        }
 
         const bool seg_end = (x == x1 - 1) || (j == nt - 1);
         if (seg_end) {
@@ -408,8 +472,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             l0 += __shfl_xor_sync(0xffffffffu, l0, 2);
             l1 += __shfl_xor_sync(0xffffffffu, l1, 1);
             l1 += __shfl_xor_sync(0xffffffffu, l1, 2);
-            if (KS > 1) {
-                // Merge the key slices' softmax states into the ks == 0 warps.
+            if (NM > 1) {
+                // Merge the NM softmax states of each m-tile into its ms == 0 warp.
                 const int r0 = lane >> 2;
                 if (quad == 0) {
                     ml[(warp * 16 + r0) * 2 + 0] = m0;
@@ -420,8 +484,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                 ptx::named_barrier_sync(1, kConsumerThreads);
                 float mf0 = -INFINITY, mf1 = -INFINITY;
 #pragma unroll
-                for (int k2 = 0; k2 < KS; ++k2) {
-                    const int w2 = mt + k2 * MT;
+                for (int k2 = 0; k2 < NM; ++k2) {
+                    const int w2 = S::kTilePar ? k2 : mt + k2 * MT;
                     mf0 = fmaxf(mf0, ml[(w2 * 16 + r0) * 2]);
                     mf1 = fmaxf(mf1, ml[(w2 * 16 + r0 + 8) * 2]);
                 }
@@ -429,8 +493,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                 const float mfu1 = (mf1 == -INFINITY) ? 0.f : mf1;
                 float lf0 = 0.f, lf1 = 0.f;
 #pragma unroll
-                for (int k2 = 0; k2 < KS; ++k2) {
-                    const int w2 = mt + k2 * MT;
+                for (int k2 = 0; k2 < NM; ++k2) {
+                    const int w2 = S::kTilePar ? k2 : mt + k2 * MT;
                     lf0 += ml[(w2 * 16 + r0) * 2 + 1] * ptx::ex2(ml[(w2 * 16 + r0) * 2] - mfu0);
                     lf1 += ml[(w2 * 16 + r0 + 8) * 2 + 1] * ptx::ex2(ml[(w2 * 16 + r0 + 8) * 2] - mfu1);
                 }
@@ -442,8 +506,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                     o[nb][2] *= f1;
                     o[nb][3] *= f1;
                 }
-                if (ks > 0) {
-                    float* ob = obuf + ((ks - 1) * MT + mt) * 16 * kD;
+                if (ms > 0) {
+                    float* ob = obuf + ((ms - 1) * MT + mt) * 16 * kD;
 #pragma unroll
                     for (int nb = 0; nb < 16; ++nb) {
                         const int col = nb * 8 + 2 * quad;
@@ -452,9 +516,9 @@ __global__ void __launch_bounds__(kThreads, 1)
                     }
                 }
                 ptx::named_barrier_sync(1, kConsumerThreads);
-                if (ks == 0) {
+                if (ms == 0) {
 #pragma unroll
-                    for (int k2 = 1; k2 < KS; ++k2) {
+                    for (int k2 = 1; k2 < NM; ++k2) {
                         const float* ob = obuf + ((k2 - 1) * MT + mt) * 16 * kD;
 #pragma unroll
                         for (int nb = 0; nb < 16; ++nb) {
@@ -475,17 +539,26 @@ __global__ void __launch_bounds__(kThreads, 1)
                 ptx::named_barrier_sync(1, kConsumerThreads);
             }
 
-            const int u = cur.q * p.Hkv + kvh;
-            const bool sole = (seg_j0 == 0) && (j == nt - 1);
-            if (sole) {
-                if (ks == 0) {
+            // Writers: in the shared-merge layout the ms == 0 warp of each
+            // m-tile; with warps owning whole tiles, every warp that took at
+            // least one tile of this unit segment.  The unit's output is written
+            // here when this writer saw all of it (the whole unit ran in this
+            // CTA, and with warps owning tiles, the unit is a single tile);
+            // otherwise a partial (m, l, O) goes to sub-slot (u + CTA) * ways +
+            // warp for the combine kernel.
+            const bool writer = S::kTilePar ? (seg_tiles > 0) : (ms == 0);
+            if (writer) {
+                const bool sole = (seg_j0 == 0) && (j == nt - 1) && (!S::kTilePar || nt == 1);
+                const int slot = (cur.q * p.Hkv + kvh + blockIdx.x) * S::kWays + (S::kTilePar ? warp : 0);
 #pragma unroll
-                    for (int h = 0; h < 2; ++h) {
-                        const int lim = h ? lim1 : lim0;
-                        if (lim < 0) continue;
+                for (int h = 0; h < 2; ++h) {
+                    const int lim = h ? lim1 : lim0;
+                    if (lim < 0) continue;  // padding row or padded query: never written here
+                    const float l = h ? l1 : l0;
+                    if (sole) {
+                        // The whole unit ran in this CTA: normalise and write the output.
                         const int r = rb * RPB + lrow0 + 8 * h;
                         const int g = r / p.T, t = r % p.T;
-                        const float l = h ? l1 : l0;
                         const float inv = l > 0.f ? 1.f / l : 0.f;
                         __nv_bfloat16* dst = static_cast<__nv_bfloat16*>(p.out) +
                                              ((static_cast<size_t>(b) * p.Hq + kvh * p.G + g) * p.T + t) * kD;
@@ -495,51 +568,123 @@ __global__ void __launch_bounds__(kThreads, 1)
                             *reinterpret_cast<uint32_t*>(dst + col) =
                                 ptx::pack_bf16x2(o[nb][2 * h] * inv, o[nb][2 * h + 1] * inv);
                         }
-                    }
-                }
-            } else {
-                const int slot = u + blockIdx.x;
-                if (ks == 0) {
-#pragma unroll
-                    for (int h = 0; h < 2; ++h) {
-                        float* part = p.partials + (static_cast<size_t>(slot) * RPB + lrow0 + 8 * h) * kPartStride;
+                    } else {
+                        // Part of a unit seen by several writers: leave (m, l, O)
+                        // for the combine kernel.
+                        float* part = p.partials + (static_cast<size_t>(slot) * p.part_rows + lrow0 + 8 * h) * kPartStride;
 #pragma unroll
                         for (int nb = 0; nb < 16; ++nb) {
                             const int col = nb * 8 + 2 * quad;
-                            __stcg(reinterpret_cast<float2*>(part + col), make_float2(o[nb][2 * h], o[nb][2 * h + 1]));
+                            *reinterpret_cast<float2*>(part + col) = make_float2(o[nb][2 * h], o[nb][2 * h + 1]);
                         }
                         if (quad == 0) {
-                            __stcg(part + kD, h ? m1 : m0);
-                            __stcg(part + kD + 1, h ? l1 : l0);
+                            part[kD] = h ? m1 : m0;
+                            part[kD + 1] = l;
                         }
                     }
                 }
-                __threadfence();
-                ptx::named_barrier_sync(1, kConsumerThreads);
-                if (tid == 0) {
-                    const long long us = static_cast<long long>(p.gstart[cur.q]) + static_cast<long long>(kvh) * nt;
-                    const int c0 = cta_of_tile(us, N, P), c1 = cta_of_tile(us + nt - 1, N, P);
-                    const int old = atomicAdd(p.counters + u, 1);
-                    if (old == c1 - c0) {
-                        p.counters[u] = 0;  // all contributors arrived: leave it clean for the next call
-                        *flag = c0 + 1;
-                    } else {
-                        *flag = 0;
-                    }
-                }
-                ptx::named_barrier_sync(1, kConsumerThreads);
-                const int f = *flag;
-                if (f) {
-                    __threadfence();
-                    const long long us = static_cast<long long>(p.gstart[cur.q]) + static_cast<long long>(kvh) * nt;
-                    const int c1 = cta_of_tile(us + nt - 1, N, P);
-                    merge_unit<RPB>(p, u, f - 1, c1, b, rb, kvh, tid);
-                }
-                ptx::named_barrier_sync(1, kConsumerThreads);
             }
         }
         cur.advance(p);
     }
+}
+
+// One CTA per unit.  Units written in full by the attention kernel return at
+// once; for the others, the log-sum-exp merge of the partials (m_i, l_i, O_i)
+// of every writer, o = sum_i 2^(m_i - M) O_i / sum_i 2^(m_i - M) l_i with
+// M = max_i m_i, is written for the unit's valid rows.  Writers: CTAs c0..c1
+// (those whose tile ranges meet the unit) and, when warps own whole tiles,
+// each warp w of such a CTA that took one of the unit's tiles (tile k of the
+// CTA's range goes to warp k mod ways).
+constexpr int kCombineThreads = 128;
+constexpr int kCombineChunk = 8;   // partials loaded together (independent loads)
+
+// CTA whose tile range holds tile x: largest i with cta_start[i] <= x.
+__device__ __forceinline__ int cta_holding(const CombineParams& p, long long x) {
+    int lo = 0, hi = p.num_ctas - 1;
+    while (lo < hi) {
+        const int mid = (lo + hi + 1) >> 1;
+        if (p.cta_start[mid] <= x) lo = mid; else hi = mid - 1;
+    }
+    return lo;
+}
+
+__global__ void __launch_bounds__(kCombineThreads) combine_bf16_kernel(const __grid_constant__ CombineParams p) {
+    ptx::grid_dependency_wait();
+    ptx::launch_dependents();
+    const int u = blockIdx.x;
+    const int q = u / p.Hkv, kvh = u - q * p.Hkv;
+    const int nt = (p.gstart[q + 1] - p.gstart[q]) / p.Hkv;
+    if (nt == 0) return;
+    const int us = p.gstart[q] + kvh * nt, ue = us + nt - 1;
+    const int c0 = cta_holding(p, us), c1 = cta_holding(p, ue);
+    if (c0 == c1 && (p.ways == 1 || nt == 1)) return;  // written by the attention kernel
+    const int ncand = (c1 - c0 + 1) * p.ways;
+    const int b = q / p.RB, rb = q - b * p.RB;
+    const int nn = p.n_new[b];
+    for (int idx = threadIdx.x; idx < p.part_rows * (kD / 4); idx += kCombineThreads) {
+        const int lr = idx >> 5, c4 = idx & 31;
+        const int r = rb * p.RPB + lr;
+        if (r >= p.R || (r % p.T) >= nn) continue;
+        const float* base = p.partials + ((static_cast<size_t>(u + c0) * p.ways) * p.part_rows + lr) * kPartStride;
+        const size_t stride = static_cast<size_t>(p.part_rows) * kPartStride;  // next sub-slot
+        // One pass, merging chunks of partials online: (m, l, acc) <- merge.
+        float m = -INFINITY, l = 0.f;
+        float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+        for (int e0 = 0; e0 < ncand; e0 += kCombineChunk) {
+            float mi[kCombineChunk], li[kCombineChunk];
+            float4 oi[kCombineChunk];
+#pragma unroll
+            for (int k = 0; k < kCombineChunk; ++k) {
+                // Candidate e = (CTA c0 + e / ways, warp e % ways): did it write?
+                const int e = e0 + k;
+                bool valid = e < ncand;
+                if (valid) {
+                    const int ci = e / p.ways, w = e - ci * p.ways;
+                    const int x0 = p.cta_start[c0 + ci], x1 = p.cta_start[c0 + ci + 1];
+                    const int la = max(us, x0) - x0, lb = min(ue, x1 - 1) - x0;
+                    valid = (lb - la + 1 >= p.ways) || ((w - la % p.ways + p.ways) % p.ways <= lb - la);
+                }
+                const float* part = base + (valid ? e : 0) * stride;
+                mi[k] = valid ? part[kD] : -INFINITY;
+                li[k] = valid ? part[kD + 1] : 0.f;
+                oi[k] = valid ? reinterpret_cast<const float4*>(part)[c4] : make_float4(0.f, 0.f, 0.f, 0.f);
+            }
+#pragma unroll
+            for (int k = 0; k < kCombineChunk; ++k) {
+                const float mn = fmaxf(m, mi[k]);
+                if (mn == -INFINITY) continue;
+                const float a = ptx::ex2(m - mn), c = ptx::ex2(mi[k] - mn);
+                l = l * a + li[k] * c;
+                acc.x = acc.x * a + oi[k].x * c;
+                acc.y = acc.y * a + oi[k].y * c;
+                acc.z = acc.z * a + oi[k].z * c;
+                acc.w = acc.w * a + oi[k].w * c;
+                m = mn;
+            }
+        }
+        const float inv = l > 0.f ? 1.f / l : 0.f;
+        const int g = r / p.T, t = r % p.T;
+        __nv_bfloat16* dst = static_cast<__nv_bfloat16*>(p.out) +
+                             ((static_cast<size_t>(b) * p.Hq + kvh * p.G + g) * p.T + t) * kD + c4 * 4;
+        store_bf16x4(dst, acc.x * inv, acc.y * inv, acc.z * inv, acc.w * inv);
+    }
+}
+
+template <typename... KArgs, typename... Args>
+cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t stream,
+                       Args&&... args) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, kernel, std::forward<Args>(args)...);
 }
 
 template <int MT>
@@ -548,11 +693,14 @@ cudaError_t launch_mt(const DecodeParams& p, const CUtensorMap& tmK, const CUten
     static bool attr_set = false;
     if (!attr_set) {
         cudaError_t e = cudaFuncSetAttribute(decode_splitkv_bf16_kernel<MT>,
-                                             cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(kSmemBytes));
+                                             cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                             static_cast<int>(Shape<MT>::kSmem));
         if (e != cudaSuccess) return e;
         attr_set = true;
     }
-    decode_splitkv_bf16_kernel<MT><<<grid, kThreads, kSmemBytes, stream>>>(p, tmK, tmV);
+    cudaError_t e = launch_pdl(decode_splitkv_bf16_kernel<MT>, dim3(grid), dim3(kThreads), Shape<MT>::kSmem, stream,
+                               p, tmK, tmV);
+    if (e != cudaSuccess) return e;
     return cudaGetLastError();
 }
 
@@ -571,7 +719,13 @@ __global__ void wait_selftest_kernel(int* err, unsigned long long limit_ns) {
 
 }  // namespace
 
-DecodeLaunch decode_launch_shape(int mt) { return DecodeLaunch{mt, kThreads, kSmemBytes}; }
+DecodeLaunch decode_launch_shape(int mt) {
+    switch (mt) {
+        case 1: return DecodeLaunch{1, kThreads, Shape<1>::kSmem, Shape<1>::kWays};
+        case 2: return DecodeLaunch{2, kThreads, Shape<2>::kSmem, Shape<2>::kWays};
+        default: return DecodeLaunch{4, kThreads, Shape<4>::kSmem, Shape<4>::kWays};
+    }
+}
 
 cudaError_t launch_decode_bf16(const DecodeParams& p, const CUtensorMap& tmK, const CUtensorMap& tmV, int mt,
                                int grid, cudaStream_t stream) {
@@ -581,6 +735,12 @@ cudaError_t launch_decode_bf16(const DecodeParams& p, const CUtensorMap& tmK, co
         case 4: return launch_mt<4>(p, tmK, tmV, grid, stream);
         default: return cudaErrorInvalidValue;
     }
+}
+
+cudaError_t launch_combine_bf16(const CombineParams& p, cudaStream_t stream) {
+    cudaError_t e = launch_pdl(combine_bf16_kernel, dim3(p.NB * p.Hkv), dim3(kCombineThreads), 0, stream, p);
+    if (e != cudaSuccess) return e;
+    return cudaGetLastError();
 }
 
 cudaError_t launch_wait_selftest(int* err, unsigned long long limit_ns, cudaStream_t stream) {

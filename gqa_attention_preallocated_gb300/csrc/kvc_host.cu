@@ -38,6 +38,7 @@ struct kvc_cache {
     std::vector<CUtensorMap> tmK, tmV;
     std::vector<char> tm_ready;
     const void* last_ws = nullptr;
+    uint64_t launches = 0;  // kernels this handle has enqueued
 };
 
 namespace {
@@ -154,7 +155,7 @@ kvc_status validate_append(const kvc_cache* c, int layer, const void* k_new, con
 
 struct AttnPlan {
     int Hq = 0, G = 0, T = 0, R = 0;
-    int mt = 0, RPB = 0, RB = 0, NB = 0, units = 0;
+    int mt = 0, RPB = 0, RB = 0, NB = 0, units = 0, ways = 1, part_rows = 0;
     size_t ws_err = 0, ws_counters = 0, ws_partials = 0, ws_total = 0;
 };
 
@@ -179,13 +180,15 @@ kvc_status plan_shape(const kvc_cache* c, int Hq, int T, int num_ctas, AttnPlan*
             return fail(KVC_ERR_ARG, "B * ceil(G*T / %d) = %lld exceeds %d row blocks", pl->RPB, NB, kMaxGroups);
         pl->NB = static_cast<int>(NB);
         pl->units = pl->NB * c->Hkv;
-        // Fixed layout for every call shape of this handle: error word, then
-        // room for the largest possible number of unit counters, then the
-        // partials.  The counters therefore always sit at the same place and
-        // stay zero between calls, whatever shapes the calls have.
+        // Layout: the error word (256 B), then the partials of the units that
+        // straddle CTAs.  Nothing in it needs to start at zero but the error
+        // word.
         pl->ws_err = 256;
-        pl->ws_counters = round_up(static_cast<size_t>(kMaxGroups) * c->Hkv * sizeof(int), 256);
-        pl->ws_partials = static_cast<size_t>(pl->units + num_ctas) * pl->RPB * (kHeadDimBf16 + 4) * sizeof(float);
+        pl->ws_counters = 0;
+        pl->ways = decode_launch_shape(pl->mt).ways;
+        pl->part_rows = std::min(pl->R, pl->RPB);
+        pl->ws_partials = static_cast<size_t>(pl->units + num_ctas) * pl->ways * pl->part_rows *
+                          (kHeadDimBf16 + 4) * sizeof(float);
         pl->ws_total = pl->ws_err + pl->ws_counters + pl->ws_partials;
     }
     return ok();
@@ -237,11 +240,17 @@ kvc_status do_append(kvc_cache* c, int layer, const void* k_new, const void* v_n
     }
     cudaError_t e = launch_append(p, max_n, stream);
     if (e != cudaSuccess) return cuda_fail(e, "kv_append launch");
+    ++c->launches;
     return ok();
 }
 
+// With k_new / v_new given (bf16, warps owning whole tiles) the attention
+// kernel also performs the append; *main_enqueued tells whether the attention
+// kernel was enqueued (so a caller can undo its length update if not).
 kvc_status do_attention(kvc_cache* c, int layer, const void* q, const AttnPlan& pl, const int32_t* n_new, void* out,
-                        void* ws, size_t ws_bytes, cudaStream_t stream) {
+                        void* ws, size_t ws_bytes, cudaStream_t stream, const void* k_new = nullptr,
+                        const void* v_new = nullptr, bool* main_enqueued = nullptr) {
+    if (main_enqueued) *main_enqueued = false;
     const int64_t* lens = c->lens.data() + static_cast<size_t>(layer) * c->B;
     if (c->B == 0 || pl.T == 0) return ok();
     if (c->dtype == KVC_F32) {
@@ -266,6 +275,7 @@ kvc_status do_attention(kvc_cache* c, int layer, const void* q, const AttnPlan& 
         }
         cudaError_t e = launch_attn_f32(p, stream);
         if (e != cudaSuccess) return cuda_fail(e, "attn_f32 launch");
+        ++c->launches;
         return ok();
     }
 
@@ -276,7 +286,6 @@ kvc_status do_attention(kvc_cache* c, int layer, const void* q, const AttnPlan& 
     DecodeParams p;
     uint8_t* wsb = static_cast<uint8_t*>(ws);
     p.err = reinterpret_cast<int*>(wsb);
-    p.counters = reinterpret_cast<int*>(wsb + pl.ws_err);
     p.partials = reinterpret_cast<float*>(wsb + pl.ws_err + pl.ws_counters);
     p.q = q;
     p.out = out;
@@ -290,6 +299,13 @@ kvc_status do_attention(kvc_cache* c, int layer, const void* q, const AttnPlan& 
     p.RPB = pl.RPB;
     p.RB = pl.RB;
     p.NB = pl.NB;
+    p.part_rows = pl.part_rows;
+    p.append_new = (k_new != nullptr && v_new != nullptr) ? 1 : 0;
+    p.k_new = k_new;
+    p.v_new = v_new;
+    p.k_cache = c->k[layer];
+    p.v_cache = c->v[layer];
+    p.Tn = pl.T;
     p.scale_log2 = static_cast<float>(1.4426950408889634 / sqrt(static_cast<double>(c->d)));
     long long tiles = 0;
     for (int b = 0; b < c->B; ++b) {
@@ -323,15 +339,64 @@ kvc_status do_attention(kvc_cache* c, int layer, const void* q, const AttnPlan& 
     const int grid = static_cast<int>(std::max(1ll, std::min<long long>(c->num_sms, tiles)));
     p.num_ctas = grid;
 
+    // Does any unit need the combine kernel?  A unit is written in full by the
+    // attention kernel when all its tiles fall in one CTA (CTA i owns tiles
+    // floor(iN/P) .. floor((i+1)N/P)-1, so tile x belongs to CTA
+    // ((x+1)P - 1) / N) and, when warps own whole tiles, it is one tile.
+    bool need_combine = false;
+    {
+        const long long N = tiles, P = grid;
+        for (int q = 0; q < pl.NB && !need_combine; ++q) {
+            const int nt = (p.gstart[q + 1] - p.gstart[q]) / c->Hkv;
+            if (nt == 0) continue;
+            if (pl.ways > 1 && nt > 1) {
+                need_combine = true;
+                break;
+            }
+            for (int kvh = 0; kvh < c->Hkv; ++kvh) {
+                const long long us = p.gstart[q] + static_cast<long long>(kvh) * nt, ue = us + nt - 1;
+                if (((us + 1) * P - 1) / N != ((ue + 1) * P - 1) / N) {
+                    need_combine = true;
+                    break;
+                }
+            }
+        }
+    }
+
     if (ws != c->last_ws) {
-        // New workspace: clear the error word and the per-unit counters once;
-        // every later call leaves them zero again.
-        cudaError_t e = cudaMemsetAsync(ws, 0, pl.ws_err + pl.ws_counters, stream);
+        // New workspace: clear the error word once; kernels only ever set it.
+        cudaError_t e = cudaMemsetAsync(ws, 0, pl.ws_err, stream);
         if (e != cudaSuccess) return cuda_fail(e, "cudaMemsetAsync(workspace)");
         c->last_ws = ws;
     }
     cudaError_t e = launch_decode_bf16(p, c->tmK[layer], c->tmV[layer], pl.mt, grid, stream);
     if (e != cudaSuccess) return cuda_fail(e, "split-KV attention launch");
+    ++c->launches;
+    if (main_enqueued) *main_enqueued = true;
+    if (need_combine) {
+        static_assert(sizeof(CombineParams) < 32000, "kernel parameter block too large");
+        CombineParams cp;
+        cp.partials = p.partials;
+        cp.out = out;
+        cp.Hq = pl.Hq;
+        cp.Hkv = c->Hkv;
+        cp.G = pl.G;
+        cp.T = pl.T;
+        cp.R = pl.R;
+        cp.RPB = pl.RPB;
+        cp.RB = pl.RB;
+        cp.NB = pl.NB;
+        cp.ways = pl.ways;
+        cp.part_rows = pl.part_rows;
+        cp.total_tiles = p.total_tiles;
+        cp.num_ctas = grid;
+        for (int b = 0; b < c->B; ++b) cp.n_new[b] = n_new[b];
+        for (int q = 0; q <= pl.NB; ++q) cp.gstart[q] = p.gstart[q];
+        for (int i = 0; i <= grid; ++i) cp.cta_start[i] = static_cast<int>(static_cast<long long>(i) * tiles / grid);
+        e = launch_combine_bf16(cp, stream);
+        if (e != cudaSuccess) return cuda_fail(e, "split-KV combine launch");
+        ++c->launches;
+    }
     (void)ws_bytes;
     return ok();
 }
@@ -470,9 +535,19 @@ kvc_status kvc_append_attention(kvc_cache* c, int layer, const void* q, const vo
     s = ensure_device(c);
     if (s) return s;
     cudaStream_t st = static_cast<cudaStream_t>(stream);
+    int64_t* lw = c->lens.data() + static_cast<size_t>(layer) * c->B;
+    if (c->dtype == KVC_BF16 && pl.mt == 1 && max_n > 0) {
+        // Warps own whole tiles: the attention kernel writes the new rows into
+        // the cache itself (one launch instead of two).
+        for (int b = 0; b < c->B; ++b) lw[b] += n_new[b];
+        bool enqueued = false;
+        s = do_attention(c, layer, q, pl, n_new, out, workspace, workspace_bytes, st, k_new, v_new, &enqueued);
+        if (s && !enqueued)
+            for (int b = 0; b < c->B; ++b) lw[b] -= n_new[b];  // nothing ran: lengths unchanged
+        return s;
+    }
     s = do_append(c, layer, k_new, v_new, T, n_new, max_n, st);
     if (s) return s;
-    int64_t* lw = c->lens.data() + static_cast<size_t>(layer) * c->B;
     for (int b = 0; b < c->B; ++b) lw[b] += n_new[b];
     s = do_attention(c, layer, q, pl, n_new, out, workspace, workspace_bytes, st);
     if (s) {
@@ -545,8 +620,7 @@ kvc_status kvc_device_status(kvc_cache* c, void* workspace, void* stream, int32_
     if (e != cudaSuccess) return cuda_fail(e, "reading the device error word");
     *code = v;
     if (v != 0) {
-        // An interrupted call may have left unit counters set: make the next
-        // call on this handle clear the workspace header again.
+        // Make the next call on this handle clear the workspace header again.
         c->last_ws = nullptr;
         e = cudaMemsetAsync(workspace, 0, sizeof v, st);
         if (e == cudaSuccess) e = cudaStreamSynchronize(st);
@@ -563,6 +637,8 @@ kvc_status kvc_selftest_bounded_wait(void* workspace, uint64_t limit_ns, void* s
     return ok();
 }
 
+uint64_t kvc_kernel_launches(const kvc_cache* c) { return c ? c->launches : 0; }
+
 const char* kvc_last_error(void) { return g_last_error.c_str(); }
 
 const char* kvc_version(void) { return "kvc 0.1 (sm_103a)"; }
@@ -573,7 +649,7 @@ const char* kvc_version(void) { return "kvc 0.1 (sm_103a)"; }
 // Allocation-free attention (kvc_gqa_attention_noalloc)
 //
 // For callers that cannot allocate device memory themselves: the split-KV
-// scratch (error word, unit counters, partial results) lives in one
+// scratch (error word and partial results) lives in one
 // file-scope device array instead of a caller-provided workspace.  The array
 // is part of this library's device image, so every GPU that loads the
 // library holds its KVC_NOALLOC_SCRATCH_BYTES until the process exits.
@@ -631,9 +707,9 @@ extern "C" kvc_status kvc_gqa_attention_noalloc(kvc_cache* c, int layer, const v
     s = noalloc_scratch_address(dev, &scratch);
     if (s) return s;
     cudaStream_t st = static_cast<cudaStream_t>(stream);
-    // The array keeps whatever the previous call left: zero the error word and
-    // the unit counters, which the kernel needs to start at zero.
-    e = cudaMemsetAsync(scratch, 0, pl.ws_err + pl.ws_counters, st);
+    // The array keeps whatever the previous call left: zero the error word,
+    // the one part the kernels need to start at zero.
+    e = cudaMemsetAsync(scratch, 0, pl.ws_err, st);
     if (e != cudaSuccess) return cuda_fail(e, "cudaMemsetAsync(static scratch)");
     c->last_ws = scratch;
     return do_attention(c, layer, q, pl, n_new, out, scratch, KVC_NOALLOC_SCRATCH_BYTES, st);

@@ -11,6 +11,7 @@ namespace kvc {
 
 constexpr int kMaxBatch = KVC_MAX_BATCH;
 constexpr int kMaxGroups = 1024;  // (row, row-block) groups of one attention call
+constexpr int kMaxCtas = 1024;    // attention CTAs (one per SM)
 
 // Keys per K/V tile of the split-KV kernel, and the head width it is built for.
 constexpr int kKeyTile = 64;
@@ -43,29 +44,64 @@ cudaError_t launch_append(const AppendParams& p, int max_n_new, cudaStream_t str
 // Tiles are numbered unit after unit: group q's units own tiles
 // gstart[q] .. gstart[q+1]-1, kvh after kvh.  CTA i of P processes tiles
 // floor(i*N/P) .. floor((i+1)*N/P)-1, so every CTA gets the same number of
-// tiles (+-1) whatever the row lengths.
+// tiles (+-1) whatever the row lengths.  A unit seen in full by one writer is
+// written to `out` directly; otherwise each writer (a CTA, or with warps
+// owning whole tiles a warp of it) leaves its partial softmax state in
+// sub-slot (u + i) * ways + w, where i is the CTA (u + i is unique per
+// (unit, CTA) pair: along the unit/CTA staircase every step raises it), and
+// the combine kernel merges them.
 // ---------------------------------------------------------------------------
 struct DecodeParams {
     const void* q;      // [B, Hq, T, d] bf16
     void* out;          // [B, Hq, T, d] bf16
-    float* partials;    // [(units + P) slots][RPB rows][d + 2] : O (d), m, l
-    int* counters;      // [units] contributor counters, zero between calls
+    float* partials;    // [(units + P) * ways sub-slots][part_rows][d + 4] : O (d), m, l, pad
     int* err;           // device error word
     int B, Hq, Hkv, G, T, max_len;
     int R, RPB, RB, NB;
+    int part_rows;      // rows stored per partial sub-slot: min(R, RPB)
     int total_tiles;
     int num_ctas;
     float scale_log2;   // log2(e) / sqrt(d)
+    // In-kernel append (warps owning whole tiles only): when append_new is set
+    // the chunk's rows k_new/v_new [B, Hkv, Tn, d] are written to the layer's
+    // cache at positions prior[b] .. prior[b]+n_new[b]-1 by the warp that
+    // processes the tile holding them, which also patches them into its
+    // staged tile, so the append needs no launch of its own.
+    const void* k_new;
+    const void* v_new;
+    void* k_cache;
+    void* v_cache;
+    int append_new;
+    int Tn;
     int prior[kMaxBatch];    // lens[b] - n_new[b]
     int n_new[kMaxBatch];
     int gstart[kMaxGroups + 1];
 };
+
+// Log-sum-exp merge of the units the attention kernel left as partials (one
+// CTA per unit; the grid covers every unit and the ones written in full
+// return at once).  Partial rows live at
+// ((u + cta) * ways + warp) * part_rows + row.
+struct CombineParams {
+    const float* partials;
+    void* out;
+    int Hq, Hkv, G, T, R, RPB, RB, NB;
+    int ways;       // partial sub-slots per (unit, CTA)
+    int part_rows;  // rows stored per partial sub-slot
+    int total_tiles, num_ctas;
+    int n_new[kMaxBatch];
+    int gstart[kMaxGroups + 1];
+    int cta_start[kMaxCtas + 1];  // first tile of each attention CTA: floor(i * N / P)
+};
+
+cudaError_t launch_combine_bf16(const CombineParams& p, cudaStream_t stream);
 
 // Grid / block / shared memory of the split-KV kernel for a given MT.
 struct DecodeLaunch {
     int mt;
     int threads;
     size_t smem_bytes;
+    int ways;  // partial sub-slots per (unit, CTA): 4 when warps own whole tiles
 };
 DecodeLaunch decode_launch_shape(int mt);
 
@@ -96,7 +132,8 @@ enum DeviceError : int {
     kDevTimeoutFull = 1,   // consumer gave up waiting for a K/V tile
     kDevTimeoutEmpty = 2,  // producer gave up waiting for a free stage
     kDevTimeoutDrain = 3,  // abort path gave up waiting for copies in flight
-    kDevTimeoutTest = 4    // the self-test wait expired, as it is meant to
+    kDevTimeoutTest = 4,   // the self-test wait expired, as it is meant to
+    kDevTimeoutTag = 5     // consumer gave up waiting for the producer to claim a stage
 };
 
 // Self-test of the bounded wait: waits on an mbarrier that nothing arrives at,

@@ -99,7 +99,7 @@ kvc_status kvc_append(kvc_cache* c, int layer, const void* k_new, const void* v_
                       const int32_t* n_new, void* stream);
 
 /* Bytes of device workspace kvc_gqa_attention needs for this handle, q_heads
- * and T (split-KV partial results, per-unit counters and an error word).
+ * and T (an error word and the split-KV partial results).
  * 0 means no workspace is needed (f32 path).  Returns 0 for invalid input. */
 size_t kvc_workspace_bytes(const kvc_cache* c, int q_heads, int T);
 
@@ -111,9 +111,9 @@ size_t kvc_workspace_bytes(const kvc_cache* c, int q_heads, int T);
  * Accumulation is fp32; out has the cache's element type.
  * workspace: device buffer of at least kvc_workspace_bytes(c, Hq, T) bytes,
  * 256-byte aligned, used by one call at a time (calls that share a workspace
- * must be ordered on one stream).  The library keeps its counters zero
- * between calls; it clears them itself when a call sees a workspace pointer
- * different from the previous call's.
+ * must be ordered on one stream).  Its contents need no initialisation: the
+ * library clears the error word itself the first time a handle sees a
+ * workspace pointer.
  * Errors (out untouched): KVC_ERR_ARG, KVC_ERR_SHAPE (Hq % Hkv != 0,
  * n_new[b] < 0, n_new[b] > T, n_new[b] > lens[b]), KVC_ERR_WORKSPACE,
  * KVC_ERR_CUDA. */
@@ -128,7 +128,7 @@ kvc_status kvc_append_attention(kvc_cache* c, int layer, const void* q, const vo
                                 size_t workspace_bytes, void* stream);
 
 /* Size of the device scratch array behind kvc_gqa_attention_noalloc. */
-#define KVC_NOALLOC_SCRATCH_BYTES (16u << 20)
+#define KVC_NOALLOC_SCRATCH_BYTES (32u << 20)
 
 /* kvc_gqa_attention without a workspace argument, for callers that cannot
  * allocate device memory: for instance a plugin inside a host program that
@@ -139,18 +139,19 @@ kvc_status kvc_append_attention(kvc_cache* c, int layer, const void* q, const vo
  * result) and serves bf16 caches only.
  *
  * Its scratch is one static device array of KVC_NOALLOC_SCRATCH_BYTES
- * (16 MiB) inside the library: every GPU that loads the library holds it
+ * (32 MiB) inside the library: every GPU that loads the library holds it
  * until the process exits.  No cudaMalloc, cudaFree or other allocating
  * call is made.  A call whose split-KV scratch would exceed the array
  * (kvc_workspace_bytes(c, q_heads, T) > KVC_NOALLOC_SCRATCH_BYTES, e.g.
  * long prefill chunks) is rejected with KVC_ERR_WORKSPACE before anything
- * is enqueued; decode and speculative-verify shapes fit.
+ * is enqueued; decode and speculative-verify shapes (up to 64 query rows
+ * per KV head) of batches up to 64 rows fit.
  *
  * The first call on each device looks up the array's device address
  * (cudaGetSymbolAddress, with that device current) and caches it; make that
  * first call before any stream capture.  Every call on a device shares the
  * one array, which keeps the last call's contents; each call clears the
- * parts that must start at zero.  Calls that overlap on the GPU (different
+ * part that must start at zero (the error word).  Calls that overlap on the GPU (different
  * streams, or several caches at once) race on the array: order them on one
  * stream.  The device must be the cache's device (else KVC_ERR_ARG). */
 kvc_status kvc_gqa_attention_noalloc(kvc_cache* c, int layer, const void* q, int q_heads, int T,
@@ -182,9 +183,8 @@ kvc_status kvc_length(const kvc_cache* c, int64_t* out);
 /* Read the device error word of a workspace used by handle c after the
  * stream's work ends: synchronizes `stream`, copies the word and stores it in
  * *code (0 = clean; otherwise a kernel's bounded wait expired and that call's
- * output is not valid), then clears the word and makes the handle's next call
- * re-clear the workspace's counters.  Returns KVC_ERR_DEVICE_TIMEOUT when
- * *code != 0. */
+ * output is not valid), then clears the word.  Returns KVC_ERR_DEVICE_TIMEOUT
+ * when *code != 0. */
 kvc_status kvc_device_status(kvc_cache* c, void* workspace, void* stream, int32_t* code);
 
 /* Self-test of the kernels' bounded waits: launches one CTA that waits on an
@@ -193,6 +193,11 @@ kvc_status kvc_device_status(kvc_cache* c, void* workspace, void* stream, int32_
  * so a following kvc_device_status reports KVC_ERR_DEVICE_TIMEOUT.  No fault,
  * no hang. */
 kvc_status kvc_selftest_bounded_wait(void* workspace, uint64_t limit_ns, void* stream);
+
+/* Number of kernels this handle has enqueued so far (append, attention and,
+ * when a call's units were split across CTAs, the combine kernel).  Host
+ * counter only; lets a caller check how many launches a region issued. */
+uint64_t kvc_kernel_launches(const kvc_cache* c);
 
 /* Message of the calling thread's last failed call ("" if none). */
 const char* kvc_last_error(void);

@@ -68,7 +68,7 @@ def test_noalloc_rejects_oversized_calls():
     B, Hkv, G, d, T = 4, 8, 4, 128, 512  # a long prefill chunk needs more than the static scratch
     cache = KVCache(1, B, Hkv, 1024, d)
     cache.append(0, _bf16(1, 1, (B, Hkv, T, d)), _bf16(1, 2, (B, Hkv, T, d)), np.full(B, T))
-    assert cache.workspace_bytes(Hkv * G, T) > (16 << 20)
+    assert cache.workspace_bytes(Hkv * G, T) > (32 << 20)
     q = _bf16(3, 3, (B, Hkv * G, T, d))
     out = torch.zeros_like(q)
     assert _noalloc(cache, q, np.full(B, T), out) == 7  # KVC_ERR_WORKSPACE, nothing enqueued
