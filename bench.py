@@ -350,7 +350,7 @@ def run_oracle_sample(w: Workload, budget_s: float = 12.0):
     rng = np.random.default_rng(0)
     done_work, t_total, calls, rows = 0, 0.0, 0, 0
     b = 0
-    while t_total < budget_s and rows < 64:
+    while t_total < budget_s and rows < 4096:
         L = int(w.lens_at(0)[b])
         n = int(w.n_new[b])
         c = ref.OracleCache(1, 1, s.Hkv, L, s.d)
