@@ -22,7 +22,7 @@ INCLUDE = os.path.join(ROOT, "include")
 BUILD_DIR = os.path.join(ROOT, "_build")
 LIB_PATH = os.path.join(PKG_DIR, "libkvc.so")
 
-SOURCES = ["kvc_host.cu", "append.cu", "attn_f32.cu", "decode_bf16.cu"]
+SOURCES = ["kvc_host.cu", "append.cu", "attn_f32.cu", "decode_bf16.cu", "prefill_tc.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC,-O2", "-I" + INCLUDE, "-I" + CSRC]
 

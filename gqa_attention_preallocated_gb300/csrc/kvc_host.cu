@@ -35,7 +35,8 @@ struct kvc_cache {
     bool dev_ready = false;
     int device = -1;
     int num_sms = 0;
-    std::vector<CUtensorMap> tmK, tmV;
+    std::vector<CUtensorMap> tmK, tmV;        // 64-row boxes (split-KV kernel)
+    std::vector<CUtensorMap> tmK128, tmV128;  // 128-row boxes (prefill kernel)
     std::vector<char> tm_ready;
     const void* last_ws = nullptr;
     uint64_t launches = 0;  // kernels this handle has enqueued
@@ -95,24 +96,31 @@ kvc_status ensure_device(kvc_cache* c) {
     return ok();
 }
 
-// 2-D view of one layer's K or V: rows = B*Hkv*max_len, 128 bf16 per row;
-// boxes of 64 rows x 64 columns (128 bytes) with the 128-byte swizzle.
-kvc_status encode_layer_maps(kvc_cache* c, int layer) {
-    if (c->tm_ready[layer]) return ok();
+// 2-D bf16 view [rows, 128] with boxes of box_rows rows x 64 columns (128
+// bytes) and the 128-byte swizzle.
+kvc_status encode_rows_map(CUtensorMap* m, const void* base, cuuint64_t rows, cuuint32_t box_rows) {
     EncodeTiledFn fn = encode_fn();
     if (!fn) return fail(KVC_ERR_CUDA, "cuTensorMapEncodeTiled unavailable");
-    const cuuint64_t rows = static_cast<cuuint64_t>(c->B) * c->Hkv * c->max_len;
-    cuuint64_t dims[2] = {static_cast<cuuint64_t>(c->d), rows};
-    cuuint64_t strides[1] = {static_cast<cuuint64_t>(c->d) * 2};
-    cuuint32_t box[2] = {64, static_cast<cuuint32_t>(kKeyTile)};
+    cuuint64_t dims[2] = {static_cast<cuuint64_t>(kHeadDimBf16), rows};
+    cuuint64_t strides[1] = {static_cast<cuuint64_t>(kHeadDimBf16) * 2};
+    cuuint32_t box[2] = {64, box_rows};
     cuuint32_t estr[2] = {1, 1};
-    for (int w = 0; w < 2; ++w) {
-        CUtensorMap* m = w ? &c->tmV[layer] : &c->tmK[layer];
-        CUresult r = fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, w ? c->v[layer] : c->k[layer], dims, strides, box, estr,
-                        CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-                        CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
-        if (r != CUDA_SUCCESS) return fail(KVC_ERR_CUDA, "cuTensorMapEncodeTiled failed (%d)", static_cast<int>(r));
-    }
+    CUresult r = fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box, estr,
+                    CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                    CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    if (r != CUDA_SUCCESS) return fail(KVC_ERR_CUDA, "cuTensorMapEncodeTiled failed (%d)", static_cast<int>(r));
+    return ok();
+}
+
+// One layer's K and V as rows = B*Hkv*max_len: 64-row and 128-row boxes.
+kvc_status encode_layer_maps(kvc_cache* c, int layer) {
+    if (c->tm_ready[layer]) return ok();
+    const cuuint64_t rows = static_cast<cuuint64_t>(c->B) * c->Hkv * c->max_len;
+    kvc_status s;
+    if ((s = encode_rows_map(&c->tmK[layer], c->k[layer], rows, kKeyTile))) return s;
+    if ((s = encode_rows_map(&c->tmV[layer], c->v[layer], rows, kKeyTile))) return s;
+    if ((s = encode_rows_map(&c->tmK128[layer], c->k[layer], rows, 128))) return s;
+    if ((s = encode_rows_map(&c->tmV128[layer], c->v[layer], rows, 128))) return s;
     c->tm_ready[layer] = 1;
     return ok();
 }
@@ -279,9 +287,62 @@ kvc_status do_attention(kvc_cache* c, int layer, const void* q, const AttnPlan& 
         return ok();
     }
 
-    // bf16 split-KV path
     kvc_status s = encode_layer_maps(c, layer);
     if (s) return s;
+    if (pl.R > 64 && k_new == nullptr) {
+        // Chunked prefill: tensor-core kernel, one CTA per (b, kvh, 128
+        // positions, pair of heads), longest first.
+        static_assert(sizeof(PrefillParams) < 32000, "kernel parameter block too large");
+        PrefillParams pp;
+        pp.q = q;
+        pp.out = out;
+        pp.err = static_cast<int*>(ws);
+        pp.B = c->B;
+        pp.Hq = pl.Hq;
+        pp.Hkv = c->Hkv;
+        pp.G = pl.G;
+        pp.T = pl.T;
+        pp.max_len = c->max_len;
+        pp.ntb = (pl.T + 127) / 128;
+        pp.npair = (pl.G + 1) / 2;
+        pp.scale_log2 = static_cast<float>(1.4426950408889634 / sqrt(static_cast<double>(c->d)));
+        std::vector<std::pair<int, int>> items;  // (cost, code)
+        for (int b = 0; b < c->B; ++b) {
+            pp.prior[b] = static_cast<int>(lens[b] - n_new[b]);
+            pp.n_new[b] = n_new[b];
+            for (int kvh = 0; kvh < c->Hkv; ++kvh)
+                for (int tb = 0; tb < pp.ntb; ++tb) {
+                    const int t0 = tb * 128;
+                    if (t0 >= n_new[b]) continue;
+                    const int kmax = pp.prior[b] + std::min(t0 + 127, static_cast<int>(n_new[b]) - 1);
+                    for (int pr = 0; pr < pp.npair; ++pr) {
+                        const int code = ((b * c->Hkv + kvh) * pp.ntb + tb) * pp.npair + pr;
+                        items.push_back({(kmax / 128 + 1) * std::min(2, pl.G - 2 * pr), code});
+                    }
+                }
+        }
+        if (!items.empty() && static_cast<int>(items.size()) <= kMaxPrefillItems) {
+            std::stable_sort(items.begin(), items.end(),
+                             [](const std::pair<int, int>& a, const std::pair<int, int>& b2) { return a.first > b2.first; });
+            pp.n_items = static_cast<int>(items.size());
+            for (int i = 0; i < pp.n_items; ++i) pp.items[i] = items[i].second;
+            CUtensorMap tmQ;
+            if ((s = encode_rows_map(&tmQ, q, static_cast<cuuint64_t>(c->B) * pl.Hq * pl.T, 128))) return s;
+            if (ws != c->last_ws) {
+                cudaError_t e = cudaMemsetAsync(ws, 0, pl.ws_err, stream);
+                if (e != cudaSuccess) return cuda_fail(e, "cudaMemsetAsync(workspace)");
+                c->last_ws = ws;
+            }
+            cudaError_t e = launch_prefill_tc(pp, tmQ, c->tmK128[layer], c->tmV128[layer], stream);
+            if (e != cudaSuccess) return cuda_fail(e, "prefill attention launch");
+            ++c->launches;
+            if (main_enqueued) *main_enqueued = true;
+            return ok();
+        }
+        // otherwise (no rows to attend, or too many items): the split-KV path below
+    }
+
+    // bf16 split-KV path
     static_assert(sizeof(DecodeParams) < 32000, "kernel parameter block too large");
     DecodeParams p;
     uint8_t* wsb = static_cast<uint8_t*>(ws);
@@ -453,6 +514,8 @@ kvc_status kvc_create(kvc_cache** out, int layers, int batch, int kv_heads, int 
     c->lens.assign(static_cast<size_t>(layers) * batch, 0);
     c->tmK.resize(layers);
     c->tmV.resize(layers);
+    c->tmK128.resize(layers);
+    c->tmV128.resize(layers);
     c->tm_ready.assign(layers, 0);
     *out = c;
     return ok();

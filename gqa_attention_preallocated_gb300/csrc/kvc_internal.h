@@ -126,6 +126,29 @@ struct F32Params {
 
 cudaError_t launch_attn_f32(const F32Params& p, cudaStream_t stream);
 
+// ---------------------------------------------------------------------------
+// Chunked prefill on tcgen05 (bf16, d = 128, G*T > 64 query rows per KV head).
+// One CTA per item = (b, kvh, block of 128 query positions, pair of query
+// heads); items are packed as ((b * Hkv + kvh) * ntb + tb) * npair + pair and
+// listed longest first.
+// ---------------------------------------------------------------------------
+constexpr int kMaxPrefillItems = 4096;
+struct PrefillParams {
+    const void* q;
+    void* out;
+    int* err;
+    int B, Hq, Hkv, G, T, max_len;
+    int ntb, npair, n_items;
+    float scale_log2;
+    int prior[kMaxBatch];
+    int n_new[kMaxBatch];
+    int items[kMaxPrefillItems];
+};
+
+size_t prefill_smem_bytes();
+cudaError_t launch_prefill_tc(const PrefillParams& p, const CUtensorMap& tmQ, const CUtensorMap& tmK,
+                              const CUtensorMap& tmV, cudaStream_t stream);
+
 // Device error codes written to the workspace error word.
 enum DeviceError : int {
     kDevOk = 0,

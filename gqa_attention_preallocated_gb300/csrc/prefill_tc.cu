@@ -1,0 +1,465 @@
+// Chunked-prefill GQA attention on the 5th-generation tensor cores (tcgen05 + TMEM), bf16, d = 128.
+//
+// What it computes ("Implement grouped-query attention over a preallocated KV
+// cache...", "A strong answer", gqa_attention): query t < n_new[b] of head h
+// sits at position prior[b] + t (prior = lens - n_new) and attends to keys
+// 0 .. prior[b] + t of KV head h / G with softmax scale 1/sqrt(d).  Padded
+// queries (t >= n_new[b]) give 0.  This is the dense-contraction regime of the
+// method (T = chunk): QK^T and PV are 128 x 128 x 128 MMAs.
+//
+// Work item = (row b, KV head, block of 128 query positions, pair of query
+// heads of that KV head's group): both heads share every K/V tile staged in
+// shared memory, so each 64 KB K/V tile feeds four 128x128x128 MMAs.
+// Items are launched longest first (the host sorts them by key-tile count).
+//
+// Warp roles (12 warps):
+//   warp 0      TMA producer: Q tiles once, then K and V tiles (128 keys) into
+//               two-stage rings guarded by mbarriers.
+//   warp 1      MMA issuer (one lane): S_i = Q_i K^T into TMEM, then, once the
+//               softmax has written P_i into TMEM over S_i, O_i += P_i V with
+//               P_i as the TMEM A operand.  Issue order S0(j), S1(j), PV0(j),
+//               S0(j+1), PV1(j), S1(j+1), ... keeps the tensor core busy while
+//               each softmax warpgroup works on the other head's tile.
+//   warps 4-7   softmax of head 0 of the pair, one thread per query row
+//   warps 8-11  softmax of head 1 of the pair
+// TMEM (512 columns): S0 [0,128), S1 [128,256), O0 [256,384), O1 [384,512).
+//
+// Softmax is online in base 2 (log2(e)/sqrt(d) folded into one scale) with a
+// lazy rescale: the running max used for the exponentials only moves when
+// the row max exceeds it by more than 8 (a factor 256), and only then is O
+// rescaled in TMEM; O and l share the same reference, so the result is exact.
+// Causal mask ("Write the causal mask for a decode step...", bottom-right):
+// key tiles past the block's last visible key are never loaded; tiles fully
+// visible to every row of the block skip the mask; the rest mask per element
+// with a select.  V rows past the last visible key are cleared in shared
+// memory before PV, so stale or NaN cache slots never meet p = 0.
+// Every wait is bounded in time; on expiry an error code is recorded.
+
+#include <math.h>
+
+#include <utility>
+
+#include "kvc_internal.h"
+#include "ptx.cuh"
+
+namespace kvc {
+
+namespace {
+
+constexpr int kThreadsPF = 384;
+constexpr int kD = 128;
+constexpr int kBoxBytes = 128 * 128;           // 128 rows x 64 columns x 2 B (one swizzled box)
+constexpr int kTile128 = 2 * kBoxBytes;         // 128 rows x 128 columns
+constexpr uint64_t kWaitNs = 2000000000ull;
+constexpr float kRescaleThreshold = 8.0f;       // log2 of the largest factor kept unrescaled
+
+// Shared memory map (offsets from the 1024-aligned base).
+constexpr int kOffQ = 0;                        // Q0, Q1
+constexpr int kOffK = 2 * kTile128;             // K stages 0, 1
+constexpr int kOffV = 4 * kTile128;             // V stages 0, 1
+constexpr int kOffBar = 6 * kTile128;
+// barrier indices
+constexpr int kBarQ = 0, kBarKFull = 1, kBarKEmpty = 3, kBarVFull = 5, kBarVEmpty = 7, kBarS = 9, kBarP = 11,
+              kBarO = 13, kNumBars = 15;
+constexpr size_t kSmemPF = 1024 + kOffBar + kNumBars * 8 + 16;
+
+__device__ __forceinline__ uint64_t smem_desc(uint32_t addr, uint32_t lbo, uint32_t sbo) {
+    // tcgen05 shared-memory matrix descriptor: start >> 4, leading / stride byte
+    // offsets >> 4, fixed 0b001 at bits 46-48, 128-byte swizzle.
+    return static_cast<uint64_t>((addr & 0x3FFFF) >> 4) | (static_cast<uint64_t>((lbo >> 4) & 0x3FFF) << 16) |
+           (static_cast<uint64_t>((sbo >> 4) & 0x3FFF) << 32) | (1ull << 46) | (2ull << 61);
+}
+
+// Instruction descriptor, kind::f16: fp32 accumulator, bf16 A and B, M = N = 128.
+__device__ __forceinline__ uint32_t instr_desc(bool b_mn_major) {
+    return (1u << 4) | (1u << 7) | (1u << 10) | (static_cast<uint32_t>(b_mn_major) << 16) | ((128u >> 3) << 17) |
+           ((128u >> 4) << 24);
+}
+
+__device__ __forceinline__ void mma_ss(uint32_t d_tmem, uint64_t a, uint64_t b, uint32_t id, uint32_t acc) {
+    asm volatile(
+        "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+        "l"(a), "l"(b), "r"(id), "r"(acc)
+        : "memory");
+}
+
+__device__ __forceinline__ void mma_ts(uint32_t d_tmem, uint32_t a_tmem, uint64_t b, uint32_t id, uint32_t acc) {
+    asm volatile(
+        "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d_tmem),
+        "r"(a_tmem), "l"(b), "r"(id), "r"(acc)
+        : "memory");
+}
+
+__device__ __forceinline__ void mma_commit(uint32_t bar) {
+    asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar) : "memory");
+}
+
+__device__ __forceinline__ void tc_fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
+__device__ __forceinline__ void tc_fence_after() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
+
+// 32 consecutive 32-bit TMEM columns of this thread's lane.
+__device__ __forceinline__ void tmem_ld32(uint32_t taddr, uint32_t (&r)[32]) {
+    asm volatile(
+        "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16,%17,%18,"
+        "%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%32];"
+        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]), "=r"(r[8]),
+          "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15]), "=r"(r[16]),
+          "=r"(r[17]), "=r"(r[18]), "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]), "=r"(r[24]),
+          "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
+        : "r"(taddr)
+        : "memory");
+}
+
+__device__ __forceinline__ void tmem_st32(uint32_t taddr, const uint32_t (&r)[32]) {
+    asm volatile(
+        "tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16,%17,%18,"
+        "%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31,%32};" ::"r"(taddr),
+        "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7]), "r"(r[8]), "r"(r[9]),
+        "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]), "r"(r[14]), "r"(r[15]), "r"(r[16]), "r"(r[17]), "r"(r[18]),
+        "r"(r[19]), "r"(r[20]), "r"(r[21]), "r"(r[22]), "r"(r[23]), "r"(r[24]), "r"(r[25]), "r"(r[26]), "r"(r[27]),
+        "r"(r[28]), "r"(r[29]), "r"(r[30]), "r"(r[31])
+        : "memory");
+}
+
+__device__ __forceinline__ void tmem_ld_wait() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
+__device__ __forceinline__ void tmem_st_wait() { asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory"); }
+
+struct Item {
+    int b, kvh, tb, pair;
+};
+
+__device__ __forceinline__ Item decode_item(const PrefillParams& p, int code) {
+    Item it;
+    it.pair = code % p.npair;
+    code /= p.npair;
+    it.tb = code % p.ntb;
+    code /= p.ntb;
+    it.kvh = code % p.Hkv;
+    it.b = code / p.Hkv;
+    return it;
+}
+
+__global__ void __launch_bounds__(kThreadsPF, 1)
+    prefill_tc_kernel(const __grid_constant__ PrefillParams p, const __grid_constant__ CUtensorMap tmQ,
+                      const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmV) {
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    const uint32_t sbase = ptx::smem_addr(smem);
+    const uint32_t bar0 = sbase + kOffBar;
+    auto bar = [&](int i) { return bar0 + 8 * i; };
+    volatile uint32_t* tmem_slot = reinterpret_cast<volatile uint32_t*>(smem + kOffBar + kNumBars * 8);
+    volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + kOffBar + kNumBars * 8 + 8);
+
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+
+    if (tid == 0) {
+        ptx::mbar_init(bar(kBarQ), 1);
+        for (int s = 0; s < 2; ++s) {
+            ptx::mbar_init(bar(kBarKFull + s), 1);
+            ptx::mbar_init(bar(kBarKEmpty + s), 1);
+            ptx::mbar_init(bar(kBarVFull + s), 1);
+            ptx::mbar_init(bar(kBarVEmpty + s), 1);
+            ptx::mbar_init(bar(kBarS + s), 1);
+            ptx::mbar_init(bar(kBarP + s), 4);
+            ptx::mbar_init(bar(kBarO + s), 1);
+        }
+        *abort_flag = 0;
+        ptx::fence_barrier_init();
+    }
+    if (warp == 0 && lane == 0) {
+        ptx::tma_prefetch_desc(&tmQ);
+        ptx::tma_prefetch_desc(&tmK);
+        ptx::tma_prefetch_desc(&tmV);
+    }
+    if (warp == 1) {
+        asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], 512;" ::"r"(
+                         sbase + kOffBar + kNumBars * 8)
+                     : "memory");
+        asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = *tmem_slot;
+    ptx::grid_dependency_wait();
+    ptx::launch_dependents();
+
+    // Padded queries (t >= n_new[b]) output zeros; spread over the whole grid.
+    {
+        const int rows_total = p.B * p.Hq * p.T;
+        for (int row = blockIdx.x * kThreadsPF + tid; row < rows_total; row += gridDim.x * kThreadsPF) {
+            const int t = row % p.T;
+            const int b = row / (p.Hq * p.T);
+            if (t >= p.n_new[b]) {
+                uint4* dst = reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(p.out) + static_cast<size_t>(row) * kD);
+#pragma unroll
+                for (int i = 0; i < kD * 2 / 16; ++i) dst[i] = make_uint4(0u, 0u, 0u, 0u);
+            }
+        }
+    }
+
+    const Item item = decode_item(p, p.items[blockIdx.x]);
+    const int b = item.b, kvh = item.kvh;
+    const int prior = p.prior[b], nn = p.n_new[b];
+    const int t0 = item.tb * 128;
+    const int h0 = kvh * p.G + 2 * item.pair;
+    const int nh = min(2, p.G - 2 * item.pair);            // heads in this pair (1 or 2)
+    const int kmax = prior + min(t0 + 127, nn - 1);         // last visible key of the block
+    const int nkt = kmax / 128 + 1;                         // key tiles
+    const int full_below = prior + t0;                      // keys <= this are visible to every row
+    const int unit_row0 = (b * p.Hkv + kvh) * p.max_len;    // first cache row of (b, kvh)
+
+    if (warp == 0) {
+        // ------------------------------------------------------------ TMA producer
+        if (lane == 0) {
+            ptx::mbar_arrive_expect_tx(bar(kBarQ), nh * kTile128);
+            for (int i = 0; i < nh; ++i) {
+                const int qrow = ((b * p.Hq) + h0 + i) * p.T + t0;
+                for (int hf = 0; hf < 2; ++hf)
+                    ptx::tma_load_2d(sbase + kOffQ + i * kTile128 + hf * kBoxBytes, &tmQ, hf * 64, qrow, bar(kBarQ));
+            }
+            for (int j = 0; j < nkt && !*abort_flag; ++j) {
+                const int s = j & 1;
+                const int row = unit_row0 + j * 128;
+                if (j >= 2 && !ptx::mbar_wait_bounded(bar(kBarKEmpty + s), ((j >> 1) & 1) ^ 1, kWaitNs)) {
+                    atomicExch(p.err, kDevTimeoutEmpty);
+                    *abort_flag = 1;
+                    break;
+                }
+                ptx::mbar_arrive_expect_tx(bar(kBarKFull + s), kTile128);
+                for (int hf = 0; hf < 2; ++hf)
+                    ptx::tma_load_2d(sbase + kOffK + s * kTile128 + hf * kBoxBytes, &tmK, hf * 64, row,
+                                     bar(kBarKFull + s));
+                if (j >= 2 && !ptx::mbar_wait_bounded(bar(kBarVEmpty + s), ((j >> 1) & 1) ^ 1, kWaitNs)) {
+                    atomicExch(p.err, kDevTimeoutEmpty);
+                    *abort_flag = 1;
+                    break;
+                }
+                ptx::mbar_arrive_expect_tx(bar(kBarVFull + s), kTile128);
+                for (int hf = 0; hf < 2; ++hf)
+                    ptx::tma_load_2d(sbase + kOffV + s * kTile128 + hf * kBoxBytes, &tmV, hf * 64, row,
+                                     bar(kBarVFull + s));
+            }
+        }
+    } else if (warp == 1) {
+        // ------------------------------------------------------------ MMA issuer
+        const uint32_t id_qk = instr_desc(false), id_pv = instr_desc(true);
+        auto wait = [&](int b_idx, int parity) {
+            if (!ptx::mbar_wait_bounded(bar(b_idx), parity, *abort_flag ? 0ull : kWaitNs)) {
+                atomicExch(p.err, kDevTimeoutFull);
+                *abort_flag = 1;
+            }
+        };
+        auto issue_s = [&](int i, int j) {  // S_i = Q_i K_j^T
+            const uint32_t qa = sbase + kOffQ + i * kTile128, ka = sbase + kOffK + (j & 1) * kTile128;
+            for (int k = 0; k < 8; ++k) {
+                const uint32_t off = (k >> 2) * kBoxBytes + (k & 3) * 32;
+                mma_ss(tmem + i * 128, smem_desc(qa + off, 16, 1024), smem_desc(ka + off, 16, 1024), id_qk, k > 0);
+            }
+            mma_commit(bar(kBarS + i));
+        };
+        auto issue_pv = [&](int i, int j) {  // O_i += P_i V_j (P_i in TMEM over S_i)
+            const uint32_t va = sbase + kOffV + (j & 1) * kTile128;
+            for (int k = 0; k < 8; ++k)
+                mma_ts(tmem + 256 + i * 128, tmem + i * 128 + k * 8, smem_desc(va + k * 2048, kBoxBytes, 1024), id_pv,
+                       (j > 0 || k > 0) ? 1u : 0u);
+            mma_commit(bar(kBarO + i));
+        };
+        if (lane == 0) {
+            wait(kBarQ, 0);
+            wait(kBarKFull, 0);
+            tc_fence_after();
+            issue_s(0, 0);
+            if (nh == 2) issue_s(1, 0);
+            mma_commit(bar(kBarKEmpty + 0));
+        }
+        for (int j = 0; j < nkt; ++j) {
+            const int s = j & 1;
+            // V rows past the block's last visible key: clear them (whole warp)
+            // before the PV MMAs read the stage.
+            if (lane == 0) wait(kBarVFull + s, (j >> 1) & 1);
+            __syncwarp();
+            if (j == nkt - 1) {
+                const int vr0 = kmax - j * 128 + 1;  // first row to clear, 1..128
+                uint8_t* vb = smem + kOffV + s * kTile128;
+                for (int idx = lane; idx < 2 * (128 - vr0) * 8; idx += 32) {
+                    const int per = (128 - vr0) * 8;
+                    const int hf = idx / per, rem = idx - hf * per;
+                    *reinterpret_cast<uint4*>(vb + hf * kBoxBytes + (vr0 + (rem >> 3)) * 128 + (rem & 7) * 16) =
+                        make_uint4(0u, 0u, 0u, 0u);
+                }
+                ptx::fence_proxy_async_smem();
+                __syncwarp();
+            }
+            if (lane == 0) {
+                wait(kBarP + 0, j & 1);
+                tc_fence_after();
+                issue_pv(0, j);
+                if (j + 1 < nkt) {
+                    wait(kBarKFull + ((j + 1) & 1), ((j + 1) >> 1) & 1);
+                    tc_fence_after();
+                    issue_s(0, j + 1);
+                }
+                if (nh == 2) {
+                    wait(kBarP + 1, j & 1);
+                    tc_fence_after();
+                    issue_pv(1, j);
+                }
+                mma_commit(bar(kBarVEmpty + s));
+                if (j + 1 < nkt) {
+                    if (nh == 2) issue_s(1, j + 1);
+                    mma_commit(bar(kBarKEmpty + ((j + 1) & 1)));
+                }
+            }
+            __syncwarp();
+        }
+    } else if (warp >= 4) {
+        // ------------------------------------------------------------ softmax (one thread per query row)
+        const int i = (warp - 4) >> 2;  // head of the pair
+        const int r = tid & 127;        // row in the block = TMEM lane
+        if (i < nh) {
+            const uint32_t lane_off = static_cast<uint32_t>((warp & 3) * 32) << 16;
+            const uint32_t tS = tmem + lane_off + i * 128, tO = tmem + lane_off + 256 + i * 128;
+            const int t = t0 + r;
+            const bool valid = (t < nn) && (t < p.T);
+            const int lim = valid ? prior + t : -1;
+            float m_ref = -INFINITY, l = 0.f;
+            for (int j = 0; j < nkt; ++j) {
+                if (!ptx::mbar_wait_bounded(bar(kBarS + i), j & 1, *abort_flag ? 0ull : kWaitNs)) {
+                    atomicExch(p.err, kDevTimeoutFull);
+                    *abort_flag = 1;
+                }
+                tc_fence_after();
+                const bool full_tile = (j * 128 + 127 <= full_below);
+                const int key0 = j * 128;
+                // pass 1: row max of the scaled, masked scores
+                float mx = -INFINITY;
+                uint32_t v[32];
+#pragma unroll
+                for (int c = 0; c < 4; ++c) {
+                    tmem_ld32(tS + c * 32, v);
+                    tmem_ld_wait();
+#pragma unroll
+                    for (int e = 0; e < 32; ++e) {
+                        float x = __uint_as_float(v[e]) * p.scale_log2;
+                        if (!full_tile && key0 + c * 32 + e > lim) x = -INFINITY;
+                        mx = fmaxf(mx, x);
+                    }
+                }
+                if (mx > m_ref + kRescaleThreshold || (m_ref == -INFINITY && mx != -INFINITY)) {
+                    // Move the reference max.  O_i holds the PV sums up to tile
+                    // j-1 (all with the old reference): wait for the last of them
+                    // and scale O_i and l by 2^(old - new).
+                    const float f = (m_ref == -INFINITY) ? 0.f : ptx::ex2(m_ref - mx);
+                    if (j > 0) {
+                        if (!ptx::mbar_wait_bounded(bar(kBarO + i), (j - 1) & 1, *abort_flag ? 0ull : kWaitNs)) {
+                            atomicExch(p.err, kDevTimeoutFull);
+                            *abort_flag = 1;
+                        }
+                        tc_fence_after();
+#pragma unroll
+                        for (int c = 0; c < 4; ++c) {
+                            tmem_ld32(tO + c * 32, v);
+                            tmem_ld_wait();
+#pragma unroll
+                            for (int e = 0; e < 32; ++e) v[e] = __float_as_uint(__uint_as_float(v[e]) * f);
+                            tmem_st32(tO + c * 32, v);
+                        }
+                        tmem_st_wait();
+                    }
+                    l *= f;
+                    m_ref = mx;
+                }
+                // pass 2: p = 2^(x - m_ref) as bf16 pairs into TMEM over S_i
+                const float mu = (m_ref == -INFINITY) ? 0.f : m_ref;
+                uint32_t pk[32];
+#pragma unroll
+                for (int c = 0; c < 4; ++c) {
+                    tmem_ld32(tS + c * 32, v);
+                    tmem_ld_wait();
+#pragma unroll
+                    for (int e = 0; e < 32; e += 2) {
+                        float x0 = __uint_as_float(v[e]) * p.scale_log2, x1 = __uint_as_float(v[e + 1]) * p.scale_log2;
+                        if (!full_tile) {
+                            if (key0 + c * 32 + e > lim) x0 = -INFINITY;
+                            if (key0 + c * 32 + e + 1 > lim) x1 = -INFINITY;
+                        }
+                        const float p0 = ptx::ex2(x0 - mu), p1 = ptx::ex2(x1 - mu);
+                        l += p0 + p1;
+                        pk[(c & 1) * 16 + (e >> 1)] = ptx::pack_bf16x2(p0, p1);
+                    }
+                    if (c & 1) tmem_st32(tS + (c >> 1) * 32, pk);
+                }
+                tmem_st_wait();
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) ptx::mbar_arrive(bar(kBarP + i));
+            }
+            // epilogue: O_i / l for valid rows
+            if (!ptx::mbar_wait_bounded(bar(kBarO + i), (nkt - 1) & 1, *abort_flag ? 0ull : kWaitNs)) {
+                atomicExch(p.err, kDevTimeoutFull);
+                *abort_flag = 1;
+            }
+            tc_fence_after();
+            const float inv = (valid && l > 0.f) ? 1.f / l : 0.f;
+            __nv_bfloat16* dst = static_cast<__nv_bfloat16*>(p.out) +
+                                 ((static_cast<size_t>(b) * p.Hq + h0 + i) * p.T + t) * kD;
+#pragma unroll
+            for (int c = 0; c < 4; ++c) {
+                uint32_t v[32];
+                tmem_ld32(tO + c * 32, v);
+                tmem_ld_wait();
+                if (valid) {
+#pragma unroll
+                    for (int e = 0; e < 32; e += 8) {
+                        uint4 w;
+                        w.x = ptx::pack_bf16x2(__uint_as_float(v[e]) * inv, __uint_as_float(v[e + 1]) * inv);
+                        w.y = ptx::pack_bf16x2(__uint_as_float(v[e + 2]) * inv, __uint_as_float(v[e + 3]) * inv);
+                        w.z = ptx::pack_bf16x2(__uint_as_float(v[e + 4]) * inv, __uint_as_float(v[e + 5]) * inv);
+                        w.w = ptx::pack_bf16x2(__uint_as_float(v[e + 6]) * inv, __uint_as_float(v[e + 7]) * inv);
+                        *reinterpret_cast<uint4*>(dst + c * 32 + e) = w;
+                    }
+                }
+            }
+        }
+    }
+
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 1) {
+        tc_fence_after();
+        asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, 512;" ::"r"(tmem) : "memory");
+    }
+}
+
+}  // namespace
+
+size_t prefill_smem_bytes() { return kSmemPF; }
+
+cudaError_t launch_prefill_tc(const PrefillParams& p, const CUtensorMap& tmQ, const CUtensorMap& tmK,
+                              const CUtensorMap& tmV, cudaStream_t stream) {
+    static bool attr_set = false;
+    if (!attr_set) {
+        cudaError_t e = cudaFuncSetAttribute(prefill_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                             static_cast<int>(kSmemPF));
+        if (e != cudaSuccess) return e;
+        attr_set = true;
+    }
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(p.n_items);
+    cfg.blockDim = dim3(kThreadsPF);
+    cfg.dynamicSmemBytes = kSmemPF;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    cudaError_t e = cudaLaunchKernelEx(&cfg, prefill_tc_kernel, p, tmQ, tmK, tmV);
+    if (e != cudaSuccess) return e;
+    return cudaGetLastError();
+}
+
+}  // namespace kvc
