@@ -293,6 +293,7 @@ kvc_status do_attention(kvc_cache* c, int layer, const void* q, const AttnPlan& 
         // Chunked prefill: tensor-core kernel, one CTA per (b, kvh, 128
         // positions, pair of heads), longest first.
         static_assert(sizeof(PrefillParams) < 32000, "kernel parameter block too large");
+        static_assert(sizeof(PrefillCombineParams) < 32000, "kernel parameter block too large");
         PrefillParams pp;
         pp.q = q;
         pp.out = out;
@@ -306,7 +307,15 @@ kvc_status do_attention(kvc_cache* c, int layer, const void* q, const AttnPlan& 
         pp.ntb = (pl.T + 127) / 128;
         pp.npair = (pl.G + 1) / 2;
         pp.scale_log2 = static_cast<float>(1.4426950408889634 / sqrt(static_cast<double>(c->d)));
-        std::vector<std::pair<int, int>> items;  // (cost, code)
+        // Items: (b, kvh, 128 positions, head pair) with cost = key tiles x
+        // heads.  An item costing more than one SM's share of the call is cut
+        // into key-range pieces (each leaves a partial for the combine kernel),
+        // so no SM is left with a long tail; pieces run longest first.
+        struct Piece {
+            int cost, code, lo, hi, slot;
+        };
+        std::vector<Piece> raw;
+        long long total_cost = 0;
         for (int b = 0; b < c->B; ++b) {
             pp.prior[b] = static_cast<int>(lens[b] - n_new[b]);
             pp.n_new[b] = n_new[b];
@@ -317,15 +326,49 @@ kvc_status do_attention(kvc_cache* c, int layer, const void* q, const AttnPlan& 
                     const int kmax = pp.prior[b] + std::min(t0 + 127, static_cast<int>(n_new[b]) - 1);
                     for (int pr = 0; pr < pp.npair; ++pr) {
                         const int code = ((b * c->Hkv + kvh) * pp.ntb + tb) * pp.npair + pr;
-                        items.push_back({(kmax / 128 + 1) * std::min(2, pl.G - 2 * pr), code});
+                        const int nkt = kmax / 128 + 1, nh = std::min(2, pl.G - 2 * pr);
+                        raw.push_back({nkt * nh, code, 0, nkt, kPrefillNoSlot});
+                        total_cost += static_cast<long long>(nkt) * nh;
                     }
                 }
         }
-        if (!items.empty() && static_cast<int>(items.size()) <= kMaxPrefillItems) {
-            std::stable_sort(items.begin(), items.end(),
-                             [](const std::pair<int, int>& a, const std::pair<int, int>& b2) { return a.first > b2.first; });
-            pp.n_items = static_cast<int>(items.size());
-            for (int i = 0; i < pp.n_items; ++i) pp.items[i] = items[i].second;
+        const size_t slot_bytes = static_cast<size_t>(2) * 128 * (kHeadDimBf16 + 4) * sizeof(float);
+        const int slot_room = static_cast<int>(std::min<size_t>(kMaxPrefillSlots, (ws_bytes - pl.ws_err) / slot_bytes));
+        const long long share = std::max(1ll, (total_cost + c->num_sms - 1) / c->num_sms);
+        std::vector<Piece> pieces;
+        PrefillCombineParams pc;
+        pc.n_groups = 0;
+        int slots_used = 0;
+        std::vector<int> order(raw.size());
+        for (size_t k = 0; k < raw.size(); ++k) order[k] = static_cast<int>(k);
+        std::stable_sort(order.begin(), order.end(), [&](int a, int b2) { return raw[a].cost > raw[b2].cost; });
+        for (int k : order) {
+            const Piece& it = raw[k];
+            const int nh = std::max(1, it.cost / it.hi);
+            int np = static_cast<int>(std::min<long long>(it.hi, (it.cost + share - 1) / share));
+            if (np > 1 && (slots_used + np > slot_room || pc.n_groups >= kMaxPrefillGroups)) np = 1;
+            if (np == 1) {
+                pieces.push_back(it);
+                continue;
+            }
+            pc.group_code[pc.n_groups] = it.code;
+            pc.group_slot0[pc.n_groups] = slots_used;
+            pc.group_pieces[pc.n_groups] = np;
+            ++pc.n_groups;
+            for (int q2 = 0; q2 < np; ++q2) {
+                const int lo = static_cast<int>(static_cast<long long>(q2) * it.hi / np);
+                const int hi = static_cast<int>(static_cast<long long>(q2 + 1) * it.hi / np);
+                pieces.push_back({(hi - lo) * nh, it.code, lo, hi, slots_used++});
+            }
+        }
+        if (!pieces.empty() && static_cast<int>(pieces.size()) <= kMaxPrefillItems) {
+            std::stable_sort(pieces.begin(), pieces.end(), [](const Piece& a, const Piece& b2) { return a.cost > b2.cost; });
+            pp.n_items = static_cast<int>(pieces.size());
+            for (int k = 0; k < pp.n_items; ++k) {
+                pp.items[k] = pieces[k].code;
+                pp.spans[k] = pieces[k].lo | (pieces[k].hi << 12) | (pieces[k].slot << 24);
+            }
+            pp.partials = reinterpret_cast<float*>(static_cast<uint8_t*>(ws) + pl.ws_err);
             CUtensorMap tmQ;
             if ((s = encode_rows_map(&tmQ, q, static_cast<cuuint64_t>(c->B) * pl.Hq * pl.T, 128))) return s;
             if (ws != c->last_ws) {
@@ -337,6 +380,20 @@ kvc_status do_attention(kvc_cache* c, int layer, const void* q, const AttnPlan& 
             if (e != cudaSuccess) return cuda_fail(e, "prefill attention launch");
             ++c->launches;
             if (main_enqueued) *main_enqueued = true;
+            if (pc.n_groups > 0) {
+                pc.partials = pp.partials;
+                pc.out = out;
+                pc.Hq = pl.Hq;
+                pc.Hkv = c->Hkv;
+                pc.G = pl.G;
+                pc.T = pl.T;
+                pc.ntb = pp.ntb;
+                pc.npair = pp.npair;
+                for (int b = 0; b < c->B; ++b) pc.n_new[b] = n_new[b];
+                e = launch_prefill_combine(pc, stream);
+                if (e != cudaSuccess) return cuda_fail(e, "prefill combine launch");
+                ++c->launches;
+            }
             return ok();
         }
         // otherwise (no rows to attend, or too many items): the split-KV path below

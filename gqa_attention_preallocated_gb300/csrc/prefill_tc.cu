@@ -46,7 +46,7 @@ namespace kvc {
 
 namespace {
 
-constexpr int kThreadsPF = 384;
+constexpr int kThreadsPF = 384;  // 4 warps (producer, MMA issuer, 2 idle) + 8 softmax warps
 constexpr int kD = 128;
 constexpr int kBoxBytes = 128 * 128;           // 128 rows x 64 columns x 2 B (one swizzled box)
 constexpr int kTile128 = 2 * kBoxBytes;         // 128 rows x 128 columns
@@ -61,7 +61,7 @@ constexpr int kOffBar = 6 * kTile128;
 // barrier indices
 constexpr int kBarQ = 0, kBarKFull = 1, kBarKEmpty = 3, kBarVFull = 5, kBarVEmpty = 7, kBarS = 9, kBarP = 11,
               kBarO = 13, kNumBars = 15;
-constexpr size_t kSmemPF = 1024 + kOffBar + kNumBars * 8 + 16;
+constexpr size_t kSmemPF = 1024 + kOffBar + 256;
 
 __device__ __forceinline__ uint64_t smem_desc(uint32_t addr, uint32_t lbo, uint32_t sbo) {
     // tcgen05 shared-memory matrix descriptor: start >> 4, leading / stride byte
@@ -112,6 +112,14 @@ __device__ __forceinline__ void tmem_ld32(uint32_t taddr, uint32_t (&r)[32]) {
         : "memory");
 }
 
+// 64 consecutive 32-bit TMEM columns of this thread's lane.
+__device__ __forceinline__ void tmem_ld64(uint32_t taddr, uint32_t (&r)[64]) {
+    asm volatile("tcgen05.ld.sync.aligned.32x32b.x64.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31,%32,%33,%34,%35,%36,%37,%38,%39,%40,%41,%42,%43,%44,%45,%46,%47,%48,%49,%50,%51,%52,%53,%54,%55,%56,%57,%58,%59,%60,%61,%62,%63}, [%64];"
+                 : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15]), "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]), "=r"(r[24]), "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31]), "=r"(r[32]), "=r"(r[33]), "=r"(r[34]), "=r"(r[35]), "=r"(r[36]), "=r"(r[37]), "=r"(r[38]), "=r"(r[39]), "=r"(r[40]), "=r"(r[41]), "=r"(r[42]), "=r"(r[43]), "=r"(r[44]), "=r"(r[45]), "=r"(r[46]), "=r"(r[47]), "=r"(r[48]), "=r"(r[49]), "=r"(r[50]), "=r"(r[51]), "=r"(r[52]), "=r"(r[53]), "=r"(r[54]), "=r"(r[55]), "=r"(r[56]), "=r"(r[57]), "=r"(r[58]), "=r"(r[59]), "=r"(r[60]), "=r"(r[61]), "=r"(r[62]), "=r"(r[63])
+                 : "r"(taddr)
+                 : "memory");
+}
+
 __device__ __forceinline__ void tmem_st32(uint32_t taddr, const uint32_t (&r)[32]) {
     asm volatile(
         "tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16,%17,%18,"
@@ -125,6 +133,31 @@ __device__ __forceinline__ void tmem_st32(uint32_t taddr, const uint32_t (&r)[32
 
 __device__ __forceinline__ void tmem_ld_wait() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
 __device__ __forceinline__ void tmem_st_wait() { asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory"); }
+
+// Packed fp32 pair arithmetic (two lanes per instruction) and a 3-input max.
+__device__ __forceinline__ uint64_t f2pack(float lo, float hi) {
+    uint64_t r;
+    asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(lo), "f"(hi));
+    return r;
+}
+__device__ __forceinline__ void f2unpack(uint64_t v, float& lo, float& hi) {
+    asm("mov.b64 {%0, %1}, %2;" : "=f"(lo), "=f"(hi) : "l"(v));
+}
+__device__ __forceinline__ uint64_t ffma2(uint64_t a, uint64_t b, uint64_t c) {
+    uint64_t d;
+    asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(d) : "l"(a), "l"(b), "l"(c));
+    return d;
+}
+__device__ __forceinline__ uint64_t fadd2(uint64_t a, uint64_t b) {
+    uint64_t d;
+    asm("add.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+    return d;
+}
+__device__ __forceinline__ float fmax3(float a, float b, float c) {
+    float d;
+    asm("max.f32 %0, %1, %2, %3;" : "=f"(d) : "f"(a), "f"(b), "f"(c));
+    return d;
+}
 
 struct Item {
     int b, kvh, tb, pair;
@@ -207,7 +240,11 @@ __global__ void __launch_bounds__(kThreadsPF, 1)
     const int h0 = kvh * p.G + 2 * item.pair;
     const int nh = min(2, p.G - 2 * item.pair);            // heads in this pair (1 or 2)
     const int kmax = prior + min(t0 + 127, nn - 1);         // last visible key of the block
-    const int nkt = kmax / 128 + 1;                         // key tiles
+    const int nkt_all = kmax / 128 + 1;                     // key tiles of the block
+    const int span = p.spans[blockIdx.x];
+    const int kt0 = span & 0xFFF;                           // this CTA's tiles: kt0 .. kt0 + nkt - 1
+    const int nkt = ((span >> 12) & 0xFFF) - kt0;
+    const int slot = (span >> 24) & 0xFF;                   // partial slot, or kPrefillNoSlot
     const int full_below = prior + t0;                      // keys <= this are visible to every row
     const int unit_row0 = (b * p.Hkv + kvh) * p.max_len;    // first cache row of (b, kvh)
 
@@ -222,7 +259,7 @@ __global__ void __launch_bounds__(kThreadsPF, 1)
             }
             for (int j = 0; j < nkt && !*abort_flag; ++j) {
                 const int s = j & 1;
-                const int row = unit_row0 + j * 128;
+                const int row = unit_row0 + (kt0 + j) * 128;
                 if (j >= 2 && !ptx::mbar_wait_bounded(bar(kBarKEmpty + s), ((j >> 1) & 1) ^ 1, kWaitNs)) {
                     atomicExch(p.err, kDevTimeoutEmpty);
                     *abort_flag = 1;
@@ -254,6 +291,7 @@ __global__ void __launch_bounds__(kThreadsPF, 1)
         };
         auto issue_s = [&](int i, int j) {  // S_i = Q_i K_j^T
             const uint32_t qa = sbase + kOffQ + i * kTile128, ka = sbase + kOffK + (j & 1) * kTile128;
+#pragma unroll
             for (int k = 0; k < 8; ++k) {
                 const uint32_t off = (k >> 2) * kBoxBytes + (k & 3) * 32;
                 mma_ss(tmem + i * 128, smem_desc(qa + off, 16, 1024), smem_desc(ka + off, 16, 1024), id_qk, k > 0);
@@ -262,6 +300,7 @@ __global__ void __launch_bounds__(kThreadsPF, 1)
         };
         auto issue_pv = [&](int i, int j) {  // O_i += P_i V_j (P_i in TMEM over S_i)
             const uint32_t va = sbase + kOffV + (j & 1) * kTile128;
+#pragma unroll
             for (int k = 0; k < 8; ++k)
                 mma_ts(tmem + 256 + i * 128, tmem + i * 128 + k * 8, smem_desc(va + k * 2048, kBoxBytes, 1024), id_pv,
                        (j > 0 || k > 0) ? 1u : 0u);
@@ -281,9 +320,10 @@ __global__ void __launch_bounds__(kThreadsPF, 1)
             // before the PV MMAs read the stage.
             if (lane == 0) wait(kBarVFull + s, (j >> 1) & 1);
             __syncwarp();
-            if (j == nkt - 1) {
-                const int vr0 = kmax - j * 128 + 1;  // first row to clear, 1..128
+            if (kt0 + j == nkt_all - 1) {
+                const int vr0 = kmax - (kt0 + j) * 128 + 1;  // first row to clear, 1..128
                 uint8_t* vb = smem + kOffV + s * kTile128;
+#pragma unroll 1
                 for (int idx = lane; idx < 2 * (128 - vr0) * 8; idx += 32) {
                     const int per = (128 - vr0) * 8;
                     const int hf = idx / per, rem = idx - hf * per;
@@ -332,22 +372,27 @@ __global__ void __launch_bounds__(kThreadsPF, 1)
                     *abort_flag = 1;
                 }
                 tc_fence_after();
-                const bool full_tile = (j * 128 + 127 <= full_below);
-                const int key0 = j * 128;
-                // pass 1: row max of the scaled, masked scores
+                const bool full_tile = ((kt0 + j) * 128 + 127 <= full_below);
+                const int key0 = (kt0 + j) * 128;
+                // pass 1: row max of the raw scores (scale > 0, so it scales after);
+                // 64 columns per TMEM load, one wait each
                 float mx = -INFINITY;
-                uint32_t v[32];
+                uint32_t v[64];
 #pragma unroll
-                for (int c = 0; c < 4; ++c) {
-                    tmem_ld32(tS + c * 32, v);
+                for (int c = 0; c < 2; ++c) {
+                    tmem_ld64(tS + c * 64, v);
                     tmem_ld_wait();
+                    if (full_tile) {
 #pragma unroll
-                    for (int e = 0; e < 32; ++e) {
-                        float x = __uint_as_float(v[e]) * p.scale_log2;
-                        if (!full_tile && key0 + c * 32 + e > lim) x = -INFINITY;
-                        mx = fmaxf(mx, x);
+                        for (int e = 0; e < 64; e += 2) mx = fmax3(mx, __uint_as_float(v[e]), __uint_as_float(v[e + 1]));
+                    } else {
+                        const int kl = lim - key0 - c * 64;  // elements e <= kl are visible
+#pragma unroll
+                        for (int e = 0; e < 64; ++e)
+                            if (e <= kl) mx = fmaxf(mx, __uint_as_float(v[e]));
                     }
                 }
+                mx = (mx == -INFINITY) ? -INFINITY : mx * p.scale_log2;
                 if (mx > m_ref + kRescaleThreshold || (m_ref == -INFINITY && mx != -INFINITY)) {
                     // Move the reference max.  O_i holds the PV sums up to tile
                     // j-1 (all with the old reference): wait for the last of them
@@ -360,37 +405,51 @@ __global__ void __launch_bounds__(kThreadsPF, 1)
                         }
                         tc_fence_after();
 #pragma unroll
-                        for (int c = 0; c < 4; ++c) {
-                            tmem_ld32(tO + c * 32, v);
+                        for (int c = 0; c < 2; ++c) {
+                            tmem_ld64(tO + c * 64, v);
                             tmem_ld_wait();
+                            uint32_t w[32];
 #pragma unroll
-                            for (int e = 0; e < 32; ++e) v[e] = __float_as_uint(__uint_as_float(v[e]) * f);
-                            tmem_st32(tO + c * 32, v);
+                            for (int h = 0; h < 2; ++h) {
+#pragma unroll
+                                for (int e = 0; e < 32; ++e) w[e] = __float_as_uint(__uint_as_float(v[h * 32 + e]) * f);
+                                tmem_st32(tO + c * 64 + h * 32, w);
+                            }
                         }
                         tmem_st_wait();
                     }
                     l *= f;
                     m_ref = mx;
                 }
-                // pass 2: p = 2^(x - m_ref) as bf16 pairs into TMEM over S_i
+                // pass 2: p = 2^(s * scale - m_ref) as bf16 pairs into TMEM over S_i
                 const float mu = (m_ref == -INFINITY) ? 0.f : m_ref;
+                const uint64_t sc2 = f2pack(p.scale_log2, p.scale_log2), nmu2 = f2pack(-mu, -mu);
+                uint64_t sum2 = f2pack(0.f, 0.f);
                 uint32_t pk[32];
 #pragma unroll
-                for (int c = 0; c < 4; ++c) {
-                    tmem_ld32(tS + c * 32, v);
+                for (int c = 0; c < 2; ++c) {
+                    tmem_ld64(tS + c * 64, v);
                     tmem_ld_wait();
+                    const int kl = full_tile ? 1 << 30 : lim - key0 - c * 64;
 #pragma unroll
-                    for (int e = 0; e < 32; e += 2) {
-                        float x0 = __uint_as_float(v[e]) * p.scale_log2, x1 = __uint_as_float(v[e + 1]) * p.scale_log2;
+                    for (int e = 0; e < 64; e += 2) {
+                        float x0, x1;
+                        f2unpack(ffma2(f2pack(__uint_as_float(v[e]), __uint_as_float(v[e + 1])), sc2, nmu2), x0, x1);
+                        float p0 = ptx::ex2(x0), p1 = ptx::ex2(x1);
                         if (!full_tile) {
-                            if (key0 + c * 32 + e > lim) x0 = -INFINITY;
-                            if (key0 + c * 32 + e + 1 > lim) x1 = -INFINITY;
+                            if (e > kl) p0 = 0.f;
+                            if (e + 1 > kl) p1 = 0.f;
                         }
-                        const float p0 = ptx::ex2(x0 - mu), p1 = ptx::ex2(x1 - mu);
-                        l += p0 + p1;
-                        pk[(c & 1) * 16 + (e >> 1)] = ptx::pack_bf16x2(p0, p1);
+                        sum2 = fadd2(sum2, f2pack(p0, p1));
+                        pk[e >> 1] = ptx::pack_bf16x2(p0, p1);
                     }
-                    if (c & 1) tmem_st32(tS + (c >> 1) * 32, pk);
+                    // keys c*64 .. c*64+63 -> P columns c*32 .. c*32+31 (S columns already read)
+                    tmem_st32(tS + c * 32, pk);
+                }
+                {
+                    float s0, s1;
+                    f2unpack(sum2, s0, s1);
+                    l += s0 + s1;
                 }
                 tmem_st_wait();
                 tc_fence_before();
@@ -403,25 +462,45 @@ __global__ void __launch_bounds__(kThreadsPF, 1)
                 *abort_flag = 1;
             }
             tc_fence_after();
+            if (slot != kPrefillNoSlot) {
+                // A piece of a key-split block: leave (O, m, l) for the combine kernel.
+                float* part = p.partials + ((static_cast<size_t>(slot) * 2 + i) * 128 + r) * (kD + 4);
+#pragma unroll
+                for (int c = 0; c < 4; ++c) {
+                    uint32_t w[32];
+                    tmem_ld32(tO + c * 32, w);
+                    tmem_ld_wait();
+                    if (valid) {
+#pragma unroll
+                        for (int e = 0; e < 32; e += 4)
+                            *reinterpret_cast<uint4*>(part + c * 32 + e) = make_uint4(w[e], w[e + 1], w[e + 2], w[e + 3]);
+                    }
+                }
+                if (valid) {
+                    part[kD] = m_ref;
+                    part[kD + 1] = l;
+                }
+            } else {
             const float inv = (valid && l > 0.f) ? 1.f / l : 0.f;
             __nv_bfloat16* dst = static_cast<__nv_bfloat16*>(p.out) +
                                  ((static_cast<size_t>(b) * p.Hq + h0 + i) * p.T + t) * kD;
 #pragma unroll
             for (int c = 0; c < 4; ++c) {
-                uint32_t v[32];
-                tmem_ld32(tO + c * 32, v);
+                uint32_t w[32];
+                tmem_ld32(tO + c * 32, w);
                 tmem_ld_wait();
                 if (valid) {
 #pragma unroll
                     for (int e = 0; e < 32; e += 8) {
-                        uint4 w;
-                        w.x = ptx::pack_bf16x2(__uint_as_float(v[e]) * inv, __uint_as_float(v[e + 1]) * inv);
-                        w.y = ptx::pack_bf16x2(__uint_as_float(v[e + 2]) * inv, __uint_as_float(v[e + 3]) * inv);
-                        w.z = ptx::pack_bf16x2(__uint_as_float(v[e + 4]) * inv, __uint_as_float(v[e + 5]) * inv);
-                        w.w = ptx::pack_bf16x2(__uint_as_float(v[e + 6]) * inv, __uint_as_float(v[e + 7]) * inv);
-                        *reinterpret_cast<uint4*>(dst + c * 32 + e) = w;
+                        uint4 q4;
+                        q4.x = ptx::pack_bf16x2(__uint_as_float(w[e]) * inv, __uint_as_float(w[e + 1]) * inv);
+                        q4.y = ptx::pack_bf16x2(__uint_as_float(w[e + 2]) * inv, __uint_as_float(w[e + 3]) * inv);
+                        q4.z = ptx::pack_bf16x2(__uint_as_float(w[e + 4]) * inv, __uint_as_float(w[e + 5]) * inv);
+                        q4.w = ptx::pack_bf16x2(__uint_as_float(w[e + 6]) * inv, __uint_as_float(w[e + 7]) * inv);
+                        *reinterpret_cast<uint4*>(dst + c * 32 + e) = q4;
                     }
                 }
+            }
             }
         }
     }
@@ -434,9 +513,66 @@ __global__ void __launch_bounds__(kThreadsPF, 1)
     }
 }
 
+// Merge the key-split pieces of a (b, kvh, 128 positions, head pair) group:
+// o = sum_k 2^(m_k - M) O_k / sum_k 2^(m_k - M) l_k, M = max_k m_k, per row.
+__global__ void __launch_bounds__(256) prefill_combine_kernel(const __grid_constant__ PrefillCombineParams p) {
+    ptx::grid_dependency_wait();
+    ptx::launch_dependents();
+    int code = p.group_code[blockIdx.x];
+    const int pair = code % p.npair;
+    code /= p.npair;
+    const int tb = code % p.ntb;
+    code /= p.ntb;
+    const int kvh = code % p.Hkv, b = code / p.Hkv;
+    const int h0 = kvh * p.G + 2 * pair, nh = min(2, p.G - 2 * pair);
+    const int slot0 = p.group_slot0[blockIdx.x], np = p.group_pieces[blockIdx.x];
+    for (int idx = threadIdx.x; idx < nh * 128 * (kD / 4); idx += blockDim.x) {
+        const int c4 = idx & 31, r = (idx >> 5) & 127, i = idx >> 12;
+        const int t = tb * 128 + r;
+        if (t >= p.n_new[b] || t >= p.T) continue;
+        float m = -INFINITY, l = 0.f;
+        float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+        for (int k = 0; k < np; ++k) {
+            const float* part = p.partials + ((static_cast<size_t>(slot0 + k) * 2 + i) * 128 + r) * (kD + 4);
+            const float mk = part[kD];
+            const float mn = fmaxf(m, mk);
+            if (mn == -INFINITY) continue;
+            const float a = ptx::ex2(m - mn), c = ptx::ex2(mk - mn);
+            const float4 o = reinterpret_cast<const float4*>(part)[c4];
+            l = l * a + part[kD + 1] * c;
+            acc.x = acc.x * a + o.x * c;
+            acc.y = acc.y * a + o.y * c;
+            acc.z = acc.z * a + o.z * c;
+            acc.w = acc.w * a + o.w * c;
+            m = mn;
+        }
+        const float inv = l > 0.f ? 1.f / l : 0.f;
+        uint2 w;
+        w.x = ptx::pack_bf16x2(acc.x * inv, acc.y * inv);
+        w.y = ptx::pack_bf16x2(acc.z * inv, acc.w * inv);
+        *reinterpret_cast<uint2*>(static_cast<__nv_bfloat16*>(p.out) +
+                                  ((static_cast<size_t>(b) * p.Hq + h0 + i) * p.T + t) * kD + c4 * 4) = w;
+    }
+}
+
 }  // namespace
 
 size_t prefill_smem_bytes() { return kSmemPF; }
+
+cudaError_t launch_prefill_combine(const PrefillCombineParams& p, cudaStream_t stream) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(p.n_groups);
+    cfg.blockDim = dim3(256);
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    cudaError_t e = cudaLaunchKernelEx(&cfg, prefill_combine_kernel, p);
+    if (e != cudaSuccess) return e;
+    return cudaGetLastError();
+}
 
 cudaError_t launch_prefill_tc(const PrefillParams& p, const CUtensorMap& tmQ, const CUtensorMap& tmK,
                               const CUtensorMap& tmV, cudaStream_t stream) {

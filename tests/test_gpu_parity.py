@@ -345,3 +345,11 @@ def test_prefill_chunk_sampled(ragged):
     nn = wl.ragged_chunk(0, s.B) if ragged else np.full(s.B, T, dtype=np.int64)
     units = [(int(np.argmax(priors)), 3), (int(np.argmin(priors)), 0)]
     _decode_case(s, s.Hq, priors, [T], [nn], 3, units)
+
+
+@pytest.mark.parametrize("B,Hkv,G,prior,T", [(1, 2, 4, 3000, 256), (2, 1, 2, 700, 200), (1, 1, 3, 2500, 130)])
+def test_prefill_key_split_pieces(B, Hkv, G, prior, T):
+    """Few long items on many SMs: the prefill work is cut into key-range pieces
+    merged by the combine kernel (odd G also leaves a pair with one head)."""
+    calls = [np.full(B, prior), np.full(B, T)]
+    _run_calls(13, B, Hkv, G, 128, prior + T + 5, torch.bfloat16, calls)
