@@ -18,6 +18,7 @@
 
 #include <algorithm>
 #include <mutex>
+#include <queue>
 #include <string>
 #include <vector>
 
@@ -188,15 +189,22 @@ kvc_status plan_shape(const kvc_cache* c, int Hq, int T, int num_ctas, AttnPlan*
             return fail(KVC_ERR_ARG, "B * ceil(G*T / %d) = %lld exceeds %d row blocks", pl->RPB, NB, kMaxGroups);
         pl->NB = static_cast<int>(NB);
         pl->units = pl->NB * c->Hkv;
-        // Layout: the error word (256 B), then the partials of the units that
-        // straddle CTAs.  Nothing in it needs to start at zero but the error
-        // word.
-        pl->ws_err = 256;
+        // Layout: the header (error word, merge counters), then the partials of
+        // the units that straddle CTAs.  Only the header needs to start at
+        // zero; the merge counters return to zero after each use.
+        pl->ws_err = kWsHeaderBytes;
         pl->ws_counters = 0;
         pl->ways = decode_launch_shape(pl->mt).ways;
         pl->part_rows = std::min(pl->R, pl->RPB);
         pl->ws_partials = static_cast<size_t>(pl->units + num_ctas) * pl->ways * pl->part_rows *
                           (kHeadDimBf16 + 4) * sizeof(float);
+        if (pl->R > 64) {
+            // The chunked-prefill kernel: up to two partial slots (2 heads x
+            // 128 rows x (d + 4) floats) per SM share boundary.
+            const size_t prefill = static_cast<size_t>(2) * std::min(num_ctas, kMaxCtas) * 2 * 128 *
+                                   (kHeadDimBf16 + 4) * sizeof(float);
+            pl->ws_partials = std::max(pl->ws_partials, prefill);
+        }
         pl->ws_total = pl->ws_err + pl->ws_counters + pl->ws_partials;
     }
     return ok();
@@ -289,15 +297,28 @@ kvc_status do_attention(kvc_cache* c, int layer, const void* q, const AttnPlan& 
 
     kvc_status s = encode_layer_maps(c, layer);
     if (s) return s;
-    if (pl.R > 64 && k_new == nullptr) {
-        // Chunked prefill: tensor-core kernel, one CTA per (b, kvh, 128
-        // positions, pair of heads), longest first.
+    if (pl.R > 64 && k_new == nullptr && c->max_len <= 0xFFFF * 128) {
+        // Chunked prefill: tensor-core kernel, one CTA per piece.  Work items
+        // are (b, kvh, 128 positions, head pair); an item's key tiles cost its
+        // head count each, plus a fixed start-up cost per CTA.  The launch order
+        // comes from a longest-first list schedule simulated on the SMs (the
+        // block scheduler hands the next CTA to the first SM that frees up):
+        // an item that would run past the SMs' common finishing time is cut
+        // there, and the rest of it is scheduled like any other item.  The
+        // pieces of a cut item leave partials that its last piece merges.
+        // Items of equal length (the 128-position blocks and head pairs that
+        // read the same K/V) stay side by side, so their K/V tiles are read
+        // from HBM about once and then hit in L2.
         static_assert(sizeof(PrefillParams) < 32000, "kernel parameter block too large");
-        static_assert(sizeof(PrefillCombineParams) < 32000, "kernel parameter block too large");
+        struct WorkItem {
+            int code, nkt, nh;
+        };
+        std::vector<WorkItem> items;
         PrefillParams pp;
         pp.q = q;
         pp.out = out;
         pp.err = static_cast<int*>(ws);
+        pp.partials = reinterpret_cast<float*>(static_cast<uint8_t*>(ws) + pl.ws_err);
         pp.B = c->B;
         pp.Hq = pl.Hq;
         pp.Hkv = c->Hkv;
@@ -307,15 +328,6 @@ kvc_status do_attention(kvc_cache* c, int layer, const void* q, const AttnPlan& 
         pp.ntb = (pl.T + 127) / 128;
         pp.npair = (pl.G + 1) / 2;
         pp.scale_log2 = static_cast<float>(1.4426950408889634 / sqrt(static_cast<double>(c->d)));
-        // Items: (b, kvh, 128 positions, head pair) with cost = key tiles x
-        // heads.  An item costing more than one SM's share of the call is cut
-        // into key-range pieces (each leaves a partial for the combine kernel),
-        // so no SM is left with a long tail; pieces run longest first.
-        struct Piece {
-            int cost, code, lo, hi, slot;
-        };
-        std::vector<Piece> raw;
-        long long total_cost = 0;
         for (int b = 0; b < c->B; ++b) {
             pp.prior[b] = static_cast<int>(lens[b] - n_new[b]);
             pp.n_new[b] = n_new[b];
@@ -326,49 +338,18 @@ kvc_status do_attention(kvc_cache* c, int layer, const void* q, const AttnPlan& 
                     const int kmax = pp.prior[b] + std::min(t0 + 127, static_cast<int>(n_new[b]) - 1);
                     for (int pr = 0; pr < pp.npair; ++pr) {
                         const int code = ((b * c->Hkv + kvh) * pp.ntb + tb) * pp.npair + pr;
-                        const int nkt = kmax / 128 + 1, nh = std::min(2, pl.G - 2 * pr);
-                        raw.push_back({nkt * nh, code, 0, nkt, kPrefillNoSlot});
-                        total_cost += static_cast<long long>(nkt) * nh;
+                        items.push_back({code, kmax / 128 + 1, std::min(2, pl.G - 2 * pr)});
                     }
                 }
         }
         const size_t slot_bytes = static_cast<size_t>(2) * 128 * (kHeadDimBf16 + 4) * sizeof(float);
-        const int slot_room = static_cast<int>(std::min<size_t>(kMaxPrefillSlots, (ws_bytes - pl.ws_err) / slot_bytes));
-        const long long share = std::max(1ll, (total_cost + c->num_sms - 1) / c->num_sms);
-        std::vector<Piece> pieces;
-        PrefillCombineParams pc;
-        pc.n_groups = 0;
-        int slots_used = 0;
-        std::vector<int> order(raw.size());
-        for (size_t k = 0; k < raw.size(); ++k) order[k] = static_cast<int>(k);
-        std::stable_sort(order.begin(), order.end(), [&](int a, int b2) { return raw[a].cost > raw[b2].cost; });
-        for (int k : order) {
-            const Piece& it = raw[k];
-            const int nh = std::max(1, it.cost / it.hi);
-            int np = static_cast<int>(std::min<long long>(it.hi, (it.cost + share - 1) / share));
-            if (np > 1 && (slots_used + np > slot_room || pc.n_groups >= kMaxPrefillGroups)) np = 1;
-            if (np == 1) {
-                pieces.push_back(it);
-                continue;
-            }
-            pc.group_code[pc.n_groups] = it.code;
-            pc.group_slot0[pc.n_groups] = slots_used;
-            pc.group_pieces[pc.n_groups] = np;
-            ++pc.n_groups;
-            for (int q2 = 0; q2 < np; ++q2) {
-                const int lo = static_cast<int>(static_cast<long long>(q2) * it.hi / np);
-                const int hi = static_cast<int>(static_cast<long long>(q2 + 1) * it.hi / np);
-                pieces.push_back({(hi - lo) * nh, it.code, lo, hi, slots_used++});
-            }
-        }
-        if (!pieces.empty() && static_cast<int>(pieces.size()) <= kMaxPrefillItems) {
-            std::stable_sort(pieces.begin(), pieces.end(), [](const Piece& a, const Piece& b2) { return a.cost > b2.cost; });
-            pp.n_items = static_cast<int>(pieces.size());
-            for (int k = 0; k < pp.n_items; ++k) {
-                pp.items[k] = pieces[k].code;
-                pp.spans[k] = pieces[k].lo | (pieces[k].hi << 12) | (pieces[k].slot << 24);
-            }
-            pp.partials = reinterpret_cast<float*>(static_cast<uint8_t*>(ws) + pl.ws_err);
+        const long long slot_room =
+            std::min<long long>(kMaxPrefillSlots, static_cast<long long>((ws_bytes - pl.ws_err) / slot_bytes));
+        const int nsm = std::max(1, c->num_sms);
+        // Items per launch, leaving room for the pieces that cuts add.
+        const size_t chunk = static_cast<size_t>(kMaxPrefillPieces - std::min(nsm, kMaxPrefillPieces / 4));
+        bool launched = false;
+        if (!items.empty()) {
             CUtensorMap tmQ;
             if ((s = encode_rows_map(&tmQ, q, static_cast<cuuint64_t>(c->B) * pl.Hq * pl.T, 128))) return s;
             if (ws != c->last_ws) {
@@ -376,27 +357,89 @@ kvc_status do_attention(kvc_cache* c, int layer, const void* q, const AttnPlan& 
                 if (e != cudaSuccess) return cuda_fail(e, "cudaMemsetAsync(workspace)");
                 c->last_ws = ws;
             }
-            cudaError_t e = launch_prefill_tc(pp, tmQ, c->tmK128[layer], c->tmV128[layer], stream);
-            if (e != cudaSuccess) return cuda_fail(e, "prefill attention launch");
-            ++c->launches;
-            if (main_enqueued) *main_enqueued = true;
-            if (pc.n_groups > 0) {
-                pc.partials = pp.partials;
-                pc.out = out;
-                pc.Hq = pl.Hq;
-                pc.Hkv = c->Hkv;
-                pc.G = pl.G;
-                pc.T = pl.T;
-                pc.ntb = pp.ntb;
-                pc.npair = pp.npair;
-                for (int b = 0; b < c->B; ++b) pc.n_new[b] = n_new[b];
-                e = launch_prefill_combine(pc, stream);
-                if (e != cudaSuccess) return cuda_fail(e, "prefill combine launch");
+            for (size_t i0 = 0; i0 < items.size(); i0 += chunk) {
+                const size_t i1 = std::min(items.size(), i0 + chunk);
+                const int n_items = static_cast<int>(i1 - i0);
+                constexpr long long kStartCost = 5;  // per-CTA start-up, in tile x head units
+                constexpr int kMinPieceTiles = 4;
+                long long W = 0;
+                for (size_t k = i0; k < i1; ++k) W += static_cast<long long>(items[k].nkt) * items[k].nh + kStartCost;
+                const long long target = W / nsm + kStartCost;  // the SMs' common finishing time
+                // Remaining parts of items, longest first (ties: item order).
+                struct Part {
+                    long long cost;
+                    int item, lo;
+                    bool operator<(const Part& o) const { return cost != o.cost ? cost < o.cost : item > o.item; }
+                };
+                std::priority_queue<Part> parts;
+                for (int k = 0; k < n_items; ++k) {
+                    const WorkItem& it = items[i0 + k];
+                    parts.push({static_cast<long long>(it.nkt) * it.nh, k, 0});
+                }
+                using Sm = std::pair<long long, int>;  // (busy until, SM)
+                std::priority_queue<Sm, std::vector<Sm>, std::greater<Sm>> sms;
+                for (int m = 0; m < nsm; ++m) sms.push({0, m});
+                struct Placed {
+                    long long start;
+                    int seq, item, lo, hi;
+                };
+                std::vector<Placed> placed;
+                int cuts = 0;
+                while (!parts.empty()) {
+                    const Part pt = parts.top();
+                    parts.pop();
+                    const WorkItem& it = items[i0 + pt.item];
+                    const Sm sm = sms.top();
+                    sms.pop();
+                    int hi = it.nkt;
+                    const long long room = target - sm.first - kStartCost;  // work that fits before the target
+                    const int fit = static_cast<int>(std::max(0ll, room) / it.nh);
+                    const bool can_cut = n_items + cuts + 1 <= kMaxPrefillPieces && 2ll * (cuts + 1) <= slot_room;
+                    if (pt.cost + kStartCost > target - sm.first && can_cut && fit >= kMinPieceTiles &&
+                        it.nkt - (pt.lo + fit) >= kMinPieceTiles) {
+                        hi = pt.lo + fit;
+                        ++cuts;
+                        parts.push({static_cast<long long>(it.nkt - hi) * it.nh, pt.item, hi});
+                    }
+                    placed.push_back({sm.first, static_cast<int>(placed.size()), pt.item, pt.lo, hi});
+                    sms.push({sm.first + kStartCost + static_cast<long long>(hi - pt.lo) * it.nh, sm.second});
+                }
+                std::sort(placed.begin(), placed.end(), [](const Placed& x, const Placed& y) {
+                    return x.start != y.start ? x.start < y.start : x.seq < y.seq;
+                });
+                // Slots: the pieces of a cut item take consecutive slots.
+                std::vector<int> npieces(n_items, 0), slot0(n_items, -1), seen(n_items, 0);
+                for (const Placed& pc : placed) ++npieces[pc.item];
+                int slots = 0;
+                for (int k = 0; k < n_items; ++k)
+                    if (npieces[k] > 1) {
+                        slot0[k] = slots;
+                        slots += npieces[k];
+                    }
+                pp.n_pieces = static_cast<int>(placed.size());
+                for (int q2 = 0; q2 < pp.n_pieces; ++q2) {
+                    const Placed& pc = placed[q2];
+                    const WorkItem& it = items[i0 + pc.item];
+                    pp.piece_code[q2] = static_cast<uint32_t>(it.code);
+                    pp.piece_tiles[q2] = static_cast<uint32_t>(pc.lo) | (static_cast<uint32_t>(pc.hi) << 16);
+                    if (npieces[pc.item] > 1) {
+                        const int kidx = seen[pc.item]++;
+                        pp.piece_aux[q2] = static_cast<uint32_t>(slot0[pc.item] + kidx) |
+                                           (static_cast<uint32_t>(kidx) << 12) |
+                                           (static_cast<uint32_t>(npieces[pc.item]) << 22);
+                    } else {
+                        pp.piece_aux[q2] = static_cast<uint32_t>(kPrefillNoSlot);
+                    }
+                }
+                cudaError_t e = launch_prefill_tc(pp, tmQ, c->tmK128[layer], c->tmV128[layer], stream);
+                if (e != cudaSuccess) return cuda_fail(e, "prefill attention launch");
                 ++c->launches;
+                launched = true;
+                if (main_enqueued) *main_enqueued = true;
             }
-            return ok();
         }
-        // otherwise (no rows to attend, or too many items): the split-KV path below
+        if (launched) return ok();
+        // otherwise (no rows to attend, or no room for the partials): the split-KV path below
     }
 
     // bf16 split-KV path

@@ -132,39 +132,30 @@ cudaError_t launch_attn_f32(const F32Params& p, cudaStream_t stream);
 // heads); items are packed as ((b * Hkv + kvh) * ntb + tb) * npair + pair and
 // listed longest first.
 // ---------------------------------------------------------------------------
-constexpr int kMaxPrefillItems = 2048;
-constexpr int kPrefillNoSlot = 255;     // span slot meaning "whole key range: write out directly"
-constexpr int kMaxPrefillSlots = 255;   // key-split pieces per call (each has a partial slot)
+constexpr int kMaxPrefillPieces = 1920;
+constexpr int kPrefillNoSlot = 0xFFF;   // piece covers all keys of its block: write out directly
+constexpr int kMaxPrefillSlots = 4095;  // key-split pieces per launch (each has a partial slot)
+// Workspace header: the error word, then one merge counter per (first slot of
+// a split block, head); the partials follow the header.
+constexpr size_t kWsCounterOffset = 256;
+constexpr size_t kWsHeaderBytes = kWsCounterOffset + static_cast<size_t>(kMaxPrefillSlots + 1) * 2 * sizeof(int);
 struct PrefillParams {
     const void* q;
     void* out;
-    int* err;
+    int* err;         // workspace start: error word, merge counters
     float* partials;  // [slot][2 heads][128 rows][d + 4]: O (d), m, l, pad
     int B, Hq, Hkv, G, T, max_len;
-    int ntb, npair, n_items;
+    int ntb, npair, n_pieces;
     float scale_log2;
     int prior[kMaxBatch];
     int n_new[kMaxBatch];
-    int items[kMaxPrefillItems];  // packed (b, kvh, tb, pair)
-    // key-tile range of each item and its partial slot: lo | hi << 12 | slot << 24
-    // (tiles of 128 keys; slot = kPrefillNoSlot when the item covers all of its keys)
-    int spans[kMaxPrefillItems];
+    // One CTA per piece, in launch order.
+    uint32_t piece_code[kMaxPrefillPieces];   // packed (b, kvh, tb, pair)
+    uint32_t piece_tiles[kMaxPrefillPieces];  // key tiles lo | hi << 16 (tiles of 128 keys)
+    // slot | index of the piece within its block << 12 | pieces of the block << 22
+    // (slot = kPrefillNoSlot when the piece covers all keys of its block)
+    uint32_t piece_aux[kMaxPrefillPieces];
 };
-
-// Merge of the key-split pieces of one (b, kvh, 128 positions, head pair):
-// one CTA per group, pieces in consecutive partial slots.
-constexpr int kMaxPrefillGroups = 255;
-struct PrefillCombineParams {
-    const float* partials;
-    void* out;
-    int Hq, Hkv, G, T, ntb, npair, n_groups;
-    int n_new[kMaxBatch];
-    int group_code[kMaxPrefillGroups];
-    int group_slot0[kMaxPrefillGroups];
-    int group_pieces[kMaxPrefillGroups];
-};
-
-cudaError_t launch_prefill_combine(const PrefillCombineParams& p, cudaStream_t stream);
 
 size_t prefill_smem_bytes();
 cudaError_t launch_prefill_tc(const PrefillParams& p, const CUtensorMap& tmQ, const CUtensorMap& tmK,

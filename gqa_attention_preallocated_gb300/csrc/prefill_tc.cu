@@ -159,19 +159,126 @@ __device__ __forceinline__ float fmax3(float a, float b, float c) {
     return d;
 }
 
-struct Item {
-    int b, kvh, tb, pair;
+// One piece: a key-tile range of one work item (b, KV head, 128 query
+// positions, head pair).
+struct Piece {
+    int b, kvh, t0, h0, nh;      // row, KV head, first position, first head, heads (1 or 2)
+    int prior, nn;               // prior length and new tokens of row b
+    int kmax, nkt_all;           // last visible key of the block, its key tiles
+    int kt0, nkt;                // this piece's tiles: kt0 .. kt0 + nkt - 1
+    int slot;                    // partial slot, or kPrefillNoSlot
+    int kidx, npc;               // index of the piece within its block, pieces of the block
 };
 
-__device__ __forceinline__ Item decode_item(const PrefillParams& p, int code) {
-    Item it;
-    it.pair = code % p.npair;
+__device__ __forceinline__ Piece decode_piece(const PrefillParams& p, int idx) {
+    Piece pc;
+    int code = static_cast<int>(p.piece_code[idx]);
+    const int pair = code % p.npair;
     code /= p.npair;
-    it.tb = code % p.ntb;
+    const int tb = code % p.ntb;
     code /= p.ntb;
-    it.kvh = code % p.Hkv;
-    it.b = code / p.Hkv;
-    return it;
+    pc.kvh = code % p.Hkv;
+    pc.b = code / p.Hkv;
+    pc.t0 = tb * 128;
+    pc.h0 = pc.kvh * p.G + 2 * pair;
+    pc.nh = min(2, p.G - 2 * pair);
+    pc.prior = p.prior[pc.b];
+    pc.nn = p.n_new[pc.b];
+    pc.kmax = pc.prior + min(pc.t0 + 127, pc.nn - 1);
+    pc.nkt_all = pc.kmax / 128 + 1;
+    const uint32_t tiles = p.piece_tiles[idx];
+    pc.kt0 = static_cast<int>(tiles & 0xFFFF);
+    pc.nkt = static_cast<int>(tiles >> 16) - pc.kt0;
+    const uint32_t aux = p.piece_aux[idx];
+    pc.slot = static_cast<int>(aux & 0xFFF);
+    pc.kidx = static_cast<int>((aux >> 12) & 0x3FF);
+    pc.npc = static_cast<int>(aux >> 22);
+    return pc;
+}
+
+// Epilogue of one piece of a key-split block (head i, row r): leave
+// (O, m, l) in the piece's partial slot; the piece that finishes last (a
+// counter per block and head) merges all of them:
+// o = sum_k 2^(m_k - M) O_k / sum_k 2^(m_k - M) l_k.  Kept out of line so its
+// registers do not press on the softmax loop.
+__device__ __noinline__ void split_epilogue(float* partials, int* err, uint32_t tO, int i, int r, bool valid,
+                                            float m_ref, float l, int slot, int kidx, int npc, __nv_bfloat16* dst,
+                                            volatile int* merge_flag) {
+    const int slot0 = slot - kidx;
+    auto part_of = [&](int sl) {
+        return partials + ((static_cast<size_t>(sl) * 2 + i) * 128 + r) * (kD + 4);
+    };
+    float* part = part_of(slot);
+#pragma unroll
+    for (int c = 0; c < 4; ++c) {
+        uint32_t w[32];
+        tmem_ld32(tO + c * 32, w);
+        tmem_ld_wait();
+        if (valid) {
+#pragma unroll
+            for (int e = 0; e < 32; e += 4)
+                *reinterpret_cast<uint4*>(part + c * 32 + e) = make_uint4(w[e], w[e + 1], w[e + 2], w[e + 3]);
+        }
+    }
+    if (valid) {
+        part[kD] = m_ref;
+        part[kD + 1] = l;
+    }
+    __threadfence();
+    ptx::named_barrier_sync(1 + i, 128);
+    int* counter = err + kWsCounterOffset / sizeof(int) + slot0 * 2 + i;
+    if (r == 0) merge_flag[i] = (atomicAdd(counter, 1) == npc - 1) ? 1 : 0;
+    ptx::named_barrier_sync(1 + i, 128);
+    if (merge_flag[i]) {
+        __threadfence();
+        float M = m_ref;
+        if (valid)
+            for (int k = 0; k < npc; ++k)
+                if (k != kidx) M = fmaxf(M, __ldcg(part_of(slot0 + k) + kD));
+        const float w_own = valid ? ptx::ex2(m_ref - M) : 0.f;
+        float L = l * w_own;
+        if (valid)
+            for (int k = 0; k < npc; ++k)
+                if (k != kidx) {
+                    const float* pk_ = part_of(slot0 + k);
+                    L += __ldcg(pk_ + kD + 1) * ptx::ex2(__ldcg(pk_ + kD) - M);
+                }
+        const float inv = (valid && L > 0.f) ? 1.f / L : 0.f;
+#pragma unroll 1
+        for (int c = 0; c < 4; ++c) {
+            uint32_t w[32];
+            tmem_ld32(tO + c * 32, w);
+            tmem_ld_wait();
+            if (valid) {
+                float acc[32];
+#pragma unroll
+                for (int e = 0; e < 32; ++e) acc[e] = __uint_as_float(w[e]) * w_own;
+                for (int k = 0; k < npc; ++k) {
+                    if (k == kidx) continue;
+                    const float* pk_ = part_of(slot0 + k);
+                    const float wk = ptx::ex2(__ldcg(pk_ + kD) - M);
+#pragma unroll
+                    for (int e = 0; e < 32; e += 4) {
+                        const float4 o = __ldcg(reinterpret_cast<const float4*>(pk_ + c * 32 + e));
+                        acc[e] += wk * o.x;
+                        acc[e + 1] += wk * o.y;
+                        acc[e + 2] += wk * o.z;
+                        acc[e + 3] += wk * o.w;
+                    }
+                }
+#pragma unroll
+                for (int e = 0; e < 32; e += 8) {
+                    uint4 q4;
+                    q4.x = ptx::pack_bf16x2(acc[e] * inv, acc[e + 1] * inv);
+                    q4.y = ptx::pack_bf16x2(acc[e + 2] * inv, acc[e + 3] * inv);
+                    q4.z = ptx::pack_bf16x2(acc[e + 4] * inv, acc[e + 5] * inv);
+                    q4.w = ptx::pack_bf16x2(acc[e + 6] * inv, acc[e + 7] * inv);
+                    *reinterpret_cast<uint4*>(dst + c * 32 + e) = q4;
+                }
+            }
+        }
+        if (r == 0) *counter = 0;  // ready for the next call
+    }
 }
 
 __global__ void __launch_bounds__(kThreadsPF, 1)
@@ -184,6 +291,7 @@ __global__ void __launch_bounds__(kThreadsPF, 1)
     auto bar = [&](int i) { return bar0 + 8 * i; };
     volatile uint32_t* tmem_slot = reinterpret_cast<volatile uint32_t*>(smem + kOffBar + kNumBars * 8);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + kOffBar + kNumBars * 8 + 8);
+    volatile int* merge_flag = reinterpret_cast<volatile int*>(smem + kOffBar + kNumBars * 8 + 16);  // per head
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
 
@@ -233,18 +341,9 @@ __global__ void __launch_bounds__(kThreadsPF, 1)
         }
     }
 
-    const Item item = decode_item(p, p.items[blockIdx.x]);
-    const int b = item.b, kvh = item.kvh;
-    const int prior = p.prior[b], nn = p.n_new[b];
-    const int t0 = item.tb * 128;
-    const int h0 = kvh * p.G + 2 * item.pair;
-    const int nh = min(2, p.G - 2 * item.pair);            // heads in this pair (1 or 2)
-    const int kmax = prior + min(t0 + 127, nn - 1);         // last visible key of the block
-    const int nkt_all = kmax / 128 + 1;                     // key tiles of the block
-    const int span = p.spans[blockIdx.x];
-    const int kt0 = span & 0xFFF;                           // this CTA's tiles: kt0 .. kt0 + nkt - 1
-    const int nkt = ((span >> 12) & 0xFFF) - kt0;
-    const int slot = (span >> 24) & 0xFF;                   // partial slot, or kPrefillNoSlot
+    const Piece pc = decode_piece(p, blockIdx.x);
+    const int b = pc.b, kvh = pc.kvh, prior = pc.prior, nn = pc.nn, t0 = pc.t0, h0 = pc.h0, nh = pc.nh;
+    const int kmax = pc.kmax, nkt_all = pc.nkt_all, kt0 = pc.kt0, nkt = pc.nkt;
     const int full_below = prior + t0;                      // keys <= this are visible to every row
     const int unit_row0 = (b * p.Hkv + kvh) * p.max_len;    // first cache row of (b, kvh)
 
@@ -462,28 +561,12 @@ __global__ void __launch_bounds__(kThreadsPF, 1)
                 *abort_flag = 1;
             }
             tc_fence_after();
-            if (slot != kPrefillNoSlot) {
-                // A piece of a key-split block: leave (O, m, l) for the combine kernel.
-                float* part = p.partials + ((static_cast<size_t>(slot) * 2 + i) * 128 + r) * (kD + 4);
-#pragma unroll
-                for (int c = 0; c < 4; ++c) {
-                    uint32_t w[32];
-                    tmem_ld32(tO + c * 32, w);
-                    tmem_ld_wait();
-                    if (valid) {
-#pragma unroll
-                        for (int e = 0; e < 32; e += 4)
-                            *reinterpret_cast<uint4*>(part + c * 32 + e) = make_uint4(w[e], w[e + 1], w[e + 2], w[e + 3]);
-                    }
-                }
-                if (valid) {
-                    part[kD] = m_ref;
-                    part[kD + 1] = l;
-                }
-            } else {
-            const float inv = (valid && l > 0.f) ? 1.f / l : 0.f;
             __nv_bfloat16* dst = static_cast<__nv_bfloat16*>(p.out) +
                                  ((static_cast<size_t>(b) * p.Hq + h0 + i) * p.T + t) * kD;
+            if (pc.slot != kPrefillNoSlot) {
+                split_epilogue(p.partials, p.err, tO, i, r, valid, m_ref, l, pc.slot, pc.kidx, pc.npc, dst, merge_flag);
+            } else {
+            const float inv = (valid && l > 0.f) ? 1.f / l : 0.f;
 #pragma unroll
             for (int c = 0; c < 4; ++c) {
                 uint32_t w[32];
@@ -513,66 +596,9 @@ __global__ void __launch_bounds__(kThreadsPF, 1)
     }
 }
 
-// Merge the key-split pieces of a (b, kvh, 128 positions, head pair) group:
-// o = sum_k 2^(m_k - M) O_k / sum_k 2^(m_k - M) l_k, M = max_k m_k, per row.
-__global__ void __launch_bounds__(256) prefill_combine_kernel(const __grid_constant__ PrefillCombineParams p) {
-    ptx::grid_dependency_wait();
-    ptx::launch_dependents();
-    int code = p.group_code[blockIdx.x];
-    const int pair = code % p.npair;
-    code /= p.npair;
-    const int tb = code % p.ntb;
-    code /= p.ntb;
-    const int kvh = code % p.Hkv, b = code / p.Hkv;
-    const int h0 = kvh * p.G + 2 * pair, nh = min(2, p.G - 2 * pair);
-    const int slot0 = p.group_slot0[blockIdx.x], np = p.group_pieces[blockIdx.x];
-    for (int idx = threadIdx.x; idx < nh * 128 * (kD / 4); idx += blockDim.x) {
-        const int c4 = idx & 31, r = (idx >> 5) & 127, i = idx >> 12;
-        const int t = tb * 128 + r;
-        if (t >= p.n_new[b] || t >= p.T) continue;
-        float m = -INFINITY, l = 0.f;
-        float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-        for (int k = 0; k < np; ++k) {
-            const float* part = p.partials + ((static_cast<size_t>(slot0 + k) * 2 + i) * 128 + r) * (kD + 4);
-            const float mk = part[kD];
-            const float mn = fmaxf(m, mk);
-            if (mn == -INFINITY) continue;
-            const float a = ptx::ex2(m - mn), c = ptx::ex2(mk - mn);
-            const float4 o = reinterpret_cast<const float4*>(part)[c4];
-            l = l * a + part[kD + 1] * c;
-            acc.x = acc.x * a + o.x * c;
-            acc.y = acc.y * a + o.y * c;
-            acc.z = acc.z * a + o.z * c;
-            acc.w = acc.w * a + o.w * c;
-            m = mn;
-        }
-        const float inv = l > 0.f ? 1.f / l : 0.f;
-        uint2 w;
-        w.x = ptx::pack_bf16x2(acc.x * inv, acc.y * inv);
-        w.y = ptx::pack_bf16x2(acc.z * inv, acc.w * inv);
-        *reinterpret_cast<uint2*>(static_cast<__nv_bfloat16*>(p.out) +
-                                  ((static_cast<size_t>(b) * p.Hq + h0 + i) * p.T + t) * kD + c4 * 4) = w;
-    }
-}
-
 }  // namespace
 
 size_t prefill_smem_bytes() { return kSmemPF; }
-
-cudaError_t launch_prefill_combine(const PrefillCombineParams& p, cudaStream_t stream) {
-    cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3(p.n_groups);
-    cfg.blockDim = dim3(256);
-    cfg.stream = stream;
-    cudaLaunchAttribute attr[1];
-    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-    attr[0].val.programmaticStreamSerializationAllowed = 1;
-    cfg.attrs = attr;
-    cfg.numAttrs = 1;
-    cudaError_t e = cudaLaunchKernelEx(&cfg, prefill_combine_kernel, p);
-    if (e != cudaSuccess) return e;
-    return cudaGetLastError();
-}
 
 cudaError_t launch_prefill_tc(const PrefillParams& p, const CUtensorMap& tmQ, const CUtensorMap& tmK,
                               const CUtensorMap& tmV, cudaStream_t stream) {
@@ -584,7 +610,7 @@ cudaError_t launch_prefill_tc(const PrefillParams& p, const CUtensorMap& tmQ, co
         attr_set = true;
     }
     cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3(p.n_items);
+    cfg.gridDim = dim3(p.n_pieces);
     cfg.blockDim = dim3(kThreadsPF);
     cfg.dynamicSmemBytes = kSmemPF;
     cfg.stream = stream;
