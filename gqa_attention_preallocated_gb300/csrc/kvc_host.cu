@@ -360,8 +360,14 @@ kvc_status do_attention(kvc_cache* c, int layer, const void* q, const AttnPlan& 
             for (size_t i0 = 0; i0 < items.size(); i0 += chunk) {
                 const size_t i1 = std::min(items.size(), i0 + chunk);
                 const int n_items = static_cast<int>(i1 - i0);
-                constexpr long long kStartCost = 5;  // per-CTA start-up, in tile x head units
-                constexpr int kMinPieceTiles = 4;
+#ifndef KVC_PF_START_COST
+#define KVC_PF_START_COST 13
+#endif
+#ifndef KVC_PF_MIN_PIECE
+#define KVC_PF_MIN_PIECE 8
+#endif
+                constexpr long long kStartCost = KVC_PF_START_COST;  // per-CTA start-up, in tile x head units
+                constexpr int kMinPieceTiles = KVC_PF_MIN_PIECE;
                 long long W = 0;
                 for (size_t k = i0; k < i1; ++k) W += static_cast<long long>(items[k].nkt) * items[k].nh + kStartCost;
                 const long long target = W / nsm + kStartCost;  // the SMs' common finishing time
