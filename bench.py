@@ -201,6 +201,17 @@ class Workload:
         return kv_bytes(self.lens_at(i), s.Hkv, s.d) * self.layers
 
     @property
+    def kernel_name(self):
+        """The dominant kernel of the timed attention call."""
+        if self.name == "prefill":
+            return "prefill_tc_kernel (tcgen05/TMEM; cut blocks merged in-kernel)"
+        return "decode_splitkv_bf16_kernel (+ combine_bf16_kernel" + (", append fused in)" if self.fused else ")")
+
+    @property
+    def kernel_source(self):
+        return "prefill_tc.cu" if self.name == "prefill" else "decode_bf16.cu"
+
+    @property
     def fused(self):
         """The library appends inside the attention launch when G*T <= 16 (warps own whole tiles)."""
         return (self.Hq // self.shape.Hkv) * self.T <= 16
@@ -434,7 +445,7 @@ def main():
         roof = {"bound": "hbm", "achieved": kb / (attn_ms * 1e-3) * 1e-9, "peak": hbm, "unit": "GB/s"}
     roof["frac"] = roof["achieved"] / roof["peak"]
     roof["peak_source"] = f"{peak_kind} (MEASURED_PEAKS.json)" if peak_kind == "measured" else "fallback"
-    roof["kernel"] = "decode_splitkv_bf16_kernel (+ combine_bf16_kernel" + (", append fused in)" if w.fused else ")")
+    roof["kernel"] = w.kernel_name
     roof["kernel_ms"] = attn_ms
     roof["traffic"] = _committed_traffic(w, kb)
 
@@ -474,7 +485,7 @@ def _committed_traffic(w: Workload, mean_kernel_bytes: float):
     if not os.path.exists(path):
         return None
     kv = dict(line.strip().split("=", 1) for line in open(path) if "=" in line and not line.startswith("#"))
-    src = os.path.join(ROOT, "gqa_attention_preallocated_gb300", "csrc", "decode_bf16.cu")
+    src = os.path.join(ROOT, "gqa_attention_preallocated_gb300", "csrc", w.kernel_source)
     sha = hashlib.sha256(open(src, "rb").read()).hexdigest()[:16]
     if kv.get("kernel_source_sha256_16") != sha:
         return None

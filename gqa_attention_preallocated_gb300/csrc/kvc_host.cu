@@ -818,7 +818,7 @@ const char* kvc_version(void) { return "kvc 0.1 (sm_103a)"; }
 // Allocation-free attention (kvc_gqa_attention_noalloc)
 //
 // For callers that cannot allocate device memory themselves: the split-KV
-// scratch (error word and partial results) lives in one
+// scratch (header and partial results) lives in one
 // file-scope device array instead of a caller-provided workspace.  The array
 // is part of this library's device image, so every GPU that loads the
 // library holds its KVC_NOALLOC_SCRATCH_BYTES until the process exits.
@@ -876,8 +876,8 @@ extern "C" kvc_status kvc_gqa_attention_noalloc(kvc_cache* c, int layer, const v
     s = noalloc_scratch_address(dev, &scratch);
     if (s) return s;
     cudaStream_t st = static_cast<cudaStream_t>(stream);
-    // The array keeps whatever the previous call left: zero the error word,
-    // the one part the kernels need to start at zero.
+    // The array keeps whatever the previous call left: zero the header (error
+    // word and merge counters), the one part the kernels need to start at zero.
     e = cudaMemsetAsync(scratch, 0, pl.ws_err, st);
     if (e != cudaSuccess) return cuda_fail(e, "cudaMemsetAsync(static scratch)");
     c->last_ws = scratch;
