@@ -348,8 +348,64 @@ def test_prefill_chunk_sampled(ragged):
 
 
 @pytest.mark.parametrize("B,Hkv,G,prior,T", [(1, 2, 4, 3000, 256), (2, 1, 2, 700, 200), (1, 1, 3, 2500, 130)])
-def test_prefill_key_split_pieces(B, Hkv, G, prior, T):
-    """Few long items on many SMs: the prefill work is cut into key-range pieces
-    merged by the combine kernel (odd G also leaves a pair with one head)."""
+def test_prefill_few_long_items(B, Hkv, G, prior, T):
+    """Few long prefill items on many SMs, every output compared (odd G also
+    leaves a head pair with one head)."""
     calls = [np.full(B, prior), np.full(B, T)]
     _run_calls(13, B, Hkv, G, 128, prior + T + 5, torch.bfloat16, calls)
+
+
+def _prefill_cuts(priors, n_new, Hkv, G, T, nsm, start_cost=13, min_piece=8):
+    """Cuts made by the library's prefill schedule (a longest-first list
+    schedule on the SMs, items cut at the SMs' common finish); restated here
+    only to show that a test case exercises the in-kernel merge."""
+    import heapq
+    items = []
+    for b, (pr, nn) in enumerate(zip(priors, n_new)):
+        for _ in range(Hkv):
+            for t0 in range(0, T, 128):
+                if t0 >= nn:
+                    continue
+                nkt = (int(pr) + min(t0 + 127, int(nn) - 1)) // 128 + 1
+                for pair in range((G + 1) // 2):
+                    items.append((nkt, min(2, G - 2 * pair)))
+    W = sum(n * h + start_cost for n, h in items)
+    target = W // nsm + start_cost
+    parts = [(-n * h, k, 0) for k, (n, h) in enumerate(items)]
+    heapq.heapify(parts)
+    sms = [(0, m) for m in range(nsm)]
+    cuts = 0
+    while parts:
+        c, k, lo = heapq.heappop(parts)
+        n, h = items[k]
+        t, m = heapq.heappop(sms)
+        hi, fit = n, max(0, target - t - start_cost) // h
+        if -c + start_cost > target - t and fit >= min_piece and n - (lo + fit) >= min_piece:
+            hi = lo + fit
+            cuts += 1
+            heapq.heappush(parts, (-(n - hi) * h, k, hi))
+        heapq.heappush(sms, (t + start_cost + (hi - lo) * h, m))
+    return cuts
+
+
+@pytest.mark.parametrize("Hq,T", [(32, 512), (24, 256)])
+def test_prefill_cut_blocks_merged_in_kernel(Hq, T):
+    """Long blocks on one row: the schedule cuts most blocks into key-range
+    pieces, whose partials the last piece merges inside the launch; sampled
+    (b, kvh) units are compared query by query (G = 3 adds one-head pieces)."""
+    _cuda_or_skip()
+    nsm = torch.cuda.get_device_properties(0).multi_processor_count
+    prior = 12000
+    s = wl.Shape("one_row_long_prefill", B=1, Hq=Hq, Hkv=8, d=128, max_len=prior + T + 8, dtype="bf16")
+    nn = np.full(1, T, dtype=np.int64)
+    assert _prefill_cuts([prior], nn, s.Hkv, Hq // s.Hkv, T, nsm) > 0
+    _decode_case(s, Hq, np.array([prior]), [T], [nn], 21, [(0, 0), (0, 7)])
+
+
+def test_longctx_layer_sampled():
+    """One layer of the long-context shape ([4, 8, 131072, 128] bf16, lengths
+    in [32768, 131008]): two decode steps, sampled units against the oracle."""
+    s = wl.LONGCTX
+    lens0 = wl.decode_lens(0, s.B, 32768, s.max_len - 64)
+    units = [(int(np.argmax(lens0)), 3), (int(np.argmin(lens0)), 6), (1, 0)]
+    _decode_case(s, s.Hq, lens0, [1, 1], [np.ones(s.B, dtype=np.int64)] * 2, 5, units)
