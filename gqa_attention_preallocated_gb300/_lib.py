@@ -43,6 +43,10 @@ SIGNATURES = [
     ("kvc_length", _I, [_VP, _I64P]),
     ("kvc_device_status", _I, [_VP, _VP, _VP, _I32P]),
     ("kvc_selftest_bounded_wait", _I, [_VP, ctypes.c_uint64, _VP]),
+    ("kvc_device_lens_bytes", _SZ, [_VP]),
+    ("kvc_lens_to_device", _I, [_VP, _VP, _VP]),
+    ("kvc_lens_from_device", _I, [_VP, _VP]),
+    ("kvc_decode_step", _I, [_VP, _I, _VP, _VP, _VP, _I, _I, _VP, _VP, _VP, _SZ, _VP]),
     ("kvc_kernel_launches", ctypes.c_uint64, [_VP]),
     ("kvc_last_error", ctypes.c_char_p, []),
     ("kvc_version", ctypes.c_char_p, []),

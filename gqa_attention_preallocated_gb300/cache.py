@@ -78,6 +78,7 @@ class KVCache:
         check(lib().kvc_create(ctypes.byref(h), layers, batch, kv_heads, max_len, head_dim, _DTYPES[dtype], kp, vp))
         self._h = h
         self._ws = None
+        self._dev_lens = None
 
     # ------------------------------------------------------------------ state
     def close(self) -> None:
@@ -201,6 +202,42 @@ class KVCache:
         check(lib().kvc_append_attention(self._h, layer, _ptr(q), _ptr(k_new), _ptr(v_new), Hq, T,
                                          nn.ctypes.data_as(_I32P), _ptr(out), _ptr(ws),
                                          0 if ws is None else ws.numel(), _stream_ptr(self.device, stream)))
+        return out
+
+    # ------------------------------------------------ device-resident lengths
+    def lens_to_device(self, stream=None) -> torch.Tensor:
+        """Hand the lengths over to a device array (int32 [layers, B]) owned by this object.
+
+        Until ``lens_from_device``, only ``decode_step`` may run: it reads and
+        advances the device lengths, so a step can be captured in a CUDA graph.
+        """
+        n = int(lib().kvc_device_lens_bytes(self._h)) // 4
+        self._dev_lens = torch.zeros(max(n, 1), dtype=torch.int32, device=self.device)
+        check(lib().kvc_lens_to_device(self._h, self._dev_lens.data_ptr(), _stream_ptr(self.device, stream)))
+        return self._dev_lens[:n].view(self.layers, self.B)
+
+    def lens_from_device(self, stream=None) -> None:
+        """Make the host lengths authoritative again (copies the device lengths back)."""
+        check(lib().kvc_lens_from_device(self._h, _stream_ptr(self.device, stream)))
+
+    def decode_step(self, layer: int, q: torch.Tensor, k_new: torch.Tensor, v_new: torch.Tensor,
+                    n_new: torch.Tensor, out: torch.Tensor, workspace: torch.Tensor, stream=None) -> torch.Tensor:
+        """``append_attention`` with the lengths on the device and ``n_new`` a device int32 [B].
+
+        Nothing per-step comes from the host, so the call can be captured in a
+        CUDA graph; ``out`` and ``workspace`` must be passed in.
+        """
+        if q.dim() != 4:
+            raise KVCError(1, "q must be [B, Hq, T, d]")
+        B, Hq, T, d = q.shape
+        self._check_tensor(q, (self.B, Hq, T, self.d), "q")
+        self._check_tensor(k_new, (self.B, self.Hkv, T, self.d), "k_new")
+        self._check_tensor(v_new, (self.B, self.Hkv, T, self.d), "v_new")
+        self._check_tensor(out, q.shape, "out")
+        if n_new.dtype != torch.int32 or n_new.device != self.device or n_new.numel() != self.B or not n_new.is_contiguous():
+            raise KVCError(1, f"n_new must be a contiguous int32 tensor of {self.B} entries on {self.device}")
+        check(lib().kvc_decode_step(self._h, layer, _ptr(q), _ptr(k_new), _ptr(v_new), Hq, T, n_new.data_ptr(),
+                                    _ptr(out), _ptr(workspace), workspace.numel(), _stream_ptr(self.device, stream)))
         return out
 
     def selftest_bounded_wait(self, limit_ns: int, workspace: torch.Tensor | None = None, stream=None) -> None:

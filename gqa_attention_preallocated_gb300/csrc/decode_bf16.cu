@@ -84,33 +84,61 @@ struct Shape {
     static_assert(kSmem <= 232448, "shared memory per CTA");
 };
 
+// The call's work partition: from the kernel parameters (host-planned) or
+// from a plan the device computed from device-resident lengths.  Read only
+// after the grid-dependency wait.
+struct Partition {
+    const int* gstart;
+    const int* prior;
+    const int* n_new;
+    int total_tiles;
+    int NB, Hkv;
+    __device__ __forceinline__ static Partition of(const DecodeParams& p) {
+        Partition w;
+        if (p.dplan) {
+            w.gstart = p.dplan->gstart;
+            w.prior = p.dplan->prior;
+            w.n_new = p.dplan->n_new;
+            w.total_tiles = p.dplan->total_tiles;
+        } else {
+            w.gstart = p.gstart;
+            w.prior = p.prior;
+            w.n_new = p.n_new;
+            w.total_tiles = p.total_tiles;
+        }
+        w.NB = p.NB;
+        w.Hkv = p.Hkv;
+        return w;
+    }
+};
+
 // Largest q with gstart[q] <= x (gstart nondecreasing, x < gstart[NB]).
-__device__ __forceinline__ int locate_group(const DecodeParams& p, int x) {
-    int lo = 0, hi = p.NB;
+__device__ __forceinline__ int locate_group(const int* gstart, int NB, int x) {
+    int lo = 0, hi = NB;
     while (lo < hi) {
         const int mid = (lo + hi + 1) >> 1;
-        if (p.gstart[mid] <= x) lo = mid; else hi = mid - 1;
+        if (gstart[mid] <= x) lo = mid; else hi = mid - 1;
     }
     return lo;
 }
 
 struct Cursor {
     int q, kvh, j, nt;
-    __device__ __forceinline__ void init(const DecodeParams& p, int x) {
-        q = locate_group(p, x);
-        nt = (p.gstart[q + 1] - p.gstart[q]) / p.Hkv;
-        const int off = x - p.gstart[q];
+    __device__ __forceinline__ void init(const Partition& w, int x) {
+        q = locate_group(w.gstart, w.NB, x);
+        nt = (w.gstart[q + 1] - w.gstart[q]) / w.Hkv;
+        const int off = x - w.gstart[q];
         kvh = off / nt;
         j = off - kvh * nt;
     }
-    __device__ __forceinline__ void advance(const DecodeParams& p) {
+    __device__ __forceinline__ void advance(const Partition& w) {
         if (++j < nt) return;
         j = 0;
-        if (++kvh < p.Hkv) return;
+        if (++kvh < w.Hkv) return;
         kvh = 0;
         ++q;
-        while (q < p.NB && p.gstart[q + 1] == p.gstart[q]) ++q;
-        if (q < p.NB) nt = (p.gstart[q + 1] - p.gstart[q]) / p.Hkv;
+        while (q < w.NB && w.gstart[q + 1] == w.gstart[q]) ++q;
+        if (q < w.NB) nt = (w.gstart[q + 1] - w.gstart[q]) / w.Hkv;
     }
 };
 
@@ -154,9 +182,6 @@ __global__ void __launch_bounds__(kThreads, 1)
     volatile int* stage_tag = abort_flag + 4;  // tile index the producer last put in each stage
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-    const long long N = p.total_tiles, P = gridDim.x;
-    const int x0 = static_cast<int>(static_cast<long long>(blockIdx.x) * N / P);
-    const int x1 = static_cast<int>(static_cast<long long>(blockIdx.x + 1) * N / P);
 
     // Prologue: touches no memory that earlier work in the stream may write.
     const uint32_t stage0 = ptx::smem_addr(stages);
@@ -177,6 +202,11 @@ __global__ void __launch_bounds__(kThreads, 1)
     __syncthreads();
     ptx::grid_dependency_wait();
     ptx::launch_dependents();
+    if (p.dplan && p.dplan->skip) return;  // a rejected device-resident step: nothing is written
+    const Partition wp = Partition::of(p);
+    const long long N = wp.total_tiles, P = gridDim.x;
+    const int x0 = static_cast<int>(static_cast<long long>(blockIdx.x) * N / P);
+    const int x1 = static_cast<int>(static_cast<long long>(blockIdx.x + 1) * N / P);
 
     // Padded queries (t >= n_new[b]) output zeros; spread over the whole grid.
     {
@@ -184,7 +214,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int row = blockIdx.x * kThreads + tid; row < rows_total; row += gridDim.x * kThreads) {
             const int t = row % p.T;
             const int b = row / (p.Hq * p.T);
-            if (t >= p.n_new[b]) {
+            if (t >= wp.n_new[b]) {
                 uint4* dst = reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(p.out) + static_cast<size_t>(row) * kD);
 #pragma unroll
                 for (int i = 0; i < kD * 2 / 16; ++i) dst[i] = make_uint4(0u, 0u, 0u, 0u);
@@ -197,7 +227,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (warp == kConsumerWarps) {
         if (lane == 0) {
             Cursor cur;
-            cur.init(p, x0);
+            cur.init(wp, x0);
             int issued = 0;
             for (int x = x0, it = 0; x < x1; ++x, ++it) {
                 const int s = it % kStages;
@@ -219,7 +249,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 ptx::tma_load_2d(sK + kTileBytes, &tmV, 0, row, full);
                 ptx::tma_load_2d(sK + kTileBytes + kHalfBytes, &tmV, 64, row, full);
                 ++issued;
-                cur.advance(p);
+                cur.advance(wp);
             }
             // Never leave the CTA with copies in flight: wait (bounded) for the
             // last phase armed on every stage.  In a clean run these phases
@@ -244,7 +274,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int lrow0 = mt * 16 + (lane >> 2);  // this thread's block rows: lrow0, lrow0 + 8
 
     Cursor cur;
-    cur.init(p, x0);
+    cur.init(wp, x0);
 
     float o[16][4];
     float m0 = -INFINITY, m1 = -INFINITY, l0 = 0.f, l1 = 0.f;
@@ -260,7 +290,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 
         if (x == x0 || j == 0) {
             // New unit segment: row limits, extent, query fragments, fresh state.
-            const int prior = p.prior[b], nn = p.n_new[b];
+            const int prior = wp.prior[b], nn = wp.n_new[b];
             min_lim = 0x7fffffff;
             extent = 0;
             for (int i = 0; i < RPB; ++i) {
@@ -585,7 +615,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 }
             }
         }
-        cur.advance(p);
+        cur.advance(wp);
     }
 }
 
@@ -599,12 +629,13 @@ __global__ void __launch_bounds__(kThreads, 1)
 constexpr int kCombineThreads = 128;
 constexpr int kCombineChunk = 8;   // partials loaded together (independent loads)
 
-// CTA whose tile range holds tile x: largest i with cta_start[i] <= x.
-__device__ __forceinline__ int cta_holding(const CombineParams& p, long long x) {
-    int lo = 0, hi = p.num_ctas - 1;
+// CTA whose tile range holds tile x: largest i with cta_start[i] <= x (CTAs
+// with empty ranges repeat the next start, so the owner is the last of them).
+__device__ __forceinline__ int cta_holding(const int* cta_start, int num_ctas, long long x) {
+    int lo = 0, hi = num_ctas - 1;
     while (lo < hi) {
         const int mid = (lo + hi + 1) >> 1;
-        if (p.cta_start[mid] <= x) lo = mid; else hi = mid - 1;
+        if (cta_start[mid] <= x) lo = mid; else hi = mid - 1;
     }
     return lo;
 }
@@ -612,16 +643,20 @@ __device__ __forceinline__ int cta_holding(const CombineParams& p, long long x) 
 __global__ void __launch_bounds__(kCombineThreads) combine_bf16_kernel(const __grid_constant__ CombineParams p) {
     ptx::grid_dependency_wait();
     ptx::launch_dependents();
+    if (p.dplan && p.dplan->skip) return;
+    const int* gstart = p.dplan ? p.dplan->gstart : p.gstart;
+    const int* cta_start = p.dplan ? p.dplan->cta_start : p.cta_start;
+    const int* n_new = p.dplan ? p.dplan->n_new : p.n_new;
     const int u = blockIdx.x;
     const int q = u / p.Hkv, kvh = u - q * p.Hkv;
-    const int nt = (p.gstart[q + 1] - p.gstart[q]) / p.Hkv;
+    const int nt = (gstart[q + 1] - gstart[q]) / p.Hkv;
     if (nt == 0) return;
-    const int us = p.gstart[q] + kvh * nt, ue = us + nt - 1;
-    const int c0 = cta_holding(p, us), c1 = cta_holding(p, ue);
+    const int us = gstart[q] + kvh * nt, ue = us + nt - 1;
+    const int c0 = cta_holding(cta_start, p.num_ctas, us), c1 = cta_holding(cta_start, p.num_ctas, ue);
     if (c0 == c1 && (p.ways == 1 || nt == 1)) return;  // written by the attention kernel
     const int ncand = (c1 - c0 + 1) * p.ways;
     const int b = q / p.RB, rb = q - b * p.RB;
-    const int nn = p.n_new[b];
+    const int nn = n_new[b];
     for (int idx = threadIdx.x; idx < p.part_rows * (kD / 4); idx += kCombineThreads) {
         const int lr = idx >> 5, c4 = idx & 31;
         const int r = rb * p.RPB + lr;
@@ -641,7 +676,7 @@ __global__ void __launch_bounds__(kCombineThreads) combine_bf16_kernel(const __g
                 bool valid = e < ncand;
                 if (valid) {
                     const int ci = e / p.ways, w = e - ci * p.ways;
-                    const int x0 = p.cta_start[c0 + ci], x1 = p.cta_start[c0 + ci + 1];
+                    const int x0 = cta_start[c0 + ci], x1 = cta_start[c0 + ci + 1];
                     const int la = max(us, x0) - x0, lb = min(ue, x1 - 1) - x0;
                     valid = (lb - la + 1 >= p.ways) || ((w - la % p.ways + p.ways) % p.ways <= lb - la);
                 }
@@ -669,6 +704,87 @@ __global__ void __launch_bounds__(kCombineThreads) combine_bf16_kernel(const __g
                              ((static_cast<size_t>(b) * p.Hq + kvh * p.G + g) * p.T + t) * kD + c4 * 4;
         store_bf16x4(dst, acc.x * inv, acc.y * inv, acc.z * inv, acc.w * inv);
     }
+}
+
+// Plan of one device-resident step (one CTA of 1024 threads): check every
+// row (0 <= n_new <= T, lens + n_new <= max_len; a bad row rejects the whole
+// step, nothing is written and the error word records it), then the same work
+// partition the host planner builds (per-group tile starts, per-CTA tile
+// starts) from the device lengths, and finally advance the lengths.
+constexpr int kPlanThreads = 1024;
+__global__ void __launch_bounds__(kPlanThreads) decode_plan_kernel(const __grid_constant__ PlanParams p) {
+    ptx::grid_dependency_wait();
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    DevicePlan* plan = p.plan;
+    int bad = 0;
+    for (int b = tid; b < p.B; b += kPlanThreads) {
+        const int L = p.lens[b], n = p.n_new[b];
+        bad |= (L < 0 || n < 0 || n > p.T || L > p.max_len - n) ? 1 : 0;
+    }
+    if (__syncthreads_or(bad)) {
+        if (tid == 0) {
+            plan->skip = 1;
+            plan->total_tiles = 0;
+            atomicExch(p.err, kDevOverflow);
+        }
+        ptx::launch_dependents();
+        return;
+    }
+    for (int b = tid; b < p.B; b += kPlanThreads) {
+        plan->prior[b] = p.lens[b];
+        plan->n_new[b] = p.n_new[b];
+    }
+    // Tiles of group q = b * RB + rb: Hkv units of ceil(extent / 64) tiles,
+    // extent = one past the largest visible key of the block's valid rows.
+    int tiles = 0;
+    if (tid < p.NB) {
+        const int b = tid / p.RB, rb = tid - b * p.RB;
+        const int prior = p.lens[b], n = p.n_new[b];
+        const int r0 = rb * p.RPB, r1 = min(p.R, r0 + p.RPB);
+        int extent = 0;
+        if (r1 - r0 >= p.T) {
+            if (n > 0) extent = prior + min(p.T, n);
+        } else {
+            for (int r = r0; r < r1; ++r) {
+                const int t = r % p.T;
+                if (t < n) extent = max(extent, prior + t + 1);
+            }
+        }
+        tiles = (extent + kKeyTile - 1) / kKeyTile * p.Hkv;
+    }
+    // Block-wide exclusive scan of the group tile counts.
+    __shared__ int warp_sum[kPlanThreads / 32];
+    int incl = tiles;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        const int v = __shfl_up_sync(0xffffffffu, incl, o);
+        if (lane >= o) incl += v;
+    }
+    if (lane == 31) warp_sum[warp] = incl;
+    __syncthreads();
+    if (warp == 0) {
+        int w = warp_sum[lane];
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const int v = __shfl_up_sync(0xffffffffu, w, o);
+            if (lane >= o) w += v;
+        }
+        warp_sum[lane] = w;  // inclusive over warps
+    }
+    __syncthreads();
+    const int excl = incl - tiles + (warp > 0 ? warp_sum[warp - 1] : 0);
+    const int total = warp_sum[kPlanThreads / 32 - 1];
+    if (tid < p.NB) plan->gstart[tid] = excl;
+    if (tid == 0) {
+        plan->gstart[p.NB] = total;
+        plan->total_tiles = total;
+        plan->skip = 0;
+    }
+    for (int i = tid; i <= p.num_ctas; i += kPlanThreads)
+        plan->cta_start[i] = static_cast<int>(static_cast<long long>(i) * total / p.num_ctas);
+    __syncthreads();  // every read of lens above is done
+    for (int b = tid; b < p.B; b += kPlanThreads) p.lens[b] += p.n_new[b];
+    ptx::launch_dependents();
 }
 
 template <typename... KArgs, typename... Args>
@@ -739,6 +855,12 @@ cudaError_t launch_decode_bf16(const DecodeParams& p, const CUtensorMap& tmK, co
 
 cudaError_t launch_combine_bf16(const CombineParams& p, cudaStream_t stream) {
     cudaError_t e = launch_pdl(combine_bf16_kernel, dim3(p.NB * p.Hkv), dim3(kCombineThreads), 0, stream, p);
+    if (e != cudaSuccess) return e;
+    return cudaGetLastError();
+}
+
+cudaError_t launch_decode_plan(const PlanParams& p, cudaStream_t stream) {
+    cudaError_t e = launch_pdl(decode_plan_kernel, dim3(1), dim3(kPlanThreads), 0, stream, p);
     if (e != cudaSuccess) return e;
     return cudaGetLastError();
 }

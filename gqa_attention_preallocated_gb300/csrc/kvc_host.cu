@@ -41,6 +41,10 @@ struct kvc_cache {
     std::vector<char> tm_ready;
     const void* last_ws = nullptr;
     uint64_t launches = 0;  // kernels this handle has enqueued
+    // Device-resident lengths (caller-owned int32 [layers][B]) while a run of
+    // graph-capturable steps owns them; the host copy is stale meanwhile.
+    int32_t* dev_lens = nullptr;
+    bool lens_on_device = false;
 };
 
 namespace {
@@ -165,7 +169,7 @@ kvc_status validate_append(const kvc_cache* c, int layer, const void* k_new, con
 struct AttnPlan {
     int Hq = 0, G = 0, T = 0, R = 0;
     int mt = 0, RPB = 0, RB = 0, NB = 0, units = 0, ways = 1, part_rows = 0;
-    size_t ws_err = 0, ws_counters = 0, ws_partials = 0, ws_total = 0;
+    size_t ws_err = 0, ws_plan = 0, ws_partials = 0, ws_total = 0;
 };
 
 size_t round_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
@@ -193,7 +197,7 @@ kvc_status plan_shape(const kvc_cache* c, int Hq, int T, int num_ctas, AttnPlan*
         // the units that straddle CTAs.  Only the header needs to start at
         // zero; the merge counters return to zero after each use.
         pl->ws_err = kWsHeaderBytes;
-        pl->ws_counters = 0;
+        pl->ws_plan = (sizeof(DevicePlan) + 255) / 256 * 256;  // device-computed plans of resident-length steps
         pl->ways = decode_launch_shape(pl->mt).ways;
         pl->part_rows = std::min(pl->R, pl->RPB);
         pl->ws_partials = static_cast<size_t>(pl->units + num_ctas) * pl->ways * pl->part_rows *
@@ -205,7 +209,7 @@ kvc_status plan_shape(const kvc_cache* c, int Hq, int T, int num_ctas, AttnPlan*
                                    (kHeadDimBf16 + 4) * sizeof(float);
             pl->ws_partials = std::max(pl->ws_partials, prefill);
         }
-        pl->ws_total = pl->ws_err + pl->ws_counters + pl->ws_partials;
+        pl->ws_total = pl->ws_err + pl->ws_plan + pl->ws_partials;
     }
     return ok();
 }
@@ -318,7 +322,7 @@ kvc_status do_attention(kvc_cache* c, int layer, const void* q, const AttnPlan& 
         pp.q = q;
         pp.out = out;
         pp.err = static_cast<int*>(ws);
-        pp.partials = reinterpret_cast<float*>(static_cast<uint8_t*>(ws) + pl.ws_err);
+        pp.partials = reinterpret_cast<float*>(static_cast<uint8_t*>(ws) + pl.ws_err + pl.ws_plan);
         pp.B = c->B;
         pp.Hq = pl.Hq;
         pp.Hkv = c->Hkv;
@@ -344,7 +348,7 @@ kvc_status do_attention(kvc_cache* c, int layer, const void* q, const AttnPlan& 
         }
         const size_t slot_bytes = static_cast<size_t>(2) * 128 * (kHeadDimBf16 + 4) * sizeof(float);
         const long long slot_room =
-            std::min<long long>(kMaxPrefillSlots, static_cast<long long>((ws_bytes - pl.ws_err) / slot_bytes));
+            std::min<long long>(kMaxPrefillSlots, static_cast<long long>((ws_bytes - pl.ws_err - pl.ws_plan) / slot_bytes));
         const int nsm = std::max(1, c->num_sms);
         // Items per launch, leaving room for the pieces that cuts add.
         const size_t chunk = static_cast<size_t>(kMaxPrefillPieces - std::min(nsm, kMaxPrefillPieces / 4));
@@ -453,7 +457,8 @@ kvc_status do_attention(kvc_cache* c, int layer, const void* q, const AttnPlan& 
     DecodeParams p;
     uint8_t* wsb = static_cast<uint8_t*>(ws);
     p.err = reinterpret_cast<int*>(wsb);
-    p.partials = reinterpret_cast<float*>(wsb + pl.ws_err + pl.ws_counters);
+    p.partials = reinterpret_cast<float*>(wsb + pl.ws_err + pl.ws_plan);
+    p.dplan = nullptr;
     p.q = q;
     p.out = out;
     p.B = c->B;
@@ -543,6 +548,7 @@ kvc_status do_attention(kvc_cache* c, int layer, const void* q, const AttnPlan& 
     if (need_combine) {
         static_assert(sizeof(CombineParams) < 32000, "kernel parameter block too large");
         CombineParams cp;
+        cp.dplan = nullptr;
         cp.partials = p.partials;
         cp.out = out;
         cp.Hq = pl.Hq;
@@ -582,6 +588,14 @@ kvc_status check_workspace(const kvc_cache* c, const AttnPlan& pl, const void* w
 // ===========================================================================
 // C ABI
 // ===========================================================================
+
+// Calls that read or write the host copy of the lengths refuse while the
+// device copy is authoritative.
+kvc_status check_host_lens(const kvc_cache* c) {
+    if (c && c->lens_on_device)
+        return fail(KVC_ERR_ARG, "the lengths live on the device (kvc_lens_to_device); call kvc_lens_from_device first");
+    return ok();
+}
 
 extern "C" {
 
@@ -631,6 +645,8 @@ void kvc_destroy(kvc_cache* c) { delete c; }
 
 kvc_status kvc_append(kvc_cache* c, int layer, const void* k_new, const void* v_new, int T, const int32_t* n_new,
                       void* stream) {
+    kvc_status s0 = check_host_lens(c);
+    if (s0) return s0;
     int max_n = 0;
     kvc_status s = validate_append(c, layer, k_new, v_new, T, n_new, &max_n);
     if (s) return s;
@@ -657,6 +673,8 @@ size_t kvc_workspace_bytes(const kvc_cache* c, int q_heads, int T) {
 
 kvc_status kvc_gqa_attention(kvc_cache* c, int layer, const void* q, int q_heads, int T, const int32_t* n_new,
                              void* out, void* workspace, size_t workspace_bytes, void* stream) {
+    kvc_status s0 = check_host_lens(c);
+    if (s0) return s0;
     kvc_status s = check_layer(c, layer);
     if (s) return s;
     AttnPlan pl;
@@ -680,6 +698,8 @@ kvc_status kvc_gqa_attention(kvc_cache* c, int layer, const void* q, int q_heads
 kvc_status kvc_append_attention(kvc_cache* c, int layer, const void* q, const void* k_new, const void* v_new,
                                 int q_heads, int T, const int32_t* n_new, void* out, void* workspace,
                                 size_t workspace_bytes, void* stream) {
+    kvc_status s0 = check_host_lens(c);
+    if (s0) return s0;
     int max_n = 0;
     kvc_status s = validate_append(c, layer, k_new, v_new, T, n_new, &max_n);
     if (s) return s;
@@ -727,6 +747,8 @@ kvc_status kvc_append_attention(kvc_cache* c, int layer, const void* q, const vo
 }
 
 kvc_status kvc_length(const kvc_cache* c, int64_t* out) {
+    kvc_status s0 = check_host_lens(c);
+    if (s0) return s0;
     if (!c || !out) return fail(KVC_ERR_ARG, "null argument");
     for (int l = 1; l < c->layers; ++l)
         for (int b = 0; b < c->B; ++b)
@@ -740,6 +762,8 @@ kvc_status kvc_length(const kvc_cache* c, int64_t* out) {
 }
 
 kvc_status kvc_truncate(kvc_cache* c, const int64_t* new_lens) {
+    kvc_status s0 = check_host_lens(c);
+    if (s0) return s0;
     if (!c) return fail(KVC_ERR_ARG, "null cache handle");
     if (c->B > 0 && !new_lens) return fail(KVC_ERR_ARG, "new_lens is null");
     std::vector<int64_t> cur(c->B);
@@ -755,12 +779,16 @@ kvc_status kvc_truncate(kvc_cache* c, const int64_t* new_lens) {
 }
 
 kvc_status kvc_reset(kvc_cache* c) {
+    kvc_status s0 = check_host_lens(c);
+    if (s0) return s0;
     if (!c) return fail(KVC_ERR_ARG, "null cache handle");
     std::fill(c->lens.begin(), c->lens.end(), 0);
     return ok();
 }
 
 kvc_status kvc_set_lens(kvc_cache* c, int layer, const int64_t* lens) {
+    kvc_status s0 = check_host_lens(c);
+    if (s0) return s0;
     kvc_status s = check_layer(c, layer);
     if (s) return s;
     if (!lens && c->B > 0) return fail(KVC_ERR_ARG, "lens is null");
@@ -773,6 +801,8 @@ kvc_status kvc_set_lens(kvc_cache* c, int layer, const int64_t* lens) {
 }
 
 kvc_status kvc_get_lens(const kvc_cache* c, int layer, int64_t* out) {
+    kvc_status s0 = check_host_lens(c);
+    if (s0) return s0;
     kvc_status s = check_layer(c, layer);
     if (s) return s;
     if (!out && c->B > 0) return fail(KVC_ERR_ARG, "out is null");
@@ -794,6 +824,9 @@ kvc_status kvc_device_status(kvc_cache* c, void* workspace, void* stream, int32_
         e = cudaMemsetAsync(workspace, 0, sizeof v, st);
         if (e == cudaSuccess) e = cudaStreamSynchronize(st);
         if (e != cudaSuccess) return cuda_fail(e, "clearing the device error word");
+        if (v == kDevOverflow)
+            return fail(KVC_ERR_OVERFLOW, "a device-resident step was rejected: a row would pass max_len or n_new "
+                                          "was outside 0..T (nothing was written, lengths unchanged)");
         return fail(KVC_ERR_DEVICE_TIMEOUT, "a kernel's bounded wait expired (code %d)", v);
     }
     return ok();
@@ -803,6 +836,157 @@ kvc_status kvc_selftest_bounded_wait(void* workspace, uint64_t limit_ns, void* s
     if (!workspace) return fail(KVC_ERR_ARG, "workspace is null");
     cudaError_t e = launch_wait_selftest(static_cast<int*>(workspace), limit_ns, static_cast<cudaStream_t>(stream));
     if (e != cudaSuccess) return cuda_fail(e, "self-test launch");
+    return ok();
+}
+
+size_t kvc_device_lens_bytes(const kvc_cache* c) {
+    return c ? static_cast<size_t>(c->layers) * c->B * sizeof(int32_t) : 0;
+}
+
+kvc_status kvc_lens_to_device(kvc_cache* c, int32_t* dev_lens, void* stream) {
+    if (!c) return fail(KVC_ERR_ARG, "null cache handle");
+    if (c->lens_on_device) return fail(KVC_ERR_ARG, "the lengths are already on the device");
+    if (c->B > 0 && !dev_lens) return fail(KVC_ERR_ARG, "dev_lens is null");
+    if ((reinterpret_cast<uintptr_t>(dev_lens) & 3u) != 0) return fail(KVC_ERR_ARG, "dev_lens not 4-byte aligned");
+    kvc_status s = ensure_device(c);
+    if (s) return s;
+    std::vector<int32_t> h(c->lens.size());
+    for (size_t i = 0; i < h.size(); ++i) h[i] = static_cast<int32_t>(c->lens[i]);
+    if (!h.empty()) {
+        cudaStream_t st = static_cast<cudaStream_t>(stream);
+        cudaError_t e = cudaMemcpyAsync(dev_lens, h.data(), h.size() * sizeof(int32_t), cudaMemcpyHostToDevice, st);
+        if (e == cudaSuccess) e = cudaStreamSynchronize(st);  // h is local
+        if (e != cudaSuccess) return cuda_fail(e, "copying the lengths to the device");
+    }
+    c->dev_lens = dev_lens;
+    c->lens_on_device = true;
+    return ok();
+}
+
+kvc_status kvc_lens_from_device(kvc_cache* c, void* stream) {
+    if (!c) return fail(KVC_ERR_ARG, "null cache handle");
+    if (!c->lens_on_device) return fail(KVC_ERR_ARG, "the lengths are on the host");
+    std::vector<int32_t> h(c->lens.size());
+    if (!h.empty()) {
+        cudaStream_t st = static_cast<cudaStream_t>(stream);
+        cudaError_t e = cudaMemcpyAsync(h.data(), c->dev_lens, h.size() * sizeof(int32_t), cudaMemcpyDeviceToHost, st);
+        if (e == cudaSuccess) e = cudaStreamSynchronize(st);
+        if (e != cudaSuccess) return cuda_fail(e, "copying the lengths from the device");
+    }
+    for (size_t i = 0; i < h.size(); ++i)
+        if (h[i] < 0 || h[i] > c->max_len)
+            return fail(KVC_ERR_ARG, "device length %d of slot %zu is outside 0..%d (left on the device)", h[i], i,
+                        c->max_len);
+    for (size_t i = 0; i < h.size(); ++i) c->lens[i] = h[i];
+    c->lens_on_device = false;
+    c->dev_lens = nullptr;
+    return ok();
+}
+
+kvc_status kvc_decode_step(kvc_cache* c, int layer, const void* q, const void* k_new, const void* v_new, int q_heads,
+                           int T, const int32_t* n_new_dev, void* out, void* workspace, size_t workspace_bytes,
+                           void* stream) {
+    kvc_status s = check_layer(c, layer);
+    if (s) return s;
+    if (!c->lens_on_device) return fail(KVC_ERR_ARG, "the lengths are on the host: call kvc_lens_to_device first");
+    if (c->dtype != KVC_BF16) return fail(KVC_ERR_ARG, "device-resident steps serve bf16 caches only");
+    if (c->B == 0 || T == 0) return ok();
+    if (T < 0) return fail(KVC_ERR_ARG, "T = %d < 0", T);
+    if (!q || !k_new || !v_new || !out || !n_new_dev) return fail(KVC_ERR_ARG, "null pointer argument");
+    if (!aligned16(q) || !aligned16(k_new) || !aligned16(v_new) || !aligned16(out))
+        return fail(KVC_ERR_ARG, "q / k_new / v_new / out not 16-byte aligned");
+    if ((reinterpret_cast<uintptr_t>(n_new_dev) & 3u) != 0) return fail(KVC_ERR_ARG, "n_new not 4-byte aligned");
+    s = ensure_device(c);
+    if (s) return s;
+    AttnPlan pl;
+    s = plan_shape(c, q_heads, T, c->num_sms, &pl);
+    if (s) return s;
+    if (pl.mt != 1)
+        return fail(KVC_ERR_SHAPE, "device-resident steps take G * T <= 16 query rows per KV head (G * T = %d)",
+                    pl.R);
+    if (static_cast<long long>(pl.NB) * ((c->max_len + kKeyTile - 1) / kKeyTile) * c->Hkv > 0x7fffffffll)
+        return fail(KVC_ERR_ARG, "too many key tiles for one call");
+    s = check_workspace(c, pl, workspace, workspace_bytes);
+    if (s) return s;
+    s = encode_layer_maps(c, layer);
+    if (s) return s;
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    uint8_t* wsb = static_cast<uint8_t*>(workspace);
+    if (workspace != c->last_ws) {
+        cudaError_t e = cudaMemsetAsync(workspace, 0, pl.ws_err, st);
+        if (e != cudaSuccess) return cuda_fail(e, "cudaMemsetAsync(workspace)");
+        c->last_ws = workspace;
+    }
+    DevicePlan* plan = reinterpret_cast<DevicePlan*>(wsb + pl.ws_err);
+    const int grid = c->num_sms;
+
+    PlanParams pp;
+    pp.n_new = n_new_dev;
+    pp.lens = c->dev_lens + static_cast<size_t>(layer) * c->B;
+    pp.plan = plan;
+    pp.err = reinterpret_cast<int*>(wsb);
+    pp.B = c->B;
+    pp.T = T;
+    pp.R = pl.R;
+    pp.RPB = pl.RPB;
+    pp.RB = pl.RB;
+    pp.NB = pl.NB;
+    pp.Hkv = c->Hkv;
+    pp.num_ctas = grid;
+    pp.max_len = c->max_len;
+    cudaError_t e = launch_decode_plan(pp, st);
+    if (e != cudaSuccess) return cuda_fail(e, "device plan launch");
+    ++c->launches;
+
+    static_assert(sizeof(DecodeParams) < 32000, "kernel parameter block too large");
+    DecodeParams p{};
+    p.dplan = plan;
+    p.err = reinterpret_cast<int*>(wsb);
+    p.partials = reinterpret_cast<float*>(wsb + pl.ws_err + pl.ws_plan);
+    p.q = q;
+    p.out = out;
+    p.B = c->B;
+    p.Hq = pl.Hq;
+    p.Hkv = c->Hkv;
+    p.G = pl.G;
+    p.T = pl.T;
+    p.max_len = c->max_len;
+    p.R = pl.R;
+    p.RPB = pl.RPB;
+    p.RB = pl.RB;
+    p.NB = pl.NB;
+    p.part_rows = pl.part_rows;
+    p.num_ctas = grid;
+    p.scale_log2 = static_cast<float>(1.4426950408889634 / sqrt(static_cast<double>(c->d)));
+    p.append_new = 1;
+    p.k_new = k_new;
+    p.v_new = v_new;
+    p.k_cache = c->k[layer];
+    p.v_cache = c->v[layer];
+    p.Tn = T;
+    e = launch_decode_bf16(p, c->tmK[layer], c->tmV[layer], 1, grid, st);
+    if (e != cudaSuccess) return cuda_fail(e, "split-KV attention launch");
+    ++c->launches;
+
+    static_assert(sizeof(CombineParams) < 32000, "kernel parameter block too large");
+    CombineParams cp{};
+    cp.dplan = plan;
+    cp.partials = p.partials;
+    cp.out = out;
+    cp.Hq = pl.Hq;
+    cp.Hkv = c->Hkv;
+    cp.G = pl.G;
+    cp.T = pl.T;
+    cp.R = pl.R;
+    cp.RPB = pl.RPB;
+    cp.RB = pl.RB;
+    cp.NB = pl.NB;
+    cp.ways = pl.ways;
+    cp.part_rows = pl.part_rows;
+    cp.num_ctas = grid;
+    e = launch_combine_bf16(cp, st);
+    if (e != cudaSuccess) return cuda_fail(e, "split-KV combine launch");
+    ++c->launches;
     return ok();
 }
 
@@ -853,6 +1037,8 @@ kvc_status noalloc_scratch_address(int device, void** out) {
 
 extern "C" kvc_status kvc_gqa_attention_noalloc(kvc_cache* c, int layer, const void* q, int q_heads, int T,
                                                 const int32_t* n_new, void* out, void* stream) {
+    kvc_status s0 = check_host_lens(c);
+    if (s0) return s0;
     kvc_status s = check_layer(c, layer);
     if (s) return s;
     if (c->dtype != KVC_BF16) return fail(KVC_ERR_ARG, "the allocation-free variant serves bf16 caches only");

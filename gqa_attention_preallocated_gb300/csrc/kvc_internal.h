@@ -51,7 +51,30 @@ cudaError_t launch_append(const AppendParams& p, int max_n_new, cudaStream_t str
 // (unit, CTA) pair: along the unit/CTA staircase every step raises it), and
 // the combine kernel merges them.
 // ---------------------------------------------------------------------------
+// Per-step plan of the split-KV kernels computed on the device from
+// device-resident lengths (graph-capturable steps): the fields the host
+// planner otherwise puts in DecodeParams / CombineParams.
+struct DevicePlan {
+    int skip;         // the step was rejected (a row would overflow): nothing runs
+    int total_tiles;
+    int prior[kMaxBatch];
+    int n_new[kMaxBatch];
+    int gstart[kMaxGroups + 1];
+    int cta_start[kMaxCtas + 1];
+};
+
+struct PlanParams {
+    const int32_t* n_new;  // device [B]
+    int32_t* lens;         // device [B]: this layer's lengths, advanced by n_new
+    DevicePlan* plan;
+    int* err;
+    int B, T, R, RPB, RB, NB, Hkv, num_ctas, max_len;
+};
+
+cudaError_t launch_decode_plan(const PlanParams& p, cudaStream_t stream);
+
 struct DecodeParams {
+    const DevicePlan* dplan;  // when set, prior / n_new / gstart / total_tiles come from it
     const void* q;      // [B, Hq, T, d] bf16
     void* out;          // [B, Hq, T, d] bf16
     float* partials;    // [(units + P) * ways sub-slots][part_rows][d + 4] : O (d), m, l, pad
@@ -83,6 +106,7 @@ struct DecodeParams {
 // return at once).  Partial rows live at
 // ((u + cta) * ways + warp) * part_rows + row.
 struct CombineParams {
+    const DevicePlan* dplan;  // when set, n_new / gstart / cta_start / total_tiles come from it
     const float* partials;
     void* out;
     int Hq, Hkv, G, T, R, RPB, RB, NB;
@@ -168,7 +192,8 @@ enum DeviceError : int {
     kDevTimeoutEmpty = 2,  // producer gave up waiting for a free stage
     kDevTimeoutDrain = 3,  // abort path gave up waiting for copies in flight
     kDevTimeoutTest = 4,   // the self-test wait expired, as it is meant to
-    kDevTimeoutTag = 5     // consumer gave up waiting for the producer to claim a stage
+    kDevTimeoutTag = 5,    // consumer gave up waiting for the producer to claim a stage
+    kDevOverflow = 6       // a device-resident step was rejected: a row would pass max_len
 };
 
 // Self-test of the bounded wait: waits on an mbarrier that nothing arrives at,

@@ -184,7 +184,8 @@ kvc_status kvc_length(const kvc_cache* c, int64_t* out);
  * stream's work ends: synchronizes `stream`, copies the word and stores it in
  * *code (0 = clean; otherwise a kernel's bounded wait expired and that call's
  * output is not valid), then clears the word.  Returns KVC_ERR_DEVICE_TIMEOUT
- * when *code != 0. */
+ * when *code != 0, or KVC_ERR_OVERFLOW when the code records a rejected
+ * device-resident step (kvc_decode_step). */
 kvc_status kvc_device_status(kvc_cache* c, void* workspace, void* stream, int32_t* code);
 
 /* Self-test of the kernels' bounded waits: launches one CTA that waits on an
@@ -193,6 +194,51 @@ kvc_status kvc_device_status(kvc_cache* c, void* workspace, void* stream, int32_
  * so a following kvc_device_status reports KVC_ERR_DEVICE_TIMEOUT.  No fault,
  * no hang. */
 kvc_status kvc_selftest_bounded_wait(void* workspace, uint64_t limit_ns, void* stream);
+
+/* ---- Device-resident lengths: graph-capturable decode steps -------------
+ *
+ * "16. Prefill, decode and the KV cache", the cache protocol paragraph after
+ * "Design choices worth noticing": a static cache lets a step be captured in
+ * a CUDA graph.  A captured step must take nothing from the host that changes
+ * per step, so while these calls are in use the lengths live in a caller-owned
+ * device array and the step's work partition is computed on the device.
+ *
+ * Bytes of that array: int32 [layers][B]. */
+size_t kvc_device_lens_bytes(const kvc_cache* c);
+
+/* Copy the host lengths into dev_lens (caller-owned device memory of
+ * kvc_device_lens_bytes(c) bytes, 4-byte aligned; synchronizes `stream`) and
+ * hand them over to the device: from now on kvc_decode_step reads and
+ * advances them, and every call that reads or writes the host lengths
+ * (append, attention, truncate, reset, set/get lens, length, noalloc)
+ * returns KVC_ERR_ARG until kvc_lens_from_device.  dev_lens must stay valid
+ * until then. */
+kvc_status kvc_lens_to_device(kvc_cache* c, int32_t* dev_lens, void* stream);
+
+/* Copy the device lengths back to the host (synchronizes `stream`) and make
+ * the host copy authoritative again.  KVC_ERR_ARG if the lengths are not on
+ * the device, or if a device length lies outside 0..max_len (then they stay
+ * on the device). */
+kvc_status kvc_lens_from_device(kvc_cache* c, void* stream);
+
+/* One step of kvc_append_attention with the lengths on the device: appends
+ * n_new[b] rows of k_new / v_new [B, Hkv, T, d] at row b's device length, then
+ * the T queries q [B, Hq, T, d] attend exactly as in kvc_gqa_attention, and
+ * the device lengths advance by n_new.  n_new is a device int32 [B].  bf16
+ * caches with G * T <= 16 query rows per KV head (decode and short verify).
+ * Three kernels are enqueued (device plan, attention with the append fused
+ * in, combine), with nothing read from the host that changes per step, so
+ * the call can be captured in a CUDA graph and replayed with new contents of
+ * q, k_new, v_new and n_new.  The workspace is the one kvc_workspace_bytes
+ * sizes (plus its device plan region, included there).
+ * Errors found on the host (nothing enqueued): KVC_ERR_ARG (lengths on the
+ * host, pointers, dtype), KVC_ERR_SHAPE (G * T > 16, Hq % Hkv), KVC_ERR_WORKSPACE,
+ * KVC_ERR_CUDA.  A row with n_new[b] outside 0..T or past max_len rejects the
+ * whole step on the device: nothing is written, no length changes, and the
+ * next kvc_device_status returns KVC_ERR_OVERFLOW. */
+kvc_status kvc_decode_step(kvc_cache* c, int layer, const void* q, const void* k_new, const void* v_new, int q_heads,
+                           int T, const int32_t* n_new, void* out, void* workspace, size_t workspace_bytes,
+                           void* stream);
 
 /* Number of kernels this handle has enqueued so far (append, attention and,
  * when a call's units were split across CTAs, the combine kernel).  Host

@@ -187,3 +187,16 @@ def test_workspace_query_without_gpu_or_for_f32(L):
     assert L.kvc_workspace_bytes(h, 4, 1) == 0  # the f32 path needs no workspace
     L.kvc_destroy(h)
     assert L.kvc_workspace_bytes(None, 4, 1) == 0
+
+
+def test_device_lens_calls_without_device_state(L):
+    st, h = _create(L, layers=2, B=3)
+    assert L.kvc_device_lens_bytes(h) == 2 * 3 * 4
+    assert L.kvc_lens_from_device(h, None) == 1  # the lengths are on the host
+    q = ctypes.c_void_p(1 << 42)
+    # a resident-length step before the lengths were handed over
+    assert L.kvc_decode_step(h, 0, q, q, q, 4, 1, q, q, q, 1 << 20, None) == 1
+    assert b"kvc_lens_to_device" in L.kvc_last_error()
+    assert L.kvc_lens_to_device(h, None, None) == 1  # null array
+    L.kvc_destroy(h)
+    assert L.kvc_device_lens_bytes(None) == 0
