@@ -84,61 +84,64 @@ struct Shape {
     static_assert(kSmem <= 232448, "shared memory per CTA");
 };
 
-// The call's work partition: from the kernel parameters (host-planned) or
-// from a plan the device computed from device-resident lengths.  Read only
-// after the grid-dependency wait.
-struct Partition {
-    const int* gstart;
-    const int* prior;
-    const int* n_new;
-    int total_tiles;
-    int NB, Hkv;
-    __device__ __forceinline__ static Partition of(const DecodeParams& p) {
-        Partition w;
-        if (p.dplan) {
-            w.gstart = p.dplan->gstart;
-            w.prior = p.dplan->prior;
-            w.n_new = p.dplan->n_new;
-            w.total_tiles = p.dplan->total_tiles;
-        } else {
-            w.gstart = p.gstart;
-            w.prior = p.prior;
-            w.n_new = p.n_new;
-            w.total_tiles = p.total_tiles;
-        }
-        w.NB = p.NB;
-        w.Hkv = p.Hkv;
-        return w;
-    }
+// The call's work partition, read only after the grid-dependency wait.
+// Part<false>: planned on the host, in the kernel parameters (indexed in
+// parameter space).  Part<true>: planned on the device from device-resident
+// lengths (a DevicePlan in the workspace).
+template <bool DP>
+struct Part;
+
+template <>
+struct Part<false> {
+    const DecodeParams& p;
+    __device__ __forceinline__ int gstart(int i) const { return p.gstart[i]; }
+    __device__ __forceinline__ int prior(int b) const { return p.prior[b]; }
+    __device__ __forceinline__ int n_new(int b) const { return p.n_new[b]; }
+    __device__ __forceinline__ int total_tiles() const { return p.total_tiles; }
+    __device__ __forceinline__ int NB() const { return p.NB; }
+    __device__ __forceinline__ int Hkv() const { return p.Hkv; }
+};
+
+template <>
+struct Part<true> {
+    const DecodeParams& p;
+    __device__ __forceinline__ int gstart(int i) const { return p.dplan->gstart[i]; }
+    __device__ __forceinline__ int prior(int b) const { return p.dplan->prior[b]; }
+    __device__ __forceinline__ int n_new(int b) const { return p.dplan->n_new[b]; }
+    __device__ __forceinline__ int total_tiles() const { return p.dplan->total_tiles; }
+    __device__ __forceinline__ int NB() const { return p.NB; }
+    __device__ __forceinline__ int Hkv() const { return p.Hkv; }
 };
 
 // Largest q with gstart[q] <= x (gstart nondecreasing, x < gstart[NB]).
-__device__ __forceinline__ int locate_group(const int* gstart, int NB, int x) {
-    int lo = 0, hi = NB;
+template <bool DP>
+__device__ __forceinline__ int locate_group(const Part<DP>& w, int x) {
+    int lo = 0, hi = w.NB();
     while (lo < hi) {
         const int mid = (lo + hi + 1) >> 1;
-        if (gstart[mid] <= x) lo = mid; else hi = mid - 1;
+        if (w.gstart(mid) <= x) lo = mid; else hi = mid - 1;
     }
     return lo;
 }
 
+template <bool DP>
 struct Cursor {
     int q, kvh, j, nt;
-    __device__ __forceinline__ void init(const Partition& w, int x) {
-        q = locate_group(w.gstart, w.NB, x);
-        nt = (w.gstart[q + 1] - w.gstart[q]) / w.Hkv;
-        const int off = x - w.gstart[q];
+    __device__ __forceinline__ void init(const Part<DP>& w, int x) {
+        q = locate_group(w, x);
+        nt = (w.gstart(q + 1) - w.gstart(q)) / w.Hkv();
+        const int off = x - w.gstart(q);
         kvh = off / nt;
         j = off - kvh * nt;
     }
-    __device__ __forceinline__ void advance(const Partition& w) {
+    __device__ __forceinline__ void advance(const Part<DP>& w) {
         if (++j < nt) return;
         j = 0;
-        if (++kvh < w.Hkv) return;
+        if (++kvh < w.Hkv()) return;
         kvh = 0;
         ++q;
-        while (q < w.NB && w.gstart[q + 1] == w.gstart[q]) ++q;
-        if (q < w.NB) nt = (w.gstart[q + 1] - w.gstart[q]) / w.Hkv;
+        while (q < w.NB() && w.gstart(q + 1) == w.gstart(q)) ++q;
+        if (q < w.NB()) nt = (w.gstart(q + 1) - w.gstart(q)) / w.Hkv();
     }
 };
 
@@ -160,7 +163,7 @@ __device__ __forceinline__ bool wait_stage_tag(const volatile int* tag, int it, 
     }
 }
 
-template <int MT>
+template <int MT, bool DP>
 __global__ void __launch_bounds__(kThreads, 1)
     decode_splitkv_bf16_kernel(const __grid_constant__ DecodeParams p, const __grid_constant__ CUtensorMap tmK,
                                const __grid_constant__ CUtensorMap tmV) {
@@ -182,6 +185,12 @@ __global__ void __launch_bounds__(kThreads, 1)
     volatile int* stage_tag = abort_flag + 4;  // tile index the producer last put in each stage
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const Part<DP> wp{p};
+    // This CTA's tiles (host plan: known before the dependency wait).
+    long long N = DP ? 0 : wp.total_tiles();
+    const long long P = gridDim.x;
+    int x0 = static_cast<int>(static_cast<long long>(blockIdx.x) * N / P);
+    int x1 = static_cast<int>(static_cast<long long>(blockIdx.x + 1) * N / P);
 
     // Prologue: touches no memory that earlier work in the stream may write.
     const uint32_t stage0 = ptx::smem_addr(stages);
@@ -202,11 +211,12 @@ __global__ void __launch_bounds__(kThreads, 1)
     __syncthreads();
     ptx::grid_dependency_wait();
     ptx::launch_dependents();
-    if (p.dplan && p.dplan->skip) return;  // a rejected device-resident step: nothing is written
-    const Partition wp = Partition::of(p);
-    const long long N = wp.total_tiles, P = gridDim.x;
-    const int x0 = static_cast<int>(static_cast<long long>(blockIdx.x) * N / P);
-    const int x1 = static_cast<int>(static_cast<long long>(blockIdx.x + 1) * N / P);
+    if (DP) {
+        if (p.dplan->skip) return;  // a rejected device-resident step: nothing is written
+        N = wp.total_tiles();
+        x0 = static_cast<int>(static_cast<long long>(blockIdx.x) * N / P);
+        x1 = static_cast<int>(static_cast<long long>(blockIdx.x + 1) * N / P);
+    }
 
     // Padded queries (t >= n_new[b]) output zeros; spread over the whole grid.
     {
@@ -214,7 +224,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int row = blockIdx.x * kThreads + tid; row < rows_total; row += gridDim.x * kThreads) {
             const int t = row % p.T;
             const int b = row / (p.Hq * p.T);
-            if (t >= wp.n_new[b]) {
+            if (t >= wp.n_new(b)) {
                 uint4* dst = reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(p.out) + static_cast<size_t>(row) * kD);
 #pragma unroll
                 for (int i = 0; i < kD * 2 / 16; ++i) dst[i] = make_uint4(0u, 0u, 0u, 0u);
@@ -226,7 +236,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     // ------------------------------------------------------------------ producer
     if (warp == kConsumerWarps) {
         if (lane == 0) {
-            Cursor cur;
+            Cursor<DP> cur;
             cur.init(wp, x0);
             int issued = 0;
             for (int x = x0, it = 0; x < x1; ++x, ++it) {
@@ -273,7 +283,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int quad = lane & 3;
     const int lrow0 = mt * 16 + (lane >> 2);  // this thread's block rows: lrow0, lrow0 + 8
 
-    Cursor cur;
+    Cursor<DP> cur;
     cur.init(wp, x0);
 
     float o[16][4];
@@ -290,7 +300,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 
         if (x == x0 || j == 0) {
             // New unit segment: row limits, extent, query fragments, fresh state.
-            const int prior = wp.prior[b], nn = wp.n_new[b];
+            const int prior = wp.prior(b), nn = wp.n_new(b);
             min_lim = 0x7fffffff;
             extent = 0;
             for (int i = 0; i < RPB; ++i) {
@@ -629,34 +639,53 @@ __global__ void __launch_bounds__(kThreads, 1)
 constexpr int kCombineThreads = 128;
 constexpr int kCombineChunk = 8;   // partials loaded together (independent loads)
 
+// The partition as the combine kernel sees it: host plan in the parameters
+// (parameter space) or the device plan.
+template <bool DP>
+struct CPart;
+template <>
+struct CPart<false> {
+    const CombineParams& p;
+    __device__ __forceinline__ int gstart(int i) const { return p.gstart[i]; }
+    __device__ __forceinline__ int cta_start(int i) const { return p.cta_start[i]; }
+    __device__ __forceinline__ int n_new(int b) const { return p.n_new[b]; }
+};
+template <>
+struct CPart<true> {
+    const CombineParams& p;
+    __device__ __forceinline__ int gstart(int i) const { return p.dplan->gstart[i]; }
+    __device__ __forceinline__ int cta_start(int i) const { return p.dplan->cta_start[i]; }
+    __device__ __forceinline__ int n_new(int b) const { return p.dplan->n_new[b]; }
+};
+
 // CTA whose tile range holds tile x: largest i with cta_start[i] <= x (CTAs
 // with empty ranges repeat the next start, so the owner is the last of them).
-__device__ __forceinline__ int cta_holding(const int* cta_start, int num_ctas, long long x) {
+template <bool DP>
+__device__ __forceinline__ int cta_holding(const CPart<DP>& w, int num_ctas, long long x) {
     int lo = 0, hi = num_ctas - 1;
     while (lo < hi) {
         const int mid = (lo + hi + 1) >> 1;
-        if (cta_start[mid] <= x) lo = mid; else hi = mid - 1;
+        if (w.cta_start(mid) <= x) lo = mid; else hi = mid - 1;
     }
     return lo;
 }
 
+template <bool DP>
 __global__ void __launch_bounds__(kCombineThreads) combine_bf16_kernel(const __grid_constant__ CombineParams p) {
     ptx::grid_dependency_wait();
     ptx::launch_dependents();
-    if (p.dplan && p.dplan->skip) return;
-    const int* gstart = p.dplan ? p.dplan->gstart : p.gstart;
-    const int* cta_start = p.dplan ? p.dplan->cta_start : p.cta_start;
-    const int* n_new = p.dplan ? p.dplan->n_new : p.n_new;
+    if (DP && p.dplan->skip) return;
+    const CPart<DP> cw{p};
     const int u = blockIdx.x;
     const int q = u / p.Hkv, kvh = u - q * p.Hkv;
-    const int nt = (gstart[q + 1] - gstart[q]) / p.Hkv;
+    const int nt = (cw.gstart(q + 1) - cw.gstart(q)) / p.Hkv;
     if (nt == 0) return;
-    const int us = gstart[q] + kvh * nt, ue = us + nt - 1;
-    const int c0 = cta_holding(cta_start, p.num_ctas, us), c1 = cta_holding(cta_start, p.num_ctas, ue);
+    const int us = cw.gstart(q) + kvh * nt, ue = us + nt - 1;
+    const int c0 = cta_holding(cw, p.num_ctas, us), c1 = cta_holding(cw, p.num_ctas, ue);
     if (c0 == c1 && (p.ways == 1 || nt == 1)) return;  // written by the attention kernel
     const int ncand = (c1 - c0 + 1) * p.ways;
     const int b = q / p.RB, rb = q - b * p.RB;
-    const int nn = n_new[b];
+    const int nn = cw.n_new(b);
     for (int idx = threadIdx.x; idx < p.part_rows * (kD / 4); idx += kCombineThreads) {
         const int lr = idx >> 5, c4 = idx & 31;
         const int r = rb * p.RPB + lr;
@@ -676,7 +705,7 @@ __global__ void __launch_bounds__(kCombineThreads) combine_bf16_kernel(const __g
                 bool valid = e < ncand;
                 if (valid) {
                     const int ci = e / p.ways, w = e - ci * p.ways;
-                    const int x0 = cta_start[c0 + ci], x1 = cta_start[c0 + ci + 1];
+                    const int x0 = cw.cta_start(c0 + ci), x1 = cw.cta_start(c0 + ci + 1);
                     const int la = max(us, x0) - x0, lb = min(ue, x1 - 1) - x0;
                     valid = (lb - la + 1 >= p.ways) || ((w - la % p.ways + p.ways) % p.ways <= lb - la);
                 }
@@ -803,19 +832,19 @@ cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t s
     return cudaLaunchKernelEx(&cfg, kernel, std::forward<Args>(args)...);
 }
 
-template <int MT>
+template <int MT, bool DP>
 cudaError_t launch_mt(const DecodeParams& p, const CUtensorMap& tmK, const CUtensorMap& tmV, int grid,
                       cudaStream_t stream) {
     static bool attr_set = false;
     if (!attr_set) {
-        cudaError_t e = cudaFuncSetAttribute(decode_splitkv_bf16_kernel<MT>,
+        cudaError_t e = cudaFuncSetAttribute(decode_splitkv_bf16_kernel<MT, DP>,
                                              cudaFuncAttributeMaxDynamicSharedMemorySize,
                                              static_cast<int>(Shape<MT>::kSmem));
         if (e != cudaSuccess) return e;
         attr_set = true;
     }
-    cudaError_t e = launch_pdl(decode_splitkv_bf16_kernel<MT>, dim3(grid), dim3(kThreads), Shape<MT>::kSmem, stream,
-                               p, tmK, tmV);
+    cudaError_t e = launch_pdl(decode_splitkv_bf16_kernel<MT, DP>, dim3(grid), dim3(kThreads), Shape<MT>::kSmem,
+                               stream, p, tmK, tmV);
     if (e != cudaSuccess) return e;
     return cudaGetLastError();
 }
@@ -845,16 +874,20 @@ DecodeLaunch decode_launch_shape(int mt) {
 
 cudaError_t launch_decode_bf16(const DecodeParams& p, const CUtensorMap& tmK, const CUtensorMap& tmV, int mt,
                                int grid, cudaStream_t stream) {
+    if (p.dplan) return mt == 1 ? launch_mt<1, true>(p, tmK, tmV, grid, stream) : cudaErrorInvalidValue;
     switch (mt) {
-        case 1: return launch_mt<1>(p, tmK, tmV, grid, stream);
-        case 2: return launch_mt<2>(p, tmK, tmV, grid, stream);
-        case 4: return launch_mt<4>(p, tmK, tmV, grid, stream);
+        case 1: return launch_mt<1, false>(p, tmK, tmV, grid, stream);
+        case 2: return launch_mt<2, false>(p, tmK, tmV, grid, stream);
+        case 4: return launch_mt<4, false>(p, tmK, tmV, grid, stream);
         default: return cudaErrorInvalidValue;
     }
 }
 
 cudaError_t launch_combine_bf16(const CombineParams& p, cudaStream_t stream) {
-    cudaError_t e = launch_pdl(combine_bf16_kernel, dim3(p.NB * p.Hkv), dim3(kCombineThreads), 0, stream, p);
+    cudaError_t e = p.dplan ? launch_pdl(combine_bf16_kernel<true>, dim3(p.NB * p.Hkv), dim3(kCombineThreads), 0,
+                                         stream, p)
+                            : launch_pdl(combine_bf16_kernel<false>, dim3(p.NB * p.Hkv), dim3(kCombineThreads), 0,
+                                         stream, p);
     if (e != cudaSuccess) return e;
     return cudaGetLastError();
 }
