@@ -492,11 +492,14 @@ __global__ void __launch_bounds__(kThreadsPF, 1)
                     }
                 }
                 mx = (mx == -INFINITY) ? -INFINITY : mx * p.scale_log2;
-                if (mx > m_ref + kRescaleThreshold || (m_ref == -INFINITY && mx != -INFINITY)) {
+                const bool move = mx > m_ref + kRescaleThreshold || (m_ref == -INFINITY && mx != -INFINITY);
+                if (__any_sync(0xffffffffu, move)) {
                     // Move the reference max.  O_i holds the PV sums up to tile
                     // j-1 (all with the old reference): wait for the last of them
-                    // and scale O_i and l by 2^(old - new).
-                    const float f = (m_ref == -INFINITY) ? 0.f : ptx::ex2(m_ref - mx);
+                    // and scale O_i and l by 2^(old - new).  The TMEM loads and
+                    // stores are warp-collective, so the warp rescales together;
+                    // rows that keep their reference scale by 1.
+                    const float f = !move ? 1.f : (m_ref == -INFINITY) ? 0.f : ptx::ex2(m_ref - mx);
                     if (j > 0) {
                         if (!ptx::mbar_wait_bounded(bar(kBarO + i), (j - 1) & 1, *abort_flag ? 0ull : kWaitNs)) {
                             atomicExch(p.err, kDevTimeoutFull);
@@ -518,7 +521,7 @@ __global__ void __launch_bounds__(kThreadsPF, 1)
                         tmem_st_wait();
                     }
                     l *= f;
-                    m_ref = mx;
+                    if (move) m_ref = mx;
                 }
                 // pass 2: p = 2^(s * scale - m_ref) as bf16 pairs into TMEM over S_i
                 const float mu = (m_ref == -INFINITY) ? 0.f : m_ref;

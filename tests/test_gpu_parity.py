@@ -409,3 +409,38 @@ def test_longctx_layer_sampled():
     lens0 = wl.decode_lens(0, s.B, 32768, s.max_len - 64)
     units = [(int(np.argmax(lens0)), 3), (int(np.argmin(lens0)), 6), (1, 0)]
     _decode_case(s, s.Hq, lens0, [1, 1], [np.ones(s.B, dtype=np.int64)] * 2, 5, units)
+
+
+@pytest.mark.parametrize("T", [256, 200])
+def test_prefill_score_jumps(T):
+    """Scores that jump by about 25, 75 and 200 (log2 units) at keys further into
+    the row: the running maximum moves at the next tile (jumps above 8) or
+    inside the tile (jumps above 64, in either 64-key half), and the result
+    still matches the oracle."""
+    _cuda_or_skip()
+    B, Hkv, G, d, prior = 1, 2, 2, 128, 1300
+    max_len = prior + T + 8
+    rng = np.random.default_rng(11)
+    u = np.ones(d)
+    k0 = rng.standard_normal((B, Hkv, prior, d))
+    for pos, alpha in ((300, 0.5), (700, 1.5), (868, 4.0), (1190, 4.0)):
+        k0[:, :, pos] = alpha * u + 0.1 * rng.standard_normal(d)
+    v0 = rng.standard_normal((B, Hkv, prior, d))
+    kn = rng.standard_normal((B, Hkv, T, d))
+    vn = rng.standard_normal((B, Hkv, T, d))
+    q = rng.standard_normal((B, Hkv * G, T, d)) + 3.0 * u
+    store = [_store(torch.from_numpy(x), torch.bfloat16) for x in (k0, v0, kn, vn, q)]
+    k0s, v0s, kns, vns, qs = store
+    cache = KVCache(1, B, Hkv, max_len, d)
+    cache.k[0].fill_(float("nan"))
+    cache.v[0].fill_(float("nan"))
+    cache.append(0, k0s.cuda(), v0s.cuda(), [prior])
+    out = cache.append_attention(0, qs.cuda(), kns.cuda(), vns.cuda(), [T])
+    orc = ref.OracleCache(1, B, Hkv, max_len, d)
+    ref.append_attention(orc, 0, np.zeros((B, Hkv * G, prior, d)), k0s.double().numpy(), v0s.double().numpy(), [prior])
+    want = ref.append_attention(orc, 0, qs.double().numpy(), kns.double().numpy(), vns.double().numpy(), [T])
+    got = out.double().cpu().numpy()
+    assert np.all(np.isfinite(got))
+    err = float(np.max(np.abs(got - want)))
+    assert err <= 2e-2, err
+    assert cache.device_status() == 0
