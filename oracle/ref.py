@@ -48,6 +48,20 @@ design notes):
   any two layers disagree.
 * Output for a padded query (t >= n_new[b]), for an empty batch, an empty
   chunk (T = 0) or an empty cache is zero.
+
+Sliding window and ring buffer (p2 "A strong answer", its last paragraph, and
+"Common mistakes"; p3 exercise 3):
+
+* With a window W >= 1, the query at absolute position p sees the keys at
+  positions a with p - W < a <= p (the lower bound j > (S - T) + i - W).
+* A ring cache keeps max_len slots; the token at position a lives in slot
+  a mod max_len, and the cache records the position stored in every slot.
+  Attention selects keys by those stored positions, never by slot index.
+  Lengths count every token appended (they may pass max_len).
+* A ring chunk must fit beside its window: n_new[b] <= max_len - W + 1
+  (else the chunk's first query would need a key already overwritten).
+  Truncation to a length n needs the keys n - W + 1 .. n - 1 still in the
+  ring (or n = 0) for the same reason.
 """
 
 from __future__ import annotations
@@ -66,7 +80,9 @@ __all__ = [
     "gqa_attention",
     "append_attention",
     "decode_causal_mask",
+    "decode_window_mask",
     "top_left_causal_mask",
+    "visible_slots",
     "kv_cache_bytes",
 ]
 
@@ -138,6 +154,28 @@ class OracleCache:
         self.k = [np.zeros(shape, dtype=np.float64) for _ in range(layers)]
         self.v = [np.zeros(shape, dtype=np.float64) for _ in range(layers)]
         self.lens = np.zeros((layers, batch), dtype=np.int64)
+        # absolute position stored in every slot (-1: never written)
+        self.pos = [np.full((batch, max_len), -1, dtype=np.int64) for _ in range(layers)]
+        self.window = 0   # 0: no window (keys 0..p)
+        self.ring = False
+
+    def set_window(self, window: int, ring: bool = False) -> None:
+        """Attention window W (0 = none) and ring storage (slot = position mod max_len).
+
+        Ring storage needs a window of 1..max_len and may only be switched
+        on or off while the cache is empty.
+        """
+        if window < 0:
+            raise CacheError("window must be >= 0")
+        if ring and not 1 <= window <= self.max_len:
+            raise CacheError("a ring cache needs a window of 1..max_len")
+        if bool(ring) != self.ring and np.any(self.lens != 0):
+            raise CacheError("ring storage can only change on an empty cache")
+        self.window, self.ring = int(window), bool(ring)
+
+    def slot_of(self, position: int) -> int:
+        """Slot holding an absolute position: the position itself, or position mod max_len in a ring."""
+        return position % self.max_len if self.ring else position
 
     # -- p1 ``KVCache.append`` / p3 ``KVCache.update`` ----------------------
     def append(self, layer: int, k_new: np.ndarray, v_new: np.ndarray, n_new) -> None:
@@ -164,12 +202,18 @@ class OracleCache:
         for b in range(self.B):
             if n_new[b] < 0 or n_new[b] > T:
                 raise CacheError(f"row {b}: n_new={n_new[b]} outside 0..{T}")
-            if lens[b] + n_new[b] > self.max_len:
+            if self.ring:
+                if n_new[b] > self.max_len - self.window + 1:
+                    raise CacheError(f"row {b}: a ring chunk of {n_new[b]} tokens does not fit beside its window")
+            elif lens[b] + n_new[b] > self.max_len:
                 raise CacheError(f"row {b}: {lens[b] + n_new[b]} tokens > max_len {self.max_len}")
         for b in range(self.B):
-            s, n = int(lens[b]), int(n_new[b])
-            self.k[layer][b, :, s : s + n] = k_new[b, :, :n]
-            self.v[layer][b, :, s : s + n] = v_new[b, :, :n]
+            for t in range(int(n_new[b])):
+                a = int(lens[b]) + t
+                slot = self.slot_of(a)
+                self.k[layer][b, :, slot] = k_new[b, :, t]
+                self.v[layer][b, :, slot] = v_new[b, :, t]
+                self.pos[layer][b, slot] = a
         self.lens[layer] = lens + n_new
 
     def lens_of(self, layer: int) -> np.ndarray:
@@ -190,6 +234,13 @@ class OracleCache:
         cur = self.length()
         if np.any(new_lens < 0) or np.any(new_lens > cur):
             raise CacheError("invalid truncation length")
+        if self.ring:
+            # Keys positions max(0, new - W + 1) .. new - 1 must still be in the
+            # ring (it holds positions cur - max_len .. cur - 1); new = 0 needs none.
+            for b in range(self.B):
+                n = int(new_lens[b])
+                if n > 0 and max(0, n - self.window + 1) < int(cur[b]) - self.max_len:
+                    raise CacheError("a ring cache cannot go back past the keys it still holds")
         self.lens[:] = new_lens[None, :]
 
     def reset(self) -> None:
@@ -198,6 +249,36 @@ class OracleCache:
     def bytes(self) -> int:
         """Bytes held by every K and V buffer (p3 ``bytes``), at 8 B a value."""
         return sum(a.nbytes for a in self.k + self.v)
+
+
+def visible_slots(stored: np.ndarray, lens_b: int, p: int, window: int) -> np.ndarray:
+    """Slots whose stored position a a query at position p may see.
+
+    a must be a written, valid position (0 <= a < lens), at most p, and with a
+    window above p - W (p2: the mask compares stored positions, never slot
+    indices, and gains the lower bound j > (S - T) + i - W).  Ascending
+    position order.
+    """
+    a = stored
+    ok = (a >= 0) & (a < lens_b) & (a <= p)
+    if window > 0:
+        ok &= a > p - window
+    slots = np.nonzero(ok)[0]
+    return slots[np.argsort(a[slots], kind="stable")]
+
+
+def attend_slots(q_vec: np.ndarray, K_rows: np.ndarray, V_rows: np.ndarray, slots: np.ndarray) -> np.ndarray:
+    """Plain softmax attention of one query over the given slots (zeros if none)."""
+    d = q_vec.shape[-1]
+    if slots.size == 0:
+        return np.zeros(d, dtype=np.float64)
+    keys = np.asarray(K_rows[slots], dtype=np.float64)
+    vals = np.asarray(V_rows[slots], dtype=np.float64)
+    s = (keys @ np.asarray(q_vec, dtype=np.float64)) * score_scale(d)
+    s = s - s.max()
+    p = np.exp(s)
+    p = p / p.sum()
+    return p @ vals
 
 
 def gqa_attention(q: np.ndarray, cache: OracleCache, layer: int, n_new) -> np.ndarray:
@@ -238,7 +319,11 @@ def gqa_attention(q: np.ndarray, cache: OracleCache, layer: int, n_new) -> np.nd
                 if t >= n_new[b]:
                     continue  # padded query slot: stays zero
                 pos = query_position(int(lens[b]), int(n_new[b]), t)
-                out[b, h, t] = attend_one_query(q[b, h, t], K_rows, V_rows, pos)
+                if cache.window == 0 and not cache.ring:
+                    out[b, h, t] = attend_one_query(q[b, h, t], K_rows, V_rows, pos)
+                else:
+                    slots = visible_slots(cache.pos[layer][b], int(lens[b]), pos, cache.window)
+                    out[b, h, t] = attend_slots(q[b, h, t], K_rows, V_rows, slots)
     return out
 
 
@@ -253,6 +338,13 @@ def decode_causal_mask(T: int, S: int) -> np.ndarray:
     q_pos = np.arange(S - T, S)[:, None]
     k_pos = np.arange(S)[None, :]
     return k_pos <= q_pos
+
+
+def decode_window_mask(T: int, S: int, W: int) -> np.ndarray:
+    """Bool [T, S] with a sliding window: (S - T) + i - W < j <= (S - T) + i (p2)."""
+    q_pos = np.arange(S - T, S)[:, None]
+    k_pos = np.arange(S)[None, :]
+    return (k_pos <= q_pos) & (k_pos > q_pos - W)
 
 
 def top_left_causal_mask(T: int, S: int) -> np.ndarray:
