@@ -119,6 +119,10 @@ class KVCache:
     def reset(self) -> None:
         check(lib().kvc_reset(self._h))
 
+    def set_window(self, window: int, ring: bool = False) -> None:
+        """Sliding window (0 = none) and ring storage (slot = position mod max_len), for every layer."""
+        check(lib().kvc_set_window(self._h, int(window), 1 if ring else 0))
+
     def kernel_launches(self) -> int:
         """Kernels this cache's handle has enqueued so far."""
         return int(lib().kvc_kernel_launches(self._h))

@@ -6,7 +6,9 @@
 // contiguous, so the copy is n_new[b] * d * elem bytes of 16-byte vectors:
 // every thread moves one uint4, consecutive threads consecutive vectors, so
 // loads and stores are fully coalesced 128-bit accesses.  blockIdx.y selects
-// (h, K or V), blockIdx.z the row b.
+// (h, K or V), blockIdx.z the row b.  In a ring cache ("Write the causal mask
+// for a decode step...", "A strong answer": a ring buffer whose physical index
+// is not the position) position a goes to slot a mod max_len.
 
 #include "kvc_internal.h"
 
@@ -31,9 +33,15 @@ __global__ void __launch_bounds__(kAppendThreads) kv_append_kernel(const __grid_
     if (vec * 16 >= bytes) return;
     const size_t unit = static_cast<size_t>(b) * p.Hkv + h;
     const uint8_t* src = (is_v ? p.v_new : p.k_new) + unit * p.T * p.row_bytes;
-    uint8_t* dst = (is_v ? p.v_cache : p.k_cache) + (unit * p.max_len + p.lens[b]) * p.row_bytes;
     const uint4 val = __ldg(reinterpret_cast<const uint4*>(src) + vec);
-    reinterpret_cast<uint4*>(dst)[vec] = val;
+    uint8_t* base = (is_v ? p.v_cache : p.k_cache) + unit * p.max_len * p.row_bytes;
+    if (!p.ring) {
+        reinterpret_cast<uint4*>(base + static_cast<size_t>(p.lens[b]) * p.row_bytes)[vec] = val;
+    } else {
+        const size_t byte = vec * 16, t = byte / p.row_bytes;
+        const size_t slot = (static_cast<size_t>(p.lens[b]) + t) % static_cast<size_t>(p.max_len);
+        *reinterpret_cast<uint4*>(base + slot * p.row_bytes + (byte - t * p.row_bytes)) = val;
+    }
 }
 
 }  // namespace

@@ -13,6 +13,11 @@
 // scores key j of the 32-key tile, the warp keeps a running max and sum
 // (online softmax) and lane e accumulates output dims e, e+32, ...  Masked
 // keys are skipped outright, so stale or NaN slots past lens never enter.
+//
+// Sliding window and ring storage ("Write the causal mask for a decode
+// step...", "A strong answer", last paragraph): with a window W the query at
+// position p sees keys p - W < a <= p, and in a ring cache key a is read from
+// slot a mod max_len; keys are chosen by position, never by slot.
 
 #include <math.h>
 
@@ -38,16 +43,19 @@ __global__ void __launch_bounds__(kWarps * 32) attn_f32_kernel(const __grid_cons
     const int d = p.d, T = p.T;
     const int prior = p.prior[b], nn = p.n_new[b];
 
-    // Row limits (largest visible key; -1 = padded / missing row) and extent.
+    // Row limits (largest visible key; -1 = padded / missing row), the keys'
+    // extent and, with a window, the first key any row of the block sees.
     int lim[4];
-    int extent = 0;
+    int extent = 0, first = 0x7fffffff;
     for (int i = 0; i < kRows; ++i) {
         const int r = row0 + i;
         int l = -1;
         if (r < p.R && (r % T) < nn) l = prior + (r % T);
         if (l + 1 > extent) extent = l + 1;
+        if (l >= 0) first = min(first, p.window > 0 ? max(0, l - p.window + 1) : 0);
         if ((i & 3) == warp) lim[i >> 2] = l;
     }
+    if (extent == 0) first = 0;
 
     // Stage the block's query rows.
     for (int idx = threadIdx.x; idx < kRows * d; idx += blockDim.x) {
@@ -70,14 +78,16 @@ __global__ void __launch_bounds__(kWarps * 32) attn_f32_kernel(const __grid_cons
     }
 
     const size_t unit_base = (static_cast<size_t>(b) * p.Hkv + kvh) * p.max_len;
-    for (int k0 = 0; k0 < extent; k0 += kKeys) {
+    for (int k0 = first; k0 < extent; k0 += kKeys) {
         __syncthreads();
         const int nk = min(kKeys, extent - k0);
         for (int idx = threadIdx.x; idx < kKeys * d / 4; idx += blockDim.x) {
             const int j = (idx * 4) / d;
             float4 kv4 = make_float4(0.f, 0.f, 0.f, 0.f), vv4 = kv4;
             if (j < nk) {
-                const size_t off = (unit_base + k0) * d + static_cast<size_t>(idx) * 4;
+                const int a = k0 + j;  // key position
+                const size_t slot = p.ring ? static_cast<size_t>(a % p.max_len) : static_cast<size_t>(a);
+                const size_t off = (unit_base + slot) * d + static_cast<size_t>(idx * 4 - j * d);
                 kv4 = *reinterpret_cast<const float4*>(p.k_cache + off);
                 vv4 = *reinterpret_cast<const float4*>(p.v_cache + off);
             }
@@ -88,11 +98,12 @@ __global__ void __launch_bounds__(kWarps * 32) attn_f32_kernel(const __grid_cons
 #pragma unroll
         for (int i = 0; i < 4; ++i) {
             const int li = lim[i];
-            if (li < k0) continue;  // row sees nothing in this tile (warp-uniform)
+            const int lo = p.window > 0 ? li - p.window : -1;  // keys <= lo are outside the window
+            if (li < k0 || lo >= k0 + nk - 1) continue;  // row sees nothing in this tile (warp-uniform)
             const float* qr = sq + (warp + 4 * i) * d;
             const int key = k0 + lane;
             float s = -INFINITY;
-            if (lane < nk && key <= li) {
+            if (lane < nk && key <= li && key > lo) {
                 float acc = 0.f;
                 const float* kr = sk + lane * d;
                 for (int e = 0; e < d; ++e) acc = fmaf(qr[e], kr[e], acc);
@@ -112,7 +123,7 @@ __global__ void __launch_bounds__(kWarps * 32) attn_f32_kernel(const __grid_cons
 #pragma unroll
             for (int c = 0; c < kMaxD / 32; ++c) o[i][c] *= alpha;
             const int jmax = min(nk, li - k0 + 1);
-            for (int j = 0; j < jmax; ++j) {
+            for (int j = max(0, lo - k0 + 1); j < jmax; ++j) {
                 const float pb = __shfl_sync(0xffffffffu, pj, j);
                 const float* vr = sv + j * d;
 #pragma unroll

@@ -95,6 +95,7 @@ template <>
 struct Part<false> {
     const DecodeParams& p;
     __device__ __forceinline__ int gstart(int i) const { return p.gstart[i]; }
+    __device__ __forceinline__ int tile0(int q) const { return p.tile0[q]; }
     __device__ __forceinline__ int prior(int b) const { return p.prior[b]; }
     __device__ __forceinline__ int n_new(int b) const { return p.n_new[b]; }
     __device__ __forceinline__ int total_tiles() const { return p.total_tiles; }
@@ -106,6 +107,7 @@ template <>
 struct Part<true> {
     const DecodeParams& p;
     __device__ __forceinline__ int gstart(int i) const { return p.dplan->gstart[i]; }
+    __device__ __forceinline__ int tile0(int q) const { return p.dplan->tile0[q]; }
     __device__ __forceinline__ int prior(int b) const { return p.dplan->prior[b]; }
     __device__ __forceinline__ int n_new(int b) const { return p.dplan->n_new[b]; }
     __device__ __forceinline__ int total_tiles() const { return p.dplan->total_tiles; }
@@ -144,6 +146,10 @@ struct Cursor {
         if (q < w.NB()) nt = (w.gstart(q + 1) - w.gstart(q)) / w.Hkv();
     }
 };
+
+// Cache slot of the key at absolute position a (ring storage: a mod max_len;
+// max_len is a multiple of the tile size there, so a tile never wraps).
+__device__ __forceinline__ int slot_of(const DecodeParams& p, int a) { return p.ring ? a % p.max_len : a; }
 
 __device__ __forceinline__ void store_bf16x4(void* dst, float a, float b, float c, float d) {
     uint2 v;
@@ -249,7 +255,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 }
                 if (*abort_flag) break;  // the producer is in no named barrier, so it may stop early
                 const int b = cur.q / p.RB;
-                const int row = (b * p.Hkv + cur.kvh) * p.max_len + cur.j * kKeyTile;
+                const int row = (b * p.Hkv + cur.kvh) * p.max_len + slot_of(p, (wp.tile0(cur.q) + cur.j) * kKeyTile);
                 const uint32_t full = bar0 + 8 * s;
                 const uint32_t sK = stage0 + s * kStageBytes;
                 stage_tag[s] = it;
@@ -290,6 +296,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     float m0 = -INFINITY, m1 = -INFINITY, l0 = 0.f, l1 = 0.f;
     uint32_t qa[8][4];
     int lim0 = -1, lim1 = -1, min_lim = 0, extent = 0, seg_j0 = 0, seg_tiles = 0;
+    // Window lower bounds (keys <= lo are outside the window): this thread's
+    // two rows, and the largest and smallest over the block's valid rows.
+    int lo0 = -1, lo1 = -1, max_lo = -1, min_lo = -1;
     int seg_prior = 0, seg_nn = 0;
     uint4 new_row0 = make_uint4(0u, 0u, 0u, 0u);  // first appended row, lane's 16-byte chunk (K: lanes 0-15, V: 16-31)
 
@@ -312,6 +321,9 @@ __global__ void __launch_bounds__(kThreads, 1)
                     extent = max(extent, prior + t + 1);
                 }
             }
+            // With a window the block's rows see keys lim - W < a <= lim.
+            max_lo = (p.window > 0 && extent > 0) ? extent - 1 - p.window : -1;
+            min_lo = (p.window > 0 && extent > 0) ? min_lim - p.window : -1;
             seg_j0 = j;
             seg_tiles = 0;
             seg_prior = prior;
@@ -333,6 +345,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                            ((static_cast<size_t>(b) * p.Hq + kvh * p.G + g) * p.T + t) * kD;
                 }
                 if (h == 0) lim0 = lim; else lim1 = lim;
+                const int lo = (p.window > 0 && lim >= 0) ? lim - p.window : -1;
+                if (h == 0) lo0 = lo; else lo1 = lo;
 #pragma unroll
                 for (int kk = 0; kk < 8; ++kk) {
                     qa[kk][h] = qrow ? *reinterpret_cast<const uint32_t*>(qrow + 16 * kk + 2 * quad) : 0u;
@@ -370,7 +384,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 
             const uint32_t sK = stage0 + s * kStageBytes;
             const uint32_t sV = sK + kTileBytes;
-            const int tile0 = j * kKeyTile;
+            const int tile0 = (wp.tile0(cur.q) + j) * kKeyTile;  // first key position of the tile
 
             if (S::kTilePar && p.append_new) {
                 // In-kernel append: rows prior .. prior+n_new-1 of this unit that
@@ -384,13 +398,14 @@ __global__ void __launch_bounds__(kThreads, 1)
                     const size_t unit = static_cast<size_t>(b) * p.Hkv + kvh;
                     const uint8_t* src = static_cast<const uint8_t*>(is_v ? p.v_new : p.k_new) + unit * p.Tn * (kD * 2);
                     uint8_t* dst = static_cast<uint8_t*>(is_v ? p.v_cache : p.k_cache) + unit * p.max_len * (kD * 2);
+                    const int slot_shift = slot_of(p, tile0) - tile0;  // ring: the tile's slots are contiguous
                     uint8_t* stg = stages + s * kStageBytes + (is_v ? kTileBytes : 0) + (chunk >> 3) * kHalfBytes;
                     for (int pos = lo; pos < hi; ++pos) {
                         const int t = pos - seg_prior, r = pos - tile0;
                         const uint4 val = (t == 0) ? new_row0
                                                    : __ldg(reinterpret_cast<const uint4*>(src + t * (kD * 2) + chunk * 16));
                         *reinterpret_cast<uint4*>(stg + r * 128 + (((chunk & 7) ^ (r & 7)) << 4)) = val;
-                        *reinterpret_cast<uint4*>(dst + static_cast<size_t>(pos) * (kD * 2) + chunk * 16) = val;
+                        *reinterpret_cast<uint4*>(dst + static_cast<size_t>(pos + slot_shift) * (kD * 2) + chunk * 16) = val;
                     }
                     ptx::fence_proxy_async_smem();
                     __syncwarp();
@@ -413,7 +428,23 @@ __global__ void __launch_bounds__(kThreads, 1)
                 ptx::fence_proxy_async_smem();
                 if (S::kTilePar) __syncwarp(); else ptx::named_barrier_sync(1, kConsumerThreads);
             }
-            const bool full_tile = (tile0 + kKeyTile - 1 <= min_lim);
+            if (tile0 <= min_lo) {
+                // Clear V rows outside every row's window as well (a stale slot
+                // must never meet p = 0).
+                const int vr1 = min(kKeyTile, min_lo - tile0 + 1);
+                const int per_half = vr1 * 8;
+                uint8_t* vbase = stages + s * kStageBytes + kTileBytes;
+                const int t0 = S::kTilePar ? lane : tid;
+                const int step = S::kTilePar ? 32 : kConsumerThreads;
+                for (int idx = t0; idx < 2 * per_half; idx += step) {
+                    const int hf = idx / per_half, rem = idx - hf * per_half;
+                    *reinterpret_cast<uint4*>(vbase + hf * kHalfBytes + (rem >> 3) * 128 + (rem & 7) * 16) =
+                        make_uint4(0u, 0u, 0u, 0u);
+                }
+                ptx::fence_proxy_async_smem();
+                if (S::kTilePar) __syncwarp(); else ptx::named_barrier_sync(1, kConsumerThreads);
+            }
+            const bool full_tile = (tile0 + kKeyTile - 1 <= min_lim) && (tile0 > max_lo);
 
             // S = Q K^T for this warp's 16 rows x KW keys.
             float sc[NBS][4];
@@ -444,7 +475,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     float v = sc[nb][e] * p.scale_log2;
                     if (!full_tile) {
                         const int key = kbase + nb * 8 + (e & 1);
-                        if (key > ((e < 2) ? lim0 : lim1)) v = -INFINITY;
+                        if (key > ((e < 2) ? lim0 : lim1) || key <= ((e < 2) ? lo0 : lo1)) v = -INFINITY;
                     }
                     sc[nb][e] = v;
                 }
@@ -748,7 +779,9 @@ __global__ void __launch_bounds__(kPlanThreads) decode_plan_kernel(const __grid_
     int bad = 0;
     for (int b = tid; b < p.B; b += kPlanThreads) {
         const int L = p.lens[b], n = p.n_new[b];
-        bad |= (L < 0 || n < 0 || n > p.T || L > p.max_len - n) ? 1 : 0;
+        const bool room = p.ring ? (n <= p.max_len - p.window + 1 && L <= 0x7fffffff - p.max_len - n)
+                                 : (L <= p.max_len - n);
+        bad |= (L < 0 || n < 0 || n > p.T || !room) ? 1 : 0;
     }
     if (__syncthreads_or(bad)) {
         if (tid == 0) {
@@ -763,23 +796,31 @@ __global__ void __launch_bounds__(kPlanThreads) decode_plan_kernel(const __grid_
         plan->prior[b] = p.lens[b];
         plan->n_new[b] = p.n_new[b];
     }
-    // Tiles of group q = b * RB + rb: Hkv units of ceil(extent / 64) tiles,
-    // extent = one past the largest visible key of the block's valid rows.
-    int tiles = 0;
+    // Tiles of group q = b * RB + rb: Hkv units over the key tiles from the
+    // window of the block's earliest query to one past its largest visible key.
+    int tiles = 0, first_tile = 0;
     if (tid < p.NB) {
         const int b = tid / p.RB, rb = tid - b * p.RB;
         const int prior = p.lens[b], n = p.n_new[b];
         const int r0 = rb * p.RPB, r1 = min(p.R, r0 + p.RPB);
-        int extent = 0;
+        int extent = 0, qmin = 0x7fffffff;
         if (r1 - r0 >= p.T) {
-            if (n > 0) extent = prior + min(p.T, n);
+            if (n > 0) {
+                extent = prior + min(p.T, n);
+                qmin = prior;
+            }
         } else {
             for (int r = r0; r < r1; ++r) {
                 const int t = r % p.T;
-                if (t < n) extent = max(extent, prior + t + 1);
+                if (t < n) {
+                    extent = max(extent, prior + t + 1);
+                    qmin = min(qmin, prior + t);
+                }
             }
         }
-        tiles = (extent + kKeyTile - 1) / kKeyTile * p.Hkv;
+        const int kfirst = (extent > 0 && p.window > 0) ? max(0, qmin - p.window + 1) : 0;
+        first_tile = kfirst / kKeyTile;
+        tiles = extent > 0 ? ((extent - 1) / kKeyTile + 1 - first_tile) * p.Hkv : 0;
     }
     // Block-wide exclusive scan of the group tile counts.
     __shared__ int warp_sum[kPlanThreads / 32];
@@ -803,7 +844,10 @@ __global__ void __launch_bounds__(kPlanThreads) decode_plan_kernel(const __grid_
     __syncthreads();
     const int excl = incl - tiles + (warp > 0 ? warp_sum[warp - 1] : 0);
     const int total = warp_sum[kPlanThreads / 32 - 1];
-    if (tid < p.NB) plan->gstart[tid] = excl;
+    if (tid < p.NB) {
+        plan->gstart[tid] = excl;
+        plan->tile0[tid] = first_tile;
+    }
     if (tid == 0) {
         plan->gstart[p.NB] = total;
         plan->total_tiles = total;

@@ -45,6 +45,9 @@ struct kvc_cache {
     // graph-capturable steps owns them; the host copy is stale meanwhile.
     int32_t* dev_lens = nullptr;
     bool lens_on_device = false;
+    // Sliding window (0 = none) and ring storage (slot = position mod max_len).
+    int window = 0;
+    bool ring = false;
 };
 
 namespace {
@@ -154,9 +157,18 @@ kvc_status validate_append(const kvc_cache* c, int layer, const void* k_new, con
         mx = std::max(mx, static_cast<int>(n_new[b]));
     }
     for (int b = 0; b < c->B; ++b) {
-        if (lens[b] + n_new[b] > c->max_len)
+        if (c->ring) {
+            // A ring chunk must fit beside its window: its first query still
+            // needs the window - 1 keys before it.
+            if (n_new[b] > c->max_len - c->window + 1)
+                return fail(KVC_ERR_OVERFLOW, "row %d: a ring chunk of %d tokens does not fit beside a window of %d in %d slots",
+                            b, n_new[b], c->window, c->max_len);
+            if (lens[b] + n_new[b] > 0x7fffffffll - c->max_len)
+                return fail(KVC_ERR_OVERFLOW, "row %d: position count past the int32 range", b);
+        } else if (lens[b] + n_new[b] > c->max_len) {
             return fail(KVC_ERR_OVERFLOW, "row %d: %lld tokens > max_len %d", b,
                         static_cast<long long>(lens[b] + n_new[b]), c->max_len);
+        }
     }
     if (mx > 0) {
         if (!k_new || !v_new) return fail(KVC_ERR_ARG, "k_new / v_new is null");
@@ -253,6 +265,7 @@ kvc_status do_append(kvc_cache* c, int layer, const void* k_new, const void* v_n
     p.T = T;
     p.max_len = c->max_len;
     p.row_bytes = c->d * c->esize;
+    p.ring = c->ring ? 1 : 0;
     const int64_t* lens = c->lens.data() + static_cast<size_t>(layer) * c->B;
     for (int b = 0; b < c->B; ++b) {
         p.lens[b] = static_cast<int>(lens[b]);
@@ -288,6 +301,8 @@ kvc_status do_attention(kvc_cache* c, int layer, const void* q, const AttnPlan& 
         p.max_len = c->max_len;
         p.d = c->d;
         p.R = pl.R;
+        p.window = c->window;
+        p.ring = c->ring ? 1 : 0;
         p.scale = 1.0f / sqrtf(static_cast<float>(c->d));
         for (int b = 0; b < c->B; ++b) {
             p.prior[b] = static_cast<int>(lens[b] - n_new[b]);
@@ -315,7 +330,7 @@ kvc_status do_attention(kvc_cache* c, int layer, const void* q, const AttnPlan& 
         // from HBM about once and then hit in L2.
         static_assert(sizeof(PrefillParams) < 32000, "kernel parameter block too large");
         struct WorkItem {
-            int code, nkt, nh;
+            int code, kt0, nkt, nh;  // key tiles kt0 .. nkt - 1 (absolute position / 128)
         };
         std::vector<WorkItem> items;
         PrefillParams pp;
@@ -331,6 +346,8 @@ kvc_status do_attention(kvc_cache* c, int layer, const void* q, const AttnPlan& 
         pp.max_len = c->max_len;
         pp.ntb = (pl.T + 127) / 128;
         pp.npair = (pl.G + 1) / 2;
+        pp.window = c->window;
+        pp.ring = c->ring ? 1 : 0;
         pp.scale_log2 = static_cast<float>(1.4426950408889634 / sqrt(static_cast<double>(c->d)));
         for (int b = 0; b < c->B; ++b) {
             pp.prior[b] = static_cast<int>(lens[b] - n_new[b]);
@@ -340,9 +357,11 @@ kvc_status do_attention(kvc_cache* c, int layer, const void* q, const AttnPlan& 
                     const int t0 = tb * 128;
                     if (t0 >= n_new[b]) continue;
                     const int kmax = pp.prior[b] + std::min(t0 + 127, static_cast<int>(n_new[b]) - 1);
+                    // First key any query of the block sees: its first query's window start.
+                    const int kfirst = c->window > 0 ? std::max(0, pp.prior[b] + t0 - c->window + 1) : 0;
                     for (int pr = 0; pr < pp.npair; ++pr) {
                         const int code = ((b * c->Hkv + kvh) * pp.ntb + tb) * pp.npair + pr;
-                        items.push_back({code, kmax / 128 + 1, std::min(2, pl.G - 2 * pr)});
+                        items.push_back({code, kfirst / 128, kmax / 128 + 1, std::min(2, pl.G - 2 * pr)});
                     }
                 }
         }
@@ -373,7 +392,8 @@ kvc_status do_attention(kvc_cache* c, int layer, const void* q, const AttnPlan& 
                 constexpr long long kStartCost = KVC_PF_START_COST;  // per-CTA start-up, in tile x head units
                 constexpr int kMinPieceTiles = KVC_PF_MIN_PIECE;
                 long long W = 0;
-                for (size_t k = i0; k < i1; ++k) W += static_cast<long long>(items[k].nkt) * items[k].nh + kStartCost;
+                for (size_t k = i0; k < i1; ++k)
+                    W += static_cast<long long>(items[k].nkt - items[k].kt0) * items[k].nh + kStartCost;
                 const long long target = W / nsm + kStartCost;  // the SMs' common finishing time
                 // Remaining parts of items, longest first (ties: item order).
                 struct Part {
@@ -384,7 +404,7 @@ kvc_status do_attention(kvc_cache* c, int layer, const void* q, const AttnPlan& 
                 std::priority_queue<Part> parts;
                 for (int k = 0; k < n_items; ++k) {
                     const WorkItem& it = items[i0 + k];
-                    parts.push({static_cast<long long>(it.nkt) * it.nh, k, 0});
+                    parts.push({static_cast<long long>(it.nkt - it.kt0) * it.nh, k, it.kt0});
                 }
                 using Sm = std::pair<long long, int>;  // (busy until, SM)
                 std::priority_queue<Sm, std::vector<Sm>, std::greater<Sm>> sms;
@@ -478,6 +498,8 @@ kvc_status do_attention(kvc_cache* c, int layer, const void* q, const AttnPlan& 
     p.k_cache = c->k[layer];
     p.v_cache = c->v[layer];
     p.Tn = pl.T;
+    p.window = c->window;
+    p.ring = c->ring ? 1 : 0;
     p.scale_log2 = static_cast<float>(1.4426950408889634 / sqrt(static_cast<double>(c->d)));
     long long tiles = 0;
     for (int b = 0; b < c->B; ++b) {
@@ -486,19 +508,31 @@ kvc_status do_attention(kvc_cache* c, int layer, const void* q, const AttnPlan& 
     }
     for (int b = 0; b < c->B; ++b) {
         for (int rb = 0; rb < pl.RB; ++rb) {
-            // Extent of the row block: one past the largest visible key of its valid rows.
-            int extent = 0;
+            // Extent of the row block: one past the largest visible key of its
+            // valid rows; with a window its keys start at the window of its
+            // earliest query (tiles before that are never scheduled).
+            int extent = 0, qmin = 0x7fffffff;
             const int r0 = rb * pl.RPB, r1 = std::min(pl.R, r0 + pl.RPB);
             if (r1 - r0 >= pl.T) {
-                if (n_new[b] > 0) extent = p.prior[b] + std::min(pl.T, static_cast<int>(n_new[b]));
+                if (n_new[b] > 0) {
+                    extent = p.prior[b] + std::min(pl.T, static_cast<int>(n_new[b]));
+                    qmin = p.prior[b];
+                }
             } else {
                 for (int r = r0; r < r1; ++r) {
                     const int t = r % pl.T;
-                    if (t < n_new[b]) extent = std::max(extent, p.prior[b] + t + 1);
+                    if (t < n_new[b]) {
+                        extent = std::max(extent, p.prior[b] + t + 1);
+                        qmin = std::min(qmin, p.prior[b] + t);
+                    }
                 }
             }
+            const int kfirst = (extent > 0 && c->window > 0) ? std::max(0, qmin - c->window + 1) : 0;
+            const int first_tile = kfirst / kKeyTile;
+            const int ntiles = extent > 0 ? (extent - 1) / kKeyTile + 1 - first_tile : 0;
             p.gstart[b * pl.RB + rb] = static_cast<int>(tiles);
-            tiles += static_cast<long long>((extent + kKeyTile - 1) / kKeyTile) * c->Hkv;
+            p.tile0[b * pl.RB + rb] = first_tile;
+            tiles += static_cast<long long>(ntiles) * c->Hkv;
         }
     }
     if (tiles > 0x7fffffffll) return fail(KVC_ERR_ARG, "too many key tiles in one call");
@@ -769,10 +803,18 @@ kvc_status kvc_truncate(kvc_cache* c, const int64_t* new_lens) {
     std::vector<int64_t> cur(c->B);
     kvc_status s = kvc_length(c, cur.data());
     if (s) return s;
-    for (int b = 0; b < c->B; ++b)
+    for (int b = 0; b < c->B; ++b) {
         if (new_lens[b] < 0 || new_lens[b] > cur[b])
             return fail(KVC_ERR_ARG, "row %d: invalid truncation length %lld (length %lld)", b,
                         static_cast<long long>(new_lens[b]), static_cast<long long>(cur[b]));
+        // A ring still holds positions cur - max_len .. cur - 1; the keys a
+        // query after the truncation may need, new - window + 1 .. new - 1,
+        // must be among them (nothing is needed after a truncation to 0).
+        if (c->ring && new_lens[b] > 0 &&
+            std::max<int64_t>(0, new_lens[b] - c->window + 1) < cur[b] - c->max_len)
+            return fail(KVC_ERR_ARG, "row %d: a ring cache cannot go back to %lld from %lld", b,
+                        static_cast<long long>(new_lens[b]), static_cast<long long>(cur[b]));
+    }
     for (int l = 0; l < c->layers; ++l)
         for (int b = 0; b < c->B; ++b) c->lens[static_cast<size_t>(l) * c->B + b] = new_lens[b];
     return ok();
@@ -792,10 +834,11 @@ kvc_status kvc_set_lens(kvc_cache* c, int layer, const int64_t* lens) {
     kvc_status s = check_layer(c, layer);
     if (s) return s;
     if (!lens && c->B > 0) return fail(KVC_ERR_ARG, "lens is null");
+    const int64_t top = c->ring ? 0x7fffffffll - c->max_len : c->max_len;  // a ring counts every position
     for (int b = 0; b < c->B; ++b)
-        if (lens[b] < 0 || lens[b] > c->max_len)
-            return fail(KVC_ERR_ARG, "row %d: length %lld outside 0..%d", b, static_cast<long long>(lens[b]),
-                        c->max_len);
+        if (lens[b] < 0 || lens[b] > top)
+            return fail(KVC_ERR_ARG, "row %d: length %lld outside 0..%lld", b, static_cast<long long>(lens[b]),
+                        static_cast<long long>(top));
     for (int b = 0; b < c->B; ++b) c->lens[static_cast<size_t>(layer) * c->B + b] = lens[b];
     return ok();
 }
@@ -839,6 +882,25 @@ kvc_status kvc_selftest_bounded_wait(void* workspace, uint64_t limit_ns, void* s
     return ok();
 }
 
+kvc_status kvc_set_window(kvc_cache* c, int window, int ring) {
+    if (!c) return fail(KVC_ERR_ARG, "null cache handle");
+    kvc_status s = check_host_lens(c);
+    if (s) return s;
+    if (window < 0) return fail(KVC_ERR_ARG, "window = %d < 0", window);
+    if (ring != 0 && ring != 1) return fail(KVC_ERR_ARG, "ring must be 0 or 1");
+    if (ring) {
+        if (window < 1 || window > c->max_len) return fail(KVC_ERR_ARG, "a ring cache needs a window of 1..max_len");
+        if (c->dtype == KVC_BF16 && c->max_len % 128 != 0)
+            return fail(KVC_ERR_ARG, "a bf16 ring cache needs max_len %% 128 == 0 (key tiles never wrap)");
+    }
+    if ((ring != 0) != c->ring)
+        for (int64_t L : c->lens)
+            if (L != 0) return fail(KVC_ERR_ARG, "ring storage can only change on an empty cache");
+    c->window = window;
+    c->ring = ring != 0;
+    return ok();
+}
+
 size_t kvc_device_lens_bytes(const kvc_cache* c) {
     return c ? static_cast<size_t>(c->layers) * c->B * sizeof(int32_t) : 0;
 }
@@ -873,10 +935,11 @@ kvc_status kvc_lens_from_device(kvc_cache* c, void* stream) {
         if (e == cudaSuccess) e = cudaStreamSynchronize(st);
         if (e != cudaSuccess) return cuda_fail(e, "copying the lengths from the device");
     }
+    const int64_t top = c->ring ? 0x7fffffffll - c->max_len : c->max_len;
     for (size_t i = 0; i < h.size(); ++i)
-        if (h[i] < 0 || h[i] > c->max_len)
-            return fail(KVC_ERR_ARG, "device length %d of slot %zu is outside 0..%d (left on the device)", h[i], i,
-                        c->max_len);
+        if (h[i] < 0 || h[i] > top)
+            return fail(KVC_ERR_ARG, "device length %d of slot %zu is outside 0..%lld (left on the device)", h[i], i,
+                        static_cast<long long>(top));
     for (size_t i = 0; i < h.size(); ++i) c->lens[i] = h[i];
     c->lens_on_device = false;
     c->dev_lens = nullptr;
@@ -934,6 +997,8 @@ kvc_status kvc_decode_step(kvc_cache* c, int layer, const void* q, const void* k
     pp.Hkv = c->Hkv;
     pp.num_ctas = grid;
     pp.max_len = c->max_len;
+    pp.window = c->window;
+    pp.ring = c->ring ? 1 : 0;
     cudaError_t e = launch_decode_plan(pp, st);
     if (e != cudaSuccess) return cuda_fail(e, "device plan launch");
     ++c->launches;
@@ -964,6 +1029,8 @@ kvc_status kvc_decode_step(kvc_cache* c, int layer, const void* q, const void* k
     p.k_cache = c->k[layer];
     p.v_cache = c->v[layer];
     p.Tn = T;
+    p.window = c->window;
+    p.ring = c->ring ? 1 : 0;
     e = launch_decode_bf16(p, c->tmK[layer], c->tmV[layer], 1, grid, st);
     if (e != cudaSuccess) return cuda_fail(e, "split-KV attention launch");
     ++c->launches;

@@ -27,6 +27,7 @@ struct AppendParams {
     uint8_t* v_cache;
     int B, Hkv, T, max_len;
     int row_bytes;  // d * element size, a multiple of 16
+    int ring;       // slots are positions mod max_len
     int lens[kMaxBatch];
     int n_new[kMaxBatch];
 };
@@ -60,6 +61,7 @@ struct DevicePlan {
     int prior[kMaxBatch];
     int n_new[kMaxBatch];
     int gstart[kMaxGroups + 1];
+    int tile0[kMaxGroups];
     int cta_start[kMaxCtas + 1];
 };
 
@@ -69,6 +71,7 @@ struct PlanParams {
     DevicePlan* plan;
     int* err;
     int B, T, R, RPB, RB, NB, Hkv, num_ctas, max_len;
+    int window, ring;
 };
 
 cudaError_t launch_decode_plan(const PlanParams& p, cudaStream_t stream);
@@ -96,9 +99,13 @@ struct DecodeParams {
     void* v_cache;
     int append_new;
     int Tn;
+    // Sliding window (0 = none): a query at position p sees keys p - window < a <= p.
+    // Ring storage: the key at position a lives in slot a mod max_len.
+    int window, ring;
     int prior[kMaxBatch];    // lens[b] - n_new[b]
     int n_new[kMaxBatch];
     int gstart[kMaxGroups + 1];
+    int tile0[kMaxGroups];   // first key tile (absolute position / 64) of group q's units
 };
 
 // Log-sum-exp merge of the units the attention kernel left as partials (one
@@ -143,6 +150,7 @@ struct F32Params {
     float* out;
     int B, Hq, Hkv, G, T, max_len, d;
     int R;
+    int window, ring;  // sliding window (0 = none) and ring storage, as in DecodeParams
     float scale;  // 1 / sqrt(d)
     int prior[kMaxBatch];
     int n_new[kMaxBatch];
@@ -170,6 +178,7 @@ struct PrefillParams {
     float* partials;  // [slot][2 heads][128 rows][d + 4]: O (d), m, l, pad
     int B, Hq, Hkv, G, T, max_len;
     int ntb, npair, n_pieces;
+    int window, ring;  // sliding window (0 = none) and ring storage, as in DecodeParams
     float scale_log2;
     int prior[kMaxBatch];
     int n_new[kMaxBatch];

@@ -33,6 +33,12 @@
 // visible to every row of the block skip the mask; the rest mask per element
 // with a select.  V rows past the last visible key are cleared in shared
 // memory before PV, so stale or NaN cache slots never meet p = 0.
+// Sliding window and ring storage (same page, "A strong answer", last
+// paragraph): with a window W a row sees keys lim - W < a <= lim, tiles before
+// the window of the block's first query are never loaded, tiles fully inside
+// every row's window skip the mask, and V rows outside every row's window are
+// cleared too; in a ring cache key a lives in slot a mod max_len (max_len a
+// multiple of 128, so a tile never wraps).
 // Every wait is bounded in time; on expiry an error code is recorded.
 
 #include <math.h>
@@ -281,6 +287,9 @@ __device__ __noinline__ void split_epilogue(float* partials, int* err, uint32_t 
     }
 }
 
+// kWin: the cache has a sliding window (and possibly ring storage); without
+// one the window code is compiled out.
+template <bool kWin>
 __global__ void __launch_bounds__(kThreadsPF, 1)
     prefill_tc_kernel(const __grid_constant__ PrefillParams p, const __grid_constant__ CUtensorMap tmQ,
                       const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmV) {
@@ -346,6 +355,11 @@ __global__ void __launch_bounds__(kThreadsPF, 1)
     const int kmax = pc.kmax, nkt_all = pc.nkt_all, kt0 = pc.kt0, nkt = pc.nkt;
     const int full_below = prior + t0;                      // keys <= this are visible to every row
     const int unit_row0 = (b * p.Hkv + kvh) * p.max_len;    // first cache row of (b, kvh)
+    // Window bounds of the block's rows: keys <= min_lo are outside every row's
+    // window, keys > max_lo inside every row's window (-1: no window).
+    const int min_lo = kWin ? full_below - p.window : -1;
+    const int max_lo = kWin ? kmax - p.window : -1;
+    auto slot_row = [&](int kt) { return unit_row0 + ((kWin && p.ring) ? (kt * 128) % p.max_len : kt * 128); };
 
     if (warp == 0) {
         // ------------------------------------------------------------ TMA producer
@@ -358,7 +372,7 @@ __global__ void __launch_bounds__(kThreadsPF, 1)
             }
             for (int j = 0; j < nkt && !*abort_flag; ++j) {
                 const int s = j & 1;
-                const int row = unit_row0 + (kt0 + j) * 128;
+                const int row = slot_row(kt0 + j);
                 if (j >= 2 && !ptx::mbar_wait_bounded(bar(kBarKEmpty + s), ((j >> 1) & 1) ^ 1, kWaitNs)) {
                     atomicExch(p.err, kDevTimeoutEmpty);
                     *abort_flag = 1;
@@ -419,14 +433,18 @@ __global__ void __launch_bounds__(kThreadsPF, 1)
             // before the PV MMAs read the stage.
             if (lane == 0) wait(kBarVFull + s, (j >> 1) & 1);
             __syncwarp();
-            if (kt0 + j == nkt_all - 1) {
-                const int vr0 = kmax - (kt0 + j) * 128 + 1;  // first row to clear, 1..128
+            const int key0 = (kt0 + j) * 128;
+            if (kt0 + j == nkt_all - 1 || (kWin && key0 <= min_lo)) {
+                // rows [0, vr1) are outside every row's window, rows [vr0, 128)
+                // past the last visible key
+                const int vr0 = min(128, kmax - key0 + 1), vr1 = max(0, min(128, min_lo - key0 + 1));
                 uint8_t* vb = smem + kOffV + s * kTile128;
+                const int per_hi = (128 - vr0) * 8, per_lo = vr1 * 8;
 #pragma unroll 1
-                for (int idx = lane; idx < 2 * (128 - vr0) * 8; idx += 32) {
-                    const int per = (128 - vr0) * 8;
-                    const int hf = idx / per, rem = idx - hf * per;
-                    *reinterpret_cast<uint4*>(vb + hf * kBoxBytes + (vr0 + (rem >> 3)) * 128 + (rem & 7) * 16) =
+                for (int idx = lane; idx < 2 * (per_hi + per_lo); idx += 32) {
+                    const int hf = idx / (per_hi + per_lo), rem = idx - hf * (per_hi + per_lo);
+                    const int row = rem < per_lo ? (rem >> 3) : vr0 + ((rem - per_lo) >> 3);
+                    *reinterpret_cast<uint4*>(vb + hf * kBoxBytes + row * 128 + (rem & 7) * 16) =
                         make_uint4(0u, 0u, 0u, 0u);
                 }
                 ptx::fence_proxy_async_smem();
@@ -464,6 +482,7 @@ __global__ void __launch_bounds__(kThreadsPF, 1)
             const int t = t0 + r;
             const bool valid = (t < nn) && (t < p.T);
             const int lim = valid ? prior + t : -1;
+            const int lo_row = (kWin && valid) ? lim - p.window : -(1 << 30);  // keys <= lo_row: outside the window
             float m_ref = -INFINITY, l = 0.f;
             for (int j = 0; j < nkt; ++j) {
                 if (!ptx::mbar_wait_bounded(bar(kBarS + i), j & 1, *abort_flag ? 0ull : kWaitNs)) {
@@ -471,7 +490,7 @@ __global__ void __launch_bounds__(kThreadsPF, 1)
                     *abort_flag = 1;
                 }
                 tc_fence_after();
-                const bool full_tile = ((kt0 + j) * 128 + 127 <= full_below);
+                const bool full_tile = ((kt0 + j) * 128 + 127 <= full_below) && (!kWin || (kt0 + j) * 128 > max_lo);
                 const int key0 = (kt0 + j) * 128;
                 // pass 1: row max of the raw scores (scale > 0, so it scales after);
                 // 64 columns per TMEM load, one wait each
@@ -485,10 +504,11 @@ __global__ void __launch_bounds__(kThreadsPF, 1)
 #pragma unroll
                         for (int e = 0; e < 64; e += 2) mx = fmax3(mx, __uint_as_float(v[e]), __uint_as_float(v[e + 1]));
                     } else {
-                        const int kl = lim - key0 - c * 64;  // elements e <= kl are visible
+                        const int kl = lim - key0 - c * 64;    // elements e <= kl are visible
+                        const int kll = kWin ? lo_row - key0 - c * 64 : -1;  // ... and e > kll (the window)
 #pragma unroll
                         for (int e = 0; e < 64; ++e)
-                            if (e <= kl) mx = fmaxf(mx, __uint_as_float(v[e]));
+                            if (e <= kl && e > kll) mx = fmaxf(mx, __uint_as_float(v[e]));
                     }
                 }
                 mx = (mx == -INFINITY) ? -INFINITY : mx * p.scale_log2;
@@ -533,14 +553,15 @@ __global__ void __launch_bounds__(kThreadsPF, 1)
                     tmem_ld64(tS + c * 64, v);
                     tmem_ld_wait();
                     const int kl = full_tile ? 1 << 30 : lim - key0 - c * 64;
+                    const int kll = (full_tile || !kWin) ? -1 : lo_row - key0 - c * 64;
 #pragma unroll
                     for (int e = 0; e < 64; e += 2) {
                         float x0, x1;
                         f2unpack(ffma2(f2pack(__uint_as_float(v[e]), __uint_as_float(v[e + 1])), sc2, nmu2), x0, x1);
                         float p0 = ptx::ex2(x0), p1 = ptx::ex2(x1);
                         if (!full_tile) {
-                            if (e > kl) p0 = 0.f;
-                            if (e + 1 > kl) p1 = 0.f;
+                            if (e > kl || e <= kll) p0 = 0.f;
+                            if (e + 1 > kl || e + 1 <= kll) p1 = 0.f;
                         }
                         sum2 = fadd2(sum2, f2pack(p0, p1));
                         pk[e >> 1] = ptx::pack_bf16x2(p0, p1);
@@ -607,9 +628,11 @@ cudaError_t launch_prefill_tc(const PrefillParams& p, const CUtensorMap& tmQ, co
                               const CUtensorMap& tmV, cudaStream_t stream) {
     static bool attr_set = false;
     if (!attr_set) {
-        cudaError_t e = cudaFuncSetAttribute(prefill_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                             static_cast<int>(kSmemPF));
-        if (e != cudaSuccess) return e;
+        for (auto* k : {prefill_tc_kernel<false>, prefill_tc_kernel<true>}) {
+            cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                                 static_cast<int>(kSmemPF));
+            if (e != cudaSuccess) return e;
+        }
         attr_set = true;
     }
     cudaLaunchConfig_t cfg = {};
@@ -622,7 +645,8 @@ cudaError_t launch_prefill_tc(const PrefillParams& p, const CUtensorMap& tmQ, co
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    cudaError_t e = cudaLaunchKernelEx(&cfg, prefill_tc_kernel, p, tmQ, tmK, tmV);
+    cudaError_t e = (p.window > 0 || p.ring) ? cudaLaunchKernelEx(&cfg, prefill_tc_kernel<true>, p, tmQ, tmK, tmV)
+                                              : cudaLaunchKernelEx(&cfg, prefill_tc_kernel<false>, p, tmQ, tmK, tmV);
     if (e != cudaSuccess) return e;
     return cudaGetLastError();
 }

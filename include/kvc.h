@@ -157,6 +157,25 @@ kvc_status kvc_append_attention(kvc_cache* c, int layer, const void* q, const vo
 kvc_status kvc_gqa_attention_noalloc(kvc_cache* c, int layer, const void* q, int q_heads, int T,
                                      const int32_t* n_new, void* out, void* stream);
 
+/* Sliding window and ring storage ("Write the causal mask for a decode step
+ * with a KV cache...", "A strong answer", last paragraph, and "Common
+ * mistakes"; "16. Prefill, decode and the KV cache", exercise 3).
+ *
+ * window > 0: the query at absolute position p attends only to the keys at
+ * positions a with p - window < a <= p (window = 0: all keys 0..p).
+ * ring = 1: the cache is a ring of max_len slots per (row, KV head); the key
+ * at position a lives in slot a mod max_len, and keys are chosen by position,
+ * never by slot.  Lengths then count every token appended and may pass
+ * max_len; each call's n_new[b] must be <= max_len - window + 1 (so the
+ * chunk's first query still finds its window; else KVC_ERR_OVERFLOW), and
+ * kvc_truncate may only go back to a length n whose window keys
+ * n - window + 1 .. n - 1 are still stored (or to 0).
+ * Requirements: ring needs 1 <= window <= max_len and, for bf16 caches,
+ * max_len % 128 == 0; ring storage changes only while every length is 0.
+ * Applies to every layer and to every later call (including
+ * kvc_decode_step).  Host only.  KVC_ERR_ARG otherwise. */
+kvc_status kvc_set_window(kvc_cache* c, int window, int ring);
+
 /* Forget everything after new_lens[b] tokens of row b in every layer
  * ("Layout and validity", truncate; speculative-decoding rollback).  No data
  * moves.  Requires the layers to agree (else KVC_ERR_LAYER_MISMATCH) and

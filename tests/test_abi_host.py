@@ -200,3 +200,28 @@ def test_device_lens_calls_without_device_state(L):
     assert L.kvc_lens_to_device(h, None, None) == 1  # null array
     L.kvc_destroy(h)
     assert L.kvc_device_lens_bytes(None) == 0
+
+
+def test_window_and_ring_host_rules(L):
+    st, h = _create(L, layers=2, B=2, max_len=16, dtype=_lib.KVC_F32)
+    assert L.kvc_set_window(h, -1, 0) == 1
+    assert L.kvc_set_window(h, 0, 1) == 1    # a ring needs a window
+    assert L.kvc_set_window(h, 17, 1) == 1   # window past max_len
+    assert L.kvc_set_window(h, 5, 1) == 0
+    kn = ctypes.c_void_p(1 << 41)
+    _, p = _i32(13, 0)
+    assert L.kvc_append(h, 0, kn, kn, 13, p, None) == 3  # 13 > 16 - 5 + 1
+    _, big = _i64(40, 3)
+    for layer in range(2):
+        assert L.kvc_set_lens(h, layer, big) == 0       # a ring counts every position
+    _, p = _i64(27, 3)
+    assert L.kvc_truncate(h, p) == 1  # would need key 23; the ring holds 24..39
+    _, p = _i64(28, 3)
+    assert L.kvc_truncate(h, p) == 0  # needs keys 24..27
+    assert L.kvc_set_window(h, 5, 0) == 1  # storage changes only on an empty cache
+    assert L.kvc_reset(h) == 0
+    assert L.kvc_set_window(h, 5, 0) == 0
+    L.kvc_destroy(h)
+    st, h = _create(L, layers=1, B=1, max_len=200, d=128, dtype=_lib.KVC_BF16)
+    assert L.kvc_set_window(h, 50, 1) == 1  # bf16 ring: max_len % 128
+    L.kvc_destroy(h)
