@@ -62,6 +62,14 @@ Sliding window and ring buffer (p2 "A strong answer", its last paragraph, and
   (else the chunk's first query would need a key already overwritten).
   Truncation to a length n needs the keys n - W + 1 .. n - 1 still in the
   ring (or n = 0) for the same reason.
+
+Tree speculative verify (p2 "What interviewers probe next", the tree-based
+speculative decoding question): the chunk's T draft tokens form a tree given
+by parent pointers.  Draft token t sees every key before the chunk plus the
+draft tokens on its own path to the root (itself and its ancestors), so the
+T x T corner is an ancestor mask instead of a triangle.  Readings: parents
+precede their children (parent[t] < t) and parent -1 means the token hangs
+directly off the cached prefix; trees do not combine with a window.
 """
 
 from __future__ import annotations
@@ -83,6 +91,8 @@ __all__ = [
     "decode_window_mask",
     "top_left_causal_mask",
     "visible_slots",
+    "tree_path",
+    "tree_corner_mask",
     "kv_cache_bytes",
 ]
 
@@ -281,13 +291,42 @@ def attend_slots(q_vec: np.ndarray, K_rows: np.ndarray, V_rows: np.ndarray, slot
     return p @ vals
 
 
-def gqa_attention(q: np.ndarray, cache: OracleCache, layer: int, n_new) -> np.ndarray:
+def tree_path(parents_row, t: int) -> list:
+    """Draft tokens token t may see: itself and its ancestors (p2, tree verify)."""
+    path = []
+    u = t
+    while u >= 0:
+        path.append(u)
+        u = int(parents_row[u])
+    return path
+
+
+def tree_corner_mask(parents_row) -> np.ndarray:
+    """Bool [T, T]: True where draft token t may see draft token u (u on t's path)."""
+    T = len(parents_row)
+    m = np.zeros((T, T), dtype=bool)
+    for t in range(T):
+        m[t, tree_path(parents_row, t)] = True
+    return m
+
+
+def check_parents(parents: np.ndarray, T: int) -> None:
+    """parents[b, t] in -1 .. t-1 (a parent precedes its child)."""
+    for b in range(parents.shape[0]):
+        for t in range(T):
+            if not -1 <= int(parents[b, t]) < t:
+                raise CacheError(f"row {b}: parent of draft token {t} must be in -1..{t - 1}")
+
+
+def gqa_attention(q: np.ndarray, cache: OracleCache, layer: int, n_new, parents=None) -> np.ndarray:
     """Attention of the T queries of the chunk just appended (p1 ``gqa_attention``).
 
     q is [B, Hq, T, d] with Hq a multiple of Hkv.  The KV heads are explicitly
     repeated to Hq heads, then every query (b, h, t) with t < n_new[b] attends
     to keys 0..lens[b]-n_new[b]+t of KV head h // G with a plain softmax.
     Padded queries and empty cases give zeros.  Returns float64 [B, Hq, T, d].
+    With ``parents`` (int [B, T], a draft tree per row) query t sees the keys
+    before the chunk plus the chunk's tokens on its path to the root.
     """
     q = np.asarray(q, dtype=np.float64)
     if q.ndim != 4:
@@ -304,6 +343,11 @@ def gqa_attention(q: np.ndarray, cache: OracleCache, layer: int, n_new) -> np.nd
     lens = cache.lens[layer]
     if np.any(n_new < 0) or np.any(n_new > T) or np.any(n_new > lens):
         raise CacheError("n_new must satisfy 0 <= n_new <= min(T, lens)")
+    if parents is not None:
+        parents = np.asarray(parents, dtype=np.int64).reshape(B, T)
+        check_parents(parents, T)
+        if cache.window or cache.ring:
+            raise CacheError("a draft tree does not combine with a window")
     out = np.zeros((B, Hq, T, d), dtype=np.float64)
     if B == 0 or T == 0:
         return out
@@ -319,7 +363,11 @@ def gqa_attention(q: np.ndarray, cache: OracleCache, layer: int, n_new) -> np.nd
                 if t >= n_new[b]:
                     continue  # padded query slot: stays zero
                 pos = query_position(int(lens[b]), int(n_new[b]), t)
-                if cache.window == 0 and not cache.ring:
+                if parents is not None:
+                    prior = int(lens[b] - n_new[b])
+                    keys = list(range(prior)) + sorted(prior + u for u in tree_path(parents[b], t))
+                    out[b, h, t] = attend_slots(q[b, h, t], K_rows, V_rows, np.asarray(keys, dtype=np.int64))
+                elif cache.window == 0 and not cache.ring:
                     out[b, h, t] = attend_one_query(q[b, h, t], K_rows, V_rows, pos)
                 else:
                     slots = visible_slots(cache.pos[layer][b], int(lens[b]), pos, cache.window)
@@ -327,10 +375,12 @@ def gqa_attention(q: np.ndarray, cache: OracleCache, layer: int, n_new) -> np.nd
     return out
 
 
-def append_attention(cache: OracleCache, layer: int, q, k_new, v_new, n_new) -> np.ndarray:
+def append_attention(cache: OracleCache, layer: int, q, k_new, v_new, n_new, parents=None) -> np.ndarray:
     """One call of the path: in-place append, then attention of the chunk."""
+    if parents is not None:
+        check_parents(np.asarray(parents, dtype=np.int64).reshape(cache.B, -1), np.asarray(k_new).shape[2])
     cache.append(layer, k_new, v_new, n_new)
-    return gqa_attention(q, cache, layer, n_new)
+    return gqa_attention(q, cache, layer, n_new, parents)
 
 
 def decode_causal_mask(T: int, S: int) -> np.ndarray:
