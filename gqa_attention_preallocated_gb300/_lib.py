@@ -35,6 +35,8 @@ SIGNATURES = [
     ("kvc_workspace_bytes", _SZ, [_VP, _I, _I]),
     ("kvc_gqa_attention", _I, [_VP, _I, _VP, _I, _I, _I32P, _VP, _VP, _SZ, _VP]),
     ("kvc_append_attention", _I, [_VP, _I, _VP, _VP, _VP, _I, _I, _I32P, _VP, _VP, _SZ, _VP]),
+    ("kvc_gqa_attention_tree", _I, [_VP, _I, _VP, _I, _I, _I32P, _I32P, _VP, _VP, _SZ, _VP]),
+    ("kvc_append_attention_tree", _I, [_VP, _I, _VP, _VP, _VP, _I, _I, _I32P, _I32P, _VP, _VP, _SZ, _VP]),
     ("kvc_gqa_attention_noalloc", _I, [_VP, _I, _VP, _I, _I, _I32P, _VP, _VP]),
     ("kvc_set_window", _I, [_VP, _I, _I]),
     ("kvc_truncate", _I, [_VP, _I64P]),

@@ -244,6 +244,46 @@ class KVCache:
                                     _ptr(out), _ptr(workspace), workspace.numel(), _stream_ptr(self.device, stream)))
         return out
 
+    def append_attention_tree(self, layer: int, q: torch.Tensor, k_new: torch.Tensor, v_new: torch.Tensor, n_new,
+                              parents, out: torch.Tensor | None = None, workspace: torch.Tensor | None = None,
+                              stream=None) -> torch.Tensor:
+        """``append_attention`` for a draft tree: parents [B, T] (-1 = off the cached prefix)."""
+        if q.dim() != 4:
+            raise KVCError(1, "q must be [B, Hq, T, d]")
+        B, Hq, T, d = q.shape
+        self._check_tensor(q, (self.B, Hq, T, self.d), "q")
+        self._check_tensor(k_new, (self.B, self.Hkv, T, self.d), "k_new")
+        self._check_tensor(v_new, (self.B, self.Hkv, T, self.d), "v_new")
+        if out is None:
+            out = torch.empty_like(q)
+        self._check_tensor(out, q.shape, "out")
+        ws = workspace if workspace is not None else self.workspace(Hq, T)
+        nn = _i32(n_new, self.B)
+        par = _i32(parents, self.B * T)
+        check(lib().kvc_append_attention_tree(self._h, layer, _ptr(q), _ptr(k_new), _ptr(v_new), Hq, T,
+                                              nn.ctypes.data_as(_I32P), par.ctypes.data_as(_I32P), _ptr(out),
+                                              _ptr(ws), 0 if ws is None else ws.numel(),
+                                              _stream_ptr(self.device, stream)))
+        return out
+
+    def gqa_attention_tree(self, layer: int, q: torch.Tensor, n_new, parents, out: torch.Tensor | None = None,
+                           workspace: torch.Tensor | None = None, stream=None) -> torch.Tensor:
+        """``gqa_attention`` of a chunk already appended, for a draft tree (parents [B, T])."""
+        if q.dim() != 4:
+            raise KVCError(1, "q must be [B, Hq, T, d]")
+        B, Hq, T, d = q.shape
+        self._check_tensor(q, (self.B, Hq, T, self.d), "q")
+        if out is None:
+            out = torch.empty_like(q)
+        self._check_tensor(out, q.shape, "out")
+        ws = workspace if workspace is not None else self.workspace(Hq, T)
+        nn = _i32(n_new, self.B)
+        par = _i32(parents, self.B * T)
+        check(lib().kvc_gqa_attention_tree(self._h, layer, _ptr(q), Hq, T, nn.ctypes.data_as(_I32P),
+                                           par.ctypes.data_as(_I32P), _ptr(out), _ptr(ws),
+                                           0 if ws is None else ws.numel(), _stream_ptr(self.device, stream)))
+        return out
+
     def selftest_bounded_wait(self, limit_ns: int, workspace: torch.Tensor | None = None, stream=None) -> None:
         """Launch the bounded-wait self-test into the workspace's error word."""
         ws = workspace if workspace is not None else self._ws

@@ -17,7 +17,9 @@
 // Sliding window and ring storage ("Write the causal mask for a decode
 // step...", "A strong answer", last paragraph): with a window W the query at
 // position p sees keys p - W < a <= p, and in a ring cache key a is read from
-// slot a mod max_len; keys are chosen by position, never by slot.
+// slot a mod max_len; keys are chosen by position, never by slot.  Tree
+// verify ("What interviewers probe next", tree-based speculative decoding):
+// a query sees the chunk's tokens on its own path to the root only.
 
 #include <math.h>
 
@@ -103,7 +105,10 @@ __global__ void __launch_bounds__(kWarps * 32) attn_f32_kernel(const __grid_cons
             const float* qr = sq + (warp + 4 * i) * d;
             const int key = k0 + lane;
             float s = -INFINITY;
-            if (lane < nk && key <= li && key > lo) {
+            // (key - prior <= li - prior < T <= 64 whenever the bit is read)
+            const bool on_path =
+                !p.tree || key < prior || key > li || ((p.anc[b * T + (li - prior)] >> (key - prior)) & 1ull);
+            if (lane < nk && key <= li && key > lo && on_path) {
                 float acc = 0.f;
                 const float* kr = sk + lane * d;
                 for (int e = 0; e < d; ++e) acc = fmaf(qr[e], kr[e], acc);

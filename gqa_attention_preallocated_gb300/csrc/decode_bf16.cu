@@ -95,7 +95,6 @@ template <>
 struct Part<false> {
     const DecodeParams& p;
     __device__ __forceinline__ int gstart(int i) const { return p.gstart[i]; }
-    __device__ __forceinline__ int tile0(int q) const { return p.tile0[q]; }
     __device__ __forceinline__ int prior(int b) const { return p.prior[b]; }
     __device__ __forceinline__ int n_new(int b) const { return p.n_new[b]; }
     __device__ __forceinline__ int total_tiles() const { return p.total_tiles; }
@@ -107,13 +106,32 @@ template <>
 struct Part<true> {
     const DecodeParams& p;
     __device__ __forceinline__ int gstart(int i) const { return p.dplan->gstart[i]; }
-    __device__ __forceinline__ int tile0(int q) const { return p.dplan->tile0[q]; }
     __device__ __forceinline__ int prior(int b) const { return p.dplan->prior[b]; }
     __device__ __forceinline__ int n_new(int b) const { return p.dplan->n_new[b]; }
     __device__ __forceinline__ int total_tiles() const { return p.dplan->total_tiles; }
     __device__ __forceinline__ int NB() const { return p.NB; }
     __device__ __forceinline__ int Hkv() const { return p.Hkv; }
 };
+
+// First key tile (absolute position / 64) of group q's units: 0, or with a
+// window the tile holding the window start of the block's earliest query
+// (the same rule as the planners'; tiles before it are never scheduled).
+template <bool DP>
+__device__ __forceinline__ int first_tile(const Part<DP>& w, int q) {
+    const DecodeParams& p = w.p;
+    if (p.window <= 0) return 0;
+    const int b = q / p.RB, rb = q - b * p.RB;
+    const int prior = w.prior(b), nn = w.n_new(b);
+    const int r0 = rb * p.RPB, r1 = min(p.R, r0 + p.RPB);
+    int qmin = 0x7fffffff;
+    if (r1 - r0 >= p.T) {
+        if (nn > 0) qmin = prior;
+    } else {
+        for (int r = r0; r < r1; ++r)
+            if (r % p.T < nn) qmin = min(qmin, prior + r % p.T);
+    }
+    return qmin == 0x7fffffff ? 0 : max(0, qmin - p.window + 1) / kKeyTile;
+}
 
 // Largest q with gstart[q] <= x (gstart nondecreasing, x < gstart[NB]).
 template <bool DP>
@@ -128,13 +146,14 @@ __device__ __forceinline__ int locate_group(const Part<DP>& w, int x) {
 
 template <bool DP>
 struct Cursor {
-    int q, kvh, j, nt;
+    int q, kvh, j, nt, t0;  // t0: the group's first key tile
     __device__ __forceinline__ void init(const Part<DP>& w, int x) {
         q = locate_group(w, x);
         nt = (w.gstart(q + 1) - w.gstart(q)) / w.Hkv();
         const int off = x - w.gstart(q);
         kvh = off / nt;
         j = off - kvh * nt;
+        t0 = first_tile(w, q);
     }
     __device__ __forceinline__ void advance(const Part<DP>& w) {
         if (++j < nt) return;
@@ -143,7 +162,10 @@ struct Cursor {
         kvh = 0;
         ++q;
         while (q < w.NB() && w.gstart(q + 1) == w.gstart(q)) ++q;
-        if (q < w.NB()) nt = (w.gstart(q + 1) - w.gstart(q)) / w.Hkv();
+        if (q < w.NB()) {
+            nt = (w.gstart(q + 1) - w.gstart(q)) / w.Hkv();
+            t0 = first_tile(w, q);
+        }
     }
 };
 
@@ -169,7 +191,9 @@ __device__ __forceinline__ bool wait_stage_tag(const volatile int* tag, int it, 
     }
 }
 
-template <int MT, bool DP>
+// MT: m-tiles of 16 query rows; DP: the partition comes from a device plan;
+// TREE: draft-tree ancestor masks apply (compiled out otherwise).
+template <int MT, bool DP, bool TREE>
 __global__ void __launch_bounds__(kThreads, 1)
     decode_splitkv_bf16_kernel(const __grid_constant__ DecodeParams p, const __grid_constant__ CUtensorMap tmK,
                                const __grid_constant__ CUtensorMap tmV) {
@@ -255,7 +279,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 }
                 if (*abort_flag) break;  // the producer is in no named barrier, so it may stop early
                 const int b = cur.q / p.RB;
-                const int row = (b * p.Hkv + cur.kvh) * p.max_len + slot_of(p, (wp.tile0(cur.q) + cur.j) * kKeyTile);
+                const int row = (b * p.Hkv + cur.kvh) * p.max_len + slot_of(p, (cur.t0 + cur.j) * kKeyTile);
                 const uint32_t full = bar0 + 8 * s;
                 const uint32_t sK = stage0 + s * kStageBytes;
                 stage_tag[s] = it;
@@ -384,7 +408,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 
             const uint32_t sK = stage0 + s * kStageBytes;
             const uint32_t sV = sK + kTileBytes;
-            const int tile0 = (wp.tile0(cur.q) + j) * kKeyTile;  // first key position of the tile
+            const int tile0 = (cur.t0 + j) * kKeyTile;  // first key position of the tile
 
             if (S::kTilePar && p.append_new) {
                 // In-kernel append: rows prior .. prior+n_new-1 of this unit that
@@ -444,7 +468,9 @@ __global__ void __launch_bounds__(kThreads, 1)
                 ptx::fence_proxy_async_smem();
                 if (S::kTilePar) __syncwarp(); else ptx::named_barrier_sync(1, kConsumerThreads);
             }
-            const bool full_tile = (tile0 + kKeyTile - 1 <= min_lim) && (tile0 > max_lo);
+            // With a draft tree only tiles wholly before the chunk are free of the mask.
+            const bool full_tile = (tile0 + kKeyTile - 1 <= min_lim) && (tile0 > max_lo) &&
+                                   (!TREE || tile0 + kKeyTile <= seg_prior);
 
             // S = Q K^T for this warp's 16 rows x KW keys.
             float sc[NBS][4];
@@ -475,7 +501,11 @@ __global__ void __launch_bounds__(kThreads, 1)
                     float v = sc[nb][e] * p.scale_log2;
                     if (!full_tile) {
                         const int key = kbase + nb * 8 + (e & 1);
-                        if (key > ((e < 2) ? lim0 : lim1) || key <= ((e < 2) ? lo0 : lo1)) v = -INFINITY;
+                        const int lim = (e < 2) ? lim0 : lim1;
+                        if (key > lim || key <= ((e < 2) ? lo0 : lo1)) v = -INFINITY;
+                        else if (TREE && key >= seg_prior &&
+                                 !((p.anc[b * p.T + (lim - seg_prior)] >> (key - seg_prior)) & 1ull))
+                            v = -INFINITY;  // a draft token off this query's path to the root
                     }
                     sc[nb][e] = v;
                 }
@@ -798,7 +828,7 @@ __global__ void __launch_bounds__(kPlanThreads) decode_plan_kernel(const __grid_
     }
     // Tiles of group q = b * RB + rb: Hkv units over the key tiles from the
     // window of the block's earliest query to one past its largest visible key.
-    int tiles = 0, first_tile = 0;
+    int tiles = 0, ft = 0;
     if (tid < p.NB) {
         const int b = tid / p.RB, rb = tid - b * p.RB;
         const int prior = p.lens[b], n = p.n_new[b];
@@ -819,8 +849,8 @@ __global__ void __launch_bounds__(kPlanThreads) decode_plan_kernel(const __grid_
             }
         }
         const int kfirst = (extent > 0 && p.window > 0) ? max(0, qmin - p.window + 1) : 0;
-        first_tile = kfirst / kKeyTile;
-        tiles = extent > 0 ? ((extent - 1) / kKeyTile + 1 - first_tile) * p.Hkv : 0;
+        ft = kfirst / kKeyTile;
+        tiles = extent > 0 ? ((extent - 1) / kKeyTile + 1 - ft) * p.Hkv : 0;
     }
     // Block-wide exclusive scan of the group tile counts.
     __shared__ int warp_sum[kPlanThreads / 32];
@@ -844,10 +874,7 @@ __global__ void __launch_bounds__(kPlanThreads) decode_plan_kernel(const __grid_
     __syncthreads();
     const int excl = incl - tiles + (warp > 0 ? warp_sum[warp - 1] : 0);
     const int total = warp_sum[kPlanThreads / 32 - 1];
-    if (tid < p.NB) {
-        plan->gstart[tid] = excl;
-        plan->tile0[tid] = first_tile;
-    }
+    if (tid < p.NB) plan->gstart[tid] = excl;
     if (tid == 0) {
         plan->gstart[p.NB] = total;
         plan->total_tiles = total;
@@ -876,19 +903,19 @@ cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t s
     return cudaLaunchKernelEx(&cfg, kernel, std::forward<Args>(args)...);
 }
 
-template <int MT, bool DP>
+template <int MT, bool DP, bool TREE>
 cudaError_t launch_mt(const DecodeParams& p, const CUtensorMap& tmK, const CUtensorMap& tmV, int grid,
                       cudaStream_t stream) {
     static bool attr_set = false;
     if (!attr_set) {
-        cudaError_t e = cudaFuncSetAttribute(decode_splitkv_bf16_kernel<MT, DP>,
+        cudaError_t e = cudaFuncSetAttribute(decode_splitkv_bf16_kernel<MT, DP, TREE>,
                                              cudaFuncAttributeMaxDynamicSharedMemorySize,
                                              static_cast<int>(Shape<MT>::kSmem));
         if (e != cudaSuccess) return e;
         attr_set = true;
     }
-    cudaError_t e = launch_pdl(decode_splitkv_bf16_kernel<MT, DP>, dim3(grid), dim3(kThreads), Shape<MT>::kSmem,
-                               stream, p, tmK, tmV);
+    cudaError_t e = launch_pdl(decode_splitkv_bf16_kernel<MT, DP, TREE>, dim3(grid), dim3(kThreads),
+                               Shape<MT>::kSmem, stream, p, tmK, tmV);
     if (e != cudaSuccess) return e;
     return cudaGetLastError();
 }
@@ -918,11 +945,19 @@ DecodeLaunch decode_launch_shape(int mt) {
 
 cudaError_t launch_decode_bf16(const DecodeParams& p, const CUtensorMap& tmK, const CUtensorMap& tmV, int mt,
                                int grid, cudaStream_t stream) {
-    if (p.dplan) return mt == 1 ? launch_mt<1, true>(p, tmK, tmV, grid, stream) : cudaErrorInvalidValue;
+    if (p.dplan) return (mt == 1 && !p.anc) ? launch_mt<1, true, false>(p, tmK, tmV, grid, stream) : cudaErrorInvalidValue;
+    if (p.anc) {
+        switch (mt) {
+            case 1: return launch_mt<1, false, true>(p, tmK, tmV, grid, stream);
+            case 2: return launch_mt<2, false, true>(p, tmK, tmV, grid, stream);
+            case 4: return launch_mt<4, false, true>(p, tmK, tmV, grid, stream);
+            default: return cudaErrorInvalidValue;
+        }
+    }
     switch (mt) {
-        case 1: return launch_mt<1, false>(p, tmK, tmV, grid, stream);
-        case 2: return launch_mt<2, false>(p, tmK, tmV, grid, stream);
-        case 4: return launch_mt<4, false>(p, tmK, tmV, grid, stream);
+        case 1: return launch_mt<1, false, false>(p, tmK, tmV, grid, stream);
+        case 2: return launch_mt<2, false, false>(p, tmK, tmV, grid, stream);
+        case 4: return launch_mt<4, false, false>(p, tmK, tmV, grid, stream);
         default: return cudaErrorInvalidValue;
     }
 }

@@ -209,7 +209,9 @@ kvc_status plan_shape(const kvc_cache* c, int Hq, int T, int num_ctas, AttnPlan*
         // the units that straddle CTAs.  Only the header needs to start at
         // zero; the merge counters return to zero after each use.
         pl->ws_err = kWsHeaderBytes;
-        pl->ws_plan = (sizeof(DevicePlan) + 255) / 256 * 256;  // device-computed plans of resident-length steps
+        // device-computed plans of resident-length steps, then the ancestor
+        // masks of a tree-verify call
+        pl->ws_plan = round_up(sizeof(DevicePlan), 256) + round_up(kMaxTreeQueries * sizeof(uint64_t), 256);
         pl->ways = decode_launch_shape(pl->mt).ways;
         pl->part_rows = std::min(pl->R, pl->RPB);
         pl->ws_partials = static_cast<size_t>(pl->units + num_ctas) * pl->ways * pl->part_rows *
@@ -282,7 +284,7 @@ kvc_status do_append(kvc_cache* c, int layer, const void* k_new, const void* v_n
 // kernel was enqueued (so a caller can undo its length update if not).
 kvc_status do_attention(kvc_cache* c, int layer, const void* q, const AttnPlan& pl, const int32_t* n_new, void* out,
                         void* ws, size_t ws_bytes, cudaStream_t stream, const void* k_new = nullptr,
-                        const void* v_new = nullptr, bool* main_enqueued = nullptr) {
+                        const void* v_new = nullptr, bool* main_enqueued = nullptr, const uint64_t* anc = nullptr) {
     if (main_enqueued) *main_enqueued = false;
     const int64_t* lens = c->lens.data() + static_cast<size_t>(layer) * c->B;
     if (c->B == 0 || pl.T == 0) return ok();
@@ -303,6 +305,8 @@ kvc_status do_attention(kvc_cache* c, int layer, const void* q, const AttnPlan& 
         p.R = pl.R;
         p.window = c->window;
         p.ring = c->ring ? 1 : 0;
+        p.tree = anc ? 1 : 0;
+        if (anc) std::copy(anc, anc + static_cast<size_t>(c->B) * pl.T, p.anc);
         p.scale = 1.0f / sqrtf(static_cast<float>(c->d));
         for (int b = 0; b < c->B; ++b) {
             p.prior[b] = static_cast<int>(lens[b] - n_new[b]);
@@ -316,7 +320,7 @@ kvc_status do_attention(kvc_cache* c, int layer, const void* q, const AttnPlan& 
 
     kvc_status s = encode_layer_maps(c, layer);
     if (s) return s;
-    if (pl.R > 64 && k_new == nullptr && c->max_len <= 0xFFFF * 128) {
+    if (pl.R > 64 && k_new == nullptr && anc == nullptr && c->max_len <= 0xFFFF * 128) {
         // Chunked prefill: tensor-core kernel, one CTA per piece.  Work items
         // are (b, kvh, 128 positions, head pair); an item's key tiles cost its
         // head count each, plus a fixed start-up cost per CTA.  The launch order
@@ -500,6 +504,15 @@ kvc_status do_attention(kvc_cache* c, int layer, const void* q, const AttnPlan& 
     p.Tn = pl.T;
     p.window = c->window;
     p.ring = c->ring ? 1 : 0;
+    p.anc = nullptr;
+    if (anc) {
+        // The masks go to the workspace (the parameter block stays small).
+        uint64_t* dev_anc = reinterpret_cast<uint64_t*>(wsb + pl.ws_err + round_up(sizeof(DevicePlan), 256));
+        cudaError_t e = cudaMemcpyAsync(dev_anc, anc, static_cast<size_t>(c->B) * pl.T * sizeof(uint64_t),
+                                        cudaMemcpyHostToDevice, stream);
+        if (e != cudaSuccess) return cuda_fail(e, "copying the draft-tree masks");
+        p.anc = dev_anc;
+    }
     p.scale_log2 = static_cast<float>(1.4426950408889634 / sqrt(static_cast<double>(c->d)));
     long long tiles = 0;
     for (int b = 0; b < c->B; ++b) {
@@ -531,7 +544,6 @@ kvc_status do_attention(kvc_cache* c, int layer, const void* q, const AttnPlan& 
             const int first_tile = kfirst / kKeyTile;
             const int ntiles = extent > 0 ? (extent - 1) / kKeyTile + 1 - first_tile : 0;
             p.gstart[b * pl.RB + rb] = static_cast<int>(tiles);
-            p.tile0[b * pl.RB + rb] = first_tile;
             tiles += static_cast<long long>(ntiles) * c->Hkv;
         }
     }
@@ -623,6 +635,33 @@ kvc_status check_workspace(const kvc_cache* c, const AttnPlan& pl, const void* w
 // C ABI
 // ===========================================================================
 
+// Ancestor masks of a draft tree ("Write the causal mask for a decode
+// step...", "What interviewers probe next": tree-based speculative decoding):
+// query t of row b may see chunk token u iff u is on t's path to the root.
+// parents[b * T + t] in -1 .. t - 1 for t < n_new[b] (a parent precedes its
+// child; -1: the token hangs directly off the cached prefix).
+kvc_status tree_masks(const kvc_cache* c, const AttnPlan& pl, const int32_t* n_new, const int32_t* parents,
+                      std::vector<uint64_t>* anc) {
+    if (!parents && c->B > 0) return fail(KVC_ERR_ARG, "parents is null");
+    if (pl.T > 64) return fail(KVC_ERR_SHAPE, "a draft tree takes at most 64 tokens per row (T = %d)", pl.T);
+    if (static_cast<long long>(c->B) * pl.T > kMaxTreeQueries)
+        return fail(KVC_ERR_SHAPE, "B * T = %lld draft tokens exceed %d", static_cast<long long>(c->B) * pl.T,
+                    kMaxTreeQueries);
+    if (c->window > 0 || c->ring) return fail(KVC_ERR_ARG, "a draft tree does not combine with a window");
+    if (c->dtype == KVC_BF16 && pl.R > 64)
+        return fail(KVC_ERR_SHAPE, "a bf16 draft tree takes G * T <= 64 query rows per KV head (G * T = %d)", pl.R);
+    anc->assign(static_cast<size_t>(c->B) * pl.T, 0);
+    for (int b = 0; b < c->B; ++b)
+        for (int t = 0; t < n_new[b]; ++t) {
+            const int pa = parents[static_cast<size_t>(b) * pl.T + t];
+            if (pa < -1 || pa >= t)
+                return fail(KVC_ERR_SHAPE, "row %d: parent %d of draft token %d outside -1..%d", b, pa, t, t - 1);
+            (*anc)[static_cast<size_t>(b) * pl.T + t] =
+                (1ull << t) | (pa >= 0 ? (*anc)[static_cast<size_t>(b) * pl.T + pa] : 0ull);
+        }
+    return ok();
+}
+
 // Calls that read or write the host copy of the lengths refuse while the
 // device copy is authoritative.
 kvc_status check_host_lens(const kvc_cache* c) {
@@ -705,8 +744,9 @@ size_t kvc_workspace_bytes(const kvc_cache* c, int q_heads, int T) {
     return pl.ws_total;
 }
 
-kvc_status kvc_gqa_attention(kvc_cache* c, int layer, const void* q, int q_heads, int T, const int32_t* n_new,
-                             void* out, void* workspace, size_t workspace_bytes, void* stream) {
+static kvc_status gqa_attention_impl(kvc_cache* c, int layer, const void* q, int q_heads, int T, const int32_t* n_new,
+                              const int32_t* parents, void* out, void* workspace, size_t workspace_bytes,
+                              void* stream) {
     kvc_status s0 = check_host_lens(c);
     if (s0) return s0;
     kvc_status s = check_layer(c, layer);
@@ -721,17 +761,23 @@ kvc_status kvc_gqa_attention(kvc_cache* c, int layer, const void* q, int q_heads
         s = plan_shape(c, q_heads, T, c->num_sms, &pl);
         if (s) return s;
     }
+    std::vector<uint64_t> anc;
+    if (parents) {
+        s = tree_masks(c, pl, n_new, parents, &anc);
+        if (s) return s;
+    }
     s = check_workspace(c, pl, workspace, workspace_bytes);
     if (s) return s;
     if (c->B == 0 || T == 0) return ok();
     s = ensure_device(c);
     if (s) return s;
-    return do_attention(c, layer, q, pl, n_new, out, workspace, workspace_bytes, static_cast<cudaStream_t>(stream));
+    return do_attention(c, layer, q, pl, n_new, out, workspace, workspace_bytes, static_cast<cudaStream_t>(stream),
+                        nullptr, nullptr, nullptr, parents ? anc.data() : nullptr);
 }
 
-kvc_status kvc_append_attention(kvc_cache* c, int layer, const void* q, const void* k_new, const void* v_new,
-                                int q_heads, int T, const int32_t* n_new, void* out, void* workspace,
-                                size_t workspace_bytes, void* stream) {
+static kvc_status append_attention_impl(kvc_cache* c, int layer, const void* q, const void* k_new, const void* v_new,
+                                 int q_heads, int T, const int32_t* n_new, const int32_t* parents, void* out,
+                                 void* workspace, size_t workspace_bytes, void* stream) {
     kvc_status s0 = check_host_lens(c);
     if (s0) return s0;
     int max_n = 0;
@@ -750,6 +796,12 @@ kvc_status kvc_append_attention(kvc_cache* c, int layer, const void* q, const vo
         s = plan_shape(c, q_heads, T, c->num_sms, &pl);
         if (s) return s;
     }
+    std::vector<uint64_t> anc;
+    if (parents) {
+        s = tree_masks(c, pl, n_new, parents, &anc);
+        if (s) return s;
+    }
+    const uint64_t* ancp = parents ? anc.data() : nullptr;
     s = check_workspace(c, pl, workspace, workspace_bytes);
     if (s) return s;
     if (c->B == 0 || T == 0) {
@@ -764,7 +816,7 @@ kvc_status kvc_append_attention(kvc_cache* c, int layer, const void* q, const vo
         // the cache itself (one launch instead of two).
         for (int b = 0; b < c->B; ++b) lw[b] += n_new[b];
         bool enqueued = false;
-        s = do_attention(c, layer, q, pl, n_new, out, workspace, workspace_bytes, st, k_new, v_new, &enqueued);
+        s = do_attention(c, layer, q, pl, n_new, out, workspace, workspace_bytes, st, k_new, v_new, &enqueued, ancp);
         if (s && !enqueued)
             for (int b = 0; b < c->B; ++b) lw[b] -= n_new[b];  // nothing ran: lengths unchanged
         return s;
@@ -772,12 +824,39 @@ kvc_status kvc_append_attention(kvc_cache* c, int layer, const void* q, const vo
     s = do_append(c, layer, k_new, v_new, T, n_new, max_n, st);
     if (s) return s;
     for (int b = 0; b < c->B; ++b) lw[b] += n_new[b];
-    s = do_attention(c, layer, q, pl, n_new, out, workspace, workspace_bytes, st);
+    s = do_attention(c, layer, q, pl, n_new, out, workspace, workspace_bytes, st, nullptr, nullptr, nullptr, ancp);
     if (s) {
         // The append already ran on the stream; its lengths stand.
         return s;
     }
     return ok();
+}
+
+kvc_status kvc_gqa_attention(kvc_cache* c, int layer, const void* q, int q_heads, int T, const int32_t* n_new,
+                             void* out, void* workspace, size_t workspace_bytes, void* stream) {
+    return gqa_attention_impl(c, layer, q, q_heads, T, n_new, nullptr, out, workspace, workspace_bytes, stream);
+}
+
+kvc_status kvc_gqa_attention_tree(kvc_cache* c, int layer, const void* q, int q_heads, int T, const int32_t* n_new,
+                                  const int32_t* parents, void* out, void* workspace, size_t workspace_bytes,
+                                  void* stream) {
+    if (c && c->B > 0 && !parents) return fail(KVC_ERR_ARG, "parents is null");
+    return gqa_attention_impl(c, layer, q, q_heads, T, n_new, parents, out, workspace, workspace_bytes, stream);
+}
+
+kvc_status kvc_append_attention(kvc_cache* c, int layer, const void* q, const void* k_new, const void* v_new,
+                                int q_heads, int T, const int32_t* n_new, void* out, void* workspace,
+                                size_t workspace_bytes, void* stream) {
+    return append_attention_impl(c, layer, q, k_new, v_new, q_heads, T, n_new, nullptr, out, workspace,
+                                 workspace_bytes, stream);
+}
+
+kvc_status kvc_append_attention_tree(kvc_cache* c, int layer, const void* q, const void* k_new, const void* v_new,
+                                     int q_heads, int T, const int32_t* n_new, const int32_t* parents, void* out,
+                                     void* workspace, size_t workspace_bytes, void* stream) {
+    if (c && c->B > 0 && !parents) return fail(KVC_ERR_ARG, "parents is null");
+    return append_attention_impl(c, layer, q, k_new, v_new, q_heads, T, n_new, parents, out, workspace,
+                                 workspace_bytes, stream);
 }
 
 kvc_status kvc_length(const kvc_cache* c, int64_t* out) {

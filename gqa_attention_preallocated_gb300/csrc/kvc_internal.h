@@ -12,6 +12,7 @@ namespace kvc {
 constexpr int kMaxBatch = KVC_MAX_BATCH;
 constexpr int kMaxGroups = 1024;  // (row, row-block) groups of one attention call
 constexpr int kMaxCtas = 1024;    // attention CTAs (one per SM)
+constexpr int kMaxTreeQueries = 1024;  // B * T of a tree-verify call (one ancestor mask per query)
 
 // Keys per K/V tile of the split-KV kernel, and the head width it is built for.
 constexpr int kKeyTile = 64;
@@ -61,7 +62,6 @@ struct DevicePlan {
     int prior[kMaxBatch];
     int n_new[kMaxBatch];
     int gstart[kMaxGroups + 1];
-    int tile0[kMaxGroups];
     int cta_start[kMaxCtas + 1];
 };
 
@@ -102,10 +102,13 @@ struct DecodeParams {
     // Sliding window (0 = none): a query at position p sees keys p - window < a <= p.
     // Ring storage: the key at position a lives in slot a mod max_len.
     int window, ring;
+    // Tree verify: query t of row b sees the chunk's tokens u with bit u of
+    // anc[b * T + t] set (its path to the root), besides every key before the
+    // chunk.  anc is device memory (the workspace); null without a tree.
+    const uint64_t* anc;
     int prior[kMaxBatch];    // lens[b] - n_new[b]
     int n_new[kMaxBatch];
     int gstart[kMaxGroups + 1];
-    int tile0[kMaxGroups];   // first key tile (absolute position / 64) of group q's units
 };
 
 // Log-sum-exp merge of the units the attention kernel left as partials (one
@@ -151,9 +154,11 @@ struct F32Params {
     int B, Hq, Hkv, G, T, max_len, d;
     int R;
     int window, ring;  // sliding window (0 = none) and ring storage, as in DecodeParams
+    int tree;          // ancestor masks in anc, as in DecodeParams
     float scale;  // 1 / sqrt(d)
     int prior[kMaxBatch];
     int n_new[kMaxBatch];
+    uint64_t anc[kMaxTreeQueries];
 };
 
 cudaError_t launch_attn_f32(const F32Params& p, cudaStream_t stream);

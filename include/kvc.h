@@ -127,6 +127,27 @@ kvc_status kvc_append_attention(kvc_cache* c, int layer, const void* q, const vo
                                 int q_heads, int T, const int32_t* n_new, void* out, void* workspace,
                                 size_t workspace_bytes, void* stream);
 
+/* Tree speculative verify ("Write the causal mask for a decode step with a KV
+ * cache...", "What interviewers probe next": tree-based speculative
+ * decoding).  The chunk's draft tokens form one tree per row, given by
+ * parents (host int32 [B * T]): parents[b * T + t] in -1 .. t - 1 for
+ * t < n_new[b] (a parent precedes its child; -1: the token hangs directly off
+ * the cached prefix; entries for t >= n_new[b] are ignored).  Query t then
+ * sees every key before the chunk plus the chunk's tokens on its own path to
+ * the root (itself and its ancestors) instead of the triangle; everything
+ * else is as in kvc_gqa_attention / kvc_append_attention.  Limits: T <= 64,
+ * B * T <= 1024, no sliding window; bf16 caches take G * T <= 64 query rows
+ * per KV head.  Errors (nothing enqueued): those of the plain calls, and
+ * KVC_ERR_SHAPE for a parent outside -1 .. t-1 or a shape past the limits,
+ * KVC_ERR_ARG for a null parents or a cache with a window. */
+kvc_status kvc_gqa_attention_tree(kvc_cache* c, int layer, const void* q, int q_heads, int T,
+                                  const int32_t* n_new, const int32_t* parents, void* out, void* workspace,
+                                  size_t workspace_bytes, void* stream);
+kvc_status kvc_append_attention_tree(kvc_cache* c, int layer, const void* q, const void* k_new,
+                                     const void* v_new, int q_heads, int T, const int32_t* n_new,
+                                     const int32_t* parents, void* out, void* workspace, size_t workspace_bytes,
+                                     void* stream);
+
 /* Size of the device scratch array behind kvc_gqa_attention_noalloc. */
 #define KVC_NOALLOC_SCRATCH_BYTES (32u << 20)
 
