@@ -70,6 +70,14 @@ draft tokens on its own path to the root (itself and its ancestors), so the
 T x T corner is an ancestor mask instead of a triangle.  Readings: parents
 precede their children (parent[t] < t) and parent -1 means the token hangs
 directly off the cached prefix; trees do not combine with a window.
+
+Paged storage (p1 "A strong answer", the reversal condition: wildly ragged
+rows call for a block table and a paged kernel; p3 "Design choices worth
+noticing": a paged cache avoids reserving max_len per row up front): K and
+V live in pages of P tokens, and a per-row block table maps logical page
+a // P of row b to a physical page.  Attention is defined on the logical
+sequence: ``PagedOracleCache.view`` gathers every row through the table into
+an ordinary cache, and the ordinary attention runs on that.
 """
 
 from __future__ import annotations
@@ -93,6 +101,7 @@ __all__ = [
     "visible_slots",
     "tree_path",
     "tree_corner_mask",
+    "PagedOracleCache",
     "kv_cache_bytes",
 ]
 
@@ -405,3 +414,80 @@ def top_left_causal_mask(T: int, S: int) -> np.ndarray:
 def kv_cache_bytes(layers: int, batch: int, tokens: int, kv_heads: int, head_dim: int, bytes_per_value: int = 2) -> int:
     """2 (K and V) x layers x batch x tokens x Hkv x d x bytes (p3 "How big is the cache?")."""
     return 2 * layers * batch * tokens * kv_heads * head_dim * bytes_per_value
+
+
+class PagedOracleCache:
+    """K/V in pages [num_pages, Hkv, P, d] per layer behind a block table.
+
+    ``table[b, i]`` is the physical page of row b's tokens i*P .. i*P+P-1
+    (-1: not mapped).  Each row holds up to max_pages_per_row * P tokens.
+    """
+
+    def __init__(self, layers, batch, kv_heads, page_size, num_pages, max_pages_per_row, head_dim):
+        if min(layers, kv_heads, page_size, num_pages, max_pages_per_row, head_dim) < 1 or batch < 0:
+            raise CacheError("bad paged geometry")
+        self.layers, self.B, self.Hkv, self.d = layers, batch, kv_heads, head_dim
+        self.P, self.num_pages, self.mpr = page_size, num_pages, max_pages_per_row
+        self.max_len = max_pages_per_row * page_size
+        shape = (num_pages, kv_heads, page_size, head_dim)
+        self.k = [np.zeros(shape, dtype=np.float64) for _ in range(layers)]
+        self.v = [np.zeros(shape, dtype=np.float64) for _ in range(layers)]
+        self.lens = np.zeros((layers, batch), dtype=np.int64)
+        self.table = np.full((batch, max_pages_per_row), -1, dtype=np.int64)
+        self.window = 0
+
+    def set_block_table(self, table) -> None:
+        table = np.asarray(table, dtype=np.int64).reshape(self.B, self.mpr)
+        if np.any(table < -1) or np.any(table >= self.num_pages):
+            raise CacheError("block table entry outside -1..num_pages-1")
+        self.table = table.copy()
+
+    def page_of(self, b: int, position: int) -> tuple:
+        """(physical page, offset) of row b's token at a logical position."""
+        return int(self.table[b, position // self.P]), position % self.P
+
+    def append(self, layer, k_new, v_new, n_new) -> None:
+        """Write row b's chunk at logical positions lens .. lens+n_new-1 through the table.
+
+        Every row is checked first (n_new in 0..T, capacity, every target page
+        mapped); nothing is written on error.
+        """
+        k_new, v_new = np.asarray(k_new), np.asarray(v_new)
+        T = k_new.shape[2]
+        n_new = np.asarray(n_new, dtype=np.int64).reshape(-1)
+        lens = self.lens[layer]
+        for b in range(self.B):
+            if n_new[b] < 0 or n_new[b] > T:
+                raise CacheError(f"row {b}: n_new={n_new[b]} outside 0..{T}")
+            if lens[b] + n_new[b] > self.max_len:
+                raise CacheError(f"row {b}: {lens[b] + n_new[b]} tokens > capacity {self.max_len}")
+            for a in range(int(lens[b]), int(lens[b] + n_new[b])):
+                if self.page_of(b, a)[0] < 0:
+                    raise CacheError(f"row {b}: position {a} falls in an unmapped page")
+        for b in range(self.B):
+            for t in range(int(n_new[b])):
+                page, off = self.page_of(b, int(lens[b]) + t)
+                self.k[layer][page, :, off] = k_new[b, :, t]
+                self.v[layer][page, :, off] = v_new[b, :, t]
+        self.lens[layer] = lens + n_new
+
+    def view(self, layer: int) -> OracleCache:
+        """An ordinary cache holding every row's logical sequence, gathered through the table."""
+        c = OracleCache(1, self.B, self.Hkv, self.max_len, self.d)
+        c.set_window(self.window)
+        for b in range(self.B):
+            for a in range(int(self.lens[layer, b])):
+                page, off = self.page_of(b, a)
+                c.k[0][b, :, a] = self.k[layer][page, :, off]
+                c.v[0][b, :, a] = self.v[layer][page, :, off]
+                c.pos[0][b, a] = a
+        c.lens[0] = self.lens[layer]
+        return c
+
+
+def paged_append_attention(cache: PagedOracleCache, layer: int, q, k_new, v_new, n_new, parents=None) -> np.ndarray:
+    """One call on a paged cache: append through the table, then attention on the logical view."""
+    if parents is not None:
+        check_parents(np.asarray(parents, dtype=np.int64).reshape(cache.B, -1), np.asarray(k_new).shape[2])
+    cache.append(layer, k_new, v_new, n_new)
+    return gqa_attention(q, cache.view(layer), 0, n_new, parents)
