@@ -7,6 +7,6 @@ There is no CPU fallback: calls raise if the library is missing.
 """
 
 from ._lib import KVCError, LIB_PATH, lib  # noqa: F401
-from .cache import KVCache, gqa_attention  # noqa: F401
+from .cache import KVCache, PagedKVCache, gqa_attention  # noqa: F401
 
-__all__ = ["KVCache", "KVCError", "gqa_attention", "lib", "LIB_PATH"]
+__all__ = ["KVCache", "PagedKVCache", "KVCError", "gqa_attention", "lib", "LIB_PATH"]

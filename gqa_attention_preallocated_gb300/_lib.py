@@ -30,6 +30,8 @@ _I32P = ctypes.POINTER(ctypes.c_int32)
 _I64P = ctypes.POINTER(ctypes.c_int64)
 SIGNATURES = [
     ("kvc_create", _I, [ctypes.POINTER(_VP), _I, _I, _I, _I, _I, _I, ctypes.POINTER(_VP), ctypes.POINTER(_VP)]),
+    ("kvc_create_paged", _I, [ctypes.POINTER(_VP), _I, _I, _I, _I, _I, _I, _I, _I, ctypes.POINTER(_VP),
+                              ctypes.POINTER(_VP), _VP]),
     ("kvc_destroy", None, [_VP]),
     ("kvc_append", _I, [_VP, _I, _VP, _VP, _I, _I32P, _VP]),
     ("kvc_workspace_bytes", _SZ, [_VP, _I, _I]),

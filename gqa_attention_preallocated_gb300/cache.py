@@ -301,6 +301,43 @@ class KVCache:
         return code.value
 
 
+class PagedKVCache(KVCache):
+    """K/V in pages [num_pages, Hkv, page_size, d] per layer behind a device block table.
+
+    ``block_table`` (int32 [B, max_pages_per_row], on the device, owned by
+    this object) maps row b's logical page i to a physical page; it starts as
+    row b owning pages b * max_pages_per_row .. (as long as num_pages allows,
+    else -1) and may be rewritten between calls.  Every call works on the
+    logical sequence, with max_len = max_pages_per_row * page_size.
+    """
+
+    def __init__(self, layers: int, batch: int, kv_heads: int, page_size: int, num_pages: int,
+                 max_pages_per_row: int, head_dim: int, dtype: torch.dtype = torch.bfloat16, device="cuda"):
+        if dtype not in _DTYPES:
+            raise KVCError(1, f"unsupported dtype {dtype}")
+        dev = torch.device(device)
+        if dev.type == "cuda" and dev.index is None:
+            dev = torch.device("cuda", torch.cuda.current_device())
+        self.layers, self.B, self.Hkv, self.d = layers, batch, kv_heads, head_dim
+        self.page_size, self.num_pages, self.max_pages_per_row = page_size, num_pages, max_pages_per_row
+        self.max_len = max_pages_per_row * page_size
+        self.dtype, self.device = dtype, dev
+        shape = (num_pages, kv_heads, page_size, head_dim)
+        self.k = [torch.empty(shape, dtype=dtype, device=dev) for _ in range(layers)]
+        self.v = [torch.empty(shape, dtype=dtype, device=dev) for _ in range(layers)]
+        ids = torch.arange(batch * max_pages_per_row, dtype=torch.int32, device=dev)
+        self.block_table = torch.where(ids < num_pages, ids, torch.full_like(ids, -1)).view(batch, max_pages_per_row)
+        kp = (ctypes.c_void_p * layers)(*[t.data_ptr() for t in self.k])
+        vp = (ctypes.c_void_p * layers)(*[t.data_ptr() for t in self.v])
+        h = ctypes.c_void_p()
+        check(lib().kvc_create_paged(ctypes.byref(h), layers, batch, kv_heads, page_size, num_pages,
+                                     max_pages_per_row, head_dim, _DTYPES[dtype], kp, vp,
+                                     self.block_table.data_ptr()))
+        self._h = h
+        self._ws = None
+        self._dev_lens = None
+
+
 def gqa_attention(q: torch.Tensor, cache: KVCache, n_new, layer: int = 0, **kw) -> torch.Tensor:
     """Module-level form of ``KVCache.gqa_attention`` (the pages' call signature)."""
     return cache.gqa_attention(layer, q, n_new, **kw)

@@ -34,13 +34,18 @@ __global__ void __launch_bounds__(kAppendThreads) kv_append_kernel(const __grid_
     const size_t unit = static_cast<size_t>(b) * p.Hkv + h;
     const uint8_t* src = (is_v ? p.v_new : p.k_new) + unit * p.T * p.row_bytes;
     const uint4 val = __ldg(reinterpret_cast<const uint4*>(src) + vec);
-    uint8_t* base = (is_v ? p.v_cache : p.k_cache) + unit * p.max_len * p.row_bytes;
-    if (!p.ring) {
+    uint8_t* cache = is_v ? p.v_cache : p.k_cache;
+    if (!p.ring && !p.pg.table) {
+        uint8_t* base = cache + unit * p.max_len * p.row_bytes;
         reinterpret_cast<uint4*>(base + static_cast<size_t>(p.lens[b]) * p.row_bytes)[vec] = val;
     } else {
+        // Ring or paged storage: the row of each position on its own.  A
+        // position whose block-table entry is bad is not written (the next
+        // attention call over it reports the entry).
         const size_t byte = vec * 16, t = byte / p.row_bytes;
-        const size_t slot = (static_cast<size_t>(p.lens[b]) + t) % static_cast<size_t>(p.max_len);
-        *reinterpret_cast<uint4*>(base + slot * p.row_bytes + (byte - t * p.row_bytes)) = val;
+        bool bad = false;
+        const int row = phys_row(p.pg, p.ring, p.Hkv, p.max_len, b, h, p.lens[b] + static_cast<int>(t), &bad);
+        if (!bad) *reinterpret_cast<uint4*>(cache + static_cast<size_t>(row) * p.row_bytes + (byte - t * p.row_bytes)) = val;
     }
 }
 

@@ -88,10 +88,13 @@ __global__ void __launch_bounds__(kWarps * 32) attn_f32_kernel(const __grid_cons
             float4 kv4 = make_float4(0.f, 0.f, 0.f, 0.f), vv4 = kv4;
             if (j < nk) {
                 const int a = k0 + j;  // key position
-                const size_t slot = p.ring ? static_cast<size_t>(a % p.max_len) : static_cast<size_t>(a);
-                const size_t off = (unit_base + slot) * d + static_cast<size_t>(idx * 4 - j * d);
-                kv4 = *reinterpret_cast<const float4*>(p.k_cache + off);
-                vv4 = *reinterpret_cast<const float4*>(p.v_cache + off);
+                bool bad = false;
+                const int row = phys_row(p.pg, p.ring, p.Hkv, p.max_len, b, kvh, a, &bad);
+                if (!bad) {  // a bad block-table entry reads as zeros
+                    const size_t off = static_cast<size_t>(row) * d + static_cast<size_t>(idx * 4 - j * d);
+                    kv4 = *reinterpret_cast<const float4*>(p.k_cache + off);
+                    vv4 = *reinterpret_cast<const float4*>(p.v_cache + off);
+                }
             }
             reinterpret_cast<float4*>(sk)[idx] = kv4;
             reinterpret_cast<float4*>(sv)[idx] = vv4;

@@ -169,9 +169,16 @@ struct Cursor {
     }
 };
 
-// Cache slot of the key at absolute position a (ring storage: a mod max_len;
-// max_len is a multiple of the tile size there, so a tile never wraps).
-__device__ __forceinline__ int slot_of(const DecodeParams& p, int a) { return p.ring ? a % p.max_len : a; }
+// Row (of the cache's 2-D view) of the key at absolute position a of unit
+// (b, kvh): contiguous, ring (a mod max_len) or paged (through the block
+// table).  Tiles never straddle a ring wrap or a page (max_len / page are
+// multiples of the tile size there).  A bad table entry records an error.
+__device__ __forceinline__ int key_row(const DecodeParams& p, int b, int kvh, int a) {
+    bool bad = false;
+    const int row = phys_row(p.pg, p.ring, p.Hkv, p.max_len, b, kvh, a, &bad);
+    if (bad) atomicExch(p.err, kDevBadPage);
+    return row;
+}
 
 __device__ __forceinline__ void store_bf16x4(void* dst, float a, float b, float c, float d) {
     uint2 v;
@@ -279,7 +286,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 }
                 if (*abort_flag) break;  // the producer is in no named barrier, so it may stop early
                 const int b = cur.q / p.RB;
-                const int row = (b * p.Hkv + cur.kvh) * p.max_len + slot_of(p, (cur.t0 + cur.j) * kKeyTile);
+                const int row = key_row(p, b, cur.kvh, (cur.t0 + cur.j) * kKeyTile);
                 const uint32_t full = bar0 + 8 * s;
                 const uint32_t sK = stage0 + s * kStageBytes;
                 stage_tag[s] = it;
@@ -421,15 +428,16 @@ __global__ void __launch_bounds__(kThreads, 1)
                     const bool is_v = lane >= 16;
                     const size_t unit = static_cast<size_t>(b) * p.Hkv + kvh;
                     const uint8_t* src = static_cast<const uint8_t*>(is_v ? p.v_new : p.k_new) + unit * p.Tn * (kD * 2);
-                    uint8_t* dst = static_cast<uint8_t*>(is_v ? p.v_cache : p.k_cache) + unit * p.max_len * (kD * 2);
-                    const int slot_shift = slot_of(p, tile0) - tile0;  // ring: the tile's slots are contiguous
+                    uint8_t* dst = static_cast<uint8_t*>(is_v ? p.v_cache : p.k_cache);
+                    bool bad = false;
+                    const int row0 = phys_row(p.pg, p.ring, p.Hkv, p.max_len, b, kvh, tile0, &bad) - tile0;  // the tile's rows are contiguous
                     uint8_t* stg = stages + s * kStageBytes + (is_v ? kTileBytes : 0) + (chunk >> 3) * kHalfBytes;
                     for (int pos = lo; pos < hi; ++pos) {
                         const int t = pos - seg_prior, r = pos - tile0;
                         const uint4 val = (t == 0) ? new_row0
                                                    : __ldg(reinterpret_cast<const uint4*>(src + t * (kD * 2) + chunk * 16));
                         *reinterpret_cast<uint4*>(stg + r * 128 + (((chunk & 7) ^ (r & 7)) << 4)) = val;
-                        *reinterpret_cast<uint4*>(dst + static_cast<size_t>(pos + slot_shift) * (kD * 2) + chunk * 16) = val;
+                        if (!bad) *reinterpret_cast<uint4*>(dst + static_cast<size_t>(row0 + pos) * (kD * 2) + chunk * 16) = val;
                     }
                     ptx::fence_proxy_async_smem();
                     __syncwarp();

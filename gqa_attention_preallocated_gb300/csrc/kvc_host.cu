@@ -48,6 +48,9 @@ struct kvc_cache {
     // Sliding window (0 = none) and ring storage (slot = position mod max_len).
     int window = 0;
     bool ring = false;
+    // Paged storage (table set): buffers [num_pages, Hkv, page, d], a device
+    // block table [B, mpr]; max_len is the logical capacity mpr * page.
+    Paging pg{nullptr, 0, 0, 0};
 };
 
 namespace {
@@ -123,7 +126,8 @@ kvc_status encode_rows_map(CUtensorMap* m, const void* base, cuuint64_t rows, cu
 // One layer's K and V as rows = B*Hkv*max_len: 64-row and 128-row boxes.
 kvc_status encode_layer_maps(kvc_cache* c, int layer) {
     if (c->tm_ready[layer]) return ok();
-    const cuuint64_t rows = static_cast<cuuint64_t>(c->B) * c->Hkv * c->max_len;
+    const cuuint64_t rows = c->pg.table ? static_cast<cuuint64_t>(c->pg.num_pages) * c->Hkv * c->pg.page
+                                        : static_cast<cuuint64_t>(c->B) * c->Hkv * c->max_len;
     kvc_status s;
     if ((s = encode_rows_map(&c->tmK[layer], c->k[layer], rows, kKeyTile))) return s;
     if ((s = encode_rows_map(&c->tmV[layer], c->v[layer], rows, kKeyTile))) return s;
@@ -268,6 +272,7 @@ kvc_status do_append(kvc_cache* c, int layer, const void* k_new, const void* v_n
     p.max_len = c->max_len;
     p.row_bytes = c->d * c->esize;
     p.ring = c->ring ? 1 : 0;
+    p.pg = c->pg;
     const int64_t* lens = c->lens.data() + static_cast<size_t>(layer) * c->B;
     for (int b = 0; b < c->B; ++b) {
         p.lens[b] = static_cast<int>(lens[b]);
@@ -307,6 +312,7 @@ kvc_status do_attention(kvc_cache* c, int layer, const void* q, const AttnPlan& 
         p.ring = c->ring ? 1 : 0;
         p.tree = anc ? 1 : 0;
         if (anc) std::copy(anc, anc + static_cast<size_t>(c->B) * pl.T, p.anc);
+        p.pg = c->pg;
         p.scale = 1.0f / sqrtf(static_cast<float>(c->d));
         for (int b = 0; b < c->B; ++b) {
             p.prior[b] = static_cast<int>(lens[b] - n_new[b]);
@@ -352,6 +358,7 @@ kvc_status do_attention(kvc_cache* c, int layer, const void* q, const AttnPlan& 
         pp.npair = (pl.G + 1) / 2;
         pp.window = c->window;
         pp.ring = c->ring ? 1 : 0;
+        pp.pg = c->pg;
         pp.scale_log2 = static_cast<float>(1.4426950408889634 / sqrt(static_cast<double>(c->d)));
         for (int b = 0; b < c->B; ++b) {
             pp.prior[b] = static_cast<int>(lens[b] - n_new[b]);
@@ -504,6 +511,7 @@ kvc_status do_attention(kvc_cache* c, int layer, const void* q, const AttnPlan& 
     p.Tn = pl.T;
     p.window = c->window;
     p.ring = c->ring ? 1 : 0;
+    p.pg = c->pg;
     p.anc = nullptr;
     if (anc) {
         // The masks go to the workspace (the parameter block stays small).
@@ -711,6 +719,31 @@ kvc_status kvc_create(kvc_cache** out, int layers, int batch, int kv_heads, int 
     c->tmV128.resize(layers);
     c->tm_ready.assign(layers, 0);
     *out = c;
+    return ok();
+}
+
+kvc_status kvc_create_paged(kvc_cache** out, int layers, int batch, int kv_heads, int page_size, int num_pages,
+                            int max_pages_per_row, int head_dim, kvc_dtype dtype, void* const* k_bufs,
+                            void* const* v_bufs, const int32_t* block_table) {
+    if (!out) return fail(KVC_ERR_ARG, "out is null");
+    *out = nullptr;
+    if (page_size < 1 || num_pages < 1 || max_pages_per_row < 1)
+        return fail(KVC_ERR_ARG, "bad paging: page_size=%d num_pages=%d max_pages_per_row=%d", page_size, num_pages,
+                    max_pages_per_row);
+    if (dtype == KVC_BF16 && page_size % 128 != 0)
+        return fail(KVC_ERR_ARG, "bf16 pages hold a multiple of 128 tokens (key tiles never cross a page)");
+    if (batch > 0 && !block_table) return fail(KVC_ERR_ARG, "block_table is null");
+    if ((reinterpret_cast<uintptr_t>(block_table) & 3u) != 0) return fail(KVC_ERR_ARG, "block_table not 4-byte aligned");
+    const long long cap = static_cast<long long>(max_pages_per_row) * page_size;
+    if (cap >= (1ll << 30)) return fail(KVC_ERR_ARG, "max_pages_per_row * page_size too large");
+    if (static_cast<long long>(num_pages) * kv_heads * page_size + kKeyTile >= (1ll << 31))
+        return fail(KVC_ERR_ARG, "num_pages * kv_heads * page_size too large");
+    if (static_cast<long long>(batch) * max_pages_per_row >= (1ll << 31))
+        return fail(KVC_ERR_ARG, "batch * max_pages_per_row too large");
+    // The ordinary handle over the logical geometry; the buffers are pages.
+    kvc_status s = kvc_create(out, layers, batch, kv_heads, static_cast<int>(cap), head_dim, dtype, k_bufs, v_bufs);
+    if (s) return s;
+    (*out)->pg = Paging{block_table, page_size, max_pages_per_row, num_pages};
     return ok();
 }
 
@@ -949,6 +982,9 @@ kvc_status kvc_device_status(kvc_cache* c, void* workspace, void* stream, int32_
         if (v == kDevOverflow)
             return fail(KVC_ERR_OVERFLOW, "a device-resident step was rejected: a row would pass max_len or n_new "
                                           "was outside 0..T (nothing was written, lengths unchanged)");
+        if (v == kDevBadPage)
+            return fail(KVC_ERR_ARG, "a block-table entry under an attended or appended position was outside "
+                                     "0..num_pages-1 (not dereferenced; the call's output is not valid)");
         return fail(KVC_ERR_DEVICE_TIMEOUT, "a kernel's bounded wait expired (code %d)", v);
     }
     return ok();
@@ -968,6 +1004,7 @@ kvc_status kvc_set_window(kvc_cache* c, int window, int ring) {
     if (window < 0) return fail(KVC_ERR_ARG, "window = %d < 0", window);
     if (ring != 0 && ring != 1) return fail(KVC_ERR_ARG, "ring must be 0 or 1");
     if (ring) {
+        if (c->pg.table) return fail(KVC_ERR_ARG, "a paged cache cannot also be a ring");
         if (window < 1 || window > c->max_len) return fail(KVC_ERR_ARG, "a ring cache needs a window of 1..max_len");
         if (c->dtype == KVC_BF16 && c->max_len % 128 != 0)
             return fail(KVC_ERR_ARG, "a bf16 ring cache needs max_len %% 128 == 0 (key tiles never wrap)");
@@ -1110,6 +1147,7 @@ kvc_status kvc_decode_step(kvc_cache* c, int layer, const void* q, const void* k
     p.Tn = T;
     p.window = c->window;
     p.ring = c->ring ? 1 : 0;
+    p.pg = c->pg;
     e = launch_decode_bf16(p, c->tmK[layer], c->tmV[layer], 1, grid, st);
     if (e != cudaSuccess) return cuda_fail(e, "split-KV attention launch");
     ++c->launches;

@@ -14,6 +14,26 @@ constexpr int kMaxGroups = 1024;  // (row, row-block) groups of one attention ca
 constexpr int kMaxCtas = 1024;    // attention CTAs (one per SM)
 constexpr int kMaxTreeQueries = 1024;  // B * T of a tree-verify call (one ancestor mask per query)
 
+// Paged storage: a row's logical position a lives at page table[b * mpr + a / page],
+// offset a % page, of buffers shaped [num_pages, Hkv, page, d]; table null:
+// contiguous [B, Hkv, max_len, d] (or a ring).  Row index of the 2-D
+// (rows x d) view of the buffer, for (row b, KV head kvh, position a); *bad is
+// set for an entry outside 0 .. num_pages - 1, whose row is then page 0's.
+struct Paging {
+    const int32_t* table;
+    int page, mpr, num_pages;
+};
+__host__ __device__ __forceinline__ int phys_row(const Paging& pg, int ring, int Hkv, int max_len, int b, int kvh,
+                                                 int a, bool* bad) {
+    if (pg.table) {
+        const int e = pg.table[b * pg.mpr + a / pg.page];
+        const bool ok = e >= 0 && e < pg.num_pages;
+        if (!ok) *bad = true;
+        return ((ok ? e : 0) * Hkv + kvh) * pg.page + a % pg.page;
+    }
+    return (b * Hkv + kvh) * max_len + (ring ? a % max_len : a);
+}
+
 // Keys per K/V tile of the split-KV kernel, and the head width it is built for.
 constexpr int kKeyTile = 64;
 constexpr int kHeadDimBf16 = 128;
@@ -29,6 +49,7 @@ struct AppendParams {
     int B, Hkv, T, max_len;
     int row_bytes;  // d * element size, a multiple of 16
     int ring;       // slots are positions mod max_len
+    Paging pg;
     int lens[kMaxBatch];
     int n_new[kMaxBatch];
 };
@@ -106,6 +127,7 @@ struct DecodeParams {
     // anc[b * T + t] set (its path to the root), besides every key before the
     // chunk.  anc is device memory (the workspace); null without a tree.
     const uint64_t* anc;
+    Paging pg;
     int prior[kMaxBatch];    // lens[b] - n_new[b]
     int n_new[kMaxBatch];
     int gstart[kMaxGroups + 1];
@@ -155,6 +177,7 @@ struct F32Params {
     int R;
     int window, ring;  // sliding window (0 = none) and ring storage, as in DecodeParams
     int tree;          // ancestor masks in anc, as in DecodeParams
+    Paging pg;
     float scale;  // 1 / sqrt(d)
     int prior[kMaxBatch];
     int n_new[kMaxBatch];
@@ -184,6 +207,7 @@ struct PrefillParams {
     int B, Hq, Hkv, G, T, max_len;
     int ntb, npair, n_pieces;
     int window, ring;  // sliding window (0 = none) and ring storage, as in DecodeParams
+    Paging pg;
     float scale_log2;
     int prior[kMaxBatch];
     int n_new[kMaxBatch];
@@ -207,7 +231,8 @@ enum DeviceError : int {
     kDevTimeoutDrain = 3,  // abort path gave up waiting for copies in flight
     kDevTimeoutTest = 4,   // the self-test wait expired, as it is meant to
     kDevTimeoutTag = 5,    // consumer gave up waiting for the producer to claim a stage
-    kDevOverflow = 6       // a device-resident step was rejected: a row would pass max_len
+    kDevOverflow = 6,      // a device-resident step was rejected: a row would pass max_len
+    kDevBadPage = 7        // a block-table entry outside 0 .. num_pages - 1 was met (not read / written)
 };
 
 // Self-test of the bounded wait: waits on an mbarrier that nothing arrives at,

@@ -359,7 +359,13 @@ __global__ void __launch_bounds__(kThreadsPF, 1)
     // window, keys > max_lo inside every row's window (-1: no window).
     const int min_lo = kWin ? full_below - p.window : -1;
     const int max_lo = kWin ? kmax - p.window : -1;
-    auto slot_row = [&](int kt) { return unit_row0 + ((kWin && p.ring) ? (kt * 128) % p.max_len : kt * 128); };
+    auto slot_row = [&](int kt) {
+        if (!p.pg.table) return unit_row0 + ((kWin && p.ring) ? (kt * 128) % p.max_len : kt * 128);
+        bool bad = false;  // paged: the tile lies in one page
+        const int row = phys_row(p.pg, 0, p.Hkv, p.max_len, b, kvh, kt * 128, &bad);
+        if (bad) atomicExch(p.err, kDevBadPage);
+        return row;
+    };
 
     if (warp == 0) {
         // ------------------------------------------------------------ TMA producer

@@ -88,6 +88,28 @@ kvc_status kvc_create(kvc_cache** out, int layers, int batch, int kv_heads, int 
 /* Free the handle (not the buffers).  NULL is accepted. */
 void kvc_destroy(kvc_cache* c);
 
+/* A cache whose K/V live in pages ("Implement grouped-query attention over a
+ * preallocated KV cache...", "A strong answer", the reversal condition: rows of
+ * wildly different lengths call for a block table; "16. Prefill, decode and the
+ * KV cache", "Design choices worth noticing": a paged cache reserves no
+ * max_len per row).  k_bufs[l] / v_bufs[l] are caller-owned device buffers
+ * [num_pages, kv_heads, page_size, head_dim]; block_table is a caller-owned
+ * device int32 [batch, max_pages_per_row]: row b's tokens
+ * i * page_size .. (i + 1) * page_size - 1 live in page block_table[b][i]
+ * (-1: not mapped).  Every later call works on the logical sequence exactly as
+ * with kvc_create, with max_len = max_pages_per_row * page_size.  The caller
+ * keeps the entries under every position a call appends or attends to valid
+ * (0 .. num_pages - 1) and may change the table between calls (stream-ordered).
+ * A bad entry is never dereferenced: appended rows aimed at it are not
+ * written, and reads take page 0 and set the workspace error word (the next
+ * kvc_device_status reports it); the fp32 path reads it as zeros.  bf16
+ * needs page_size % 128 == 0.  Paged storage does not combine with ring
+ * storage (kvc_set_window ring = 1).  Errors: as kvc_create, and KVC_ERR_ARG
+ * for bad paging arguments. */
+kvc_status kvc_create_paged(kvc_cache** out, int layers, int batch, int kv_heads, int page_size, int num_pages,
+                            int max_pages_per_row, int head_dim, kvc_dtype dtype, void* const* k_bufs,
+                            void* const* v_bufs, const int32_t* block_table);
+
 /* Append in place ("A strong answer", KVCache.append): for every row b and
  * t < n_new[b], copy k_new[b, :, t, :] to K[b, :, lens[b] + t, :] (same for
  * V), then lens[layer][b] += n_new[b].  n_new is a HOST array of B entries.
@@ -224,8 +246,10 @@ kvc_status kvc_length(const kvc_cache* c, int64_t* out);
  * stream's work ends: synchronizes `stream`, copies the word and stores it in
  * *code (0 = clean; otherwise a kernel's bounded wait expired and that call's
  * output is not valid), then clears the word.  Returns KVC_ERR_DEVICE_TIMEOUT
- * when *code != 0, or KVC_ERR_OVERFLOW when the code records a rejected
- * device-resident step (kvc_decode_step). */
+ * when *code != 0, KVC_ERR_OVERFLOW when the code records a rejected
+ * device-resident step (kvc_decode_step), or KVC_ERR_ARG when a kernel met a
+ * block-table entry outside 0 .. num_pages - 1 (kvc_create_paged; nothing was
+ * read from or written to it, and that call's output is not valid). */
 kvc_status kvc_device_status(kvc_cache* c, void* workspace, void* stream, int32_t* code);
 
 /* Self-test of the kernels' bounded waits: launches one CTA that waits on an

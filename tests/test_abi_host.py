@@ -225,3 +225,36 @@ def test_window_and_ring_host_rules(L):
     st, h = _create(L, layers=1, B=1, max_len=200, d=128, dtype=_lib.KVC_BF16)
     assert L.kvc_set_window(h, 50, 1) == 1  # bf16 ring: max_len % 128
     L.kvc_destroy(h)
+
+
+def _create_paged(L, layers=1, B=2, Hkv=2, page=4, num_pages=5, mpr=3, d=16, dtype=_lib.KVC_F32, table=1 << 42):
+    h = ctypes.c_void_p()
+    k, v = _fake_buffers(layers)
+    st = L.kvc_create_paged(ctypes.byref(h), layers, B, Hkv, page, num_pages, mpr, d, dtype, k, v,
+                            ctypes.c_void_p(table))
+    return st, h
+
+
+def test_paged_host_rules(L):
+    assert _create_paged(L, page=0)[0] == 1
+    assert _create_paged(L, num_pages=0)[0] == 1
+    assert _create_paged(L, mpr=0)[0] == 1
+    assert _create_paged(L, table=0)[0] == 1          # no block table
+    assert _create_paged(L, table=(1 << 42) + 2)[0] == 1  # misaligned table
+    assert _create_paged(L, page=64, d=128, dtype=_lib.KVC_BF16)[0] == 1  # bf16 pages: multiples of 128
+    st, h = _create_paged(L, page=128, d=128, dtype=_lib.KVC_BF16)
+    assert st == 0
+    L.kvc_destroy(h)
+    st, h = _create_paged(L, B=2, page=4, mpr=3)
+    assert st == 0
+    _, big = _i64(12, 0)
+    assert L.kvc_set_lens(h, 0, big) == 0   # logical max_len = 3 pages * 4
+    _, over = _i64(13, 0)
+    assert L.kvc_set_lens(h, 0, over) == 1
+    kn = ctypes.c_void_p(1 << 41)
+    _, p = _i32(1, 0)
+    assert L.kvc_append(h, 0, kn, kn, 1, p, None) == 3  # row 0 is full
+    assert L.kvc_set_window(h, 6, 1) == 1   # ring storage is not paged
+    assert L.kvc_reset(h) == 0
+    assert L.kvc_set_window(h, 6, 0) == 0   # a window over pages is fine
+    L.kvc_destroy(h)
