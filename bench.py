@@ -146,7 +146,7 @@ def step_inputs(shape, Hq, T, n_distinct, seed, device="cuda"):
 class Workload:
     """One named workload: set-up, one step, and the step's algorithmic work."""
 
-    def __init__(self, name, seed=0):
+    def __init__(self, name, seed=0, verify_t=4, verify_g=4):
         self.name = name
         self.seed = seed
         if name == "decode8b":
@@ -158,7 +158,8 @@ class Workload:
             self.metric, self.unit = "GQA decode KV-read HBM GB/s", "GB/s"
         elif name == "verify":
             s = self.shape = wl.VERIFY
-            self.layers, self.Hq, self.T = 1, s.Hq, 4
+            # the verify sweep: T drafts in {4, 8}, G = Hq / Hkv in {1, 2, 4, 8}
+            self.layers, self.Hq, self.T = 1, verify_g * s.Hkv, verify_t
             self.lens0 = np.full(s.B, s.max_len - self.T, dtype=np.int64)
             self.n_new = np.full(s.B, self.T, dtype=np.int64)
             self.rollback_every = 1  # speculative verify: append T, attend, truncate back
@@ -444,12 +445,15 @@ def main():
     ap.add_argument("--impl", choices=["native", "reference"], default="native")
     ap.add_argument("--workload", choices=["decode8b", "verify", "prefill", "longctx"], default="decode8b")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--verify-t", type=int, choices=[4, 8], default=4, help="drafts per row (verify workload)")
+    ap.add_argument("--verify-g", type=int, choices=[1, 2, 4, 8], default=4,
+                    help="query heads per KV head, Hq = G * 8 (verify workload)")
     args = ap.parse_args()
 
     world = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
     local = int(os.environ.get("LOCAL_RANK", "0"))
-    w = Workload(args.workload)
+    w = Workload(args.workload, verify_t=args.verify_t, verify_g=args.verify_g)
     scale = 1e-12 if w.unit == "TFLOP/s" else 1e-9
 
     if args.impl == "reference":
