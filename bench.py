@@ -158,7 +158,7 @@ class Workload:
             self.metric, self.unit = "GQA decode KV-read HBM GB/s", "GB/s"
         elif name == "verify":
             s = self.shape = wl.VERIFY
-            # the verify sweep: T drafts in {4, 8}, G = Hq / Hkv in {1, 2, 4, 8}
+            # the verify sweep: T drafts in {4, 8} (16 beyond it), G = Hq / Hkv in {1, 2, 4, 8} (16 beyond it)
             self.layers, self.Hq, self.T = 1, verify_g * s.Hkv, verify_t
             self.lens0 = np.full(s.B, s.max_len - self.T, dtype=np.int64)
             self.n_new = np.full(s.B, self.T, dtype=np.int64)
@@ -202,15 +202,21 @@ class Workload:
         return kv_bytes(self.lens_at(i), s.Hkv, s.d) * self.layers
 
     @property
+    def tensor_core(self):
+        """The library runs attention on the tcgen05 kernel above 16 query rows per KV head."""
+        return (self.Hq // self.shape.Hkv) * self.T > 16
+
+    @property
     def kernel_name(self):
         """The dominant kernel of the timed attention call."""
-        if self.name == "prefill":
-            return "prefill_tc_kernel (tcgen05/TMEM; cut blocks merged in-kernel)"
+        if self.tensor_core:
+            rows = "128 positions per head" if self.T >= 128 else "packed rows g*T+t of a KV head"
+            return f"prefill_tc_kernel (tcgen05/TMEM, {rows}; cut items merged in-kernel)"
         return "decode_splitkv_bf16_kernel (+ combine_bf16_kernel" + (", append fused in)" if self.fused else ")")
 
     @property
     def kernel_source(self):
-        return "prefill_tc.cu" if self.name == "prefill" else "decode_bf16.cu"
+        return "prefill_tc.cu" if self.tensor_core else "decode_bf16.cu"
 
     @property
     def fused(self):
@@ -445,8 +451,8 @@ def main():
     ap.add_argument("--impl", choices=["native", "reference"], default="native")
     ap.add_argument("--workload", choices=["decode8b", "verify", "prefill", "longctx"], default="decode8b")
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--verify-t", type=int, choices=[4, 8], default=4, help="drafts per row (verify workload)")
-    ap.add_argument("--verify-g", type=int, choices=[1, 2, 4, 8], default=4,
+    ap.add_argument("--verify-t", type=int, choices=[4, 8, 16], default=4, help="drafts per row (verify workload)")
+    ap.add_argument("--verify-g", type=int, choices=[1, 2, 4, 8, 16], default=4,
                     help="query heads per KV head, Hq = G * 8 (verify workload)")
     args = ap.parse_args()
 

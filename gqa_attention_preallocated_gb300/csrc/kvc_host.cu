@@ -55,6 +55,11 @@ struct kvc_cache {
 
 namespace {
 
+// Query rows per KV head (G * T) above which attention runs on the tcgen05
+// kernel; at or below it, on the split-KV kernel (mma.sync, appends fused).
+constexpr int kTcMinRows = 16;
+constexpr int kTcMaxLen = 0xFFFF * 128;  // key tiles of a piece are packed in 16 bits
+
 thread_local std::string g_last_error;
 
 kvc_status fail(kvc_status s, const char* fmt, ...) __attribute__((format(printf, 2, 3)));
@@ -186,6 +191,9 @@ struct AttnPlan {
     int Hq = 0, G = 0, T = 0, R = 0;
     int mt = 0, RPB = 0, RB = 0, NB = 0, units = 0, ways = 1, part_rows = 0;
     size_t ws_err = 0, ws_plan = 0, ws_partials = 0, ws_total = 0;
+    // Least workspace the call runs with: the tensor-core path needs only the
+    // header (with less room it cuts fewer items into pieces).
+    size_t ws_min = 0;
 };
 
 size_t round_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
@@ -220,12 +228,14 @@ kvc_status plan_shape(const kvc_cache* c, int Hq, int T, int num_ctas, AttnPlan*
         pl->part_rows = std::min(pl->R, pl->RPB);
         pl->ws_partials = static_cast<size_t>(pl->units + num_ctas) * pl->ways * pl->part_rows *
                           (kHeadDimBf16 + 4) * sizeof(float);
-        if (pl->R > 64) {
-            // The chunked-prefill kernel: up to two partial slots (2 heads x
+        pl->ws_min = pl->ws_err + pl->ws_plan + pl->ws_partials;
+        if (pl->R > kTcMinRows) {
+            // The tensor-core kernel: up to two partial slots (2 row tiles x
             // 128 rows x (d + 4) floats) per SM share boundary.
             const size_t prefill = static_cast<size_t>(2) * std::min(num_ctas, kMaxCtas) * 2 * 128 *
                                    (kHeadDimBf16 + 4) * sizeof(float);
             pl->ws_partials = std::max(pl->ws_partials, prefill);
+            if (c->max_len <= kTcMaxLen) pl->ws_min = pl->ws_err + pl->ws_plan;
         }
         pl->ws_total = pl->ws_err + pl->ws_plan + pl->ws_partials;
     }
@@ -326,10 +336,14 @@ kvc_status do_attention(kvc_cache* c, int layer, const void* q, const AttnPlan& 
 
     kvc_status s = encode_layer_maps(c, layer);
     if (s) return s;
-    if (pl.R > 64 && k_new == nullptr && anc == nullptr && c->max_len <= 0xFFFF * 128) {
-        // Chunked prefill: tensor-core kernel, one CTA per piece.  Work items
-        // are (b, kvh, 128 positions, head pair); an item's key tiles cost its
-        // head count each, plus a fixed start-up cost per CTA.  The launch order
+    if (pl.R > kTcMinRows && k_new == nullptr && anc == nullptr && c->max_len <= kTcMaxLen) {
+        // Many query rows per KV head: tensor-core kernel, one CTA per piece.
+        // Work items are (b, kvh, row block, pair of 128-row tiles): with
+        // T >= 128, 128 positions of two query heads (mode 0); with T < 128 the
+        // G*T rows r = g*T + t of the KV head packed into 128-row tiles (mode 1),
+        // or all in one tile whose two TMEM buffers take alternate key tiles
+        // (mode 2, G*T <= 128).  An item's key tiles cost its tile count each
+        // (one in mode 2), plus a fixed start-up cost per CTA.  The launch order
         // comes from a longest-first list schedule simulated on the SMs (the
         // block scheduler hands the next CTA to the first SM that frees up):
         // an item that would run past the SMs' common finishing time is cut
@@ -354,8 +368,9 @@ kvc_status do_attention(kvc_cache* c, int layer, const void* q, const AttnPlan& 
         pp.G = pl.G;
         pp.T = pl.T;
         pp.max_len = c->max_len;
-        pp.ntb = (pl.T + 127) / 128;
-        pp.npair = (pl.G + 1) / 2;
+        pp.mode = pl.T >= 128 ? 0 : (pl.R <= 128 ? 2 : 1);
+        pp.ntb = pp.mode == 0 ? (pl.T + 127) / 128 : 1;
+        pp.npair = pp.mode == 0 ? (pl.G + 1) / 2 : (pl.R + 255) / 256;
         pp.window = c->window;
         pp.ring = c->ring ? 1 : 0;
         pp.pg = c->pg;
@@ -363,7 +378,18 @@ kvc_status do_attention(kvc_cache* c, int layer, const void* q, const AttnPlan& 
         for (int b = 0; b < c->B; ++b) {
             pp.prior[b] = static_cast<int>(lens[b] - n_new[b]);
             pp.n_new[b] = n_new[b];
-            for (int kvh = 0; kvh < c->Hkv; ++kvh)
+            for (int kvh = 0; kvh < c->Hkv && pp.mode != 0 && n_new[b] > 0; ++kvh) {
+                // Packed rows: the last key any row sees is prior + min(T, n_new) - 1,
+                // and the first key any row's window starts at is prior - W + 1 or later.
+                const int kmax = pp.prior[b] + std::min(pl.T, static_cast<int>(n_new[b])) - 1;
+                const int kfirst = c->window > 0 ? std::max(0, pp.prior[b] - c->window + 1) : 0;
+                for (int pr = 0; pr < pp.npair; ++pr) {
+                    const int code = (b * c->Hkv + kvh) * pp.npair + pr;
+                    const int cost = pp.mode == 2 ? 1 : std::min(2, (pl.R - pr * 256 + 127) / 128);
+                    items.push_back({code, kfirst / 128, kmax / 128 + 1, cost});
+                }
+            }
+            for (int kvh = 0; kvh < c->Hkv && pp.mode == 0; ++kvh)
                 for (int tb = 0; tb < pp.ntb; ++tb) {
                     const int t0 = tb * 128;
                     if (t0 >= n_new[b]) continue;
@@ -1239,9 +1265,9 @@ extern "C" kvc_status kvc_gqa_attention_noalloc(kvc_cache* c, int layer, const v
     if (dev != c->device) return fail(KVC_ERR_ARG, "current device %d is not the cache's device %d", dev, c->device);
     s = plan_shape(c, q_heads, T, c->num_sms, &pl);
     if (s) return s;
-    if (pl.ws_total > static_cast<size_t>(KVC_NOALLOC_SCRATCH_BYTES))
+    if (pl.ws_min > static_cast<size_t>(KVC_NOALLOC_SCRATCH_BYTES))
         return fail(KVC_ERR_WORKSPACE, "this call needs %zu bytes of scratch; the static scratch holds %zu",
-                    pl.ws_total, static_cast<size_t>(KVC_NOALLOC_SCRATCH_BYTES));
+                    pl.ws_min, static_cast<size_t>(KVC_NOALLOC_SCRATCH_BYTES));
     void* scratch = nullptr;
     s = noalloc_scratch_address(dev, &scratch);
     if (s) return s;

@@ -187,10 +187,17 @@ struct F32Params {
 cudaError_t launch_attn_f32(const F32Params& p, cudaStream_t stream);
 
 // ---------------------------------------------------------------------------
-// Chunked prefill on tcgen05 (bf16, d = 128, G*T > 64 query rows per KV head).
-// One CTA per item = (b, kvh, block of 128 query positions, pair of query
-// heads); items are packed as ((b * Hkv + kvh) * ntb + tb) * npair + pair and
-// listed longest first.
+// Attention on tcgen05 (bf16, d = 128) for many query rows per KV head.  One
+// CTA per piece of an item; items are packed as
+// ((b * Hkv + kvh) * ntb + tb) * npair + pair.  An item's query rows form up to
+// two 128-row tiles that share every K/V tile:
+//   mode 0 (chunked prefill, T >= 128): tile i = 128 positions tb*128 .. of
+//          query head kvh*G + 2*pair + i;
+//   mode 1 (packed, T < 128, G*T > 128): tile i = packed rows
+//          (2*pair + i)*128 .. of the KV head, row r = g*T + t (ntb = 1);
+//   mode 2 (packed, G*T <= 128): one tile of packed rows; the two TMEM S/O
+//          buffers and softmax warpgroups take alternate key tiles and their
+//          states are merged at the end (ntb = npair = 1).
 // ---------------------------------------------------------------------------
 constexpr int kMaxPrefillPieces = 1920;
 constexpr int kPrefillNoSlot = 0xFFF;   // piece covers all keys of its block: write out directly
@@ -206,6 +213,7 @@ struct PrefillParams {
     float* partials;  // [slot][2 heads][128 rows][d + 4]: O (d), m, l, pad
     int B, Hq, Hkv, G, T, max_len;
     int ntb, npair, n_pieces;
+    int mode;          // 0 positions, 1 packed rows in tile pairs, 2 one packed tile (see above)
     int window, ring;  // sliding window (0 = none) and ring storage, as in DecodeParams
     Paging pg;
     float scale_log2;

@@ -1,15 +1,22 @@
-// Chunked-prefill GQA attention on the 5th-generation tensor cores (tcgen05 + TMEM), bf16, d = 128.
+// GQA attention on the 5th-generation tensor cores (tcgen05 + TMEM), bf16,
+// d = 128, for calls with more than 16 query rows per KV head: chunked
+// prefill, speculative verify with large G*T.
 //
 // What it computes ("Implement grouped-query attention over a preallocated KV
 // cache...", "A strong answer", gqa_attention): query t < n_new[b] of head h
 // sits at position prior[b] + t (prior = lens - n_new) and attends to keys
 // 0 .. prior[b] + t of KV head h / G with softmax scale 1/sqrt(d).  Padded
-// queries (t >= n_new[b]) give 0.  This is the dense-contraction regime of the
-// method (T = chunk): QK^T and PV are 128 x 128 x 128 MMAs.
+// queries (t >= n_new[b]) give 0.  QK^T and PV are 128 x 128 x 128 MMAs.
 //
-// Work item = (row b, KV head, block of 128 query positions, pair of query
-// heads of that KV head's group): both heads share every K/V tile staged in
-// shared memory, so each 64 KB K/V tile feeds four 128x128x128 MMAs.
+// A work item's query rows form up to two 128-row tiles that share every K/V
+// tile staged in shared memory (each 64 KB K/V tile then feeds four
+// 128x128x128 MMAs):
+//   mode 0 (T >= 128): 128 positions of a pair of query heads of the group;
+//   mode 1 (T < 128): 128-row tiles of the G*T rows r = g*T + t of one KV
+//          head, packed (in [B, Hq, T, d] they are consecutive rows);
+//   mode 2 (G*T <= 128): one packed tile; the two TMEM S/O buffers and the two
+//          softmax warpgroups take alternate key tiles, so one buffer's softmax
+//          runs under the other's MMAs, and the two states are merged at the end.
 // Items are launched longest first (the host sorts them by key-tile count).
 //
 // Warp roles (12 warps):
@@ -20,8 +27,8 @@
 //               P_i as the TMEM A operand.  Issue order S0(j), S1(j), PV0(j),
 //               S0(j+1), PV1(j), S1(j+1), ... keeps the tensor core busy while
 //               each softmax warpgroup works on the other head's tile.
-//   warps 4-7   softmax of head 0 of the pair, one thread per query row
-//   warps 8-11  softmax of head 1 of the pair
+//   warps 4-7   softmax of row tile 0 (mode 2: even key tiles), one thread per query row
+//   warps 8-11  softmax of row tile 1 (mode 2: odd key tiles)
 // TMEM (512 columns): S0 [0,128), S1 [128,256), O0 [256,384), O1 [384,512).
 //
 // Softmax is online in base 2 (log2(e)/sqrt(d) folded into one scale) with a
@@ -165,12 +172,13 @@ __device__ __forceinline__ float fmax3(float a, float b, float c) {
     return d;
 }
 
-// One piece: a key-tile range of one work item (b, KV head, 128 query
-// positions, head pair).
+// One piece: a key-tile range of one work item (b, KV head, row block, pair).
 struct Piece {
-    int b, kvh, t0, h0, nh;      // row, KV head, first position, first head, heads (1 or 2)
+    int b, kvh, t0, h0, nh;      // row, KV head; mode 0: first position, first head; row tiles (1 or 2)
+    int pr0;                     // modes 1, 2: first packed row of tile 0 (row r = g*T + t of the KV head)
     int prior, nn;               // prior length and new tokens of row b
     int kmax, nkt_all;           // last visible key of the block, its key tiles
+    int full_below;              // keys <= this are visible to every valid row of the item
     int kt0, nkt;                // this piece's tiles: kt0 .. kt0 + nkt - 1
     int slot;                    // partial slot, or kPrefillNoSlot
     int kidx, npc;               // index of the piece within its block, pieces of the block
@@ -185,12 +193,26 @@ __device__ __forceinline__ Piece decode_piece(const PrefillParams& p, int idx) {
     code /= p.ntb;
     pc.kvh = code % p.Hkv;
     pc.b = code / p.Hkv;
-    pc.t0 = tb * 128;
-    pc.h0 = pc.kvh * p.G + 2 * pair;
-    pc.nh = min(2, p.G - 2 * pair);
     pc.prior = p.prior[pc.b];
     pc.nn = p.n_new[pc.b];
-    pc.kmax = pc.prior + min(pc.t0 + 127, pc.nn - 1);
+    if (p.mode == 0) {
+        pc.t0 = tb * 128;
+        pc.h0 = pc.kvh * p.G + 2 * pair;
+        pc.nh = min(2, p.G - 2 * pair);
+        pc.pr0 = 0;
+        pc.kmax = pc.prior + min(pc.t0 + 127, pc.nn - 1);
+        pc.full_below = pc.prior + pc.t0;
+    } else {
+        // Packed rows: every valid row has 0 <= t < min(T, nn), so keys up to
+        // prior are visible to all of them and prior + min(T, nn) - 1 is the
+        // last key any of them sees.
+        pc.t0 = 0;
+        pc.h0 = pc.kvh * p.G;
+        pc.pr0 = 2 * pair * 128;
+        pc.nh = (p.mode == 2) ? 1 : min(2, (p.G * p.T - pc.pr0 + 127) / 128);
+        pc.kmax = pc.prior + min(p.T, pc.nn) - 1;
+        pc.full_below = pc.prior;
+    }
     pc.nkt_all = pc.kmax / 128 + 1;
     const uint32_t tiles = p.piece_tiles[idx];
     pc.kt0 = static_cast<int>(tiles & 0xFFFF);
@@ -288,8 +310,9 @@ __device__ __noinline__ void split_epilogue(float* partials, int* err, uint32_t 
 }
 
 // kWin: the cache has a sliding window (and possibly ring storage); without
-// one the window code is compiled out.
-template <bool kWin>
+// one the window code is compiled out.  kAlt: mode 2 (one packed row tile,
+// alternate key tiles per TMEM buffer); modes 0 and 1 otherwise.
+template <bool kWin, bool kAlt>
 __global__ void __launch_bounds__(kThreadsPF, 1)
     prefill_tc_kernel(const __grid_constant__ PrefillParams p, const __grid_constant__ CUtensorMap tmQ,
                       const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmV) {
@@ -353,7 +376,7 @@ __global__ void __launch_bounds__(kThreadsPF, 1)
     const Piece pc = decode_piece(p, blockIdx.x);
     const int b = pc.b, kvh = pc.kvh, prior = pc.prior, nn = pc.nn, t0 = pc.t0, h0 = pc.h0, nh = pc.nh;
     const int kmax = pc.kmax, nkt_all = pc.nkt_all, kt0 = pc.kt0, nkt = pc.nkt;
-    const int full_below = prior + t0;                      // keys <= this are visible to every row
+    const int full_below = pc.full_below;                   // keys <= this are visible to every row
     const int unit_row0 = (b * p.Hkv + kvh) * p.max_len;    // first cache row of (b, kvh)
     // Window bounds of the block's rows: keys <= min_lo are outside every row's
     // window, keys > max_lo inside every row's window (-1: no window).
@@ -372,7 +395,9 @@ __global__ void __launch_bounds__(kThreadsPF, 1)
         if (lane == 0) {
             ptx::mbar_arrive_expect_tx(bar(kBarQ), nh * kTile128);
             for (int i = 0; i < nh; ++i) {
-                const int qrow = ((b * p.Hq) + h0 + i) * p.T + t0;
+                // mode 0: 128 positions of head h0 + i; modes 1, 2: 128 packed rows
+                const int qrow = (p.mode == 0) ? ((b * p.Hq) + h0 + i) * p.T + t0
+                                               : (b * p.Hq + h0) * p.T + pc.pr0 + i * 128;
                 for (int hf = 0; hf < 2; ++hf)
                     ptx::tma_load_2d(sbase + kOffQ + i * kTile128 + hf * kBoxBytes, &tmQ, hf * 64, qrow, bar(kBarQ));
             }
@@ -408,8 +433,8 @@ __global__ void __launch_bounds__(kThreadsPF, 1)
                 *abort_flag = 1;
             }
         };
-        auto issue_s = [&](int i, int j) {  // S_i = Q_i K_j^T
-            const uint32_t qa = sbase + kOffQ + i * kTile128, ka = sbase + kOffK + (j & 1) * kTile128;
+        auto issue_s = [&](int i, int j, int qi) {  // S_i = Q_qi K_j^T
+            const uint32_t qa = sbase + kOffQ + qi * kTile128, ka = sbase + kOffK + (j & 1) * kTile128;
 #pragma unroll
             for (int k = 0; k < 8; ++k) {
                 const uint32_t off = (k >> 2) * kBoxBytes + (k & 3) * 32;
@@ -417,21 +442,31 @@ __global__ void __launch_bounds__(kThreadsPF, 1)
             }
             mma_commit(bar(kBarS + i));
         };
-        auto issue_pv = [&](int i, int j) {  // O_i += P_i V_j (P_i in TMEM over S_i)
+        auto issue_pv = [&](int i, int j, bool acc) {  // O_i (+)= P_i V_j (P_i in TMEM over S_i)
             const uint32_t va = sbase + kOffV + (j & 1) * kTile128;
 #pragma unroll
             for (int k = 0; k < 8; ++k)
                 mma_ts(tmem + 256 + i * 128, tmem + i * 128 + k * 8, smem_desc(va + k * 2048, kBoxBytes, 1024), id_pv,
-                       (j > 0 || k > 0) ? 1u : 0u);
+                       (acc || k > 0) ? 1u : 0u);
             mma_commit(bar(kBarO + i));
         };
+        // Mode 2 (one packed row tile): key tile j goes to S/O buffer j & 1,
+        // which is also its K/V stage, so one buffer's softmax overlaps the
+        // other's MMAs.  Issue order S(0), S(1), PV(0), S(2), PV(1), S(3), ...
+        constexpr bool alt = kAlt;
         if (lane == 0) {
             wait(kBarQ, 0);
             wait(kBarKFull, 0);
             tc_fence_after();
-            issue_s(0, 0);
-            if (nh == 2) issue_s(1, 0);
+            issue_s(0, 0, 0);
+            if (!alt && nh == 2) issue_s(1, 0, 1);
             mma_commit(bar(kBarKEmpty + 0));
+            if (alt && nkt > 1) {
+                wait(kBarKFull + 1, 0);
+                tc_fence_after();
+                issue_s(1, 1, 0);
+                mma_commit(bar(kBarKEmpty + 1));
+            }
         }
         for (int j = 0; j < nkt; ++j) {
             const int s = j & 1;
@@ -456,23 +491,34 @@ __global__ void __launch_bounds__(kThreadsPF, 1)
                 ptx::fence_proxy_async_smem();
                 __syncwarp();
             }
-            if (lane == 0) {
+            if (lane == 0 && alt) {
+                wait(kBarP + s, (j >> 1) & 1);
+                tc_fence_after();
+                issue_pv(s, j, j >= 2);
+                mma_commit(bar(kBarVEmpty + s));
+                if (j + 2 < nkt) {
+                    wait(kBarKFull + s, ((j + 2) >> 1) & 1);
+                    tc_fence_after();
+                    issue_s(s, j + 2, 0);
+                    mma_commit(bar(kBarKEmpty + s));
+                }
+            } else if (lane == 0) {
                 wait(kBarP + 0, j & 1);
                 tc_fence_after();
-                issue_pv(0, j);
+                issue_pv(0, j, j > 0);
                 if (j + 1 < nkt) {
                     wait(kBarKFull + ((j + 1) & 1), ((j + 1) >> 1) & 1);
                     tc_fence_after();
-                    issue_s(0, j + 1);
+                    issue_s(0, j + 1, 0);
                 }
                 if (nh == 2) {
                     wait(kBarP + 1, j & 1);
                     tc_fence_after();
-                    issue_pv(1, j);
+                    issue_pv(1, j, j > 0);
                 }
                 mma_commit(bar(kBarVEmpty + s));
                 if (j + 1 < nkt) {
-                    if (nh == 2) issue_s(1, j + 1);
+                    if (nh == 2) issue_s(1, j + 1, 1);
                     mma_commit(bar(kBarKEmpty + ((j + 1) & 1)));
                 }
             }
@@ -480,18 +526,30 @@ __global__ void __launch_bounds__(kThreadsPF, 1)
         }
     } else if (warp >= 4) {
         // ------------------------------------------------------------ softmax (one thread per query row)
-        const int i = (warp - 4) >> 2;  // head of the pair
+        const int i = (warp - 4) >> 2;  // S/O buffer: row tile of the pair, or in mode 2 key-tile parity
         const int r = tid & 127;        // row in the block = TMEM lane
-        if (i < nh) {
+        constexpr bool alt = kAlt;
+        if (i < nh || alt) {
             const uint32_t lane_off = static_cast<uint32_t>((warp & 3) * 32) << 16;
             const uint32_t tS = tmem + lane_off + i * 128, tO = tmem + lane_off + 256 + i * 128;
-            const int t = t0 + r;
-            const bool valid = (t < nn) && (t < p.T);
-            const int lim = valid ? prior + t : -1;
+            int lim;
+            if (p.mode == 0) {
+                const int t = t0 + r;
+                lim = ((t < nn) && (t < p.T)) ? prior + t : -1;
+            } else {
+                const int pr = pc.pr0 + (alt ? 0 : i * 128) + r;  // packed row g*T + t of the KV head
+                const int t = pr % p.T;
+                lim = ((pr < p.G * p.T) && (t < nn)) ? prior + t : -1;
+            }
+            const bool valid = lim >= 0;
+            // key tiles of this buffer: all of the piece's, or in mode 2 every other one
+            const int jfirst = alt ? i : 0, jstep = alt ? 2 : 1;
+            const int nloc = alt ? (nkt - i + 1) / 2 : nkt;
             const int lo_row = (kWin && valid) ? lim - p.window : -(1 << 30);  // keys <= lo_row: outside the window
             float m_ref = -INFINITY, l = 0.f;
-            for (int j = 0; j < nkt; ++j) {
-                if (!ptx::mbar_wait_bounded(bar(kBarS + i), j & 1, *abort_flag ? 0ull : kWaitNs)) {
+            for (int jj = 0; jj < nloc; ++jj) {
+                const int j = jfirst + jj * jstep;
+                if (!ptx::mbar_wait_bounded(bar(kBarS + i), jj & 1, *abort_flag ? 0ull : kWaitNs)) {
                     atomicExch(p.err, kDevTimeoutFull);
                     *abort_flag = 1;
                 }
@@ -526,8 +584,8 @@ __global__ void __launch_bounds__(kThreadsPF, 1)
                     // stores are warp-collective, so the warp rescales together;
                     // rows that keep their reference scale by 1.
                     const float f = !move ? 1.f : (m_ref == -INFINITY) ? 0.f : ptx::ex2(m_ref - mx);
-                    if (j > 0) {
-                        if (!ptx::mbar_wait_bounded(bar(kBarO + i), (j - 1) & 1, *abort_flag ? 0ull : kWaitNs)) {
+                    if (jj > 0) {
+                        if (!ptx::mbar_wait_bounded(bar(kBarO + i), (jj - 1) & 1, *abort_flag ? 0ull : kWaitNs)) {
                             atomicExch(p.err, kDevTimeoutFull);
                             *abort_flag = 1;
                         }
@@ -586,14 +644,53 @@ __global__ void __launch_bounds__(kThreadsPF, 1)
                 if (lane == 0) ptx::mbar_arrive(bar(kBarP + i));
             }
             // epilogue: O_i / l for valid rows
-            if (!ptx::mbar_wait_bounded(bar(kBarO + i), (nkt - 1) & 1, *abort_flag ? 0ull : kWaitNs)) {
+            if (nloc > 0 && !ptx::mbar_wait_bounded(bar(kBarO + i), (nloc - 1) & 1, *abort_flag ? 0ull : kWaitNs)) {
                 atomicExch(p.err, kDevTimeoutFull);
                 *abort_flag = 1;
             }
             tc_fence_after();
-            __nv_bfloat16* dst = static_cast<__nv_bfloat16*>(p.out) +
-                                 ((static_cast<size_t>(b) * p.Hq + h0 + i) * p.T + t) * kD;
-            if (pc.slot != kPrefillNoSlot) {
+            if (alt) {
+                // Merge the odd-tile state (m, l, O_1) into the even-tile one:
+                // o = (2^(m0-M) O_0 + 2^(m1-M) O_1) / (2^(m0-M) l0 + 2^(m1-M) l1).
+                // Both buffers sit in the same TMEM lanes, so warpgroup 0 reads
+                // O_1 directly once warpgroup 1 has seen its last PV land.
+                float* ml1 = reinterpret_cast<float*>(smem + kOffQ + kTile128);  // second Q tile: unused here
+                if (i == 1) {
+                    ml1[r] = m_ref;
+                    ml1[128 + r] = l;
+                }
+                tc_fence_before();
+                ptx::named_barrier_sync(3, 256);
+                tc_fence_after();
+                if (i == 0 && nkt > 1) {
+                    const float m1 = ml1[r], l1 = ml1[128 + r];
+                    const float M = fmaxf(m_ref, m1);
+                    const float Mu = (M == -INFINITY) ? 0.f : M;
+                    const float f0 = (m_ref == -INFINITY) ? 0.f : ptx::ex2(m_ref - Mu);
+                    const float f1 = (m1 == -INFINITY) ? 0.f : ptx::ex2(m1 - Mu);
+#pragma unroll 1
+                    for (int c = 0; c < 4; ++c) {
+                        uint32_t w0[32], w1[32];
+                        tmem_ld32(tO + c * 32, w0);
+                        tmem_ld32(tO + 128 + c * 32, w1);
+                        tmem_ld_wait();
+#pragma unroll
+                        for (int e = 0; e < 32; ++e)
+                            w0[e] = __float_as_uint(__uint_as_float(w0[e]) * f0 + __uint_as_float(w1[e]) * f1);
+                        tmem_st32(tO + c * 32, w0);
+                    }
+                    tmem_st_wait();
+                    m_ref = M;
+                    l = l * f0 + l1 * f1;
+                }
+            }
+            // output row: head h0 + i, position t0 + r (mode 0), or packed row pr of the KV head
+            const int qrow = (p.mode == 0) ? ((b * p.Hq) + h0 + i) * p.T + t0 + r
+                                           : (b * p.Hq + h0) * p.T + pc.pr0 + (alt ? 0 : i * 128) + r;
+            __nv_bfloat16* dst = static_cast<__nv_bfloat16*>(p.out) + static_cast<size_t>(qrow) * kD;
+            if (alt && i == 1) {
+                // state handed to warpgroup 0
+            } else if (pc.slot != kPrefillNoSlot) {
                 split_epilogue(p.partials, p.err, tO, i, r, valid, m_ref, l, pc.slot, pc.kidx, pc.npc, dst, merge_flag);
             } else {
             const float inv = (valid && l > 0.f) ? 1.f / l : 0.f;
@@ -634,7 +731,8 @@ cudaError_t launch_prefill_tc(const PrefillParams& p, const CUtensorMap& tmQ, co
                               const CUtensorMap& tmV, cudaStream_t stream) {
     static bool attr_set = false;
     if (!attr_set) {
-        for (auto* k : {prefill_tc_kernel<false>, prefill_tc_kernel<true>}) {
+        for (auto* k : {prefill_tc_kernel<false, false>, prefill_tc_kernel<true, false>, prefill_tc_kernel<false, true>,
+                        prefill_tc_kernel<true, true>}) {
             cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                                  static_cast<int>(kSmemPF));
             if (e != cudaSuccess) return e;
@@ -651,8 +749,12 @@ cudaError_t launch_prefill_tc(const PrefillParams& p, const CUtensorMap& tmQ, co
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    cudaError_t e = (p.window > 0 || p.ring) ? cudaLaunchKernelEx(&cfg, prefill_tc_kernel<true>, p, tmQ, tmK, tmV)
-                                              : cudaLaunchKernelEx(&cfg, prefill_tc_kernel<false>, p, tmQ, tmK, tmV);
+    const bool win = p.window > 0 || p.ring;
+    const bool alt = p.mode == 2;
+    cudaError_t e = win ? (alt ? cudaLaunchKernelEx(&cfg, prefill_tc_kernel<true, true>, p, tmQ, tmK, tmV)
+                               : cudaLaunchKernelEx(&cfg, prefill_tc_kernel<true, false>, p, tmQ, tmK, tmV))
+                        : (alt ? cudaLaunchKernelEx(&cfg, prefill_tc_kernel<false, true>, p, tmQ, tmK, tmV)
+                               : cudaLaunchKernelEx(&cfg, prefill_tc_kernel<false, false>, p, tmQ, tmK, tmV));
     if (e != cudaSuccess) return e;
     return cudaGetLastError();
 }

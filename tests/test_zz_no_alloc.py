@@ -61,13 +61,34 @@ def test_noalloc_matches_workspace_entry_point_twice():
         assert err <= TOL_BF16, (call, err)
 
 
-def test_noalloc_rejects_oversized_calls():
+def test_noalloc_long_chunk_runs_in_the_static_scratch():
+    """A long prefill chunk (the tensor-core path needs only the workspace
+    header) runs through the static scratch and matches the workspace entry
+    point, although its full workspace is larger than the scratch."""
     if not torch.cuda.is_available():
         pytest.skip("needs a GPU")
     build_library()
-    B, Hkv, G, d, T = 4, 8, 4, 128, 512  # a long prefill chunk needs more than the static scratch
+    B, Hkv, G, d, T = 4, 8, 4, 128, 512
     cache = KVCache(1, B, Hkv, 1024, d)
     cache.append(0, _bf16(1, 1, (B, Hkv, T, d)), _bf16(1, 2, (B, Hkv, T, d)), np.full(B, T))
+    assert cache.workspace_bytes(Hkv * G, T) > (32 << 20)
+    q = _bf16(3, 3, (B, Hkv * G, T, d))
+    ref_out = cache.gqa_attention(0, q, np.full(B, T))
+    out = torch.full_like(q, float("nan"))
+    assert _noalloc(cache, q, np.full(B, T), out) == 0, _lib.lib().kvc_last_error()
+    torch.cuda.synchronize()
+    assert float((out.float() - ref_out.float()).abs().max()) <= TOL_BF16
+
+
+def test_noalloc_rejects_oversized_calls():
+    """A decode call on a very large batch needs more split-KV scratch than the
+    static array holds: refused before anything is enqueued."""
+    if not torch.cuda.is_available():
+        pytest.skip("needs a GPU")
+    build_library()
+    B, Hkv, G, d, T = 512, 8, 16, 128, 1
+    cache = KVCache(1, B, Hkv, 16, d)
+    cache.set_lens(0, np.full(B, 8))
     assert cache.workspace_bytes(Hkv * G, T) > (32 << 20)
     q = _bf16(3, 3, (B, Hkv * G, T, d))
     out = torch.zeros_like(q)
