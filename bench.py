@@ -203,8 +203,8 @@ class Workload:
 
     @property
     def tensor_core(self):
-        """The library runs attention on the tcgen05 kernel above 16 query rows per KV head."""
-        return (self.Hq // self.shape.Hkv) * self.T > 16
+        """The library runs attention on the tcgen05 kernel above 12 query rows per KV head."""
+        return (self.Hq // self.shape.Hkv) * self.T > 12
 
     @property
     def kernel_name(self):
@@ -220,8 +220,8 @@ class Workload:
 
     @property
     def fused(self):
-        """The library appends inside the attention launch when G*T <= 16 (warps own whole tiles)."""
-        return (self.Hq // self.shape.Hkv) * self.T <= 16
+        """The library appends inside the attention launch when G*T <= 12 (split-KV kernel, warps own whole tiles)."""
+        return (self.Hq // self.shape.Hkv) * self.T <= 12
 
     def kernel_bytes(self, i):
         """Algorithmic bytes of the timed attention call: live K/V + q + out (+ the append when fused)."""

@@ -1,5 +1,5 @@
 // GQA attention on the 5th-generation tensor cores (tcgen05 + TMEM), bf16,
-// d = 128, for calls with more than 16 query rows per KV head: chunked
+// d = 128, for calls with more than 12 query rows per KV head: chunked
 // prefill, speculative verify with large G*T.
 //
 // What it computes ("Implement grouped-query attention over a preallocated KV

@@ -184,10 +184,10 @@ kvc_status kvc_append_attention_tree(kvc_cache* c, int layer, const void* q, con
  * Its scratch is one static device array of KVC_NOALLOC_SCRATCH_BYTES
  * (32 MiB) inside the library: every GPU that loads the library holds it
  * until the process exits.  No cudaMalloc, cudaFree or other allocating
- * call is made.  Calls with more than 16 query rows per KV head (G * T)
+ * call is made.  Calls with more than 12 query rows per KV head (G * T)
  * run on the tensor-core kernel, which needs only the workspace header and
  * uses the rest of the array for the partials of the items it cuts; they
- * always fit.  A call with at most 16 rows per KV head whose split-KV
+ * always fit.  A call with at most 12 rows per KV head whose split-KV
  * scratch would exceed the array (very large batches; kvc_workspace_bytes
  * gives its size) is rejected with KVC_ERR_WORKSPACE before anything is
  * enqueued; decode shapes of batches up to 64 rows fit.
