@@ -67,7 +67,12 @@ def test_decode_step_matches_host_path(T, G):
         want = host.append_attention(0, q, k, v, nn)
         dev.decode_step(0, q, k, v, torch.from_numpy(nn.astype(np.int32)).cuda(), out_dev, ws)
         torch.cuda.synchronize()
-        assert torch.equal(out_dev, want), step
+        if G * T <= 12:
+            # both calls run the split-KV kernel: the same arithmetic, bit for bit
+            assert torch.equal(out_dev, want), step
+        else:
+            # the host path runs above 12 rows per KV head on the tensor-core kernel
+            assert float((out_dev.float() - want.float()).abs().max()) <= 2e-2, step
     assert dev.device_status(ws) == 0
     dev.lens_from_device()
     assert np.array_equal(dev.lens(0), host.lens(0))
