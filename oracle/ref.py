@@ -78,6 +78,23 @@ V live in pages of P tokens, and a per-row block table maps logical page
 a // P of row b to a physical page.  Attention is defined on the logical
 sequence: ``PagedOracleCache.view`` gathers every row through the table into
 an ordinary cache, and the ordinary attention runs on that.
+
+FP8 storage (p3 "16. Prefill, decode and the KV cache", exercise 4: keep the
+cache in FP8 E4M3 with one scale per head and dequantize on read; the
+bandwidth bullet of the same page gives the motive).  Readings where the page
+is silent (each also listed in the design notes):
+
+* E4M3 is the 8-bit format with 1 sign bit, 4 exponent bits (bias 7) and 3
+  mantissa bits: exponent field 0 holds the subnormals m/8 * 2^-6, fields
+  1..15 hold (1 + m/8) * 2^(e - 7), and exponent 15 with mantissa 7 is NaN;
+  there is no infinity, so the largest finite value is 448.
+* "One scale per head" is one positive scale per (layer, KV head), separate
+  for K and V, set by the caller while the layer is empty.
+* A value x is stored as the E4M3 code nearest to x * (1/s), where the
+  reciprocal 1/s and the product are each rounded to float32; ties go to
+  the code with an even mantissa, and values beyond +-448 saturate to +-448.
+* Attention reads code value * s (dequantize on read) and is otherwise the
+  ordinary attention.
 """
 
 from __future__ import annotations
@@ -103,6 +120,9 @@ __all__ = [
     "tree_corner_mask",
     "PagedOracleCache",
     "kv_cache_bytes",
+    "e4m3_value",
+    "e4m3_encode",
+    "e4m3_quantize",
 ]
 
 
@@ -157,6 +177,84 @@ def attend_one_query(q_vec: np.ndarray, K_rows: np.ndarray, V_rows: np.ndarray, 
     return p @ vals
 
 
+# ---------------------------------------------------------------------------
+# FP8 E4M3 (p3 exercise 4), written out from the format's definition.
+# ---------------------------------------------------------------------------
+
+
+def e4m3_value(code: int) -> float:
+    """The real number an E4M3 byte encodes (NaN for the two NaN codes)."""
+    code = int(code) & 0xFF
+    sign = -1.0 if code & 0x80 else 1.0
+    e = (code >> 3) & 0xF
+    m = code & 0x7
+    if e == 0xF and m == 0x7:
+        return math.nan
+    if e == 0:
+        return sign * (m / 8.0) * 2.0 ** -6
+    return sign * (1.0 + m / 8.0) * 2.0 ** (e - 7)
+
+
+def _e4m3_positive_table():
+    """(value, code) for the 127 non-negative finite codes, ascending."""
+    return [(e4m3_value(c), c) for c in range(0x7F)]
+
+
+def e4m3_encode(x: float) -> int:
+    """Nearest E4M3 code to x: ties to the even mantissa, beyond +-448 saturates to +-448, NaN to 0x7F."""
+    x = float(x)
+    if math.isnan(x):
+        return 0x7F
+    sign = 0x80 if (x < 0 or (x == 0 and math.copysign(1.0, x) < 0)) else 0x00
+    a = abs(x)
+    table = _e4m3_positive_table()
+    if a >= table[-1][0]:
+        return sign | table[-1][1]
+    for i in range(len(table) - 1):
+        lo, hi = table[i], table[i + 1]
+        if lo[0] <= a <= hi[0]:
+            if a - lo[0] < hi[0] - a:
+                return sign | lo[1]
+            if a - lo[0] > hi[0] - a:
+                return sign | hi[1]
+            return sign | (lo[1] if lo[1] % 2 == 0 else hi[1])
+    raise AssertionError("unreachable")
+
+
+def e4m3_encode_array(x) -> np.ndarray:
+    """``e4m3_encode`` applied to every element (same rule, vectorised with a sorted table)."""
+    x = np.asarray(x, dtype=np.float64)
+    table = _e4m3_positive_table()
+    vals = np.array([v for v, _ in table])
+    codes = np.array([c for _, c in table], dtype=np.int64)
+    a = np.abs(x)
+    hi = np.clip(np.searchsorted(vals, a, side="left"), 1, len(vals) - 1)  # vals[hi-1] < a <= vals[hi]
+    lo = hi - 1
+    d_lo, d_hi = a - vals[lo], vals[hi] - a
+    pick_hi = (d_hi < d_lo) | ((d_hi == d_lo) & (codes[lo] % 2 == 1))
+    out = np.where(pick_hi, codes[hi], codes[lo])
+    out = np.where(a >= vals[-1], codes[-1], out)
+    out = np.where(a == 0, 0, out)
+    neg = np.signbit(x)
+    out = np.where(neg, out | 0x80, out)
+    out = np.where(np.isnan(x), 0x7F, out)
+    return out.astype(np.uint8)
+
+
+def e4m3_quantize(x, scale: float) -> np.ndarray:
+    """Codes (uint8) of the values x stored with scale s: e4m3_encode(f32(x * f32(1/s)))."""
+    inv = np.float32(1.0) / np.float32(scale)
+    y = np.asarray(x, dtype=np.float64).astype(np.float32) * inv
+    return e4m3_encode_array(np.asarray(y, dtype=np.float32).astype(np.float64))
+
+
+def e4m3_dequantize(codes, scale: float) -> np.ndarray:
+    """Values read back from codes stored with scale s: value(code) * s."""
+    codes = np.asarray(codes, dtype=np.uint8)
+    lut = np.array([e4m3_value(c) for c in range(256)], dtype=np.float64)
+    return lut[codes] * float(scale)
+
+
 class OracleCache:
     """Preallocated KV cache with per-layer, per-row valid lengths.
 
@@ -177,6 +275,34 @@ class OracleCache:
         self.pos = [np.full((batch, max_len), -1, dtype=np.int64) for _ in range(layers)]
         self.window = 0   # 0: no window (keys 0..p)
         self.ring = False
+        # FP8 E4M3 storage: codes per slot, one scale per (layer, KV head) for K and for V
+        self.fp8 = False
+        self.k_code = self.v_code = None
+        self.k_scale = np.ones((layers, kv_heads))
+        self.v_scale = np.ones((layers, kv_heads))
+
+    def set_fp8(self) -> None:
+        """Store K and V as E4M3 codes (p3 exercise 4); only on an empty cache."""
+        if np.any(self.lens != 0):
+            raise CacheError("the storage format can only change on an empty cache")
+        self.fp8 = True
+        shape = (self.B, self.Hkv, self.max_len, self.d)
+        self.k_code = [np.zeros(shape, dtype=np.uint8) for _ in range(self.layers)]
+        self.v_code = [np.zeros(shape, dtype=np.uint8) for _ in range(self.layers)]
+
+    def set_kv_scales(self, layer: int, k_scale, v_scale) -> None:
+        """One positive finite scale per KV head for K and for V; only while the layer is empty."""
+        k_scale = np.asarray(k_scale, dtype=np.float64).reshape(-1)
+        v_scale = np.asarray(v_scale, dtype=np.float64).reshape(-1)
+        if k_scale.shape[0] != self.Hkv or v_scale.shape[0] != self.Hkv:
+            raise CacheError("one scale per KV head")
+        if not (np.all(np.isfinite(k_scale)) and np.all(np.isfinite(v_scale)) and np.all(k_scale > 0)
+                and np.all(v_scale > 0)):
+            raise CacheError("scales must be positive and finite")
+        if np.any(self.lens[layer] != 0):
+            raise CacheError("scales can only change while the layer is empty")
+        self.k_scale[layer] = k_scale
+        self.v_scale[layer] = v_scale
 
     def set_window(self, window: int, ring: bool = False) -> None:
         """Attention window W (0 = none) and ring storage (slot = position mod max_len).
@@ -230,8 +356,17 @@ class OracleCache:
             for t in range(int(n_new[b])):
                 a = int(lens[b]) + t
                 slot = self.slot_of(a)
-                self.k[layer][b, :, slot] = k_new[b, :, t]
-                self.v[layer][b, :, slot] = v_new[b, :, t]
+                if self.fp8:
+                    for h in range(self.Hkv):
+                        kc = e4m3_quantize(k_new[b, h, t], self.k_scale[layer, h])
+                        vc = e4m3_quantize(v_new[b, h, t], self.v_scale[layer, h])
+                        self.k_code[layer][b, h, slot] = kc
+                        self.v_code[layer][b, h, slot] = vc
+                        self.k[layer][b, h, slot] = e4m3_dequantize(kc, self.k_scale[layer, h])
+                        self.v[layer][b, h, slot] = e4m3_dequantize(vc, self.v_scale[layer, h])
+                else:
+                    self.k[layer][b, :, slot] = k_new[b, :, t]
+                    self.v[layer][b, :, slot] = v_new[b, :, t]
                 self.pos[layer][b, slot] = a
         self.lens[layer] = lens + n_new
 
