@@ -122,13 +122,34 @@ def visible_pairs(priors, n_new):
     return int(sum(int(n) * int(p) + int(n) * (int(n) + 1) // 2 for p, n in zip(priors, n_new)))
 
 
-def make_cache(shape, layers, lens0, seed):
+FP8_SCALE = 4.0 / 448  # N(0,1) content: 4 sigma maps to the largest E4M3 value
+
+
+def _fill_fp8_(dst: torch.Tensor, seed: int, stream: int, chunk: int = 1 << 26) -> None:
+    """Synthetic FP8 cache content: codes of normal(seed, stream) / FP8_SCALE (clamped to +-448)."""
+    flat = dst.view(-1)
+    for start in range(0, flat.numel(), chunk):
+        stop = min(flat.numel(), start + chunk)
+        idx = torch.arange(start, stop, dtype=torch.int64, device=dst.device)
+        x = wl.normal_at(seed, stream, idx).to(torch.float32) / FP8_SCALE
+        flat[start:stop] = x.clamp_(-448.0, 448.0).to(torch.float8_e4m3fn)
+
+
+def make_cache(shape, layers, lens0, seed, kv_dtype="bf16"):
     from gqa_attention_preallocated_gb300 import KVCache
 
-    cache = KVCache(layers, shape.B, shape.Hkv, shape.max_len, shape.d, dtype=torch.bfloat16, device="cuda")
+    fp8 = kv_dtype == "fp8"
+    cache = KVCache(layers, shape.B, shape.Hkv, shape.max_len, shape.d,
+                    dtype=torch.float8_e4m3fn if fp8 else torch.bfloat16, device="cuda")
     for layer in range(layers):
-        wl.fill_normal_(cache.k[layer], seed, wl.STREAM_CACHE_K + 16 * layer)
-        wl.fill_normal_(cache.v[layer], seed, wl.STREAM_CACHE_V + 16 * layer)
+        if fp8:
+            sc = np.full(shape.Hkv, FP8_SCALE, dtype=np.float32)
+            cache.set_kv_scales(layer, sc, sc)
+            _fill_fp8_(cache.k[layer], seed, wl.STREAM_CACHE_K + 16 * layer)
+            _fill_fp8_(cache.v[layer], seed, wl.STREAM_CACHE_V + 16 * layer)
+        else:
+            wl.fill_normal_(cache.k[layer], seed, wl.STREAM_CACHE_K + 16 * layer)
+            wl.fill_normal_(cache.v[layer], seed, wl.STREAM_CACHE_V + 16 * layer)
         cache.set_lens(layer, lens0)
     return cache
 
@@ -146,9 +167,11 @@ def step_inputs(shape, Hq, T, n_distinct, seed, device="cuda"):
 class Workload:
     """One named workload: set-up, one step, and the step's algorithmic work."""
 
-    def __init__(self, name, seed=0, verify_t=4, verify_g=4):
+    def __init__(self, name, seed=0, verify_t=4, verify_g=4, kv_dtype="bf16"):
         self.name = name
         self.seed = seed
+        self.kv_dtype = kv_dtype  # "bf16", or "fp8": E4M3 cache with one scale per KV head
+        self.esize = 1 if kv_dtype == "fp8" else 2
         if name == "decode8b":
             s = self.shape = wl.DECODE_8B
             self.layers, self.Hq, self.T = 1, s.Hq, 1
@@ -183,8 +206,10 @@ class Workload:
 
     def config(self):
         s = self.shape
-        return {"workload": s.name, "B": s.B, "Hq": self.Hq, "Hkv": s.Hkv, "d": s.d, "max_len": s.max_len,
+        return {"workload": s.name + ("_fp8_cache" if self.kv_dtype == "fp8" else ""), "B": s.B, "Hq": self.Hq,
+                "Hkv": s.Hkv, "d": s.d, "max_len": s.max_len,
                 "layers": self.layers, "T": self.T, "dtype": "bf16",
+                "kv_storage": "fp8_e4m3 (one scale per KV head)" if self.kv_dtype == "fp8" else "bf16",
                 "initial_lens": {"min": int(self.lens0.min()), "max": int(self.lens0.max()),
                                  "mean": float(self.lens0.mean())},
                 "l2": "inputs larger than L2 (live KV per step exceeds the 129 MB L2)" if self.name != "prefill"
@@ -199,12 +224,12 @@ class Workload:
         s = self.shape
         if self.unit == "TFLOP/s":
             return 4 * s.d * self.Hq * visible_pairs(self.lens0, self.n_new)
-        return kv_bytes(self.lens_at(i), s.Hkv, s.d) * self.layers
+        return kv_bytes(self.lens_at(i), s.Hkv, s.d, self.esize) * self.layers
 
     @property
     def tensor_core(self):
-        """The library runs attention on the tcgen05 kernel above 12 query rows per KV head."""
-        return (self.Hq // self.shape.Hkv) * self.T > 12
+        """The library runs bf16 attention on the tcgen05 kernel above 12 query rows per KV head."""
+        return (self.Hq // self.shape.Hkv) * self.T > 12 and self.kv_dtype == "bf16"
 
     @property
     def kernel_name(self):
@@ -220,15 +245,17 @@ class Workload:
 
     @property
     def fused(self):
-        """The library appends inside the attention launch when G*T <= 12 (split-KV kernel, warps own whole tiles)."""
-        return (self.Hq // self.shape.Hkv) * self.T <= 12
+        """The library appends inside the attention launch on the split-KV kernel with warps owning whole
+        tiles: G*T <= 12 (bf16), G*T <= 16 (FP8 caches, which have no tensor-core path)."""
+        return (self.Hq // self.shape.Hkv) * self.T <= (16 if self.kv_dtype == "fp8" else 12)
 
     def kernel_bytes(self, i):
         """Algorithmic bytes of the timed attention call: live K/V + q + out (+ the append when fused)."""
         s = self.shape
         qo = 2 * s.B * self.Hq * self.T * s.d * 2
-        app = 2 * int(np.sum(self.n_new)) * s.Hkv * s.d * 2 * 2 if self.fused else 0
-        return kv_bytes(self.lens_at(i), s.Hkv, s.d) + qo + app
+        # fused append: bf16 rows read, stored rows written (K and V)
+        app = 2 * int(np.sum(self.n_new)) * s.Hkv * s.d * (2 + self.esize) if self.fused else 0
+        return kv_bytes(self.lens_at(i), s.Hkv, s.d, self.esize) + qo + app
 
 
 def run_native(w: Workload, steps: int, warmup: int, rank: int, world: int):
@@ -236,7 +263,7 @@ def run_native(w: Workload, steps: int, warmup: int, rank: int, world: int):
 
     s = w.shape
     torch.cuda.synchronize()
-    cache = make_cache(s, w.layers, w.lens0, w.seed + rank)
+    cache = make_cache(s, w.layers, w.lens0, w.seed + rank, w.kv_dtype)
     n_distinct = min(max(steps, 1), 16)
     q, k, v = step_inputs(s, w.Hq, w.T, n_distinct, w.seed + rank)
     out = torch.empty_like(q[0])
@@ -454,12 +481,14 @@ def main():
     ap.add_argument("--verify-t", type=int, choices=[4, 8, 16], default=4, help="drafts per row (verify workload)")
     ap.add_argument("--verify-g", type=int, choices=[1, 2, 4, 8, 16], default=4,
                     help="query heads per KV head, Hq = G * 8 (verify workload)")
+    ap.add_argument("--kv-dtype", choices=["bf16", "fp8"], default="bf16",
+                    help="cache storage: bf16, or FP8 E4M3 with one scale per KV head")
     args = ap.parse_args()
 
     world = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
     local = int(os.environ.get("LOCAL_RANK", "0"))
-    w = Workload(args.workload, verify_t=args.verify_t, verify_g=args.verify_g)
+    w = Workload(args.workload, verify_t=args.verify_t, verify_g=args.verify_g, kv_dtype=args.kv_dtype)
     scale = 1e-12 if w.unit == "TFLOP/s" else 1e-9
 
     if args.impl == "reference":
@@ -508,7 +537,8 @@ def main():
     line = {
         "metric": w.metric, "value": value, "unit": w.unit, "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": ms / args.steps, "higher_is_better": True, "scaling": "weak",
-        "vs_baseline": None, "dtype": "bf16", "data": "synthetic (seeded counter-based generator, ~N(0,1))",
+        "vs_baseline": None, "dtype": "bf16" if w.kv_dtype == "bf16" else "fp8 storage, f16 MMA, fp32 accumulate",
+        "data": "synthetic (seeded counter-based generator, ~N(0,1))",
         "config": dict(w.config(), parallelism="replicas only" if world > 1 else "single GPU"),
         "roofline": roof,
         "e2e": {"value": e2e_value, "unit": w.unit, "h2d_bytes_per_step": res["e2e"]["h2d"],
@@ -543,7 +573,7 @@ def _committed_traffic(w: Workload, mean_kernel_bytes: float):
     """
     import hashlib
 
-    path = os.path.join(ROOT, "profiles", f"traffic_{w.name}.txt")
+    path = os.path.join(ROOT, "profiles", f"traffic_{w.name}{'_fp8' if w.kv_dtype == 'fp8' else ''}.txt")
     if not os.path.exists(path):
         return None
     kv = dict(line.strip().split("=", 1) for line in open(path) if "=" in line and not line.startswith("#"))

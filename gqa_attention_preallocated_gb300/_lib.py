@@ -11,7 +11,7 @@ import os
 _PKG = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(_PKG, "libkvc.so")
 
-KVC_F32, KVC_BF16 = 0, 1
+KVC_F32, KVC_BF16, KVC_FP8_E4M3 = 0, 1, 2
 STATUS_NAMES = {
     0: "KVC_OK",
     1: "KVC_ERR_ARG",
@@ -33,6 +33,7 @@ SIGNATURES = [
     ("kvc_create_paged", _I, [ctypes.POINTER(_VP), _I, _I, _I, _I, _I, _I, _I, _I, ctypes.POINTER(_VP),
                               ctypes.POINTER(_VP), _VP]),
     ("kvc_destroy", None, [_VP]),
+    ("kvc_set_kv_scales", _I, [_VP, _I, ctypes.POINTER(ctypes.c_float), ctypes.POINTER(ctypes.c_float)]),
     ("kvc_append", _I, [_VP, _I, _VP, _VP, _I, _I32P, _VP]),
     ("kvc_workspace_bytes", _SZ, [_VP, _I, _I]),
     ("kvc_gqa_attention", _I, [_VP, _I, _VP, _I, _I, _I32P, _VP, _VP, _SZ, _VP]),

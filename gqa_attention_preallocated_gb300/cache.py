@@ -17,12 +17,13 @@ import ctypes
 import numpy as np
 import torch
 
-from ._lib import KVC_BF16, KVC_F32, KVCError, check, lib
+from ._lib import KVC_BF16, KVC_F32, KVC_FP8_E4M3, KVCError, check, lib
 
 _I32P = ctypes.POINTER(ctypes.c_int32)
 _I64P = ctypes.POINTER(ctypes.c_int64)
 
-_DTYPES = {torch.float32: KVC_F32, torch.bfloat16: KVC_BF16}
+# storage dtype -> library dtype; an FP8 E4M3 cache takes bf16 q / k_new / v_new / out
+_DTYPES = {torch.float32: KVC_F32, torch.bfloat16: KVC_BF16, torch.float8_e4m3fn: KVC_FP8_E4M3}
 
 
 def _stream_ptr(device: torch.device, stream=None) -> int:
@@ -59,6 +60,7 @@ class KVCache:
             raise KVCError(1, f"unsupported dtype {dtype}")
         self.layers, self.B, self.Hkv, self.max_len, self.d = layers, batch, kv_heads, max_len, head_dim
         self.dtype = dtype
+        self.io_dtype = torch.bfloat16 if dtype == torch.float8_e4m3fn else dtype
         dev = torch.device(device)
         if dev.type == "cuda" and dev.index is None:
             dev = torch.device("cuda", torch.cuda.current_device())
@@ -119,6 +121,15 @@ class KVCache:
     def reset(self) -> None:
         check(lib().kvc_reset(self._h))
 
+    def set_kv_scales(self, layer: int, k_scale, v_scale) -> None:
+        """One K and one V scale per KV head of an FP8 E4M3 cache's layer (only while it is empty)."""
+        ks = np.ascontiguousarray(np.asarray(k_scale, dtype=np.float32).reshape(-1))
+        vs = np.ascontiguousarray(np.asarray(v_scale, dtype=np.float32).reshape(-1))
+        if ks.shape[0] != self.Hkv or vs.shape[0] != self.Hkv:
+            raise KVCError(1, f"k_scale and v_scale need {self.Hkv} entries")
+        fp = ctypes.POINTER(ctypes.c_float)
+        check(lib().kvc_set_kv_scales(self._h, layer, ks.ctypes.data_as(fp), vs.ctypes.data_as(fp)))
+
     def set_window(self, window: int, ring: bool = False) -> None:
         """Sliding window (0 = none) and ring storage (slot = position mod max_len), for every layer."""
         check(lib().kvc_set_window(self._h, int(window), 1 if ring else 0))
@@ -141,8 +152,8 @@ class KVCache:
         return self._ws
 
     def _check_tensor(self, t: torch.Tensor, shape, name: str) -> None:
-        if tuple(t.shape) != tuple(shape) or t.dtype != self.dtype or not t.is_contiguous() or t.device != self.device:
-            raise KVCError(1, f"{name} must be a contiguous {self.dtype} tensor of shape {tuple(shape)} on {self.device}")
+        if tuple(t.shape) != tuple(shape) or t.dtype != self.io_dtype or not t.is_contiguous() or t.device != self.device:
+            raise KVCError(1, f"{name} must be a contiguous {self.io_dtype} tensor of shape {tuple(shape)} on {self.device}")
 
     def append(self, layer: int, k_new: torch.Tensor, v_new: torch.Tensor, n_new, stream=None) -> None:
         """Write k_new[b, :, :n_new[b]] at each row's current length (in place)."""
@@ -322,6 +333,7 @@ class PagedKVCache(KVCache):
         self.page_size, self.num_pages, self.max_pages_per_row = page_size, num_pages, max_pages_per_row
         self.max_len = max_pages_per_row * page_size
         self.dtype, self.device = dtype, dev
+        self.io_dtype = torch.bfloat16 if dtype == torch.float8_e4m3fn else dtype
         shape = (num_pages, kv_heads, page_size, head_dim)
         self.k = [torch.empty(shape, dtype=dtype, device=dev) for _ in range(layers)]
         self.v = [torch.empty(shape, dtype=dtype, device=dev) for _ in range(layers)]

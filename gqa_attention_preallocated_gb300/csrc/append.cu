@@ -9,8 +9,17 @@
 // (h, K or V), blockIdx.z the row b.  In a ring cache ("Write the causal mask
 // for a decode step...", "A strong answer": a ring buffer whose physical index
 // is not the position) position a goes to slot a mod max_len.
+//
+// FP8 E4M3 caches ("16. Prefill, decode and the KV cache", exercise 4): the
+// bf16 rows are quantized on the way in, each value x of KV head h stored as
+// the E4M3 code of x * (1/scale[h]) (float32 reciprocal and product, round to
+// nearest even, saturating at +-448); a thread turns one 16-byte source
+// vector (8 values) into 8 bytes.
+
+#include <cuda_bf16.h>
 
 #include "kvc_internal.h"
+#include "ptx.cuh"
 
 namespace kvc {
 
@@ -35,6 +44,22 @@ __global__ void __launch_bounds__(kAppendThreads) kv_append_kernel(const __grid_
     const uint8_t* src = (is_v ? p.v_new : p.k_new) + unit * p.T * p.row_bytes;
     const uint4 val = __ldg(reinterpret_cast<const uint4*>(src) + vec);
     uint8_t* cache = is_v ? p.v_cache : p.k_cache;
+    if (p.fp8) {
+        const float inv = __frcp_rn(is_v ? p.vscale[h] : p.kscale[h]);
+        const uint32_t w[4] = {val.x, val.y, val.z, val.w};
+        uint32_t c[4];
+#pragma unroll
+        for (int i = 0; i < 4; ++i)  // bf16 pair -> float32 (exact) -> scaled -> two E4M3 bytes
+            c[i] = ptx::f32x2_to_e4m3x2(__fmul_rn(__uint_as_float(w[i] << 16), inv),
+                                        __fmul_rn(__uint_as_float(w[i] & 0xFFFF0000u), inv));
+        const uint2 q8 = make_uint2(c[0] | (c[1] << 16), c[2] | (c[3] << 16));
+        const int dst_row = p.row_bytes / 2;  // d bytes a cache row
+        const size_t byte = vec * 16, t = byte / p.row_bytes, off = (byte - t * p.row_bytes) / 2;
+        bool bad = false;
+        const int row = phys_row(p.pg, p.ring, p.Hkv, p.max_len, b, h, p.lens[b] + static_cast<int>(t), &bad);
+        if (!bad) *reinterpret_cast<uint2*>(cache + static_cast<size_t>(row) * dst_row + off) = q8;
+        return;
+    }
     if (!p.ring && !p.pg.table) {
         uint8_t* base = cache + unit * p.max_len * p.row_bytes;
         reinterpret_cast<uint4*>(base + static_cast<size_t>(p.lens[b]) * p.row_bytes)[vec] = val;

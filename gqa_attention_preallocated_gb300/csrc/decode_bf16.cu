@@ -49,15 +49,14 @@ namespace kvc {
 
 namespace {
 
-constexpr int kConsumerWarps = 4;
-constexpr int kConsumerThreads = kConsumerWarps * 32;
-constexpr int kThreads = kConsumerThreads + 32;
+constexpr int kConsumerWarps = 4;  // consumer warps, except FP8 caches with warps owning whole tiles
 constexpr int kD = kHeadDimBf16;
 constexpr int kHalfBytes = kKeyTile * 128;   // 64 keys x 64 dims x 2 B (one swizzled box)
 constexpr int kTileBytes = 2 * kHalfBytes;   // 64 keys x 128 dims
 constexpr int kStageBytes = 2 * kTileBytes;  // K tile + V tile
 constexpr int kPartStride = kD + 4;          // floats per partial row: O[128], m, l, pad
 constexpr uint64_t kWaitLimitNs = 2000000000ull;
+constexpr float kLazyRescale = 8.0f;  // log2 of the largest factor p may reach above the reference
 constexpr size_t kObufBytes = 3 * 16 * kD * sizeof(float);
 constexpr size_t kMlBytes = kConsumerWarps * 16 * 2 * sizeof(float);
 
@@ -68,19 +67,30 @@ constexpr size_t kMlBytes = kConsumerWarps * 16 * 2 * sizeof(float);
 // so no shared merge buffer is needed and the ring gets a seventh stage.  With
 // MT = 2 or 4 the warps split every tile and merge their states in shared
 // memory at the end of a unit.
-template <int MT>
+template <int MT, bool F8>
 struct Shape {
     static constexpr bool kTilePar = (MT == 1);                // warps own whole tiles
-    static constexpr int kStages = kTilePar ? 7 : 4;
-    static constexpr int kKeySlices = kTilePar ? 1 : kConsumerWarps / MT;
+    // bytes of one K (or V) tile of 64 keys: two 64-column boxes of bf16, or
+    // one 128-byte-row box of E4M3 codes
+    static constexpr int kTileB = F8 ? kKeyTile * 128 : kTileBytes;
+    static constexpr int kStageB = 2 * kTileB;
+    static constexpr int kStages = F8 ? (kTilePar ? 14 : 8) : (kTilePar ? 7 : 4);
+    // Consumer warps: with FP8 storage a tile holds half the bytes for the same
+    // MMA and conversion work, so one warp per SM sub-partition cannot keep up
+    // with HBM; seven tile-owning warps (two per sub-partition, with the
+    // producer) hide each other's latency.
+    static constexpr int kCW = (F8 && kTilePar) ? 7 : kConsumerWarps;
+    static constexpr int kCT = kCW * 32;
+    static constexpr int kThreads = kCT + 32;
+    static constexpr int kKeySlices = kTilePar ? 1 : kCW / MT;
     static constexpr int kKW = kKeyTile / kKeySlices;          // keys per warp per tile
     static constexpr int kMerge = kTilePar ? 1 : kKeySlices;   // states per m-tile merged in shared memory
-    static constexpr int kWays = kTilePar ? kConsumerWarps : 1;  // partial sub-slots per (unit, CTA)
+    static constexpr int kWays = kTilePar ? kCW : 1;  // partial sub-slots per (unit, CTA)
     static constexpr int kRPB = 16 * MT;
-    static constexpr int kEmptyCount = kTilePar ? 1 : kConsumerWarps;
+    static constexpr int kEmptyCount = kTilePar ? 1 : kCW;
     static constexpr size_t kObuf = kTilePar ? 0 : kObufBytes;
     static constexpr size_t kMl = kTilePar ? 0 : kMlBytes;
-    static constexpr size_t kSmem = 1024 + kStages * kStageBytes + kObuf + kMl + 2 * kStages * 8 + (kStages + 4) * 4;
+    static constexpr size_t kSmem = 1024 + kStages * kStageB + kObuf + kMl + 2 * kStages * 8 + (kStages + 4) * 4;
     static_assert(kSmem <= 232448, "shared memory per CTA");
 };
 
@@ -180,6 +190,12 @@ __device__ __forceinline__ int key_row(const DecodeParams& p, int b, int kvh, in
     return row;
 }
 
+// bf16 pair -> f16 pair (exact for |x| in f16's range: bf16 has fewer
+// significant bits); used for the queries of an FP8 cache's f16 MMAs.
+__device__ __forceinline__ uint32_t bf16x2_to_f16x2(uint32_t w) {
+    return ptx::pack_f16x2(__uint_as_float(w << 16), __uint_as_float(w & 0xFFFF0000u));
+}
+
 __device__ __forceinline__ void store_bf16x4(void* dst, float a, float b, float c, float d) {
     uint2 v;
     v.x = ptx::pack_bf16x2(a, b);
@@ -200,11 +216,11 @@ __device__ __forceinline__ bool wait_stage_tag(const volatile int* tag, int it, 
 
 // MT: m-tiles of 16 query rows; DP: the partition comes from a device plan;
 // TREE: draft-tree ancestor masks apply (compiled out otherwise).
-template <int MT, bool DP, bool TREE>
-__global__ void __launch_bounds__(kThreads, 1)
+template <int MT, bool DP, bool TREE, bool F8>
+__global__ void __launch_bounds__(Shape<MT, F8>::kThreads, 1)
     decode_splitkv_bf16_kernel(const __grid_constant__ DecodeParams p, const __grid_constant__ CUtensorMap tmK,
                                const __grid_constant__ CUtensorMap tmV) {
-    using S = Shape<MT>;
+    using S = Shape<MT, F8>;
     constexpr int kStages = S::kStages;
     constexpr int KW = S::kKW;
     constexpr int RPB = S::kRPB;
@@ -215,9 +231,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     uint8_t* stages = smem;
-    float* obuf = reinterpret_cast<float*>(smem + kStages * kStageBytes);
-    float* ml = reinterpret_cast<float*>(smem + kStages * kStageBytes + S::kObuf);
-    uint64_t* bars = reinterpret_cast<uint64_t*>(smem + kStages * kStageBytes + S::kObuf + S::kMl);
+    float* obuf = reinterpret_cast<float*>(smem + kStages * S::kStageB);
+    float* ml = reinterpret_cast<float*>(smem + kStages * S::kStageB + S::kObuf);
+    uint64_t* bars = reinterpret_cast<uint64_t*>(smem + kStages * S::kStageB + S::kObuf + S::kMl);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(bars + 2 * kStages);
     volatile int* stage_tag = abort_flag + 4;  // tile index the producer last put in each stage
 
@@ -241,7 +257,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         *abort_flag = 0;
         ptx::fence_barrier_init();
     }
-    if (warp == kConsumerWarps && lane == 0) {
+    if (warp == S::kCW && lane == 0) {
         ptx::tma_prefetch_desc(&tmK);
         ptx::tma_prefetch_desc(&tmV);
     }
@@ -258,7 +274,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     // Padded queries (t >= n_new[b]) output zeros; spread over the whole grid.
     {
         const int rows_total = p.B * p.Hq * p.T;
-        for (int row = blockIdx.x * kThreads + tid; row < rows_total; row += gridDim.x * kThreads) {
+        for (int row = blockIdx.x * S::kThreads + tid; row < rows_total; row += gridDim.x * S::kThreads) {
             const int t = row % p.T;
             const int b = row / (p.Hq * p.T);
             if (t >= wp.n_new(b)) {
@@ -271,7 +287,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (x0 >= x1) return;
 
     // ------------------------------------------------------------------ producer
-    if (warp == kConsumerWarps) {
+    if (warp == S::kCW) {
         if (lane == 0) {
             Cursor<DP> cur;
             cur.init(wp, x0);
@@ -288,13 +304,18 @@ __global__ void __launch_bounds__(kThreads, 1)
                 const int b = cur.q / p.RB;
                 const int row = key_row(p, b, cur.kvh, (cur.t0 + cur.j) * kKeyTile);
                 const uint32_t full = bar0 + 8 * s;
-                const uint32_t sK = stage0 + s * kStageBytes;
+                const uint32_t sK = stage0 + s * S::kStageB;
                 stage_tag[s] = it;
-                ptx::mbar_arrive_expect_tx(full, kStageBytes);
-                ptx::tma_load_2d(sK, &tmK, 0, row, full);
-                ptx::tma_load_2d(sK + kHalfBytes, &tmK, 64, row, full);
-                ptx::tma_load_2d(sK + kTileBytes, &tmV, 0, row, full);
-                ptx::tma_load_2d(sK + kTileBytes + kHalfBytes, &tmV, 64, row, full);
+                ptx::mbar_arrive_expect_tx(full, S::kStageB);
+                if constexpr (F8) {  // one 64-row x 128-byte box each
+                    ptx::tma_load_2d(sK, &tmK, 0, row, full);
+                    ptx::tma_load_2d(sK + S::kTileB, &tmV, 0, row, full);
+                } else {
+                    ptx::tma_load_2d(sK, &tmK, 0, row, full);
+                    ptx::tma_load_2d(sK + kHalfBytes, &tmK, 64, row, full);
+                    ptx::tma_load_2d(sK + kTileBytes, &tmV, 0, row, full);
+                    ptx::tma_load_2d(sK + kTileBytes + kHalfBytes, &tmV, 64, row, full);
+                }
                 ++issued;
                 cur.advance(wp);
             }
@@ -331,6 +352,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     // two rows, and the largest and smallest over the block's valid rows.
     int lo0 = -1, lo1 = -1, max_lo = -1, min_lo = -1;
     int seg_prior = 0, seg_nn = 0;
+    float sl2 = p.scale_log2;  // score scale in base 2 (times the K scale of an FP8 cache)
     uint4 new_row0 = make_uint4(0u, 0u, 0u, 0u);  // first appended row, lane's 16-byte chunk (K: lanes 0-15, V: 16-31)
 
     for (int x = x0, it = 0; x < x1; ++x, ++it) {
@@ -359,6 +381,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             seg_tiles = 0;
             seg_prior = prior;
             seg_nn = nn;
+            if constexpr (F8) sl2 = p.scale_log2 * p.kscale[kvh];
             if (S::kTilePar && p.append_new && nn > 0) {
                 const uint8_t* src = static_cast<const uint8_t*>((lane < 16) ? p.k_new : p.v_new) +
                                      (static_cast<size_t>(b) * p.Hkv + kvh) * p.Tn * (kD * 2) + (lane & 15) * 16;
@@ -378,10 +401,26 @@ __global__ void __launch_bounds__(kThreads, 1)
                 if (h == 0) lim0 = lim; else lim1 = lim;
                 const int lo = (p.window > 0 && lim >= 0) ? lim - p.window : -1;
                 if (h == 0) lo0 = lo; else lo1 = lo;
+                if constexpr (F8) {
+                    // f16 fragments with the head dimension permuted: MMA
+                    // k-step kk's logical columns 2*quad + {0, 1} and
+                    // 2*quad + {8, 9} read d = 32*quad + 4*kk + {0, 1} and
+                    // + {2, 3}, so each thread's K bytes are 32 consecutive ones.
 #pragma unroll
-                for (int kk = 0; kk < 8; ++kk) {
-                    qa[kk][h] = qrow ? *reinterpret_cast<const uint32_t*>(qrow + 16 * kk + 2 * quad) : 0u;
-                    qa[kk][2 + h] = qrow ? *reinterpret_cast<const uint32_t*>(qrow + 16 * kk + 8 + 2 * quad) : 0u;
+                    for (int c = 0; c < 4; ++c) {
+                        const uint4 w = qrow ? __ldg(reinterpret_cast<const uint4*>(qrow + 32 * quad) + c)
+                                             : make_uint4(0u, 0u, 0u, 0u);
+                        qa[2 * c][h] = bf16x2_to_f16x2(w.x);
+                        qa[2 * c][2 + h] = bf16x2_to_f16x2(w.y);
+                        qa[2 * c + 1][h] = bf16x2_to_f16x2(w.z);
+                        qa[2 * c + 1][2 + h] = bf16x2_to_f16x2(w.w);
+                    }
+                } else {
+#pragma unroll
+                    for (int kk = 0; kk < 8; ++kk) {
+                        qa[kk][h] = qrow ? *reinterpret_cast<const uint32_t*>(qrow + 16 * kk + 2 * quad) : 0u;
+                        qa[kk][2 + h] = qrow ? *reinterpret_cast<const uint32_t*>(qrow + 16 * kk + 8 + 2 * quad) : 0u;
+                    }
                 }
             }
 #pragma unroll
@@ -390,7 +429,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             l0 = l1 = 0.f;
         }
 
-        const bool mine = S::kTilePar ? ((it & (kConsumerWarps - 1)) == warp) : true;
+        const bool mine = S::kTilePar ? ((it % S::kCW) == warp) : true;
         if (mine) {
             ++seg_tiles;
             // On expiry the warp records the error and carries on with whatever
@@ -413,8 +452,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                 *abort_flag = 1;
             }
 
-            const uint32_t sK = stage0 + s * kStageBytes;
-            const uint32_t sV = sK + kTileBytes;
+            const uint32_t sK = stage0 + s * S::kStageB;
+            const uint32_t sV = sK + S::kTileB;
             const int tile0 = (cur.t0 + j) * kKeyTile;  // first key position of the tile
 
             if (S::kTilePar && p.append_new) {
@@ -424,20 +463,41 @@ __global__ void __launch_bounds__(kThreads, 1)
                 // the cache (this tile is processed exactly once).
                 const int lo = max(seg_prior, tile0), hi = min(seg_prior + seg_nn, tile0 + kKeyTile);
                 if (lo < hi) {
-                    const int chunk = lane & 15;  // 16-byte chunk of the 256-byte row
+                    const int chunk = lane & 15;  // 16-byte chunk of the 256-byte bf16 row
                     const bool is_v = lane >= 16;
                     const size_t unit = static_cast<size_t>(b) * p.Hkv + kvh;
                     const uint8_t* src = static_cast<const uint8_t*>(is_v ? p.v_new : p.k_new) + unit * p.Tn * (kD * 2);
                     uint8_t* dst = static_cast<uint8_t*>(is_v ? p.v_cache : p.k_cache);
                     bool bad = false;
                     const int row0 = phys_row(p.pg, p.ring, p.Hkv, p.max_len, b, kvh, tile0, &bad) - tile0;  // the tile's rows are contiguous
-                    uint8_t* stg = stages + s * kStageBytes + (is_v ? kTileBytes : 0) + (chunk >> 3) * kHalfBytes;
-                    for (int pos = lo; pos < hi; ++pos) {
-                        const int t = pos - seg_prior, r = pos - tile0;
-                        const uint4 val = (t == 0) ? new_row0
-                                                   : __ldg(reinterpret_cast<const uint4*>(src + t * (kD * 2) + chunk * 16));
-                        *reinterpret_cast<uint4*>(stg + r * 128 + (((chunk & 7) ^ (r & 7)) << 4)) = val;
-                        if (!bad) *reinterpret_cast<uint4*>(dst + static_cast<size_t>(row0 + pos) * (kD * 2) + chunk * 16) = val;
+                    if constexpr (F8) {
+                        // quantize: code of x * (1/scale), 8 values -> 8 bytes at
+                        // bytes 8*chunk .. of the 128-byte row
+                        const float inv = __frcp_rn(is_v ? p.vscale[kvh] : p.kscale[kvh]);
+                        uint8_t* stg = stages + s * S::kStageB + (is_v ? S::kTileB : 0);
+                        for (int pos = lo; pos < hi; ++pos) {
+                            const int t = pos - seg_prior, r = pos - tile0;
+                            const uint4 val = (t == 0) ? new_row0
+                                                       : __ldg(reinterpret_cast<const uint4*>(src + t * (kD * 2) + chunk * 16));
+                            const uint32_t w[4] = {val.x, val.y, val.z, val.w};
+                            uint32_t c[4];
+#pragma unroll
+                            for (int i = 0; i < 4; ++i)
+                                c[i] = ptx::f32x2_to_e4m3x2(__fmul_rn(__uint_as_float(w[i] << 16), inv),
+                                                            __fmul_rn(__uint_as_float(w[i] & 0xFFFF0000u), inv));
+                            const uint2 q8 = make_uint2(c[0] | (c[1] << 16), c[2] | (c[3] << 16));
+                            *reinterpret_cast<uint2*>(stg + r * 128 + ((((chunk >> 1) ^ (r & 7))) << 4) + (chunk & 1) * 8) = q8;
+                            if (!bad) *reinterpret_cast<uint2*>(dst + static_cast<size_t>(row0 + pos) * kD + chunk * 8) = q8;
+                        }
+                    } else {
+                        uint8_t* stg = stages + s * S::kStageB + (is_v ? kTileBytes : 0) + (chunk >> 3) * kHalfBytes;
+                        for (int pos = lo; pos < hi; ++pos) {
+                            const int t = pos - seg_prior, r = pos - tile0;
+                            const uint4 val = (t == 0) ? new_row0
+                                                       : __ldg(reinterpret_cast<const uint4*>(src + t * (kD * 2) + chunk * 16));
+                            *reinterpret_cast<uint4*>(stg + r * 128 + (((chunk & 7) ^ (r & 7)) << 4)) = val;
+                            if (!bad) *reinterpret_cast<uint4*>(dst + static_cast<size_t>(row0 + pos) * (kD * 2) + chunk * 16) = val;
+                        }
                     }
                     ptx::fence_proxy_async_smem();
                     __syncwarp();
@@ -449,32 +509,32 @@ __global__ void __launch_bounds__(kThreads, 1)
                 // lens may hold NaN; their probabilities are 0 but 0 * NaN is NaN).
                 const int vr0 = extent - tile0;
                 const int per_half = (kKeyTile - vr0) * 8;
-                uint8_t* vbase = stages + s * kStageBytes + kTileBytes;
+                uint8_t* vbase = stages + s * S::kStageB + S::kTileB;
                 const int t0 = S::kTilePar ? lane : tid;
-                const int step = S::kTilePar ? 32 : kConsumerThreads;
-                for (int idx = t0; idx < 2 * per_half; idx += step) {
+                const int step = S::kTilePar ? 32 : S::kCT;
+                for (int idx = t0; idx < (F8 ? 1 : 2) * per_half; idx += step) {
                     const int hf = idx / per_half, rem = idx - hf * per_half;
                     *reinterpret_cast<uint4*>(vbase + hf * kHalfBytes + (vr0 + (rem >> 3)) * 128 + (rem & 7) * 16) =
                         make_uint4(0u, 0u, 0u, 0u);
                 }
                 ptx::fence_proxy_async_smem();
-                if (S::kTilePar) __syncwarp(); else ptx::named_barrier_sync(1, kConsumerThreads);
+                if (S::kTilePar) __syncwarp(); else ptx::named_barrier_sync(1, S::kCT);
             }
             if (tile0 <= min_lo) {
                 // Clear V rows outside every row's window as well (a stale slot
                 // must never meet p = 0).
                 const int vr1 = min(kKeyTile, min_lo - tile0 + 1);
                 const int per_half = vr1 * 8;
-                uint8_t* vbase = stages + s * kStageBytes + kTileBytes;
+                uint8_t* vbase = stages + s * S::kStageB + S::kTileB;
                 const int t0 = S::kTilePar ? lane : tid;
-                const int step = S::kTilePar ? 32 : kConsumerThreads;
-                for (int idx = t0; idx < 2 * per_half; idx += step) {
+                const int step = S::kTilePar ? 32 : S::kCT;
+                for (int idx = t0; idx < (F8 ? 1 : 2) * per_half; idx += step) {
                     const int hf = idx / per_half, rem = idx - hf * per_half;
                     *reinterpret_cast<uint4*>(vbase + hf * kHalfBytes + (rem >> 3) * 128 + (rem & 7) * 16) =
                         make_uint4(0u, 0u, 0u, 0u);
                 }
                 ptx::fence_proxy_async_smem();
-                if (S::kTilePar) __syncwarp(); else ptx::named_barrier_sync(1, kConsumerThreads);
+                if (S::kTilePar) __syncwarp(); else ptx::named_barrier_sync(1, S::kCT);
             }
             // With a draft tree only tiles wholly before the chunk are free of the mask.
             const bool full_tile = (tile0 + kKeyTile - 1 <= min_lim) && (tile0 > max_lo) &&
@@ -484,38 +544,62 @@ __global__ void __launch_bounds__(kThreads, 1)
             float sc[NBS][4];
 #pragma unroll
             for (int nb = 0; nb < NBS; ++nb) sc[nb][0] = sc[nb][1] = sc[nb][2] = sc[nb][3] = 0.f;
+            if constexpr (F8) {
+                // Key n-block nb: this thread's key is koff + 8*nb + lane/4, and
+                // its 32 bytes d = 32*quad .. 32*quad + 31 (two swizzled 16-byte
+                // chunks) hold k-step kk's four values at bytes 4*kk .. 4*kk + 3.
 #pragma unroll
-            for (int kk = 0; kk < 8; ++kk) {
+                for (int nb = 0; nb < NBS; ++nb) {
+                    const int key = koff + nb * 8 + (lane >> 2);
+                    const uint32_t row = sK + key * 128;
+                    const uint4 u0 = ptx::ld_shared_v4(row + (((2 * quad) ^ (key & 7)) << 4));
+                    const uint4 u1 = ptx::ld_shared_v4(row + (((2 * quad + 1) ^ (key & 7)) << 4));
+                    const uint32_t w[8] = {u0.x, u0.y, u0.z, u0.w, u1.x, u1.y, u1.z, u1.w};
 #pragma unroll
-                for (int kb = 0; kb < KB; ++kb) {
-                    const int mi = lane >> 3;
-                    const int key = koff + kb * 16 + (mi >> 1) * 8 + (lane & 7);
-                    const int chunk = 2 * kk + (mi & 1);
-                    const uint32_t addr = sK + (chunk >> 3) * kHalfBytes + key * 128 + (((chunk & 7) ^ (key & 7)) << 4);
-                    uint32_t b0, b1, b2, b3;
-                    ptx::ldmatrix_x4(addr, b0, b1, b2, b3);
-                    ptx::mma_bf16_16816(sc[2 * kb], qa[kk], b0, b1);
-                    ptx::mma_bf16_16816(sc[2 * kb + 1], qa[kk], b2, b3);
+                    for (int kk = 0; kk < 8; ++kk) {
+                        uint32_t b0, b1;
+                        ptx::e4m3x4_to_f16x2x2(w[kk], b0, b1);
+                        ptx::mma_f16_16816(sc[nb], qa[kk], b0, b1);
+                    }
+                }
+            } else {
+#pragma unroll
+                for (int kk = 0; kk < 8; ++kk) {
+#pragma unroll
+                    for (int kb = 0; kb < KB; ++kb) {
+                        const int mi = lane >> 3;
+                        const int key = koff + kb * 16 + (mi >> 1) * 8 + (lane & 7);
+                        const int chunk = 2 * kk + (mi & 1);
+                        const uint32_t addr = sK + (chunk >> 3) * kHalfBytes + key * 128 + (((chunk & 7) ^ (key & 7)) << 4);
+                        uint32_t b0, b1, b2, b3;
+                        ptx::ldmatrix_x4(addr, b0, b1, b2, b3);
+                        ptx::mma_bf16_16816(sc[2 * kb], qa[kk], b0, b1);
+                        ptx::mma_bf16_16816(sc[2 * kb + 1], qa[kk], b2, b3);
+                    }
                 }
             }
 
             // Mask (diagonal / ragged tiles only) and online softmax in base 2.
+            // The row maximum is taken on the raw scores (the scale is
+            // positive) and the scale is folded into the exponent's FMA.  The
+            // reference used for the exponentials only moves when a row's
+            // maximum passes it by more than kLazyRescale (a factor 2^8 at
+            // most on p), and only then are O and l rescaled; O, l and the
+            // stored m share that reference, so the result is exact.
             const int kbase = tile0 + koff + 2 * quad;
             float mx0 = -INFINITY, mx1 = -INFINITY;
 #pragma unroll
             for (int nb = 0; nb < NBS; ++nb) {
+                if (!full_tile) {
 #pragma unroll
-                for (int e = 0; e < 4; ++e) {
-                    float v = sc[nb][e] * p.scale_log2;
-                    if (!full_tile) {
+                    for (int e = 0; e < 4; ++e) {
                         const int key = kbase + nb * 8 + (e & 1);
                         const int lim = (e < 2) ? lim0 : lim1;
-                        if (key > lim || key <= ((e < 2) ? lo0 : lo1)) v = -INFINITY;
+                        if (key > lim || key <= ((e < 2) ? lo0 : lo1)) sc[nb][e] = -INFINITY;
                         else if (TREE && key >= seg_prior &&
                                  !((p.anc[b * p.T + (lim - seg_prior)] >> (key - seg_prior)) & 1ull))
-                            v = -INFINITY;  // a draft token off this query's path to the root
+                            sc[nb][e] = -INFINITY;  // a draft token off this query's path to the root
                     }
-                    sc[nb][e] = v;
                 }
                 mx0 = fmaxf(mx0, fmaxf(sc[nb][0], sc[nb][1]));
                 mx1 = fmaxf(mx1, fmaxf(sc[nb][2], sc[nb][3]));
@@ -524,35 +608,70 @@ __global__ void __launch_bounds__(kThreads, 1)
             mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, 2));
             mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, 1));
             mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, 2));
-            const float mn0 = fmaxf(m0, mx0), mn1 = fmaxf(m1, mx1);
-            const float mu0 = (mn0 == -INFINITY) ? 0.f : mn0;
-            const float mu1 = (mn1 == -INFINITY) ? 0.f : mn1;
-            const float al0 = ptx::ex2(m0 - mu0), al1 = ptx::ex2(m1 - mu1);
-            m0 = mn0;
-            m1 = mn1;
+            mx0 *= sl2;  // -inf stays -inf
+            mx1 *= sl2;
+            const bool mv0 = mx0 > m0 + kLazyRescale, mv1 = mx1 > m1 + kLazyRescale;
+            if (mv0 || mv1) {
+                const float n0 = mv0 ? mx0 : m0, n1 = mv1 ? mx1 : m1;
+                const float al0 = (m0 == -INFINITY) ? 0.f : ptx::ex2(m0 - n0);
+                const float al1 = (m1 == -INFINITY) ? 0.f : ptx::ex2(m1 - n1);
+                l0 *= al0;
+                l1 *= al1;
+#pragma unroll
+                for (int nb = 0; nb < 16; ++nb) {
+                    o[nb][0] *= al0;
+                    o[nb][1] *= al0;
+                    o[nb][2] *= al1;
+                    o[nb][3] *= al1;
+                }
+                m0 = n0;
+                m1 = n1;
+            }
+            const float nmu0 = (m0 == -INFINITY) ? 0.f : -m0;
+            const float nmu1 = (m1 == -INFINITY) ? 0.f : -m1;
             float ps0 = 0.f, ps1 = 0.f;
 #pragma unroll
             for (int nb = 0; nb < NBS; ++nb) {
-                sc[nb][0] = ptx::ex2(sc[nb][0] - mu0);
-                sc[nb][1] = ptx::ex2(sc[nb][1] - mu0);
-                sc[nb][2] = ptx::ex2(sc[nb][2] - mu1);
-                sc[nb][3] = ptx::ex2(sc[nb][3] - mu1);
+                sc[nb][0] = ptx::ex2(fmaf(sc[nb][0], sl2, nmu0));
+                sc[nb][1] = ptx::ex2(fmaf(sc[nb][1], sl2, nmu0));
+                sc[nb][2] = ptx::ex2(fmaf(sc[nb][2], sl2, nmu1));
+                sc[nb][3] = ptx::ex2(fmaf(sc[nb][3], sl2, nmu1));
                 ps0 += sc[nb][0] + sc[nb][1];
                 ps1 += sc[nb][2] + sc[nb][3];
             }
-            l0 = l0 * al0 + ps0;
-            l1 = l1 * al1 + ps1;
-#pragma unroll
-            for (int nb = 0; nb < 16; ++nb) {
-                o[nb][0] *= al0;
-                o[nb][1] *= al0;
-                o[nb][2] *= al1;
-                o[nb][3] *= al1;
-            }
+            l0 += ps0;
+            l1 += ps1;
 
             // O += P V.
 #pragma unroll
-            for (int kb = 0; kb < KB; ++kb) {
+            for (int kb = 0; kb < KB && F8; ++kb) {
+                // P (f16) x V (E4M3 -> f16).  Output n-block jd, column
+                // lane/4 = g stands for d = 16*g + jd, so this thread reads one
+                // 16-byte chunk (g) of each of its four key rows, and the two
+                // keys of a B register pair come from two rows (byte permute).
+                uint32_t a[4];
+                a[0] = ptx::pack_f16x2(sc[2 * kb][0], sc[2 * kb][1]);
+                a[1] = ptx::pack_f16x2(sc[2 * kb][2], sc[2 * kb][3]);
+                a[2] = ptx::pack_f16x2(sc[2 * kb + 1][0], sc[2 * kb + 1][1]);
+                a[3] = ptx::pack_f16x2(sc[2 * kb + 1][2], sc[2 * kb + 1][3]);
+                const int k0 = koff + kb * 16 + 2 * quad, g = lane >> 2;
+                auto vrow = [&](int k) { return ptx::ld_shared_v4(sV + k * 128 + ((g ^ (k & 7)) << 4)); };
+                const uint4 r0 = vrow(k0), r1 = vrow(k0 + 1), r8 = vrow(k0 + 8), r9 = vrow(k0 + 9);
+                const uint32_t x0[4] = {r0.x, r0.y, r0.z, r0.w}, x1[4] = {r1.x, r1.y, r1.z, r1.w};
+                const uint32_t x8[4] = {r8.x, r8.y, r8.z, r8.w}, x9[4] = {r9.x, r9.y, r9.z, r9.w};
+#pragma unroll
+                for (int i = 0; i < 4; ++i) {
+                    uint32_t b0[4], b1[4];  // n-blocks 4i .. 4i+3: keys (k0, k0+1) and (k0+8, k0+9)
+                    ptx::e4m3x4_to_f16x2x2(ptx::prmt(x0[i], x1[i], 0x5140), b0[0], b0[1]);
+                    ptx::e4m3x4_to_f16x2x2(ptx::prmt(x0[i], x1[i], 0x7362), b0[2], b0[3]);
+                    ptx::e4m3x4_to_f16x2x2(ptx::prmt(x8[i], x9[i], 0x5140), b1[0], b1[1]);
+                    ptx::e4m3x4_to_f16x2x2(ptx::prmt(x8[i], x9[i], 0x7362), b1[2], b1[3]);
+#pragma unroll
+                    for (int m = 0; m < 4; ++m) ptx::mma_f16_16816(o[4 * i + m], a, b0[m], b1[m]);
+                }
+            }
+#pragma unroll
+            for (int kb = 0; kb < KB && !F8; ++kb) {
                 uint32_t a[4];
                 a[0] = ptx::pack_bf16x2(sc[2 * kb][0], sc[2 * kb][1]);
                 a[1] = ptx::pack_bf16x2(sc[2 * kb][2], sc[2 * kb][3]);
@@ -590,7 +709,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     ml[(warp * 16 + r0 + 8) * 2 + 0] = m1;
                     ml[(warp * 16 + r0 + 8) * 2 + 1] = l1;
                 }
-                ptx::named_barrier_sync(1, kConsumerThreads);
+                ptx::named_barrier_sync(1, S::kCT);
                 float mf0 = -INFINITY, mf1 = -INFINITY;
 #pragma unroll
                 for (int k2 = 0; k2 < NM; ++k2) {
@@ -624,7 +743,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                         *reinterpret_cast<float2*>(ob + (r0 + 8) * kD + col) = make_float2(o[nb][2], o[nb][3]);
                     }
                 }
-                ptx::named_barrier_sync(1, kConsumerThreads);
+                ptx::named_barrier_sync(1, S::kCT);
                 if (ms == 0) {
 #pragma unroll
                     for (int k2 = 1; k2 < NM; ++k2) {
@@ -645,7 +764,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 m1 = mf1;
                 l0 = lf0;
                 l1 = lf1;
-                ptx::named_barrier_sync(1, kConsumerThreads);
+                ptx::named_barrier_sync(1, S::kCT);
             }
 
             // Writers: in the shared-merge layout the ms == 0 warp of each
@@ -668,23 +787,50 @@ __global__ void __launch_bounds__(kThreads, 1)
                         // The whole unit ran in this CTA: normalise and write the output.
                         const int r = rb * RPB + lrow0 + 8 * h;
                         const int g = r / p.T, t = r % p.T;
-                        const float inv = l > 0.f ? 1.f / l : 0.f;
+                        const float inv = l > 0.f ? (F8 ? p.vscale[kvh] : 1.f) / l : 0.f;
                         __nv_bfloat16* dst = static_cast<__nv_bfloat16*>(p.out) +
                                              ((static_cast<size_t>(b) * p.Hq + kvh * p.G + g) * p.T + t) * kD;
+                        if constexpr (F8) {
+                            // o[jd][2h] is d = 32*quad + jd, o[jd][2h+1] is d = 32*quad + 16 + jd
 #pragma unroll
-                        for (int nb = 0; nb < 16; ++nb) {
-                            const int col = nb * 8 + 2 * quad;
-                            *reinterpret_cast<uint32_t*>(dst + col) =
-                                ptx::pack_bf16x2(o[nb][2 * h] * inv, o[nb][2 * h + 1] * inv);
+                            for (int half = 0; half < 2; ++half) {
+                                uint32_t w[8];
+#pragma unroll
+                                for (int m = 0; m < 8; ++m)
+                                    w[m] = ptx::pack_bf16x2(o[2 * m][2 * h + half] * inv, o[2 * m + 1][2 * h + half] * inv);
+                                uint4* d4 = reinterpret_cast<uint4*>(dst + 32 * quad + 16 * half);
+                                d4[0] = make_uint4(w[0], w[1], w[2], w[3]);
+                                d4[1] = make_uint4(w[4], w[5], w[6], w[7]);
+                            }
+                        } else {
+#pragma unroll
+                            for (int nb = 0; nb < 16; ++nb) {
+                                const int col = nb * 8 + 2 * quad;
+                                *reinterpret_cast<uint32_t*>(dst + col) =
+                                    ptx::pack_bf16x2(o[nb][2 * h] * inv, o[nb][2 * h + 1] * inv);
+                            }
                         }
                     } else {
                         // Part of a unit seen by several writers: leave (m, l, O)
                         // for the combine kernel.
                         float* part = p.partials + (static_cast<size_t>(slot) * p.part_rows + lrow0 + 8 * h) * kPartStride;
+                        if constexpr (F8) {
+                            // natural column order, V scale applied (the merge is linear in O)
+                            const float vs = p.vscale[kvh];
 #pragma unroll
-                        for (int nb = 0; nb < 16; ++nb) {
-                            const int col = nb * 8 + 2 * quad;
-                            *reinterpret_cast<float2*>(part + col) = make_float2(o[nb][2 * h], o[nb][2 * h + 1]);
+                            for (int half = 0; half < 2; ++half) {
+                                float4* d4 = reinterpret_cast<float4*>(part + 32 * quad + 16 * half);
+#pragma unroll
+                                for (int m = 0; m < 4; ++m)
+                                    d4[m] = make_float4(o[4 * m][2 * h + half] * vs, o[4 * m + 1][2 * h + half] * vs,
+                                                        o[4 * m + 2][2 * h + half] * vs, o[4 * m + 3][2 * h + half] * vs);
+                            }
+                        } else {
+#pragma unroll
+                            for (int nb = 0; nb < 16; ++nb) {
+                                const int col = nb * 8 + 2 * quad;
+                                *reinterpret_cast<float2*>(part + col) = make_float2(o[nb][2 * h], o[nb][2 * h + 1]);
+                            }
                         }
                         if (quad == 0) {
                             part[kD] = h ? m1 : m0;
@@ -911,19 +1057,19 @@ cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t s
     return cudaLaunchKernelEx(&cfg, kernel, std::forward<Args>(args)...);
 }
 
-template <int MT, bool DP, bool TREE>
+template <int MT, bool DP, bool TREE, bool F8>
 cudaError_t launch_mt(const DecodeParams& p, const CUtensorMap& tmK, const CUtensorMap& tmV, int grid,
                       cudaStream_t stream) {
     static bool attr_set = false;
     if (!attr_set) {
-        cudaError_t e = cudaFuncSetAttribute(decode_splitkv_bf16_kernel<MT, DP, TREE>,
+        cudaError_t e = cudaFuncSetAttribute(decode_splitkv_bf16_kernel<MT, DP, TREE, F8>,
                                              cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                             static_cast<int>(Shape<MT>::kSmem));
+                                             static_cast<int>(Shape<MT, F8>::kSmem));
         if (e != cudaSuccess) return e;
         attr_set = true;
     }
-    cudaError_t e = launch_pdl(decode_splitkv_bf16_kernel<MT, DP, TREE>, dim3(grid), dim3(kThreads),
-                               Shape<MT>::kSmem, stream, p, tmK, tmV);
+    cudaError_t e = launch_pdl(decode_splitkv_bf16_kernel<MT, DP, TREE, F8>, dim3(grid), dim3(Shape<MT, F8>::kThreads),
+                               Shape<MT, F8>::kSmem, stream, p, tmK, tmV);
     if (e != cudaSuccess) return e;
     return cudaGetLastError();
 }
@@ -943,31 +1089,46 @@ __global__ void wait_selftest_kernel(int* err, unsigned long long limit_ns) {
 
 }  // namespace
 
-DecodeLaunch decode_launch_shape(int mt) {
+DecodeLaunch decode_launch_shape(int mt, bool fp8) {
+    if (fp8) {
+        switch (mt) {
+            case 1: return DecodeLaunch{1, Shape<1, true>::kThreads, Shape<1, true>::kSmem, Shape<1, true>::kWays};
+            case 2: return DecodeLaunch{2, Shape<2, true>::kThreads, Shape<2, true>::kSmem, Shape<2, true>::kWays};
+            default: return DecodeLaunch{4, Shape<4, true>::kThreads, Shape<4, true>::kSmem, Shape<4, true>::kWays};
+        }
+    }
     switch (mt) {
-        case 1: return DecodeLaunch{1, kThreads, Shape<1>::kSmem, Shape<1>::kWays};
-        case 2: return DecodeLaunch{2, kThreads, Shape<2>::kSmem, Shape<2>::kWays};
-        default: return DecodeLaunch{4, kThreads, Shape<4>::kSmem, Shape<4>::kWays};
+        case 1: return DecodeLaunch{1, Shape<1, false>::kThreads, Shape<1, false>::kSmem, Shape<1, false>::kWays};
+        case 2: return DecodeLaunch{2, Shape<2, false>::kThreads, Shape<2, false>::kSmem, Shape<2, false>::kWays};
+        default: return DecodeLaunch{4, Shape<4, false>::kThreads, Shape<4, false>::kSmem, Shape<4, false>::kWays};
     }
 }
 
-cudaError_t launch_decode_bf16(const DecodeParams& p, const CUtensorMap& tmK, const CUtensorMap& tmV, int mt,
-                               int grid, cudaStream_t stream) {
-    if (p.dplan) return (mt == 1 && !p.anc) ? launch_mt<1, true, false>(p, tmK, tmV, grid, stream) : cudaErrorInvalidValue;
+template <bool F8>
+cudaError_t launch_decode_t(const DecodeParams& p, const CUtensorMap& tmK, const CUtensorMap& tmV, int mt, int grid,
+                            cudaStream_t stream) {
+    if (p.dplan)
+        return (mt == 1 && !p.anc) ? launch_mt<1, true, false, F8>(p, tmK, tmV, grid, stream) : cudaErrorInvalidValue;
     if (p.anc) {
         switch (mt) {
-            case 1: return launch_mt<1, false, true>(p, tmK, tmV, grid, stream);
-            case 2: return launch_mt<2, false, true>(p, tmK, tmV, grid, stream);
-            case 4: return launch_mt<4, false, true>(p, tmK, tmV, grid, stream);
+            case 1: return launch_mt<1, false, true, F8>(p, tmK, tmV, grid, stream);
+            case 2: return launch_mt<2, false, true, F8>(p, tmK, tmV, grid, stream);
+            case 4: return launch_mt<4, false, true, F8>(p, tmK, tmV, grid, stream);
             default: return cudaErrorInvalidValue;
         }
     }
     switch (mt) {
-        case 1: return launch_mt<1, false, false>(p, tmK, tmV, grid, stream);
-        case 2: return launch_mt<2, false, false>(p, tmK, tmV, grid, stream);
-        case 4: return launch_mt<4, false, false>(p, tmK, tmV, grid, stream);
+        case 1: return launch_mt<1, false, false, F8>(p, tmK, tmV, grid, stream);
+        case 2: return launch_mt<2, false, false, F8>(p, tmK, tmV, grid, stream);
+        case 4: return launch_mt<4, false, false, F8>(p, tmK, tmV, grid, stream);
         default: return cudaErrorInvalidValue;
     }
+}
+
+cudaError_t launch_decode_bf16(const DecodeParams& p, const CUtensorMap& tmK, const CUtensorMap& tmV, int mt,
+                               int grid, bool fp8, cudaStream_t stream) {
+    return fp8 ? launch_decode_t<true>(p, tmK, tmV, mt, grid, stream)
+               : launch_decode_t<false>(p, tmK, tmV, mt, grid, stream);
 }
 
 cudaError_t launch_combine_bf16(const CombineParams& p, cudaStream_t stream) {

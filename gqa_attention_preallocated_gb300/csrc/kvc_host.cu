@@ -12,6 +12,8 @@
 // forward pass stopped part-way, truncate, reset).
 
 #include <math.h>
+
+#include <cmath>
 #include <stdarg.h>
 #include <stdio.h>
 #include <string.h>
@@ -29,7 +31,9 @@ using namespace kvc;
 struct kvc_cache {
     int layers = 0, B = 0, Hkv = 0, max_len = 0, d = 0;
     kvc_dtype dtype = KVC_F32;
-    int esize = 4;
+    int esize = 4;  // bytes a stored value
+    // FP8 E4M3 caches: K and V scale of every (layer, KV head), [layers * Hkv]
+    std::vector<float> kscale, vscale;
     std::vector<void*> k, v;
     std::vector<int64_t> lens;  // [layers * B]
     // device state, set up on first launch
@@ -114,16 +118,17 @@ kvc_status ensure_device(kvc_cache* c) {
     return ok();
 }
 
-// 2-D bf16 view [rows, 128] with boxes of box_rows rows x 64 columns (128
-// bytes) and the 128-byte swizzle.
-kvc_status encode_rows_map(CUtensorMap* m, const void* base, cuuint64_t rows, cuuint32_t box_rows) {
+// 2-D view [rows, 128 values] with boxes of box_rows rows x 128 bytes (64
+// bf16 columns, or all 128 one-byte E4M3 columns) and the 128-byte swizzle.
+kvc_status encode_rows_map(CUtensorMap* m, const void* base, cuuint64_t rows, cuuint32_t box_rows, bool fp8 = false) {
     EncodeTiledFn fn = encode_fn();
     if (!fn) return fail(KVC_ERR_CUDA, "cuTensorMapEncodeTiled unavailable");
     cuuint64_t dims[2] = {static_cast<cuuint64_t>(kHeadDimBf16), rows};
-    cuuint64_t strides[1] = {static_cast<cuuint64_t>(kHeadDimBf16) * 2};
-    cuuint32_t box[2] = {64, box_rows};
+    cuuint64_t strides[1] = {static_cast<cuuint64_t>(kHeadDimBf16) * (fp8 ? 1 : 2)};
+    cuuint32_t box[2] = {fp8 ? 128u : 64u, box_rows};
     cuuint32_t estr[2] = {1, 1};
-    CUresult r = fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box, estr,
+    CUresult r = fn(m, fp8 ? CU_TENSOR_MAP_DATA_TYPE_UINT8 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base),
+                    dims, strides, box, estr,
                     CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                     CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     if (r != CUDA_SUCCESS) return fail(KVC_ERR_CUDA, "cuTensorMapEncodeTiled failed (%d)", static_cast<int>(r));
@@ -136,10 +141,13 @@ kvc_status encode_layer_maps(kvc_cache* c, int layer) {
     const cuuint64_t rows = c->pg.table ? static_cast<cuuint64_t>(c->pg.num_pages) * c->Hkv * c->pg.page
                                         : static_cast<cuuint64_t>(c->B) * c->Hkv * c->max_len;
     kvc_status s;
-    if ((s = encode_rows_map(&c->tmK[layer], c->k[layer], rows, kKeyTile))) return s;
-    if ((s = encode_rows_map(&c->tmV[layer], c->v[layer], rows, kKeyTile))) return s;
-    if ((s = encode_rows_map(&c->tmK128[layer], c->k[layer], rows, 128))) return s;
-    if ((s = encode_rows_map(&c->tmV128[layer], c->v[layer], rows, 128))) return s;
+    const bool fp8 = c->dtype == KVC_FP8_E4M3;
+    if ((s = encode_rows_map(&c->tmK[layer], c->k[layer], rows, kKeyTile, fp8))) return s;
+    if ((s = encode_rows_map(&c->tmV[layer], c->v[layer], rows, kKeyTile, fp8))) return s;
+    if (!fp8) {  // the tensor-core kernel (128-row boxes) serves bf16 caches only
+        if ((s = encode_rows_map(&c->tmK128[layer], c->k[layer], rows, 128))) return s;
+        if ((s = encode_rows_map(&c->tmV128[layer], c->v[layer], rows, 128))) return s;
+    }
     c->tm_ready[layer] = 1;
     return ok();
 }
@@ -210,7 +218,7 @@ kvc_status plan_shape(const kvc_cache* c, int Hq, int T, int num_ctas, AttnPlan*
     const long long R = static_cast<long long>(pl->G) * T;
     if (R > (1ll << 30)) return fail(KVC_ERR_ARG, "G * T too large");
     pl->R = static_cast<int>(R);
-    if (c->dtype == KVC_BF16) {
+    if (c->dtype != KVC_F32) {
         pl->mt = pl->R <= 16 ? 1 : (pl->R <= 32 ? 2 : 4);
         pl->RPB = 16 * pl->mt;
         pl->RB = std::max(1, (pl->R + pl->RPB - 1) / pl->RPB);
@@ -226,12 +234,12 @@ kvc_status plan_shape(const kvc_cache* c, int Hq, int T, int num_ctas, AttnPlan*
         // device-computed plans of resident-length steps, then the ancestor
         // masks of a tree-verify call
         pl->ws_plan = round_up(sizeof(DevicePlan), 256) + round_up(kMaxTreeQueries * sizeof(uint64_t), 256);
-        pl->ways = decode_launch_shape(pl->mt).ways;
+        pl->ways = decode_launch_shape(pl->mt, c->dtype == KVC_FP8_E4M3).ways;
         pl->part_rows = std::min(pl->R, pl->RPB);
         pl->ws_partials = static_cast<size_t>(pl->units + num_ctas) * pl->ways * pl->part_rows *
                           (kHeadDimBf16 + 4) * sizeof(float);
         pl->ws_min = pl->ws_err + pl->ws_plan + pl->ws_partials;
-        if (pl->R > kTcMinRows) {
+        if (pl->R > kTcMinRows && c->dtype == KVC_BF16) {
             // The tensor-core kernel: up to two partial slots (2 row tiles x
             // 128 rows x (d + 4) floats) per SM share boundary.
             const size_t prefill = static_cast<size_t>(2) * std::min(num_ctas, kMaxCtas) * 2 * 128 *
@@ -269,6 +277,15 @@ kvc_status validate_attention(const kvc_cache* c, int layer, const void* q, int 
 // Launches (arguments already validated)
 // ---------------------------------------------------------------------------
 
+// The layer's FP8 scales into a split-KV parameter block (no-op for bf16).
+void set_decode_scales(const kvc_cache* c, int layer, DecodeParams* p) {
+    if (c->dtype != KVC_FP8_E4M3) return;
+    for (int h = 0; h < c->Hkv; ++h) {
+        p->kscale[h] = c->kscale[static_cast<size_t>(layer) * c->Hkv + h];
+        p->vscale[h] = c->vscale[static_cast<size_t>(layer) * c->Hkv + h];
+    }
+}
+
 kvc_status do_append(kvc_cache* c, int layer, const void* k_new, const void* v_new, int T, const int32_t* n_new,
                      int max_n, cudaStream_t stream) {
     if (max_n == 0) return ok();
@@ -282,9 +299,15 @@ kvc_status do_append(kvc_cache* c, int layer, const void* k_new, const void* v_n
     p.Hkv = c->Hkv;
     p.T = T;
     p.max_len = c->max_len;
-    p.row_bytes = c->d * c->esize;
+    p.fp8 = c->dtype == KVC_FP8_E4M3 ? 1 : 0;
+    p.row_bytes = c->d * (p.fp8 ? 2 : c->esize);  // source rows (bf16 for an FP8 cache)
     p.ring = c->ring ? 1 : 0;
     p.pg = c->pg;
+    if (p.fp8)
+        for (int h = 0; h < c->Hkv; ++h) {
+            p.kscale[h] = c->kscale[static_cast<size_t>(layer) * c->Hkv + h];
+            p.vscale[h] = c->vscale[static_cast<size_t>(layer) * c->Hkv + h];
+        }
     const int64_t* lens = c->lens.data() + static_cast<size_t>(layer) * c->B;
     for (int b = 0; b < c->B; ++b) {
         p.lens[b] = static_cast<int>(lens[b]);
@@ -338,7 +361,7 @@ kvc_status do_attention(kvc_cache* c, int layer, const void* q, const AttnPlan& 
 
     kvc_status s = encode_layer_maps(c, layer);
     if (s) return s;
-    if (pl.R > kTcMinRows && k_new == nullptr && anc == nullptr && c->max_len <= kTcMaxLen) {
+    if (c->dtype == KVC_BF16 && pl.R > kTcMinRows && k_new == nullptr && anc == nullptr && c->max_len <= kTcMaxLen) {
         // Many query rows per KV head: tensor-core kernel, one CTA per piece.
         // Work items are (b, kvh, row block, pair of 128-row tiles): with
         // T >= 128, 128 positions of two query heads (mode 0); with T < 128 the
@@ -540,6 +563,7 @@ kvc_status do_attention(kvc_cache* c, int layer, const void* q, const AttnPlan& 
     p.window = c->window;
     p.ring = c->ring ? 1 : 0;
     p.pg = c->pg;
+    set_decode_scales(c, layer, &p);
     p.anc = nullptr;
     if (anc) {
         // The masks go to the workspace (the parameter block stays small).
@@ -623,7 +647,8 @@ kvc_status do_attention(kvc_cache* c, int layer, const void* q, const AttnPlan& 
         if (e != cudaSuccess) return cuda_fail(e, "cudaMemsetAsync(workspace)");
         c->last_ws = ws;
     }
-    cudaError_t e = launch_decode_bf16(p, c->tmK[layer], c->tmV[layer], pl.mt, grid, stream);
+    cudaError_t e =
+        launch_decode_bf16(p, c->tmK[layer], c->tmV[layer], pl.mt, grid, c->dtype == KVC_FP8_E4M3, stream);
     if (e != cudaSuccess) return cuda_fail(e, "split-KV attention launch");
     ++c->launches;
     if (main_enqueued) *main_enqueued = true;
@@ -657,7 +682,7 @@ kvc_status do_attention(kvc_cache* c, int layer, const void* q, const AttnPlan& 
 }
 
 kvc_status check_workspace(const kvc_cache* c, const AttnPlan& pl, const void* ws, size_t ws_bytes) {
-    if (c->dtype != KVC_BF16 || c->B == 0 || pl.T == 0) return ok();
+    if (c->dtype == KVC_F32 || c->B == 0 || pl.T == 0) return ok();
     if (!ws) return fail(KVC_ERR_WORKSPACE, "workspace is null (need %zu bytes)", pl.ws_total);
     if ((reinterpret_cast<uintptr_t>(ws) & 255u) != 0) return fail(KVC_ERR_WORKSPACE, "workspace not 256-byte aligned");
     if (ws_bytes < pl.ws_total)
@@ -684,8 +709,8 @@ kvc_status tree_masks(const kvc_cache* c, const AttnPlan& pl, const int32_t* n_n
         return fail(KVC_ERR_SHAPE, "B * T = %lld draft tokens exceed %d", static_cast<long long>(c->B) * pl.T,
                     kMaxTreeQueries);
     if (c->window > 0 || c->ring) return fail(KVC_ERR_ARG, "a draft tree does not combine with a window");
-    if (c->dtype == KVC_BF16 && pl.R > 64)
-        return fail(KVC_ERR_SHAPE, "a bf16 draft tree takes G * T <= 64 query rows per KV head (G * T = %d)", pl.R);
+    if (c->dtype != KVC_F32 && pl.R > 64)
+        return fail(KVC_ERR_SHAPE, "a bf16 / fp8 draft tree takes G * T <= 64 query rows per KV head (G * T = %d)", pl.R);
     anc->assign(static_cast<size_t>(c->B) * pl.T, 0);
     for (int b = 0; b < c->B; ++b)
         for (int t = 0; t < n_new[b]; ++t) {
@@ -716,12 +741,15 @@ kvc_status kvc_create(kvc_cache** out, int layers, int batch, int kv_heads, int 
         return fail(KVC_ERR_ARG, "bad geometry: layers=%d batch=%d kv_heads=%d max_len=%d head_dim=%d", layers, batch,
                     kv_heads, max_len, head_dim);
     if (batch > KVC_MAX_BATCH) return fail(KVC_ERR_ARG, "batch %d > %d", batch, KVC_MAX_BATCH);
-    if (dtype != KVC_F32 && dtype != KVC_BF16) return fail(KVC_ERR_ARG, "unknown dtype %d", static_cast<int>(dtype));
-    const int esize = dtype == KVC_F32 ? 4 : 2;
+    if (dtype != KVC_F32 && dtype != KVC_BF16 && dtype != KVC_FP8_E4M3)
+        return fail(KVC_ERR_ARG, "unknown dtype %d", static_cast<int>(dtype));
+    const int esize = dtype == KVC_F32 ? 4 : (dtype == KVC_BF16 ? 2 : 1);
     if ((head_dim * esize) % 16 != 0) return fail(KVC_ERR_ARG, "head_dim * element size must be a multiple of 16");
     if (dtype == KVC_F32 && head_dim > 256) return fail(KVC_ERR_ARG, "f32 path takes head_dim <= 256");
-    if (dtype == KVC_BF16 && head_dim != kHeadDimBf16)
-        return fail(KVC_ERR_ARG, "bf16 path takes head_dim = %d", kHeadDimBf16);
+    if (dtype != KVC_F32 && head_dim != kHeadDimBf16)
+        return fail(KVC_ERR_ARG, "bf16 and fp8 caches take head_dim = %d", kHeadDimBf16);
+    if (dtype == KVC_FP8_E4M3 && kv_heads > kMaxScaleHeads)
+        return fail(KVC_ERR_ARG, "fp8 caches take at most %d KV heads", kMaxScaleHeads);
     const long long rows = static_cast<long long>(batch) * kv_heads * max_len;
     if (rows + kKeyTile >= (1ll << 31)) return fail(KVC_ERR_ARG, "batch * kv_heads * max_len too large");
     if (!k_bufs || !v_bufs) return fail(KVC_ERR_ARG, "k_bufs / v_bufs is null");
@@ -746,7 +774,26 @@ kvc_status kvc_create(kvc_cache** out, int layers, int batch, int kv_heads, int 
     c->tmK128.resize(layers);
     c->tmV128.resize(layers);
     c->tm_ready.assign(layers, 0);
+    c->kscale.assign(static_cast<size_t>(layers) * kv_heads, 1.0f);
+    c->vscale.assign(static_cast<size_t>(layers) * kv_heads, 1.0f);
     *out = c;
+    return ok();
+}
+
+kvc_status kvc_set_kv_scales(kvc_cache* c, int layer, const float* k_scale, const float* v_scale) {
+    if (!c) return fail(KVC_ERR_ARG, "null handle");
+    if (c->dtype != KVC_FP8_E4M3) return fail(KVC_ERR_ARG, "scales apply to fp8 caches only");
+    if (layer < 0 || layer >= c->layers) return fail(KVC_ERR_ARG, "layer %d out of range", layer);
+    if (!k_scale || !v_scale) return fail(KVC_ERR_ARG, "k_scale / v_scale is null");
+    for (int h = 0; h < c->Hkv; ++h)
+        if (!(std::isfinite(k_scale[h]) && std::isfinite(v_scale[h]) && k_scale[h] > 0.f && v_scale[h] > 0.f))
+            return fail(KVC_ERR_ARG, "head %d: scales must be positive and finite", h);
+    if (c->lens_on_device) return fail(KVC_ERR_ARG, "lengths are on the device; call kvc_lens_from_device first");
+    for (int b = 0; b < c->B; ++b)
+        if (c->lens[static_cast<size_t>(layer) * c->B + b] != 0)
+            return fail(KVC_ERR_ARG, "layer %d holds data: scales change only while it is empty", layer);
+    std::copy(k_scale, k_scale + c->Hkv, c->kscale.begin() + static_cast<size_t>(layer) * c->Hkv);
+    std::copy(v_scale, v_scale + c->Hkv, c->vscale.begin() + static_cast<size_t>(layer) * c->Hkv);
     return ok();
 }
 
@@ -758,8 +805,8 @@ kvc_status kvc_create_paged(kvc_cache** out, int layers, int batch, int kv_heads
     if (page_size < 1 || num_pages < 1 || max_pages_per_row < 1)
         return fail(KVC_ERR_ARG, "bad paging: page_size=%d num_pages=%d max_pages_per_row=%d", page_size, num_pages,
                     max_pages_per_row);
-    if (dtype == KVC_BF16 && page_size % 128 != 0)
-        return fail(KVC_ERR_ARG, "bf16 pages hold a multiple of 128 tokens (key tiles never cross a page)");
+    if (dtype != KVC_F32 && page_size % 128 != 0)
+        return fail(KVC_ERR_ARG, "bf16 and fp8 pages hold a multiple of 128 tokens (key tiles never cross a page)");
     if (batch > 0 && !block_table) return fail(KVC_ERR_ARG, "block_table is null");
     if ((reinterpret_cast<uintptr_t>(block_table) & 3u) != 0) return fail(KVC_ERR_ARG, "block_table not 4-byte aligned");
     const long long cap = static_cast<long long>(max_pages_per_row) * page_size;
@@ -797,7 +844,7 @@ kvc_status kvc_append(kvc_cache* c, int layer, const void* k_new, const void* v_
 
 size_t kvc_workspace_bytes(const kvc_cache* c, int q_heads, int T) {
     if (!c) return 0;
-    if (c->dtype != KVC_BF16) return 0;
+    if (c->dtype == KVC_F32) return 0;
     kvc_cache* mc = const_cast<kvc_cache*>(c);
     if (ensure_device(mc) != KVC_OK) return 0;
     AttnPlan pl;
@@ -816,7 +863,7 @@ static kvc_status gqa_attention_impl(kvc_cache* c, int layer, const void* q, int
     const int64_t* lens = c->lens.data() + static_cast<size_t>(layer) * c->B;
     s = validate_attention(c, layer, q, q_heads, T, n_new, out, lens, &pl, 0);
     if (s) return s;
-    if (c->dtype == KVC_BF16 && c->B > 0 && T > 0) {
+    if (c->dtype != KVC_F32 && c->B > 0 && T > 0) {
         s = ensure_device(c);
         if (s) return s;
         s = plan_shape(c, q_heads, T, c->num_sms, &pl);
@@ -851,7 +898,7 @@ static kvc_status append_attention_impl(kvc_cache* c, int layer, const void* q, 
     AttnPlan pl;
     s = validate_attention(c, layer, q, q_heads, T, n_new, out, after.data(), &pl, 0);
     if (s) return s;
-    if (c->dtype == KVC_BF16 && c->B > 0 && T > 0) {
+    if (c->dtype != KVC_F32 && c->B > 0 && T > 0) {
         s = ensure_device(c);
         if (s) return s;
         s = plan_shape(c, q_heads, T, c->num_sms, &pl);
@@ -872,7 +919,8 @@ static kvc_status append_attention_impl(kvc_cache* c, int layer, const void* q, 
     if (s) return s;
     cudaStream_t st = static_cast<cudaStream_t>(stream);
     int64_t* lw = c->lens.data() + static_cast<size_t>(layer) * c->B;
-    if (c->dtype == KVC_BF16 && pl.mt == 1 && max_n > 0 && pl.R <= kTcMinRows) {
+    // (an FP8 cache has no tensor-core path: its split-KV kernel fuses the append up to 16 rows)
+    if (c->dtype != KVC_F32 && pl.mt == 1 && max_n > 0 && (pl.R <= kTcMinRows || c->dtype == KVC_FP8_E4M3)) {
         // Warps own whole tiles: the attention kernel writes the new rows into
         // the cache itself (one launch instead of two).
         for (int b = 0; b < c->B; ++b) lw[b] += n_new[b];
@@ -1034,7 +1082,7 @@ kvc_status kvc_set_window(kvc_cache* c, int window, int ring) {
     if (ring) {
         if (c->pg.table) return fail(KVC_ERR_ARG, "a paged cache cannot also be a ring");
         if (window < 1 || window > c->max_len) return fail(KVC_ERR_ARG, "a ring cache needs a window of 1..max_len");
-        if (c->dtype == KVC_BF16 && c->max_len % 128 != 0)
+        if (c->dtype != KVC_F32 && c->max_len % 128 != 0)
             return fail(KVC_ERR_ARG, "a bf16 ring cache needs max_len %% 128 == 0 (key tiles never wrap)");
     }
     if ((ring != 0) != c->ring)
@@ -1096,7 +1144,7 @@ kvc_status kvc_decode_step(kvc_cache* c, int layer, const void* q, const void* k
     kvc_status s = check_layer(c, layer);
     if (s) return s;
     if (!c->lens_on_device) return fail(KVC_ERR_ARG, "the lengths are on the host: call kvc_lens_to_device first");
-    if (c->dtype != KVC_BF16) return fail(KVC_ERR_ARG, "device-resident steps serve bf16 caches only");
+    if (c->dtype == KVC_F32) return fail(KVC_ERR_ARG, "device-resident steps serve bf16 and fp8 caches only");
     if (c->B == 0 || T == 0) return ok();
     if (T < 0) return fail(KVC_ERR_ARG, "T = %d < 0", T);
     if (!q || !k_new || !v_new || !out || !n_new_dev) return fail(KVC_ERR_ARG, "null pointer argument");
@@ -1176,7 +1224,8 @@ kvc_status kvc_decode_step(kvc_cache* c, int layer, const void* q, const void* k
     p.window = c->window;
     p.ring = c->ring ? 1 : 0;
     p.pg = c->pg;
-    e = launch_decode_bf16(p, c->tmK[layer], c->tmV[layer], 1, grid, st);
+    set_decode_scales(c, layer, &p);
+    e = launch_decode_bf16(p, c->tmK[layer], c->tmV[layer], 1, grid, c->dtype == KVC_FP8_E4M3, st);
     if (e != cudaSuccess) return cuda_fail(e, "split-KV attention launch");
     ++c->launches;
 
@@ -1253,7 +1302,7 @@ extern "C" kvc_status kvc_gqa_attention_noalloc(kvc_cache* c, int layer, const v
     if (s0) return s0;
     kvc_status s = check_layer(c, layer);
     if (s) return s;
-    if (c->dtype != KVC_BF16) return fail(KVC_ERR_ARG, "the allocation-free variant serves bf16 caches only");
+    if (c->dtype == KVC_F32) return fail(KVC_ERR_ARG, "the allocation-free variant serves bf16 and fp8 caches only");
     AttnPlan pl;
     const int64_t* lens = c->lens.data() + static_cast<size_t>(layer) * c->B;
     s = validate_attention(c, layer, q, q_heads, T, n_new, out, lens, &pl, 0);

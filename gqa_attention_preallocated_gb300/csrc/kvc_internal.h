@@ -37,6 +37,8 @@ __host__ __device__ __forceinline__ int phys_row(const Paging& pg, int ring, int
 // Keys per K/V tile of the split-KV kernel, and the head width it is built for.
 constexpr int kKeyTile = 64;
 constexpr int kHeadDimBf16 = 128;
+// FP8 E4M3 caches: one K and one V scale per KV head (at most this many heads).
+constexpr int kMaxScaleHeads = 64;
 
 // ---------------------------------------------------------------------------
 // In-place append: k_new/v_new [B, Hkv, T, d] -> cache rows lens[b] .. lens[b]+n_new[b]-1.
@@ -50,6 +52,11 @@ struct AppendParams {
     int row_bytes;  // d * element size, a multiple of 16
     int ring;       // slots are positions mod max_len
     Paging pg;
+    // FP8 E4M3 cache: k_new / v_new rows are bf16 (row_bytes = 2 * d) and are
+    // stored as E4M3 codes of x * (1/scale) (d bytes a row).
+    int fp8;
+    float kscale[kMaxScaleHeads];
+    float vscale[kMaxScaleHeads];
     int lens[kMaxBatch];
     int n_new[kMaxBatch];
 };
@@ -128,6 +135,10 @@ struct DecodeParams {
     // chunk.  anc is device memory (the workspace); null without a tree.
     const uint64_t* anc;
     Paging pg;
+    // FP8 E4M3 cache (kernel variant F8): K of head h reads code * kscale[h],
+    // V reads code * vscale[h]; appended rows are quantized with 1/scale.
+    float kscale[kMaxScaleHeads];
+    float vscale[kMaxScaleHeads];
     int prior[kMaxBatch];    // lens[b] - n_new[b]
     int n_new[kMaxBatch];
     int gstart[kMaxGroups + 1];
@@ -159,10 +170,10 @@ struct DecodeLaunch {
     size_t smem_bytes;
     int ways;  // partial sub-slots per (unit, CTA): 4 when warps own whole tiles
 };
-DecodeLaunch decode_launch_shape(int mt);
+DecodeLaunch decode_launch_shape(int mt, bool fp8);
 
 cudaError_t launch_decode_bf16(const DecodeParams& p, const CUtensorMap& tmK, const CUtensorMap& tmV, int mt,
-                               int grid, cudaStream_t stream);
+                               int grid, bool fp8, cudaStream_t stream);
 
 // ---------------------------------------------------------------------------
 // f32 attention (any d <= 256, d % 4 == 0): one CTA per (16-row block, kvh, b),

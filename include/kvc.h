@@ -56,7 +56,14 @@
 extern "C" {
 #endif
 
-typedef enum { KVC_F32 = 0, KVC_BF16 = 1 } kvc_dtype;
+/* Storage type of the cache.  q, out, k_new and v_new have the same type,
+ * except for KVC_FP8_E4M3 caches: those store one byte per value (E4M3:
+ * 1 sign, 4 exponent bits with bias 7, 3 mantissa bits; largest finite 448,
+ * no infinity) with one scale per (layer, KV head) for K and for V
+ * (kvc_set_kv_scales), and take bf16 q / k_new / v_new / out ("16. Prefill,
+ * decode and the KV cache", exercise 4: store the cache in FP8 E4M3 with one
+ * scale per head and dequantize on read). */
+typedef enum { KVC_F32 = 0, KVC_BF16 = 1, KVC_FP8_E4M3 = 2 } kvc_dtype;
 
 typedef enum {
     KVC_OK = 0,
@@ -81,12 +88,23 @@ typedef struct kvc_cache kvc_cache;
  * No CUDA call is made here; device state (tensor-map descriptors, SM
  * count) is set up on the first launch.
  * Errors: KVC_ERR_ARG for non-positive sizes, B > KVC_MAX_BATCH, null or
- * misaligned buffers, or d * element size not a multiple of 16. */
+ * misaligned buffers, or d * element size not a multiple of 16; bf16 and
+ * FP8 caches take d = 128, FP8 caches at most 64 KV heads. */
 kvc_status kvc_create(kvc_cache** out, int layers, int batch, int kv_heads, int max_len, int head_dim,
                       kvc_dtype dtype, void* const* k_bufs, void* const* v_bufs);
 
 /* Free the handle (not the buffers).  NULL is accepted. */
 void kvc_destroy(kvc_cache* c);
+
+/* Scales of an FP8 E4M3 cache's layer: k_scale[h], v_scale[h] (host arrays of
+ * kv_heads floats, copied) for KV head h.  Appends store a value x of head h
+ * as the E4M3 code nearest to x * (1/s) (the reciprocal and the product each
+ * rounded to float32; ties to even; beyond +-448 saturating to +-448), and
+ * attention reads code * s.  Every scale starts at 1.  Only while every row
+ * of the layer has length 0 (the stored codes depend on the scale).
+ * Errors: KVC_ERR_ARG (not an FP8 cache, bad layer, null arrays, a scale not
+ * positive and finite, or the layer holds data); nothing changes on error. */
+kvc_status kvc_set_kv_scales(kvc_cache* c, int layer, const float* k_scale, const float* v_scale);
 
 /* A cache whose K/V live in pages ("Implement grouped-query attention over a
  * preallocated KV cache...", "A strong answer", the reversal condition: rows of

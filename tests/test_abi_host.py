@@ -258,3 +258,34 @@ def test_paged_host_rules(L):
     assert L.kvc_reset(h) == 0
     assert L.kvc_set_window(h, 6, 0) == 0   # a window over pages is fine
     L.kvc_destroy(h)
+
+
+def test_fp8_host_rules(L):
+    FP = ctypes.POINTER(ctypes.c_float)
+
+    def scales(*xs):
+        a = np.array(xs, dtype=np.float32)
+        return a, a.ctypes.data_as(FP)
+
+    assert _create(L, d=64, dtype=_lib.KVC_FP8_E4M3)[0] == 1      # fp8 takes d = 128
+    assert _create(L, Hkv=65, d=128, dtype=_lib.KVC_FP8_E4M3)[0] == 1
+    st, h = _create(L, layers=2, B=2, Hkv=2, max_len=256, d=128, dtype=_lib.KVC_FP8_E4M3)
+    assert st == 0
+    _, ok = scales(0.5, 2.0)
+    assert L.kvc_set_kv_scales(h, 0, ok, ok) == 0
+    assert L.kvc_set_kv_scales(h, 2, ok, ok) == 1                 # layer out of range
+    for bad in [(0.0, 1.0), (-1.0, 1.0), (float("inf"), 1.0), (float("nan"), 1.0)]:
+        _, b = scales(*bad)
+        assert L.kvc_set_kv_scales(h, 0, b, ok) == 1
+        assert L.kvc_set_kv_scales(h, 0, ok, b) == 1
+    _, lens = _i64(3, 0)
+    assert L.kvc_set_lens(h, 1, lens) == 0
+    assert L.kvc_set_kv_scales(h, 1, ok, ok) == 1                 # layer 1 holds data
+    assert L.kvc_set_kv_scales(h, 0, ok, ok) == 0                 # layer 0 is still empty
+    assert L.kvc_reset(h) == 0
+    assert L.kvc_set_kv_scales(h, 1, ok, ok) == 0
+    L.kvc_destroy(h)
+    st, h = _create(L, d=16)
+    _, ok = scales(1.0, 1.0)
+    assert L.kvc_set_kv_scales(h, 0, ok, ok) == 1                 # not an fp8 cache
+    L.kvc_destroy(h)

@@ -1,0 +1,217 @@
+"""FP8 E4M3 cache on the GPU against the oracle.
+
+"16. Prefill, decode and the KV cache", exercise 4: the cache is stored in
+FP8 E4M3 with one scale per KV head and dequantized on read.  Appends
+quantize bf16 rows (code of x * (1/s), float32 reciprocal and product, ties
+to even, saturating at +-448); the stored codes must equal the oracle's bit
+for bit, and every attention output must be within 2e-2 of the float64
+oracle reading the same codes.  Slots never written hold the NaN code 0x7F,
+so a read of them fails.
+"""
+
+import numpy as np
+import pytest
+import torch
+
+import oracle.ref as ref
+from gqa_attention_preallocated_gb300 import KVCache, PagedKVCache
+from gqa_attention_preallocated_gb300 import workloads as wl
+
+pytestmark = pytest.mark.gpu
+
+TOL = 2e-2
+FP8 = torch.float8_e4m3fn
+
+
+def _cuda_or_skip():
+    if not torch.cuda.is_available():
+        pytest.skip("needs a GPU")
+
+
+def _scales(Hkv, seed, lo=2.0 / 448, hi=6.0 / 448):
+    """Per-head scales: N(0,1) data saturates beyond 448 * s (about 2 to 6 sigma)."""
+    rng = np.random.default_rng(seed)
+    return rng.uniform(lo, hi, Hkv).astype(np.float32), rng.uniform(lo, hi, Hkv).astype(np.float32)
+
+
+def _pair(B, Hkv, max_len, seed, window=0, paged=None):
+    if paged is None:
+        cache = KVCache(1, B, Hkv, max_len, 128, dtype=FP8)
+        orc = ref.OracleCache(1, B, Hkv, max_len, 128)
+    else:
+        page, num_pages, mpr, table = paged
+        cache = PagedKVCache(1, B, Hkv, page, num_pages, mpr, 128, dtype=FP8)
+        cache.block_table.copy_(torch.as_tensor(table, dtype=torch.int32).view(B, mpr))
+        orc = ref.OracleCache(1, B, Hkv, mpr * page, 128)
+    cache.k[0].view(torch.uint8).fill_(0x7F)
+    cache.v[0].view(torch.uint8).fill_(0x7F)
+    ks, vs = _scales(Hkv, seed)
+    cache.set_kv_scales(0, ks, vs)
+    orc.set_fp8()
+    orc.set_kv_scales(0, ks.astype(np.float64), vs.astype(np.float64))
+    if window:
+        cache.set_window(window)
+        orc.set_window(window)
+    return cache, orc
+
+
+def _codes_of(cache, orc, paged=None):
+    """Compare every written slot's codes with the oracle's, bit for bit."""
+    kc = cache.k[0].view(torch.uint8).cpu().numpy()
+    vc = cache.v[0].view(torch.uint8).cpu().numpy()
+    for b in range(orc.B):
+        for a in range(int(orc.lens[0, b])):
+            if paged is None:
+                got_k, got_v = kc[b, :, a], vc[b, :, a]
+            else:
+                page, _, mpr, table = paged
+                pg = int(np.asarray(table).reshape(orc.B, mpr)[b, a // page])
+                got_k, got_v = kc[pg, :, a % page], vc[pg, :, a % page]
+            assert np.array_equal(got_k, orc.k_code[0][b, :, a]), (b, a)
+            assert np.array_equal(got_v, orc.v_code[0][b, :, a]), (b, a)
+
+
+def _step(cache, orc, seed, ci, G, n_new, T=None, parents=None):
+    B, Hkv, d = orc.B, orc.Hkv, orc.d
+    n_new = np.asarray(n_new, dtype=np.int64)
+    T = (max(int(n_new.max()), 1) if T is None else T) if parents is None else np.asarray(parents).shape[1]
+    bf = torch.bfloat16
+    k = wl.to_storage(wl.normal(seed, 100 + 3 * ci, (B, Hkv, T, d)), bf)
+    v = wl.to_storage(wl.normal(seed, 101 + 3 * ci, (B, Hkv, T, d)), bf)
+    q = wl.to_storage(wl.normal(seed, 102 + 3 * ci, (B, Hkv * G, T, d)), bf)
+    if parents is None:
+        out = cache.append_attention(0, q.cuda(), k.cuda(), v.cuda(), n_new)
+    else:
+        out = cache.append_attention_tree(0, q.cuda(), k.cuda(), v.cuda(), n_new, parents)
+    want = ref.append_attention(orc, 0, q.double().numpy(), k.double().numpy(), v.double().numpy(), n_new,
+                                parents=parents)
+    got = out.double().cpu().numpy()
+    assert np.array_equal(cache.lens(0), orc.lens[0])
+    assert np.all(np.isfinite(got))
+    for b in range(B):
+        assert np.all(got[b, :, n_new[b]:] == 0.0)
+    err = float(np.max(np.abs(got - want)))
+    assert err <= TOL, (ci, err)
+    return err
+
+
+@pytest.mark.parametrize(
+    "B,Hkv,G,chunks",
+    [
+        (4, 2, 4, [300, 1, 1, 1]),        # prefill, then decode (4 rows: append fused into attention)
+        (3, 2, 4, [200, 4, 4]),           # verify at 16 rows (fused)
+        (2, 2, 8, [150, 4, 8, 1]),        # 32 and 64 rows per KV head (append kernel, split rows)
+        (2, 1, 1, [77, 5, 16, 1]),        # MHA
+        (1, 8, 4, [1, 63, 64, 65, 129]),  # tile boundaries
+    ],
+)
+def test_fp8_chunks_against_oracle(B, Hkv, G, chunks):
+    _cuda_or_skip()
+    rng = np.random.default_rng(B * 100 + Hkv * 10 + G)
+    cache, orc = _pair(B, Hkv, int(sum(chunks)) + 7, B + G)
+    for ci, c in enumerate(chunks):
+        n = rng.integers(max(0, c - 3), c + 1, size=B)
+        n[0] = c
+        _step(cache, orc, 11, ci, G, n)
+    _codes_of(cache, orc)
+    assert cache.device_status() == 0
+
+
+def test_fp8_long_rows_split_over_ctas():
+    """Rows long enough that units straddle CTAs (partials merged by the combine kernel)."""
+    _cuda_or_skip()
+    B, Hkv, G = 2, 2, 4
+    cache, orc = _pair(B, Hkv, 6000, 3)
+    _step(cache, orc, 12, 0, G, [5000, 3300])
+    for ci in range(1, 4):
+        _step(cache, orc, 12, ci, G, [1, 1])
+    _codes_of(cache, orc)
+
+
+def test_fp8_with_window():
+    _cuda_or_skip()
+    cache, orc = _pair(2, 2, 1024, 4, window=300)
+    _step(cache, orc, 13, 0, 4, [700, 500])
+    for ci in range(1, 5):
+        _step(cache, orc, 13, ci, 4, [1, 4], T=4)
+    _codes_of(cache, orc)
+
+
+def test_fp8_over_pages():
+    _cuda_or_skip()
+    B, Hkv, page, mpr = 3, 2, 128, 8
+    table = np.random.default_rng(5).permutation(B * mpr)
+    paged = (page, B * mpr, mpr, table)
+    cache, orc = _pair(B, Hkv, None, 5, paged=paged)
+    _step(cache, orc, 14, 0, 4, [600, 300, 900])
+    for ci in range(1, 4):
+        _step(cache, orc, 14, ci, 4, [1, 1, 1])
+    _codes_of(cache, orc, paged=paged)
+    assert cache.device_status() == 0
+
+
+def test_fp8_tree_verify():
+    _cuda_or_skip()
+    B, Hkv, G, T = 4, 2, 4, 8
+    cache, orc = _pair(B, Hkv, 1200, 6)
+    _step(cache, orc, 15, 0, G, [700, 300, 1000, 128])
+    rng = np.random.default_rng(7)
+    parents = np.stack([np.array([-1] + [int(rng.integers(-1, t)) for t in range(1, T)]) for _ in range(B)])
+    _step(cache, orc, 15, 1, G, np.full(B, T), parents=parents)
+
+
+def test_fp8_decode_step_matches_host_path():
+    _cuda_or_skip()
+    B, Hkv, G, T = 8, 4, 4, 1
+    caches = []
+    for _ in range(2):
+        c, _ = _pair(B, Hkv, 2048, 8)
+        k = wl.to_storage(wl.normal(9, 1, (B, Hkv, 1500, 128)), torch.bfloat16).cuda()
+        v = wl.to_storage(wl.normal(9, 2, (B, Hkv, 1500, 128)), torch.bfloat16).cuda()
+        c.append(0, k, v, wl.decode_lens(9, B, 600, 1500))
+        caches.append(c)
+    host, dev = caches
+    ws = dev.workspace(Hkv * G, T)
+    dev.lens_to_device()
+    out = torch.empty((B, Hkv * G, T, 128), dtype=torch.bfloat16, device="cuda")
+    nn = torch.ones(B, dtype=torch.int32, device="cuda")
+    for step in range(5):
+        q = wl.to_storage(wl.normal(9, 500 + step, (B, Hkv * G, T, 128)), torch.bfloat16).cuda()
+        k = wl.to_storage(wl.normal(9, 600 + step, (B, Hkv, T, 128)), torch.bfloat16).cuda()
+        v = wl.to_storage(wl.normal(9, 700 + step, (B, Hkv, T, 128)), torch.bfloat16).cuda()
+        want = host.append_attention(0, q, k, v, np.ones(B))
+        dev.decode_step(0, q, k, v, nn, out, ws)
+        torch.cuda.synchronize()
+        assert torch.equal(out, want), step
+    assert dev.device_status(ws) == 0
+    dev.lens_from_device()
+    assert np.array_equal(dev.lens(0), host.lens(0))
+    assert torch.equal(dev.k[0].view(torch.uint8), host.k[0].view(torch.uint8))
+
+
+def test_fp8_against_bf16_cache_over_many_decode_steps():
+    """The page's experiment, on attention outputs (no model here): the same
+    1,000 decode steps through an FP8 cache and a bf16 cache.  The difference
+    is the quantization error only; it is reported and must stay small."""
+    _cuda_or_skip()
+    B, Hkv, G, steps, d = 4, 2, 4, 1000, 128
+    f8 = KVCache(1, B, Hkv, 2048, d, dtype=FP8)
+    bf = KVCache(1, B, Hkv, 2048, d, dtype=torch.bfloat16)
+    s = np.full(Hkv, 4.0 / 448, dtype=np.float32)  # N(0,1): 4 sigma maps to 448
+    f8.set_kv_scales(0, s, s)
+    k0 = wl.to_storage(wl.normal(10, 1, (B, Hkv, 512, d)), torch.bfloat16).cuda()
+    v0 = wl.to_storage(wl.normal(10, 2, (B, Hkv, 512, d)), torch.bfloat16).cuda()
+    for c in (f8, bf):
+        c.append(0, k0, v0, np.full(B, 512))
+    worst, total = 0.0, 0.0
+    for step in range(steps):
+        q = wl.to_storage(wl.normal(10, 10000 + step, (B, Hkv * G, 1, d), device="cuda"), torch.bfloat16)
+        k = wl.to_storage(wl.normal(10, 20000 + step, (B, Hkv, 1, d), device="cuda"), torch.bfloat16)
+        v = wl.to_storage(wl.normal(10, 30000 + step, (B, Hkv, 1, d), device="cuda"), torch.bfloat16)
+        a = f8.append_attention(0, q, k, v, np.ones(B)).float()
+        b = bf.append_attention(0, q, k, v, np.ones(B)).float()
+        diff = (a - b).abs()
+        worst = max(worst, float(diff.max()))
+        total += float(diff.mean())
+    print(f"fp8 vs bf16 cache over {steps} decode steps: max-abs {worst:.4f}, mean-abs {total / steps:.5f}")
+    assert worst < 0.1 and total / steps < 0.01
