@@ -511,14 +511,10 @@ def main():
         torch.cuda.set_device(0)
 
     res = run_native(w, args.steps, args.warmup, rank, world)
-    ms = res["ms"]
-    e2e_ms = res["e2e"]["ms"]
-    if world > 1:
-        t = torch.tensor([ms, e2e_ms], device="cuda")
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        ms, e2e_ms = float(t[0]), float(t[1])
-    value = res["work"] * world * scale / (ms * 1e-3)
-    e2e_value = res["e2e"]["work"] * world * scale / (e2e_ms * 1e-3)
+    graph_ms = res["graph"]["ms"] if "graph" in res else 0.0
+    ms, e2e_ms, graph_ms = max_over_ranks([res["ms"], res["e2e"]["ms"], graph_ms], world, "cuda")
+    value = whole_job_value(res["work"], world, ms, scale)
+    e2e_value = whole_job_value(res["e2e"]["work"], world, e2e_ms, scale)
 
     hbm, bf16, bf16_sus, peak_kind = _peaks()
     attn_ms = float(np.mean(res["attn_ms"]))
@@ -552,8 +548,8 @@ def main():
         line["frac_of_hbm_peak"] = value / hbm
     if "graph" in res:
         gr = res["graph"]
-        line["graph_replay"] = {"value": gr["work"] * world * scale / (gr["ms"] * 1e-3), "unit": w.unit,
-                                "ms_per_step": gr["ms"] / args.steps, "kernels_per_step": 3 * w.layers,
+        line["graph_replay"] = {"value": whole_job_value(gr["work"], world, graph_ms, scale), "unit": w.unit,
+                                "ms_per_step": graph_ms / args.steps, "kernels_per_step": 3 * w.layers,
                                 "note": "lengths resident on the device; one CUDA graph replay per step",
                                 "device_status": gr["status"]}
     if rank == 0 and not args.no_cpu_baseline:
@@ -563,6 +559,20 @@ def main():
         print(json.dumps(line))
     if world > 1:
         torch.distributed.destroy_process_group()
+
+
+def max_over_ranks(times_ms, world: int, device) -> list:
+    """Each timing's maximum over the ranks (the job is as slow as its slowest replica)."""
+    if world <= 1:
+        return [float(t) for t in times_ms]
+    t = torch.tensor([float(x) for x in times_ms], dtype=torch.float64, device=device)
+    torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+    return [float(x) for x in t]
+
+
+def whole_job_value(work_per_rank: float, world: int, max_ms: float, scale: float) -> float:
+    """Whole-job throughput: every rank's units (replicas do equal work) over the slowest rank's time."""
+    return work_per_rank * world * scale / (max_ms * 1e-3)
 
 
 def _committed_traffic(w: Workload, mean_kernel_bytes: float):
