@@ -227,9 +227,13 @@ class Workload:
         return kv_bytes(self.lens_at(i), s.Hkv, s.d, self.esize) * self.layers
 
     @property
+    def tc_min_rows(self):
+        """Query rows per KV head above which the library runs attention on the tcgen05 kernel."""
+        return 16 if self.kv_dtype == "fp8" else 12
+
+    @property
     def tensor_core(self):
-        """The library runs bf16 attention on the tcgen05 kernel above 12 query rows per KV head."""
-        return (self.Hq // self.shape.Hkv) * self.T > 12 and self.kv_dtype == "bf16"
+        return (self.Hq // self.shape.Hkv) * self.T > self.tc_min_rows
 
     @property
     def kernel_name(self):
@@ -245,9 +249,8 @@ class Workload:
 
     @property
     def fused(self):
-        """The library appends inside the attention launch on the split-KV kernel with warps owning whole
-        tiles: G*T <= 12 (bf16), G*T <= 16 (FP8 caches, which have no tensor-core path)."""
-        return (self.Hq // self.shape.Hkv) * self.T <= (16 if self.kv_dtype == "fp8" else 12)
+        """The library appends inside the attention launch whenever the split-KV kernel runs it."""
+        return not self.tensor_core
 
     def kernel_bytes(self, i):
         """Algorithmic bytes of the timed attention call: live K/V + q + out (+ the append when fused)."""

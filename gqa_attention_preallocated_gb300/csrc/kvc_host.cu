@@ -61,9 +61,14 @@ namespace {
 
 // Query rows per KV head (G * T) above which attention runs on the tcgen05
 // kernel; at or below it, on the split-KV kernel (mma.sync, appends fused).
-// Measured on the verify shape (B = 64, S = 4096): at 8 rows the split-KV
-// kernel is ahead by about 2 %, at 16 rows the tcgen05 kernel by about 3 %.
+// Measured on the verify shape (B = 64, S = 4096): bf16 at 8 rows, the
+// split-KV kernel is ahead by about 2 %, at 16 rows the tcgen05 kernel by
+// about 3 %.  An FP8 cache converts its tiles in shared memory on the tcgen05
+// kernel, so there the split-KV kernel leads up to 16 rows (427 K against
+// 303 K tokens/s at 16) and the tcgen05 kernel from 32 (1.7x at 64).
 constexpr int kTcMinRows = 12;
+constexpr int kTcMinRowsFp8 = 16;
+int tc_min_rows(const kvc_cache* c) { return c->dtype == KVC_FP8_E4M3 ? kTcMinRowsFp8 : kTcMinRows; }
 constexpr int kTcMaxLen = 0xFFFF * 128;  // key tiles of a piece are packed in 16 bits
 
 thread_local std::string g_last_error;
@@ -144,10 +149,8 @@ kvc_status encode_layer_maps(kvc_cache* c, int layer) {
     const bool fp8 = c->dtype == KVC_FP8_E4M3;
     if ((s = encode_rows_map(&c->tmK[layer], c->k[layer], rows, kKeyTile, fp8))) return s;
     if ((s = encode_rows_map(&c->tmV[layer], c->v[layer], rows, kKeyTile, fp8))) return s;
-    if (!fp8) {  // the tensor-core kernel (128-row boxes) serves bf16 caches only
-        if ((s = encode_rows_map(&c->tmK128[layer], c->k[layer], rows, 128))) return s;
-        if ((s = encode_rows_map(&c->tmV128[layer], c->v[layer], rows, 128))) return s;
-    }
+    if ((s = encode_rows_map(&c->tmK128[layer], c->k[layer], rows, 128, fp8))) return s;
+    if ((s = encode_rows_map(&c->tmV128[layer], c->v[layer], rows, 128, fp8))) return s;
     c->tm_ready[layer] = 1;
     return ok();
 }
@@ -239,7 +242,7 @@ kvc_status plan_shape(const kvc_cache* c, int Hq, int T, int num_ctas, AttnPlan*
         pl->ws_partials = static_cast<size_t>(pl->units + num_ctas) * pl->ways * pl->part_rows *
                           (kHeadDimBf16 + 4) * sizeof(float);
         pl->ws_min = pl->ws_err + pl->ws_plan + pl->ws_partials;
-        if (pl->R > kTcMinRows && c->dtype == KVC_BF16) {
+        if (pl->R > tc_min_rows(c)) {
             // The tensor-core kernel: up to two partial slots (2 row tiles x
             // 128 rows x (d + 4) floats) per SM share boundary.
             const size_t prefill = static_cast<size_t>(2) * std::min(num_ctas, kMaxCtas) * 2 * 128 *
@@ -361,7 +364,7 @@ kvc_status do_attention(kvc_cache* c, int layer, const void* q, const AttnPlan& 
 
     kvc_status s = encode_layer_maps(c, layer);
     if (s) return s;
-    if (c->dtype == KVC_BF16 && pl.R > kTcMinRows && k_new == nullptr && anc == nullptr && c->max_len <= kTcMaxLen) {
+    if (pl.R > tc_min_rows(c) && k_new == nullptr && anc == nullptr && c->max_len <= kTcMaxLen) {
         // Many query rows per KV head: tensor-core kernel, one CTA per piece.
         // Work items are (b, kvh, row block, pair of 128-row tiles): with
         // T >= 128, 128 positions of two query heads (mode 0); with T < 128 the
@@ -394,6 +397,12 @@ kvc_status do_attention(kvc_cache* c, int layer, const void* q, const AttnPlan& 
         pp.T = pl.T;
         pp.max_len = c->max_len;
         pp.mode = pl.T >= 128 ? 0 : (pl.R <= 128 ? 2 : 1);
+        pp.fp8 = c->dtype == KVC_FP8_E4M3 ? 1 : 0;
+        if (pp.fp8)
+            for (int h = 0; h < c->Hkv; ++h) {
+                pp.kscale[h] = c->kscale[static_cast<size_t>(layer) * c->Hkv + h];
+                pp.vscale[h] = c->vscale[static_cast<size_t>(layer) * c->Hkv + h];
+            }
         pp.ntb = pp.mode == 0 ? (pl.T + 127) / 128 : 1;
         pp.npair = pp.mode == 0 ? (pl.G + 1) / 2 : (pl.R + 255) / 256;
         pp.window = c->window;
@@ -919,8 +928,7 @@ static kvc_status append_attention_impl(kvc_cache* c, int layer, const void* q, 
     if (s) return s;
     cudaStream_t st = static_cast<cudaStream_t>(stream);
     int64_t* lw = c->lens.data() + static_cast<size_t>(layer) * c->B;
-    // (an FP8 cache has no tensor-core path: its split-KV kernel fuses the append up to 16 rows)
-    if (c->dtype != KVC_F32 && pl.mt == 1 && max_n > 0 && (pl.R <= kTcMinRows || c->dtype == KVC_FP8_E4M3)) {
+    if (c->dtype != KVC_F32 && pl.mt == 1 && max_n > 0 && pl.R <= tc_min_rows(c)) {
         // Warps own whole tiles: the attention kernel writes the new rows into
         // the cache itself (one launch instead of two).
         for (int b = 0; b < c->B; ++b) lw[b] += n_new[b];

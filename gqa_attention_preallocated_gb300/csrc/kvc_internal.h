@@ -225,6 +225,9 @@ struct PrefillParams {
     int B, Hq, Hkv, G, T, max_len;
     int ntb, npair, n_pieces;
     int mode;          // 0 positions, 1 packed rows in tile pairs, 2 one packed tile (see above)
+    int fp8;           // FP8 E4M3 cache: K of head h reads code * kscale[h], V code * vscale[h]
+    float kscale[kMaxScaleHeads];
+    float vscale[kMaxScaleHeads];
     int window, ring;  // sliding window (0 = none) and ring storage, as in DecodeParams
     Paging pg;
     float scale_log2;

@@ -19,6 +19,12 @@
 //          runs under the other's MMAs, and the two states are merged at the end.
 // Items are launched longest first (the host sorts them by key-tile count).
 //
+// FP8 E4M3 caches ("16. Prefill, decode and the KV cache", exercise 4): each
+// 128-key tile arrives as 128 x 128 bytes in the second half of its stage;
+// warps 2 and 3 convert it in place to the f16 tile (and the queries from bf16
+// to f16 once), and the MMAs run kind::f16 on f16 operands; the K scale folds
+// into the softmax scale and the V scale into the output normalisation.
+//
 // Warp roles (12 warps):
 //   warp 0      TMA producer: Q tiles once, then K and V tiles (128 keys) into
 //               two-stage rings guarded by mbarriers.
@@ -59,7 +65,7 @@ namespace kvc {
 
 namespace {
 
-constexpr int kThreadsPF = 384;  // 4 warps (producer, MMA issuer, 2 idle) + 8 softmax warps
+constexpr int kThreadsPF = 384;  // 4 warps (producer, MMA issuer, 2 converters / idle) + 8 softmax warps
 constexpr int kD = 128;
 constexpr int kBoxBytes = 128 * 128;           // 128 rows x 64 columns x 2 B (one swizzled box)
 constexpr int kTile128 = 2 * kBoxBytes;         // 128 rows x 128 columns
@@ -72,8 +78,11 @@ constexpr int kOffK = 2 * kTile128;             // K stages 0, 1
 constexpr int kOffV = 4 * kTile128;             // V stages 0, 1
 constexpr int kOffBar = 6 * kTile128;
 // barrier indices
+// (FP8 caches: TMA completes the *Raw barriers, the converter warps then arm
+// Q / KFull / VFull once the tiles are f16)
 constexpr int kBarQ = 0, kBarKFull = 1, kBarKEmpty = 3, kBarVFull = 5, kBarVEmpty = 7, kBarS = 9, kBarP = 11,
-              kBarO = 13, kNumBars = 15;
+              kBarO = 13, kBarQRaw = 15, kBarKRaw = 16, kBarVRaw = 18, kNumBars = 20;
+constexpr int kConvThreads = 64;  // warps 2 and 3
 constexpr size_t kSmemPF = 1024 + kOffBar + 256;
 
 __device__ __forceinline__ uint64_t smem_desc(uint32_t addr, uint32_t lbo, uint32_t sbo) {
@@ -83,10 +92,49 @@ __device__ __forceinline__ uint64_t smem_desc(uint32_t addr, uint32_t lbo, uint3
            (static_cast<uint64_t>((sbo >> 4) & 0x3FFF) << 32) | (1ull << 46) | (2ull << 61);
 }
 
-// Instruction descriptor, kind::f16: fp32 accumulator, bf16 A and B, M = N = 128.
-__device__ __forceinline__ uint32_t instr_desc(bool b_mn_major) {
-    return (1u << 4) | (1u << 7) | (1u << 10) | (static_cast<uint32_t>(b_mn_major) << 16) | ((128u >> 3) << 17) |
-           ((128u >> 4) << 24);
+// Instruction descriptor, kind::f16: fp32 accumulator, bf16 (or f16) A and B, M = N = 128.
+__device__ __forceinline__ uint32_t instr_desc(bool b_mn_major, bool f16 = false) {
+    const uint32_t ab = f16 ? 0u : ((1u << 7) | (1u << 10));  // A and B format: 0 = f16, 1 = bf16
+    return (1u << 4) | ab | (static_cast<uint32_t>(b_mn_major) << 16) | ((128u >> 3) << 17) | ((128u >> 4) << 24);
+}
+
+// FP8 caches: one 128-key tile of E4M3 codes (128 rows x 128 bytes, 128-byte
+// swizzle) sits in the second half of a stage; convert it in place to the f16
+// tile the MMAs read (two 64-column boxes, 128-byte swizzle).  Each thread
+// owns whole rows: it reads its row's 128 bytes before writing the row's
+// 256, and no other row is touched, so the in-place order is safe.
+__device__ __forceinline__ void convert_e4m3_tile(uint8_t* slot, int ct) {
+    for (int r = ct; r < 128; r += kConvThreads) {
+        const uint8_t* src = slot + kBoxBytes + r * 128;
+        uint4 c8[8];
+#pragma unroll
+        for (int c = 0; c < 8; ++c) c8[c] = *reinterpret_cast<const uint4*>(src + (((c ^ (r & 7))) << 4));
+#pragma unroll
+        for (int c = 0; c < 8; ++c) {
+            // fp8 chunk c = columns 16c .. 16c + 15 -> f16 chunks 2c, 2c + 1
+            const uint32_t w[4] = {c8[c].x, c8[c].y, c8[c].z, c8[c].w};
+            uint32_t h[8];
+#pragma unroll
+            for (int i = 0; i < 4; ++i) ptx::e4m3x4_to_f16x2x2(w[i], h[2 * i], h[2 * i + 1]);
+#pragma unroll
+            for (int half = 0; half < 2; ++half) {
+                const int cc = 2 * c + half;  // f16 chunk of the 256-byte row
+                uint8_t* dst = slot + (cc >> 3) * kBoxBytes + r * 128 + ((((cc & 7) ^ (r & 7))) << 4);
+                *reinterpret_cast<uint4*>(dst) = make_uint4(h[4 * half], h[4 * half + 1], h[4 * half + 2], h[4 * half + 3]);
+            }
+        }
+    }
+}
+
+// bf16 -> f16 in place (same layout): the queries of an FP8 cache's MMAs.
+__device__ __forceinline__ void convert_bf16_tiles(uint8_t* base, int bytes, int ct) {
+    for (int off = ct * 16; off < bytes; off += kConvThreads * 16) {
+        uint4 v = *reinterpret_cast<const uint4*>(base + off);
+        uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+        for (int i = 0; i < 4; ++i) w[i] = ptx::pack_f16x2(__uint_as_float(w[i] << 16), __uint_as_float(w[i] & 0xFFFF0000u));
+        *reinterpret_cast<uint4*>(base + off) = make_uint4(w[0], w[1], w[2], w[3]);
+    }
 }
 
 __device__ __forceinline__ void mma_ss(uint32_t d_tmem, uint64_t a, uint64_t b, uint32_t id, uint32_t acc) {
@@ -231,7 +279,7 @@ __device__ __forceinline__ Piece decode_piece(const PrefillParams& p, int idx) {
 // registers do not press on the softmax loop.
 __device__ __noinline__ void split_epilogue(float* partials, int* err, uint32_t tO, int i, int r, bool valid,
                                             float m_ref, float l, int slot, int kidx, int npc, __nv_bfloat16* dst,
-                                            volatile int* merge_flag) {
+                                            volatile int* merge_flag, float out_scale) {
     const int slot0 = slot - kidx;
     auto part_of = [&](int sl) {
         return partials + ((static_cast<size_t>(sl) * 2 + i) * 128 + r) * (kD + 4);
@@ -271,7 +319,7 @@ __device__ __noinline__ void split_epilogue(float* partials, int* err, uint32_t 
                     const float* pk_ = part_of(slot0 + k);
                     L += __ldcg(pk_ + kD + 1) * ptx::ex2(__ldcg(pk_ + kD) - M);
                 }
-        const float inv = (valid && L > 0.f) ? 1.f / L : 0.f;
+        const float inv = (valid && L > 0.f) ? out_scale / L : 0.f;  // out_scale: an FP8 cache's V scale
 #pragma unroll 1
         for (int c = 0; c < 4; ++c) {
             uint32_t w[32];
@@ -311,8 +359,10 @@ __device__ __noinline__ void split_epilogue(float* partials, int* err, uint32_t 
 
 // kWin: the cache has a sliding window (and possibly ring storage); without
 // one the window code is compiled out.  kAlt: mode 2 (one packed row tile,
-// alternate key tiles per TMEM buffer); modes 0 and 1 otherwise.
-template <bool kWin, bool kAlt>
+// alternate key tiles per TMEM buffer); modes 0 and 1 otherwise.  kF8: the
+// cache holds E4M3 codes (converted to f16 in shared memory by warps 2 and 3;
+// the MMAs run on f16 with the queries converted too).
+template <bool kWin, bool kAlt, bool kF8>
 __global__ void __launch_bounds__(kThreadsPF, 1)
     prefill_tc_kernel(const __grid_constant__ PrefillParams p, const __grid_constant__ CUtensorMap tmQ,
                       const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmV) {
@@ -328,11 +378,15 @@ __global__ void __launch_bounds__(kThreadsPF, 1)
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
 
     if (tid == 0) {
-        ptx::mbar_init(bar(kBarQ), 1);
+        const int ready = kF8 ? 2 : 1;  // FP8: both converter warps arrive; else the TMA's arrive
+        ptx::mbar_init(bar(kBarQ), ready);
+        ptx::mbar_init(bar(kBarQRaw), 1);
         for (int s = 0; s < 2; ++s) {
-            ptx::mbar_init(bar(kBarKFull + s), 1);
+            ptx::mbar_init(bar(kBarKFull + s), ready);
+            ptx::mbar_init(bar(kBarKRaw + s), 1);
+            ptx::mbar_init(bar(kBarVRaw + s), 1);
             ptx::mbar_init(bar(kBarKEmpty + s), 1);
-            ptx::mbar_init(bar(kBarVFull + s), 1);
+            ptx::mbar_init(bar(kBarVFull + s), ready);
             ptx::mbar_init(bar(kBarVEmpty + s), 1);
             ptx::mbar_init(bar(kBarS + s), 1);
             ptx::mbar_init(bar(kBarP + s), 4);
@@ -393,13 +447,14 @@ __global__ void __launch_bounds__(kThreadsPF, 1)
     if (warp == 0) {
         // ------------------------------------------------------------ TMA producer
         if (lane == 0) {
-            ptx::mbar_arrive_expect_tx(bar(kBarQ), nh * kTile128);
+            const int qbar = kF8 ? kBarQRaw : kBarQ;
+            ptx::mbar_arrive_expect_tx(bar(qbar), nh * kTile128);
             for (int i = 0; i < nh; ++i) {
                 // mode 0: 128 positions of head h0 + i; modes 1, 2: 128 packed rows
                 const int qrow = (p.mode == 0) ? ((b * p.Hq) + h0 + i) * p.T + t0
                                                : (b * p.Hq + h0) * p.T + pc.pr0 + i * 128;
                 for (int hf = 0; hf < 2; ++hf)
-                    ptx::tma_load_2d(sbase + kOffQ + i * kTile128 + hf * kBoxBytes, &tmQ, hf * 64, qrow, bar(kBarQ));
+                    ptx::tma_load_2d(sbase + kOffQ + i * kTile128 + hf * kBoxBytes, &tmQ, hf * 64, qrow, bar(qbar));
             }
             for (int j = 0; j < nkt && !*abort_flag; ++j) {
                 const int s = j & 1;
@@ -409,24 +464,60 @@ __global__ void __launch_bounds__(kThreadsPF, 1)
                     *abort_flag = 1;
                     break;
                 }
-                ptx::mbar_arrive_expect_tx(bar(kBarKFull + s), kTile128);
-                for (int hf = 0; hf < 2; ++hf)
-                    ptx::tma_load_2d(sbase + kOffK + s * kTile128 + hf * kBoxBytes, &tmK, hf * 64, row,
-                                     bar(kBarKFull + s));
+                if constexpr (kF8) {  // one 128 x 128-byte box into the stage's second half
+                    ptx::mbar_arrive_expect_tx(bar(kBarKRaw + s), kBoxBytes);
+                    ptx::tma_load_2d(sbase + kOffK + s * kTile128 + kBoxBytes, &tmK, 0, row, bar(kBarKRaw + s));
+                } else {
+                    ptx::mbar_arrive_expect_tx(bar(kBarKFull + s), kTile128);
+                    for (int hf = 0; hf < 2; ++hf)
+                        ptx::tma_load_2d(sbase + kOffK + s * kTile128 + hf * kBoxBytes, &tmK, hf * 64, row,
+                                         bar(kBarKFull + s));
+                }
                 if (j >= 2 && !ptx::mbar_wait_bounded(bar(kBarVEmpty + s), ((j >> 1) & 1) ^ 1, kWaitNs)) {
                     atomicExch(p.err, kDevTimeoutEmpty);
                     *abort_flag = 1;
                     break;
                 }
-                ptx::mbar_arrive_expect_tx(bar(kBarVFull + s), kTile128);
-                for (int hf = 0; hf < 2; ++hf)
-                    ptx::tma_load_2d(sbase + kOffV + s * kTile128 + hf * kBoxBytes, &tmV, hf * 64, row,
-                                     bar(kBarVFull + s));
+                if constexpr (kF8) {
+                    ptx::mbar_arrive_expect_tx(bar(kBarVRaw + s), kBoxBytes);
+                    ptx::tma_load_2d(sbase + kOffV + s * kTile128 + kBoxBytes, &tmV, 0, row, bar(kBarVRaw + s));
+                } else {
+                    ptx::mbar_arrive_expect_tx(bar(kBarVFull + s), kTile128);
+                    for (int hf = 0; hf < 2; ++hf)
+                        ptx::tma_load_2d(sbase + kOffV + s * kTile128 + hf * kBoxBytes, &tmV, hf * 64, row,
+                                         bar(kBarVFull + s));
+                }
             }
+        }
+    } else if (kF8 && (warp == 2 || warp == 3)) {
+        // ------------------------------------------------------------ E4M3 -> f16 converters
+        const int ct = tid - 64;
+        auto wait_raw = [&](int b_idx, int parity) {
+            if (!ptx::mbar_wait_bounded(bar(b_idx), parity, *abort_flag ? 0ull : kWaitNs)) {
+                atomicExch(p.err, kDevTimeoutFull);
+                *abort_flag = 1;
+            }
+        };
+        auto ready = [&](int b_idx) {  // generic writes -> visible to the tensor core, then arrive
+            ptx::fence_proxy_async_smem();
+            __syncwarp();
+            if (lane == 0) ptx::mbar_arrive(bar(b_idx));
+        };
+        wait_raw(kBarQRaw, 0);
+        convert_bf16_tiles(smem + kOffQ, nh * kTile128, ct);
+        ready(kBarQ);
+        for (int j = 0; j < nkt; ++j) {
+            const int s = j & 1;
+            wait_raw(kBarKRaw + s, (j >> 1) & 1);
+            convert_e4m3_tile(smem + kOffK + s * kTile128, ct);
+            ready(kBarKFull + s);
+            wait_raw(kBarVRaw + s, (j >> 1) & 1);
+            convert_e4m3_tile(smem + kOffV + s * kTile128, ct);
+            ready(kBarVFull + s);
         }
     } else if (warp == 1) {
         // ------------------------------------------------------------ MMA issuer
-        const uint32_t id_qk = instr_desc(false), id_pv = instr_desc(true);
+        const uint32_t id_qk = instr_desc(false, kF8), id_pv = instr_desc(true, kF8);
         auto wait = [&](int b_idx, int parity) {
             if (!ptx::mbar_wait_bounded(bar(b_idx), parity, *abort_flag ? 0ull : kWaitNs)) {
                 atomicExch(p.err, kDevTimeoutFull);
@@ -546,6 +637,8 @@ __global__ void __launch_bounds__(kThreadsPF, 1)
             const int jfirst = alt ? i : 0, jstep = alt ? 2 : 1;
             const int nloc = alt ? (nkt - i + 1) / 2 : nkt;
             const int lo_row = (kWin && valid) ? lim - p.window : -(1 << 30);  // keys <= lo_row: outside the window
+            // score scale in base 2 (times the K scale of an FP8 cache)
+            const float sl2 = kF8 ? p.scale_log2 * p.kscale[kvh] : p.scale_log2;
             float m_ref = -INFINITY, l = 0.f;
             for (int jj = 0; jj < nloc; ++jj) {
                 const int j = jfirst + jj * jstep;
@@ -575,7 +668,7 @@ __global__ void __launch_bounds__(kThreadsPF, 1)
                             if (e <= kl && e > kll) mx = fmaxf(mx, __uint_as_float(v[e]));
                     }
                 }
-                mx = (mx == -INFINITY) ? -INFINITY : mx * p.scale_log2;
+                mx = (mx == -INFINITY) ? -INFINITY : mx * sl2;
                 const bool move = mx > m_ref + kRescaleThreshold || (m_ref == -INFINITY && mx != -INFINITY);
                 if (__any_sync(0xffffffffu, move)) {
                     // Move the reference max.  O_i holds the PV sums up to tile
@@ -609,7 +702,7 @@ __global__ void __launch_bounds__(kThreadsPF, 1)
                 }
                 // pass 2: p = 2^(s * scale - m_ref) as bf16 pairs into TMEM over S_i
                 const float mu = (m_ref == -INFINITY) ? 0.f : m_ref;
-                const uint64_t sc2 = f2pack(p.scale_log2, p.scale_log2), nmu2 = f2pack(-mu, -mu);
+                const uint64_t sc2 = f2pack(sl2, sl2), nmu2 = f2pack(-mu, -mu);
                 uint64_t sum2 = f2pack(0.f, 0.f);
                 uint32_t pk[32];
 #pragma unroll
@@ -628,7 +721,7 @@ __global__ void __launch_bounds__(kThreadsPF, 1)
                             if (e + 1 > kl || e + 1 <= kll) p1 = 0.f;
                         }
                         sum2 = fadd2(sum2, f2pack(p0, p1));
-                        pk[e >> 1] = ptx::pack_bf16x2(p0, p1);
+                        pk[e >> 1] = kF8 ? ptx::pack_f16x2(p0, p1) : ptx::pack_bf16x2(p0, p1);
                     }
                     // keys c*64 .. c*64+63 -> P columns c*32 .. c*32+31 (S columns already read)
                     tmem_st32(tS + c * 32, pk);
@@ -691,9 +784,10 @@ __global__ void __launch_bounds__(kThreadsPF, 1)
             if (alt && i == 1) {
                 // state handed to warpgroup 0
             } else if (pc.slot != kPrefillNoSlot) {
-                split_epilogue(p.partials, p.err, tO, i, r, valid, m_ref, l, pc.slot, pc.kidx, pc.npc, dst, merge_flag);
+                split_epilogue(p.partials, p.err, tO, i, r, valid, m_ref, l, pc.slot, pc.kidx, pc.npc, dst, merge_flag,
+                               kF8 ? p.vscale[kvh] : 1.f);
             } else {
-            const float inv = (valid && l > 0.f) ? 1.f / l : 0.f;
+            const float inv = (valid && l > 0.f) ? (kF8 ? p.vscale[kvh] : 1.f) / l : 0.f;
 #pragma unroll
             for (int c = 0; c < 4; ++c) {
                 uint32_t w[32];
@@ -731,8 +825,10 @@ cudaError_t launch_prefill_tc(const PrefillParams& p, const CUtensorMap& tmQ, co
                               const CUtensorMap& tmV, cudaStream_t stream) {
     static bool attr_set = false;
     if (!attr_set) {
-        for (auto* k : {prefill_tc_kernel<false, false>, prefill_tc_kernel<true, false>, prefill_tc_kernel<false, true>,
-                        prefill_tc_kernel<true, true>}) {
+        for (auto* k : {prefill_tc_kernel<false, false, false>, prefill_tc_kernel<true, false, false>,
+                        prefill_tc_kernel<false, true, false>, prefill_tc_kernel<true, true, false>,
+                        prefill_tc_kernel<false, false, true>, prefill_tc_kernel<true, false, true>,
+                        prefill_tc_kernel<false, true, true>, prefill_tc_kernel<true, true, true>}) {
             cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                                  static_cast<int>(kSmemPF));
             if (e != cudaSuccess) return e;
@@ -751,10 +847,15 @@ cudaError_t launch_prefill_tc(const PrefillParams& p, const CUtensorMap& tmQ, co
     cfg.numAttrs = 1;
     const bool win = p.window > 0 || p.ring;
     const bool alt = p.mode == 2;
-    cudaError_t e = win ? (alt ? cudaLaunchKernelEx(&cfg, prefill_tc_kernel<true, true>, p, tmQ, tmK, tmV)
-                               : cudaLaunchKernelEx(&cfg, prefill_tc_kernel<true, false>, p, tmQ, tmK, tmV))
-                        : (alt ? cudaLaunchKernelEx(&cfg, prefill_tc_kernel<false, true>, p, tmQ, tmK, tmV)
-                               : cudaLaunchKernelEx(&cfg, prefill_tc_kernel<false, false>, p, tmQ, tmK, tmV));
+    using Kernel = void (*)(PrefillParams, CUtensorMap, CUtensorMap, CUtensorMap);
+    Kernel k;
+    if (p.fp8)
+        k = win ? (alt ? prefill_tc_kernel<true, true, true> : prefill_tc_kernel<true, false, true>)
+                : (alt ? prefill_tc_kernel<false, true, true> : prefill_tc_kernel<false, false, true>);
+    else
+        k = win ? (alt ? prefill_tc_kernel<true, true, false> : prefill_tc_kernel<true, false, false>)
+                : (alt ? prefill_tc_kernel<false, true, false> : prefill_tc_kernel<false, false, false>);
+    cudaError_t e = cudaLaunchKernelEx(&cfg, k, p, tmQ, tmK, tmV);
     if (e != cudaSuccess) return e;
     return cudaGetLastError();
 }

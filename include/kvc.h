@@ -62,7 +62,9 @@ extern "C" {
  * no infinity) with one scale per (layer, KV head) for K and for V
  * (kvc_set_kv_scales), and take bf16 q / k_new / v_new / out ("16. Prefill,
  * decode and the KV cache", exercise 4: store the cache in FP8 E4M3 with one
- * scale per head and dequantize on read). */
+ * scale per head and dequantize on read).  Their MMAs run in f16 (E4M3 and
+ * bf16 convert to f16 exactly within f16's range), so an FP8 cache needs
+ * |q| < 65504. */
 typedef enum { KVC_F32 = 0, KVC_BF16 = 1, KVC_FP8_E4M3 = 2 } kvc_dtype;
 
 typedef enum {
@@ -202,10 +204,10 @@ kvc_status kvc_append_attention_tree(kvc_cache* c, int layer, const void* q, con
  * Its scratch is one static device array of KVC_NOALLOC_SCRATCH_BYTES
  * (32 MiB) inside the library: every GPU that loads the library holds it
  * until the process exits.  No cudaMalloc, cudaFree or other allocating
- * call is made.  Calls with more than 12 query rows per KV head (G * T)
- * run on the tensor-core kernel, which needs only the workspace header and
+ * call is made.  Calls with more than 12 query rows per KV head (G * T; 16
+ * for FP8 caches) run on the tensor-core kernel, which needs only the workspace header and
  * uses the rest of the array for the partials of the items it cuts; they
- * always fit.  A call with at most 12 rows per KV head whose split-KV
+ * always fit.  A call with fewer rows per KV head whose split-KV
  * scratch would exceed the array (very large batches; kvc_workspace_bytes
  * gives its size) is rejected with KVC_ERR_WORKSPACE before anything is
  * enqueued; decode shapes of batches up to 64 rows fit.
