@@ -1,4 +1,5 @@
-// Split-KV GQA attention over the preallocated cache, bf16 storage, d = 128.
+// Split-KV GQA attention over the preallocated cache, bf16 or FP8 E4M3
+// storage, d = 128.
 //
 // What it computes ("Implement grouped-query attention over a preallocated KV
 // cache...", "A strong answer", gqa_attention): for every row b, KV head kvh
@@ -35,6 +36,13 @@
 //  * Cache slots past lens may hold anything (stale or NaN).  Masked scores
 //    are replaced, never multiplied, and V rows past the unit's last visible
 //    key are cleared in shared memory before PV, so 0 * NaN cannot occur.
+//  * FP8 E4M3 storage ("16. Prefill, decode and the KV cache", exercise 4;
+//    template argument F8): 64-key tiles of one byte a value, converted to f16
+//    exactly in registers (one cvt per pair) and multiplied by f16 queries,
+//    with the head dimension permuted so each thread's K bytes are contiguous
+//    and the output columns permuted so its V bytes are one 16-byte chunk per
+//    key; the per-head K scale folds into the softmax scale, the V scale into
+//    the output.  Appends fused into the launch quantize the new rows.
 //  * Every wait is bounded in time; on expiry the kernel records an error code
 //    in the workspace and finishes instead of hanging.
 

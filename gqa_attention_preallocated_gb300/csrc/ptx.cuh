@@ -1,5 +1,5 @@
 // Thin inline-PTX wrappers (PTX ISA: mbarrier, cp.async.bulk.tensor, ldmatrix,
-// mma.sync, ex2.approx) used by the attention kernels.
+// mma.sync, ex2.approx, E4M3 conversions, prmt) used by the attention kernels.
 #pragma once
 
 #include <cuda_bf16.h>
@@ -124,14 +124,9 @@ __device__ __forceinline__ void mma_f16_16816(float (&d)[4], const uint32_t (&a)
         : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
 }
 
-// Two E4M3 bytes (low byte = first element) -> f16x2 (low half = first); exact.
-__device__ __forceinline__ uint32_t e4m3x2_to_f16x2(uint32_t two_bytes) {
-    uint32_t d;
-    asm("{\n\t.reg .b16 t;\n\tcvt.u16.u32 t, %1;\n\tcvt.rn.f16x2.e4m3x2 %0, t;\n\t}" : "=r"(d) : "r"(two_bytes));
-    return d;
-}
-
-// Four E4M3 bytes -> two f16x2: bytes 0, 1 -> lo, bytes 2, 3 -> hi (low half = lower byte).
+// Four E4M3 bytes -> two f16x2, exactly: bytes 0, 1 -> lo, bytes 2, 3 -> hi
+// (low half = lower byte).  Splitting the word into its 16-bit halves is a
+// register-pair view, so each pair costs one conversion instruction.
 __device__ __forceinline__ void e4m3x4_to_f16x2x2(uint32_t four_bytes, uint32_t& lo, uint32_t& hi) {
     asm("{\n\t.reg .b16 a, b;\n\tmov.b32 {a, b}, %2;\n\tcvt.rn.f16x2.e4m3x2 %0, a;\n\t"
         "cvt.rn.f16x2.e4m3x2 %1, b;\n\t}"
