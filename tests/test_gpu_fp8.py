@@ -216,3 +216,67 @@ def test_fp8_against_bf16_cache_over_many_decode_steps():
         total += float(diff.mean())
     print(f"fp8 vs bf16 cache over {steps} decode steps: max-abs {worst:.4f}, mean-abs {total / steps:.5f}")
     assert worst < 0.1 and total / steps < 0.01
+
+
+@pytest.mark.parametrize("T,G", [(1, 4), (8, 8)])
+def test_fp8_full_size_sampled(T, G):
+    """The decode8b shape (B=32, Hkv=8, [32, 8, 8192, 128]) on an FP8 cache at full size, in the
+    launch configuration the benchmark times: one step, then sampled (row, KV head) units checked
+    query by query against the oracle reading the cache's own codes (T = 8, G = 8 runs on the
+    tensor-core kernel's FP8 variant)."""
+    _cuda_or_skip()
+    s = wl.DECODE_8B
+    B, Hkv, L, d = s.B, s.Hkv, s.max_len, s.d
+    cache = KVCache(1, B, Hkv, L, d, dtype=FP8)
+    sc = np.full(Hkv, 4.0 / 448, dtype=np.float32)
+    cache.set_kv_scales(0, sc, sc)
+    for buf, stream in ((cache.k[0], wl.STREAM_CACHE_K), (cache.v[0], wl.STREAM_CACHE_V)):
+        flat = buf.view(-1)
+        for start in range(0, flat.numel(), 1 << 26):
+            stop = min(flat.numel(), start + (1 << 26))
+            idx = torch.arange(start, stop, dtype=torch.int64, device="cuda")
+            x = wl.normal_at(21, stream, idx).to(torch.float32) * (448 / 4.0)
+            flat[start:stop] = x.clamp_(-448.0, 448.0).to(FP8)
+    lens0 = wl.decode_lens(21, B, 1024, L - 256)
+    cache.set_lens(0, lens0)
+    Hq = Hkv * G
+    q = wl.to_storage(wl.normal(21, 5, (B, Hq, T, d)), torch.bfloat16)
+    k = wl.to_storage(wl.normal(21, 6, (B, Hkv, T, d)), torch.bfloat16)
+    v = wl.to_storage(wl.normal(21, 7, (B, Hkv, T, d)), torch.bfloat16)
+    nn = np.full(B, T)
+    out = cache.append_attention(0, q.cuda(), k.cuda(), v.cuda(), nn).double().cpu().numpy()
+    assert cache.device_status() == 0
+    qd = q.double().numpy()
+    worst = 0.0
+    for b, kvh in [(0, 0), (int(np.argmax(lens0)), 7), (17, 3)]:
+        Lb = int(lens0[b]) + T
+        K = ref.e4m3_dequantize(cache.k[0][b, kvh, :Lb].view(torch.uint8).cpu().numpy(), sc[kvh])
+        V = ref.e4m3_dequantize(cache.v[0][b, kvh, :Lb].view(torch.uint8).cpu().numpy(), sc[kvh])
+        for g in range(G):
+            for t in range(T):
+                want = ref.attend_one_query(qd[b, kvh * G + g, t], K, V, ref.query_position(Lb, T, t))
+                worst = max(worst, float(np.max(np.abs(out[b, kvh * G + g, t] - want))))
+    assert worst <= TOL, worst
+
+
+def test_fp8_ring_storage():
+    """Ring storage (slot = position mod max_len) with a window over an FP8 cache, past the wrap."""
+    _cuda_or_skip()
+    B, Hkv, G, max_len, W = 2, 2, 4, 512, 300
+    cache = KVCache(1, B, Hkv, max_len, 128, dtype=FP8)
+    cache.k[0].view(torch.uint8).fill_(0x7F)
+    cache.v[0].view(torch.uint8).fill_(0x7F)
+    ks, vs = _scales(Hkv, 16)
+    cache.set_kv_scales(0, ks, vs)
+    cache.set_window(W, ring=True)
+    orc = ref.OracleCache(1, B, Hkv, max_len, 128)
+    orc.set_fp8()
+    orc.set_kv_scales(0, ks.astype(np.float64), vs.astype(np.float64))
+    orc.set_window(W, ring=True)
+    rng = np.random.default_rng(17)
+    for ci in range(6):
+        _step(cache, orc, 18, ci, G, rng.integers(100, max_len - W + 2, size=B))
+    for ci in range(6, 10):
+        _step(cache, orc, 18, ci, G, [1, 1])
+    assert np.all(orc.lens[0] > max_len)  # the ring wrapped
+    assert cache.device_status() == 0
