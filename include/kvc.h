@@ -199,7 +199,7 @@ kvc_status kvc_append_attention_tree(kvc_cache* c, int layer, const void* q, con
  * a latency-critical loop that must not pay cudaMalloc's cost and implicit
  * synchronization.  The pages have no counterpart of this entry point; it
  * computes exactly what kvc_gqa_attention computes (same kernel, same
- * result) and serves bf16 caches only.
+ * result) and serves bf16 and FP8 caches.
  *
  * Its scratch is one static device array of KVC_NOALLOC_SCRATCH_BYTES
  * (32 MiB) inside the library: every GPU that loads the library holds it
