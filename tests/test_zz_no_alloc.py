@@ -95,3 +95,27 @@ def test_noalloc_rejects_oversized_calls():
     assert _noalloc(cache, q, np.full(B, T), out) == 7  # KVC_ERR_WORKSPACE, nothing enqueued
     torch.cuda.synchronize()
     assert bool((out == 0).all())
+
+
+def test_noalloc_fp8_cache():
+    """An FP8 E4M3 cache through the static scratch: decode on the split-KV kernel and a 64-row verify on
+    the tensor-core kernel, each equal to the workspace entry point (same kernel, same bits)."""
+    if not torch.cuda.is_available():
+        pytest.skip("needs a GPU")
+    build_library()
+    B, Hkv, d, max_len = 8, 4, 128, 2048
+    cache = KVCache(1, B, Hkv, max_len, d, dtype=torch.float8_e4m3fn)
+    sc = np.full(Hkv, 4.0 / 448, dtype=np.float32)
+    cache.set_kv_scales(0, sc, sc)
+    prefill = np.random.default_rng(6).integers(600, 1500, size=B)
+    T0 = int(prefill.max())
+    cache.append(0, _bf16(4, 1, (B, Hkv, T0, d)), _bf16(4, 2, (B, Hkv, T0, d)), prefill)
+    for call, (T, G) in enumerate([(1, 4), (8, 8)]):
+        n_new = np.full(B, T)
+        cache.append(0, _bf16(5, 10 + call, (B, Hkv, T, d)), _bf16(5, 20 + call, (B, Hkv, T, d)), n_new)
+        q = _bf16(6, 30 + call, (B, Hkv * G, T, d))
+        ref_out = cache.gqa_attention(0, q, n_new)
+        out = torch.full_like(q, float("nan"))
+        assert _noalloc(cache, q, n_new, out) == 0, _lib.lib().kvc_last_error()
+        torch.cuda.synchronize()
+        assert torch.equal(out, ref_out), call
