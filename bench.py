@@ -27,6 +27,7 @@ import math
 import os
 import subprocess
 import sys
+import tempfile
 import time
 
 for _v in ("OPENBLAS_NUM_THREADS", "OMP_NUM_THREADS", "MKL_NUM_THREADS"):
@@ -62,7 +63,8 @@ class ClockSampler:
     def __init__(self, index: int):
         self.index = index
         self.proc = None
-        self.path = os.path.join(ROOT, "gpurun_out", f"clocks_gpu{index}.csv")
+        # the raw samples go to a temporary file; the JSON line carries their summary
+        self.path = os.path.join(tempfile.gettempdir(), f"kvc_bench_clocks_gpu{index}_{os.getpid()}.csv")
 
     def __enter__(self):
         try:
