@@ -876,10 +876,22 @@ struct CPart<false> {
 template <>
 struct CPart<true> {
     const CombineParams& p;
+    const int* cta_start_sh;  // the plan's CTA starts, staged in shared memory (searched per thread)
     __device__ __forceinline__ int gstart(int i) const { return p.dplan->gstart[i]; }
-    __device__ __forceinline__ int cta_start(int i) const { return p.dplan->cta_start[i]; }
+    __device__ __forceinline__ int cta_start(int i) const { return cta_start_sh[i]; }
     __device__ __forceinline__ int n_new(int b) const { return p.dplan->n_new[b]; }
 };
+
+template <bool DP>
+__device__ __forceinline__ CPart<DP> make_cpart(const CombineParams& p, const int* sh);
+template <>
+__device__ __forceinline__ CPart<false> make_cpart<false>(const CombineParams& p, const int*) {
+    return CPart<false>{p};
+}
+template <>
+__device__ __forceinline__ CPart<true> make_cpart<true>(const CombineParams& p, const int* sh) {
+    return CPart<true>{p, sh};
+}
 
 // CTA whose tile range holds tile x: largest i with cta_start[i] <= x (CTAs
 // with empty ranges repeat the next start, so the owner is the last of them).
@@ -898,7 +910,14 @@ __global__ void __launch_bounds__(kCombineThreads) combine_bf16_kernel(const __g
     ptx::grid_dependency_wait();
     ptx::launch_dependents();
     if (DP && p.dplan->skip) return;
-    const CPart<DP> cw{p};
+    // A device plan lives in global memory: stage its CTA starts in shared
+    // memory once (one parallel round trip) instead of searching them there.
+    __shared__ int cta_start_sh[DP ? kMaxCtas + 1 : 1];
+    if constexpr (DP) {
+        for (int i = threadIdx.x; i <= p.num_ctas; i += kCombineThreads) cta_start_sh[i] = p.dplan->cta_start[i];
+        __syncthreads();
+    }
+    const CPart<DP> cw = make_cpart<DP>(p, cta_start_sh);
     const int u = blockIdx.x;
     const int q = u / p.Hkv, kvh = u - q * p.Hkv;
     const int nt = (cw.gstart(q + 1) - cw.gstart(q)) / p.Hkv;
