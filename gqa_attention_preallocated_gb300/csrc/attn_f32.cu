@@ -1,4 +1,9 @@
-// GQA attention for fp32 storage (any d <= 256 with d % 4 == 0).
+// Generic GQA attention: fp32 storage (d <= 256, d % 4 == 0), and bf16
+// storage of a head dimension other than the 128 the TMA / tensor-core
+// kernels take (d <= 256, d % 8 == 0).  Values are widened to fp32 as they
+// are staged in shared memory; scores, softmax and the output accumulate in
+// fp32; a bf16 cache takes bf16 queries and writes bf16 outputs (rounded to
+// nearest even).
 //
 // Semantics ("Implement grouped-query attention over a preallocated KV
 // cache...", "A strong answer", gqa_attention): query (b, h, t) with
@@ -21,6 +26,7 @@
 // verify ("What interviewers probe next", tree-based speculative decoding):
 // a query sees the chunk's tokens on its own path to the root only.
 
+#include <cuda_bf16.h>
 #include <math.h>
 
 #include "kvc_internal.h"
@@ -34,7 +40,35 @@ constexpr int kKeys = 32;
 constexpr int kWarps = 4;
 constexpr int kMaxD = 256;
 
+__device__ __forceinline__ float widen(float x) { return x; }
+__device__ __forceinline__ float widen(__nv_bfloat16 x) { return __bfloat162float(x); }
+__device__ __forceinline__ void store_out(float* dst, float x) { *dst = x; }
+__device__ __forceinline__ void store_out(__nv_bfloat16* dst, float x) { *dst = __float2bfloat16_rn(x); }
+
+// 16 stored bytes (4 fp32 or 8 bf16 values) into fp32 shared memory.
+__device__ __forceinline__ void stage16(float* dst, const float* src) {
+    *reinterpret_cast<float4*>(dst) = *reinterpret_cast<const float4*>(src);
+}
+__device__ __forceinline__ void stage16(float* dst, const __nv_bfloat16* src) {
+    const uint4 w = *reinterpret_cast<const uint4*>(src);
+    const uint32_t u[4] = {w.x, w.y, w.z, w.w};
+    float f[8];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {  // bf16 -> fp32 is exact: the bits move up 16
+        f[2 * i] = __uint_as_float(u[i] << 16);
+        f[2 * i + 1] = __uint_as_float(u[i] & 0xffff0000u);
+    }
+    reinterpret_cast<float4*>(dst)[0] = make_float4(f[0], f[1], f[2], f[3]);
+    reinterpret_cast<float4*>(dst)[1] = make_float4(f[4], f[5], f[6], f[7]);
+}
+
+template <typename E>
 __global__ void __launch_bounds__(kWarps * 32) attn_f32_kernel(const __grid_constant__ F32Params p) {
+    constexpr int kVec = 16 / static_cast<int>(sizeof(E));  // values per 16-byte load
+    const E* qg = static_cast<const E*>(p.q);
+    const E* kg = static_cast<const E*>(p.k_cache);
+    const E* vg = static_cast<const E*>(p.v_cache);
+    E* og = static_cast<E*>(p.out);
     extern __shared__ float4 smem4[];
     float* sq = reinterpret_cast<float*>(smem4);  // [kRows][d]
     float* sk = sq + kRows * p.d;                 // [kKeys][d]
@@ -65,7 +99,7 @@ __global__ void __launch_bounds__(kWarps * 32) attn_f32_kernel(const __grid_cons
         float v = 0.f;
         if (r < p.R) {
             const int g = r / T, t = r % T;
-            v = p.q[((static_cast<size_t>(b) * p.Hq + kvh * p.G + g) * T + t) * d + e];
+            v = widen(qg[((static_cast<size_t>(b) * p.Hq + kvh * p.G + g) * T + t) * d + e]);
         }
         sq[idx] = v;
     }
@@ -83,21 +117,24 @@ __global__ void __launch_bounds__(kWarps * 32) attn_f32_kernel(const __grid_cons
     for (int k0 = first; k0 < extent; k0 += kKeys) {
         __syncthreads();
         const int nk = min(kKeys, extent - k0);
-        for (int idx = threadIdx.x; idx < kKeys * d / 4; idx += blockDim.x) {
-            const int j = (idx * 4) / d;
-            float4 kv4 = make_float4(0.f, 0.f, 0.f, 0.f), vv4 = kv4;
+        for (int idx = threadIdx.x; idx < kKeys * d / kVec; idx += blockDim.x) {
+            const int j = (idx * kVec) / d;
+            bool live = false;
+            size_t off = 0;
             if (j < nk) {
                 const int a = k0 + j;  // key position
                 bool bad = false;
                 const int row = phys_row(p.pg, p.ring, p.Hkv, p.max_len, b, kvh, a, &bad);
-                if (!bad) {  // a bad block-table entry reads as zeros
-                    const size_t off = static_cast<size_t>(row) * d + static_cast<size_t>(idx * 4 - j * d);
-                    kv4 = *reinterpret_cast<const float4*>(p.k_cache + off);
-                    vv4 = *reinterpret_cast<const float4*>(p.v_cache + off);
-                }
+                live = !bad;  // a bad block-table entry reads as zeros
+                off = static_cast<size_t>(row) * d + static_cast<size_t>(idx * kVec - j * d);
             }
-            reinterpret_cast<float4*>(sk)[idx] = kv4;
-            reinterpret_cast<float4*>(sv)[idx] = vv4;
+            if (live) {
+                stage16(sk + idx * kVec, kg + off);
+                stage16(sv + idx * kVec, vg + off);
+            } else {
+#pragma unroll
+                for (int i = 0; i < kVec; ++i) sk[idx * kVec + i] = sv[idx * kVec + i] = 0.f;
+            }
         }
         __syncthreads();
 #pragma unroll
@@ -148,30 +185,35 @@ __global__ void __launch_bounds__(kWarps * 32) attn_f32_kernel(const __grid_cons
         const int r = row0 + warp + 4 * i;
         if (r >= p.R) continue;
         const int g = r / T, t = r % T;
-        float* dst = p.out + ((static_cast<size_t>(b) * p.Hq + kvh * p.G + g) * T + t) * d;
+        E* dst = og + ((static_cast<size_t>(b) * p.Hq + kvh * p.G + g) * T + t) * d;
         const float inv = (lim[i] >= 0 && l[i] > 0.f) ? 1.f / l[i] : 0.f;
 #pragma unroll
         for (int c = 0; c < kMaxD / 32; ++c) {
             const int e = lane + 32 * c;
-            if (e < d) dst[e] = (lim[i] >= 0) ? o[i][c] * inv : 0.f;
+            if (e < d) store_out(dst + e, (lim[i] >= 0) ? o[i][c] * inv : 0.f);
         }
     }
 }
 
-}  // namespace
-
-cudaError_t launch_attn_f32(const F32Params& p, cudaStream_t stream) {
+template <typename E>
+cudaError_t launch_generic(const F32Params& p, cudaStream_t stream) {
     const size_t smem = static_cast<size_t>(kRows + 2 * kKeys) * p.d * sizeof(float);
     static bool attr_set = false;
     if (!attr_set) {
-        cudaError_t e = cudaFuncSetAttribute(attn_f32_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+        cudaError_t e = cudaFuncSetAttribute(attn_f32_kernel<E>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                              static_cast<int>((kRows + 2 * kKeys) * kMaxD * sizeof(float)));
         if (e != cudaSuccess) return e;
         attr_set = true;
     }
     dim3 grid((p.R + kRows - 1) / kRows, p.Hkv, p.B);
-    attn_f32_kernel<<<grid, kWarps * 32, smem, stream>>>(p);
+    attn_f32_kernel<E><<<grid, kWarps * 32, smem, stream>>>(p);
     return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t launch_attn_f32(const F32Params& p, cudaStream_t stream) {
+    return p.bf16 ? launch_generic<__nv_bfloat16>(p, stream) : launch_generic<float>(p, stream);
 }
 
 }  // namespace kvc

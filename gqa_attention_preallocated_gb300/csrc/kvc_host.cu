@@ -69,6 +69,10 @@ namespace {
 constexpr int kTcMinRows = 12;
 constexpr int kTcMinRowsFp8 = 16;
 int tc_min_rows(const kvc_cache* c) { return c->dtype == KVC_FP8_E4M3 ? kTcMinRowsFp8 : kTcMinRows; }
+// Caches served by the generic kernel (attn_f32.cu): fp32 storage, and bf16
+// storage whose head dimension is not the 128 that the TMA / tensor-core
+// kernels are built for.
+bool generic_path(const kvc_cache* c) { return c->dtype == KVC_F32 || c->d != kHeadDimBf16; }
 constexpr int kTcMaxLen = 0xFFFF * 128;  // key tiles of a piece are packed in 16 bits
 
 thread_local std::string g_last_error;
@@ -221,7 +225,7 @@ kvc_status plan_shape(const kvc_cache* c, int Hq, int T, int num_ctas, AttnPlan*
     const long long R = static_cast<long long>(pl->G) * T;
     if (R > (1ll << 30)) return fail(KVC_ERR_ARG, "G * T too large");
     pl->R = static_cast<int>(R);
-    if (c->dtype != KVC_F32) {
+    if (!generic_path(c)) {
         pl->mt = pl->R <= 16 ? 1 : (pl->R <= 32 ? 2 : 4);
         pl->RPB = 16 * pl->mt;
         pl->RB = std::max(1, (pl->R + pl->RPB - 1) / pl->RPB);
@@ -331,13 +335,14 @@ kvc_status do_attention(kvc_cache* c, int layer, const void* q, const AttnPlan& 
     if (main_enqueued) *main_enqueued = false;
     const int64_t* lens = c->lens.data() + static_cast<size_t>(layer) * c->B;
     if (c->B == 0 || pl.T == 0) return ok();
-    if (c->dtype == KVC_F32) {
+    if (generic_path(c)) {
         static_assert(sizeof(F32Params) < 32000, "kernel parameter block too large");
         F32Params p;
-        p.q = static_cast<const float*>(q);
-        p.k_cache = static_cast<const float*>(c->k[layer]);
-        p.v_cache = static_cast<const float*>(c->v[layer]);
-        p.out = static_cast<float*>(out);
+        p.q = q;
+        p.k_cache = c->k[layer];
+        p.v_cache = c->v[layer];
+        p.out = out;
+        p.bf16 = c->dtype == KVC_BF16 ? 1 : 0;
         p.B = c->B;
         p.Hq = pl.Hq;
         p.Hkv = c->Hkv;
@@ -357,7 +362,7 @@ kvc_status do_attention(kvc_cache* c, int layer, const void* q, const AttnPlan& 
             p.n_new[b] = n_new[b];
         }
         cudaError_t e = launch_attn_f32(p, stream);
-        if (e != cudaSuccess) return cuda_fail(e, "attn_f32 launch");
+        if (e != cudaSuccess) return cuda_fail(e, "generic attention launch");
         ++c->launches;
         return ok();
     }
@@ -688,7 +693,7 @@ kvc_status do_attention(kvc_cache* c, int layer, const void* q, const AttnPlan& 
 }
 
 kvc_status check_workspace(const kvc_cache* c, const AttnPlan& pl, const void* ws, size_t ws_bytes) {
-    if (c->dtype == KVC_F32 || c->B == 0 || pl.T == 0) return ok();
+    if (generic_path(c) || c->B == 0 || pl.T == 0) return ok();
     if (!ws) return fail(KVC_ERR_WORKSPACE, "workspace is null (need %zu bytes)", pl.ws_total);
     if ((reinterpret_cast<uintptr_t>(ws) & 255u) != 0) return fail(KVC_ERR_WORKSPACE, "workspace not 256-byte aligned");
     if (ws_bytes < pl.ws_total)
@@ -715,7 +720,7 @@ kvc_status tree_masks(const kvc_cache* c, const AttnPlan& pl, const int32_t* n_n
         return fail(KVC_ERR_SHAPE, "B * T = %lld draft tokens exceed %d", static_cast<long long>(c->B) * pl.T,
                     kMaxTreeQueries);
     if (c->window > 0 || c->ring) return fail(KVC_ERR_ARG, "a draft tree does not combine with a window");
-    if (c->dtype != KVC_F32 && pl.R > 64)
+    if (!generic_path(c) && pl.R > 64)
         return fail(KVC_ERR_SHAPE, "a bf16 / fp8 draft tree takes G * T <= 64 query rows per KV head (G * T = %d)", pl.R);
     anc->assign(static_cast<size_t>(c->B) * pl.T, 0);
     for (int b = 0; b < c->B; ++b)
@@ -751,9 +756,9 @@ kvc_status kvc_create(kvc_cache** out, int layers, int batch, int kv_heads, int 
         return fail(KVC_ERR_ARG, "unknown dtype %d", static_cast<int>(dtype));
     const int esize = dtype == KVC_F32 ? 4 : (dtype == KVC_BF16 ? 2 : 1);
     if ((head_dim * esize) % 16 != 0) return fail(KVC_ERR_ARG, "head_dim * element size must be a multiple of 16");
-    if (dtype == KVC_F32 && head_dim > 256) return fail(KVC_ERR_ARG, "f32 path takes head_dim <= 256");
-    if (dtype != KVC_F32 && head_dim != kHeadDimBf16)
-        return fail(KVC_ERR_ARG, "bf16 and fp8 caches take head_dim = %d", kHeadDimBf16);
+    if (head_dim > 256) return fail(KVC_ERR_ARG, "head_dim %d > 256", head_dim);
+    if (dtype == KVC_FP8_E4M3 && head_dim != kHeadDimBf16)
+        return fail(KVC_ERR_ARG, "fp8 caches take head_dim = %d", kHeadDimBf16);
     if (dtype == KVC_FP8_E4M3 && kv_heads > kMaxScaleHeads)
         return fail(KVC_ERR_ARG, "fp8 caches take at most %d KV heads", kMaxScaleHeads);
     const long long rows = static_cast<long long>(batch) * kv_heads * max_len;
@@ -811,8 +816,9 @@ kvc_status kvc_create_paged(kvc_cache** out, int layers, int batch, int kv_heads
     if (page_size < 1 || num_pages < 1 || max_pages_per_row < 1)
         return fail(KVC_ERR_ARG, "bad paging: page_size=%d num_pages=%d max_pages_per_row=%d", page_size, num_pages,
                     max_pages_per_row);
-    if (dtype != KVC_F32 && page_size % 128 != 0)
-        return fail(KVC_ERR_ARG, "bf16 and fp8 pages hold a multiple of 128 tokens (key tiles never cross a page)");
+    if (dtype != KVC_F32 && head_dim == kHeadDimBf16 && page_size % 128 != 0)
+        return fail(KVC_ERR_ARG, "bf16 and fp8 pages of head_dim %d hold a multiple of 128 tokens (key tiles never cross a page)",
+                    kHeadDimBf16);
     if (batch > 0 && !block_table) return fail(KVC_ERR_ARG, "block_table is null");
     if ((reinterpret_cast<uintptr_t>(block_table) & 3u) != 0) return fail(KVC_ERR_ARG, "block_table not 4-byte aligned");
     const long long cap = static_cast<long long>(max_pages_per_row) * page_size;
@@ -850,7 +856,7 @@ kvc_status kvc_append(kvc_cache* c, int layer, const void* k_new, const void* v_
 
 size_t kvc_workspace_bytes(const kvc_cache* c, int q_heads, int T) {
     if (!c) return 0;
-    if (c->dtype == KVC_F32) return 0;
+    if (generic_path(c)) return 0;
     kvc_cache* mc = const_cast<kvc_cache*>(c);
     if (ensure_device(mc) != KVC_OK) return 0;
     AttnPlan pl;
@@ -869,7 +875,7 @@ static kvc_status gqa_attention_impl(kvc_cache* c, int layer, const void* q, int
     const int64_t* lens = c->lens.data() + static_cast<size_t>(layer) * c->B;
     s = validate_attention(c, layer, q, q_heads, T, n_new, out, lens, &pl, 0);
     if (s) return s;
-    if (c->dtype != KVC_F32 && c->B > 0 && T > 0) {
+    if (!generic_path(c) && c->B > 0 && T > 0) {
         s = ensure_device(c);
         if (s) return s;
         s = plan_shape(c, q_heads, T, c->num_sms, &pl);
@@ -904,7 +910,7 @@ static kvc_status append_attention_impl(kvc_cache* c, int layer, const void* q, 
     AttnPlan pl;
     s = validate_attention(c, layer, q, q_heads, T, n_new, out, after.data(), &pl, 0);
     if (s) return s;
-    if (c->dtype != KVC_F32 && c->B > 0 && T > 0) {
+    if (!generic_path(c) && c->B > 0 && T > 0) {
         s = ensure_device(c);
         if (s) return s;
         s = plan_shape(c, q_heads, T, c->num_sms, &pl);
@@ -925,7 +931,7 @@ static kvc_status append_attention_impl(kvc_cache* c, int layer, const void* q, 
     if (s) return s;
     cudaStream_t st = static_cast<cudaStream_t>(stream);
     int64_t* lw = c->lens.data() + static_cast<size_t>(layer) * c->B;
-    if (c->dtype != KVC_F32 && pl.mt == 1 && max_n > 0 && pl.R <= tc_min_rows(c)) {
+    if (!generic_path(c) && pl.mt == 1 && max_n > 0 && pl.R <= tc_min_rows(c)) {
         // Warps own whole tiles: the attention kernel writes the new rows into
         // the cache itself (one launch instead of two).
         for (int b = 0; b < c->B; ++b) lw[b] += n_new[b];
@@ -1087,7 +1093,7 @@ kvc_status kvc_set_window(kvc_cache* c, int window, int ring) {
     if (ring) {
         if (c->pg.table) return fail(KVC_ERR_ARG, "a paged cache cannot also be a ring");
         if (window < 1 || window > c->max_len) return fail(KVC_ERR_ARG, "a ring cache needs a window of 1..max_len");
-        if (c->dtype != KVC_F32 && c->max_len % 128 != 0)
+        if (!generic_path(c) && c->max_len % 128 != 0)
             return fail(KVC_ERR_ARG, "a bf16 ring cache needs max_len %% 128 == 0 (key tiles never wrap)");
     }
     if ((ring != 0) != c->ring)
@@ -1149,7 +1155,8 @@ kvc_status kvc_decode_step(kvc_cache* c, int layer, const void* q, const void* k
     kvc_status s = check_layer(c, layer);
     if (s) return s;
     if (!c->lens_on_device) return fail(KVC_ERR_ARG, "the lengths are on the host: call kvc_lens_to_device first");
-    if (c->dtype == KVC_F32) return fail(KVC_ERR_ARG, "device-resident steps serve bf16 and fp8 caches only");
+    if (generic_path(c))
+        return fail(KVC_ERR_ARG, "device-resident steps serve bf16 and fp8 caches of head_dim %d only", kHeadDimBf16);
     if (c->B == 0 || T == 0) return ok();
     if (T < 0) return fail(KVC_ERR_ARG, "T = %d < 0", T);
     if (!q || !k_new || !v_new || !out || !n_new_dev) return fail(KVC_ERR_ARG, "null pointer argument");
@@ -1307,7 +1314,9 @@ extern "C" kvc_status kvc_gqa_attention_noalloc(kvc_cache* c, int layer, const v
     if (s0) return s0;
     kvc_status s = check_layer(c, layer);
     if (s) return s;
-    if (c->dtype == KVC_F32) return fail(KVC_ERR_ARG, "the allocation-free variant serves bf16 and fp8 caches only");
+    if (generic_path(c))
+        return fail(KVC_ERR_ARG, "the allocation-free variant serves bf16 and fp8 caches of head_dim %d only",
+                    kHeadDimBf16);
     AttnPlan pl;
     const int64_t* lens = c->lens.data() + static_cast<size_t>(layer) * c->B;
     s = validate_attention(c, layer, q, q_heads, T, n_new, out, lens, &pl, 0);

@@ -180,10 +180,12 @@ cudaError_t launch_decode_bf16(const DecodeParams& p, const CUtensorMap& tmK, co
 // all keys of the unit, output written directly; no workspace.
 // ---------------------------------------------------------------------------
 struct F32Params {
-    const float* q;
-    const float* k_cache;
-    const float* v_cache;
-    float* out;
+    // Stored values, queries and outputs are fp32, or bf16 when bf16 is set.
+    const void* q;
+    const void* k_cache;
+    const void* v_cache;
+    void* out;
+    int bf16;
     int B, Hq, Hkv, G, T, max_len, d;
     int R;
     int window, ring;  // sliding window (0 = none) and ring storage, as in DecodeParams

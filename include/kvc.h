@@ -27,8 +27,11 @@
  *   k_new, v_new              [B, Hkv, T, d]
  *   q, out                    [B, Hq, T, d]
  * All device pointers must be 16-byte aligned.  d * sizeof(element) must be a
- * multiple of 16.  The bf16 attention path takes d = 128 (the other sizes of
- * d are served by the f32 path only).
+ * multiple of 16, and d <= 256.  bf16 caches of d = 128 and all FP8 caches
+ * (d = 128 only) run on the TMA / tensor-core kernels.  fp32 caches and bf16
+ * caches of any other d run on a generic kernel.  That kernel widens the
+ * stored values to fp32 and has no workspace, fused append, device-resident
+ * steps or allocation-free entry point.
  *
  * Ownership.  The caller allocates every device buffer (cache, inputs,
  * outputs, workspace) and keeps it alive while the handle or a launched call
@@ -90,8 +93,8 @@ typedef struct kvc_cache kvc_cache;
  * No CUDA call is made here; device state (tensor-map descriptors, SM
  * count) is set up on the first launch.
  * Errors: KVC_ERR_ARG for non-positive sizes, B > KVC_MAX_BATCH, null or
- * misaligned buffers, or d * element size not a multiple of 16; bf16 and
- * FP8 caches take d = 128, FP8 caches at most 64 KV heads. */
+ * misaligned buffers, d * element size not a multiple of 16, or d > 256;
+ * FP8 caches take d = 128 and at most 64 KV heads. */
 kvc_status kvc_create(kvc_cache** out, int layers, int batch, int kv_heads, int max_len, int head_dim,
                       kvc_dtype dtype, void* const* k_bufs, void* const* v_bufs);
 
@@ -122,8 +125,8 @@ kvc_status kvc_set_kv_scales(kvc_cache* c, int layer, const float* k_scale, cons
  * (0 .. num_pages - 1) and may change the table between calls (stream-ordered).
  * A bad entry is never dereferenced: appended rows aimed at it are not
  * written, and reads take page 0 and set the workspace error word (the next
- * kvc_device_status reports it); the fp32 path reads it as zeros.  bf16
- * needs page_size % 128 == 0.  Paged storage does not combine with ring
+ * kvc_device_status reports it); the generic kernel (fp32, bf16 of d != 128)
+ * reads it as zeros.  bf16 and FP8 caches of d = 128 need page_size % 128 == 0.  Paged storage does not combine with ring
  * storage (kvc_set_window ring = 1).  Errors: as kvc_create, and KVC_ERR_ARG
  * for bad paging arguments. */
 kvc_status kvc_create_paged(kvc_cache** out, int layers, int batch, int kv_heads, int page_size, int num_pages,
@@ -142,7 +145,8 @@ kvc_status kvc_append(kvc_cache* c, int layer, const void* k_new, const void* v_
 
 /* Bytes of device workspace kvc_gqa_attention needs for this handle, q_heads
  * and T (an error word and the split-KV partial results).
- * 0 means no workspace is needed (f32 path).  Returns 0 for invalid input. */
+ * 0 means no workspace is needed (the generic kernel: fp32 caches, bf16 of
+ * d != 128).  Returns 0 for invalid input. */
 size_t kvc_workspace_bytes(const kvc_cache* c, int q_heads, int T);
 
 /* Attention of the chunk just appended ("A strong answer", gqa_attention):
@@ -199,7 +203,7 @@ kvc_status kvc_append_attention_tree(kvc_cache* c, int layer, const void* q, con
  * a latency-critical loop that must not pay cudaMalloc's cost and implicit
  * synchronization.  The pages have no counterpart of this entry point; it
  * computes exactly what kvc_gqa_attention computes (same kernel, same
- * result) and serves bf16 and FP8 caches.
+ * result) and serves bf16 and FP8 caches of d = 128.
  *
  * Its scratch is one static device array of KVC_NOALLOC_SCRATCH_BYTES
  * (32 MiB) inside the library: every GPU that loads the library holds it
@@ -235,8 +239,8 @@ kvc_status kvc_gqa_attention_noalloc(kvc_cache* c, int layer, const void* q, int
  * chunk's first query still finds its window; else KVC_ERR_OVERFLOW), and
  * kvc_truncate may only go back to a length n whose window keys
  * n - window + 1 .. n - 1 are still stored (or to 0).
- * Requirements: ring needs 1 <= window <= max_len and, for bf16 caches,
- * max_len % 128 == 0; ring storage changes only while every length is 0.
+ * Requirements: ring needs 1 <= window <= max_len and, for bf16 and FP8
+ * caches of d = 128, max_len % 128 == 0; ring storage changes only while every length is 0.
  * Applies to every layer and to every later call (including
  * kvc_decode_step).  Host only.  KVC_ERR_ARG otherwise. */
 kvc_status kvc_set_window(kvc_cache* c, int window, int ring);
@@ -311,7 +315,8 @@ kvc_status kvc_lens_from_device(kvc_cache* c, void* stream);
  * n_new[b] rows of k_new / v_new [B, Hkv, T, d] at row b's device length, then
  * the T queries q [B, Hq, T, d] attend exactly as in kvc_gqa_attention, and
  * the device lengths advance by n_new.  n_new is a device int32 [B].  bf16
- * caches with G * T <= 16 query rows per KV head (decode and short verify).
+ * and FP8 caches of d = 128 with G * T <= 16 query rows per KV head (decode
+ * and short verify).
  * Three kernels are enqueued (device plan, attention with the append fused
  * in, combine), with nothing read from the host that changes per step, so
  * the call can be captured in a CUDA graph and replayed with new contents of

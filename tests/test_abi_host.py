@@ -77,7 +77,8 @@ def test_create_validation(L):
     k, v = _fake_buffers(1)
     assert L.kvc_create(ctypes.byref(h), 0, 2, 2, 8, 16, 0, k, v) == 1
     assert L.kvc_create(ctypes.byref(h), 1, 2, 2, 8, 6, 0, k, v) == 1  # 6 * 4 B not a multiple of 16
-    assert L.kvc_create(ctypes.byref(h), 1, 2, 2, 8, 64, 1, k, v) == 1  # bf16 path takes d = 128
+    assert L.kvc_create(ctypes.byref(h), 1, 2, 2, 8, 12, 1, k, v) == 1  # 12 * 2 B not a multiple of 16
+    assert L.kvc_create(ctypes.byref(h), 1, 2, 2, 8, 264, 1, k, v) == 1  # d <= 256
     assert L.kvc_create(ctypes.byref(h), 1, _lib.KVC_MAX_BATCH + 1, 2, 8, 16, 0, k, v) == 1
     bad = (ctypes.c_void_p * 1)(12345)  # misaligned
     assert L.kvc_create(ctypes.byref(h), 1, 2, 2, 8, 16, 0, bad, v) == 1
@@ -187,6 +188,13 @@ def test_workspace_query_without_gpu_or_for_f32(L):
     assert L.kvc_workspace_bytes(h, 4, 1) == 0  # the f32 path needs no workspace
     L.kvc_destroy(h)
     assert L.kvc_workspace_bytes(None, 4, 1) == 0
+    st, h = _create(L, d=64, dtype=_lib.KVC_BF16)  # bf16 of d != 128: the generic kernel
+    assert st == 0
+    assert L.kvc_workspace_bytes(h, 4, 1) == 0
+    _, n = _i32(3, 0)
+    assert L.kvc_gqa_attention_noalloc(h, 0, None, 4, 1, n, None, None) == 1
+    assert b"head_dim 128" in L.kvc_last_error()
+    L.kvc_destroy(h)
 
 
 def test_device_lens_calls_without_device_state(L):
@@ -242,6 +250,9 @@ def test_paged_host_rules(L):
     assert _create_paged(L, table=0)[0] == 1          # no block table
     assert _create_paged(L, table=(1 << 42) + 2)[0] == 1  # misaligned table
     assert _create_paged(L, page=64, d=128, dtype=_lib.KVC_BF16)[0] == 1  # bf16 pages: multiples of 128
+    st, h = _create_paged(L, page=16, d=64, dtype=_lib.KVC_BF16)  # off the TMA path any page size works
+    assert st == 0
+    L.kvc_destroy(h)
     st, h = _create_paged(L, page=128, d=128, dtype=_lib.KVC_BF16)
     assert st == 0
     L.kvc_destroy(h)
