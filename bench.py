@@ -169,8 +169,9 @@ def step_inputs(shape, Hq, T, n_distinct, seed, device="cuda"):
 class Workload:
     """One named workload: set-up, one step, and the step's algorithmic work."""
 
-    def __init__(self, name, seed=0, verify_t=4, verify_g=4, kv_dtype="bf16"):
+    def __init__(self, name, seed=0, verify_t=4, verify_g=4, kv_dtype="bf16", prefill_ragged=False):
         self.name = name
+        self.ragged = False
         self.seed = seed
         self.kv_dtype = kv_dtype  # "bf16", or "fp8": E4M3 cache with one scale per KV head
         self.esize = 1 if kv_dtype == "fp8" else 2
@@ -194,6 +195,9 @@ class Workload:
             self.layers, self.Hq, self.T = 1, s.Hq, 512
             self.lens0 = wl.prefill_priors(seed, s.B)
             self.n_new = np.full(s.B, 512, dtype=np.int64)
+            if prefill_ragged:  # the ragged final chunk: T = 512 padded, n_new[b] uniform in 1..512
+                self.ragged = True
+                self.n_new = wl.ragged_chunk(seed, s.B)
             self.rollback_every = 1
             self.metric, self.unit = "GQA chunked-prefill attention TFLOP/s", "TFLOP/s"
         elif name == "longctx":
@@ -208,7 +212,9 @@ class Workload:
 
     def config(self):
         s = self.shape
-        return {"workload": s.name + ("_fp8_cache" if self.kv_dtype == "fp8" else ""), "B": s.B, "Hq": self.Hq,
+        name = s.name + ("_ragged_final_chunk" if self.ragged else "") + ("_fp8_cache" if self.kv_dtype == "fp8" else "")
+        extra = {"n_new": [int(x) for x in self.n_new]} if self.ragged else {}
+        return {"workload": name, **extra, "B": s.B, "Hq": self.Hq,
                 "Hkv": s.Hkv, "d": s.d, "max_len": s.max_len,
                 "layers": self.layers, "T": self.T, "dtype": "bf16",
                 "kv_storage": "fp8_e4m3 (one scale per KV head)" if self.kv_dtype == "fp8" else "bf16",
@@ -515,12 +521,15 @@ def main():
                     help="query heads per KV head, Hq = G * 8 (verify workload)")
     ap.add_argument("--kv-dtype", choices=["bf16", "fp8"], default="bf16",
                     help="cache storage: bf16, or FP8 E4M3 with one scale per KV head")
+    ap.add_argument("--prefill-ragged", action="store_true",
+                    help="prefill workload: the ragged final chunk (n_new[b] uniform in 1..512) on the same priors")
     args = ap.parse_args()
 
     world = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
     local = int(os.environ.get("LOCAL_RANK", "0"))
-    w = Workload(args.workload, verify_t=args.verify_t, verify_g=args.verify_g, kv_dtype=args.kv_dtype)
+    w = Workload(args.workload, verify_t=args.verify_t, verify_g=args.verify_g, kv_dtype=args.kv_dtype,
+                 prefill_ragged=args.prefill_ragged)
     scale = 1e-12 if w.unit == "TFLOP/s" else 1e-9
 
     if args.impl == "reference":
@@ -530,7 +539,8 @@ def main():
         line = {"metric": w.metric, "value": value, "unit": w.unit, "n_gpus": args.gpus, "steps": args.steps,
                 "warmup": args.warmup, "higher_is_better": True, "impl": "reference", "dtype": "f64",
                 "data": "synthetic", "config": w.config(),
-                "cpu_baseline": {"value": value, "unit": w.unit, "cores": 1, "kind": "oracle", "sample": sample},
+                "cpu_baseline": {"value": value, "unit": w.unit, "cores": 1, "kind": "oracle", "sample": sample,
+                                 "host_cpus": os.cpu_count(), "blas_threads": 1},
                 "e2e": {"value": value, "unit": w.unit, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
                 "vs_baseline": None}
         print(json.dumps(line))
@@ -586,7 +596,8 @@ def main():
                                 "device_status": gr["status"]}
     if rank == 0 and not args.no_cpu_baseline:
         cv, sample, _ = run_oracle_sample(w)
-        line["cpu_baseline"] = {"value": cv, "unit": w.unit, "cores": 1, "kind": "oracle", "sample": sample}
+        line["cpu_baseline"] = {"value": cv, "unit": w.unit, "cores": 1, "kind": "oracle", "sample": sample,
+                                 "host_cpus": os.cpu_count(), "blas_threads": 1}
     if rank == 0:
         print(json.dumps(line))
     if world > 1:
@@ -615,7 +626,8 @@ def _committed_traffic(w: Workload, mean_kernel_bytes: float):
     """
     import hashlib
 
-    path = os.path.join(ROOT, "profiles", f"traffic_{w.name}{'_fp8' if w.kv_dtype == 'fp8' else ''}.txt")
+    tag = ("_ragged" if w.ragged else "") + ("_fp8" if w.kv_dtype == "fp8" else "")
+    path = os.path.join(ROOT, "profiles", f"traffic_{w.name}{tag}.txt")
     if not os.path.exists(path):
         return None
     kv = dict(line.strip().split("=", 1) for line in open(path) if "=" in line and not line.startswith("#"))

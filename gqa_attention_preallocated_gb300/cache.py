@@ -143,12 +143,16 @@ class KVCache:
         return int(lib().kvc_workspace_bytes(self._h, q_heads, T))
 
     def workspace(self, q_heads: int, T: int) -> torch.Tensor | None:
-        """A workspace buffer owned by this cache, grown as needed (reused across calls)."""
+        """A workspace buffer owned by this cache, grown as needed (reused across calls).
+
+        Allocated zeroed, so its error word reads clean (device_status) even
+        before a call has used it.
+        """
         need = self.workspace_bytes(q_heads, T)
         if need == 0:
             return None
         if self._ws is None or self._ws.numel() < need:
-            self._ws = torch.empty(need, dtype=torch.uint8, device=self.device)
+            self._ws = torch.zeros(need, dtype=torch.uint8, device=self.device)
         return self._ws
 
     def _check_tensor(self, t: torch.Tensor, shape, name: str) -> None:

@@ -275,7 +275,9 @@ kvc_status kvc_length(const kvc_cache* c, int64_t* out);
  * when *code != 0, KVC_ERR_OVERFLOW when the code records a rejected
  * device-resident step (kvc_decode_step), or KVC_ERR_ARG when a kernel met a
  * block-table entry outside 0 .. num_pages - 1 (kvc_create_paged; nothing was
- * read from or written to it, and that call's output is not valid). */
+ * read from or written to it, and that call's output is not valid).
+ * A workspace that no call has used yet holds no status: its word is
+ * whatever the buffer held (zero it, or make a call with it first). */
 kvc_status kvc_device_status(kvc_cache* c, void* workspace, void* stream, int32_t* code);
 
 /* Self-test of the kernels' bounded waits: launches one CTA that waits on an
