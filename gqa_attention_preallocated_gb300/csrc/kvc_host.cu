@@ -19,6 +19,7 @@
 #include <string.h>
 
 #include <algorithm>
+#include <atomic>
 #include <mutex>
 #include <queue>
 #include <string>
@@ -113,11 +114,23 @@ EncodeTiledFn encode_fn() {
     return fn;
 }
 
+// The device this process's handles run on: the kernels' shared-memory
+// attributes are set once, for the first device that launches them.
+std::atomic<int> g_device{-1};
+
+// Bind the handle to the current device on its first launch; afterwards every
+// launching call must find that device current (its buffers live there).
 kvc_status ensure_device(kvc_cache* c) {
-    if (c->dev_ready) return ok();
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return cuda_fail(e, "cudaGetDevice");
+    if (c->dev_ready) {
+        if (dev != c->device) return fail(KVC_ERR_ARG, "current device %d is not the cache's device %d", dev, c->device);
+        return ok();
+    }
+    int bound = -1;
+    if (!g_device.compare_exchange_strong(bound, dev) && bound != dev)
+        return fail(KVC_ERR_ARG, "the library serves one device per process (device %d; current device %d)", bound, dev);
     int sms = 0;
     e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
     if (e != cudaSuccess) return cuda_fail(e, "cudaDeviceGetAttribute");

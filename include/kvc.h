@@ -33,6 +33,11 @@
  * stored values to fp32 and has no workspace, fused append, device-resident
  * steps or allocation-free entry point.
  *
+ * Device.  One process drives one GPU through this library: a handle binds
+ * to the device current at its first launching call, every later launching
+ * call must find that device current, and handles of a second device in the
+ * same process are refused (KVC_ERR_ARG).  Run one process per GPU.
+ *
  * Ownership.  The caller allocates every device buffer (cache, inputs,
  * outputs, workspace) and keeps it alive while the handle or a launched call
  * uses it.  The handle owns only host state: per-layer, per-row lengths and
