@@ -38,6 +38,10 @@
  * call must find that device current, and handles of a second device in the
  * same process are refused (KVC_ERR_ARG).  Run one process per GPU.
  *
+ * Threads.  A handle holds host state (lengths, descriptors) without a lock:
+ * calls on one handle must not overlap in time.  Different handles may be
+ * used from different threads.
+ *
  * Ownership.  The caller allocates every device buffer (cache, inputs,
  * outputs, workspace) and keeps it alive while the handle or a launched call
  * uses it.  The handle owns only host state: per-layer, per-row lengths and
