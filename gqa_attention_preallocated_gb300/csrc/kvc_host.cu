@@ -242,7 +242,12 @@ kvc_status plan_shape(const kvc_cache* c, int Hq, int T, int num_ctas, AttnPlan*
         pl->mt = pl->R <= 16 ? 1 : (pl->R <= 32 ? 2 : 4);
         pl->RPB = 16 * pl->mt;
         pl->RB = std::max(1, (pl->R + pl->RPB - 1) / pl->RPB);
-        const long long NB = static_cast<long long>(c->B) * pl->RB;
+        // Only the split-KV kernel works in (row, row block) groups.  A call
+        // with more than 64 rows per KV head (more than any tree call takes)
+        // always runs on the tensor cores, unless the cache is too long for
+        // them; it plans no groups and needs no split-KV partials.
+        const bool tc_only = pl->R > 64 && c->max_len <= kTcMaxLen;
+        const long long NB = tc_only ? 0 : static_cast<long long>(c->B) * pl->RB;
         if (NB > kMaxGroups)
             return fail(KVC_ERR_ARG, "B * ceil(G*T / %d) = %lld exceeds %d row blocks", pl->RPB, NB, kMaxGroups);
         pl->NB = static_cast<int>(NB);
@@ -256,8 +261,9 @@ kvc_status plan_shape(const kvc_cache* c, int Hq, int T, int num_ctas, AttnPlan*
         pl->ws_plan = round_up(sizeof(DevicePlan), 256) + round_up(kMaxTreeQueries * sizeof(uint64_t), 256);
         pl->ways = decode_launch_shape(pl->mt, c->dtype == KVC_FP8_E4M3).ways;
         pl->part_rows = std::min(pl->R, pl->RPB);
-        pl->ws_partials = static_cast<size_t>(pl->units + num_ctas) * pl->ways * pl->part_rows *
-                          (kHeadDimBf16 + 4) * sizeof(float);
+        pl->ws_partials = tc_only ? 0
+                                  : static_cast<size_t>(pl->units + num_ctas) * pl->ways * pl->part_rows *
+                                        (kHeadDimBf16 + 4) * sizeof(float);
         pl->ws_min = pl->ws_err + pl->ws_plan + pl->ws_partials;
         if (pl->R > tc_min_rows(c)) {
             // The tensor-core kernel: up to two partial slots (2 row tiles x

@@ -131,6 +131,34 @@ def test_bf16_many_short_units_sole_path():
     _run_calls(7, B, Hkv, G, 128, 256, torch.bfloat16, calls)
 
 
+def test_bf16_maximum_batch():
+    """KVC_MAX_BATCH rows, every output compared.  Calls:
+    - a prefill chunk of up to 120 tokens: 480 packed rows per KV head, tensor cores;
+    - decode steps: the split-KV kernel at its limit of 1024 (row, row block) groups;
+    - verify chunks of 4 and 8: one packed tensor-core tile.
+    Some rows take zero tokens."""
+    B, Hkv, G, d, max_len = 1024, 1, 4, 128, 160
+    rng = np.random.default_rng(1024)
+    calls = [rng.integers(1, 121, size=B)]
+    calls[0][0] = 120
+    for T in (1, 1, 4, 8):
+        n = rng.integers(0, T + 1, size=B)
+        n[0] = T
+        calls.append(n)
+    _run_calls(13, B, Hkv, G, d, max_len, torch.bfloat16, calls)
+
+
+@pytest.mark.parametrize("dtype,d", [(torch.float32, 16), (torch.bfloat16, 64)])
+def test_generic_kernel_maximum_batch(dtype, d):
+    """KVC_MAX_BATCH rows on the generic kernel: ragged chunks, then decode."""
+    B, Hkv, G, max_len = 1024, 2, 2, 64
+    rng = np.random.default_rng(d)
+    calls = [rng.integers(0, 41, size=B), rng.integers(0, 2, size=B), rng.integers(0, 6, size=B)]
+    for c in calls:
+        c[0] = c.max()
+    _run_calls(17, B, Hkv, G, d, max_len, dtype, calls)
+
+
 def test_incremental_equals_full_on_gpu():
     """S = 37, T = 5: the chunked GPU output matches the full-sequence GPU output's last rows."""
     _cuda_or_skip()
