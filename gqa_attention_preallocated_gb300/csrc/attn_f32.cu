@@ -15,9 +15,10 @@
 // One CTA serves a block of 16 query rows r = g*T + t of one KV head, so the
 // K/V tile it stages in shared memory is read once for up to 16 query rows
 // (all G heads of the group when G*T <= 16).  Each warp owns 4 rows; lane j
-// scores key j of the 32-key tile, the warp keeps a running max and sum
-// (online softmax) and lane e accumulates output dims e, e+32, ...  Masked
-// keys are skipped outright, so stale or NaN slots past lens never enter.
+// scores keys j and j + 32 of the 64-key tile, the warp keeps a running max
+// and sum (online softmax) and lane e accumulates output dims e, e+32, ...
+// Masked keys are skipped outright, so stale or NaN slots past lens never
+// enter.
 //
 // Sliding window and ring storage ("Write the causal mask for a decode
 // step...", "A strong answer", last paragraph): with a window W the query at
@@ -36,7 +37,7 @@ namespace kvc {
 namespace {
 
 constexpr int kRows = 16;
-constexpr int kKeys = 32;
+constexpr int kKeys = 64;  // key tile: two keys a lane
 constexpr int kWarps = 4;
 constexpr int kMaxD = 256;
 
@@ -62,6 +63,24 @@ __device__ __forceinline__ void stage16(float* dst, const __nv_bfloat16* src) {
     reinterpret_cast<float4*>(dst)[1] = make_float4(f[4], f[5], f[6], f[7]);
 }
 
+// The same into a row of any alignment (one value a store).
+__device__ __forceinline__ void stage16_rows(float* dst, const float* src) {
+    const float4 v = *reinterpret_cast<const float4*>(src);
+    dst[0] = v.x;
+    dst[1] = v.y;
+    dst[2] = v.z;
+    dst[3] = v.w;
+}
+__device__ __forceinline__ void stage16_rows(float* dst, const __nv_bfloat16* src) {
+    const uint4 w = *reinterpret_cast<const uint4*>(src);
+    const uint32_t u[4] = {w.x, w.y, w.z, w.w};
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        dst[2 * i] = __uint_as_float(u[i] << 16);
+        dst[2 * i + 1] = __uint_as_float(u[i] & 0xffff0000u);
+    }
+}
+
 template <typename E>
 __global__ void __launch_bounds__(kWarps * 32) attn_f32_kernel(const __grid_constant__ F32Params p) {
     constexpr int kVec = 16 / static_cast<int>(sizeof(E));  // values per 16-byte load
@@ -71,8 +90,11 @@ __global__ void __launch_bounds__(kWarps * 32) attn_f32_kernel(const __grid_cons
     E* og = static_cast<E*>(p.out);
     extern __shared__ float4 smem4[];
     float* sq = reinterpret_cast<float*>(smem4);  // [kRows][d]
-    float* sk = sq + kRows * p.d;                 // [kKeys][d]
-    float* sv = sk + kKeys * p.d;                 // [kKeys][d]
+    // K rows are d + 1 floats apart: lane j reads key j's row in the score
+    // loop, and an odd stride puts the 32 lanes in 32 different banks.
+    const int dk = p.d + 1;
+    float* sk = sq + kRows * p.d;                 // [kKeys][d + 1]
+    float* sv = sk + kKeys * dk;                  // [kKeys][d] (16-byte aligned: 80 d + 64 floats in)
 
     const int b = blockIdx.z, kvh = blockIdx.y, row0 = blockIdx.x * kRows;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -128,12 +150,13 @@ __global__ void __launch_bounds__(kWarps * 32) attn_f32_kernel(const __grid_cons
                 live = !bad;  // a bad block-table entry reads as zeros
                 off = static_cast<size_t>(row) * d + static_cast<size_t>(idx * kVec - j * d);
             }
+            float* kdst = sk + j * dk + (idx * kVec - j * d);
             if (live) {
-                stage16(sk + idx * kVec, kg + off);
+                stage16_rows(kdst, kg + off);
                 stage16(sv + idx * kVec, vg + off);
             } else {
 #pragma unroll
-                for (int i = 0; i < kVec; ++i) sk[idx * kVec + i] = sv[idx * kVec + i] = 0.f;
+                for (int i = 0; i < kVec; ++i) kdst[i] = sv[idx * kVec + i] = 0.f;
             }
         }
         __syncthreads();
@@ -143,24 +166,38 @@ __global__ void __launch_bounds__(kWarps * 32) attn_f32_kernel(const __grid_cons
             const int lo = p.window > 0 ? li - p.window : -1;  // keys <= lo are outside the window
             if (li < k0 || lo >= k0 + nk - 1) continue;  // row sees nothing in this tile (warp-uniform)
             const float* qr = sq + (warp + 4 * i) * d;
-            const int key = k0 + lane;
-            float s = -INFINITY;
-            // (key - prior <= li - prior < T <= 64 whenever the bit is read)
-            const bool on_path =
-                !p.tree || key < prior || key > li || ((p.anc[b * T + (li - prior)] >> (key - prior)) & 1ull);
-            if (lane < nk && key <= li && key > lo && on_path) {
-                float acc = 0.f;
-                const float* kr = sk + lane * d;
-                for (int e = 0; e < d; ++e) acc = fmaf(qr[e], kr[e], acc);
-                s = acc * p.scale;
+            // lane scores keys k0 + lane and k0 + lane + 32
+            float sc[2];
+#pragma unroll
+            for (int h = 0; h < 2; ++h) {
+                const int jj = lane + 32 * h, key = k0 + jj;
+                sc[h] = -INFINITY;
+                // (key - prior <= li - prior < T <= 64 whenever the bit is read)
+                const bool on_path =
+                    !p.tree || key < prior || key > li || ((p.anc[b * T + (li - prior)] >> (key - prior)) & 1ull);
+                if (jj < nk && key <= li && key > lo && on_path) {
+                    // four independent partial sums (d is a multiple of 4)
+                    float a0 = 0.f, a1 = 0.f, a2 = 0.f, a3 = 0.f;
+                    const float* kr = sk + jj * dk;
+                    for (int e = 0; e < d; e += 4) {
+                        a0 = fmaf(qr[e], kr[e], a0);
+                        a1 = fmaf(qr[e + 1], kr[e + 1], a1);
+                        a2 = fmaf(qr[e + 2], kr[e + 2], a2);
+                        a3 = fmaf(qr[e + 3], kr[e + 3], a3);
+                    }
+                    sc[h] = ((a0 + a1) + (a2 + a3)) * p.scale;
+                }
             }
-            float tmax = s;
+            float tmax = fmaxf(sc[0], sc[1]);
 #pragma unroll
             for (int off = 16; off > 0; off >>= 1) tmax = fmaxf(tmax, __shfl_xor_sync(0xffffffffu, tmax, off));
-            const float mnew = fmaxf(m[i], tmax);  // finite: key k0 <= li is visible
-            const float alpha = expf(m[i] - mnew);
-            const float pj = (s == -INFINITY) ? 0.f : expf(s - mnew);
-            float psum = pj;
+            // A draft tree can leave a row no visible key in a tile (and none
+            // before it): then nothing changes.
+            const float mnew = fmaxf(m[i], tmax);
+            const float alpha = (mnew == -INFINITY) ? 1.f : expf(m[i] - mnew);
+            const float p0 = (sc[0] == -INFINITY) ? 0.f : expf(sc[0] - mnew);
+            const float p1 = (sc[1] == -INFINITY) ? 0.f : expf(sc[1] - mnew);
+            float psum = p0 + p1;
 #pragma unroll
             for (int off = 16; off > 0; off >>= 1) psum += __shfl_xor_sync(0xffffffffu, psum, off);
             l[i] = l[i] * alpha + psum;
@@ -169,7 +206,7 @@ __global__ void __launch_bounds__(kWarps * 32) attn_f32_kernel(const __grid_cons
             for (int c = 0; c < kMaxD / 32; ++c) o[i][c] *= alpha;
             const int jmax = min(nk, li - k0 + 1);
             for (int j = max(0, lo - k0 + 1); j < jmax; ++j) {
-                const float pb = __shfl_sync(0xffffffffu, pj, j);
+                const float pb = __shfl_sync(0xffffffffu, j < 32 ? p0 : p1, j & 31);
                 const float* vr = sv + j * d;
 #pragma unroll
                 for (int c = 0; c < kMaxD / 32; ++c) {
@@ -197,11 +234,11 @@ __global__ void __launch_bounds__(kWarps * 32) attn_f32_kernel(const __grid_cons
 
 template <typename E>
 cudaError_t launch_generic(const F32Params& p, cudaStream_t stream) {
-    const size_t smem = static_cast<size_t>(kRows + 2 * kKeys) * p.d * sizeof(float);
+    const size_t smem = (static_cast<size_t>(kRows + 2 * kKeys) * p.d + kKeys) * sizeof(float);
     static bool attr_set = false;
     if (!attr_set) {
         cudaError_t e = cudaFuncSetAttribute(attn_f32_kernel<E>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                             static_cast<int>((kRows + 2 * kKeys) * kMaxD * sizeof(float)));
+                                             static_cast<int>(((kRows + 2 * kKeys) * kMaxD + kKeys) * sizeof(float)));
         if (e != cudaSuccess) return e;
         attr_set = true;
     }

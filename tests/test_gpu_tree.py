@@ -106,3 +106,31 @@ def test_tree_rejections():
                                  [[-1, 0]])
     assert e.value.status == 1
     assert list(c2.lens(0)) == [0]  # nothing appended
+
+
+@pytest.mark.parametrize("dtype,d", [(torch.float32, 16), (torch.bfloat16, 64), (torch.bfloat16, 128)])
+@pytest.mark.parametrize("T", [48, 64])
+def test_star_trees_on_an_empty_prefix(dtype, d, T):
+    """Every draft hangs off an empty prefix: query t sees its own token only,
+    so key tiles before it hold no visible key for it (and nothing came
+    before).  The outputs are the queries' own V rows."""
+    _cuda_or_skip()
+    B, Hkv, G = 2, 1, 1
+    cache = KVCache(1, B, Hkv, T + 8, d, dtype=dtype)
+    cache.k[0].fill_(float("nan"))
+    cache.v[0].fill_(float("nan"))
+    orc = ref.OracleCache(1, B, Hkv, T + 8, d)
+    n_new = np.array([T, T - 5])
+    parents = np.full((B, T), -1)
+    k = wl.to_storage(wl.normal(9, 1, (B, Hkv, T, d)), dtype)
+    v = wl.to_storage(wl.normal(9, 2, (B, Hkv, T, d)), dtype)
+    q = wl.to_storage(wl.normal(9, 3, (B, Hkv * G, T, d)), dtype)
+    out = cache.append_attention_tree(0, q.cuda(), k.cuda(), v.cuda(), n_new, parents)
+    want = ref.append_attention(orc, 0, q.double().numpy(), k.double().numpy(), v.double().numpy(), n_new,
+                                parents=parents)
+    got = out.double().cpu().numpy()
+    assert np.all(np.isfinite(got))
+    assert float(np.max(np.abs(got - want))) <= TOL[dtype]
+    for b in range(B):  # a single visible key: the output is that key's V row
+        assert np.allclose(want[b, :, :n_new[b]], v.double().numpy()[b, :, :n_new[b]], atol=1e-12)
+    assert cache.device_status() == 0
