@@ -96,7 +96,8 @@ __global__ void __launch_bounds__(kWarps * 32) attn_f32_kernel(const __grid_cons
     float* sk = sq + kRows * p.d;                 // [kKeys][d + 1]
     float* sv = sk + kKeys * dk;                  // [kKeys][d] (16-byte aligned: 80 d + 64 floats in)
 
-    const int b = blockIdx.z, kvh = blockIdx.y, row0 = blockIdx.x * kRows;
+    const int split = blockIdx.x % p.splits, rb = blockIdx.x / p.splits;
+    const int b = blockIdx.z, kvh = blockIdx.y, row0 = rb * kRows;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int d = p.d, T = p.T;
     const int prior = p.prior[b], nn = p.n_new[b];
@@ -114,6 +115,13 @@ __global__ void __launch_bounds__(kWarps * 32) attn_f32_kernel(const __grid_cons
         if ((i & 3) == warp) lim[i >> 2] = l;
     }
     if (extent == 0) first = 0;
+    // This CTA's share of the key range: a contiguous run of 64-key tiles.
+    int kbeg = first, kend = extent;
+    if (p.splits > 1) {
+        const long long ntile = (extent - first + kKeys - 1) / kKeys;
+        kbeg = first + static_cast<int>(split * ntile / p.splits) * kKeys;
+        kend = min(extent, first + static_cast<int>((split + 1) * ntile / p.splits) * kKeys);
+    }
 
     // Stage the block's query rows.
     for (int idx = threadIdx.x; idx < kRows * d; idx += blockDim.x) {
@@ -136,9 +144,9 @@ __global__ void __launch_bounds__(kWarps * 32) attn_f32_kernel(const __grid_cons
     }
 
     const size_t unit_base = (static_cast<size_t>(b) * p.Hkv + kvh) * p.max_len;
-    for (int k0 = first; k0 < extent; k0 += kKeys) {
+    for (int k0 = kbeg; k0 < kend; k0 += kKeys) {
         __syncthreads();
-        const int nk = min(kKeys, extent - k0);
+        const int nk = min(kKeys, kend - k0);
         for (int idx = threadIdx.x; idx < kKeys * d / kVec; idx += blockDim.x) {
             const int j = (idx * kVec) / d;
             bool live = false;
@@ -217,19 +225,80 @@ __global__ void __launch_bounds__(kWarps * 32) attn_f32_kernel(const __grid_cons
         }
     }
 
+    if (p.splits == 1) {
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            const int r = row0 + warp + 4 * i;
+            if (r >= p.R) continue;
+            const int g = r / T, t = r % T;
+            E* dst = og + ((static_cast<size_t>(b) * p.Hq + kvh * p.G + g) * T + t) * d;
+            const float inv = (lim[i] >= 0 && l[i] > 0.f) ? 1.f / l[i] : 0.f;
+#pragma unroll
+            for (int c = 0; c < kMaxD / 32; ++c) {
+                const int e = lane + 32 * c;
+                if (e < d) store_out(dst + e, (lim[i] >= 0) ? o[i][c] * inv : 0.f);
+            }
+        }
+        return;
+    }
+
+    // Split key range: leave this CTA's (O, m, l) per row, then the last CTA
+    // of the unit to arrive merges every split's state (no waiting):
+    // o = sum_s e^(m_s - M) O_s / sum_s e^(m_s - M) l_s, with M = max_s m_s.
+    const int unit = (b * p.Hkv + kvh) * (gridDim.x / p.splits) + rb;
+    const size_t stride = static_cast<size_t>(d) + 2;
+    float* part = p.partials + (static_cast<size_t>(unit) * p.splits + split) * kRows * stride;
 #pragma unroll
     for (int i = 0; i < 4; ++i) {
-        const int r = row0 + warp + 4 * i;
-        if (r >= p.R) continue;
-        const int g = r / T, t = r % T;
-        E* dst = og + ((static_cast<size_t>(b) * p.Hq + kvh * p.G + g) * T + t) * d;
-        const float inv = (lim[i] >= 0 && l[i] > 0.f) ? 1.f / l[i] : 0.f;
+        float* pr = part + (warp + 4 * i) * stride;
 #pragma unroll
         for (int c = 0; c < kMaxD / 32; ++c) {
             const int e = lane + 32 * c;
-            if (e < d) store_out(dst + e, (lim[i] >= 0) ? o[i][c] * inv : 0.f);
+            if (e < d) pr[e] = o[i][c];
+        }
+        if (lane == 0) {
+            pr[d] = m[i];
+            pr[d + 1] = l[i];
         }
     }
+    __shared__ int s_last;
+    __threadfence();
+    __syncthreads();
+    if (threadIdx.x == 0) s_last = atomicAdd(p.counters + unit, 1) == p.splits - 1;
+    __syncthreads();
+    if (!s_last) return;
+    __threadfence();
+    const float* ups = p.partials + static_cast<size_t>(unit) * p.splits * kRows * stride;
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        const int rr = warp + 4 * i, r = row0 + rr;
+        if (r >= p.R) continue;
+        float M = -INFINITY;
+        for (int sp = 0; sp < p.splits; ++sp) M = fmaxf(M, __ldcg(ups + (sp * kRows + rr) * stride + d));
+        float L = 0.f, acc[kMaxD / 32];
+#pragma unroll
+        for (int c = 0; c < kMaxD / 32; ++c) acc[c] = 0.f;
+        for (int sp = 0; sp < p.splits; ++sp) {
+            const float* pr = ups + (sp * kRows + rr) * stride;
+            const float ms = __ldcg(pr + d);
+            const float w = (ms == -INFINITY) ? 0.f : expf(ms - M);
+            L += w * __ldcg(pr + d + 1);
+#pragma unroll
+            for (int c = 0; c < kMaxD / 32; ++c) {
+                const int e = lane + 32 * c;
+                if (e < d) acc[c] += w * __ldcg(pr + e);
+            }
+        }
+        const int g = r / T, t = r % T;
+        E* dst = og + ((static_cast<size_t>(b) * p.Hq + kvh * p.G + g) * T + t) * d;
+        const float inv = (lim[i] >= 0 && L > 0.f) ? 1.f / L : 0.f;
+#pragma unroll
+        for (int c = 0; c < kMaxD / 32; ++c) {
+            const int e = lane + 32 * c;
+            if (e < d) store_out(dst + e, (lim[i] >= 0) ? acc[c] * inv : 0.f);
+        }
+    }
+    if (threadIdx.x == 0) p.counters[unit] = 0;  // ready for the next call
 }
 
 template <typename E>
@@ -242,7 +311,7 @@ cudaError_t launch_generic(const F32Params& p, cudaStream_t stream) {
         if (e != cudaSuccess) return e;
         attr_set = true;
     }
-    dim3 grid((p.R + kRows - 1) / kRows, p.Hkv, p.B);
+    dim3 grid(((p.R + kRows - 1) / kRows) * p.splits, p.Hkv, p.B);
     attn_f32_kernel<E><<<grid, kWarps * 32, smem, stream>>>(p);
     return cudaGetLastError();
 }

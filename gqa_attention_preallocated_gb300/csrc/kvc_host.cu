@@ -220,6 +220,7 @@ kvc_status validate_append(const kvc_cache* c, int layer, const void* k_new, con
 struct AttnPlan {
     int Hq = 0, G = 0, T = 0, R = 0;
     int mt = 0, RPB = 0, RB = 0, NB = 0, units = 0, ways = 1, part_rows = 0;
+    int splits = 1;  // generic kernel: CTAs per (row block, KV head, row)
     size_t ws_err = 0, ws_plan = 0, ws_partials = 0, ws_total = 0;
     // Least workspace the call runs with: the tensor-core path needs only the
     // header (with less room it cuts fewer items into pieces).
@@ -274,6 +275,21 @@ kvc_status plan_shape(const kvc_cache* c, int Hq, int T, int num_ctas, AttnPlan*
             if (c->max_len <= kTcMaxLen) pl->ws_min = pl->ws_err + pl->ws_plan;
         }
         pl->ws_total = pl->ws_err + pl->ws_plan + pl->ws_partials;
+    } else {
+        // Generic kernel: one CTA per (16-row block, KV head, row).  With
+        // fewer of those than twice the SMs (decode), each one's key range is
+        // split across up to 16 CTAs (at most one a 64-key tile of max_len),
+        // which leave partials in the workspace; the last to finish merges.
+        const long long units = static_cast<long long>((pl->R + 15) / 16) * c->Hkv * c->B;
+        if (units > 0 && units < 2ll * num_ctas) {
+            const long long want = (4ll * num_ctas + units - 1) / units;  // about 4 CTAs an SM
+            pl->splits = static_cast<int>(std::min<long long>({want, kGenericMaxSplits, (c->max_len + 63) / 64}));
+        }
+        if (pl->splits > 1) {
+            pl->ws_err = kWsHeaderBytes;  // error word, then the per-unit arrival counters
+            pl->ws_partials = static_cast<size_t>(units) * pl->splits * 16 * (c->d + 2) * sizeof(float);
+            pl->ws_total = pl->ws_min = pl->ws_err + pl->ws_partials;
+        }
     }
     return ok();
 }
@@ -376,6 +392,18 @@ kvc_status do_attention(kvc_cache* c, int layer, const void* q, const AttnPlan& 
         if (anc) std::copy(anc, anc + static_cast<size_t>(c->B) * pl.T, p.anc);
         p.pg = c->pg;
         p.scale = 1.0f / sqrtf(static_cast<float>(c->d));
+        p.splits = pl.splits;
+        p.partials = nullptr;
+        p.counters = nullptr;
+        if (pl.splits > 1) {
+            p.partials = reinterpret_cast<float*>(static_cast<uint8_t*>(ws) + pl.ws_err);
+            p.counters = reinterpret_cast<int*>(static_cast<uint8_t*>(ws) + kWsCounterOffset);
+            if (ws != c->last_ws) {  // the counters start at zero and return to it after each call
+                cudaError_t e = cudaMemsetAsync(ws, 0, pl.ws_err, stream);
+                if (e != cudaSuccess) return cuda_fail(e, "cudaMemsetAsync(workspace)");
+                c->last_ws = ws;
+            }
+        }
         for (int b = 0; b < c->B; ++b) {
             p.prior[b] = static_cast<int>(lens[b] - n_new[b]);
             p.n_new[b] = n_new[b];
@@ -712,7 +740,7 @@ kvc_status do_attention(kvc_cache* c, int layer, const void* q, const AttnPlan& 
 }
 
 kvc_status check_workspace(const kvc_cache* c, const AttnPlan& pl, const void* ws, size_t ws_bytes) {
-    if (generic_path(c) || c->B == 0 || pl.T == 0) return ok();
+    if (c->B == 0 || pl.T == 0 || pl.ws_total == 0) return ok();  // (the generic kernel may need none)
     if (!ws) return fail(KVC_ERR_WORKSPACE, "workspace is null (need %zu bytes)", pl.ws_total);
     if ((reinterpret_cast<uintptr_t>(ws) & 255u) != 0) return fail(KVC_ERR_WORKSPACE, "workspace not 256-byte aligned");
     if (ws_bytes < pl.ws_total)
@@ -875,7 +903,6 @@ kvc_status kvc_append(kvc_cache* c, int layer, const void* k_new, const void* v_
 
 size_t kvc_workspace_bytes(const kvc_cache* c, int q_heads, int T) {
     if (!c) return 0;
-    if (generic_path(c)) return 0;
     kvc_cache* mc = const_cast<kvc_cache*>(c);
     if (ensure_device(mc) != KVC_OK) return 0;
     AttnPlan pl;
@@ -894,7 +921,7 @@ static kvc_status gqa_attention_impl(kvc_cache* c, int layer, const void* q, int
     const int64_t* lens = c->lens.data() + static_cast<size_t>(layer) * c->B;
     s = validate_attention(c, layer, q, q_heads, T, n_new, out, lens, &pl, 0);
     if (s) return s;
-    if (!generic_path(c) && c->B > 0 && T > 0) {
+    if (c->B > 0 && T > 0) {
         s = ensure_device(c);
         if (s) return s;
         s = plan_shape(c, q_heads, T, c->num_sms, &pl);
@@ -929,7 +956,7 @@ static kvc_status append_attention_impl(kvc_cache* c, int layer, const void* q, 
     AttnPlan pl;
     s = validate_attention(c, layer, q, q_heads, T, n_new, out, after.data(), &pl, 0);
     if (s) return s;
-    if (!generic_path(c) && c->B > 0 && T > 0) {
+    if (c->B > 0 && T > 0) {
         s = ensure_device(c);
         if (s) return s;
         s = plan_shape(c, q_heads, T, c->num_sms, &pl);

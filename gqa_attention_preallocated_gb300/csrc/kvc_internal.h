@@ -192,11 +192,18 @@ struct F32Params {
     int tree;          // ancestor masks in anc, as in DecodeParams
     Paging pg;
     float scale;  // 1 / sqrt(d)
+    // Key-range split: `splits` CTAs per (row block, KV head, row); with more
+    // than one, each leaves (m, l, O) of its 16 rows in partials
+    // [unit][split][16][d + 2] and the last to arrive (counters[unit]) merges.
+    int splits;
+    float* partials;
+    int* counters;
     int prior[kMaxBatch];
     int n_new[kMaxBatch];
     uint64_t anc[kMaxTreeQueries];
 };
 
+constexpr int kGenericMaxSplits = 16;
 cudaError_t launch_attn_f32(const F32Params& p, cudaStream_t stream);
 
 // ---------------------------------------------------------------------------

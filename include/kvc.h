@@ -30,8 +30,9 @@
  * multiple of 16, and d <= 256.  bf16 caches of d = 128 and all FP8 caches
  * (d = 128 only) run on the TMA / tensor-core kernels.  fp32 caches and bf16
  * caches of any other d run on a generic kernel.  That kernel widens the
- * stored values to fp32 and has no workspace, fused append, device-resident
- * steps or allocation-free entry point.
+ * stored values to fp32.  It has no fused append, no device-resident steps
+ * and no allocation-free entry point, and needs a workspace only for calls
+ * whose key ranges it splits (kvc_workspace_bytes).
  *
  * Device.  One process drives one GPU through this library: a handle binds
  * to the device current at its first launching call, every later launching
@@ -154,8 +155,10 @@ kvc_status kvc_append(kvc_cache* c, int layer, const void* k_new, const void* v_
 
 /* Bytes of device workspace kvc_gqa_attention needs for this handle, q_heads
  * and T (an error word and the split-KV partial results).
- * 0 means no workspace is needed (the generic kernel: fp32 caches, bf16 of
- * d != 128).  Returns 0 for invalid input. */
+ * 0 means no workspace is needed: the generic kernel (fp32 caches, bf16 of
+ * d != 128) needs one only for calls with few (row, KV head, 16-row block)
+ * units, whose key ranges it splits across CTAs.  Returns 0 for invalid
+ * input. */
 size_t kvc_workspace_bytes(const kvc_cache* c, int q_heads, int T);
 
 /* Attention of the chunk just appended ("A strong answer", gqa_attention):

@@ -154,3 +154,16 @@ def test_bf16_generic_rejects_fast_path_only_calls():
     q = torch.zeros((2, 8, 1, 64), dtype=BF16, device="cuda")
     with pytest.raises(KVCError):
         cache.gqa_attention_noalloc(0, q, [0, 0])
+
+
+@pytest.mark.parametrize("window", [0, 300])
+def test_generic_split_key_range(window):
+    """Few (row, KV head) units and long rows: the generic kernel splits each
+    unit's key range across 16 CTAs and merges them (decode and verify)."""
+    cache, orc = _contiguous(2, 2, 64, 2048, window)
+    rng = np.random.default_rng(7 + window)
+    calls = [np.array([1500, 1203]), np.ones(2, dtype=np.int64), np.array([4, 3]), np.ones(2, dtype=np.int64)]
+    for ci, n in enumerate(calls):
+        _step(cache, orc, 21, ci, 4, n)
+    assert cache.workspace_bytes(8, 1) > 0  # decode splits the key range: partials need room
+    _check_slots(cache, orc)

@@ -159,6 +159,12 @@ def test_generic_kernel_maximum_batch(dtype, d):
     _run_calls(17, B, Hkv, G, d, max_len, dtype, calls)
 
 
+def test_f32_split_key_range():
+    """fp32 decode over long rows: the generic kernel splits each unit's keys across 16 CTAs."""
+    calls = [np.array([1500, 1203]), np.ones(2, dtype=np.int64), np.array([4, 3]), np.array([1, 0])]
+    _run_calls(23, 2, 2, 4, 16, 2048, torch.float32, calls)
+
+
 def test_incremental_equals_full_on_gpu():
     """S = 37, T = 5: the chunked GPU output matches the full-sequence GPU output's last rows."""
     _cuda_or_skip()
