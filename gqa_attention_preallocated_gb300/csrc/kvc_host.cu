@@ -279,10 +279,11 @@ kvc_status plan_shape(const kvc_cache* c, int Hq, int T, int num_ctas, AttnPlan*
         // Generic kernel: one CTA per (16-row block, KV head, row).  With
         // fewer of those than twice the SMs (decode), each one's key range is
         // split across up to 16 CTAs (at most one a 64-key tile of max_len),
-        // which leave partials in the workspace; the last to finish merges.
+        // about 16 an SM, which leave partials in the workspace; the last to
+        // finish merges.
         const long long units = static_cast<long long>((pl->R + 15) / 16) * c->Hkv * c->B;
         if (units > 0 && units < 2ll * num_ctas) {
-            const long long want = (4ll * num_ctas + units - 1) / units;  // about 4 CTAs an SM
+            const long long want = (16ll * num_ctas + units - 1) / units;  // measured: 4, 8, 16 an SM
             pl->splits = static_cast<int>(std::min<long long>({want, kGenericMaxSplits, (c->max_len + 63) / 64}));
         }
         if (pl->splits > 1) {
