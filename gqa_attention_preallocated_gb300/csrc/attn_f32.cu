@@ -28,9 +28,13 @@
 // a query sees the chunk's tokens on its own path to the root only.
 
 #include <cuda_bf16.h>
+#include <cuda_fp16.h>
 #include <math.h>
 
+#include <type_traits>
+
 #include "kvc_internal.h"
+#include "ptx.cuh"
 
 namespace kvc {
 
@@ -46,7 +50,32 @@ __device__ __forceinline__ float widen(__nv_bfloat16 x) { return __bfloat162floa
 __device__ __forceinline__ void store_out(float* dst, float x) { *dst = x; }
 __device__ __forceinline__ void store_out(__nv_bfloat16* dst, float x) { *dst = __float2bfloat16_rn(x); }
 
-// 16 stored bytes (4 fp32 or 8 bf16 values) into fp32 shared memory.
+// 16 E4M3 codes -> 16 values times the head's scale (E4M3 -> f16 is exact).
+__device__ __forceinline__ void widen_e4m3x16(const uint8_t* src, float sc, float (&f)[16]) {
+    const uint4 w = *reinterpret_cast<const uint4*>(src);
+    const uint32_t u[4] = {w.x, w.y, w.z, w.w};
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        uint32_t lo, hi;
+        ptx::e4m3x4_to_f16x2x2(u[i], lo, hi);  // bytes 0, 1 -> lo; 2, 3 -> hi (low half first)
+        __half2 hl, hh;
+        memcpy(&hl, &lo, 4);
+        memcpy(&hh, &hi, 4);
+        const float2 a = __half22float2(hl), b = __half22float2(hh);
+        f[4 * i] = a.x * sc;
+        f[4 * i + 1] = a.y * sc;
+        f[4 * i + 2] = b.x * sc;
+        f[4 * i + 3] = b.y * sc;
+    }
+}
+
+// 16 stored bytes (4 fp32, 8 bf16 or 16 E4M3 values) into fp32 shared memory.
+__device__ __forceinline__ void stage16(float* dst, const uint8_t* src, float sc) {
+    float f[16];
+    widen_e4m3x16(src, sc, f);
+#pragma unroll
+    for (int i = 0; i < 4; ++i) reinterpret_cast<float4*>(dst)[i] = make_float4(f[4 * i], f[4 * i + 1], f[4 * i + 2], f[4 * i + 3]);
+}
 __device__ __forceinline__ void stage16(float* dst, const float* src) {
     *reinterpret_cast<float4*>(dst) = *reinterpret_cast<const float4*>(src);
 }
@@ -62,16 +91,24 @@ __device__ __forceinline__ void stage16(float* dst, const __nv_bfloat16* src) {
     reinterpret_cast<float4*>(dst)[0] = make_float4(f[0], f[1], f[2], f[3]);
     reinterpret_cast<float4*>(dst)[1] = make_float4(f[4], f[5], f[6], f[7]);
 }
+__device__ __forceinline__ void stage16(float* dst, const float* src, float) { stage16(dst, src); }
+__device__ __forceinline__ void stage16(float* dst, const __nv_bfloat16* src, float) { stage16(dst, src); }
 
 // The same into a row of any alignment (one value a store).
-__device__ __forceinline__ void stage16_rows(float* dst, const float* src) {
+__device__ __forceinline__ void stage16_rows(float* dst, const uint8_t* src, float sc) {
+    float f[16];
+    widen_e4m3x16(src, sc, f);
+#pragma unroll
+    for (int i = 0; i < 16; ++i) dst[i] = f[i];
+}
+__device__ __forceinline__ void stage16_rows(float* dst, const float* src, float) {
     const float4 v = *reinterpret_cast<const float4*>(src);
     dst[0] = v.x;
     dst[1] = v.y;
     dst[2] = v.z;
     dst[3] = v.w;
 }
-__device__ __forceinline__ void stage16_rows(float* dst, const __nv_bfloat16* src) {
+__device__ __forceinline__ void stage16_rows(float* dst, const __nv_bfloat16* src, float) {
     const uint4 w = *reinterpret_cast<const uint4*>(src);
     const uint32_t u[4] = {w.x, w.y, w.z, w.w};
 #pragma unroll
@@ -81,13 +118,16 @@ __device__ __forceinline__ void stage16_rows(float* dst, const __nv_bfloat16* sr
     }
 }
 
-template <typename E>
+// SE: the stored type (float, bf16, or E4M3 codes as uint8_t); IE: the type
+// of the queries and outputs.
+template <typename SE, typename IE>
 __global__ void __launch_bounds__(kWarps * 32) attn_f32_kernel(const __grid_constant__ F32Params p) {
-    constexpr int kVec = 16 / static_cast<int>(sizeof(E));  // values per 16-byte load
-    const E* qg = static_cast<const E*>(p.q);
-    const E* kg = static_cast<const E*>(p.k_cache);
-    const E* vg = static_cast<const E*>(p.v_cache);
-    E* og = static_cast<E*>(p.out);
+    constexpr int kVec = 16 / static_cast<int>(sizeof(SE));  // values per 16-byte load
+    constexpr bool kF8 = std::is_same<SE, uint8_t>::value;
+    const IE* qg = static_cast<const IE*>(p.q);
+    const SE* kg = static_cast<const SE*>(p.k_cache);
+    const SE* vg = static_cast<const SE*>(p.v_cache);
+    IE* og = static_cast<IE*>(p.out);
     extern __shared__ float4 smem4[];
     float* sq = reinterpret_cast<float*>(smem4);  // [kRows][d]
     // K rows are d + 1 floats apart: lane j reads key j's row in the score
@@ -101,6 +141,7 @@ __global__ void __launch_bounds__(kWarps * 32) attn_f32_kernel(const __grid_cons
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int d = p.d, T = p.T;
     const int prior = p.prior[b], nn = p.n_new[b];
+    const float ksc = kF8 ? p.kscale[kvh] : 1.f, vsc = kF8 ? p.vscale[kvh] : 1.f;  // FP8 code scales
 
     // Row limits (largest visible key; -1 = padded / missing row), the keys'
     // extent and, with a window, the first key any row of the block sees.
@@ -160,8 +201,8 @@ __global__ void __launch_bounds__(kWarps * 32) attn_f32_kernel(const __grid_cons
             }
             float* kdst = sk + j * dk + (idx * kVec - j * d);
             if (live) {
-                stage16_rows(kdst, kg + off);
-                stage16(sv + idx * kVec, vg + off);
+                stage16_rows(kdst, kg + off, ksc);
+                stage16(sv + idx * kVec, vg + off, vsc);
             } else {
 #pragma unroll
                 for (int i = 0; i < kVec; ++i) kdst[i] = sv[idx * kVec + i] = 0.f;
@@ -231,7 +272,7 @@ __global__ void __launch_bounds__(kWarps * 32) attn_f32_kernel(const __grid_cons
             const int r = row0 + warp + 4 * i;
             if (r >= p.R) continue;
             const int g = r / T, t = r % T;
-            E* dst = og + ((static_cast<size_t>(b) * p.Hq + kvh * p.G + g) * T + t) * d;
+            IE* dst = og + ((static_cast<size_t>(b) * p.Hq + kvh * p.G + g) * T + t) * d;
             const float inv = (lim[i] >= 0 && l[i] > 0.f) ? 1.f / l[i] : 0.f;
 #pragma unroll
             for (int c = 0; c < kMaxD / 32; ++c) {
@@ -290,7 +331,7 @@ __global__ void __launch_bounds__(kWarps * 32) attn_f32_kernel(const __grid_cons
             }
         }
         const int g = r / T, t = r % T;
-        E* dst = og + ((static_cast<size_t>(b) * p.Hq + kvh * p.G + g) * T + t) * d;
+        IE* dst = og + ((static_cast<size_t>(b) * p.Hq + kvh * p.G + g) * T + t) * d;
         const float inv = (lim[i] >= 0 && L > 0.f) ? 1.f / L : 0.f;
 #pragma unroll
         for (int c = 0; c < kMaxD / 32; ++c) {
@@ -301,25 +342,27 @@ __global__ void __launch_bounds__(kWarps * 32) attn_f32_kernel(const __grid_cons
     if (threadIdx.x == 0) p.counters[unit] = 0;  // ready for the next call
 }
 
-template <typename E>
+template <typename SE, typename IE>
 cudaError_t launch_generic(const F32Params& p, cudaStream_t stream) {
     const size_t smem = (static_cast<size_t>(kRows + 2 * kKeys) * p.d + kKeys) * sizeof(float);
     static bool attr_set = false;
     if (!attr_set) {
-        cudaError_t e = cudaFuncSetAttribute(attn_f32_kernel<E>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+        cudaError_t e = cudaFuncSetAttribute(attn_f32_kernel<SE, IE>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                              static_cast<int>(((kRows + 2 * kKeys) * kMaxD + kKeys) * sizeof(float)));
         if (e != cudaSuccess) return e;
         attr_set = true;
     }
     dim3 grid(((p.R + kRows - 1) / kRows) * p.splits, p.Hkv, p.B);
-    attn_f32_kernel<E><<<grid, kWarps * 32, smem, stream>>>(p);
+    attn_f32_kernel<SE, IE><<<grid, kWarps * 32, smem, stream>>>(p);
     return cudaGetLastError();
 }
 
 }  // namespace
 
 cudaError_t launch_attn_f32(const F32Params& p, cudaStream_t stream) {
-    return p.bf16 ? launch_generic<__nv_bfloat16>(p, stream) : launch_generic<float>(p, stream);
+    if (p.kind == 2) return launch_generic<uint8_t, __nv_bfloat16>(p, stream);
+    if (p.kind == 1) return launch_generic<__nv_bfloat16, __nv_bfloat16>(p, stream);
+    return launch_generic<float, float>(p, stream);
 }
 
 }  // namespace kvc

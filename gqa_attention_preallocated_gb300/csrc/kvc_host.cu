@@ -71,8 +71,8 @@ constexpr int kTcMinRows = 12;
 constexpr int kTcMinRowsFp8 = 16;
 int tc_min_rows(const kvc_cache* c) { return c->dtype == KVC_FP8_E4M3 ? kTcMinRowsFp8 : kTcMinRows; }
 // Caches served by the generic kernel (attn_f32.cu): fp32 storage, and bf16
-// storage whose head dimension is not the 128 that the TMA / tensor-core
-// kernels are built for.
+// or FP8 storage whose head dimension is not the 128 that the TMA /
+// tensor-core kernels are built for.
 bool generic_path(const kvc_cache* c) { return c->dtype == KVC_F32 || c->d != kHeadDimBf16; }
 constexpr int kTcMaxLen = 0xFFFF * 128;  // key tiles of a piece are packed in 16 bits
 
@@ -378,7 +378,11 @@ kvc_status do_attention(kvc_cache* c, int layer, const void* q, const AttnPlan& 
         p.k_cache = c->k[layer];
         p.v_cache = c->v[layer];
         p.out = out;
-        p.bf16 = c->dtype == KVC_BF16 ? 1 : 0;
+        p.kind = c->dtype == KVC_FP8_E4M3 ? 2 : (c->dtype == KVC_BF16 ? 1 : 0);
+        for (int h = 0; h < c->Hkv && p.kind == 2; ++h) {
+            p.kscale[h] = c->kscale[static_cast<size_t>(layer) * c->Hkv + h];
+            p.vscale[h] = c->vscale[static_cast<size_t>(layer) * c->Hkv + h];
+        }
         p.B = c->B;
         p.Hq = pl.Hq;
         p.Hkv = c->Hkv;
@@ -805,8 +809,6 @@ kvc_status kvc_create(kvc_cache** out, int layers, int batch, int kv_heads, int 
     const int esize = dtype == KVC_F32 ? 4 : (dtype == KVC_BF16 ? 2 : 1);
     if ((head_dim * esize) % 16 != 0) return fail(KVC_ERR_ARG, "head_dim * element size must be a multiple of 16");
     if (head_dim > 256) return fail(KVC_ERR_ARG, "head_dim %d > 256", head_dim);
-    if (dtype == KVC_FP8_E4M3 && head_dim != kHeadDimBf16)
-        return fail(KVC_ERR_ARG, "fp8 caches take head_dim = %d", kHeadDimBf16);
     if (dtype == KVC_FP8_E4M3 && kv_heads > kMaxScaleHeads)
         return fail(KVC_ERR_ARG, "fp8 caches take at most %d KV heads", kMaxScaleHeads);
     const long long rows = static_cast<long long>(batch) * kv_heads * max_len;

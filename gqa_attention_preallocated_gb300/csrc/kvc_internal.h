@@ -180,12 +180,16 @@ cudaError_t launch_decode_bf16(const DecodeParams& p, const CUtensorMap& tmK, co
 // all keys of the unit, output written directly; no workspace.
 // ---------------------------------------------------------------------------
 struct F32Params {
-    // Stored values, queries and outputs are fp32, or bf16 when bf16 is set.
+    // kind 0: fp32 storage, queries and outputs; 1: bf16 throughout; 2: FP8
+    // E4M3 codes (value = code * kscale / vscale of the KV head), bf16
+    // queries and outputs.
     const void* q;
     const void* k_cache;
     const void* v_cache;
     void* out;
-    int bf16;
+    int kind;
+    float kscale[kMaxScaleHeads];
+    float vscale[kMaxScaleHeads];
     int B, Hq, Hkv, G, T, max_len, d;
     int R;
     int window, ring;  // sliding window (0 = none) and ring storage, as in DecodeParams

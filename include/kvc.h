@@ -27,10 +27,10 @@
  *   k_new, v_new              [B, Hkv, T, d]
  *   q, out                    [B, Hq, T, d]
  * All device pointers must be 16-byte aligned.  d * sizeof(element) must be a
- * multiple of 16, and d <= 256.  bf16 caches of d = 128 and all FP8 caches
- * (d = 128 only) run on the TMA / tensor-core kernels.  fp32 caches and bf16
- * caches of any other d run on a generic kernel.  That kernel widens the
- * stored values to fp32.  It has no fused append, no device-resident steps
+ * multiple of 16, and d <= 256.  bf16 and FP8 caches of d = 128 run on the
+ * TMA / tensor-core kernels.  fp32 caches, and bf16 or FP8 caches of any
+ * other d, run on a generic kernel.  That kernel widens the stored values to
+ * fp32 (an FP8 code times its head's scale).  It has no fused append, no device-resident steps
  * and no allocation-free entry point, and needs a workspace only for calls
  * whose key ranges it splits (kvc_workspace_bytes).
  *
@@ -104,7 +104,7 @@ typedef struct kvc_cache kvc_cache;
  * count) is set up on the first launch.
  * Errors: KVC_ERR_ARG for non-positive sizes, B > KVC_MAX_BATCH, null or
  * misaligned buffers, d * element size not a multiple of 16, or d > 256;
- * FP8 caches take d = 128 and at most 64 KV heads. */
+ * FP8 caches take at most 64 KV heads. */
 kvc_status kvc_create(kvc_cache** out, int layers, int batch, int kv_heads, int max_len, int head_dim,
                       kvc_dtype dtype, void* const* k_bufs, void* const* v_bufs);
 
@@ -135,8 +135,8 @@ kvc_status kvc_set_kv_scales(kvc_cache* c, int layer, const float* k_scale, cons
  * (0 .. num_pages - 1) and may change the table between calls (stream-ordered).
  * A bad entry is never dereferenced: appended rows aimed at it are not
  * written, and reads take page 0 and set the workspace error word (the next
- * kvc_device_status reports it); the generic kernel (fp32, bf16 of d != 128)
- * reads it as zeros.  bf16 and FP8 caches of d = 128 need page_size % 128 == 0.  Paged storage does not combine with ring
+ * kvc_device_status reports it); the generic kernel (fp32; bf16, FP8 of
+ * d != 128) reads it as zeros.  bf16 and FP8 caches of d = 128 need page_size % 128 == 0.  Paged storage does not combine with ring
  * storage (kvc_set_window ring = 1).  Errors: as kvc_create, and KVC_ERR_ARG
  * for bad paging arguments. */
 kvc_status kvc_create_paged(kvc_cache** out, int layers, int batch, int kv_heads, int page_size, int num_pages,
@@ -155,9 +155,9 @@ kvc_status kvc_append(kvc_cache* c, int layer, const void* k_new, const void* v_
 
 /* Bytes of device workspace kvc_gqa_attention needs for this handle, q_heads
  * and T (an error word and the split-KV partial results).
- * 0 means no workspace is needed: the generic kernel (fp32 caches, bf16 of
- * d != 128) needs one only for calls with few (row, KV head, 16-row block)
- * units, whose key ranges it splits across CTAs.  Returns 0 for invalid
+ * 0 means no workspace is needed: the generic kernel (fp32 caches; bf16 and
+ * FP8 caches of d != 128) needs one only for calls with few (row, KV head,
+ * 16-row block) units, whose key ranges it splits across CTAs.  Returns 0 for invalid
  * input. */
 size_t kvc_workspace_bytes(const kvc_cache* c, int q_heads, int T);
 

@@ -278,7 +278,10 @@ def test_fp8_host_rules(L):
         a = np.array(xs, dtype=np.float32)
         return a, a.ctypes.data_as(FP)
 
-    assert _create(L, d=64, dtype=_lib.KVC_FP8_E4M3)[0] == 1      # fp8 takes d = 128
+    assert _create(L, d=24, dtype=_lib.KVC_FP8_E4M3)[0] == 1      # 24 one-byte values: not a multiple of 16
+    st, h = _create(L, d=64, dtype=_lib.KVC_FP8_E4M3)             # other head dims: the generic kernel
+    assert st == 0
+    L.kvc_destroy(h)
     assert _create(L, Hkv=65, d=128, dtype=_lib.KVC_FP8_E4M3)[0] == 1
     st, h = _create(L, layers=2, B=2, Hkv=2, max_len=256, d=128, dtype=_lib.KVC_FP8_E4M3)
     assert st == 0

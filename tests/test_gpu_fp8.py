@@ -34,10 +34,10 @@ def _scales(Hkv, seed, lo=2.0 / 448, hi=6.0 / 448):
     return rng.uniform(lo, hi, Hkv).astype(np.float32), rng.uniform(lo, hi, Hkv).astype(np.float32)
 
 
-def _pair(B, Hkv, max_len, seed, window=0, paged=None):
+def _pair(B, Hkv, max_len, seed, window=0, paged=None, d=128):
     if paged is None:
-        cache = KVCache(1, B, Hkv, max_len, 128, dtype=FP8)
-        orc = ref.OracleCache(1, B, Hkv, max_len, 128)
+        cache = KVCache(1, B, Hkv, max_len, d, dtype=FP8)
+        orc = ref.OracleCache(1, B, Hkv, max_len, d)
     else:
         page, num_pages, mpr, table = paged
         cache = PagedKVCache(1, B, Hkv, page, num_pages, mpr, 128, dtype=FP8)
@@ -280,3 +280,26 @@ def test_fp8_ring_storage():
         _step(cache, orc, 18, ci, G, [1, 1])
     assert np.all(orc.lens[0] > max_len)  # the ring wrapped
     assert cache.device_status() == 0
+
+
+@pytest.mark.parametrize("d", [64, 256])
+@pytest.mark.parametrize("window", [0, 200])
+def test_fp8_other_head_dims_on_the_generic_kernel(d, window):
+    """FP8 caches of d != 128: codes bit-exact, outputs against the oracle's
+    dequantized values.  A prefill chunk, then decode over long rows (the key
+    range split across CTAs) and a verify chunk."""
+    _cuda_or_skip()
+    cache, orc = _pair(2, 2, 1600, 31 + d, window=window, d=d)
+    for ci, n in enumerate([np.array([1200, 907]), np.array([1, 1]), np.array([4, 2]), np.array([1, 0])]):
+        _step(cache, orc, 40 + d, ci, 4, n)
+    _codes_of(cache, orc)
+    assert cache.device_status() == 0
+
+
+def test_fp8_head_dim_64_tree():
+    _cuda_or_skip()
+    cache, orc = _pair(3, 1, 400, 5, d=64)
+    _step(cache, orc, 6, 0, 8, np.array([300, 211, 77]))
+    parents = np.array([[-1, 0, 1, 2, 3, 4], [-1, -1, -1, -1, -1, -1], [-1, 0, 0, 1, 1, 2]])
+    _step(cache, orc, 6, 1, 8, np.array([6, 6, 4]), parents=parents)
+    _codes_of(cache, orc)
