@@ -79,6 +79,11 @@ def test_create_validation(L):
     assert L.kvc_create(ctypes.byref(h), 1, 2, 2, 8, 6, 0, k, v) == 1  # 6 * 4 B not a multiple of 16
     assert L.kvc_create(ctypes.byref(h), 1, 2, 2, 8, 12, 1, k, v) == 1  # 12 * 2 B not a multiple of 16
     assert L.kvc_create(ctypes.byref(h), 1, 2, 2, 8, 264, 1, k, v) == 1  # d <= 256
+    assert L.kvc_create(ctypes.byref(h), 1, 2, 2, 8, 260, 0, k, v) == 1  # fp32 too
+    assert L.kvc_create(ctypes.byref(h), 1, 2, 2, 8, 272, 2, k, v) == 1  # and FP8
+    for dt, d in ((0, 256), (1, 256), (2, 256), (1, 72), (2, 48)):      # the largest, and other sizes
+        assert L.kvc_create(ctypes.byref(h), 1, 2, 2, 8, d, dt, k, v) == 0, (dt, d)
+        L.kvc_destroy(h)
     assert L.kvc_create(ctypes.byref(h), 1, _lib.KVC_MAX_BATCH + 1, 2, 8, 16, 0, k, v) == 1
     bad = (ctypes.c_void_p * 1)(12345)  # misaligned
     assert L.kvc_create(ctypes.byref(h), 1, 2, 2, 8, 16, 0, bad, v) == 1
