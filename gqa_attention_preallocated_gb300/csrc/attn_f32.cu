@@ -184,7 +184,6 @@ __global__ void __launch_bounds__(kWarps * 32) attn_f32_kernel(const __grid_cons
         for (int c = 0; c < kMaxD / 32; ++c) o[i][c] = 0.f;
     }
 
-    const size_t unit_base = (static_cast<size_t>(b) * p.Hkv + kvh) * p.max_len;
     for (int k0 = kbeg; k0 < kend; k0 += kKeys) {
         __syncthreads();
         const int nk = min(kKeys, kend - k0);
