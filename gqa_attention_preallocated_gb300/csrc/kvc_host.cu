@@ -924,15 +924,15 @@ static kvc_status gqa_attention_impl(kvc_cache* c, int layer, const void* q, int
     const int64_t* lens = c->lens.data() + static_cast<size_t>(layer) * c->B;
     s = validate_attention(c, layer, q, q_heads, T, n_new, out, lens, &pl, 0);
     if (s) return s;
+    std::vector<uint64_t> anc;  // (validated before any CUDA call)
+    if (parents) {
+        s = tree_masks(c, pl, n_new, parents, &anc);
+        if (s) return s;
+    }
     if (c->B > 0 && T > 0) {
         s = ensure_device(c);
         if (s) return s;
         s = plan_shape(c, q_heads, T, c->num_sms, &pl);
-        if (s) return s;
-    }
-    std::vector<uint64_t> anc;
-    if (parents) {
-        s = tree_masks(c, pl, n_new, parents, &anc);
         if (s) return s;
     }
     s = check_workspace(c, pl, workspace, workspace_bytes);
@@ -959,15 +959,15 @@ static kvc_status append_attention_impl(kvc_cache* c, int layer, const void* q, 
     AttnPlan pl;
     s = validate_attention(c, layer, q, q_heads, T, n_new, out, after.data(), &pl, 0);
     if (s) return s;
+    std::vector<uint64_t> anc;  // (validated before any CUDA call)
+    if (parents) {
+        s = tree_masks(c, pl, n_new, parents, &anc);
+        if (s) return s;
+    }
     if (c->B > 0 && T > 0) {
         s = ensure_device(c);
         if (s) return s;
         s = plan_shape(c, q_heads, T, c->num_sms, &pl);
-        if (s) return s;
-    }
-    std::vector<uint64_t> anc;
-    if (parents) {
-        s = tree_masks(c, pl, n_new, parents, &anc);
         if (s) return s;
     }
     const uint64_t* ancp = parents ? anc.data() : nullptr;

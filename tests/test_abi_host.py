@@ -308,3 +308,31 @@ def test_fp8_host_rules(L):
     _, ok = scales(1.0, 1.0)
     assert L.kvc_set_kv_scales(h, 0, ok, ok) == 1                 # not an fp8 cache
     L.kvc_destroy(h)
+
+
+def test_tree_validation_before_any_device_call(L):
+    """A draft tree's parents, size and the window rule are checked on the
+    host before anything touches a GPU (so these run without one)."""
+    st, h = _create(L, layers=1, B=2, Hkv=1, max_len=80, d=16)
+    assert st == 0
+    _, lens = _i64(10, 10)
+    assert L.kvc_set_lens(h, 0, lens) == 0
+    q = ctypes.c_void_p(1 << 41)
+    out = ctypes.c_void_p(1 << 42)
+    _, nn = _i32(4, 4)
+    bad, bad_p = _i32(-1, 0, 3, 1, -1, 0, 0, 0)          # row 0: token 2's parent comes after it
+    assert L.kvc_gqa_attention_tree(h, 0, q, 1, 4, nn, bad_p, out, None, 0, None) == 2
+    assert b"parent" in L.kvc_last_error()
+    _, long_lens = _i64(70, 70)
+    assert L.kvc_set_lens(h, 0, long_lens) == 0
+    _, nn65 = _i32(65, 65)
+    chain = np.concatenate([np.arange(-1, 64), np.arange(-1, 64)]).astype(np.int32)
+    assert L.kvc_gqa_attention_tree(h, 0, q, 1, 65, nn65, chain.ctypes.data_as(I32P), out, None, 0, None) == 2
+    assert b"64" in L.kvc_last_error()
+    assert L.kvc_set_lens(h, 0, lens) == 0
+    assert L.kvc_reset(h) == 0
+    assert L.kvc_set_window(h, 5, 0) == 0
+    assert L.kvc_set_lens(h, 0, lens) == 0
+    ok, ok_p = _i32(-1, 0, 1, 2, -1, -1, -1, -1)
+    assert L.kvc_gqa_attention_tree(h, 0, q, 1, 4, nn, ok_p, out, None, 0, None) == 1  # no window with a tree
+    L.kvc_destroy(h)
