@@ -169,14 +169,19 @@ def step_inputs(shape, Hq, T, n_distinct, seed, device="cuda"):
 class Workload:
     """One named workload: set-up, one step, and the step's algorithmic work."""
 
-    def __init__(self, name, seed=0, verify_t=4, verify_g=4, kv_dtype="bf16", prefill_ragged=False):
+    def __init__(self, name, seed=0, verify_t=4, verify_g=4, kv_dtype="bf16", prefill_ragged=False, head_dim=128):
         self.name = name
         self.ragged = False
         self.seed = seed
         self.kv_dtype = kv_dtype  # "bf16", or "fp8": E4M3 cache with one scale per KV head
         self.esize = 1 if kv_dtype == "fp8" else 2
+        if head_dim not in (64, 128) or (head_dim == 64 and (name != "decode8b" or kv_dtype != "bf16")):
+            raise SystemExit("--head-dim 64 applies to the bf16 decode8b workload")
         if name == "decode8b":
             s = self.shape = wl.DECODE_8B
+            if head_dim == 64:  # the same decode shape with 64-wide heads
+                s = self.shape = wl.Shape("decode_b32_hq32_hkv8_d64_len8192_bf16", B=32, Hq=32, Hkv=8, d=64,
+                                          max_len=8192, dtype="bf16")
             self.layers, self.Hq, self.T = 1, s.Hq, 1
             self.lens0 = wl.decode_lens(seed, s.B, 1024, s.max_len - 256)
             self.n_new = np.ones(s.B, dtype=np.int64)
@@ -220,8 +225,19 @@ class Workload:
                 "kv_storage": "fp8_e4m3 (one scale per KV head)" if self.kv_dtype == "fp8" else "bf16",
                 "initial_lens": {"min": int(self.lens0.min()), "max": int(self.lens0.max()),
                                  "mean": float(self.lens0.mean())},
-                "l2": "inputs larger than L2 (live KV per step exceeds the 129 MB L2)" if self.name != "prefill"
-                else "per-step K/V working set exceeds L2 for long priors; not flushed"}
+                "l2": self.l2_statement()}
+
+    def l2_statement(self):
+        """How the timed steps meet the L2 (no flush between steps; the reason, with sizes)."""
+        l2 = torch.cuda.get_device_properties(torch.cuda.current_device()).L2_cache_size if torch.cuda.is_available() \
+            else 126 << 20
+        live = kv_bytes(self.lens_at(0), self.shape.Hkv, self.shape.d, self.esize) * self.layers
+        if self.unit == "TFLOP/s":
+            return (f"no flush: tensor-bound (about 2,000 FLOP per K/V byte); each step reads {live / 1e6:.0f} MB "
+                    f"of live K/V ({live / l2:.1f}x the {l2 / 1e6:.0f} MB L2) in about a tenth of its time")
+        return (f"no flush, no rotation: each step reads all live K/V, {live / 1e6:.0f} MB "
+                f"({live / l2:.1f}x the {l2 / 1e6:.0f} MB L2), in the same order as the step before, "
+                f"so those lines are evicted before they are read again" + _committed_l2(self))
 
     def lens_at(self, i):
         """Lengths after the append of step i (steps counted from the last rollback)."""
@@ -315,36 +331,38 @@ def run_native(w: Workload, steps: int, warmup: int, rank: int, world: int):
         torch.distributed.barrier()
     ms = start.elapsed_time(stop)
 
-    # Kernel timing for the roofline: the same K steps again, with an event
-    # pair around the layer-0 attention call of every step (for fused steps
-    # the pair holds the attention kernel, which also appends, and the
-    # combine kernel; otherwise the append runs before the first event).
+    # Kernel time for the roofline: the average duration of the attention
+    # launch when launches run back to back, as in the timed region (an event
+    # pair around every call would break the chaining of consecutive launches
+    # and time each launch's start-up alone).  Fused steps (the attention
+    # launch also appends) are one attention launch per layer call, so the
+    # timed region itself is that chain.  Otherwise the append runs once and
+    # K attention-only calls of layer 0 on the same lengths are chained
+    # between one event pair.
     cache.truncate(w.lens0)
     torch.cuda.synchronize()
-    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(steps)]
-    for i in range(steps):
-        if i > 0 and i % w.rollback_every == 0:
-            cache.truncate(w.lens0)
-        j = i % n_distinct
-        for layer in range(w.layers):
-            if layer == 0:
-                if not w.fused:
-                    cache.append(layer, k[j], v[j], w.n_new)
-                evs[i][0].record(stream)
-                if w.fused:
-                    cache.append_attention(layer, q[j], k[j], v[j], w.n_new, out=out, workspace=ws)
-                else:
-                    cache.gqa_attention(layer, q[j], w.n_new, out=out, workspace=ws)
-                evs[i][1].record(stream)
-            else:
-                cache.append_attention(layer, q[j], k[j], v[j], w.n_new, out=out, workspace=ws)
-    torch.cuda.synchronize()
-    attn_ms = [e[0].elapsed_time(e[1]) for e in evs]
+    if w.fused:
+        attn_ms = ms / (steps * w.layers)
+        kbytes = [w.kernel_bytes(i) for i in range(steps)]
+        kernel_timing = "timed region / (steps x layers): fused attention launches back to back"
+    else:
+        cache.append(0, k[0], v[0], w.n_new)
+        for _ in range(2):  # warm the chain
+            cache.gqa_attention(0, q[0], w.n_new, out=out, workspace=ws)
+        a0, a1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        torch.cuda.synchronize()
+        a0.record(stream)
+        for i in range(steps):
+            cache.gqa_attention(0, q[i % n_distinct], w.n_new, out=out, workspace=ws)
+        a1.record(stream)
+        torch.cuda.synchronize()
+        attn_ms = a0.elapsed_time(a1) / steps
+        kbytes = [w.kernel_bytes(0)] * steps
+        kernel_timing = f"{steps} attention-only calls of layer 0 back to back between one event pair (append before)"
     status = cache.device_status(ws)
     work = sum(w.work(i) for i in range(steps))
-    kbytes = [w.kernel_bytes(i) for i in range(steps)]
     res = {
-        "ms": ms, "wall_s": t_wall, "work": work, "attn_ms": attn_ms,
+        "ms": ms, "wall_s": t_wall, "work": work, "attn_ms": attn_ms, "kernel_timing": kernel_timing,
         "kernel_bytes": kbytes, "launches": launches, "clocks": clk.summary(), "status": status,
     }
     res["e2e"] = run_e2e(w, cache, steps, q, k, v)
@@ -373,12 +391,14 @@ def run_graph(w: Workload, cache, steps: int, q, k, v):
         for layer in range(w.layers):  # first use outside the capture
             cache.decode_step(layer, q[0], k[0], v[0], snn, sout, ws)
         graphs = []
+        l0 = cache.kernel_launches()
         for j in range(n_distinct):
             g = torch.cuda.CUDAGraph()
             with torch.cuda.graph(g):
                 for layer in range(w.layers):
                     cache.decode_step(layer, q[j], k[j], v[j], snn, sout, ws)
             graphs.append(g)
+        kernels_per_step = (cache.kernel_launches() - l0) // n_distinct
         dev_lens.copy_(lens0)
         stream = torch.cuda.current_stream()
         start, stop = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
@@ -394,7 +414,8 @@ def run_graph(w: Workload, cache, steps: int, q, k, v):
     finally:
         cache.lens_from_device()
     ms = start.elapsed_time(stop)
-    return {"ms": ms, "work": sum(w.work(i) for i in range(steps)), "status": status}
+    return {"ms": ms, "work": sum(w.work(i) for i in range(steps)), "status": status,
+            "kernels_per_step": kernels_per_step}
 
 
 def run_e2e(w: Workload, cache, steps: int, q, k, v):
@@ -523,26 +544,33 @@ def main():
                     help="cache storage: bf16, or FP8 E4M3 with one scale per KV head")
     ap.add_argument("--prefill-ragged", action="store_true",
                     help="prefill workload: the ragged final chunk (n_new[b] uniform in 1..512) on the same priors")
+    ap.add_argument("--head-dim", type=int, choices=[64, 128], default=128,
+                    help="decode8b: head dimension of the cache (64: the same shape with 64-wide heads)")
+    ap.add_argument("--no-prefill", action="store_true",
+                    help="decode8b: skip the chunked-prefill objects added to the line")
     args = ap.parse_args()
 
     world = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
     local = int(os.environ.get("LOCAL_RANK", "0"))
     w = Workload(args.workload, verify_t=args.verify_t, verify_g=args.verify_g, kv_dtype=args.kv_dtype,
-                 prefill_ragged=args.prefill_ragged)
-    scale = 1e-12 if w.unit == "TFLOP/s" else 1e-9
+                 prefill_ragged=args.prefill_ragged, head_dim=args.head_dim)
+    # The headline metric has two halves (decode KV-read GB/s; chunked-prefill
+    # attention TFLOP/s): the default decode run also measures both prefill
+    # cases (the full chunk and the ragged final chunk) and reports them as
+    # objects of the same line.
+    extra = []
+    if args.workload == "decode8b" and args.head_dim == 128 and not args.no_prefill:
+        extra = [("prefill", Workload("prefill", kv_dtype=args.kv_dtype)),
+                 ("prefill_ragged_final_chunk", Workload("prefill", kv_dtype=args.kv_dtype, prefill_ragged=True))]
 
     if args.impl == "reference":
         if rank != 0:
             return
-        value, sample, t_total = run_oracle_sample(w)
-        line = {"metric": w.metric, "value": value, "unit": w.unit, "n_gpus": args.gpus, "steps": args.steps,
-                "warmup": args.warmup, "higher_is_better": True, "impl": "reference", "dtype": "f64",
-                "data": "synthetic", "config": w.config(),
-                "cpu_baseline": {"value": value, "unit": w.unit, "cores": 1, "kind": "oracle", "sample": sample,
-                                 "host_cpus": os.cpu_count(), "blas_threads": 1},
-                "e2e": {"value": value, "unit": w.unit, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
-                "vs_baseline": None}
+        line = reference_line(w, args)
+        for key, wx in extra:
+            sub = reference_line(wx, args, cpu_budget_s=6.0)
+            line[key] = {k: sub[k] for k in ("metric", "value", "unit", "config", "cpu_baseline", "e2e")}
         print(json.dumps(line))
         return
 
@@ -552,6 +580,32 @@ def main():
     else:
         torch.cuda.set_device(0)
 
+    line = native_line(w, args, world, rank)
+    for key, wx in extra:
+        sub = native_line(wx, args, world, rank, cpu_budget_s=6.0)
+        line[key] = {k: sub[k] for k in ("metric", "value", "unit", "ms_per_step", "config", "roofline", "e2e",
+                                          "gpu_launches", "clocks", "device_status", "cpu_baseline") if k in sub}
+    if rank == 0:
+        print(json.dumps(line))
+    if world > 1:
+        torch.distributed.destroy_process_group()
+
+
+def reference_line(w: Workload, args, cpu_budget_s: float = 12.0) -> dict:
+    """The oracle arm: the float64 oracle timed on a bounded sample of w, on the host cores."""
+    value, sample, _ = run_oracle_sample(w, cpu_budget_s)
+    return {"metric": w.metric, "value": value, "unit": w.unit, "n_gpus": args.gpus, "steps": args.steps,
+            "warmup": args.warmup, "higher_is_better": True, "impl": "reference", "dtype": "f64",
+            "data": "synthetic", "config": w.config(),
+            "cpu_baseline": {"value": value, "unit": w.unit, "cores": 1, "kind": "oracle", "sample": sample,
+                             "host_cpus": os.cpu_count(), "blas_threads": 1},
+            "e2e": {"value": value, "unit": w.unit, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+            "vs_baseline": None}
+
+
+def native_line(w: Workload, args, world: int, rank: int, cpu_budget_s: float = 12.0) -> dict:
+    """One workload through the library: the bench line's fields for it."""
+    scale = 1e-12 if w.unit == "TFLOP/s" else 1e-9
     res = run_native(w, args.steps, args.warmup, rank, world)
     graph_ms = res["graph"]["ms"] if "graph" in res else 0.0
     ms, e2e_ms, graph_ms = max_over_ranks([res["ms"], res["e2e"]["ms"], graph_ms], world, "cuda")
@@ -559,7 +613,7 @@ def main():
     e2e_value = whole_job_value(res["e2e"]["work"], world, e2e_ms, scale)
 
     hbm, bf16, bf16_sus, peak_kind = _peaks()
-    attn_ms = float(np.mean(res["attn_ms"]))
+    attn_ms = float(res["attn_ms"])
     kb = float(np.mean(res["kernel_bytes"]))
     if w.unit == "TFLOP/s":
         flops = w.work(0)
@@ -570,6 +624,7 @@ def main():
     roof["peak_source"] = f"{peak_kind} (MEASURED_PEAKS.json)" if peak_kind == "measured" else "fallback"
     roof["kernel"] = w.kernel_name
     roof["kernel_ms"] = attn_ms
+    roof["kernel_timing"] = res["kernel_timing"]
     roof["traffic"] = _committed_traffic(w, kb)
 
     line = {
@@ -588,20 +643,19 @@ def main():
     if w.unit == "GB/s":
         line["tokens_per_s"] = w.shape.B * args.steps * world / (ms * 1e-3)
         line["frac_of_hbm_peak"] = value / hbm
+    else:
+        line["frac_of_bf16_peak"] = value / bf16
     if "graph" in res:
         gr = res["graph"]
         line["graph_replay"] = {"value": whole_job_value(gr["work"], world, graph_ms, scale), "unit": w.unit,
-                                "ms_per_step": graph_ms / args.steps, "kernels_per_step": 3 * w.layers,
+                                "ms_per_step": graph_ms / args.steps, "kernels_per_step": gr["kernels_per_step"],
                                 "note": "lengths resident on the device; one CUDA graph replay per step",
                                 "device_status": gr["status"]}
     if rank == 0 and not args.no_cpu_baseline:
-        cv, sample, _ = run_oracle_sample(w)
+        cv, sample, _ = run_oracle_sample(w, cpu_budget_s)
         line["cpu_baseline"] = {"value": cv, "unit": w.unit, "cores": 1, "kind": "oracle", "sample": sample,
                                  "host_cpus": os.cpu_count(), "blas_threads": 1}
-    if rank == 0:
-        print(json.dumps(line))
-    if world > 1:
-        torch.distributed.destroy_process_group()
+    return line
 
 
 def max_over_ranks(times_ms, world: int, device) -> list:
@@ -618,6 +672,21 @@ def whole_job_value(work_per_rank: float, world: int, max_ms: float, scale: floa
     return work_per_rank * world * scale / (max_ms * 1e-3)
 
 
+def _committed_l2(w: Workload) -> str:
+    """The back-to-back L2 measurement of this workload's kernel, if one was taken on the current source."""
+    import hashlib
+
+    path = os.path.join(ROOT, "profiles", f"l2_{w.name}.txt")
+    if w.kv_dtype != "bf16" or w.shape.d != 128 or not os.path.exists(path):
+        return ""
+    kv = dict(line.strip().split("=", 1) for line in open(path) if "=" in line and not line.startswith("#"))
+    src = os.path.join(ROOT, "gqa_attention_preallocated_gb300", "csrc", w.kernel_source)
+    if kv.get("kernel_source_sha256_16") != hashlib.sha256(open(src, "rb").read()).hexdigest()[:16]:
+        return ""
+    return (f"; measured on {kv['launches']} back-to-back launches without cache control: L2 hit rate "
+            f"{kv['lts_hit_rate_pct']} %, DRAM bytes {kv['dram_over_algorithmic']}x the algorithmic bytes")
+
+
 def _committed_traffic(w: Workload, mean_kernel_bytes: float):
     """DRAM bytes per launch from the committed ncu summary, if taken on the current kernel source.
 
@@ -626,7 +695,8 @@ def _committed_traffic(w: Workload, mean_kernel_bytes: float):
     """
     import hashlib
 
-    tag = ("_ragged" if w.ragged else "") + ("_fp8" if w.kv_dtype == "fp8" else "")
+    tag = ("_ragged" if w.ragged else "") + ("_fp8" if w.kv_dtype == "fp8" else "") + \
+        ("_d64" if w.shape.d == 64 else "")
     path = os.path.join(ROOT, "profiles", f"traffic_{w.name}{tag}.txt")
     if not os.path.exists(path):
         return None

@@ -41,6 +41,7 @@ SIGNATURES = [
     ("kvc_gqa_attention_tree", _I, [_VP, _I, _VP, _I, _I, _I32P, _I32P, _VP, _VP, _SZ, _VP]),
     ("kvc_append_attention_tree", _I, [_VP, _I, _VP, _VP, _VP, _I, _I, _I32P, _I32P, _VP, _VP, _SZ, _VP]),
     ("kvc_gqa_attention_noalloc", _I, [_VP, _I, _VP, _I, _I, _I32P, _VP, _VP]),
+    ("kvc_noalloc_status", _I, [_VP, _I32P]),
     ("kvc_set_window", _I, [_VP, _I, _I]),
     ("kvc_truncate", _I, [_VP, _I64P]),
     ("kvc_reset", _I, [_VP]),

@@ -188,15 +188,17 @@ class KVCache:
                               stream=None) -> torch.Tensor:
         """``gqa_attention`` through the allocation-free entry point (library-owned static scratch).
 
-        For callers that cannot allocate device memory; ``out`` must then be
-        passed in.  Shapes whose scratch exceeds the static array are rejected.
+        For callers that cannot allocate device memory, so ``out`` must be
+        passed in: this wrapper allocates nothing either (``out=None`` raises).
+        Shapes whose scratch exceeds the static array are rejected.  Errors of
+        the kernels stay recorded in the scratch until ``noalloc_status``.
         """
         if q.dim() != 4:
             raise KVCError(1, "q must be [B, Hq, T, d]")
         B, Hq, T, d = q.shape
         self._check_tensor(q, (self.B, Hq, T, self.d), "q")
         if out is None:
-            out = torch.empty_like(q)
+            raise KVCError(1, "the allocation-free call takes a caller-owned out tensor (out is None)")
         self._check_tensor(out, q.shape, "out")
         nn = _i32(n_new, self.B)
         check(lib().kvc_gqa_attention_noalloc(self._h, layer, _ptr(q), Hq, T, nn.ctypes.data_as(_I32P), _ptr(out),
@@ -305,6 +307,12 @@ class KVCache:
         if ws is None:
             raise KVCError(7, "no workspace")
         check(lib().kvc_selftest_bounded_wait(_ptr(ws), int(limit_ns), _stream_ptr(self.device, stream)))
+
+    def noalloc_status(self, stream=None) -> int:
+        """Synchronize and read the allocation-free calls' error word (0 = clean); raises on a non-zero code."""
+        code = ctypes.c_int32(0)
+        check(lib().kvc_noalloc_status(_stream_ptr(self.device, stream), ctypes.byref(code)))
+        return code.value
 
     def device_status(self, workspace: torch.Tensor | None = None, stream=None) -> int:
         """Synchronize and read the workspace error word (0 = clean); raises on a non-zero code."""

@@ -11,12 +11,13 @@
 // How (GB300):
 //  * One persistent CTA per SM.  All (unit, 64-key tile) pairs of the call are
 //    numbered and cut into equal contiguous ranges, one per CTA, so ragged row
-//    lengths never leave SMs idle.  A unit finished inside one CTA is written
-//    straight to `out`; a unit whose tiles straddle CTAs leaves one partial
-//    (m, l, O) per CTA, merged by the small combine kernel that follows in the
-//    stream (log-sum-exp merge).  Launches are chained with programmatic
-//    dependent launch, so a kernel's launch and prologue overlap the previous
-//    kernel's tail.
+//    lengths never leave SMs idle.  A unit finished by one writer is written
+//    straight to `out`; otherwise every writer (a CTA, or with warps owning
+//    whole tiles every warp that took some of its tiles) leaves a partial
+//    (m, l, O), merged by the small combine kernel that follows in the stream
+//    (log-sum-exp merge).  Launches are chained with programmatic dependent
+//    launch, so a kernel's launch and prologue overlap the previous kernel's
+//    tail.
 //  * Warp 4 is the producer: one lane streams K and V tiles (64 keys x 128)
 //    through TMA (cp.async.bulk.tensor, 128-byte swizzle) into a ring of
 //    stages guarded by mbarriers.  Each tile is loaded once and serves all G*T
@@ -24,8 +25,9 @@
 //  * Warps 0-3 consume.  With G*T <= 16 rows (decode, short verify) each warp
 //    owns whole tiles in turn (tile i goes to warp i mod 4) and keeps its own
 //    softmax state, so four tiles are in flight at once and each warp runs
-//    eight independent MMA chains per tile; the four states merge at the end
-//    of a unit.  With up to 32 or 64 rows the warps split rows (and keys).
+//    eight independent MMA chains per tile; the warps' states merge in the
+//    combine kernel.  With up to 32 or 64 rows the warps split rows (and
+//    keys).
 //    QK^T and PV run on mma.sync bf16 tiles (16 rows x 8 keys / 8 dims) with
 //    fp32 accumulators; softmax is online in base 2 with log2(e)/sqrt(d)
 //    folded into one scale.
@@ -58,14 +60,14 @@ namespace kvc {
 namespace {
 
 constexpr int kConsumerWarps = 4;  // consumer warps, except FP8 caches with warps owning whole tiles
-constexpr int kD = kHeadDimBf16;
-constexpr int kHalfBytes = kKeyTile * 128;   // 64 keys x 64 dims x 2 B (one swizzled box)
-constexpr int kTileBytes = 2 * kHalfBytes;   // 64 keys x 128 dims
-constexpr int kStageBytes = 2 * kTileBytes;  // K tile + V tile
-constexpr int kPartStride = kD + 4;          // floats per partial row: O[128], m, l, pad
+// Head dimensions: D = 128 (bf16 and FP8 storage) and D = 64 (bf16).  A TMA
+// box is 64 keys x 128 bytes (64 bf16 columns, or 128 E4M3 codes) with the
+// 128-byte swizzle; a bf16 tile of 64 keys is D / 64 boxes.
+constexpr int kHalfBytes = kKeyTile * 128;   // one swizzled box
+// floats per partial row: O[D], m, l, pad
+__host__ __device__ constexpr int part_stride(int D) { return D + 4; }
 constexpr uint64_t kWaitLimitNs = 2000000000ull;
 constexpr float kLazyRescale = 8.0f;  // log2 of the largest factor p may reach above the reference
-constexpr size_t kObufBytes = 3 * 16 * kD * sizeof(float);
 constexpr size_t kMlBytes = kConsumerWarps * 16 * 2 * sizeof(float);
 
 // Compile-time shape of the kernel for MT m-tiles (16 query rows each).
@@ -75,14 +77,17 @@ constexpr size_t kMlBytes = kConsumerWarps * 16 * 2 * sizeof(float);
 // so no shared merge buffer is needed and the ring gets a seventh stage.  With
 // MT = 2 or 4 the warps split every tile and merge their states in shared
 // memory at the end of a unit.
-template <int MT, bool F8>
+template <int MT, bool F8, int D>
 struct Shape {
+    static_assert(D == 128 || (D == 64 && !F8), "head dimensions: 128 (bf16, FP8) and 64 (bf16)");
     static constexpr bool kTilePar = (MT == 1);                // warps own whole tiles
-    // bytes of one K (or V) tile of 64 keys: two 64-column boxes of bf16, or
-    // one 128-byte-row box of E4M3 codes
-    static constexpr int kTileB = F8 ? kKeyTile * 128 : kTileBytes;
+    // bytes of one K (or V) tile of 64 keys: D / 64 boxes of bf16, or one
+    // 128-byte-row box of E4M3 codes
+    static constexpr int kTileB = F8 ? kKeyTile * 128 : kKeyTile * D * 2;
     static constexpr int kStageB = 2 * kTileB;
-    static constexpr int kStages = F8 ? (kTilePar ? 14 : 8) : (kTilePar ? 7 : 4);
+    // as many stages as fit: 224 KB (7 of 32 KB, 14 of 16 KB) with warps owning
+    // tiles, 128 KB beside the shared merge buffers otherwise
+    static constexpr int kStages = (kTilePar ? 229376 : 131072) / kStageB;
     // Consumer warps: with FP8 storage a tile holds half the bytes for the same
     // MMA and conversion work, so one warp per SM sub-partition cannot keep up
     // with HBM; seven tile-owning warps (two per sub-partition, with the
@@ -96,7 +101,7 @@ struct Shape {
     static constexpr int kWays = kTilePar ? kCW : 1;  // partial sub-slots per (unit, CTA)
     static constexpr int kRPB = 16 * MT;
     static constexpr int kEmptyCount = kTilePar ? 1 : kCW;
-    static constexpr size_t kObuf = kTilePar ? 0 : kObufBytes;
+    static constexpr size_t kObuf = kTilePar ? 0 : 3 * 16 * D * sizeof(float);
     static constexpr size_t kMl = kTilePar ? 0 : kMlBytes;
     static constexpr size_t kSmem = 1024 + kStages * kStageB + kObuf + kMl + 2 * kStages * 8 + (kStages + 4) * 4;
     static_assert(kSmem <= 232448, "shared memory per CTA");
@@ -224,11 +229,13 @@ __device__ __forceinline__ bool wait_stage_tag(const volatile int* tag, int it, 
 
 // MT: m-tiles of 16 query rows; DP: the partition comes from a device plan;
 // TREE: draft-tree ancestor masks apply (compiled out otherwise).
-template <int MT, bool DP, bool TREE, bool F8>
-__global__ void __launch_bounds__(Shape<MT, F8>::kThreads, 1)
+template <int MT, bool DP, bool TREE, bool F8, int D>
+__global__ void __launch_bounds__(Shape<MT, F8, D>::kThreads, 1)
     decode_splitkv_bf16_kernel(const __grid_constant__ DecodeParams p, const __grid_constant__ CUtensorMap tmK,
                                const __grid_constant__ CUtensorMap tmV) {
-    using S = Shape<MT, F8>;
+    using S = Shape<MT, F8, D>;
+    constexpr int PS = part_stride(D);
+    constexpr int CPR = D / 8;  // 16-byte chunks of a bf16 row
     constexpr int kStages = S::kStages;
     constexpr int KW = S::kKW;
     constexpr int RPB = S::kRPB;
@@ -286,9 +293,9 @@ __global__ void __launch_bounds__(Shape<MT, F8>::kThreads, 1)
             const int t = row % p.T;
             const int b = row / (p.Hq * p.T);
             if (t >= wp.n_new(b)) {
-                uint4* dst = reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(p.out) + static_cast<size_t>(row) * kD);
+                uint4* dst = reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(p.out) + static_cast<size_t>(row) * D);
 #pragma unroll
-                for (int i = 0; i < kD * 2 / 16; ++i) dst[i] = make_uint4(0u, 0u, 0u, 0u);
+                for (int i = 0; i < CPR; ++i) dst[i] = make_uint4(0u, 0u, 0u, 0u);
             }
         }
     }
@@ -319,10 +326,11 @@ __global__ void __launch_bounds__(Shape<MT, F8>::kThreads, 1)
                     ptx::tma_load_2d(sK, &tmK, 0, row, full);
                     ptx::tma_load_2d(sK + S::kTileB, &tmV, 0, row, full);
                 } else {
-                    ptx::tma_load_2d(sK, &tmK, 0, row, full);
-                    ptx::tma_load_2d(sK + kHalfBytes, &tmK, 64, row, full);
-                    ptx::tma_load_2d(sK + kTileBytes, &tmV, 0, row, full);
-                    ptx::tma_load_2d(sK + kTileBytes + kHalfBytes, &tmV, 64, row, full);
+#pragma unroll
+                    for (int hf = 0; hf < D / 64; ++hf) {  // 64-column boxes of the K and V tiles
+                        ptx::tma_load_2d(sK + hf * kHalfBytes, &tmK, 64 * hf, row, full);
+                        ptx::tma_load_2d(sK + S::kTileB + hf * kHalfBytes, &tmV, 64 * hf, row, full);
+                    }
                 }
                 ++issued;
                 cur.advance(wp);
@@ -352,16 +360,17 @@ __global__ void __launch_bounds__(Shape<MT, F8>::kThreads, 1)
     Cursor<DP> cur;
     cur.init(wp, x0);
 
-    float o[16][4];
+    float o[D / 8][4];
     float m0 = -INFINITY, m1 = -INFINITY, l0 = 0.f, l1 = 0.f;
-    uint32_t qa[8][4];
+    uint32_t qa[D / 16][4];
     int lim0 = -1, lim1 = -1, min_lim = 0, extent = 0, seg_j0 = 0, seg_tiles = 0;
     // Window lower bounds (keys <= lo are outside the window): this thread's
     // two rows, and the largest and smallest over the block's valid rows.
     int lo0 = -1, lo1 = -1, max_lo = -1, min_lo = -1;
     int seg_prior = 0, seg_nn = 0;
     float sl2 = p.scale_log2;  // score scale in base 2 (times the K scale of an FP8 cache)
-    uint4 new_row0 = make_uint4(0u, 0u, 0u, 0u);  // first appended row, lane's 16-byte chunk (K: lanes 0-15, V: 16-31)
+    // first appended row, lane's 16-byte chunk (K: lanes 0 .. CPR-1, V: CPR .. 2*CPR-1)
+    uint4 new_row0 = make_uint4(0u, 0u, 0u, 0u);
 
     for (int x = x0, it = 0; x < x1; ++x, ++it) {
         const int s = it % kStages;
@@ -390,9 +399,9 @@ __global__ void __launch_bounds__(Shape<MT, F8>::kThreads, 1)
             seg_prior = prior;
             seg_nn = nn;
             if constexpr (F8) sl2 = p.scale_log2 * p.kscale[kvh];
-            if (S::kTilePar && p.append_new && nn > 0) {
-                const uint8_t* src = static_cast<const uint8_t*>((lane < 16) ? p.k_new : p.v_new) +
-                                     (static_cast<size_t>(b) * p.Hkv + kvh) * p.Tn * (kD * 2) + (lane & 15) * 16;
+            if (S::kTilePar && p.append_new && nn > 0 && lane < 2 * CPR) {
+                const uint8_t* src = static_cast<const uint8_t*>((lane < CPR) ? p.k_new : p.v_new) +
+                                     (static_cast<size_t>(b) * p.Hkv + kvh) * p.Tn * (D * 2) + (lane % CPR) * 16;
                 new_row0 = __ldg(reinterpret_cast<const uint4*>(src));
             }
 #pragma unroll
@@ -404,7 +413,7 @@ __global__ void __launch_bounds__(Shape<MT, F8>::kThreads, 1)
                     const int g = r / p.T, t = r % p.T;
                     if (t < nn) lim = prior + t;
                     qrow = static_cast<const __nv_bfloat16*>(p.q) +
-                           ((static_cast<size_t>(b) * p.Hq + kvh * p.G + g) * p.T + t) * kD;
+                           ((static_cast<size_t>(b) * p.Hq + kvh * p.G + g) * p.T + t) * D;
                 }
                 if (h == 0) lim0 = lim; else lim1 = lim;
                 const int lo = (p.window > 0 && lim >= 0) ? lim - p.window : -1;
@@ -425,14 +434,14 @@ __global__ void __launch_bounds__(Shape<MT, F8>::kThreads, 1)
                     }
                 } else {
 #pragma unroll
-                    for (int kk = 0; kk < 8; ++kk) {
+                    for (int kk = 0; kk < D / 16; ++kk) {
                         qa[kk][h] = qrow ? *reinterpret_cast<const uint32_t*>(qrow + 16 * kk + 2 * quad) : 0u;
                         qa[kk][2 + h] = qrow ? *reinterpret_cast<const uint32_t*>(qrow + 16 * kk + 8 + 2 * quad) : 0u;
                     }
                 }
             }
 #pragma unroll
-            for (int nb = 0; nb < 16; ++nb) o[nb][0] = o[nb][1] = o[nb][2] = o[nb][3] = 0.f;
+            for (int nb = 0; nb < D / 8; ++nb) o[nb][0] = o[nb][1] = o[nb][2] = o[nb][3] = 0.f;
             m0 = m1 = -INFINITY;
             l0 = l1 = 0.f;
         }
@@ -471,10 +480,13 @@ __global__ void __launch_bounds__(Shape<MT, F8>::kThreads, 1)
                 // the cache (this tile is processed exactly once).
                 const int lo = max(seg_prior, tile0), hi = min(seg_prior + seg_nn, tile0 + kKeyTile);
                 if (lo < hi) {
-                    const int chunk = lane & 15;  // 16-byte chunk of the 256-byte bf16 row
-                    const bool is_v = lane >= 16;
+                    // lanes 0 .. CPR-1 write K, CPR .. 2*CPR-1 V, one 16-byte chunk of
+                    // the bf16 source row each (the rest idle: D = 64)
+                    const int chunk = lane % CPR;
+                    const bool is_v = lane >= CPR;
+                    const int hi_l = (lane < 2 * CPR) ? hi : lo;
                     const size_t unit = static_cast<size_t>(b) * p.Hkv + kvh;
-                    const uint8_t* src = static_cast<const uint8_t*>(is_v ? p.v_new : p.k_new) + unit * p.Tn * (kD * 2);
+                    const uint8_t* src = static_cast<const uint8_t*>(is_v ? p.v_new : p.k_new) + unit * p.Tn * (D * 2);
                     uint8_t* dst = static_cast<uint8_t*>(is_v ? p.v_cache : p.k_cache);
                     bool bad = false;
                     const int row0 = phys_row(p.pg, p.ring, p.Hkv, p.max_len, b, kvh, tile0, &bad) - tile0;  // the tile's rows are contiguous
@@ -483,10 +495,10 @@ __global__ void __launch_bounds__(Shape<MT, F8>::kThreads, 1)
                         // bytes 8*chunk .. of the 128-byte row
                         const float inv = __frcp_rn(is_v ? p.vscale[kvh] : p.kscale[kvh]);
                         uint8_t* stg = stages + s * S::kStageB + (is_v ? S::kTileB : 0);
-                        for (int pos = lo; pos < hi; ++pos) {
+                        for (int pos = lo; pos < hi_l; ++pos) {
                             const int t = pos - seg_prior, r = pos - tile0;
                             const uint4 val = (t == 0) ? new_row0
-                                                       : __ldg(reinterpret_cast<const uint4*>(src + t * (kD * 2) + chunk * 16));
+                                                       : __ldg(reinterpret_cast<const uint4*>(src + t * (D * 2) + chunk * 16));
                             const uint32_t w[4] = {val.x, val.y, val.z, val.w};
                             uint32_t c[4];
 #pragma unroll
@@ -495,16 +507,16 @@ __global__ void __launch_bounds__(Shape<MT, F8>::kThreads, 1)
                                                             __fmul_rn(__uint_as_float(w[i] & 0xFFFF0000u), inv));
                             const uint2 q8 = make_uint2(c[0] | (c[1] << 16), c[2] | (c[3] << 16));
                             *reinterpret_cast<uint2*>(stg + r * 128 + ((((chunk >> 1) ^ (r & 7))) << 4) + (chunk & 1) * 8) = q8;
-                            if (!bad) *reinterpret_cast<uint2*>(dst + static_cast<size_t>(row0 + pos) * kD + chunk * 8) = q8;
+                            if (!bad) *reinterpret_cast<uint2*>(dst + static_cast<size_t>(row0 + pos) * D + chunk * 8) = q8;
                         }
                     } else {
-                        uint8_t* stg = stages + s * S::kStageB + (is_v ? kTileBytes : 0) + (chunk >> 3) * kHalfBytes;
-                        for (int pos = lo; pos < hi; ++pos) {
+                        uint8_t* stg = stages + s * S::kStageB + (is_v ? S::kTileB : 0) + (chunk >> 3) * kHalfBytes;
+                        for (int pos = lo; pos < hi_l; ++pos) {
                             const int t = pos - seg_prior, r = pos - tile0;
                             const uint4 val = (t == 0) ? new_row0
-                                                       : __ldg(reinterpret_cast<const uint4*>(src + t * (kD * 2) + chunk * 16));
+                                                       : __ldg(reinterpret_cast<const uint4*>(src + t * (D * 2) + chunk * 16));
                             *reinterpret_cast<uint4*>(stg + r * 128 + (((chunk & 7) ^ (r & 7)) << 4)) = val;
-                            if (!bad) *reinterpret_cast<uint4*>(dst + static_cast<size_t>(row0 + pos) * (kD * 2) + chunk * 16) = val;
+                            if (!bad) *reinterpret_cast<uint4*>(dst + static_cast<size_t>(row0 + pos) * (D * 2) + chunk * 16) = val;
                         }
                     }
                     ptx::fence_proxy_async_smem();
@@ -520,7 +532,7 @@ __global__ void __launch_bounds__(Shape<MT, F8>::kThreads, 1)
                 uint8_t* vbase = stages + s * S::kStageB + S::kTileB;
                 const int t0 = S::kTilePar ? lane : tid;
                 const int step = S::kTilePar ? 32 : S::kCT;
-                for (int idx = t0; idx < (F8 ? 1 : 2) * per_half; idx += step) {
+                for (int idx = t0; idx < (F8 ? 1 : D / 64) * per_half; idx += step) {
                     const int hf = idx / per_half, rem = idx - hf * per_half;
                     *reinterpret_cast<uint4*>(vbase + hf * kHalfBytes + (vr0 + (rem >> 3)) * 128 + (rem & 7) * 16) =
                         make_uint4(0u, 0u, 0u, 0u);
@@ -536,7 +548,7 @@ __global__ void __launch_bounds__(Shape<MT, F8>::kThreads, 1)
                 uint8_t* vbase = stages + s * S::kStageB + S::kTileB;
                 const int t0 = S::kTilePar ? lane : tid;
                 const int step = S::kTilePar ? 32 : S::kCT;
-                for (int idx = t0; idx < (F8 ? 1 : 2) * per_half; idx += step) {
+                for (int idx = t0; idx < (F8 ? 1 : D / 64) * per_half; idx += step) {
                     const int hf = idx / per_half, rem = idx - hf * per_half;
                     *reinterpret_cast<uint4*>(vbase + hf * kHalfBytes + (rem >> 3) * 128 + (rem & 7) * 16) =
                         make_uint4(0u, 0u, 0u, 0u);
@@ -572,7 +584,7 @@ __global__ void __launch_bounds__(Shape<MT, F8>::kThreads, 1)
                 }
             } else {
 #pragma unroll
-                for (int kk = 0; kk < 8; ++kk) {
+                for (int kk = 0; kk < D / 16; ++kk) {
 #pragma unroll
                     for (int kb = 0; kb < KB; ++kb) {
                         const int mi = lane >> 3;
@@ -626,7 +638,7 @@ __global__ void __launch_bounds__(Shape<MT, F8>::kThreads, 1)
                 l0 *= al0;
                 l1 *= al1;
 #pragma unroll
-                for (int nb = 0; nb < 16; ++nb) {
+                for (int nb = 0; nb < D / 8; ++nb) {
                     o[nb][0] *= al0;
                     o[nb][1] *= al0;
                     o[nb][2] *= al1;
@@ -686,7 +698,7 @@ __global__ void __launch_bounds__(Shape<MT, F8>::kThreads, 1)
                 a[2] = ptx::pack_bf16x2(sc[2 * kb + 1][0], sc[2 * kb + 1][1]);
                 a[3] = ptx::pack_bf16x2(sc[2 * kb + 1][2], sc[2 * kb + 1][3]);
 #pragma unroll
-                for (int dc = 0; dc < 8; ++dc) {
+                for (int dc = 0; dc < D / 16; ++dc) {
                     const int mi = lane >> 3;
                     const int key = koff + kb * 16 + (mi & 1) * 8 + (lane & 7);
                     const int chunk = 2 * dc + (mi >> 1);
@@ -736,31 +748,31 @@ __global__ void __launch_bounds__(Shape<MT, F8>::kThreads, 1)
                 }
                 const float f0 = ptx::ex2(m0 - mfu0), f1 = ptx::ex2(m1 - mfu1);
 #pragma unroll
-                for (int nb = 0; nb < 16; ++nb) {
+                for (int nb = 0; nb < D / 8; ++nb) {
                     o[nb][0] *= f0;
                     o[nb][1] *= f0;
                     o[nb][2] *= f1;
                     o[nb][3] *= f1;
                 }
                 if (ms > 0) {
-                    float* ob = obuf + ((ms - 1) * MT + mt) * 16 * kD;
+                    float* ob = obuf + ((ms - 1) * MT + mt) * 16 * D;
 #pragma unroll
-                    for (int nb = 0; nb < 16; ++nb) {
+                    for (int nb = 0; nb < D / 8; ++nb) {
                         const int col = nb * 8 + 2 * quad;
-                        *reinterpret_cast<float2*>(ob + r0 * kD + col) = make_float2(o[nb][0], o[nb][1]);
-                        *reinterpret_cast<float2*>(ob + (r0 + 8) * kD + col) = make_float2(o[nb][2], o[nb][3]);
+                        *reinterpret_cast<float2*>(ob + r0 * D + col) = make_float2(o[nb][0], o[nb][1]);
+                        *reinterpret_cast<float2*>(ob + (r0 + 8) * D + col) = make_float2(o[nb][2], o[nb][3]);
                     }
                 }
                 ptx::named_barrier_sync(1, S::kCT);
                 if (ms == 0) {
 #pragma unroll
                     for (int k2 = 1; k2 < NM; ++k2) {
-                        const float* ob = obuf + ((k2 - 1) * MT + mt) * 16 * kD;
+                        const float* ob = obuf + ((k2 - 1) * MT + mt) * 16 * D;
 #pragma unroll
-                        for (int nb = 0; nb < 16; ++nb) {
+                        for (int nb = 0; nb < D / 8; ++nb) {
                             const int col = nb * 8 + 2 * quad;
-                            const float2 a = *reinterpret_cast<const float2*>(ob + r0 * kD + col);
-                            const float2 c = *reinterpret_cast<const float2*>(ob + (r0 + 8) * kD + col);
+                            const float2 a = *reinterpret_cast<const float2*>(ob + r0 * D + col);
+                            const float2 c = *reinterpret_cast<const float2*>(ob + (r0 + 8) * D + col);
                             o[nb][0] += a.x;
                             o[nb][1] += a.y;
                             o[nb][2] += c.x;
@@ -783,8 +795,8 @@ __global__ void __launch_bounds__(Shape<MT, F8>::kThreads, 1)
             // otherwise a partial (m, l, O) goes to sub-slot (u + CTA) * ways +
             // warp for the combine kernel.
             const bool writer = S::kTilePar ? (seg_tiles > 0) : (ms == 0);
+            const bool sole = (seg_j0 == 0) && (j == nt - 1) && (!S::kTilePar || nt == 1);
             if (writer) {
-                const bool sole = (seg_j0 == 0) && (j == nt - 1) && (!S::kTilePar || nt == 1);
                 const int slot = (cur.q * p.Hkv + kvh + blockIdx.x) * S::kWays + (S::kTilePar ? warp : 0);
 #pragma unroll
                 for (int h = 0; h < 2; ++h) {
@@ -797,7 +809,7 @@ __global__ void __launch_bounds__(Shape<MT, F8>::kThreads, 1)
                         const int g = r / p.T, t = r % p.T;
                         const float inv = l > 0.f ? (F8 ? p.vscale[kvh] : 1.f) / l : 0.f;
                         __nv_bfloat16* dst = static_cast<__nv_bfloat16*>(p.out) +
-                                             ((static_cast<size_t>(b) * p.Hq + kvh * p.G + g) * p.T + t) * kD;
+                                             ((static_cast<size_t>(b) * p.Hq + kvh * p.G + g) * p.T + t) * D;
                         if constexpr (F8) {
                             // o[jd][2h] is d = 32*quad + jd, o[jd][2h+1] is d = 32*quad + 16 + jd
 #pragma unroll
@@ -812,7 +824,7 @@ __global__ void __launch_bounds__(Shape<MT, F8>::kThreads, 1)
                             }
                         } else {
 #pragma unroll
-                            for (int nb = 0; nb < 16; ++nb) {
+                            for (int nb = 0; nb < D / 8; ++nb) {
                                 const int col = nb * 8 + 2 * quad;
                                 *reinterpret_cast<uint32_t*>(dst + col) =
                                     ptx::pack_bf16x2(o[nb][2 * h] * inv, o[nb][2 * h + 1] * inv);
@@ -821,7 +833,7 @@ __global__ void __launch_bounds__(Shape<MT, F8>::kThreads, 1)
                     } else {
                         // Part of a unit seen by several writers: leave (m, l, O)
                         // for the combine kernel.
-                        float* part = p.partials + (static_cast<size_t>(slot) * p.part_rows + lrow0 + 8 * h) * kPartStride;
+                        float* part = p.partials + (static_cast<size_t>(slot) * p.part_rows + lrow0 + 8 * h) * PS;
                         if constexpr (F8) {
                             // natural column order, V scale applied (the merge is linear in O)
                             const float vs = p.vscale[kvh];
@@ -835,14 +847,14 @@ __global__ void __launch_bounds__(Shape<MT, F8>::kThreads, 1)
                             }
                         } else {
 #pragma unroll
-                            for (int nb = 0; nb < 16; ++nb) {
+                            for (int nb = 0; nb < D / 8; ++nb) {
                                 const int col = nb * 8 + 2 * quad;
                                 *reinterpret_cast<float2*>(part + col) = make_float2(o[nb][2 * h], o[nb][2 * h + 1]);
                             }
                         }
                         if (quad == 0) {
-                            part[kD] = h ? m1 : m0;
-                            part[kD + 1] = l;
+                            part[D] = h ? m1 : m0;
+                            part[D + 1] = l;
                         }
                     }
                 }
@@ -905,8 +917,10 @@ __device__ __forceinline__ int cta_holding(const CPart<DP>& w, int num_ctas, lon
     return lo;
 }
 
-template <bool DP>
+template <bool DP, int D>
 __global__ void __launch_bounds__(kCombineThreads) combine_bf16_kernel(const __grid_constant__ CombineParams p) {
+    constexpr int PS = part_stride(D);
+    constexpr int C4 = D / 4;  // 4-column slices of a row
     ptx::grid_dependency_wait();
     ptx::launch_dependents();
     if (DP && p.dplan->skip) return;
@@ -928,12 +942,12 @@ __global__ void __launch_bounds__(kCombineThreads) combine_bf16_kernel(const __g
     const int ncand = (c1 - c0 + 1) * p.ways;
     const int b = q / p.RB, rb = q - b * p.RB;
     const int nn = cw.n_new(b);
-    for (int idx = threadIdx.x; idx < p.part_rows * (kD / 4); idx += kCombineThreads) {
-        const int lr = idx >> 5, c4 = idx & 31;
+    for (int idx = threadIdx.x; idx < p.part_rows * C4; idx += kCombineThreads) {
+        const int lr = idx / C4, c4 = idx % C4;
         const int r = rb * p.RPB + lr;
         if (r >= p.R || (r % p.T) >= nn) continue;
-        const float* base = p.partials + ((static_cast<size_t>(u + c0) * p.ways) * p.part_rows + lr) * kPartStride;
-        const size_t stride = static_cast<size_t>(p.part_rows) * kPartStride;  // next sub-slot
+        const float* base = p.partials + ((static_cast<size_t>(u + c0) * p.ways) * p.part_rows + lr) * PS;
+        const size_t stride = static_cast<size_t>(p.part_rows) * PS;  // next sub-slot
         // One pass, merging chunks of partials online: (m, l, acc) <- merge.
         float m = -INFINITY, l = 0.f;
         float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
@@ -952,8 +966,8 @@ __global__ void __launch_bounds__(kCombineThreads) combine_bf16_kernel(const __g
                     valid = (lb - la + 1 >= p.ways) || ((w - la % p.ways + p.ways) % p.ways <= lb - la);
                 }
                 const float* part = base + (valid ? e : 0) * stride;
-                mi[k] = valid ? part[kD] : -INFINITY;
-                li[k] = valid ? part[kD + 1] : 0.f;
+                mi[k] = valid ? part[D] : -INFINITY;
+                li[k] = valid ? part[D + 1] : 0.f;
                 oi[k] = valid ? reinterpret_cast<const float4*>(part)[c4] : make_float4(0.f, 0.f, 0.f, 0.f);
             }
 #pragma unroll
@@ -972,7 +986,7 @@ __global__ void __launch_bounds__(kCombineThreads) combine_bf16_kernel(const __g
         const float inv = l > 0.f ? 1.f / l : 0.f;
         const int g = r / p.T, t = r % p.T;
         __nv_bfloat16* dst = static_cast<__nv_bfloat16*>(p.out) +
-                             ((static_cast<size_t>(b) * p.Hq + kvh * p.G + g) * p.T + t) * kD + c4 * 4;
+                             ((static_cast<size_t>(b) * p.Hq + kvh * p.G + g) * p.T + t) * D + c4 * 4;
         store_bf16x4(dst, acc.x * inv, acc.y * inv, acc.z * inv, acc.w * inv);
     }
 }
@@ -1084,19 +1098,19 @@ cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t s
     return cudaLaunchKernelEx(&cfg, kernel, std::forward<Args>(args)...);
 }
 
-template <int MT, bool DP, bool TREE, bool F8>
+template <int MT, bool DP, bool TREE, bool F8, int D>
 cudaError_t launch_mt(const DecodeParams& p, const CUtensorMap& tmK, const CUtensorMap& tmV, int grid,
                       cudaStream_t stream) {
+    using S = Shape<MT, F8, D>;
     static bool attr_set = false;
     if (!attr_set) {
-        cudaError_t e = cudaFuncSetAttribute(decode_splitkv_bf16_kernel<MT, DP, TREE, F8>,
-                                             cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                             static_cast<int>(Shape<MT, F8>::kSmem));
+        cudaError_t e = cudaFuncSetAttribute(decode_splitkv_bf16_kernel<MT, DP, TREE, F8, D>,
+                                             cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(S::kSmem));
         if (e != cudaSuccess) return e;
         attr_set = true;
     }
-    cudaError_t e = launch_pdl(decode_splitkv_bf16_kernel<MT, DP, TREE, F8>, dim3(grid), dim3(Shape<MT, F8>::kThreads),
-                               Shape<MT, F8>::kSmem, stream, p, tmK, tmV);
+    cudaError_t e = launch_pdl(decode_splitkv_bf16_kernel<MT, DP, TREE, F8, D>, dim3(grid), dim3(S::kThreads),
+                               S::kSmem, stream, p, tmK, tmV);
     if (e != cudaSuccess) return e;
     return cudaGetLastError();
 }
@@ -1116,53 +1130,53 @@ __global__ void wait_selftest_kernel(int* err, unsigned long long limit_ns) {
 
 }  // namespace
 
-DecodeLaunch decode_launch_shape(int mt, bool fp8) {
-    if (fp8) {
-        switch (mt) {
-            case 1: return DecodeLaunch{1, Shape<1, true>::kThreads, Shape<1, true>::kSmem, Shape<1, true>::kWays};
-            case 2: return DecodeLaunch{2, Shape<2, true>::kThreads, Shape<2, true>::kSmem, Shape<2, true>::kWays};
-            default: return DecodeLaunch{4, Shape<4, true>::kThreads, Shape<4, true>::kSmem, Shape<4, true>::kWays};
-        }
-    }
+template <bool F8, int D>
+DecodeLaunch launch_shape_t(int mt) {
     switch (mt) {
-        case 1: return DecodeLaunch{1, Shape<1, false>::kThreads, Shape<1, false>::kSmem, Shape<1, false>::kWays};
-        case 2: return DecodeLaunch{2, Shape<2, false>::kThreads, Shape<2, false>::kSmem, Shape<2, false>::kWays};
-        default: return DecodeLaunch{4, Shape<4, false>::kThreads, Shape<4, false>::kSmem, Shape<4, false>::kWays};
+        case 1: return DecodeLaunch{1, Shape<1, F8, D>::kThreads, Shape<1, F8, D>::kSmem, Shape<1, F8, D>::kWays};
+        case 2: return DecodeLaunch{2, Shape<2, F8, D>::kThreads, Shape<2, F8, D>::kSmem, Shape<2, F8, D>::kWays};
+        default: return DecodeLaunch{4, Shape<4, F8, D>::kThreads, Shape<4, F8, D>::kSmem, Shape<4, F8, D>::kWays};
     }
 }
 
-template <bool F8>
+DecodeLaunch decode_launch_shape(int mt, bool fp8, int d) {
+    if (fp8) return launch_shape_t<true, 128>(mt);
+    return d == 64 ? launch_shape_t<false, 64>(mt) : launch_shape_t<false, 128>(mt);
+}
+
+template <bool F8, int D>
 cudaError_t launch_decode_t(const DecodeParams& p, const CUtensorMap& tmK, const CUtensorMap& tmV, int mt, int grid,
                             cudaStream_t stream) {
     if (p.dplan)
-        return (mt == 1 && !p.anc) ? launch_mt<1, true, false, F8>(p, tmK, tmV, grid, stream) : cudaErrorInvalidValue;
+        return (mt == 1 && !p.anc) ? launch_mt<1, true, false, F8, D>(p, tmK, tmV, grid, stream) : cudaErrorInvalidValue;
     if (p.anc) {
         switch (mt) {
-            case 1: return launch_mt<1, false, true, F8>(p, tmK, tmV, grid, stream);
-            case 2: return launch_mt<2, false, true, F8>(p, tmK, tmV, grid, stream);
-            case 4: return launch_mt<4, false, true, F8>(p, tmK, tmV, grid, stream);
+            case 1: return launch_mt<1, false, true, F8, D>(p, tmK, tmV, grid, stream);
+            case 2: return launch_mt<2, false, true, F8, D>(p, tmK, tmV, grid, stream);
+            case 4: return launch_mt<4, false, true, F8, D>(p, tmK, tmV, grid, stream);
             default: return cudaErrorInvalidValue;
         }
     }
     switch (mt) {
-        case 1: return launch_mt<1, false, false, F8>(p, tmK, tmV, grid, stream);
-        case 2: return launch_mt<2, false, false, F8>(p, tmK, tmV, grid, stream);
-        case 4: return launch_mt<4, false, false, F8>(p, tmK, tmV, grid, stream);
+        case 1: return launch_mt<1, false, false, F8, D>(p, tmK, tmV, grid, stream);
+        case 2: return launch_mt<2, false, false, F8, D>(p, tmK, tmV, grid, stream);
+        case 4: return launch_mt<4, false, false, F8, D>(p, tmK, tmV, grid, stream);
         default: return cudaErrorInvalidValue;
     }
 }
 
 cudaError_t launch_decode_bf16(const DecodeParams& p, const CUtensorMap& tmK, const CUtensorMap& tmV, int mt,
-                               int grid, bool fp8, cudaStream_t stream) {
-    return fp8 ? launch_decode_t<true>(p, tmK, tmV, mt, grid, stream)
-               : launch_decode_t<false>(p, tmK, tmV, mt, grid, stream);
+                               int grid, bool fp8, int d, cudaStream_t stream) {
+    if (fp8) return d == 128 ? launch_decode_t<true, 128>(p, tmK, tmV, mt, grid, stream) : cudaErrorInvalidValue;
+    if (d == 64) return launch_decode_t<false, 64>(p, tmK, tmV, mt, grid, stream);
+    return d == 128 ? launch_decode_t<false, 128>(p, tmK, tmV, mt, grid, stream) : cudaErrorInvalidValue;
 }
 
 cudaError_t launch_combine_bf16(const CombineParams& p, cudaStream_t stream) {
-    cudaError_t e = p.dplan ? launch_pdl(combine_bf16_kernel<true>, dim3(p.NB * p.Hkv), dim3(kCombineThreads), 0,
-                                         stream, p)
-                            : launch_pdl(combine_bf16_kernel<false>, dim3(p.NB * p.Hkv), dim3(kCombineThreads), 0,
-                                         stream, p);
+    if (p.d != 64 && p.d != 128) return cudaErrorInvalidValue;
+    auto k = p.dplan ? (p.d == 64 ? combine_bf16_kernel<true, 64> : combine_bf16_kernel<true, 128>)
+                     : (p.d == 64 ? combine_bf16_kernel<false, 64> : combine_bf16_kernel<false, 128>);
+    cudaError_t e = launch_pdl(k, dim3(p.NB * p.Hkv), dim3(kCombineThreads), 0, stream, p);
     if (e != cudaSuccess) return e;
     return cudaGetLastError();
 }

@@ -70,10 +70,17 @@ namespace {
 constexpr int kTcMinRows = 12;
 constexpr int kTcMinRowsFp8 = 16;
 int tc_min_rows(const kvc_cache* c) { return c->dtype == KVC_FP8_E4M3 ? kTcMinRowsFp8 : kTcMinRows; }
-// Caches served by the generic kernel (attn_f32.cu): fp32 storage, and bf16
-// or FP8 storage whose head dimension is not the 128 that the TMA /
-// tensor-core kernels are built for.
-bool generic_path(const kvc_cache* c) { return c->dtype == KVC_F32 || c->d != kHeadDimBf16; }
+// Caches served by the generic kernel (attn_f32.cu) only: fp32 storage, and
+// bf16 or FP8 storage whose head dimension has no TMA kernel (the split-KV
+// kernel takes d = 128, and d = 64 for bf16; the tensor-core kernel d = 128).
+bool generic_path(const kvc_cache* c) {
+    return c->dtype == KVC_F32 || !(c->d == kHeadDimBf16 || (c->d == kHeadDimSmall && c->dtype == KVC_BF16));
+}
+// Head dimension the tensor-core kernel is built for.
+bool tc_capable(const kvc_cache* c) { return !generic_path(c) && c->d == kHeadDimBf16; }
+// Calls with more query rows per KV head than the split-KV kernel's 64 on a
+// cache the tensor-core kernel cannot take (bf16, d = 64) run on the generic kernel.
+bool generic_call(const kvc_cache* c, int R) { return generic_path(c) || (!tc_capable(c) && R > 64); }
 constexpr int kTcMaxLen = 0xFFFF * 128;  // key tiles of a piece are packed in 16 bits
 
 thread_local std::string g_last_error;
@@ -142,11 +149,12 @@ kvc_status ensure_device(kvc_cache* c) {
 
 // 2-D view [rows, 128 values] with boxes of box_rows rows x 128 bytes (64
 // bf16 columns, or all 128 one-byte E4M3 columns) and the 128-byte swizzle.
-kvc_status encode_rows_map(CUtensorMap* m, const void* base, cuuint64_t rows, cuuint32_t box_rows, bool fp8 = false) {
+kvc_status encode_rows_map(CUtensorMap* m, const void* base, cuuint64_t rows, cuuint32_t box_rows, bool fp8 = false,
+                           int d = kHeadDimBf16) {
     EncodeTiledFn fn = encode_fn();
     if (!fn) return fail(KVC_ERR_CUDA, "cuTensorMapEncodeTiled unavailable");
-    cuuint64_t dims[2] = {static_cast<cuuint64_t>(kHeadDimBf16), rows};
-    cuuint64_t strides[1] = {static_cast<cuuint64_t>(kHeadDimBf16) * (fp8 ? 1 : 2)};
+    cuuint64_t dims[2] = {static_cast<cuuint64_t>(d), rows};
+    cuuint64_t strides[1] = {static_cast<cuuint64_t>(d) * (fp8 ? 1 : 2)};
     cuuint32_t box[2] = {fp8 ? 128u : 64u, box_rows};
     cuuint32_t estr[2] = {1, 1};
     CUresult r = fn(m, fp8 ? CU_TENSOR_MAP_DATA_TYPE_UINT8 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base),
@@ -164,10 +172,12 @@ kvc_status encode_layer_maps(kvc_cache* c, int layer) {
                                         : static_cast<cuuint64_t>(c->B) * c->Hkv * c->max_len;
     kvc_status s;
     const bool fp8 = c->dtype == KVC_FP8_E4M3;
-    if ((s = encode_rows_map(&c->tmK[layer], c->k[layer], rows, kKeyTile, fp8))) return s;
-    if ((s = encode_rows_map(&c->tmV[layer], c->v[layer], rows, kKeyTile, fp8))) return s;
-    if ((s = encode_rows_map(&c->tmK128[layer], c->k[layer], rows, 128, fp8))) return s;
-    if ((s = encode_rows_map(&c->tmV128[layer], c->v[layer], rows, 128, fp8))) return s;
+    if ((s = encode_rows_map(&c->tmK[layer], c->k[layer], rows, kKeyTile, fp8, c->d))) return s;
+    if ((s = encode_rows_map(&c->tmV[layer], c->v[layer], rows, kKeyTile, fp8, c->d))) return s;
+    if (tc_capable(c)) {
+        if ((s = encode_rows_map(&c->tmK128[layer], c->k[layer], rows, 128, fp8))) return s;
+        if ((s = encode_rows_map(&c->tmV128[layer], c->v[layer], rows, 128, fp8))) return s;
+    }
     c->tm_ready[layer] = 1;
     return ok();
 }
@@ -218,6 +228,7 @@ kvc_status validate_append(const kvc_cache* c, int layer, const void* k_new, con
 }
 
 struct AttnPlan {
+    bool generic = false;  // the call runs on the generic kernel
     int Hq = 0, G = 0, T = 0, R = 0;
     int mt = 0, RPB = 0, RB = 0, NB = 0, units = 0, ways = 1, part_rows = 0;
     int splits = 1;  // generic kernel: CTAs per (row block, KV head, row)
@@ -239,7 +250,8 @@ kvc_status plan_shape(const kvc_cache* c, int Hq, int T, int num_ctas, AttnPlan*
     const long long R = static_cast<long long>(pl->G) * T;
     if (R > (1ll << 30)) return fail(KVC_ERR_ARG, "G * T too large");
     pl->R = static_cast<int>(R);
-    if (!generic_path(c)) {
+    pl->generic = generic_call(c, pl->R);
+    if (!pl->generic) {
         pl->mt = pl->R <= 16 ? 1 : (pl->R <= 32 ? 2 : 4);
         pl->RPB = 16 * pl->mt;
         pl->RB = std::max(1, (pl->R + pl->RPB - 1) / pl->RPB);
@@ -247,7 +259,7 @@ kvc_status plan_shape(const kvc_cache* c, int Hq, int T, int num_ctas, AttnPlan*
         // with more than 64 rows per KV head (more than any tree call takes)
         // always runs on the tensor cores, unless the cache is too long for
         // them; it plans no groups and needs no split-KV partials.
-        const bool tc_only = pl->R > 64 && c->max_len <= kTcMaxLen;
+        const bool tc_only = pl->R > 64 && c->max_len <= kTcMaxLen && tc_capable(c);
         const long long NB = tc_only ? 0 : static_cast<long long>(c->B) * pl->RB;
         if (NB > kMaxGroups)
             return fail(KVC_ERR_ARG, "B * ceil(G*T / %d) = %lld exceeds %d row blocks", pl->RPB, NB, kMaxGroups);
@@ -260,13 +272,13 @@ kvc_status plan_shape(const kvc_cache* c, int Hq, int T, int num_ctas, AttnPlan*
         // device-computed plans of resident-length steps, then the ancestor
         // masks of a tree-verify call
         pl->ws_plan = round_up(sizeof(DevicePlan), 256) + round_up(kMaxTreeQueries * sizeof(uint64_t), 256);
-        pl->ways = decode_launch_shape(pl->mt, c->dtype == KVC_FP8_E4M3).ways;
+        pl->ways = decode_launch_shape(pl->mt, c->dtype == KVC_FP8_E4M3, c->d).ways;
         pl->part_rows = std::min(pl->R, pl->RPB);
         pl->ws_partials = tc_only ? 0
                                   : static_cast<size_t>(pl->units + num_ctas) * pl->ways * pl->part_rows *
-                                        (kHeadDimBf16 + 4) * sizeof(float);
+                                        (c->d + 4) * sizeof(float);
         pl->ws_min = pl->ws_err + pl->ws_plan + pl->ws_partials;
-        if (pl->R > tc_min_rows(c)) {
+        if (pl->R > tc_min_rows(c) && tc_capable(c)) {
             // The tensor-core kernel: up to two partial slots (2 row tiles x
             // 128 rows x (d + 4) floats) per SM share boundary.
             const size_t prefill = static_cast<size_t>(2) * std::min(num_ctas, kMaxCtas) * 2 * 128 *
@@ -371,7 +383,7 @@ kvc_status do_attention(kvc_cache* c, int layer, const void* q, const AttnPlan& 
     if (main_enqueued) *main_enqueued = false;
     const int64_t* lens = c->lens.data() + static_cast<size_t>(layer) * c->B;
     if (c->B == 0 || pl.T == 0) return ok();
-    if (generic_path(c)) {
+    if (pl.generic) {
         static_assert(sizeof(F32Params) < 32000, "kernel parameter block too large");
         F32Params p;
         p.q = q;
@@ -421,7 +433,7 @@ kvc_status do_attention(kvc_cache* c, int layer, const void* q, const AttnPlan& 
 
     kvc_status s = encode_layer_maps(c, layer);
     if (s) return s;
-    if (pl.R > tc_min_rows(c) && k_new == nullptr && anc == nullptr && c->max_len <= kTcMaxLen) {
+    if (pl.R > tc_min_rows(c) && k_new == nullptr && anc == nullptr && c->max_len <= kTcMaxLen && tc_capable(c)) {
         // Many query rows per KV head: tensor-core kernel, one CTA per piece.
         // Work items are (b, kvh, row block, pair of 128-row tiles): with
         // T >= 128, 128 positions of two query heads (mode 0); with T < 128 the
@@ -711,7 +723,7 @@ kvc_status do_attention(kvc_cache* c, int layer, const void* q, const AttnPlan& 
         c->last_ws = ws;
     }
     cudaError_t e =
-        launch_decode_bf16(p, c->tmK[layer], c->tmV[layer], pl.mt, grid, c->dtype == KVC_FP8_E4M3, stream);
+        launch_decode_bf16(p, c->tmK[layer], c->tmV[layer], pl.mt, grid, c->dtype == KVC_FP8_E4M3, c->d, stream);
     if (e != cudaSuccess) return cuda_fail(e, "split-KV attention launch");
     ++c->launches;
     if (main_enqueued) *main_enqueued = true;
@@ -721,6 +733,7 @@ kvc_status do_attention(kvc_cache* c, int layer, const void* q, const AttnPlan& 
         cp.dplan = nullptr;
         cp.partials = p.partials;
         cp.out = out;
+        cp.d = c->d;
         cp.Hq = pl.Hq;
         cp.Hkv = c->Hkv;
         cp.G = pl.G;
@@ -753,11 +766,37 @@ kvc_status check_workspace(const kvc_cache* c, const AttnPlan& pl, const void* w
     return ok();
 }
 
+// Copy a workspace's error word to *code after the stream's work, clear it
+// when set, and map the code to a status.
+kvc_status read_error_word(void* word, cudaStream_t st, int32_t* code) {
+    *code = 0;
+    int32_t v = 0;
+    cudaError_t e = cudaMemcpyAsync(&v, word, sizeof v, cudaMemcpyDeviceToHost, st);
+    if (e == cudaSuccess) e = cudaStreamSynchronize(st);
+    if (e != cudaSuccess) return cuda_fail(e, "reading the device error word");
+    *code = v;
+    if (v != 0) {
+        e = cudaMemsetAsync(word, 0, sizeof v, st);
+        if (e == cudaSuccess) e = cudaStreamSynchronize(st);
+        if (e != cudaSuccess) return cuda_fail(e, "clearing the device error word");
+        if (v == kDevOverflow)
+            return fail(KVC_ERR_OVERFLOW, "a device-resident step was rejected: a row would pass max_len or n_new "
+                                          "was outside 0..T (nothing was written, lengths unchanged)");
+        if (v == kDevBadPage)
+            return fail(KVC_ERR_ARG, "a block-table entry under an attended or appended position was outside "
+                                     "0..num_pages-1 (not dereferenced; the call's output is not valid)");
+        return fail(KVC_ERR_DEVICE_TIMEOUT, "a kernel's bounded wait expired (code %d)", v);
+    }
+    return ok();
+}
+
 }  // namespace
 
 // ===========================================================================
 // C ABI
 // ===========================================================================
+
+
 
 // Ancestor masks of a draft tree ("Write the causal mask for a decode
 // step...", "What interviewers probe next": tree-based speculative decoding):
@@ -772,7 +811,7 @@ kvc_status tree_masks(const kvc_cache* c, const AttnPlan& pl, const int32_t* n_n
         return fail(KVC_ERR_SHAPE, "B * T = %lld draft tokens exceed %d", static_cast<long long>(c->B) * pl.T,
                     kMaxTreeQueries);
     if (c->window > 0 || c->ring) return fail(KVC_ERR_ARG, "a draft tree does not combine with a window");
-    if (!generic_path(c) && pl.R > 64)
+    if (tc_capable(c) && pl.R > 64)
         return fail(KVC_ERR_SHAPE, "a bf16 / fp8 draft tree takes G * T <= 64 query rows per KV head (G * T = %d)", pl.R);
     anc->assign(static_cast<size_t>(c->B) * pl.T, 0);
     for (int b = 0; b < c->B; ++b)
@@ -869,6 +908,9 @@ kvc_status kvc_create_paged(kvc_cache** out, int layers, int batch, int kv_heads
     if (dtype != KVC_F32 && head_dim == kHeadDimBf16 && page_size % 128 != 0)
         return fail(KVC_ERR_ARG, "bf16 and fp8 pages of head_dim %d hold a multiple of 128 tokens (key tiles never cross a page)",
                     kHeadDimBf16);
+    if (dtype == KVC_BF16 && head_dim == kHeadDimSmall && page_size % kKeyTile != 0)
+        return fail(KVC_ERR_ARG, "bf16 pages of head_dim %d hold a multiple of %d tokens (key tiles never cross a page)",
+                    kHeadDimSmall, kKeyTile);
     if (batch > 0 && !block_table) return fail(KVC_ERR_ARG, "block_table is null");
     if ((reinterpret_cast<uintptr_t>(block_table) & 3u) != 0) return fail(KVC_ERR_ARG, "block_table not 4-byte aligned");
     const long long cap = static_cast<long long>(max_pages_per_row) * page_size;
@@ -980,7 +1022,7 @@ static kvc_status append_attention_impl(kvc_cache* c, int layer, const void* q, 
     if (s) return s;
     cudaStream_t st = static_cast<cudaStream_t>(stream);
     int64_t* lw = c->lens.data() + static_cast<size_t>(layer) * c->B;
-    if (!generic_path(c) && pl.mt == 1 && max_n > 0 && pl.R <= tc_min_rows(c)) {
+    if (!pl.generic && pl.mt == 1 && max_n > 0 && (pl.R <= tc_min_rows(c) || !tc_capable(c))) {
         // Warps own whole tiles: the attention kernel writes the new rows into
         // the cache itself (one launch instead of two).
         for (int b = 0; b < c->B; ++b) lw[b] += n_new[b];
@@ -1103,27 +1145,10 @@ kvc_status kvc_get_lens(const kvc_cache* c, int layer, int64_t* out) {
 
 kvc_status kvc_device_status(kvc_cache* c, void* workspace, void* stream, int32_t* code) {
     if (!c || !workspace || !code) return fail(KVC_ERR_ARG, "null argument");
-    cudaStream_t st = static_cast<cudaStream_t>(stream);
-    int32_t v = 0;
-    cudaError_t e = cudaMemcpyAsync(&v, workspace, sizeof v, cudaMemcpyDeviceToHost, st);
-    if (e == cudaSuccess) e = cudaStreamSynchronize(st);
-    if (e != cudaSuccess) return cuda_fail(e, "reading the device error word");
-    *code = v;
-    if (v != 0) {
-        // Make the next call on this handle clear the workspace header again.
-        c->last_ws = nullptr;
-        e = cudaMemsetAsync(workspace, 0, sizeof v, st);
-        if (e == cudaSuccess) e = cudaStreamSynchronize(st);
-        if (e != cudaSuccess) return cuda_fail(e, "clearing the device error word");
-        if (v == kDevOverflow)
-            return fail(KVC_ERR_OVERFLOW, "a device-resident step was rejected: a row would pass max_len or n_new "
-                                          "was outside 0..T (nothing was written, lengths unchanged)");
-        if (v == kDevBadPage)
-            return fail(KVC_ERR_ARG, "a block-table entry under an attended or appended position was outside "
-                                     "0..num_pages-1 (not dereferenced; the call's output is not valid)");
-        return fail(KVC_ERR_DEVICE_TIMEOUT, "a kernel's bounded wait expired (code %d)", v);
-    }
-    return ok();
+    kvc_status s = read_error_word(workspace, static_cast<cudaStream_t>(stream), code);
+    // After an error, make the next call on this handle clear the workspace header again.
+    if (*code != 0) c->last_ws = nullptr;
+    return s;
 }
 
 kvc_status kvc_selftest_bounded_wait(void* workspace, uint64_t limit_ns, void* stream) {
@@ -1142,8 +1167,9 @@ kvc_status kvc_set_window(kvc_cache* c, int window, int ring) {
     if (ring) {
         if (c->pg.table) return fail(KVC_ERR_ARG, "a paged cache cannot also be a ring");
         if (window < 1 || window > c->max_len) return fail(KVC_ERR_ARG, "a ring cache needs a window of 1..max_len");
-        if (!generic_path(c) && c->max_len % 128 != 0)
-            return fail(KVC_ERR_ARG, "a bf16 ring cache needs max_len %% 128 == 0 (key tiles never wrap)");
+        const int tile = tc_capable(c) ? 128 : kKeyTile;  // the largest key tile any kernel of this cache reads
+        if (!generic_path(c) && c->max_len % tile != 0)
+            return fail(KVC_ERR_ARG, "this ring cache needs max_len %% %d == 0 (key tiles never wrap)", tile);
     }
     if ((ring != 0) != c->ring)
         for (int64_t L : c->lens)
@@ -1205,7 +1231,8 @@ kvc_status kvc_decode_step(kvc_cache* c, int layer, const void* q, const void* k
     if (s) return s;
     if (!c->lens_on_device) return fail(KVC_ERR_ARG, "the lengths are on the host: call kvc_lens_to_device first");
     if (generic_path(c))
-        return fail(KVC_ERR_ARG, "device-resident steps serve bf16 and fp8 caches of head_dim %d only", kHeadDimBf16);
+        return fail(KVC_ERR_ARG, "device-resident steps serve bf16 and fp8 caches of head_dim %d and bf16 caches of "
+                                 "head_dim %d only", kHeadDimBf16, kHeadDimSmall);
     if (c->B == 0 || T == 0) return ok();
     if (T < 0) return fail(KVC_ERR_ARG, "T = %d < 0", T);
     if (!q || !k_new || !v_new || !out || !n_new_dev) return fail(KVC_ERR_ARG, "null pointer argument");
@@ -1286,7 +1313,7 @@ kvc_status kvc_decode_step(kvc_cache* c, int layer, const void* q, const void* k
     p.ring = c->ring ? 1 : 0;
     p.pg = c->pg;
     set_decode_scales(c, layer, &p);
-    e = launch_decode_bf16(p, c->tmK[layer], c->tmV[layer], 1, grid, c->dtype == KVC_FP8_E4M3, st);
+    e = launch_decode_bf16(p, c->tmK[layer], c->tmV[layer], 1, grid, c->dtype == KVC_FP8_E4M3, c->d, st);
     if (e != cudaSuccess) return cuda_fail(e, "split-KV attention launch");
     ++c->launches;
 
@@ -1295,6 +1322,7 @@ kvc_status kvc_decode_step(kvc_cache* c, int layer, const void* q, const void* k
     cp.dplan = plan;
     cp.partials = p.partials;
     cp.out = out;
+    cp.d = c->d;
     cp.Hq = pl.Hq;
     cp.Hkv = c->Hkv;
     cp.G = pl.G;
@@ -1364,8 +1392,8 @@ extern "C" kvc_status kvc_gqa_attention_noalloc(kvc_cache* c, int layer, const v
     kvc_status s = check_layer(c, layer);
     if (s) return s;
     if (generic_path(c))
-        return fail(KVC_ERR_ARG, "the allocation-free variant serves bf16 and fp8 caches of head_dim %d only",
-                    kHeadDimBf16);
+        return fail(KVC_ERR_ARG, "the allocation-free variant serves bf16 and fp8 caches of head_dim %d and bf16 "
+                                 "caches of head_dim %d only", kHeadDimBf16, kHeadDimSmall);
     AttnPlan pl;
     const int64_t* lens = c->lens.data() + static_cast<size_t>(layer) * c->B;
     s = validate_attention(c, layer, q, q_heads, T, n_new, out, lens, &pl, 0);
@@ -1379,6 +1407,9 @@ extern "C" kvc_status kvc_gqa_attention_noalloc(kvc_cache* c, int layer, const v
     if (dev != c->device) return fail(KVC_ERR_ARG, "current device %d is not the cache's device %d", dev, c->device);
     s = plan_shape(c, q_heads, T, c->num_sms, &pl);
     if (s) return s;
+    if (pl.generic)
+        return fail(KVC_ERR_ARG, "the allocation-free variant takes at most 64 query rows per KV head on a cache of "
+                                 "head_dim %d (G * T = %d)", kHeadDimSmall, pl.R);
     if (pl.ws_min > static_cast<size_t>(KVC_NOALLOC_SCRATCH_BYTES))
         return fail(KVC_ERR_WORKSPACE, "this call needs %zu bytes of scratch; the static scratch holds %zu",
                     pl.ws_min, static_cast<size_t>(KVC_NOALLOC_SCRATCH_BYTES));
@@ -1386,10 +1417,23 @@ extern "C" kvc_status kvc_gqa_attention_noalloc(kvc_cache* c, int layer, const v
     s = noalloc_scratch_address(dev, &scratch);
     if (s) return s;
     cudaStream_t st = static_cast<cudaStream_t>(stream);
-    // The array keeps whatever the previous call left: zero the header (error
-    // word and merge counters), the one part the kernels need to start at zero.
-    e = cudaMemsetAsync(scratch, 0, pl.ws_err, st);
+    // The array keeps whatever the previous call left: zero the merge
+    // counters, the part the kernels need to start at zero.  The error word
+    // is left alone, so an error stays recorded until kvc_noalloc_status
+    // reads and clears it.
+    e = cudaMemsetAsync(static_cast<uint8_t*>(scratch) + kWsCounterOffset, 0, pl.ws_err - kWsCounterOffset, st);
     if (e != cudaSuccess) return cuda_fail(e, "cudaMemsetAsync(static scratch)");
     c->last_ws = scratch;
     return do_attention(c, layer, q, pl, n_new, out, scratch, KVC_NOALLOC_SCRATCH_BYTES, st);
+}
+
+extern "C" kvc_status kvc_noalloc_status(void* stream, int32_t* code) {
+    if (!code) return fail(KVC_ERR_ARG, "null argument");
+    int dev = -1;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaGetDevice");
+    void* scratch = nullptr;
+    kvc_status s = noalloc_scratch_address(dev, &scratch);
+    if (s) return s;
+    return read_error_word(scratch, static_cast<cudaStream_t>(stream), code);
 }

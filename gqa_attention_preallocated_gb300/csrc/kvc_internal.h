@@ -34,9 +34,12 @@ __host__ __device__ __forceinline__ int phys_row(const Paging& pg, int ring, int
     return (b * Hkv + kvh) * max_len + (ring ? a % max_len : a);
 }
 
-// Keys per K/V tile of the split-KV kernel, and the head width it is built for.
+// Keys per K/V tile of the split-KV kernel, and the head width the TMA /
+// tensor-core kernels are built for (the split-KV kernel also takes bf16
+// storage of head width kHeadDimSmall).
 constexpr int kKeyTile = 64;
 constexpr int kHeadDimBf16 = 128;
+constexpr int kHeadDimSmall = 64;
 // FP8 E4M3 caches: one K and one V scale per KV head (at most this many heads).
 constexpr int kMaxScaleHeads = 64;
 
@@ -152,6 +155,7 @@ struct CombineParams {
     const DevicePlan* dplan;  // when set, n_new / gstart / cta_start / total_tiles come from it
     const float* partials;
     void* out;
+    int d;  // head dimension: 128 or 64
     int Hq, Hkv, G, T, R, RPB, RB, NB;
     int ways;       // partial sub-slots per (unit, CTA)
     int part_rows;  // rows stored per partial sub-slot
@@ -170,10 +174,11 @@ struct DecodeLaunch {
     size_t smem_bytes;
     int ways;  // partial sub-slots per (unit, CTA): 4 when warps own whole tiles
 };
-DecodeLaunch decode_launch_shape(int mt, bool fp8);
+// d: the head dimension (128 for bf16 and FP8 storage, or 64 for bf16).
+DecodeLaunch decode_launch_shape(int mt, bool fp8, int d);
 
 cudaError_t launch_decode_bf16(const DecodeParams& p, const CUtensorMap& tmK, const CUtensorMap& tmV, int mt,
-                               int grid, bool fp8, cudaStream_t stream);
+                               int grid, bool fp8, int d, cudaStream_t stream);
 
 // ---------------------------------------------------------------------------
 // f32 attention (any d <= 256, d % 4 == 0): one CTA per (16-row block, kvh, b),

@@ -230,13 +230,28 @@ kvc_status kvc_append_attention_tree(kvc_cache* c, int layer, const void* q, con
  *
  * The first call on each device looks up the array's device address
  * (cudaGetSymbolAddress, with that device current) and caches it; make that
- * first call before any stream capture.  Every call on a device shares the
- * one array, which keeps the last call's contents; each call clears the
- * part that must start at zero (the error word).  Calls that overlap on the GPU (different
+ * first call before any stream capture.  The cached address belongs to the
+ * device's current context: after cudaDeviceReset it is stale, like every
+ * kvc handle and device buffer of that context, so a process that resets a
+ * device must not call this entry point again.  Every call on a device
+ * shares the one array, which keeps the last call's contents; each call
+ * clears the part that must start at zero (the merge counters).  The
+ * array's error word is not cleared by a call: a kernel's error (an expired
+ * bounded wait, a bad block-table entry) stays recorded until
+ * kvc_noalloc_status reads it.  Calls that overlap on the GPU (different
  * streams, or several caches at once) race on the array: order them on one
  * stream.  The device must be the cache's device (else KVC_ERR_ARG). */
 kvc_status kvc_gqa_attention_noalloc(kvc_cache* c, int layer, const void* q, int q_heads, int T,
                                      const int32_t* n_new, void* out, void* stream);
+
+/* kvc_device_status for the static scratch of kvc_gqa_attention_noalloc on
+ * the current device: synchronizes `stream`, stores the scratch's error word
+ * in *code (0 = every allocation-free call since the last read ran clean)
+ * and clears it, and returns the same statuses as kvc_device_status
+ * (KVC_ERR_DEVICE_TIMEOUT, KVC_ERR_OVERFLOW, or KVC_ERR_ARG for a block-table
+ * entry outside 0 .. num_pages - 1).  Allocates nothing.  The pages have no
+ * counterpart of this call. */
+kvc_status kvc_noalloc_status(void* stream, int32_t* code);
 
 /* Sliding window and ring storage ("Write the causal mask for a decode step
  * with a KV cache...", "A strong answer", last paragraph, and "Common

@@ -193,12 +193,15 @@ def test_workspace_query_without_gpu_or_for_f32(L):
     assert L.kvc_workspace_bytes(h, 4, 1) == 0  # the f32 path needs no workspace
     L.kvc_destroy(h)
     assert L.kvc_workspace_bytes(None, 4, 1) == 0
-    st, h = _create(L, d=64, dtype=_lib.KVC_BF16)  # bf16 of d != 128: the generic kernel
+    st, h = _create(L, d=96, dtype=_lib.KVC_BF16)  # bf16 of d other than 64 and 128: the generic kernel
     assert st == 0
     assert L.kvc_workspace_bytes(h, 4, 1) == 0
     _, n = _i32(3, 0)
     assert L.kvc_gqa_attention_noalloc(h, 0, None, 4, 1, n, None, None) == 1
     assert b"head_dim 128" in L.kvc_last_error()
+    L.kvc_destroy(h)
+    st, h = _create(L, d=64, dtype=_lib.KVC_BF16)  # bf16 of d = 64: the split-KV kernel (sizes need a device)
+    assert st == 0
     L.kvc_destroy(h)
 
 
@@ -255,7 +258,11 @@ def test_paged_host_rules(L):
     assert _create_paged(L, table=0)[0] == 1          # no block table
     assert _create_paged(L, table=(1 << 42) + 2)[0] == 1  # misaligned table
     assert _create_paged(L, page=64, d=128, dtype=_lib.KVC_BF16)[0] == 1  # bf16 pages: multiples of 128
-    st, h = _create_paged(L, page=16, d=64, dtype=_lib.KVC_BF16)  # off the TMA path any page size works
+    st, h = _create_paged(L, page=16, d=96, dtype=_lib.KVC_BF16)  # off the TMA path any page size works
+    assert st == 0
+    L.kvc_destroy(h)
+    assert _create_paged(L, page=16, d=64, dtype=_lib.KVC_BF16)[0] == 1  # d = 64: pages of multiples of 64
+    st, h = _create_paged(L, page=64, d=64, dtype=_lib.KVC_BF16)
     assert st == 0
     L.kvc_destroy(h)
     st, h = _create_paged(L, page=128, d=128, dtype=_lib.KVC_BF16)

@@ -166,18 +166,24 @@ def test_f32_split_key_range():
 
 
 def test_incremental_equals_full_on_gpu():
-    """S = 37, T = 5: the chunked GPU output matches the full-sequence GPU output's last rows."""
+    """S = 37, T = 5: the chunked output and the full-sequence output both
+    match the oracle's full-sequence causal output (whose last T rows the
+    oracle's own incremental call reproduces exactly)."""
     _cuda_or_skip()
     S, T, d, Hkv, G = 37, 5, 128, 2, 4
-    k = _store(wl.normal(3, 1, (1, Hkv, S, d)), torch.bfloat16).cuda()
-    v = _store(wl.normal(3, 2, (1, Hkv, S, d)), torch.bfloat16).cuda()
-    q = _store(wl.normal(3, 3, (1, Hkv * G, S, d)), torch.bfloat16).cuda()
+    k = _store(wl.normal(3, 1, (1, Hkv, S, d)), torch.bfloat16)
+    v = _store(wl.normal(3, 2, (1, Hkv, S, d)), torch.bfloat16)
+    q = _store(wl.normal(3, 3, (1, Hkv * G, S, d)), torch.bfloat16)
+    orc = ref.OracleCache(1, 1, Hkv, 64, d)
+    want = ref.append_attention(orc, 0, q.double().numpy(), k.double().numpy(), v.double().numpy(), [S])
+    k, v, q = k.cuda(), v.cuda(), q.cuda()
     full = KVCache(1, 1, Hkv, 64, d).append_attention(0, q, k, v, [S])
     inc_cache = KVCache(1, 1, Hkv, 64, d)
     inc_cache.append(0, k[:, :, : S - T].contiguous(), v[:, :, : S - T].contiguous(), [S - T])
     inc = inc_cache.append_attention(0, q[:, :, S - T :].contiguous(), k[:, :, S - T :].contiguous(),
                                      v[:, :, S - T :].contiguous(), [T])
-    assert float((inc.float() - full[:, :, S - T :].float()).abs().max()) <= 2e-2
+    assert float(np.max(np.abs(full.double().cpu().numpy() - want))) <= 2e-2
+    assert float(np.max(np.abs(inc.double().cpu().numpy() - want[:, :, S - T :]))) <= 2e-2
 
 
 # ---------------------------------------------------------------------------
@@ -330,14 +336,27 @@ def _decode_case(shape, Hq, lens0, steps_T, n_steps_list, seed, units):
     return _check_units(seed, shape, lens0, steps, q, np.asarray(n_steps_list[-1]), out, units, int(steps_T[-1]), Hq)
 
 
-def test_decode_llama8b_shape_sampled():
+def test_decode_llama8b_shape_every_unit():
+    """The Llama-3.1-8B-shaped decode at full size (cache [32, 8, 8192, 128]):
+    three steps, then every (row, KV head) unit of the last step, all 1,024
+    query rows, against the oracle."""
     s = wl.DECODE_8B
     lens0 = wl.decode_lens(0, s.B, 1024, s.max_len - 256)
     n_steps = [np.ones(s.B, dtype=np.int64)] * 3
-    rng = np.random.default_rng(1)
-    units = [(int(b), int(h)) for b, h in zip(rng.integers(0, s.B, 6), rng.integers(0, s.Hkv, 6))]
-    units.append((int(np.argmax(lens0)), 7))
+    units = [(b, h) for b in range(s.B) for h in range(s.Hkv)]
     _decode_case(s, s.Hq, lens0, [1, 1, 1], n_steps, 0, units)
+
+
+def test_decode_many_short_split_units():
+    """9,216 (row, KV head) units (1,024 rows x 9 KV heads) of 2 to 3 key tiles
+    each: nearly every unit is split between warps and left to the combine
+    kernel.  Two decode steps; 200 sampled units against the oracle, every
+    output finite."""
+    s = wl.Shape("many_units_decode", B=1024, Hq=9, Hkv=9, d=128, max_len=160, dtype="bf16")
+    lens0 = wl.decode_lens(9, s.B, 70, 150)
+    rng = np.random.default_rng(9)
+    units = sorted({(int(b), int(h)) for b, h in zip(rng.integers(0, s.B, 200), rng.integers(0, s.Hkv, 200))})
+    _decode_case(s, s.Hq, lens0, [1, 1], [np.ones(s.B, dtype=np.int64)] * 2, 9, units)
 
 
 @pytest.mark.parametrize("T", [4, 8])
@@ -372,12 +391,15 @@ def test_verify_truncate_loop():
 
 
 @pytest.mark.parametrize("ragged", [False, True])
-def test_prefill_chunk_sampled(ragged):
+def test_prefill_chunk_every_unit_of_a_row(ragged):
+    """The chunked-prefill shape at full size: every KV head of the row with
+    the longest prior (all 32 query heads x 512 queries), plus one unit of the
+    shortest, against the oracle."""
     s = wl.PREFILL
     priors = wl.prefill_priors(0, s.B)
     T = 512
     nn = wl.ragged_chunk(0, s.B) if ragged else np.full(s.B, T, dtype=np.int64)
-    units = [(int(np.argmax(priors)), 3), (int(np.argmin(priors)), 0)]
+    units = [(int(np.argmax(priors)), h) for h in range(s.Hkv)] + [(int(np.argmin(priors)), 0)]
     _decode_case(s, s.Hq, priors, [T], [nn], 3, units)
 
 
