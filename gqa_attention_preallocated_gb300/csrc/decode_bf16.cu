@@ -88,11 +88,11 @@ struct Shape {
     // as many stages as fit: 224 KB (7 of 32 KB, 14 of 16 KB) with warps owning
     // tiles, 128 KB beside the shared merge buffers otherwise
     static constexpr int kStages = (kTilePar ? 229376 : 131072) / kStageB;
-    // Consumer warps: with FP8 storage a tile holds half the bytes for the same
-    // MMA and conversion work, so one warp per SM sub-partition cannot keep up
-    // with HBM; seven tile-owning warps (two per sub-partition, with the
-    // producer) hide each other's latency.
-    static constexpr int kCW = (F8 && kTilePar) ? 7 : kConsumerWarps;
+    // Consumer warps: with FP8 storage (or 64-wide heads) a tile holds half the
+    // bytes for the same per-tile work, so one warp per SM sub-partition cannot
+    // keep up with HBM; seven tile-owning warps (two per sub-partition, with
+    // the producer) hide each other's latency.
+    static constexpr int kCW = ((F8 || D == 64) && kTilePar) ? 7 : kConsumerWarps;
     static constexpr int kCT = kCW * 32;
     static constexpr int kThreads = kCT + 32;
     static constexpr int kKeySlices = kTilePar ? 1 : kCW / MT;
