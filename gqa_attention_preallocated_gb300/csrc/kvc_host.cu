@@ -1417,11 +1417,11 @@ extern "C" kvc_status kvc_gqa_attention_noalloc(kvc_cache* c, int layer, const v
     s = noalloc_scratch_address(dev, &scratch);
     if (s) return s;
     cudaStream_t st = static_cast<cudaStream_t>(stream);
-    // The array keeps whatever the previous call left: zero the merge
-    // counters, the part the kernels need to start at zero.  The error word
-    // is left alone, so an error stays recorded until kvc_noalloc_status
-    // reads and clears it.
-    e = cudaMemsetAsync(static_cast<uint8_t*>(scratch) + kWsCounterOffset, 0, pl.ws_err - kWsCounterOffset, st);
+    // The array keeps whatever the previous call left: zero the header after
+    // the error word (the counters), the part the kernels need to start at
+    // zero.  The error word is left alone, so an error stays recorded until
+    // kvc_noalloc_status reads and clears it.
+    e = cudaMemsetAsync(static_cast<uint8_t*>(scratch) + sizeof(int), 0, pl.ws_err - sizeof(int), st);
     if (e != cudaSuccess) return cuda_fail(e, "cudaMemsetAsync(static scratch)");
     c->last_ws = scratch;
     return do_attention(c, layer, q, pl, n_new, out, scratch, KVC_NOALLOC_SCRATCH_BYTES, st);

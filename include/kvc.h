@@ -235,7 +235,7 @@ kvc_status kvc_append_attention_tree(kvc_cache* c, int layer, const void* q, con
  * kvc handle and device buffer of that context, so a process that resets a
  * device must not call this entry point again.  Every call on a device
  * shares the one array, which keeps the last call's contents; each call
- * clears the part that must start at zero (the merge counters).  The
+ * clears the part that must start at zero (the header's counters).  The
  * array's error word is not cleared by a call: a kernel's error (an expired
  * bounded wait, a bad block-table entry) stays recorded until
  * kvc_noalloc_status reads it.  Calls that overlap on the GPU (different
