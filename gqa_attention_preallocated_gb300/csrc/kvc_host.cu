@@ -524,9 +524,11 @@ kvc_status do_attention(kvc_cache* c, int layer, const void* q, const AttnPlan& 
                 const size_t i1 = std::min(items.size(), i0 + chunk);
                 const int n_items = static_cast<int>(i1 - i0);
                 // Per-CTA start-up cost in (tile x head) units and the shortest piece a cut
-                // may leave; measured on the chunked-prefill shape (start-up 8 or 20 and
-                // pieces of 16 tiles were 1 to 4 % slower, pieces of 4 tiles the same).
-                constexpr long long kStartCost = 13;
+                // may leave.  A per-CTA timeline of the chunked-prefill shape fits a piece's
+                // time as 5.1 us + 1.02 us per tile x head, so start-up is 5 units (13 and 8
+                // were 1 to 10 % slower); pieces of 16 tiles were 1 to 4 % slower, pieces of
+                // 4 tiles the same.
+                constexpr long long kStartCost = 5;
                 constexpr int kMinPieceTiles = 8;
                 long long W = 0;
                 for (size_t k = i0; k < i1; ++k)

@@ -77,6 +77,11 @@ constexpr int kOffQ = 0;                        // Q0, Q1
 constexpr int kOffK = 2 * kTile128;             // K stages 0, 1
 constexpr int kOffV = 4 * kTile128;             // V stages 0, 1
 constexpr int kOffBar = 6 * kTile128;
+// A split piece's epilogue stages head i's 128 x (d + 4) float partial block
+// at kOffQ + i * kSplitStageBytes: Q, the K stages and the first 4 KB of V
+// stage 0, all idle once that head's last PV product has landed.
+constexpr int kSplitStageBytes = 128 * (kD + 4) * 4;
+static_assert(2 * kSplitStageBytes <= kOffBar, "split staging fits below the barriers");
 // barrier indices
 // (FP8 caches: TMA completes the *Raw barriers, the converter warps then arm
 // Q / KFull / VFull once the tiles are f16)
@@ -277,71 +282,89 @@ __device__ __forceinline__ Piece decode_piece(const PrefillParams& p, int idx) {
 // counter per block and head) merges all of them:
 // o = sum_k 2^(m_k - M) O_k / sum_k 2^(m_k - M) l_k.  Kept out of line so its
 // registers do not press on the softmax loop.
+//
+// `stage` is this head's 128 x (d + 4) float block of shared memory, idle
+// once the head's last PV product has landed.  Both directions go through
+// it: a row per thread on the shared side (the 4-float pad puts 8
+// consecutive rows on distinct banks) and whole 512-byte spans per warp
+// instruction on the global side.  The merging piece pulls each other
+// piece's block in with cp.async, all of it in flight at once, and folds it
+// into a running (m, l, O) state, O held in TMEM between pieces.
 __device__ __noinline__ void split_epilogue(float* partials, int* err, uint32_t tO, int i, int r, bool valid,
                                             float m_ref, float l, int slot, int kidx, int npc, __nv_bfloat16* dst,
-                                            volatile int* merge_flag, float out_scale) {
+                                            volatile int* merge_flag, float out_scale, float* stage) {
+    constexpr int kRowF = kD + 4;             // floats per partial row: O, m, l, pad
+    constexpr int kChunks = 128 * kRowF / 4;  // 16-byte chunks of one head's block
+    static_assert(kChunks % 128 == 0, "each thread moves the same number of chunks");
     const int slot0 = slot - kidx;
-    auto part_of = [&](int sl) {
-        return partials + ((static_cast<size_t>(sl) * 2 + i) * 128 + r) * (kD + 4);
-    };
-    float* part = part_of(slot);
+    auto block_of = [&](int sl) { return partials + (static_cast<size_t>(sl) * 2 + i) * 128 * kRowF; };
+    float* srow = stage + r * kRowF;
+    // The warpgroup may still be reading shared memory that overlaps the
+    // staging block (the packed mode's exchange of the odd-tile state).
+    ptx::named_barrier_sync(1 + i, 128);
 #pragma unroll
     for (int c = 0; c < 4; ++c) {
         uint32_t w[32];
         tmem_ld32(tO + c * 32, w);
         tmem_ld_wait();
-        if (valid) {
 #pragma unroll
-            for (int e = 0; e < 32; e += 4)
-                *reinterpret_cast<uint4*>(part + c * 32 + e) = make_uint4(w[e], w[e + 1], w[e + 2], w[e + 3]);
-        }
+        for (int e = 0; e < 32; e += 4)
+            *reinterpret_cast<uint4*>(srow + c * 32 + e) = make_uint4(w[e], w[e + 1], w[e + 2], w[e + 3]);
     }
-    if (valid) {
-        part[kD] = m_ref;
-        part[kD + 1] = l;
+    srow[kD] = m_ref;
+    srow[kD + 1] = l;
+    ptx::named_barrier_sync(1 + i, 128);
+    {
+        float4* g = reinterpret_cast<float4*>(block_of(slot));
+        const float4* s4 = reinterpret_cast<const float4*>(stage);
+#pragma unroll 3
+        for (int x = r; x < kChunks; x += 128) g[x] = s4[x];
     }
     __threadfence();
     ptx::named_barrier_sync(1 + i, 128);
     int* counter = err + kWsCounterOffset / sizeof(int) + slot0 * 2 + i;
     if (r == 0) merge_flag[i] = (atomicAdd(counter, 1) == npc - 1) ? 1 : 0;
     ptx::named_barrier_sync(1 + i, 128);
-    if (merge_flag[i]) {
-        __threadfence();
-        float M = m_ref;
-        if (valid)
-            for (int k = 0; k < npc; ++k)
-                if (k != kidx) M = fmaxf(M, __ldcg(part_of(slot0 + k) + kD));
-        const float w_own = valid ? ptx::ex2(m_ref - M) : 0.f;
-        float L = l * w_own;
-        if (valid)
-            for (int k = 0; k < npc; ++k)
-                if (k != kidx) {
-                    const float* pk_ = part_of(slot0 + k);
-                    L += __ldcg(pk_ + kD + 1) * ptx::ex2(__ldcg(pk_ + kD) - M);
-                }
-        const float inv = (valid && L > 0.f) ? out_scale / L : 0.f;  // out_scale: an FP8 cache's V scale
+    if (!merge_flag[i]) return;
+    __threadfence();
+    float m_run = m_ref, l_run = l;
+    const uint32_t sbase = ptx::smem_addr(stage);
+    for (int k = 0; k < npc; ++k) {
+        if (k == kidx) continue;
+        const bool last = (k == npc - 1) || (k == npc - 2 && kidx == npc - 1);
+        ptx::named_barrier_sync(1 + i, 128);  // every row of the previous block has been read
+        const float* src = block_of(slot0 + k);
+#pragma unroll 3
+        for (int x = r; x < kChunks; x += 128) ptx::cp_async_16(sbase + x * 16, src + x * 4);
+        ptx::cp_async_wait_all();
+        ptx::named_barrier_sync(1 + i, 128);
+        const float mk = srow[kD], lk = srow[kD + 1];
+        const float M = fmaxf(m_run, mk);
+        const float Mu = (M == -INFINITY) ? 0.f : M;
+        const float a = (m_run == -INFINITY) ? 0.f : ptx::ex2(m_run - Mu);
+        const float bk = (mk == -INFINITY) ? 0.f : ptx::ex2(mk - Mu);
+        m_run = M;
+        l_run = l_run * a + lk * bk;
+        const float inv = (valid && l_run > 0.f) ? out_scale / l_run : 0.f;  // out_scale: an FP8 cache's V scale
 #pragma unroll 1
         for (int c = 0; c < 4; ++c) {
             uint32_t w[32];
             tmem_ld32(tO + c * 32, w);
             tmem_ld_wait();
-            if (valid) {
-                float acc[32];
+            float acc[32];
 #pragma unroll
-                for (int e = 0; e < 32; ++e) acc[e] = __uint_as_float(w[e]) * w_own;
-                for (int k = 0; k < npc; ++k) {
-                    if (k == kidx) continue;
-                    const float* pk_ = part_of(slot0 + k);
-                    const float wk = ptx::ex2(__ldcg(pk_ + kD) - M);
+            for (int e = 0; e < 32; e += 4) {
+                const float4 o = *reinterpret_cast<const float4*>(srow + c * 32 + e);
+                acc[e] = __uint_as_float(w[e]) * a + o.x * bk;
+                acc[e + 1] = __uint_as_float(w[e + 1]) * a + o.y * bk;
+                acc[e + 2] = __uint_as_float(w[e + 2]) * a + o.z * bk;
+                acc[e + 3] = __uint_as_float(w[e + 3]) * a + o.w * bk;
+            }
+            if (!last) {
 #pragma unroll
-                    for (int e = 0; e < 32; e += 4) {
-                        const float4 o = __ldcg(reinterpret_cast<const float4*>(pk_ + c * 32 + e));
-                        acc[e] += wk * o.x;
-                        acc[e + 1] += wk * o.y;
-                        acc[e + 2] += wk * o.z;
-                        acc[e + 3] += wk * o.w;
-                    }
-                }
+                for (int e = 0; e < 32; ++e) w[e] = __float_as_uint(acc[e]);
+                tmem_st32(tO + c * 32, w);
+            } else if (valid) {
 #pragma unroll
                 for (int e = 0; e < 32; e += 8) {
                     uint4 q4;
@@ -353,8 +376,9 @@ __device__ __noinline__ void split_epilogue(float* partials, int* err, uint32_t 
                 }
             }
         }
-        if (r == 0) *counter = 0;  // ready for the next call
+        if (!last) tmem_st_wait();
     }
+    if (r == 0) *counter = 0;  // ready for the next call
 }
 
 // kWin: the cache has a sliding window (and possibly ring storage); without
@@ -785,7 +809,8 @@ __global__ void __launch_bounds__(kThreadsPF, 1)
                 // state handed to warpgroup 0
             } else if (pc.slot != kPrefillNoSlot) {
                 split_epilogue(p.partials, p.err, tO, i, r, valid, m_ref, l, pc.slot, pc.kidx, pc.npc, dst, merge_flag,
-                               kF8 ? p.vscale[kvh] : 1.f);
+                               kF8 ? p.vscale[kvh] : 1.f,
+                               reinterpret_cast<float*>(smem + kOffQ + i * kSplitStageBytes));
             } else {
             const float inv = (valid && l > 0.f) ? (kF8 ? p.vscale[kvh] : 1.f) / l : 0.f;
 #pragma unroll

@@ -98,7 +98,7 @@ def test_packed_rows_short_rows():
     _step(cache, orc, 4, 3, 8, np.array([12, 12, 3, 12]), T=12)
 
 
-def _cuts(items, nsm, start_cost=13, min_piece=8):
+def _cuts(items, nsm, start_cost=5, min_piece=8):
     """Cuts the library's schedule makes for items (key tiles, cost per tile):
     a longest-first list schedule on the SMs, items cut at the common finish.
     Restated only to show that a case exercises the in-kernel merge."""

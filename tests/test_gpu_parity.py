@@ -411,7 +411,7 @@ def test_prefill_few_long_items(B, Hkv, G, prior, T):
     _run_calls(13, B, Hkv, G, 128, prior + T + 5, torch.bfloat16, calls)
 
 
-def _prefill_cuts(priors, n_new, Hkv, G, T, nsm, start_cost=13, min_piece=8):
+def _prefill_cuts(priors, n_new, Hkv, G, T, nsm, start_cost=5, min_piece=8):
     """Cuts made by the library's prefill schedule (a longest-first list
     schedule on the SMs, items cut at the SMs' common finish); restated here
     only to show that a test case exercises the in-kernel merge."""
