@@ -288,9 +288,10 @@ __device__ __forceinline__ Piece decode_piece(const PrefillParams& p, int idx) {
 // it: a row per thread on the shared side (the 4-float pad puts 8
 // consecutive rows on distinct banks) and whole 512-byte spans per warp
 // instruction on the global side.  The merging piece pulls each other
-// piece's block in with cp.async, all of it in flight at once, and folds it
-// into a running (m, l, O) state, O held in TMEM between pieces.
-__device__ __noinline__ void split_epilogue(float* partials, int* err, uint32_t tO, int i, int r, bool valid,
+// piece's block in with cp.async, all of it in flight at once.  tS: this
+// head's S columns, idle by now, hold the running sum of O when a block has
+// more than two pieces.
+__device__ __noinline__ void split_epilogue(float* partials, int* err, uint32_t tS, uint32_t tO, int i, int r, bool valid,
                                             float m_ref, float l, int slot, int kidx, int npc, __nv_bfloat16* dst,
                                             volatile int* merge_flag, float out_scale, float* stage) {
     constexpr int kRowF = kD + 4;             // floats per partial row: O, m, l, pad
@@ -327,25 +328,57 @@ __device__ __noinline__ void split_epilogue(float* partials, int* err, uint32_t 
     ptx::named_barrier_sync(1 + i, 128);
     if (!merge_flag[i]) return;
     __threadfence();
-    float m_run = m_ref, l_run = l;
+    // The pieces are combined in the fixed order k = 0 .. npc - 1 whichever of
+    // them merges, so repeated calls give the same bits.  M and L first: with
+    // two pieces the other one is staged now and its (m, l) read from shared
+    // memory; with more, each (m, l) comes from its slot.
     const uint32_t sbase = ptx::smem_addr(stage);
-    for (int k = 0; k < npc; ++k) {
-        if (k == kidx) continue;
-        const bool last = (k == npc - 1) || (k == npc - 2 && kidx == npc - 1);
+    int staged = -1;
+    auto stage_piece = [&](int k) {
         ptx::named_barrier_sync(1 + i, 128);  // every row of the previous block has been read
         const float* src = block_of(slot0 + k);
 #pragma unroll 3
         for (int x = r; x < kChunks; x += 128) ptx::cp_async_16(sbase + x * 16, src + x * 4);
         ptx::cp_async_wait_all();
         ptx::named_barrier_sync(1 + i, 128);
-        const float mk = srow[kD], lk = srow[kD + 1];
-        const float M = fmaxf(m_run, mk);
-        const float Mu = (M == -INFINITY) ? 0.f : M;
-        const float a = (m_run == -INFINITY) ? 0.f : ptx::ex2(m_run - Mu);
-        const float bk = (mk == -INFINITY) ? 0.f : ptx::ex2(mk - Mu);
-        m_run = M;
-        l_run = l_run * a + lk * bk;
-        const float inv = (valid && l_run > 0.f) ? out_scale / l_run : 0.f;  // out_scale: an FP8 cache's V scale
+        staged = k;
+    };
+    if (npc == 2) stage_piece(1 - kidx);
+    auto m_of = [&](int k) {
+        return k == kidx ? m_ref : k == staged ? srow[kD] : __ldcg(block_of(slot0 + k) + r * kRowF + kD);
+    };
+    auto l_of = [&](int k) {
+        return k == kidx ? l : k == staged ? srow[kD + 1] : __ldcg(block_of(slot0 + k) + r * kRowF + kD + 1);
+    };
+    float M = -INFINITY;
+    for (int k = 0; k < npc; ++k) M = fmaxf(M, m_of(k));
+    const float Mu = (M == -INFINITY) ? 0.f : M;
+    float L = 0.f;
+    for (int k = 0; k < npc; ++k) {
+        const float mk = m_of(k);
+        if (mk != -INFINITY) L += l_of(k) * ptx::ex2(mk - Mu);
+    }
+    const float inv = (valid && L > 0.f) ? out_scale / L : 0.f;  // out_scale: an FP8 cache's V scale
+    auto weight = [&](int k) {
+        const float mk = m_of(k);
+        return (mk == -INFINITY) ? 0.f : ptx::ex2(mk - Mu);
+    };
+    auto write_out = [&](int c, const float (&acc)[32]) {
+        if (!valid) return;
+#pragma unroll
+        for (int e = 0; e < 32; e += 8) {
+            uint4 q4;
+            q4.x = ptx::pack_bf16x2(acc[e] * inv, acc[e + 1] * inv);
+            q4.y = ptx::pack_bf16x2(acc[e + 2] * inv, acc[e + 3] * inv);
+            q4.z = ptx::pack_bf16x2(acc[e + 4] * inv, acc[e + 5] * inv);
+            q4.w = ptx::pack_bf16x2(acc[e + 6] * inv, acc[e + 7] * inv);
+            *reinterpret_cast<uint4*>(dst + c * 32 + e) = q4;
+        }
+    };
+    if (npc == 2) {
+        // o = w_1 O_1 + w_0 O_0 in one pass: the own O from TMEM, the other from
+        // its staged block.
+        const float w_own = weight(kidx), w_oth = weight(1 - kidx);
 #pragma unroll 1
         for (int c = 0; c < 4; ++c) {
             uint32_t w[32];
@@ -354,29 +387,59 @@ __device__ __noinline__ void split_epilogue(float* partials, int* err, uint32_t 
             float acc[32];
 #pragma unroll
             for (int e = 0; e < 32; e += 4) {
-                const float4 o = *reinterpret_cast<const float4*>(srow + c * 32 + e);
-                acc[e] = __uint_as_float(w[e]) * a + o.x * bk;
-                acc[e + 1] = __uint_as_float(w[e + 1]) * a + o.y * bk;
-                acc[e + 2] = __uint_as_float(w[e + 2]) * a + o.z * bk;
-                acc[e + 3] = __uint_as_float(w[e + 3]) * a + o.w * bk;
+                const float4 o4 = *reinterpret_cast<const float4*>(srow + c * 32 + e);
+                const float oth[4] = {o4.x, o4.y, o4.z, o4.w};
+#pragma unroll
+                for (int u = 0; u < 4; ++u) {
+                    const float own = __uint_as_float(w[e + u]);
+                    acc[e + u] = kidx == 0 ? fmaf(w_oth, oth[u], w_own * own) : fmaf(w_own, own, w_oth * oth[u]);
+                }
             }
-            if (!last) {
+            write_out(c, acc);
+        }
+    } else {
+        // O = sum_k 2^(m_k - M) O_k, the running sum kept in this head's S
+        // columns (idle now) between pieces; the own O_k comes from TMEM, the
+        // others from their staged blocks.
+        for (int k = 0; k < npc; ++k) {
+            const bool own = k == kidx, first = k == 0, last = k == npc - 1;
+            if (!own) stage_piece(k);
+            const float wk = weight(k);
+#pragma unroll 1
+            for (int c = 0; c < 4; ++c) {
+                float ok[32], acc[32];
+                uint32_t w[32];
+                if (own) {
+                    tmem_ld32(tO + c * 32, w);
+                    tmem_ld_wait();
 #pragma unroll
-                for (int e = 0; e < 32; ++e) w[e] = __float_as_uint(acc[e]);
-                tmem_st32(tO + c * 32, w);
-            } else if (valid) {
+                    for (int e = 0; e < 32; ++e) ok[e] = __uint_as_float(w[e]);
+                } else {
 #pragma unroll
-                for (int e = 0; e < 32; e += 8) {
-                    uint4 q4;
-                    q4.x = ptx::pack_bf16x2(acc[e] * inv, acc[e + 1] * inv);
-                    q4.y = ptx::pack_bf16x2(acc[e + 2] * inv, acc[e + 3] * inv);
-                    q4.z = ptx::pack_bf16x2(acc[e + 4] * inv, acc[e + 5] * inv);
-                    q4.w = ptx::pack_bf16x2(acc[e + 6] * inv, acc[e + 7] * inv);
-                    *reinterpret_cast<uint4*>(dst + c * 32 + e) = q4;
+                    for (int e = 0; e < 32; e += 4) {
+                        const float4 o4 = *reinterpret_cast<const float4*>(srow + c * 32 + e);
+                        ok[e] = o4.x, ok[e + 1] = o4.y, ok[e + 2] = o4.z, ok[e + 3] = o4.w;
+                    }
+                }
+                if (first) {
+#pragma unroll
+                    for (int e = 0; e < 32; ++e) acc[e] = wk * ok[e];
+                } else {
+                    tmem_ld32(tS + c * 32, w);
+                    tmem_ld_wait();
+#pragma unroll
+                    for (int e = 0; e < 32; ++e) acc[e] = fmaf(wk, ok[e], __uint_as_float(w[e]));
+                }
+                if (!last) {
+#pragma unroll
+                    for (int e = 0; e < 32; ++e) w[e] = __float_as_uint(acc[e]);
+                    tmem_st32(tS + c * 32, w);
+                    tmem_st_wait();
+                } else {
+                    write_out(c, acc);
                 }
             }
         }
-        if (!last) tmem_st_wait();
     }
     if (r == 0) *counter = 0;  // ready for the next call
 }
@@ -808,7 +871,7 @@ __global__ void __launch_bounds__(kThreadsPF, 1)
             if (alt && i == 1) {
                 // state handed to warpgroup 0
             } else if (pc.slot != kPrefillNoSlot) {
-                split_epilogue(p.partials, p.err, tO, i, r, valid, m_ref, l, pc.slot, pc.kidx, pc.npc, dst, merge_flag,
+                split_epilogue(p.partials, p.err, tS, tO, i, r, valid, m_ref, l, pc.slot, pc.kidx, pc.npc, dst, merge_flag,
                                kF8 ? p.vscale[kvh] : 1.f,
                                reinterpret_cast<float*>(smem + kOffQ + i * kSplitStageBytes));
             } else {

@@ -390,6 +390,32 @@ def test_verify_truncate_loop():
     assert torch.equal(outs[0], outs[1]) and torch.equal(outs[1], outs[2])
 
 
+@pytest.mark.parametrize("B,Hq,T,prior", [
+    (4, 32, 512, None),   # the chunked-prefill shape: 128-position tiles, cut blocks
+    (4, 64, 40, 12000),   # packed rows in tile pairs, long rows cut across CTAs
+    (8, 32, 4, 4092),     # one packed tile per (row, KV head): verify-sized, cut
+])
+def test_prefill_repeated_calls_identical(B, Hq, T, prior):
+    """The same call four times (append, attend, truncate back) gives the same
+    bits: pieces of a cut block are combined in a fixed order whichever of
+    them finishes last, and nothing else in the launch depends on timing."""
+    _cuda_or_skip()
+    Hkv, d = 8, 128
+    lens0 = wl.prefill_priors(3, B) if prior is None else np.full(B, prior, dtype=np.int64)
+    max_len = int(lens0.max()) + T + 8
+    cache = KVCache(1, B, Hkv, max_len, d)
+    _fill_poisoned(cache, 0, 9, lens0)
+    kn, vn = (x.cuda() for x in _new_tokens(9, 0, B, Hkv, T, d))
+    q = _queries(9, 0, B, Hq, T, d).cuda()
+    outs = []
+    for _ in range(4):
+        outs.append(cache.append_attention(0, q, kn, vn, np.full(B, T)))
+        cache.truncate(lens0)
+    torch.cuda.synchronize()
+    for o in outs[1:]:
+        assert torch.equal(o, outs[0])
+
+
 @pytest.mark.parametrize("ragged", [False, True])
 def test_prefill_chunk_every_unit_of_a_row(ragged):
     """The chunked-prefill shape at full size: every KV head of the row with
