@@ -63,7 +63,6 @@ constexpr int kConsumerWarps = 4;  // consumer warps, except FP8 caches with war
 // Head dimensions: D = 128 (bf16 and FP8 storage) and D = 64 (bf16).  A TMA
 // box is 64 keys x 128 bytes (64 bf16 columns, or 128 E4M3 codes) with the
 // 128-byte swizzle; a bf16 tile of 64 keys is D / 64 boxes.
-constexpr int kHalfBytes = kKeyTile * 128;   // one swizzled box
 // floats per partial row: O[D], m, l, pad
 __host__ __device__ constexpr int part_stride(int D) { return D + 4; }
 constexpr uint64_t kWaitLimitNs = 2000000000ull;
@@ -81,8 +80,12 @@ template <int MT, bool F8, int D>
 struct Shape {
     static_assert(D == 128 || (D == 64 && !F8), "head dimensions: 128 (bf16, FP8) and 64 (bf16)");
     static constexpr bool kTilePar = (MT == 1);                // warps own whole tiles
-    // bytes of one K (or V) tile of 64 keys: D / 64 boxes of bf16, or one
-    // 128-byte-row box of E4M3 codes
+    // Keys per tile: 64, or 128 for 64-wide heads, whose 64-key tile would
+    // carry half the bytes of a 128-wide one for the same per-tile work.
+    static constexpr int kKeyTile = key_tile_keys(D, F8);
+    static constexpr int kHalfBytes = kKeyTile * 128;  // one swizzled box: kKeyTile rows x 128 bytes
+    // bytes of one K (or V) tile: D / 64 boxes of bf16, or one 128-byte-row
+    // box of E4M3 codes
     static constexpr int kTileB = F8 ? kKeyTile * 128 : kKeyTile * D * 2;
     static constexpr int kStageB = 2 * kTileB;
     // as many stages as fit: 224 KB (7 of 32 KB, 14 of 16 KB) with warps owning
@@ -139,7 +142,7 @@ struct Part<true> {
 // First key tile (absolute position / 64) of group q's units: 0, or with a
 // window the tile holding the window start of the block's earliest query
 // (the same rule as the planners'; tiles before it are never scheduled).
-template <bool DP>
+template <bool DP, int KT>
 __device__ __forceinline__ int first_tile(const Part<DP>& w, int q) {
     const DecodeParams& p = w.p;
     if (p.window <= 0) return 0;
@@ -153,7 +156,7 @@ __device__ __forceinline__ int first_tile(const Part<DP>& w, int q) {
         for (int r = r0; r < r1; ++r)
             if (r % p.T < nn) qmin = min(qmin, prior + r % p.T);
     }
-    return qmin == 0x7fffffff ? 0 : max(0, qmin - p.window + 1) / kKeyTile;
+    return qmin == 0x7fffffff ? 0 : max(0, qmin - p.window + 1) / KT;
 }
 
 // Largest q with gstart[q] <= x (gstart nondecreasing, x < gstart[NB]).
@@ -167,7 +170,7 @@ __device__ __forceinline__ int locate_group(const Part<DP>& w, int x) {
     return lo;
 }
 
-template <bool DP>
+template <bool DP, int KT>
 struct Cursor {
     int q, kvh, j, nt, t0;  // t0: the group's first key tile
     __device__ __forceinline__ void init(const Part<DP>& w, int x) {
@@ -176,7 +179,7 @@ struct Cursor {
         const int off = x - w.gstart(q);
         kvh = off / nt;
         j = off - kvh * nt;
-        t0 = first_tile(w, q);
+        t0 = first_tile<DP, KT>(w, q);
     }
     __device__ __forceinline__ void advance(const Part<DP>& w) {
         if (++j < nt) return;
@@ -187,7 +190,7 @@ struct Cursor {
         while (q < w.NB() && w.gstart(q + 1) == w.gstart(q)) ++q;
         if (q < w.NB()) {
             nt = (w.gstart(q + 1) - w.gstart(q)) / w.Hkv();
-            t0 = first_tile(w, q);
+            t0 = first_tile<DP, KT>(w, q);
         }
     }
 };
@@ -234,6 +237,7 @@ __global__ void __launch_bounds__(Shape<MT, F8, D>::kThreads, 1)
     decode_splitkv_bf16_kernel(const __grid_constant__ DecodeParams p, const __grid_constant__ CUtensorMap tmK,
                                const __grid_constant__ CUtensorMap tmV) {
     using S = Shape<MT, F8, D>;
+    constexpr int KT = S::kKeyTile;  // keys per tile
     constexpr int PS = part_stride(D);
     constexpr int CPR = D / 8;  // 16-byte chunks of a bf16 row
     constexpr int kStages = S::kStages;
@@ -304,7 +308,7 @@ __global__ void __launch_bounds__(Shape<MT, F8, D>::kThreads, 1)
     // ------------------------------------------------------------------ producer
     if (warp == S::kCW) {
         if (lane == 0) {
-            Cursor<DP> cur;
+            Cursor<DP, KT> cur;
             cur.init(wp, x0);
             int issued = 0;
             for (int x = x0, it = 0; x < x1; ++x, ++it) {
@@ -317,7 +321,7 @@ __global__ void __launch_bounds__(Shape<MT, F8, D>::kThreads, 1)
                 }
                 if (*abort_flag) break;  // the producer is in no named barrier, so it may stop early
                 const int b = cur.q / p.RB;
-                const int row = key_row(p, b, cur.kvh, (cur.t0 + cur.j) * kKeyTile);
+                const int row = key_row(p, b, cur.kvh, (cur.t0 + cur.j) * KT);
                 const uint32_t full = bar0 + 8 * s;
                 const uint32_t sK = stage0 + s * S::kStageB;
                 stage_tag[s] = it;
@@ -328,8 +332,8 @@ __global__ void __launch_bounds__(Shape<MT, F8, D>::kThreads, 1)
                 } else {
 #pragma unroll
                     for (int hf = 0; hf < D / 64; ++hf) {  // 64-column boxes of the K and V tiles
-                        ptx::tma_load_2d(sK + hf * kHalfBytes, &tmK, 64 * hf, row, full);
-                        ptx::tma_load_2d(sK + S::kTileB + hf * kHalfBytes, &tmV, 64 * hf, row, full);
+                        ptx::tma_load_2d(sK + hf * S::kHalfBytes, &tmK, 64 * hf, row, full);
+                        ptx::tma_load_2d(sK + S::kTileB + hf * S::kHalfBytes, &tmV, 64 * hf, row, full);
                     }
                 }
                 ++issued;
@@ -357,7 +361,7 @@ __global__ void __launch_bounds__(Shape<MT, F8, D>::kThreads, 1)
     const int quad = lane & 3;
     const int lrow0 = mt * 16 + (lane >> 2);  // this thread's block rows: lrow0, lrow0 + 8
 
-    Cursor<DP> cur;
+    Cursor<DP, KT> cur;
     cur.init(wp, x0);
 
     float o[D / 8][4];
@@ -471,14 +475,14 @@ __global__ void __launch_bounds__(Shape<MT, F8, D>::kThreads, 1)
 
             const uint32_t sK = stage0 + s * S::kStageB;
             const uint32_t sV = sK + S::kTileB;
-            const int tile0 = (cur.t0 + j) * kKeyTile;  // first key position of the tile
+            const int tile0 = (cur.t0 + j) * KT;  // first key position of the tile
 
             if (S::kTilePar && p.append_new) {
                 // In-kernel append: rows prior .. prior+n_new-1 of this unit that
                 // fall in this tile come from k_new / v_new.  The staged copy of
                 // those cache slots is stale, so patch it, and write the rows to
                 // the cache (this tile is processed exactly once).
-                const int lo = max(seg_prior, tile0), hi = min(seg_prior + seg_nn, tile0 + kKeyTile);
+                const int lo = max(seg_prior, tile0), hi = min(seg_prior + seg_nn, tile0 + KT);
                 if (lo < hi) {
                     // lanes 0 .. CPR-1 write K, CPR .. 2*CPR-1 V, one 16-byte chunk of
                     // the bf16 source row each (the rest idle: D = 64)
@@ -510,7 +514,7 @@ __global__ void __launch_bounds__(Shape<MT, F8, D>::kThreads, 1)
                             if (!bad) *reinterpret_cast<uint2*>(dst + static_cast<size_t>(row0 + pos) * D + chunk * 8) = q8;
                         }
                     } else {
-                        uint8_t* stg = stages + s * S::kStageB + (is_v ? S::kTileB : 0) + (chunk >> 3) * kHalfBytes;
+                        uint8_t* stg = stages + s * S::kStageB + (is_v ? S::kTileB : 0) + (chunk >> 3) * S::kHalfBytes;
                         for (int pos = lo; pos < hi_l; ++pos) {
                             const int t = pos - seg_prior, r = pos - tile0;
                             const uint4 val = (t == 0) ? new_row0
@@ -524,17 +528,17 @@ __global__ void __launch_bounds__(Shape<MT, F8, D>::kThreads, 1)
                 }
             }
 
-            if (tile0 + kKeyTile > extent) {
+            if (tile0 + KT > extent) {
                 // Clear V rows at or past the unit's last visible key (slots past
                 // lens may hold NaN; their probabilities are 0 but 0 * NaN is NaN).
                 const int vr0 = extent - tile0;
-                const int per_half = (kKeyTile - vr0) * 8;
+                const int per_half = (KT - vr0) * 8;
                 uint8_t* vbase = stages + s * S::kStageB + S::kTileB;
                 const int t0 = S::kTilePar ? lane : tid;
                 const int step = S::kTilePar ? 32 : S::kCT;
                 for (int idx = t0; idx < (F8 ? 1 : D / 64) * per_half; idx += step) {
                     const int hf = idx / per_half, rem = idx - hf * per_half;
-                    *reinterpret_cast<uint4*>(vbase + hf * kHalfBytes + (vr0 + (rem >> 3)) * 128 + (rem & 7) * 16) =
+                    *reinterpret_cast<uint4*>(vbase + hf * S::kHalfBytes + (vr0 + (rem >> 3)) * 128 + (rem & 7) * 16) =
                         make_uint4(0u, 0u, 0u, 0u);
                 }
                 ptx::fence_proxy_async_smem();
@@ -543,22 +547,22 @@ __global__ void __launch_bounds__(Shape<MT, F8, D>::kThreads, 1)
             if (tile0 <= min_lo) {
                 // Clear V rows outside every row's window as well (a stale slot
                 // must never meet p = 0).
-                const int vr1 = min(kKeyTile, min_lo - tile0 + 1);
+                const int vr1 = min(KT, min_lo - tile0 + 1);
                 const int per_half = vr1 * 8;
                 uint8_t* vbase = stages + s * S::kStageB + S::kTileB;
                 const int t0 = S::kTilePar ? lane : tid;
                 const int step = S::kTilePar ? 32 : S::kCT;
                 for (int idx = t0; idx < (F8 ? 1 : D / 64) * per_half; idx += step) {
                     const int hf = idx / per_half, rem = idx - hf * per_half;
-                    *reinterpret_cast<uint4*>(vbase + hf * kHalfBytes + (rem >> 3) * 128 + (rem & 7) * 16) =
+                    *reinterpret_cast<uint4*>(vbase + hf * S::kHalfBytes + (rem >> 3) * 128 + (rem & 7) * 16) =
                         make_uint4(0u, 0u, 0u, 0u);
                 }
                 ptx::fence_proxy_async_smem();
                 if (S::kTilePar) __syncwarp(); else ptx::named_barrier_sync(1, S::kCT);
             }
             // With a draft tree only tiles wholly before the chunk are free of the mask.
-            const bool full_tile = (tile0 + kKeyTile - 1 <= min_lim) && (tile0 > max_lo) &&
-                                   (!TREE || tile0 + kKeyTile <= seg_prior);
+            const bool full_tile = (tile0 + KT - 1 <= min_lim) && (tile0 > max_lo) &&
+                                   (!TREE || tile0 + KT <= seg_prior);
 
             // S = Q K^T for this warp's 16 rows x KW keys.
             float sc[NBS][4];
@@ -590,7 +594,7 @@ __global__ void __launch_bounds__(Shape<MT, F8, D>::kThreads, 1)
                         const int mi = lane >> 3;
                         const int key = koff + kb * 16 + (mi >> 1) * 8 + (lane & 7);
                         const int chunk = 2 * kk + (mi & 1);
-                        const uint32_t addr = sK + (chunk >> 3) * kHalfBytes + key * 128 + (((chunk & 7) ^ (key & 7)) << 4);
+                        const uint32_t addr = sK + (chunk >> 3) * S::kHalfBytes + key * 128 + (((chunk & 7) ^ (key & 7)) << 4);
                         uint32_t b0, b1, b2, b3;
                         ptx::ldmatrix_x4(addr, b0, b1, b2, b3);
                         ptx::mma_bf16_16816(sc[2 * kb], qa[kk], b0, b1);
@@ -702,7 +706,7 @@ __global__ void __launch_bounds__(Shape<MT, F8, D>::kThreads, 1)
                     const int mi = lane >> 3;
                     const int key = koff + kb * 16 + (mi & 1) * 8 + (lane & 7);
                     const int chunk = 2 * dc + (mi >> 1);
-                    const uint32_t addr = sV + (chunk >> 3) * kHalfBytes + key * 128 + (((chunk & 7) ^ (key & 7)) << 4);
+                    const uint32_t addr = sV + (chunk >> 3) * S::kHalfBytes + key * 128 + (((chunk & 7) ^ (key & 7)) << 4);
                     uint32_t b0, b1, b2, b3;
                     ptx::ldmatrix_x4_trans(addr, b0, b1, b2, b3);
                     ptx::mma_bf16_16816(o[2 * dc], a, b0, b1);
@@ -1044,8 +1048,8 @@ __global__ void __launch_bounds__(kPlanThreads) decode_plan_kernel(const __grid_
             }
         }
         const int kfirst = (extent > 0 && p.window > 0) ? max(0, qmin - p.window + 1) : 0;
-        ft = kfirst / kKeyTile;
-        tiles = extent > 0 ? ((extent - 1) / kKeyTile + 1 - ft) * p.Hkv : 0;
+        ft = kfirst / p.key_tile;
+        tiles = extent > 0 ? ((extent - 1) / p.key_tile + 1 - ft) * p.Hkv : 0;
     }
     // Block-wide exclusive scan of the group tile counts.
     __shared__ int warp_sum[kPlanThreads / 32];

@@ -172,8 +172,9 @@ kvc_status encode_layer_maps(kvc_cache* c, int layer) {
                                         : static_cast<cuuint64_t>(c->B) * c->Hkv * c->max_len;
     kvc_status s;
     const bool fp8 = c->dtype == KVC_FP8_E4M3;
-    if ((s = encode_rows_map(&c->tmK[layer], c->k[layer], rows, kKeyTile, fp8, c->d))) return s;
-    if ((s = encode_rows_map(&c->tmV[layer], c->v[layer], rows, kKeyTile, fp8, c->d))) return s;
+    const int kt = key_tile_keys(c->d, fp8);  // the split-KV kernel's tile for this cache
+    if ((s = encode_rows_map(&c->tmK[layer], c->k[layer], rows, kt, fp8, c->d))) return s;
+    if ((s = encode_rows_map(&c->tmV[layer], c->v[layer], rows, kt, fp8, c->d))) return s;
     if (tc_capable(c)) {
         if ((s = encode_rows_map(&c->tmK128[layer], c->k[layer], rows, 128, fp8))) return s;
         if ((s = encode_rows_map(&c->tmV128[layer], c->v[layer], rows, 128, fp8))) return s;
@@ -678,8 +679,9 @@ kvc_status do_attention(kvc_cache* c, int layer, const void* q, const AttnPlan& 
                 }
             }
             const int kfirst = (extent > 0 && c->window > 0) ? std::max(0, qmin - c->window + 1) : 0;
-            const int first_tile = kfirst / kKeyTile;
-            const int ntiles = extent > 0 ? (extent - 1) / kKeyTile + 1 - first_tile : 0;
+            const int kt = key_tile_keys(c->d, c->dtype == KVC_FP8_E4M3);
+            const int first_tile = kfirst / kt;
+            const int ntiles = extent > 0 ? (extent - 1) / kt + 1 - first_tile : 0;
             p.gstart[b * pl.RB + rb] = static_cast<int>(tiles);
             tiles += static_cast<long long>(ntiles) * c->Hkv;
         }
@@ -853,7 +855,7 @@ kvc_status kvc_create(kvc_cache** out, int layers, int batch, int kv_heads, int 
     if (dtype == KVC_FP8_E4M3 && kv_heads > kMaxScaleHeads)
         return fail(KVC_ERR_ARG, "fp8 caches take at most %d KV heads", kMaxScaleHeads);
     const long long rows = static_cast<long long>(batch) * kv_heads * max_len;
-    if (rows + kKeyTile >= (1ll << 31)) return fail(KVC_ERR_ARG, "batch * kv_heads * max_len too large");
+    if (rows + 2 * kKeyTile >= (1ll << 31)) return fail(KVC_ERR_ARG, "batch * kv_heads * max_len too large");
     if (!k_bufs || !v_bufs) return fail(KVC_ERR_ARG, "k_bufs / v_bufs is null");
     for (int l = 0; l < layers; ++l) {
         if (!k_bufs[l] || !v_bufs[l]) return fail(KVC_ERR_ARG, "layer %d buffer is null", l);
@@ -910,14 +912,14 @@ kvc_status kvc_create_paged(kvc_cache** out, int layers, int batch, int kv_heads
     if (dtype != KVC_F32 && head_dim == kHeadDimBf16 && page_size % 128 != 0)
         return fail(KVC_ERR_ARG, "bf16 and fp8 pages of head_dim %d hold a multiple of 128 tokens (key tiles never cross a page)",
                     kHeadDimBf16);
-    if (dtype == KVC_BF16 && head_dim == kHeadDimSmall && page_size % kKeyTile != 0)
+    if (dtype == KVC_BF16 && head_dim == kHeadDimSmall && page_size % key_tile_keys(kHeadDimSmall, false) != 0)
         return fail(KVC_ERR_ARG, "bf16 pages of head_dim %d hold a multiple of %d tokens (key tiles never cross a page)",
-                    kHeadDimSmall, kKeyTile);
+                    kHeadDimSmall, key_tile_keys(kHeadDimSmall, false));
     if (batch > 0 && !block_table) return fail(KVC_ERR_ARG, "block_table is null");
     if ((reinterpret_cast<uintptr_t>(block_table) & 3u) != 0) return fail(KVC_ERR_ARG, "block_table not 4-byte aligned");
     const long long cap = static_cast<long long>(max_pages_per_row) * page_size;
     if (cap >= (1ll << 30)) return fail(KVC_ERR_ARG, "max_pages_per_row * page_size too large");
-    if (static_cast<long long>(num_pages) * kv_heads * page_size + kKeyTile >= (1ll << 31))
+    if (static_cast<long long>(num_pages) * kv_heads * page_size + 2 * kKeyTile >= (1ll << 31))
         return fail(KVC_ERR_ARG, "num_pages * kv_heads * page_size too large");
     if (static_cast<long long>(batch) * max_pages_per_row >= (1ll << 31))
         return fail(KVC_ERR_ARG, "batch * max_pages_per_row too large");
@@ -1169,7 +1171,8 @@ kvc_status kvc_set_window(kvc_cache* c, int window, int ring) {
     if (ring) {
         if (c->pg.table) return fail(KVC_ERR_ARG, "a paged cache cannot also be a ring");
         if (window < 1 || window > c->max_len) return fail(KVC_ERR_ARG, "a ring cache needs a window of 1..max_len");
-        const int tile = tc_capable(c) ? 128 : kKeyTile;  // the largest key tile any kernel of this cache reads
+        // the largest key tile any kernel of this cache reads
+        const int tile = tc_capable(c) ? 128 : key_tile_keys(c->d, c->dtype == KVC_FP8_E4M3);
         if (!generic_path(c) && c->max_len % tile != 0)
             return fail(KVC_ERR_ARG, "this ring cache needs max_len %% %d == 0 (key tiles never wrap)", tile);
     }
@@ -1281,6 +1284,7 @@ kvc_status kvc_decode_step(kvc_cache* c, int layer, const void* q, const void* k
     pp.max_len = c->max_len;
     pp.window = c->window;
     pp.ring = c->ring ? 1 : 0;
+    pp.key_tile = key_tile_keys(c->d, c->dtype == KVC_FP8_E4M3);
     cudaError_t e = launch_decode_plan(pp, st);
     if (e != cudaSuccess) return cuda_fail(e, "device plan launch");
     ++c->launches;

@@ -34,12 +34,18 @@ __host__ __device__ __forceinline__ int phys_row(const Paging& pg, int ring, int
     return (b * Hkv + kvh) * max_len + (ring ? a % max_len : a);
 }
 
-// Keys per K/V tile of the split-KV kernel, and the head width the TMA /
-// tensor-core kernels are built for (the split-KV kernel also takes bf16
-// storage of head width kHeadDimSmall).
+// Keys per K/V tile of the split-KV kernel for 128-wide heads (see
+// key_tile_keys), and the head width the TMA / tensor-core kernels are built
+// for (the split-KV kernel also takes bf16 storage of head width kHeadDimSmall).
 constexpr int kKeyTile = 64;
 constexpr int kHeadDimBf16 = 128;
 constexpr int kHeadDimSmall = 64;
+// Keys per split-KV tile: 64, or 128 for bf16 storage of head width
+// kHeadDimSmall (a 64-key tile there would carry half the bytes of a
+// 128-wide one for the same per-tile work).
+__host__ __device__ constexpr int key_tile_keys(int d, bool fp8) {
+    return (d == kHeadDimSmall && !fp8) ? 2 * kKeyTile : kKeyTile;
+}
 // FP8 E4M3 caches: one K and one V scale per KV head (at most this many heads).
 constexpr int kMaxScaleHeads = 64;
 
@@ -103,6 +109,7 @@ struct PlanParams {
     int* err;
     int B, T, R, RPB, RB, NB, Hkv, num_ctas, max_len;
     int window, ring;
+    int key_tile;  // keys per tile of the split-KV kernel this plan feeds
 };
 
 cudaError_t launch_decode_plan(const PlanParams& p, cudaStream_t stream);

@@ -136,7 +136,8 @@ kvc_status kvc_set_kv_scales(kvc_cache* c, int layer, const float* k_scale, cons
  * A bad entry is never dereferenced: appended rows aimed at it are not
  * written, and reads take page 0 and set the workspace error word (the next
  * kvc_device_status reports it); the generic kernel (fp32; bf16, FP8 of
- * d != 128) reads it as zeros.  bf16 and FP8 caches of d = 128 need page_size % 128 == 0.  Paged storage does not combine with ring
+ * d != 128) reads it as zeros.  bf16 and FP8 caches of d = 128, and bf16 caches of d = 64, need
+ * page_size % 128 == 0 (a key tile lies in one page).  Paged storage does not combine with ring
  * storage (kvc_set_window ring = 1).  Errors: as kvc_create, and KVC_ERR_ARG
  * for bad paging arguments. */
 kvc_status kvc_create_paged(kvc_cache** out, int layers, int batch, int kv_heads, int page_size, int num_pages,
@@ -267,7 +268,8 @@ kvc_status kvc_noalloc_status(void* stream, int32_t* code);
  * kvc_truncate may only go back to a length n whose window keys
  * n - window + 1 .. n - 1 are still stored (or to 0).
  * Requirements: ring needs 1 <= window <= max_len and, for bf16 and FP8
- * caches of d = 128, max_len % 128 == 0; ring storage changes only while every length is 0.
+ * caches of d = 128 and bf16 caches of d = 64, max_len % 128 == 0 (a key
+ * tile never wraps); ring storage changes only while every length is 0.
  * Applies to every layer and to every later call (including
  * kvc_decode_step).  Host only.  KVC_ERR_ARG otherwise. */
 kvc_status kvc_set_window(kvc_cache* c, int window, int ring);

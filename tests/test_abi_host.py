@@ -261,8 +261,9 @@ def test_paged_host_rules(L):
     st, h = _create_paged(L, page=16, d=96, dtype=_lib.KVC_BF16)  # off the TMA path any page size works
     assert st == 0
     L.kvc_destroy(h)
-    assert _create_paged(L, page=16, d=64, dtype=_lib.KVC_BF16)[0] == 1  # d = 64: pages of multiples of 64
-    st, h = _create_paged(L, page=64, d=64, dtype=_lib.KVC_BF16)
+    assert _create_paged(L, page=16, d=64, dtype=_lib.KVC_BF16)[0] == 1  # d = 64: pages of multiples of 128
+    assert _create_paged(L, page=64, d=64, dtype=_lib.KVC_BF16)[0] == 1
+    st, h = _create_paged(L, page=128, d=64, dtype=_lib.KVC_BF16)
     assert st == 0
     L.kvc_destroy(h)
     st, h = _create_paged(L, page=128, d=128, dtype=_lib.KVC_BF16)

@@ -102,7 +102,7 @@ def test_bf16_generic_empty_rows_and_zero_tokens():
     _check_slots(cache, orc)
 
 
-@pytest.mark.parametrize("window,ring,max_len", [(9, False, 200), (24, True, 64), (64, True, 64)])
+@pytest.mark.parametrize("window,ring,max_len", [(9, False, 200), (24, True, 128), (128, True, 128)])
 def test_bf16_generic_window(window, ring, max_len):
     cache, orc = _contiguous(2, 2, 64, max_len, window, ring)
     rng = np.random.default_rng(window)
@@ -127,10 +127,10 @@ def test_bf16_generic_tree():
     _check_slots(cache, orc)
 
 
-@pytest.mark.parametrize("d,page", [(96, 16), (64, 64)])
+@pytest.mark.parametrize("d,page", [(96, 16), (64, 128)])
 def test_bf16_paged(d, page):
     """Pages in a shuffled pool: 16 tokens for d = 96 (any page size works off
-    the TMA path), 64 for d = 64 (a split-KV key tile lies in one page)."""
+    the TMA path), 128 for d = 64 (a 128-key split-KV tile lies in one page)."""
     _cuda_or_skip()
     B, Hkv, G, mpr = 3, 2, 4, 12
     num_pages = B * mpr + 4
