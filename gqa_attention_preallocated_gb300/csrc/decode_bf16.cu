@@ -100,6 +100,9 @@ struct Shape {
     static constexpr int kThreads = kCT + 32;
     static constexpr int kKeySlices = kTilePar ? 1 : kCW / MT;
     static constexpr int kKW = kKeyTile / kKeySlices;          // keys per warp per tile
+    // Keys per pass over the tile: an FP8 warp's registers hold the scores of
+    // 64 keys, so it takes a 128-key tile in two passes.
+    static constexpr int kKWP = (F8 && kKW > 64) ? 64 : kKW;
     static constexpr int kMerge = kTilePar ? 1 : kKeySlices;   // states per m-tile merged in shared memory
     static constexpr int kWays = kTilePar ? kCW : 1;  // partial sub-slots per (unit, CTA)
     static constexpr int kRPB = 16 * MT;
@@ -243,8 +246,9 @@ __global__ void __launch_bounds__(Shape<MT, F8, D>::kThreads, 1)
     constexpr int kStages = S::kStages;
     constexpr int KW = S::kKW;
     constexpr int RPB = S::kRPB;
-    constexpr int NBS = KW / 8;   // score n-blocks per warp per tile
-    constexpr int KB = KW / 16;   // 16-key blocks per warp per tile
+    constexpr int KWP = S::kKWP;  // keys per pass (KW / KWP passes per tile)
+    constexpr int NBS = KWP / 8;  // score n-blocks per warp per pass
+    constexpr int KB = KWP / 16;  // 16-key blocks per warp per pass
     constexpr int NM = S::kMerge;
 
     extern __shared__ uint8_t smem_raw[];
@@ -560,157 +564,161 @@ __global__ void __launch_bounds__(Shape<MT, F8, D>::kThreads, 1)
                 ptx::fence_proxy_async_smem();
                 if (S::kTilePar) __syncwarp(); else ptx::named_barrier_sync(1, S::kCT);
             }
-            // With a draft tree only tiles wholly before the chunk are free of the mask.
-            const bool full_tile = (tile0 + KT - 1 <= min_lim) && (tile0 > max_lo) &&
-                                   (!TREE || tile0 + KT <= seg_prior);
+            for (int pass = 0; pass < KW / KWP; ++pass) {
+                const int kp = koff + pass * KWP;  // this pass's first key within the tile
+                // With a draft tree only tiles wholly before the chunk are free of the mask.
+                const int kpass0 = tile0 + kp;  // first key position of this pass
+                const bool full_tile = (kpass0 + KWP - 1 <= min_lim) && (kpass0 > max_lo) &&
+                                       (!TREE || kpass0 + KWP <= seg_prior);
 
-            // S = Q K^T for this warp's 16 rows x KW keys.
-            float sc[NBS][4];
-#pragma unroll
-            for (int nb = 0; nb < NBS; ++nb) sc[nb][0] = sc[nb][1] = sc[nb][2] = sc[nb][3] = 0.f;
-            if constexpr (F8) {
-                // Key n-block nb: this thread's key is koff + 8*nb + lane/4, and
-                // its 32 bytes d = 32*quad .. 32*quad + 31 (two swizzled 16-byte
-                // chunks) hold k-step kk's four values at bytes 4*kk .. 4*kk + 3.
-#pragma unroll
+                // S = Q K^T for this warp's 16 rows x KW keys.
+                float sc[NBS][4];
+    #pragma unroll
+                for (int nb = 0; nb < NBS; ++nb) sc[nb][0] = sc[nb][1] = sc[nb][2] = sc[nb][3] = 0.f;
+                if constexpr (F8) {
+                    // Key n-block nb: this thread's key is kp + 8*nb + lane/4, and
+                    // its 32 bytes d = 32*quad .. 32*quad + 31 (two swizzled 16-byte
+                    // chunks) hold k-step kk's four values at bytes 4*kk .. 4*kk + 3.
+    #pragma unroll
+                    for (int nb = 0; nb < NBS; ++nb) {
+                        const int key = kp + nb * 8 + (lane >> 2);
+                        const uint32_t row = sK + key * 128;
+                        const uint4 u0 = ptx::ld_shared_v4(row + (((2 * quad) ^ (key & 7)) << 4));
+                        const uint4 u1 = ptx::ld_shared_v4(row + (((2 * quad + 1) ^ (key & 7)) << 4));
+                        const uint32_t w[8] = {u0.x, u0.y, u0.z, u0.w, u1.x, u1.y, u1.z, u1.w};
+    #pragma unroll
+                        for (int kk = 0; kk < 8; ++kk) {
+                            uint32_t b0, b1;
+                            ptx::e4m3x4_to_f16x2x2(w[kk], b0, b1);
+                            ptx::mma_f16_16816(sc[nb], qa[kk], b0, b1);
+                        }
+                    }
+                } else {
+    #pragma unroll
+                    for (int kk = 0; kk < D / 16; ++kk) {
+    #pragma unroll
+                        for (int kb = 0; kb < KB; ++kb) {
+                            const int mi = lane >> 3;
+                            const int key = kp + kb * 16 + (mi >> 1) * 8 + (lane & 7);
+                            const int chunk = 2 * kk + (mi & 1);
+                            const uint32_t addr = sK + (chunk >> 3) * S::kHalfBytes + key * 128 + (((chunk & 7) ^ (key & 7)) << 4);
+                            uint32_t b0, b1, b2, b3;
+                            ptx::ldmatrix_x4(addr, b0, b1, b2, b3);
+                            ptx::mma_bf16_16816(sc[2 * kb], qa[kk], b0, b1);
+                            ptx::mma_bf16_16816(sc[2 * kb + 1], qa[kk], b2, b3);
+                        }
+                    }
+                }
+
+                // Mask (diagonal / ragged tiles only) and online softmax in base 2.
+                // The row maximum is taken on the raw scores (the scale is
+                // positive) and the scale is folded into the exponent's FMA.  The
+                // reference used for the exponentials only moves when a row's
+                // maximum passes it by more than kLazyRescale (a factor 2^8 at
+                // most on p), and only then are O and l rescaled; O, l and the
+                // stored m share that reference, so the result is exact.
+                const int kbase = tile0 + kp + 2 * quad;
+                float mx0 = -INFINITY, mx1 = -INFINITY;
+    #pragma unroll
                 for (int nb = 0; nb < NBS; ++nb) {
-                    const int key = koff + nb * 8 + (lane >> 2);
-                    const uint32_t row = sK + key * 128;
-                    const uint4 u0 = ptx::ld_shared_v4(row + (((2 * quad) ^ (key & 7)) << 4));
-                    const uint4 u1 = ptx::ld_shared_v4(row + (((2 * quad + 1) ^ (key & 7)) << 4));
-                    const uint32_t w[8] = {u0.x, u0.y, u0.z, u0.w, u1.x, u1.y, u1.z, u1.w};
-#pragma unroll
-                    for (int kk = 0; kk < 8; ++kk) {
-                        uint32_t b0, b1;
-                        ptx::e4m3x4_to_f16x2x2(w[kk], b0, b1);
-                        ptx::mma_f16_16816(sc[nb], qa[kk], b0, b1);
+                    if (!full_tile) {
+    #pragma unroll
+                        for (int e = 0; e < 4; ++e) {
+                            const int key = kbase + nb * 8 + (e & 1);
+                            const int lim = (e < 2) ? lim0 : lim1;
+                            if (key > lim || key <= ((e < 2) ? lo0 : lo1)) sc[nb][e] = -INFINITY;
+                            else if (TREE && key >= seg_prior &&
+                                     !((p.anc[b * p.T + (lim - seg_prior)] >> (key - seg_prior)) & 1ull))
+                                sc[nb][e] = -INFINITY;  // a draft token off this query's path to the root
+                        }
+                    }
+                    mx0 = fmaxf(mx0, fmaxf(sc[nb][0], sc[nb][1]));
+                    mx1 = fmaxf(mx1, fmaxf(sc[nb][2], sc[nb][3]));
+                }
+                mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, 1));
+                mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, 2));
+                mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, 1));
+                mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, 2));
+                mx0 *= sl2;  // -inf stays -inf
+                mx1 *= sl2;
+                const bool mv0 = mx0 > m0 + kLazyRescale, mv1 = mx1 > m1 + kLazyRescale;
+                if (mv0 || mv1) {
+                    const float n0 = mv0 ? mx0 : m0, n1 = mv1 ? mx1 : m1;
+                    const float al0 = (m0 == -INFINITY) ? 0.f : ptx::ex2(m0 - n0);
+                    const float al1 = (m1 == -INFINITY) ? 0.f : ptx::ex2(m1 - n1);
+                    l0 *= al0;
+                    l1 *= al1;
+    #pragma unroll
+                    for (int nb = 0; nb < D / 8; ++nb) {
+                        o[nb][0] *= al0;
+                        o[nb][1] *= al0;
+                        o[nb][2] *= al1;
+                        o[nb][3] *= al1;
+                    }
+                    m0 = n0;
+                    m1 = n1;
+                }
+                const float nmu0 = (m0 == -INFINITY) ? 0.f : -m0;
+                const float nmu1 = (m1 == -INFINITY) ? 0.f : -m1;
+                float ps0 = 0.f, ps1 = 0.f;
+    #pragma unroll
+                for (int nb = 0; nb < NBS; ++nb) {
+                    sc[nb][0] = ptx::ex2(fmaf(sc[nb][0], sl2, nmu0));
+                    sc[nb][1] = ptx::ex2(fmaf(sc[nb][1], sl2, nmu0));
+                    sc[nb][2] = ptx::ex2(fmaf(sc[nb][2], sl2, nmu1));
+                    sc[nb][3] = ptx::ex2(fmaf(sc[nb][3], sl2, nmu1));
+                    ps0 += sc[nb][0] + sc[nb][1];
+                    ps1 += sc[nb][2] + sc[nb][3];
+                }
+                l0 += ps0;
+                l1 += ps1;
+
+                // O += P V.
+    #pragma unroll
+                for (int kb = 0; kb < KB && F8; ++kb) {
+                    // P (f16) x V (E4M3 -> f16).  Output n-block jd, column
+                    // lane/4 = g stands for d = 16*g + jd, so this thread reads one
+                    // 16-byte chunk (g) of each of its four key rows, and the two
+                    // keys of a B register pair come from two rows (byte permute).
+                    uint32_t a[4];
+                    a[0] = ptx::pack_f16x2(sc[2 * kb][0], sc[2 * kb][1]);
+                    a[1] = ptx::pack_f16x2(sc[2 * kb][2], sc[2 * kb][3]);
+                    a[2] = ptx::pack_f16x2(sc[2 * kb + 1][0], sc[2 * kb + 1][1]);
+                    a[3] = ptx::pack_f16x2(sc[2 * kb + 1][2], sc[2 * kb + 1][3]);
+                    const int k0 = kp + kb * 16 + 2 * quad, g = lane >> 2;
+                    auto vrow = [&](int k) { return ptx::ld_shared_v4(sV + k * 128 + ((g ^ (k & 7)) << 4)); };
+                    const uint4 r0 = vrow(k0), r1 = vrow(k0 + 1), r8 = vrow(k0 + 8), r9 = vrow(k0 + 9);
+                    const uint32_t x0[4] = {r0.x, r0.y, r0.z, r0.w}, x1[4] = {r1.x, r1.y, r1.z, r1.w};
+                    const uint32_t x8[4] = {r8.x, r8.y, r8.z, r8.w}, x9[4] = {r9.x, r9.y, r9.z, r9.w};
+    #pragma unroll
+                    for (int i = 0; i < 4; ++i) {
+                        uint32_t b0[4], b1[4];  // n-blocks 4i .. 4i+3: keys (k0, k0+1) and (k0+8, k0+9)
+                        ptx::e4m3x4_to_f16x2x2(ptx::prmt(x0[i], x1[i], 0x5140), b0[0], b0[1]);
+                        ptx::e4m3x4_to_f16x2x2(ptx::prmt(x0[i], x1[i], 0x7362), b0[2], b0[3]);
+                        ptx::e4m3x4_to_f16x2x2(ptx::prmt(x8[i], x9[i], 0x5140), b1[0], b1[1]);
+                        ptx::e4m3x4_to_f16x2x2(ptx::prmt(x8[i], x9[i], 0x7362), b1[2], b1[3]);
+    #pragma unroll
+                        for (int m = 0; m < 4; ++m) ptx::mma_f16_16816(o[4 * i + m], a, b0[m], b1[m]);
                     }
                 }
-            } else {
-#pragma unroll
-                for (int kk = 0; kk < D / 16; ++kk) {
-#pragma unroll
-                    for (int kb = 0; kb < KB; ++kb) {
+    #pragma unroll
+                for (int kb = 0; kb < KB && !F8; ++kb) {
+                    uint32_t a[4];
+                    a[0] = ptx::pack_bf16x2(sc[2 * kb][0], sc[2 * kb][1]);
+                    a[1] = ptx::pack_bf16x2(sc[2 * kb][2], sc[2 * kb][3]);
+                    a[2] = ptx::pack_bf16x2(sc[2 * kb + 1][0], sc[2 * kb + 1][1]);
+                    a[3] = ptx::pack_bf16x2(sc[2 * kb + 1][2], sc[2 * kb + 1][3]);
+    #pragma unroll
+                    for (int dc = 0; dc < D / 16; ++dc) {
                         const int mi = lane >> 3;
-                        const int key = koff + kb * 16 + (mi >> 1) * 8 + (lane & 7);
-                        const int chunk = 2 * kk + (mi & 1);
-                        const uint32_t addr = sK + (chunk >> 3) * S::kHalfBytes + key * 128 + (((chunk & 7) ^ (key & 7)) << 4);
+                        const int key = kp + kb * 16 + (mi & 1) * 8 + (lane & 7);
+                        const int chunk = 2 * dc + (mi >> 1);
+                        const uint32_t addr = sV + (chunk >> 3) * S::kHalfBytes + key * 128 + (((chunk & 7) ^ (key & 7)) << 4);
                         uint32_t b0, b1, b2, b3;
-                        ptx::ldmatrix_x4(addr, b0, b1, b2, b3);
-                        ptx::mma_bf16_16816(sc[2 * kb], qa[kk], b0, b1);
-                        ptx::mma_bf16_16816(sc[2 * kb + 1], qa[kk], b2, b3);
+                        ptx::ldmatrix_x4_trans(addr, b0, b1, b2, b3);
+                        ptx::mma_bf16_16816(o[2 * dc], a, b0, b1);
+                        ptx::mma_bf16_16816(o[2 * dc + 1], a, b2, b3);
                     }
-                }
-            }
-
-            // Mask (diagonal / ragged tiles only) and online softmax in base 2.
-            // The row maximum is taken on the raw scores (the scale is
-            // positive) and the scale is folded into the exponent's FMA.  The
-            // reference used for the exponentials only moves when a row's
-            // maximum passes it by more than kLazyRescale (a factor 2^8 at
-            // most on p), and only then are O and l rescaled; O, l and the
-            // stored m share that reference, so the result is exact.
-            const int kbase = tile0 + koff + 2 * quad;
-            float mx0 = -INFINITY, mx1 = -INFINITY;
-#pragma unroll
-            for (int nb = 0; nb < NBS; ++nb) {
-                if (!full_tile) {
-#pragma unroll
-                    for (int e = 0; e < 4; ++e) {
-                        const int key = kbase + nb * 8 + (e & 1);
-                        const int lim = (e < 2) ? lim0 : lim1;
-                        if (key > lim || key <= ((e < 2) ? lo0 : lo1)) sc[nb][e] = -INFINITY;
-                        else if (TREE && key >= seg_prior &&
-                                 !((p.anc[b * p.T + (lim - seg_prior)] >> (key - seg_prior)) & 1ull))
-                            sc[nb][e] = -INFINITY;  // a draft token off this query's path to the root
-                    }
-                }
-                mx0 = fmaxf(mx0, fmaxf(sc[nb][0], sc[nb][1]));
-                mx1 = fmaxf(mx1, fmaxf(sc[nb][2], sc[nb][3]));
-            }
-            mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, 1));
-            mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, 2));
-            mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, 1));
-            mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, 2));
-            mx0 *= sl2;  // -inf stays -inf
-            mx1 *= sl2;
-            const bool mv0 = mx0 > m0 + kLazyRescale, mv1 = mx1 > m1 + kLazyRescale;
-            if (mv0 || mv1) {
-                const float n0 = mv0 ? mx0 : m0, n1 = mv1 ? mx1 : m1;
-                const float al0 = (m0 == -INFINITY) ? 0.f : ptx::ex2(m0 - n0);
-                const float al1 = (m1 == -INFINITY) ? 0.f : ptx::ex2(m1 - n1);
-                l0 *= al0;
-                l1 *= al1;
-#pragma unroll
-                for (int nb = 0; nb < D / 8; ++nb) {
-                    o[nb][0] *= al0;
-                    o[nb][1] *= al0;
-                    o[nb][2] *= al1;
-                    o[nb][3] *= al1;
-                }
-                m0 = n0;
-                m1 = n1;
-            }
-            const float nmu0 = (m0 == -INFINITY) ? 0.f : -m0;
-            const float nmu1 = (m1 == -INFINITY) ? 0.f : -m1;
-            float ps0 = 0.f, ps1 = 0.f;
-#pragma unroll
-            for (int nb = 0; nb < NBS; ++nb) {
-                sc[nb][0] = ptx::ex2(fmaf(sc[nb][0], sl2, nmu0));
-                sc[nb][1] = ptx::ex2(fmaf(sc[nb][1], sl2, nmu0));
-                sc[nb][2] = ptx::ex2(fmaf(sc[nb][2], sl2, nmu1));
-                sc[nb][3] = ptx::ex2(fmaf(sc[nb][3], sl2, nmu1));
-                ps0 += sc[nb][0] + sc[nb][1];
-                ps1 += sc[nb][2] + sc[nb][3];
-            }
-            l0 += ps0;
-            l1 += ps1;
-
-            // O += P V.
-#pragma unroll
-            for (int kb = 0; kb < KB && F8; ++kb) {
-                // P (f16) x V (E4M3 -> f16).  Output n-block jd, column
-                // lane/4 = g stands for d = 16*g + jd, so this thread reads one
-                // 16-byte chunk (g) of each of its four key rows, and the two
-                // keys of a B register pair come from two rows (byte permute).
-                uint32_t a[4];
-                a[0] = ptx::pack_f16x2(sc[2 * kb][0], sc[2 * kb][1]);
-                a[1] = ptx::pack_f16x2(sc[2 * kb][2], sc[2 * kb][3]);
-                a[2] = ptx::pack_f16x2(sc[2 * kb + 1][0], sc[2 * kb + 1][1]);
-                a[3] = ptx::pack_f16x2(sc[2 * kb + 1][2], sc[2 * kb + 1][3]);
-                const int k0 = koff + kb * 16 + 2 * quad, g = lane >> 2;
-                auto vrow = [&](int k) { return ptx::ld_shared_v4(sV + k * 128 + ((g ^ (k & 7)) << 4)); };
-                const uint4 r0 = vrow(k0), r1 = vrow(k0 + 1), r8 = vrow(k0 + 8), r9 = vrow(k0 + 9);
-                const uint32_t x0[4] = {r0.x, r0.y, r0.z, r0.w}, x1[4] = {r1.x, r1.y, r1.z, r1.w};
-                const uint32_t x8[4] = {r8.x, r8.y, r8.z, r8.w}, x9[4] = {r9.x, r9.y, r9.z, r9.w};
-#pragma unroll
-                for (int i = 0; i < 4; ++i) {
-                    uint32_t b0[4], b1[4];  // n-blocks 4i .. 4i+3: keys (k0, k0+1) and (k0+8, k0+9)
-                    ptx::e4m3x4_to_f16x2x2(ptx::prmt(x0[i], x1[i], 0x5140), b0[0], b0[1]);
-                    ptx::e4m3x4_to_f16x2x2(ptx::prmt(x0[i], x1[i], 0x7362), b0[2], b0[3]);
-                    ptx::e4m3x4_to_f16x2x2(ptx::prmt(x8[i], x9[i], 0x5140), b1[0], b1[1]);
-                    ptx::e4m3x4_to_f16x2x2(ptx::prmt(x8[i], x9[i], 0x7362), b1[2], b1[3]);
-#pragma unroll
-                    for (int m = 0; m < 4; ++m) ptx::mma_f16_16816(o[4 * i + m], a, b0[m], b1[m]);
-                }
-            }
-#pragma unroll
-            for (int kb = 0; kb < KB && !F8; ++kb) {
-                uint32_t a[4];
-                a[0] = ptx::pack_bf16x2(sc[2 * kb][0], sc[2 * kb][1]);
-                a[1] = ptx::pack_bf16x2(sc[2 * kb][2], sc[2 * kb][3]);
-                a[2] = ptx::pack_bf16x2(sc[2 * kb + 1][0], sc[2 * kb + 1][1]);
-                a[3] = ptx::pack_bf16x2(sc[2 * kb + 1][2], sc[2 * kb + 1][3]);
-#pragma unroll
-                for (int dc = 0; dc < D / 16; ++dc) {
-                    const int mi = lane >> 3;
-                    const int key = koff + kb * 16 + (mi & 1) * 8 + (lane & 7);
-                    const int chunk = 2 * dc + (mi >> 1);
-                    const uint32_t addr = sV + (chunk >> 3) * S::kHalfBytes + key * 128 + (((chunk & 7) ^ (key & 7)) << 4);
-                    uint32_t b0, b1, b2, b3;
-                    ptx::ldmatrix_x4_trans(addr, b0, b1, b2, b3);
-                    ptx::mma_bf16_16816(o[2 * dc], a, b0, b1);
-                    ptx::mma_bf16_16816(o[2 * dc + 1], a, b2, b3);
                 }
             }
 

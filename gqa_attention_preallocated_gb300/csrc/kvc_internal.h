@@ -41,10 +41,10 @@ constexpr int kKeyTile = 64;
 constexpr int kHeadDimBf16 = 128;
 constexpr int kHeadDimSmall = 64;
 // Keys per split-KV tile: 64, or 128 for bf16 storage of head width
-// kHeadDimSmall (a 64-key tile there would carry half the bytes of a
-// 128-wide one for the same per-tile work).
+// kHeadDimSmall and for FP8 storage (a 64-key tile there would carry half the
+// bytes of a bf16 128-wide one for the same per-tile work).
 __host__ __device__ constexpr int key_tile_keys(int d, bool fp8) {
-    return (d == kHeadDimSmall && !fp8) ? 2 * kKeyTile : kKeyTile;
+    return ((d == kHeadDimSmall && !fp8) || fp8) ? 2 * kKeyTile : kKeyTile;
 }
 // FP8 E4M3 caches: one K and one V scale per KV head (at most this many heads).
 constexpr int kMaxScaleHeads = 64;
