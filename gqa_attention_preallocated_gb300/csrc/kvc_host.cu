@@ -65,10 +65,11 @@ namespace {
 // Measured on the verify shape (B = 64, S = 4096): bf16 at 8 rows, the
 // split-KV kernel is ahead by about 2 %, at 16 rows the tcgen05 kernel by
 // about 3 %.  An FP8 cache converts its tiles in shared memory on the tcgen05
-// kernel, so there the split-KV kernel leads up to 16 rows (427 K against
-// 303 K tokens/s at 16) and the tcgen05 kernel from 32 (1.7x at 64).
+// kernel, so there the split-KV kernel (128-key FP8 tiles) leads up to 32
+// rows (2,855 against 2,484 GB/s at 32) and the tcgen05 kernel from 64 (2,524
+// against 1,670).
 constexpr int kTcMinRows = 12;
-constexpr int kTcMinRowsFp8 = 16;
+constexpr int kTcMinRowsFp8 = 32;
 int tc_min_rows(const kvc_cache* c) { return c->dtype == KVC_FP8_E4M3 ? kTcMinRowsFp8 : kTcMinRows; }
 // Caches served by the generic kernel (attn_f32.cu) only: fp32 storage, and
 // bf16 or FP8 storage whose head dimension has no TMA kernel (the split-KV

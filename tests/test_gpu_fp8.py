@@ -100,7 +100,7 @@ def _step(cache, orc, seed, ci, G, n_new, T=None, parents=None):
     [
         (4, 2, 4, [300, 1, 1, 1]),        # prefill (tensor-core kernel), then decode (split-KV, append fused)
         (3, 2, 4, [200, 4, 4]),           # verify at 16 rows (split-KV kernel, append fused)
-        (2, 2, 8, [150, 4, 8, 1]),        # 32 and 64 rows per KV head
+        (2, 2, 8, [150, 4, 8, 1]),        # 32 rows (split-KV) and 64 rows (tensor-core) per KV head
         (2, 1, 1, [77, 5, 16, 1]),        # MHA
         (1, 8, 4, [1, 63, 64, 65, 129]),  # tile boundaries
         (2, 2, 8, [150, 40, 17, 12]),     # packed rows on the tensor-core kernel: 320, 136 and 96 rows
