@@ -429,6 +429,25 @@ def test_prefill_chunk_every_unit_of_a_row(ragged):
     _decode_case(s, s.Hq, priors, [T], [nn], 3, units)
 
 
+@pytest.mark.parametrize("G,tails", [(4, [1, 31, 32, 33]), (8, [64, 65, 96, 97]), (3, [127, 40, 5, 100])])
+def test_prefill_ragged_tails(G, tails):
+    """Chunks of T >= 128 whose rows end in a partial 128-position block, with
+    tails around every 32-row boundary and head counts that leave a head pair
+    with one head; every output of both calls is compared with the oracle (the
+    first call's rows end in tails of 116, 20 and 80 positions)."""
+    B, Hkv = 4, 2
+    priors = np.array([500, 1300, 0, 2000])
+    chunk = np.array([128 + t for t in tails])
+    _run_calls(17, B, Hkv, G, 128, 2000 + 300, torch.bfloat16, [priors, chunk])
+
+
+def test_prefill_ragged_tail_cut_and_merged():
+    """A long row with a partial last block on few items: the schedule cuts
+    the items, the tail block's among them, and their pieces are merged in the
+    launch; every output against the oracle."""
+    _run_calls(23, 1, 4, 4, 128, 6300, torch.bfloat16, [np.array([6000]), np.array([200])])
+
+
 @pytest.mark.parametrize("B,Hkv,G,prior,T", [(1, 2, 4, 3000, 256), (2, 1, 2, 700, 200), (1, 1, 3, 2500, 130)])
 def test_prefill_few_long_items(B, Hkv, G, prior, T):
     """Few long prefill items on many SMs, every output compared (odd G also
