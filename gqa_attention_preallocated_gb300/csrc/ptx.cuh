@@ -84,14 +84,6 @@ __device__ __forceinline__ void tma_load_2d(uint32_t dst, const void* desc, int 
         : "memory");
 }
 
-// Prefetch one box of a tiled tensor into L2 (no shared memory, no barrier).
-__device__ __forceinline__ void tma_prefetch_l2_2d(const void* desc, int x, int y) {
-    asm volatile("cp.async.bulk.prefetch.tensor.2d.L2.global.tile [%0, {%1, %2}];" ::"l"(
-                     reinterpret_cast<uint64_t>(desc)),
-                 "r"(x), "r"(y)
-                 : "memory");
-}
-
 // ---- warp-level tensor core path (used where G*T <= 64 rows) -------------------
 __device__ __forceinline__ void ldmatrix_x4(uint32_t addr, uint32_t& r0, uint32_t& r1, uint32_t& r2, uint32_t& r3) {
     asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0,%1,%2,%3}, [%4];"
