@@ -512,6 +512,42 @@ def test_longctx_layer_sampled():
     _decode_case(s, s.Hq, lens0, [1, 1], [np.ones(s.B, dtype=np.int64)] * 2, 5, units)
 
 
+@pytest.mark.parametrize("T,G,d", [(1, 4, 128), (4, 2, 128), (1, 4, 64)])
+def test_decode_score_jumps(T, G, d):
+    """Decode and short verify on the split-KV kernel with scores that jump by
+    tens to hundreds (log2 units) at keys spread over a 3,000-key row: the
+    running maximum moves inside a warp's tiles, and the combine merges
+    partials whose maxima differ by that much (each unit is cut across CTAs
+    and warps); every output against the oracle."""
+    _cuda_or_skip()
+    B, Hkv, prior = 2, 2, 3000
+    max_len = prior + T + 8
+    rng = np.random.default_rng(13)
+    u = np.ones(d)
+    k0 = rng.standard_normal((B, Hkv, prior, d))
+    for pos, alpha in ((300, 0.5), (1100, 1.5), (1900, 4.0), (2950, 4.0)):
+        k0[:, :, pos] = alpha * u + 0.1 * rng.standard_normal(d)
+    v0 = rng.standard_normal((B, Hkv, prior, d))
+    kn = rng.standard_normal((B, Hkv, T, d))
+    vn = rng.standard_normal((B, Hkv, T, d))
+    q = rng.standard_normal((B, Hkv * G, T, d)) + 3.0 * u
+    k0s, v0s, kns, vns, qs = (_store(torch.from_numpy(x), torch.bfloat16) for x in (k0, v0, kn, vn, q))
+    cache = KVCache(1, B, Hkv, max_len, d)
+    cache.k[0].fill_(float("nan"))
+    cache.v[0].fill_(float("nan"))
+    cache.append(0, k0s.cuda(), v0s.cuda(), [prior] * B)
+    out = cache.append_attention(0, qs.cuda(), kns.cuda(), vns.cuda(), [T] * B)
+    orc = ref.OracleCache(1, B, Hkv, max_len, d)
+    ref.append_attention(orc, 0, np.zeros((B, Hkv * G, prior, d)), k0s.double().numpy(), v0s.double().numpy(),
+                         [prior] * B)
+    want = ref.append_attention(orc, 0, qs.double().numpy(), kns.double().numpy(), vns.double().numpy(), [T] * B)
+    got = out.double().cpu().numpy()
+    assert np.all(np.isfinite(got))
+    err = float(np.max(np.abs(got - want)))
+    assert err <= 2e-2, err
+    assert cache.device_status() == 0
+
+
 @pytest.mark.parametrize("T", [256, 200])
 def test_prefill_score_jumps(T):
     """Scores that jump by about 25, 75 and 200 (log2 units) at keys further into
