@@ -221,7 +221,7 @@ kvc_status kvc_append_attention_tree(kvc_cache* c, int layer, const void* q, con
  * Its scratch is one static device array of KVC_NOALLOC_SCRATCH_BYTES
  * (32 MiB) inside the library: every GPU that loads the library holds it
  * until the process exits.  No cudaMalloc, cudaFree or other allocating
- * call is made.  Calls with more than 12 query rows per KV head (G * T; 16
+ * call is made.  Calls with more than 12 query rows per KV head (G * T; 32
  * for FP8 caches) run on the tensor-core kernel, which needs only the workspace header and
  * uses the rest of the array for the partials of the items it cuts; they
  * always fit.  A call with fewer rows per KV head whose split-KV
@@ -346,8 +346,8 @@ kvc_status kvc_lens_from_device(kvc_cache* c, void* stream);
  * n_new[b] rows of k_new / v_new [B, Hkv, T, d] at row b's device length, then
  * the T queries q [B, Hq, T, d] attend exactly as in kvc_gqa_attention, and
  * the device lengths advance by n_new.  n_new is a device int32 [B].  bf16
- * and FP8 caches of d = 128 with G * T <= 16 query rows per KV head (decode
- * and short verify).
+ * and FP8 caches of d = 128, and bf16 caches of d = 64, with G * T <= 16 query
+ * rows per KV head (decode and short verify).
  * Three kernels are enqueued (device plan, attention with the append fused
  * in, combine), with nothing read from the host that changes per step, so
  * the call can be captured in a CUDA graph and replayed with new contents of
