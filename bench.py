@@ -253,7 +253,7 @@ class Workload:
     @property
     def tc_min_rows(self):
         """Query rows per KV head above which the library runs attention on the tcgen05 kernel."""
-        return 16 if self.kv_dtype == "fp8" else 12
+        return 32 if self.kv_dtype == "fp8" else 12
 
     @property
     def tensor_core(self):
@@ -273,8 +273,9 @@ class Workload:
 
     @property
     def fused(self):
-        """The library appends inside the attention launch whenever the split-KV kernel runs it."""
-        return not self.tensor_core
+        """The library appends inside the attention launch when the split-KV kernel runs it on one
+        16-row MMA tile per KV head (up to 16 query rows)."""
+        return not self.tensor_core and (self.Hq // self.shape.Hkv) * self.T <= 16
 
     def kernel_bytes(self, i):
         """Algorithmic bytes of the timed attention call: live K/V + q + out (+ the append when fused)."""
@@ -421,38 +422,54 @@ def run_graph(w: Workload, cache, steps: int, q, k, v):
 def run_e2e(w: Workload, cache, steps: int, q, k, v):
     """Same steps through the public API with the step's inputs in pinned host memory.
 
-    Per step: host->device copy of q, k_new, v_new; append + attention; device->host copy of out.
-    The copies run on a second stream with double-buffered device inputs and outputs, so step i+1's
-    inputs and step i's output move while step i computes (every step still moves all its bytes;
-    the timed region ends when the last output has reached the host).
+    Per step: one host->device copy of q, k_new and v_new (laid end to end in one pinned buffer, the
+    three call arguments are views of its device copy); append + attention; device->host copy of out.
+    Inputs move on one copy stream and outputs on another, with double-buffered device inputs and
+    outputs, so step i+1's inputs and step i's output move, in opposite directions at once, while
+    step i computes (every step still moves all its bytes; the timed region ends when the last output
+    has reached the host).  Afterwards the last step runs again through the device-resident path from
+    the same cache state, and its output is compared bit for bit with what reached the host.
     """
     n_distinct = len(q)
-    hq = [t.cpu().pin_memory() for t in q]
-    hk = [t.cpu().pin_memory() for t in k]
-    hv = [t.cpu().pin_memory() for t in v]
-    dq = [torch.empty_like(q[0]) for _ in range(2)]
-    dk = [torch.empty_like(k[0]) for _ in range(2)]
-    dv = [torch.empty_like(v[0]) for _ in range(2)]
+    args = (q[0], k[0], v[0])
+    sizes = [t.numel() for t in args]
+    offs = [0]
+    for n in sizes:
+        offs.append(offs[-1] + (n + 127) // 128 * 128)  # every view starts 256-byte aligned
+
+    def packed(j):
+        h = torch.empty(offs[-1], dtype=torch.bfloat16, pin_memory=True)
+        for t, o, n in zip((q[j], k[j], v[j]), offs, sizes):
+            h[o:o + n].copy_(t.reshape(-1))
+        return h
+
+    hin = [packed(j) for j in range(n_distinct)]
+    din = [torch.empty(offs[-1], dtype=torch.bfloat16, device=q[0].device) for _ in range(2)]
+    views = [[din[b][o:o + n].view(t.shape) for t, o, n in zip(args, offs, sizes)] for b in range(2)]
     out = [torch.empty_like(q[0]) for _ in range(2)]
     hout = [torch.empty(q[0].shape, dtype=q[0].dtype, pin_memory=True) for _ in range(2)]
     ws = cache.workspace(w.Hq, w.T)
     stream = torch.cuda.current_stream()
-    copy = torch.cuda.Stream()
+    h2d, d2h = torch.cuda.Stream(), torch.cuda.Stream()
     ev = lambda: torch.cuda.Event()  # noqa: E731
     in_ready, computed, out_copied = [ev(), ev()], [ev(), ev()], [ev(), ev()]
     cache.truncate(w.lens0)
     torch.cuda.synchronize()
     start, stop = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     start.record(stream)
-    copy.wait_stream(stream)
+    h2d.wait_stream(stream)
+    d2h.wait_stream(stream)
 
-    def load(i):  # step i's inputs into buffer i % 2 (on the copy stream)
-        b, j = i % 2, i % n_distinct
-        with torch.cuda.stream(copy):
-            dq[b].copy_(hq[j], non_blocking=True)
-            dk[b].copy_(hk[j], non_blocking=True)
-            dv[b].copy_(hv[j], non_blocking=True)
-            in_ready[b].record(copy)
+    def load(i):  # step i's inputs into buffer i % 2 (on the input stream)
+        b = i % 2
+        with torch.cuda.stream(h2d):
+            din[b].copy_(hin[i % n_distinct], non_blocking=True)
+            in_ready[b].record(h2d)
+
+    def compute(b, dst):
+        qb, kb, vb = views[b]
+        for layer in range(w.layers):
+            cache.append_attention(layer, qb, kb, vb, w.n_new, out=dst, workspace=ws)
 
     load(0)
     for i in range(steps):
@@ -462,24 +479,34 @@ def run_e2e(w: Workload, cache, steps: int, q, k, v):
         stream.wait_event(in_ready[b])
         if i >= 2:
             stream.wait_event(out_copied[b])  # out[b] of step i-2 has reached the host
-        for layer in range(w.layers):
-            cache.append_attention(layer, dq[b], dk[b], dv[b], w.n_new, out=out[b], workspace=ws)
+        compute(b, out[b])
         computed[b].record(stream)
         if i + 1 < steps:
             if i >= 1:
-                copy.wait_event(computed[1 - b])  # step i-1 no longer reads buffer 1-b
+                h2d.wait_event(computed[1 - b])  # step i-1 no longer reads buffer 1-b
             load(i + 1)
-        with torch.cuda.stream(copy):
-            copy.wait_event(computed[b])
+        with torch.cuda.stream(d2h):
+            d2h.wait_event(computed[b])
             hout[b].copy_(out[b], non_blocking=True)
-            out_copied[b].record(copy)
-    stream.wait_stream(copy)
+            out_copied[b].record(d2h)
+    stream.wait_stream(d2h)
     stop.record(stream)
     torch.cuda.synchronize()
     ms = start.elapsed_time(stop)
+
+    # The last step once more from the lengths it started from, on its device-resident inputs.
+    last = steps - 1
+    if steps > 0:
+        cache.truncate(w.lens_at(last) - w.n_new)
+        check = torch.empty_like(q[0])
+        compute(last % 2, check)
+        torch.cuda.synchronize()
+        matches = bool(torch.equal(check.cpu(), hout[last % 2]))
+    else:
+        matches = None
     work = sum(w.work(i) for i in range(steps))
-    h2d = (q[0].numel() + k[0].numel() + v[0].numel()) * 2
-    return {"ms": ms, "work": work, "h2d": h2d, "d2h": q[0].numel() * 2}
+    h2d_bytes = offs[-1] * 2  # the packed buffer as copied (alignment gaps included)
+    return {"ms": ms, "work": work, "h2d": h2d_bytes, "d2h": q[0].numel() * 2, "matches_device": matches}
 
 
 # ---------------------------------------------------------------------------
@@ -611,6 +638,9 @@ def native_line(w: Workload, args, world: int, rank: int, cpu_budget_s: float = 
     ms, e2e_ms, graph_ms = max_over_ranks([res["ms"], res["e2e"]["ms"], graph_ms], world, "cuda")
     value = whole_job_value(res["work"], world, ms, scale)
     e2e_value = whole_job_value(res["e2e"]["work"], world, e2e_ms, scale)
+    if res["e2e"]["matches_device"] is False:
+        print(f"bench: {w.config()['workload']}: the end-to-end leg's last output differs from the "
+              "device-resident run of the same step", file=sys.stderr)
 
     hbm, bf16, bf16_sus, peak_kind = _peaks()
     attn_ms = float(res["attn_ms"])
@@ -635,7 +665,8 @@ def native_line(w: Workload, args, world: int, rank: int, cpu_budget_s: float = 
         "config": dict(w.config(), parallelism="replicas only" if world > 1 else "single GPU"),
         "roofline": roof,
         "e2e": {"value": e2e_value, "unit": w.unit, "h2d_bytes_per_step": res["e2e"]["h2d"],
-                "d2h_bytes_per_step": res["e2e"]["d2h"]},
+                "d2h_bytes_per_step": res["e2e"]["d2h"],
+                "last_output_matches_device": res["e2e"]["matches_device"]},
         "gpu_launches": res["launches"],
         "clocks": res["clocks"],
         "device_status": res["status"],

@@ -47,3 +47,34 @@ def test_decode_bytes_are_the_live_cache():
     # the FP8 cache reads one byte a value
     w8 = bench.Workload("decode8b", kv_dtype="fp8")
     assert w8.work(0) * 2 == w.work(0)
+
+
+def _library_row_limits():
+    """The library's routing limits, read from its host source: query rows per KV head above
+    which attention runs on the tcgen05 kernel (bf16, FP8), and the rows of the one MMA tile
+    under which the split-KV kernel appends inside its attention launch."""
+    import pathlib
+    import re
+    src = (pathlib.Path(bench.__file__).parent / "gqa_attention_preallocated_gb300" / "csrc" / "kvc_host.cu").read_text()
+    bf16 = int(re.search(r"constexpr int kTcMinRows = (\d+);", src).group(1))
+    fp8 = int(re.search(r"constexpr int kTcMinRowsFp8 = (\d+);", src).group(1))
+    mt1 = int(re.search(r"pl->mt = pl->R <= (\d+) \? 1", src).group(1))
+    assert re.search(r"pl\.mt == 1 && max_n > 0 && \(pl\.R <= tc_min_rows\(c\)", src)  # the fused-append rule
+    return bf16, fp8, mt1
+
+
+def test_bench_kernel_labels_follow_the_library_routing():
+    bf16, fp8, mt1 = _library_row_limits()
+    for kv_dtype, limit in (("bf16", bf16), ("fp8", fp8)):
+        for t, g in ((1, 1), (2, 4), (4, 4), (8, 2), (4, 8), (8, 4), (8, 8), (16, 8)):
+            w = bench.Workload("verify", verify_t=t, verify_g=g, kv_dtype=kv_dtype)
+            rows = g * t
+            assert w.tensor_core == (rows > limit), (kv_dtype, t, g)
+            assert w.fused == (rows <= limit and rows <= mt1), (kv_dtype, t, g)
+            assert w.kernel_source == ("prefill_tc.cu" if rows > limit else "decode_bf16.cu")
+    # decode and long-context steps are one row per query head: split-KV with the append fused in
+    for name in ("decode8b", "longctx"):
+        for kv_dtype in ("bf16", "fp8"):
+            w = bench.Workload(name, kv_dtype=kv_dtype)
+            assert not w.tensor_core and w.fused
+    assert bench.Workload("prefill").tensor_core
