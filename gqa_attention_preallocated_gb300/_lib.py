@@ -40,6 +40,8 @@ SIGNATURES = [
     ("kvc_append_attention", _I, [_VP, _I, _VP, _VP, _VP, _I, _I, _I32P, _VP, _VP, _SZ, _VP]),
     ("kvc_gqa_attention_tree", _I, [_VP, _I, _VP, _I, _I, _I32P, _I32P, _VP, _VP, _SZ, _VP]),
     ("kvc_append_attention_tree", _I, [_VP, _I, _VP, _VP, _VP, _I, _I, _I32P, _I32P, _VP, _VP, _SZ, _VP]),
+    ("kvc_append_attention_host", _I, [_VP, _I, _VP, _VP, _VP, _I, _I, _I32P, _VP, _VP, _SZ, _VP]),
+    ("kvc_host_copies_done", _I, [_VP, _VP]),
     ("kvc_gqa_attention_noalloc", _I, [_VP, _I, _VP, _I, _I, _I32P, _VP, _VP]),
     ("kvc_noalloc_status", _I, [_VP, _I32P]),
     ("kvc_set_window", _I, [_VP, _I, _I]),

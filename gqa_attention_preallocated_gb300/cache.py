@@ -225,6 +225,34 @@ class KVCache:
                                          0 if ws is None else ws.numel(), _stream_ptr(self.device, stream)))
         return out
 
+    def append_attention_host(self, layer: int, q: torch.Tensor, k_new: torch.Tensor, v_new: torch.Tensor, n_new,
+                              out: torch.Tensor, workspace: torch.Tensor | None = None, stream=None) -> torch.Tensor:
+        """``append_attention`` on CPU tensors (page-locked for the copies to overlap).
+
+        The library copies positions t < n_new[b] of q, k_new and v_new to its
+        own device staging, runs the step on ``stream`` and copies those
+        positions of out back; out's other positions are left as they were.
+        Returns once enqueued: after ``host_copies_done`` and a synchronize of
+        that stream, ``out`` holds the result and the inputs may change.
+        """
+        if q.dim() != 4:
+            raise KVCError(1, "q must be [B, Hq, T, d]")
+        B, Hq, T, d = q.shape
+        for t, shape, name in ((q, (self.B, Hq, T, self.d), "q"), (k_new, (self.B, self.Hkv, T, self.d), "k_new"),
+                               (v_new, (self.B, self.Hkv, T, self.d), "v_new"), (out, (self.B, Hq, T, self.d), "out")):
+            if tuple(t.shape) != shape or t.dtype != self.io_dtype or not t.is_contiguous() or t.device.type != "cpu":
+                raise KVCError(1, f"{name} must be a contiguous {self.io_dtype} CPU tensor of shape {shape}")
+        ws = workspace if workspace is not None else self.workspace(Hq, T)
+        nn = _i32(n_new, self.B)
+        check(lib().kvc_append_attention_host(self._h, layer, _ptr(q), _ptr(k_new), _ptr(v_new), Hq, T,
+                                              nn.ctypes.data_as(_I32P), _ptr(out), _ptr(ws),
+                                              0 if ws is None else ws.numel(), _stream_ptr(self.device, stream)))
+        return out
+
+    def host_copies_done(self, stream=None) -> None:
+        """Make ``stream`` wait for every output copy of the host-buffer calls enqueued so far."""
+        check(lib().kvc_host_copies_done(self._h, _stream_ptr(self.device, stream)))
+
     # ------------------------------------------------ device-resident lengths
     def lens_to_device(self, stream=None) -> torch.Tensor:
         """Hand the lengths over to a device array (int32 [layers, B]) owned by this object.

@@ -56,6 +56,17 @@ struct kvc_cache {
     // Paged storage (table set): buffers [num_pages, Hkv, page, d], a device
     // block table [B, mpr]; max_len is the logical capacity mpr * page.
     Paging pg{nullptr, 0, 0, 0};
+    // Host-buffer calls (kvc_append_attention_host): two device staging slots
+    // (q, k_new, v_new, out of one call each) used in turn, the two copy
+    // streams (inputs in, outputs out) and each slot's events.
+    struct HostSlot {
+        void* buf = nullptr;
+        size_t bytes = 0;
+        cudaEvent_t in_ready = nullptr, computed = nullptr, out_done = nullptr;
+    };
+    HostSlot hslot[2];
+    int hnext = 0;
+    cudaStream_t h2d = nullptr, d2h = nullptr;
 };
 
 namespace {
@@ -838,6 +849,68 @@ kvc_status check_host_lens(const kvc_cache* c) {
     return ok();
 }
 
+// Helpers of the host-buffer calls (kvc_append_attention_host).
+namespace {
+
+// Bytes of one element of q, k_new, v_new and out (bf16 for an FP8 cache).
+size_t io_esize(const kvc_cache* c) { return c->dtype == KVC_FP8_E4M3 ? 2 : static_cast<size_t>(c->esize); }
+
+size_t round256(size_t x) { return (x + 255) / 256 * 256; }
+
+// Streams, events and two staging slots of at least `bytes` each.  A slot that
+// grows is freed only after the calls that used it have finished with it.
+kvc_status ensure_host_staging(kvc_cache* c, size_t bytes) {
+    cudaError_t e = cudaSuccess;
+    if (!c->h2d) {
+        e = cudaStreamCreateWithFlags(&c->h2d, cudaStreamNonBlocking);
+        if (e == cudaSuccess) e = cudaStreamCreateWithFlags(&c->d2h, cudaStreamNonBlocking);
+        for (auto& hs : c->hslot)
+            for (cudaEvent_t* ev : {&hs.in_ready, &hs.computed, &hs.out_done})
+                if (e == cudaSuccess) e = cudaEventCreateWithFlags(ev, cudaEventDisableTiming);
+        if (e != cudaSuccess) return cuda_fail(e, "host-call streams / events");
+    }
+    for (auto& hs : c->hslot) {
+        if (hs.bytes >= bytes) continue;
+        if (hs.buf) {
+            e = cudaEventSynchronize(hs.computed);
+            if (e == cudaSuccess) e = cudaEventSynchronize(hs.out_done);
+            if (e == cudaSuccess) e = cudaStreamSynchronize(c->h2d);
+            if (e == cudaSuccess) e = cudaFree(hs.buf);
+            hs.buf = nullptr;
+            hs.bytes = 0;
+            if (e != cudaSuccess) return cuda_fail(e, "host-call staging release");
+        }
+        e = cudaMalloc(&hs.buf, bytes);
+        if (e != cudaSuccess) {
+            hs.buf = nullptr;
+            return cuda_fail(e, "host-call staging allocation");
+        }
+        hs.bytes = bytes;
+    }
+    return ok();
+}
+
+// Copy positions t < n_new[b] of a [B, H, T, d] tensor: the whole tensor in
+// one copy when every row is full, else one 2-D copy per row (H runs of
+// n_new[b] rows of `row_bytes`, pitch T rows).  Nothing else is touched.
+cudaError_t copy_chunk(void* dst, const void* src, int B, int H, int T, size_t row_bytes, const int32_t* n_new,
+                       cudaMemcpyKind kind, cudaStream_t st) {
+    bool full = true;
+    for (int b = 0; b < B; ++b) full = full && n_new[b] == T;
+    const size_t pitch = static_cast<size_t>(T) * row_bytes, per_row = static_cast<size_t>(H) * pitch;
+    if (full) return cudaMemcpyAsync(dst, src, static_cast<size_t>(B) * per_row, kind, st);
+    for (int b = 0; b < B; ++b) {
+        if (n_new[b] == 0) continue;
+        cudaError_t e = cudaMemcpy2DAsync(static_cast<char*>(dst) + b * per_row, pitch,
+                                          static_cast<const char*>(src) + b * per_row, pitch,
+                                          static_cast<size_t>(n_new[b]) * row_bytes, H, kind, st);
+        if (e != cudaSuccess) return e;
+    }
+    return cudaSuccess;
+}
+
+}  // namespace
+
 extern "C" {
 
 kvc_status kvc_create(kvc_cache** out, int layers, int batch, int kv_heads, int max_len, int head_dim,
@@ -931,7 +1004,22 @@ kvc_status kvc_create_paged(kvc_cache** out, int layers, int batch, int kv_heads
     return ok();
 }
 
-void kvc_destroy(kvc_cache* c) { delete c; }
+void kvc_destroy(kvc_cache* c) {
+    if (c && c->h2d) {
+        // Host-buffer calls may still be copying: let them finish first.
+        cudaStreamSynchronize(c->h2d);
+        cudaStreamSynchronize(c->d2h);
+        for (auto& hs : c->hslot) {
+            if (hs.computed) cudaEventSynchronize(hs.computed);
+            if (hs.buf) cudaFree(hs.buf);
+            for (cudaEvent_t e : {hs.in_ready, hs.computed, hs.out_done})
+                if (e) cudaEventDestroy(e);
+        }
+        cudaStreamDestroy(c->h2d);
+        cudaStreamDestroy(c->d2h);
+    }
+    delete c;
+}
 
 kvc_status kvc_append(kvc_cache* c, int layer, const void* k_new, const void* v_new, int T, const int32_t* n_new,
                       void* stream) {
@@ -1073,6 +1161,82 @@ kvc_status kvc_append_attention_tree(kvc_cache* c, int layer, const void* q, con
     if (c && c->B > 0 && !parents) return fail(KVC_ERR_ARG, "parents is null");
     return append_attention_impl(c, layer, q, k_new, v_new, q_heads, T, n_new, parents, out, workspace,
                                  workspace_bytes, stream);
+}
+
+// ---------------------------------------------------------------------------
+// Host-buffer form of append + attention
+// ---------------------------------------------------------------------------
+
+kvc_status kvc_append_attention_host(kvc_cache* c, int layer, const void* q_host, const void* k_host,
+                                     const void* v_host, int q_heads, int T, const int32_t* n_new, void* out_host,
+                                     void* workspace, size_t workspace_bytes, void* stream) {
+    if (!c) return fail(KVC_ERR_ARG, "handle is null");
+    // Everything the device call checks, checked here first on the host
+    // pointers (null, 16-byte alignment, shapes, lengths): an error enqueues
+    // nothing and reads none of the host buffers.
+    kvc_status s = check_host_lens(c);
+    if (s) return s;
+    int max_n = 0;
+    s = validate_append(c, layer, k_host, v_host, T, n_new, &max_n);
+    if (s) return s;
+    std::vector<int64_t> after(c->B);
+    const int64_t* lens = c->lens.data() + static_cast<size_t>(layer) * c->B;
+    for (int b = 0; b < c->B; ++b) after[b] = lens[b] + n_new[b];
+    AttnPlan pl;
+    s = validate_attention(c, layer, q_host, q_heads, T, n_new, out_host, after.data(), &pl, 0);
+    if (s) return s;
+    if (c->B == 0 || T == 0) return ok();
+    s = ensure_device(c);
+    if (s) return s;
+    s = plan_shape(c, q_heads, T, c->num_sms, &pl);
+    if (s) return s;
+    s = check_workspace(c, pl, workspace, workspace_bytes);
+    if (s) return s;
+
+    const size_t row = static_cast<size_t>(c->d) * io_esize(c);
+    const size_t q_bytes = static_cast<size_t>(c->B) * q_heads * T * row;
+    const size_t kv_bytes = static_cast<size_t>(c->B) * c->Hkv * T * row;
+    const size_t off_k = round256(q_bytes), off_v = off_k + round256(kv_bytes), off_o = off_v + round256(kv_bytes);
+    s = ensure_host_staging(c, off_o + round256(q_bytes));
+    if (s) return s;
+    kvc_cache::HostSlot& hs = c->hslot[c->hnext];
+    char* dev = static_cast<char*>(hs.buf);
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+
+    // Inputs into this slot once the last call that read it has computed.
+    cudaError_t e = cudaStreamWaitEvent(c->h2d, hs.computed, 0);
+    if (e == cudaSuccess) e = copy_chunk(dev, q_host, c->B, q_heads, T, row, n_new, cudaMemcpyHostToDevice, c->h2d);
+    if (e == cudaSuccess)
+        e = copy_chunk(dev + off_k, k_host, c->B, c->Hkv, T, row, n_new, cudaMemcpyHostToDevice, c->h2d);
+    if (e == cudaSuccess)
+        e = copy_chunk(dev + off_v, v_host, c->B, c->Hkv, T, row, n_new, cudaMemcpyHostToDevice, c->h2d);
+    if (e == cudaSuccess) e = cudaEventRecord(hs.in_ready, c->h2d);
+    // The step waits for its inputs and for the slot's previous output to have left.
+    if (e == cudaSuccess) e = cudaStreamWaitEvent(st, hs.in_ready, 0);
+    if (e == cudaSuccess) e = cudaStreamWaitEvent(st, hs.out_done, 0);
+    if (e != cudaSuccess) return cuda_fail(e, "host-call input copies");
+    c->hnext ^= 1;
+    s = append_attention_impl(c, layer, dev, dev + off_k, dev + off_v, q_heads, T, n_new, nullptr, dev + off_o,
+                              workspace, workspace_bytes, stream);
+    if (s) return s;
+    e = cudaEventRecord(hs.computed, st);
+    if (e == cudaSuccess) e = cudaStreamWaitEvent(c->d2h, hs.computed, 0);
+    if (e == cudaSuccess)
+        e = copy_chunk(out_host, dev + off_o, c->B, q_heads, T, row, n_new, cudaMemcpyDeviceToHost, c->d2h);
+    if (e == cudaSuccess) e = cudaEventRecord(hs.out_done, c->d2h);
+    if (e != cudaSuccess) return cuda_fail(e, "host-call output copy");
+    return ok();
+}
+
+kvc_status kvc_host_copies_done(kvc_cache* c, void* stream) {
+    if (!c) return fail(KVC_ERR_ARG, "handle is null");
+    if (!c->h2d) return ok();  // no host-buffer call yet
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    cudaError_t e = cudaSuccess;
+    for (auto& hs : c->hslot)
+        if (e == cudaSuccess) e = cudaStreamWaitEvent(st, hs.out_done, 0);
+    if (e != cudaSuccess) return cuda_fail(e, "host-call completion wait");
+    return ok();
 }
 
 kvc_status kvc_length(const kvc_cache* c, int64_t* out) {

@@ -207,6 +207,39 @@ kvc_status kvc_append_attention_tree(kvc_cache* c, int layer, const void* q, con
                                      const int32_t* parents, void* out, void* workspace, size_t workspace_bytes,
                                      void* stream);
 
+/* kvc_append_attention with q, k_new, v_new and out in HOST memory (the same
+ * shapes, [B, Hq, T, d] and [B, Hkv, T, d], element type as there: bf16 for an
+ * FP8 cache), for a caller whose step inputs start and whose outputs end on the
+ * host ("A strong answer": KVCache.append then gqa_attention, one decode or
+ * prefill step).  Host buffers should be page-locked (cudaHostAlloc or
+ * cudaHostRegister) so that the copies run asynchronously; all four must be
+ * 16-byte aligned.
+ * Only positions t < n_new[b] move: those of q, k_new and v_new to the device,
+ * those of out back to out_host.  Positions t >= n_new[b] of out_host are not
+ * written (kvc_append_attention would have written zeros there).
+ * The call returns once it has enqueued: the input copies on a copy stream of
+ * the handle, the append and attention on `stream`, the output copy on a
+ * second copy stream.  Two device staging slots of the handle alternate from
+ * call to call, so one call's output copy and the next call's input copies
+ * overlap the compute in between.  The input buffers must stay unchanged, and
+ * out_host unread, until kvc_host_copies_done has made a stream wait and that
+ * stream has reached the wait (for example cudaStreamSynchronize after it).
+ * The staging slots are allocated on the first call and grown, after the
+ * calls that use them have finished, when a call needs more; kvc_destroy
+ * frees them.  Calls on one handle must come from one host thread in order.
+ * Errors: those of kvc_append_attention, all found before anything is
+ * enqueued or any host buffer is read (nothing is written, lengths
+ * unchanged), and KVC_ERR_CUDA when a copy, an allocation or a launch fails. */
+kvc_status kvc_append_attention_host(kvc_cache* c, int layer, const void* q_host, const void* k_host,
+                                     const void* v_host, int q_heads, int T, const int32_t* n_new, void* out_host,
+                                     void* workspace, size_t workspace_bytes, void* stream);
+
+/* Make `stream` wait until every output copy of the host-buffer calls
+ * enqueued so far on this handle has reached its host buffer (and so every
+ * input copy before it).  Returns at once, without waiting on the host.
+ * Errors: KVC_ERR_ARG (null handle), KVC_ERR_CUDA. */
+kvc_status kvc_host_copies_done(kvc_cache* c, void* stream);
+
 /* Size of the device scratch array behind kvc_gqa_attention_noalloc. */
 #define KVC_NOALLOC_SCRATCH_BYTES (32u << 20)
 

@@ -156,6 +156,35 @@ def test_append_attention_validates_both_steps_first(L):
     L.kvc_destroy(h)
 
 
+def test_host_buffer_call_validates_before_any_copy(L):
+    # Every error of the host-buffer form is found before a copy is enqueued or
+    # a host buffer read: the pointers here are fake, so a copy would crash.
+    st, h = _create(L, layers=1, B=2, Hkv=2, max_len=10, d=16)
+    x = ctypes.c_void_p(1 << 41)
+    a, p = _i32(1, 1)
+    assert L.kvc_append_attention_host(h, 0, x, x, x, 3, 1, p, x, None, 0, None) == 2  # Hq % Hkv != 0
+    a, p = _i32(2, 0)
+    assert L.kvc_append_attention_host(h, 0, x, x, x, 4, 1, p, x, None, 0, None) == 2  # n_new > T
+    a, p = _i32(1, 1)
+    assert L.kvc_append_attention_host(h, 0, None, x, x, 4, 1, p, x, None, 0, None) == 1  # null q
+    assert L.kvc_append_attention_host(h, 0, x, x, x, 4, 1, p, None, None, 0, None) == 1  # null out
+    assert L.kvc_append_attention_host(h, 0, x, None, x, 4, 1, p, x, None, 0, None) == 1  # null k_new
+    odd = ctypes.c_void_p((1 << 41) + 8)
+    assert L.kvc_append_attention_host(h, 0, odd, x, x, 4, 1, p, x, None, 0, None) == 1  # q not 16-byte aligned
+    assert L.kvc_append_attention_host(h, 1, x, x, x, 4, 1, p, x, None, 0, None) == 1  # layer out of range
+    _, full = _i64(9, 0)
+    assert L.kvc_set_lens(h, 0, full) == 0
+    a, p = _i32(2, 0)
+    assert L.kvc_append_attention_host(h, 0, x, x, x, 4, 2, p, x, None, 0, None) == 3  # 9 + 2 > max_len
+    assert list(_lens(L, h, 0, 2)) == [9, 0]
+    # nothing to do: T = 0, or an empty batch
+    a, p = _i32(0, 0)
+    assert L.kvc_append_attention_host(h, 0, None, None, None, 4, 0, p, None, None, 0, None) == 0
+    assert L.kvc_host_copies_done(h, None) == 0  # no host-buffer call has enqueued anything
+    assert L.kvc_host_copies_done(None, None) == 1
+    L.kvc_destroy(h)
+
+
 def test_set_lens_truncate_reset_length(L):
     st, h = _create(L, layers=3, B=2, max_len=16)
     for layer in range(3):
