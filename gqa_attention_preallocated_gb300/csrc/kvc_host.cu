@@ -862,12 +862,26 @@ size_t round256(size_t x) { return (x + 255) / 256 * 256; }
 kvc_status ensure_host_staging(kvc_cache* c, size_t bytes) {
     cudaError_t e = cudaSuccess;
     if (!c->h2d) {
-        e = cudaStreamCreateWithFlags(&c->h2d, cudaStreamNonBlocking);
-        if (e == cudaSuccess) e = cudaStreamCreateWithFlags(&c->d2h, cudaStreamNonBlocking);
+        cudaStream_t h2d = nullptr, d2h = nullptr;
+        e = cudaStreamCreateWithFlags(&h2d, cudaStreamNonBlocking);
+        if (e == cudaSuccess) e = cudaStreamCreateWithFlags(&d2h, cudaStreamNonBlocking);
         for (auto& hs : c->hslot)
             for (cudaEvent_t* ev : {&hs.in_ready, &hs.computed, &hs.out_done})
                 if (e == cudaSuccess) e = cudaEventCreateWithFlags(ev, cudaEventDisableTiming);
-        if (e != cudaSuccess) return cuda_fail(e, "host-call streams / events");
+        if (e != cudaSuccess) {
+            // Leave nothing half made: the next call starts over.
+            for (auto& hs : c->hslot)
+                for (cudaEvent_t* ev : {&hs.in_ready, &hs.computed, &hs.out_done})
+                    if (*ev) {
+                        cudaEventDestroy(*ev);
+                        *ev = nullptr;
+                    }
+            if (h2d) cudaStreamDestroy(h2d);
+            if (d2h) cudaStreamDestroy(d2h);
+            return cuda_fail(e, "host-call streams / events");
+        }
+        c->h2d = h2d;
+        c->d2h = d2h;
     }
     for (auto& hs : c->hslot) {
         if (hs.bytes >= bytes) continue;
