@@ -108,7 +108,9 @@ typedef struct kvc_cache kvc_cache;
 kvc_status kvc_create(kvc_cache** out, int layers, int batch, int kv_heads, int max_len, int head_dim,
                       kvc_dtype dtype, void* const* k_bufs, void* const* v_bufs);
 
-/* Free the handle (not the buffers).  NULL is accepted. */
+/* Free the handle (not the cache buffers).  A handle that has served
+ * kvc_append_attention_host first waits for its copies to finish, then frees
+ * its device staging, copy streams and events.  NULL is accepted. */
 void kvc_destroy(kvc_cache* c);
 
 /* Scales of an FP8 E4M3 cache's layer: k_scale[h], v_scale[h] (host arrays of
