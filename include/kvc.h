@@ -228,7 +228,10 @@ kvc_status kvc_append_attention_tree(kvc_cache* c, int layer, const void* q, con
  * stream has reached the wait (for example cudaStreamSynchronize after it).
  * The staging slots are allocated on the first call and grown, after the
  * calls that use them have finished, when a call needs more; kvc_destroy
- * frees them.  Calls on one handle must come from one host thread in order.
+ * frees them.  Each slot holds one call's q, k_new, v_new and out:
+ * 2 * B * (Hq + Hkv) * T * d elements, each region rounded up to 256 bytes
+ * (two slots: 84 MB for a bf16 chunk of B = 4, Hq = 32, Hkv = 8, T = 512,
+ * d = 128).  Calls on one handle must come from one host thread in order.
  * Errors: those of kvc_append_attention, all found before anything is
  * enqueued or any host buffer is read (nothing is written, lengths
  * unchanged), and KVC_ERR_CUDA when a copy, an allocation or a launch fails. */
